@@ -1,0 +1,460 @@
+/*
+ * moe_oracle.c -- plain, slow CPU oracle for one routed Mixture-of-Experts layer
+ * over MLX-style affine group-quantised weights.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the yardstick the CUDA path is checked
+ * against; it is never linked into, called by, or shipped as part of the product
+ * library.  Only the tests, the smoke check and the CPU-baseline leg of the
+ * benchmark load it.  It shares no code, header, table or constant generator with
+ * the CUDA path.
+ *
+ * What it computes, and where the pages fix it (pages are cited by title and
+ * section):
+ *   - Affine 4-bit weights, group 64, w = scale*q + bias; the router at 8 bits
+ *     ("TurboFieldfare esegue Mac Gemma 4 26B in 2 GB...", section "L'affermazione
+ *     dei 2 GB trasforma la larghezza di banda dell'SSD nel nuovo vincolo";
+ *     "Correr un modelo de 26.000 millones...", section "Detalles tecnicos y
+ *     rendimiento").
+ *   - The router picks 8 experts per token per layer, a shared expert is always
+ *     used, and the outputs of both branches are combined ("Come eseguire un
+ *     modello da 26 miliardi...", section "Qual e il trucco principale
+ *     dell'architettura"; the remio.ai page, sections "Mac Gemma 4 26B entra nello
+ *     spazio disponibile..." and "L'affermazione dei 2 GB...").
+ *   - Chunked prefill of up to 128 tokens is only an efficiency device, so a chunk
+ *     is defined as that many independent decodes (devtrends page, section
+ *     "Prestazioni nel mondo reale"; remio.ai page, same section as above).
+ *   - A 16-slot least-frequently-used expert cache per layer (devtrends page,
+ *     "Qual e il trucco principale..."; remio.ai page, "Mac Gemma 4 26B entra...").
+ *
+ * Readings taken where the pages are silent (each one is listed in the design
+ * notes of the repository):
+ *   - GeGLU with the tanh form of GELU, h = gelu(gate) * up.
+ *   - Gates are the softmax over the selected logits; shared expert weight 1.
+ *   - Top-k order: larger logit first, equal logits -> lower expert index; the
+ *     selection is made on the logits rounded to fp32 (the precision the kernels
+ *     decide in); sums are fp64.
+ *   - MLX nibble order: element j of a row lives in bits 4*(j%8) of 32-bit word
+ *     j/8 (8-bit: bits 8*(j%4) of word j/4); scale and bias are fp16, one pair per
+ *     group of 64 consecutive elements of a row.
+ *   - The quantiser (encoding, used only to build test data): per group
+ *     s = fp16((max-min)/(2^bits-1)), b = fp16(min), q = clamp(rint((w-b)/s)),
+ *     all in fp32; s == 0 -> q = 0.
+ *   - In-cache LFU, ties broken by (count, last use, slot); see orc_lfu_step.
+ *
+ * Arithmetic: every dot product is summed in fp64 in ascending index order.  The
+ * only library primitives are tanh and exp from libm and the compiler's
+ * IEEE binary16 conversions.  OpenMP splits independent output rows across
+ * threads; no sum is reordered.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_OK 0
+#define ORC_EINVAL 1
+#define ORC_ECAPACITY 3
+
+#define GROUP 64
+
+/* ---- IEEE binary16 <-> host floats (compiler-provided _Float16, RNE) ---- */
+
+double orc_half_to_double(uint16_t h) {
+    _Float16 v;
+    memcpy(&v, &h, 2);
+    return (double)v;
+}
+
+static float half_to_float(uint16_t h) {
+    _Float16 v;
+    memcpy(&v, &h, 2);
+    return (float)v;
+}
+
+uint16_t orc_float_to_half(float f) {
+    _Float16 v = (_Float16)f;
+    uint16_t h;
+    memcpy(&h, &v, 2);
+    return h;
+}
+
+/* ---- affine code extraction (MLX layout) ---- */
+
+/* Code q of element j of one row whose packed words start at `row`. */
+static unsigned code_at(const uint32_t *row, int j, int bits) {
+    if (bits == 4) return (row[j / 8] >> (4 * (j % 8))) & 0xFu;
+    return (row[j / 4] >> (8 * (j % 4))) & 0xFFu;
+}
+
+static int words_per_row(int K, int bits) { return K * bits / 32; }
+
+/* w[n][j] = scale[n][j/64] * q[n][j] + bias[n][j/64], in fp64. */
+static double deq_at(const uint32_t *q, const uint16_t *s, const uint16_t *b, int K, int bits,
+                     int n, int j) {
+    const uint32_t *row = q + (size_t)n * words_per_row(K, bits);
+    size_t gi = (size_t)n * (K / GROUP) + j / GROUP;
+    return orc_half_to_double(s[gi]) * (double)code_at(row, j, bits) + orc_half_to_double(b[gi]);
+}
+
+static int shape_ok(int N, int K, int bits) {
+    return N >= 0 && K > 0 && K % GROUP == 0 && (bits == 4 || bits == 8);
+}
+
+/* Dense dequantisation of an N x K matrix into out[n*K + j]. */
+int orc_dequant(const uint32_t *q, const uint16_t *s, const uint16_t *b, int N, int K, int bits,
+                double *out) {
+    if (!shape_ok(N, K, bits)) return ORC_EINVAL;
+#pragma omp parallel for schedule(static)
+    for (int n = 0; n < N; n++)
+        for (int j = 0; j < K; j++) out[(size_t)n * K + j] = deq_at(q, s, b, K, bits, n, j);
+    return ORC_OK;
+}
+
+/* Encoding used to build test data: min/max affine quantiser, fp32 arithmetic. */
+int orc_quantise(const float *w, int N, int K, int bits, uint32_t *q, uint16_t *s, uint16_t *b) {
+    if (!shape_ok(N, K, bits)) return ORC_EINVAL;
+    const unsigned qmax = (1u << bits) - 1u;
+    const int wpr = words_per_row(K, bits);
+    const int G = K / GROUP;
+#pragma omp parallel for schedule(static)
+    for (int n = 0; n < N; n++) {
+        uint32_t *row = q + (size_t)n * wpr;
+        memset(row, 0, sizeof(uint32_t) * (size_t)wpr);
+        for (int g = 0; g < G; g++) {
+            const float *v = w + (size_t)n * K + (size_t)g * GROUP;
+            float mn = v[0], mx = v[0];
+            for (int j = 1; j < GROUP; j++) {
+                if (v[j] < mn) mn = v[j];
+                if (v[j] > mx) mx = v[j];
+            }
+            float range = mx - mn;
+            float step = range / (float)qmax;
+            uint16_t sh = orc_float_to_half(step);
+            uint16_t bh = orc_float_to_half(mn);
+            s[(size_t)n * G + g] = sh;
+            b[(size_t)n * G + g] = bh;
+            float sf = half_to_float(sh);
+            float bf = half_to_float(bh);
+            for (int j = 0; j < GROUP; j++) {
+                unsigned code = 0;
+                if (sf != 0.0f) {
+                    float t = rintf((v[j] - bf) / sf);
+                    if (t < 0.0f) t = 0.0f;
+                    if (t > (float)qmax) t = (float)qmax;
+                    code = (unsigned)t;
+                }
+                int col = g * GROUP + j;
+                if (bits == 4)
+                    row[col / 8] |= (uint32_t)code << (4 * (col % 8));
+                else
+                    row[col / 4] |= (uint32_t)code << (8 * (col % 4));
+            }
+        }
+    }
+    return ORC_OK;
+}
+
+/* y[t][n] = sum_j w[n][j] * x[t][j], fp64, j ascending. */
+int orc_qgemv(const uint32_t *q, const uint16_t *s, const uint16_t *b, int N, int K, int bits,
+              const float *x, int T, double *y) {
+    if (!shape_ok(N, K, bits) || T < 0) return ORC_EINVAL;
+    for (int t = 0; t < T; t++) {
+#pragma omp parallel for schedule(static)
+        for (int n = 0; n < N; n++) {
+            double acc = 0.0;
+            for (int j = 0; j < K; j++) acc += deq_at(q, s, b, K, bits, n, j) * (double)x[(size_t)t * K + j];
+            y[(size_t)t * N + n] = acc;
+        }
+    }
+    return ORC_OK;
+}
+
+/* ---- router: logits, top-k, softmax gates ---- */
+
+/*
+ * For each token t: logit[e] = sum_j Wr[e][j] x[t][j] (+ bias[e] if given), fp64.
+ * The k experts chosen are the k largest logits rounded to fp32, larger first,
+ * equal values -> lower index first.  Gate g_k = exp(l_k - l_max) / sum exp(...)
+ * over the chosen k, using the fp64 logits.
+ */
+int orc_route(const uint32_t *rq, const uint16_t *rs, const uint16_t *rb, int E, int H,
+              const float *x, int T, const float *logit_bias, int topk, double *logits_out,
+              int32_t *idx, double *gate) {
+    if (!shape_ok(E, H, 8) || E <= 0 || topk <= 0 || topk > E || T < 0) return ORC_EINVAL;
+    double *l = (double *)malloc(sizeof(double) * (size_t)E);
+    float *lf = (float *)malloc(sizeof(float) * (size_t)E);
+    unsigned char *taken = (unsigned char *)malloc((size_t)E);
+    if (!l || !lf || !taken) {
+        free(l); free(lf); free(taken);
+        return ORC_EINVAL;
+    }
+    for (int t = 0; t < T; t++) {
+#pragma omp parallel for schedule(static)
+        for (int e = 0; e < E; e++) {
+            double acc = 0.0;
+            for (int j = 0; j < H; j++) acc += deq_at(rq, rs, rb, H, 8, e, j) * (double)x[(size_t)t * H + j];
+            if (logit_bias) acc += (double)logit_bias[e];
+            l[e] = acc;
+        }
+        for (int e = 0; e < E; e++) {
+            lf[e] = (float)l[e];
+            taken[e] = 0;
+            if (logits_out) logits_out[(size_t)t * E + e] = l[e];
+        }
+        /* selection: repeatedly take the best remaining (value desc, index asc) */
+        for (int k = 0; k < topk; k++) {
+            int best = -1;
+            for (int e = 0; e < E; e++) {
+                if (taken[e]) continue;
+                if (best < 0 || lf[e] > lf[best]) best = e;
+            }
+            taken[best] = 1;
+            idx[(size_t)t * topk + k] = best;
+        }
+        double m = l[idx[(size_t)t * topk]];
+        for (int k = 1; k < topk; k++) {
+            double v = l[idx[(size_t)t * topk + k]];
+            if (v > m) m = v;
+        }
+        double z = 0.0;
+        for (int k = 0; k < topk; k++) z += exp(l[idx[(size_t)t * topk + k]] - m);
+        for (int k = 0; k < topk; k++) gate[(size_t)t * topk + k] = exp(l[idx[(size_t)t * topk + k]] - m) / z;
+    }
+    free(l);
+    free(lf);
+    free(taken);
+    return ORC_OK;
+}
+
+/* ---- expert blob layout ----
+ * One expert (gate/up rows [gate; up] = 2I x H, then down H x I) is one contiguous
+ * blob; each sub-array starts on a 256-byte boundary:
+ *   gu_q [2I][H/8] u32 | gu_s [2I][H/64] f16 | gu_b [2I][H/64] f16 |
+ *   d_q  [H][I/8]  u32 | d_s  [H][I/64]  f16 | d_b  [H][I/64]  f16
+ */
+static size_t up256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+typedef struct {
+    size_t gu_q, gu_s, gu_b, d_q, d_s, d_b, total;
+} blob_layout;
+
+static blob_layout layout_of(int H, int I) {
+    blob_layout L;
+    size_t off = 0;
+    L.gu_q = off; off = up256(off + (size_t)2 * I * H / 2);
+    L.gu_s = off; off = up256(off + (size_t)2 * I * (H / GROUP) * 2);
+    L.gu_b = off; off = up256(off + (size_t)2 * I * (H / GROUP) * 2);
+    L.d_q = off;  off = up256(off + (size_t)H * I / 2);
+    L.d_s = off;  off = up256(off + (size_t)H * (I / GROUP) * 2);
+    L.d_b = off;  off = up256(off + (size_t)H * (I / GROUP) * 2);
+    L.total = off;
+    return L;
+}
+
+size_t orc_expert_blob_bytes(int H, int I) { return layout_of(H, I).total; }
+
+void orc_expert_blob_offsets(int H, int I, size_t *off6) {
+    blob_layout L = layout_of(H, I);
+    off6[0] = L.gu_q; off6[1] = L.gu_s; off6[2] = L.gu_b;
+    off6[3] = L.d_q;  off6[4] = L.d_s;  off6[5] = L.d_b;
+}
+
+/* GELU, tanh form: 0.5 z (1 + tanh(sqrt(2/pi) (z + 0.044715 z^3))). */
+double orc_gelu_tanh(double z) {
+    const double c = sqrt(2.0 / 3.14159265358979323846);
+    return 0.5 * z * (1.0 + tanh(c * (z + 0.044715 * z * z * z)));
+}
+
+/*
+ * One expert applied to one token:  a = Wg x, u = Wu x, h = gelu(a) * u,
+ * out = Wd h.  Optionally returns h.
+ */
+int orc_expert(const uint8_t *blob, int H, int I, const float *x, double *out, double *h_out) {
+    if (!shape_ok(2 * I, H, 4) || !shape_ok(H, I, 4)) return ORC_EINVAL;
+    blob_layout L = layout_of(H, I);
+    const uint32_t *guq = (const uint32_t *)(blob + L.gu_q);
+    const uint16_t *gus = (const uint16_t *)(blob + L.gu_s);
+    const uint16_t *gub = (const uint16_t *)(blob + L.gu_b);
+    const uint32_t *dq = (const uint32_t *)(blob + L.d_q);
+    const uint16_t *ds = (const uint16_t *)(blob + L.d_s);
+    const uint16_t *db = (const uint16_t *)(blob + L.d_b);
+    double *h = (double *)malloc(sizeof(double) * (size_t)I);
+    if (!h) return ORC_EINVAL;
+#pragma omp parallel for schedule(static)
+    for (int i = 0; i < I; i++) {
+        double a = 0.0, u = 0.0;
+        for (int j = 0; j < H; j++) a += deq_at(guq, gus, gub, H, 4, i, j) * (double)x[j];
+        for (int j = 0; j < H; j++) u += deq_at(guq, gus, gub, H, 4, I + i, j) * (double)x[j];
+        h[i] = orc_gelu_tanh(a) * u;
+    }
+#pragma omp parallel for schedule(static)
+    for (int n = 0; n < H; n++) {
+        double acc = 0.0;
+        for (int i = 0; i < I; i++) acc += deq_at(dq, ds, db, I, 4, n, i) * h[i];
+        out[n] = acc;
+    }
+    if (h_out) memcpy(h_out, h, sizeof(double) * (size_t)I);
+    free(h);
+    return ORC_OK;
+}
+
+/*
+ * The layer.  For each token t:
+ *   (idx, g) = route(x_t);  y_t = sum_k g_k * expert_{idx_k}(x_t) + shared(x_t)
+ * and, if `residual` is set, y_t += x_t.  `experts[e]` is expert e's blob (only
+ * the routed ones are read; a routed NULL is an error).  idx/gate outputs are
+ * optional.
+ */
+int orc_moe_layer(int H, int E, int topk, int I, int Is, const uint32_t *rq, const uint16_t *rs,
+                  const uint16_t *rb, const uint8_t *const *experts, const uint8_t *shared,
+                  const float *x, int T, const float *logit_bias, int residual, double *y,
+                  int32_t *idx_out, double *gate_out) {
+    if (T < 0 || topk <= 0 || topk > E || !shape_ok(2 * I, H, 4) || !shape_ok(2 * Is, H, 4) ||
+        !shape_ok(H, I, 4) || !shape_ok(H, Is, 4) || !shared)
+        return ORC_EINVAL;
+    int32_t *idx = (int32_t *)malloc(sizeof(int32_t) * (size_t)topk);
+    double *g = (double *)malloc(sizeof(double) * (size_t)topk);
+    double *o = (double *)malloc(sizeof(double) * (size_t)H);
+    int rc = ORC_OK;
+    if (!idx || !g || !o) { rc = ORC_EINVAL; goto done; }
+    for (int t = 0; t < T; t++) {
+        const float *xt = x + (size_t)t * H;
+        double *yt = y + (size_t)t * H;
+        rc = orc_route(rq, rs, rb, E, H, xt, 1, logit_bias, topk, NULL, idx, g);
+        if (rc) goto done;
+        for (int n = 0; n < H; n++) yt[n] = 0.0;
+        for (int k = 0; k < topk; k++) {
+            const uint8_t *blob = experts[idx[k]];
+            if (!blob) { rc = ORC_EINVAL; goto done; }
+            rc = orc_expert(blob, H, I, xt, o, NULL);
+            if (rc) goto done;
+            for (int n = 0; n < H; n++) yt[n] += g[k] * o[n];
+        }
+        rc = orc_expert(shared, H, Is, xt, o, NULL);
+        if (rc) goto done;
+        for (int n = 0; n < H; n++) yt[n] += o[n];
+        if (residual)
+            for (int n = 0; n < H; n++) yt[n] += (double)xt[n];
+        if (idx_out) memcpy(idx_out + (size_t)t * topk, idx, sizeof(int32_t) * (size_t)topk);
+        if (gate_out) memcpy(gate_out + (size_t)t * topk, g, sizeof(double) * (size_t)topk);
+    }
+done:
+    free(idx);
+    free(g);
+    free(o);
+    return rc;
+}
+
+/* ---- per-layer LFU expert cache ----
+ *
+ * One call = one step with the request list R (router order; for a batch, the
+ * union of the tokens' choices in first-appearance order).
+ *   1. every requested expert already resident is a hit: count += 1, last = step;
+ *   2. every requested expert not resident, in request order, is a miss: it goes
+ *      into the lowest-numbered empty slot, else it evicts, among the slots whose
+ *      expert is not in R, the one with the smallest (count, last, slot); it is
+ *      installed with count = 1, last = step.  The evicted expert's count is
+ *      forgotten.
+ * |R| > slots is ORC_ECAPACITY; an index outside [0, E) or a repeated index is
+ * ORC_EINVAL.  On an error nothing changes.
+ */
+typedef struct {
+    int slots, E;
+    int64_t step;
+    uint64_t hits, misses;
+    int32_t *expert_of_slot; /* -1 = empty */
+    uint32_t *count;
+    int64_t *last;
+} orc_lfu;
+
+orc_lfu *orc_lfu_create(int slots, int E) {
+    if (slots <= 0 || E <= 0) return NULL;
+    orc_lfu *c = (orc_lfu *)calloc(1, sizeof(orc_lfu));
+    if (!c) return NULL;
+    c->slots = slots;
+    c->E = E;
+    c->expert_of_slot = (int32_t *)malloc(sizeof(int32_t) * (size_t)slots);
+    c->count = (uint32_t *)calloc((size_t)slots, sizeof(uint32_t));
+    c->last = (int64_t *)calloc((size_t)slots, sizeof(int64_t));
+    if (!c->expert_of_slot || !c->count || !c->last) {
+        free(c->expert_of_slot); free(c->count); free(c->last); free(c);
+        return NULL;
+    }
+    for (int i = 0; i < slots; i++) c->expert_of_slot[i] = -1;
+    return c;
+}
+
+void orc_lfu_destroy(orc_lfu *c) {
+    if (!c) return;
+    free(c->expert_of_slot);
+    free(c->count);
+    free(c->last);
+    free(c);
+}
+
+static int slot_of(const orc_lfu *c, int e) {
+    for (int i = 0; i < c->slots; i++)
+        if (c->expert_of_slot[i] == e) return i;
+    return -1;
+}
+
+/* slot_out[r] = slot now holding request r; hit_out[r] = 1 on a hit. */
+int orc_lfu_step(orc_lfu *c, const int32_t *req, int n, int32_t *slot_out, uint8_t *hit_out) {
+    if (!c || n < 0) return ORC_EINVAL;
+    for (int r = 0; r < n; r++) {
+        if (req[r] < 0 || req[r] >= c->E) return ORC_EINVAL;
+        for (int p = 0; p < r; p++)
+            if (req[p] == req[r]) return ORC_EINVAL;
+    }
+    if (n > c->slots) return ORC_ECAPACITY;
+    int64_t step = c->step;
+    /* 1. hits */
+    for (int r = 0; r < n; r++) {
+        int s = slot_of(c, req[r]);
+        hit_out[r] = (uint8_t)(s >= 0);
+        if (s >= 0) {
+            c->count[s] += 1;
+            c->last[s] = step;
+            slot_out[r] = s;
+            c->hits++;
+        }
+    }
+    /* 2. misses in request order */
+    for (int r = 0; r < n; r++) {
+        if (hit_out[r]) continue;
+        int victim = -1;
+        for (int i = 0; i < c->slots; i++)
+            if (c->expert_of_slot[i] < 0) { victim = i; break; }
+        if (victim < 0) {
+            for (int i = 0; i < c->slots; i++) {
+                int e = c->expert_of_slot[i];
+                int requested = 0;
+                for (int p = 0; p < n; p++)
+                    if (req[p] == e) requested = 1;
+                if (requested) continue;
+                if (victim < 0 || c->count[i] < c->count[victim] ||
+                    (c->count[i] == c->count[victim] && c->last[i] < c->last[victim]))
+                    victim = i;
+            }
+        }
+        /* victim >= 0 always: n <= slots and requested experts occupy < slots. */
+        c->expert_of_slot[victim] = req[r];
+        c->count[victim] = 1;
+        c->last[victim] = step;
+        slot_out[r] = victim;
+        c->misses++;
+    }
+    c->step++;
+    return ORC_OK;
+}
+
+void orc_lfu_state(const orc_lfu *c, int32_t *expert_of_slot, uint32_t *count, int64_t *last,
+                   uint64_t *hits, uint64_t *misses) {
+    for (int i = 0; i < c->slots; i++) {
+        if (expert_of_slot) expert_of_slot[i] = c->expert_of_slot[i];
+        if (count) count[i] = c->count[i];
+        if (last) last[i] = c->last[i];
+    }
+    if (hits) *hits = c->hits;
+    if (misses) *misses = c->misses;
+}
