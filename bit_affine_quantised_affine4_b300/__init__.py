@@ -1,0 +1,189 @@
+"""Thin Python binding of libmoe (include/moe.h).
+
+Argument marshalling only: every step of the MoE layer runs in the CUDA kernels
+of ``libmoe.so``.  Tensors are PyTorch CUDA tensors (used for device memory and
+streams); each function has the name of the C entry point it calls and raises
+``MoeError`` on a non-zero status.  There is no fallback: if the library cannot
+be loaded, importing the binding raises.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import torch
+
+from . import build as _build
+
+MOE_OK, MOE_EINVAL, MOE_ECUDA, MOE_ECAPACITY, MOE_ETIMEOUT, MOE_EWORKSPACE, MOE_ENOTREADY = range(7)
+MOE_RESIDUAL = 1
+MOE_MAX_TOPK = 8
+MOE_MAX_EXPERTS = 256
+MOE_MAX_DECODE_TOKENS = 16
+MOE_MAX_PREFILL_TOKENS = 128
+
+# Every function the header declares (checked against include/moe.h by the tests).
+ENTRY_POINTS = (
+    "moe_status_string", "moe_expert_blob_bytes", "moe_expert_blob_offsets",
+    "moe_workspace_bytes", "moe_workspace_init", "moe_workspace_status",
+    "affine_quantise", "qgemv_affine4", "moe_route", "moe_layer_decode",
+    "moe_layer_prefill_chunk", "moe_cache_create", "moe_cache_destroy",
+    "moe_cache_slots", "moe_cache_stats",
+)
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__("%s: %s (status %d)" % (what, status_string(status), status))
+
+
+class moe_layer_t(C.Structure):
+    _fields_ = [
+        ("H", C.c_int), ("E", C.c_int), ("topk", C.c_int), ("I", C.c_int), ("Is", C.c_int),
+        ("r_q", C.c_void_p), ("r_s", C.c_void_p), ("r_b", C.c_void_p),
+        ("experts", C.c_void_p), ("expert_stride", C.c_size_t),
+        ("shared", C.c_void_p), ("logit_bias", C.c_void_p),
+    ]
+
+
+def _load():
+    path = _build.LIB
+    if _build.stale():
+        path = _build.build()
+    if not os.path.exists(path):
+        raise ImportError("libmoe.so is missing and could not be built")
+    L = C.CDLL(path)
+    p, i, sz = C.c_void_p, C.c_int, C.c_size_t
+    L.moe_status_string.argtypes = [i]
+    L.moe_status_string.restype = C.c_char_p
+    L.moe_expert_blob_bytes.argtypes = [i, i]
+    L.moe_expert_blob_bytes.restype = sz
+    L.moe_expert_blob_offsets.argtypes = [i, i, p]
+    L.moe_workspace_bytes.argtypes = [p, i]
+    L.moe_workspace_bytes.restype = sz
+    L.moe_workspace_init.argtypes = [p, sz, p]
+    L.moe_workspace_status.argtypes = [p, sz, p]
+    L.affine_quantise.argtypes = [p, i, i, i, p, p, p, p]
+    L.qgemv_affine4.argtypes = [p, p, p, i, i, p, p, p]
+    L.moe_route.argtypes = [p, p, i, p, p, p, p, sz, p]
+    L.moe_layer_decode.argtypes = [p, p, i, i, p, p, p, p, p, sz, p]
+    L.moe_layer_prefill_chunk.argtypes = [p, p, i, i, p, p, p, p, sz, p]
+    L.moe_cache_create.argtypes = [p, i, i, i, p, sz, i]
+    L.moe_cache_destroy.argtypes = [p]
+    L.moe_cache_slots.argtypes = [p, p, p]
+    L.moe_cache_stats.argtypes = [p, p, p, p]
+    for name in ENTRY_POINTS:
+        if name not in ("moe_status_string", "moe_expert_blob_bytes", "moe_workspace_bytes"):
+            getattr(L, name).restype = i
+    return L
+
+
+lib = _load()
+
+
+def status_string(status: int) -> str:
+    return lib.moe_status_string(int(status)).decode()
+
+
+def _check(rc: int, what: str):
+    if rc != MOE_OK:
+        raise MoeError(rc, what)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return C.c_void_p(s.cuda_stream)
+
+
+# ------------------------------------------------------------------ layout
+
+def moe_expert_blob_bytes(H: int, I: int) -> int:
+    return int(lib.moe_expert_blob_bytes(H, I))
+
+
+def moe_expert_blob_offsets(H: int, I: int):
+    off = (C.c_size_t * 6)()
+    _check(lib.moe_expert_blob_offsets(H, I, off), "moe_expert_blob_offsets")
+    return list(off)
+
+
+# ------------------------------------------------------------------ kernels
+
+def affine_quantise(w: torch.Tensor, bits: int, q=None, s=None, b=None, stream=None):
+    """Quantise fp32 [N, K] on the GPU -> (q int32 [N, K*bits/32], s int16 [N, K/64], b int16)."""
+    assert w.is_cuda and w.dtype == torch.float32 and w.is_contiguous()
+    N, K = w.shape
+    dev = w.device
+    q = torch.empty((N, K * bits // 32), dtype=torch.int32, device=dev) if q is None else q
+    s = torch.empty((N, K // 64), dtype=torch.int16, device=dev) if s is None else s
+    b = torch.empty((N, K // 64), dtype=torch.int16, device=dev) if b is None else b
+    _check(lib.affine_quantise(_ptr(w), N, K, bits, _ptr(q), _ptr(s), _ptr(b), _stream(stream)),
+           "affine_quantise")
+    return q, s, b
+
+
+def qgemv_affine4(q, s, b, K: int, x, y=None, stream=None):
+    N = q.shape[0]
+    y = torch.empty(N, dtype=torch.float32, device=x.device) if y is None else y
+    _check(lib.qgemv_affine4(_ptr(q), _ptr(s), _ptr(b), N, K, _ptr(x), _ptr(y), _stream(stream)),
+           "qgemv_affine4")
+    return y
+
+
+def moe_workspace_bytes(layer: moe_layer_t, T_max: int) -> int:
+    return int(lib.moe_workspace_bytes(C.byref(layer), T_max))
+
+
+def moe_workspace_init(ws: torch.Tensor, stream=None):
+    _check(lib.moe_workspace_init(_ptr(ws), ws.numel(), _stream(stream)), "moe_workspace_init")
+
+
+def moe_workspace_status(ws: torch.Tensor, stream=None) -> int:
+    return int(lib.moe_workspace_status(_ptr(ws), ws.numel(), _stream(stream)))
+
+
+def new_workspace(layer: moe_layer_t, T_max: int, device="cuda", stream=None) -> torch.Tensor:
+    n = moe_workspace_bytes(layer, T_max)
+    if n == 0:
+        raise MoeError(MOE_EINVAL, "moe_workspace_bytes")
+    ws = torch.empty(n, dtype=torch.uint8, device=device)
+    moe_workspace_init(ws, stream)
+    return ws
+
+
+def moe_route(layer: moe_layer_t, x, ws, idx=None, gate=None, logits=None, stream=None):
+    T = x.shape[0]
+    dev = x.device
+    idx = torch.empty((T, layer.topk), dtype=torch.int32, device=dev) if idx is None else idx
+    gate = torch.empty((T, layer.topk), dtype=torch.float32, device=dev) if gate is None else gate
+    _check(lib.moe_route(C.byref(layer), _ptr(x), T, _ptr(idx), _ptr(gate), _ptr(logits), _ptr(ws),
+                         ws.numel(), _stream(stream)), "moe_route")
+    return idx, gate
+
+
+def moe_layer_decode(layer: moe_layer_t, x, ws, y=None, flags: int = 0, idx=None, gate=None,
+                     cache=None, stream=None):
+    T = x.shape[0]
+    y = torch.empty_like(x) if y is None else y
+    _check(lib.moe_layer_decode(C.byref(layer), _ptr(x), T, flags, _ptr(y), _ptr(idx), _ptr(gate),
+                                None if cache is None else cache.handle, _ptr(ws), ws.numel(),
+                                _stream(stream)), "moe_layer_decode")
+    return y
+
+
+def moe_layer_prefill_chunk(layer: moe_layer_t, x, ws, y=None, flags: int = 0, idx=None, gate=None,
+                            stream=None):
+    T = x.shape[0]
+    y = torch.empty_like(x) if y is None else y
+    _check(lib.moe_layer_prefill_chunk(C.byref(layer), _ptr(x), T, flags, _ptr(y), _ptr(idx),
+                                       _ptr(gate), _ptr(ws), ws.numel(), _stream(stream)),
+           "moe_layer_prefill_chunk")
+    return y
+
+
+from .weights import Layer, make_layer, pack_expert_blob  # noqa: E402

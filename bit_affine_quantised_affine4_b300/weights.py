@@ -1,0 +1,114 @@
+"""Device-side layer weights in the blob layout of include/moe.h.
+
+Packing fp32 weights runs the library's own quantiser kernel (affine_quantise) on
+the GPU, writing straight into the expert blobs.
+"""
+from __future__ import annotations
+
+import ctypes as C
+
+import torch
+
+from . import affine_quantise, moe_expert_blob_bytes, moe_expert_blob_offsets, moe_layer_t
+
+
+def _part(blob: torch.Tensor, off: int, nbytes: int, dtype) -> torch.Tensor:
+    return blob[off:off + nbytes].view(dtype)
+
+
+def pack_expert_blob(gu_w: torch.Tensor, d_w: torch.Tensor, blob: torch.Tensor, stream=None):
+    """Quantise one expert (gate/up [2I, H] gate rows first, down [H, I]; fp32 on the GPU)
+    into `blob` (uint8 CUDA tensor of at least moe_expert_blob_bytes(H, I) bytes)."""
+    I2, H = gu_w.shape
+    I = I2 // 2
+    assert d_w.shape == (H, I)
+    off = moe_expert_blob_offsets(H, I)
+    gq = _part(blob, off[0], I2 * H // 2, torch.int32).view(I2, H // 8)
+    gs = _part(blob, off[1], I2 * (H // 64) * 2, torch.int16).view(I2, H // 64)
+    gb = _part(blob, off[2], I2 * (H // 64) * 2, torch.int16).view(I2, H // 64)
+    dq = _part(blob, off[3], H * I // 2, torch.int32).view(H, I // 8)
+    ds = _part(blob, off[4], H * (I // 64) * 2, torch.int16).view(H, I // 64)
+    db = _part(blob, off[5], H * (I // 64) * 2, torch.int16).view(H, I // 64)
+    affine_quantise(gu_w.contiguous(), 4, gq, gs, gb, stream)
+    affine_quantise(d_w.contiguous(), 4, dq, ds, db, stream)
+    return blob
+
+
+class Layer:
+    """One MoE layer resident on the GPU: router (8-bit), E expert blobs, shared blob.
+
+    `copies` > 1 allocates that many independent copies of the expert/shared/router
+    memory (same values, different addresses) so that a benchmark can rotate through
+    more bytes than the L2 cache holds; `view(c)` returns the C struct of copy c.
+    """
+
+    def __init__(self, H, E, topk, I, Is, device="cuda", copies=1):
+        self.H, self.E, self.topk, self.I, self.Is = H, E, topk, I, Is
+        self.device = torch.device(device)
+        self.stride = moe_expert_blob_bytes(H, I)
+        self.sstride = moe_expert_blob_bytes(H, Is)
+        self.copies = copies
+        self.r_q = torch.empty((copies, E, H // 4), dtype=torch.int32, device=self.device)
+        self.r_s = torch.empty((copies, E, H // 64), dtype=torch.int16, device=self.device)
+        self.r_b = torch.empty((copies, E, H // 64), dtype=torch.int16, device=self.device)
+        self.experts = torch.empty((copies, E, self.stride), dtype=torch.uint8, device=self.device)
+        self.shared = torch.empty((copies, self.sstride), dtype=torch.uint8, device=self.device)
+        self.bias = None
+
+    # ---- filling
+    def set_router(self, w: torch.Tensor):
+        affine_quantise(w.to(self.device, torch.float32).contiguous(), 8, self.r_q[0], self.r_s[0],
+                        self.r_b[0])
+
+    def set_expert(self, e: int, gu_w: torch.Tensor, d_w: torch.Tensor):
+        pack_expert_blob(gu_w.to(self.device, torch.float32), d_w.to(self.device, torch.float32),
+                         self.experts[0, e])
+
+    def set_shared(self, gu_w: torch.Tensor, d_w: torch.Tensor):
+        pack_expert_blob(gu_w.to(self.device, torch.float32), d_w.to(self.device, torch.float32),
+                         self.shared[0])
+
+    def set_bias(self, bias):
+        self.bias = None if bias is None else torch.as_tensor(bias, dtype=torch.float32).to(self.device)
+
+    def replicate(self):
+        for c in range(1, self.copies):
+            self.r_q[c].copy_(self.r_q[0]); self.r_s[c].copy_(self.r_s[0]); self.r_b[c].copy_(self.r_b[0])
+            self.experts[c].copy_(self.experts[0]); self.shared[c].copy_(self.shared[0])
+
+    # ---- C view
+    def view(self, c: int = 0, experts: bool = True) -> moe_layer_t:
+        return moe_layer_t(
+            H=self.H, E=self.E, topk=self.topk, I=self.I, Is=self.Is,
+            r_q=self.r_q[c].data_ptr(), r_s=self.r_s[c].data_ptr(), r_b=self.r_b[c].data_ptr(),
+            experts=self.experts[c].data_ptr() if experts else None,
+            expert_stride=self.stride,
+            shared=self.shared[c].data_ptr(),
+            logit_bias=None if self.bias is None else self.bias.data_ptr(),
+        )
+
+    # ---- host copies (for comparison with the oracle)
+    def expert_blob_host(self, e: int, c: int = 0):
+        return self.experts[c, e].cpu().numpy()
+
+    def shared_blob_host(self, c: int = 0):
+        return self.shared[c].cpu().numpy()
+
+    def router_host(self, c: int = 0):
+        return (self.r_q[c].cpu().numpy().view("uint32"), self.r_s[c].cpu().numpy().view("uint16"),
+                self.r_b[c].cpu().numpy().view("uint16"))
+
+
+def make_layer(H, E, topk, I, Is, router_w, expert_w, shared_w, bias=None, device="cuda", copies=1):
+    """Build a Layer from fp32 weights: router_w [E, H]; expert_w(e) -> (gu [2I, H], d [H, I])
+    (a callable, so that the host never holds every expert at once); shared_w = (gu, d)."""
+    L = Layer(H, E, topk, I, Is, device=device, copies=copies)
+    L.set_router(torch.as_tensor(router_w))
+    for e in range(E):
+        gu, d = expert_w(e)
+        L.set_expert(e, torch.as_tensor(gu), torch.as_tensor(d))
+    L.set_shared(*(torch.as_tensor(a) for a in shared_w))
+    L.set_bias(bias)
+    L.replicate()
+    torch.cuda.synchronize(L.device)
+    return L

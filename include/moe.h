@@ -1,0 +1,222 @@
+/*
+ * moe.h -- C ABI of libmoe: one routed Mixture-of-Experts layer over MLX-style
+ * affine group-quantised weights, on one B300 (sm_103a).
+ *
+ * The operation (from the pages of the TurboFieldfare write-ups; pages are named
+ * by title and section):
+ *   - weights are affine 4-bit, group 64, w = scale * q + bias with fp16 scale and
+ *     bias; the router is 8-bit ("TurboFieldfare esegue Mac Gemma 4 26B in 2 GB...",
+ *     section "L'affermazione dei 2 GB trasforma la larghezza di banda dell'SSD nel
+ *     nuovo vincolo"; "Correr un modelo de 26.000 millones...", section "Detalles
+ *     tecnicos y rendimiento");
+ *   - per token the router picks 8 experts; an always-on shared expert runs beside
+ *     them and both branches are combined ("Come eseguire un modello da 26
+ *     miliardi...", section "Qual e il trucco principale dell'architettura";
+ *     remio.ai page, section "Mac Gemma 4 26B entra nello spazio disponibile...");
+ *   - prefill runs in chunks of up to 128 tokens so that one expert load serves
+ *     many rows (devtrends page, section "Prestazioni nel mondo reale");
+ *   - a 16-slot least-frequently-used expert cache per layer, refilled while the
+ *     shared expert computes (devtrends page, "Qual e il trucco principale...").
+ *
+ * Conventions for every call:
+ *   - Pointers named d_* or documented as "device" are CUDA device pointers owned
+ *     by the caller; the library never frees them.  Host pointers are named h_*.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Calls are stream-ordered and return before the GPU finishes, except where a
+ *     call says it synchronises.
+ *   - Every call returns an int status (MOE_OK = 0).  Arguments are checked on the
+ *     host before anything is launched; a rejected call launches nothing.  No C++
+ *     exception crosses this boundary.
+ *   - Matrices are row-major.  A 4-bit matrix [N][K] is stored as
+ *       q     uint32 [N][K/8]   element j of a row = bits 4*(j%8) of word j/8
+ *       scale fp16   [N][K/64]  (raw IEEE binary16 bits in uint16_t)
+ *       bias  fp16   [N][K/64]
+ *     An 8-bit matrix is the same with q uint32 [N][K/4], element j = byte j%4 of
+ *     word j/4.  K must be a multiple of 64.
+ *   - All fp32 outputs are accumulated in fp32; results are deterministic (no
+ *     floating-point atomics).
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---------------------------------------------------------------- status */
+#define MOE_OK 0
+#define MOE_EINVAL 1     /* bad shape, size, flag or NULL pointer */
+#define MOE_ECUDA 2      /* a CUDA runtime call failed */
+#define MOE_ECAPACITY 3  /* more distinct experts requested than cache slots */
+#define MOE_ETIMEOUT 4   /* a bounded device-side wait gave up */
+#define MOE_EWORKSPACE 5 /* workspace missing or smaller than moe_workspace_bytes */
+#define MOE_ENOTREADY 6  /* handle not initialised for this use */
+
+MOE_API const char *moe_status_string(int status);
+
+/* flags for moe_layer_decode / moe_layer_prefill_chunk */
+#define MOE_RESIDUAL 1 /* y = x + MoE(x) instead of y = MoE(x) */
+
+#define MOE_GROUP 64
+#define MOE_MAX_TOPK 8
+#define MOE_MAX_EXPERTS 256
+#define MOE_MAX_DECODE_TOKENS 16
+#define MOE_MAX_PREFILL_TOKENS 128
+
+/* ---------------------------------------------------------------- layout */
+
+/*
+ * One expert is one contiguous blob (the unit the cache copies):
+ *   gu_q [2I][H/8] u32 | gu_s [2I][H/64] f16 | gu_b [2I][H/64] f16 |
+ *   d_q  [H][I/8]  u32 | d_s  [H][I/64]  f16 | d_b  [H][I/64]  f16
+ * The gate/up matrix holds the I gate rows first, then the I up rows.  Every
+ * part starts on a 256-byte boundary; the blob size is a multiple of 256.
+ * moe_expert_blob_offsets writes the six byte offsets.  Returns 0 for bad shapes.
+ */
+MOE_API size_t moe_expert_blob_bytes(int H, int I);
+MOE_API int moe_expert_blob_offsets(int H, int I, size_t offsets_out[6]);
+
+/*
+ * A layer.  All pointers are device pointers owned by the caller.
+ *   H hidden size, E experts (<= MOE_MAX_EXPERTS), topk (1..MOE_MAX_TOPK),
+ *   I routed-expert intermediate size, Is shared-expert intermediate size;
+ *   H, I and Is multiples of 64 (H also a multiple of 128).
+ *   r_q/r_s/r_b: 8-bit router matrix [E][H].
+ *   experts: E blobs of shape (H, I), blob e at experts + e * expert_stride
+ *     (expert_stride a multiple of 256 and >= moe_expert_blob_bytes(H, I)).
+ *     May be NULL when a cache supplies the experts.
+ *   shared: one blob of shape (H, Is).
+ *   logit_bias: optional fp32 [E] added to the router logits (NULL = none).
+ */
+typedef struct moe_layer {
+    int H, E, topk, I, Is;
+    const uint32_t *r_q;
+    const uint16_t *r_s, *r_b;
+    const void *experts;
+    size_t expert_stride;
+    const void *shared;
+    const float *logit_bias;
+} moe_layer_t;
+
+/* ---------------------------------------------------------------- workspace */
+
+/*
+ * Scratch for moe_route / moe_layer_decode / moe_layer_prefill_chunk on up to
+ * T_max tokens (T_max <= MOE_MAX_PREFILL_TOKENS).  The caller allocates it on the
+ * device (256-byte aligned) and must zero it once with moe_workspace_init before
+ * first use; every call leaves it ready for the next one.  One workspace serves
+ * one call at a time: calls that overlap on the GPU must use different
+ * workspaces.  Returns 0 for an invalid layer or T_max.
+ */
+MOE_API size_t moe_workspace_bytes(const moe_layer_t *layer, int T_max);
+MOE_API int moe_workspace_init(void *d_ws, size_t ws_bytes, void *stream);
+
+/*
+ * Synchronises `stream`, then reports whether a device-side wait of an earlier
+ * call on this workspace gave up (MOE_ETIMEOUT) and re-initialises the workspace
+ * in that case.  MOE_OK otherwise.
+ */
+MOE_API int moe_workspace_status(void *d_ws, size_t ws_bytes, void *stream);
+
+/* ---------------------------------------------------------------- kernels */
+
+/*
+ * Affine quantiser (encoding used to build packed weights): for each row and
+ * group of 64, s = fp16((max-min)/(2^bits-1)), b = fp16(min),
+ * q = clamp(rint((w - b)/s), 0, 2^bits-1) in fp32 (q = 0 when s == 0).
+ * w: device fp32 [N][K]; q/s/b: device outputs in the layout above.
+ * bits is 4 or 8.  The MLX affine format is named by the remio.ai page, section
+ * "L'affermazione dei 2 GB...".
+ */
+MOE_API int affine_quantise(const float *w, int N, int K, int bits, uint32_t *q, uint16_t *s, uint16_t *b,
+                    void *stream);
+
+/*
+ * One 4-bit quantised GEMV, y[n] = sum_j (s[n][j/64] q[n][j] + b[n][j/64]) x[j]
+ * (the "quantised GEMV" kernel of the devtrends page, section "Senza dipendenze
+ * da llama.cpp e MLX").  q/s/b device [N][K] 4-bit; x device fp32 [K];
+ * y device fp32 [N].  N >= 1, K a multiple of 64.
+ */
+MOE_API int qgemv_affine4(const uint32_t *q, const uint16_t *s, const uint16_t *b, int N, int K,
+                  const float *x, float *y, void *stream);
+
+/*
+ * Router on T tokens (1..MOE_MAX_PREFILL_TOKENS): logits = deq(Wr) x (+ bias),
+ * idx = the topk largest logits, larger first, equal -> lower expert index;
+ * gate = softmax over the chosen logits.  x device fp32 [T][H]; idx device int32
+ * [T][topk]; gate device fp32 [T][topk]; logits (optional, NULL = not written)
+ * device fp32 [T][E].  (devtrends page, "Qual e il trucco principale..."; remio.ai
+ * page, "L'affermazione dei 2 GB...".)
+ */
+MOE_API int moe_route(const moe_layer_t *layer, const float *x, int T, int32_t *idx, float *gate,
+              float *logits, void *d_ws, size_t ws_bytes, void *stream);
+
+typedef struct moe_cache moe_cache_t;
+
+/*
+ * Decode step on T = 1..MOE_MAX_DECODE_TOKENS independent tokens:
+ *   y_t = sum_k gate_tk * expert_{idx_tk}(x_t) + shared(x_t)   (+ x_t with MOE_RESIDUAL)
+ * expert(x) = Wd (gelu_tanh(Wg x) * (Wu x)).  Every distinct expert is read once
+ * for all the tokens that chose it.  x, y: device fp32 [T][H] (y must not alias
+ * x).  idx_out / gate_out: optional device outputs [T][topk].
+ * cache == NULL: experts come from layer->experts; the call does not synchronise.
+ * cache != NULL: experts come from the cache's device slots; the call copies the
+ *   routing to the host, synchronises on it, runs the LFU policy, issues the
+ *   missing experts' host->device copies on the cache's side stream while the
+ *   shared expert runs on `stream`, and then computes the routed experts.  It
+ *   returns once all work is enqueued (not finished).  MOE_ECAPACITY if the
+ *   tokens request more distinct experts than the cache has slots.
+ */
+MOE_API int moe_layer_decode(const moe_layer_t *layer, const float *x, int T, int flags, float *y,
+                     int32_t *idx_out, float *gate_out, moe_cache_t *cache, void *d_ws,
+                     size_t ws_bytes, void *stream);
+
+/*
+ * Prefill chunk of T = 1..MOE_MAX_PREFILL_TOKENS tokens: the same result as T
+ * independent decodes (chunking only lets one expert load serve many rows).  The
+ * tokens routed to each expert are gathered, multiplied on the tensor cores with
+ * fp16 operands and fp32 accumulation, and scattered back through the gates.
+ * Arguments as moe_layer_decode (no cache).
+ */
+MOE_API int moe_layer_prefill_chunk(const moe_layer_t *layer, const float *x, int T, int flags, float *y,
+                            int32_t *idx_out, float *gate_out, void *d_ws, size_t ws_bytes,
+                            void *stream);
+
+/* ---------------------------------------------------------------- LFU cache */
+
+/*
+ * Per-layer expert cache: `slots` device slots (<= 64) of blob size for (H, I),
+ * filled from the E expert blobs held by the caller in host memory at
+ * h_experts + e * host_stride (page-locked memory is required for the copies to
+ * overlap compute; it is not copied or freed by the library).  The library
+ * allocates the slot pool, a non-blocking side stream and its events; all are
+ * released by moe_cache_destroy.
+ *
+ * Policy (the pages give "16 slots, LFU, per layer"; the tie rules are this
+ * library's reading): per step with request list R (the tokens' choices, first
+ * appearance order) every resident expert in R is a hit (count += 1, last = step);
+ * every missing one, in order, takes the lowest empty slot, else evicts the slot
+ * not in R with the smallest (count, last, slot), and starts at count 1.
+ */
+MOE_API int moe_cache_create(moe_cache_t **out, int H, int E, int I, const void *h_experts,
+                     size_t host_stride, int slots);
+MOE_API int moe_cache_destroy(moe_cache_t *cache);
+/* expert_of_slot[slots] (-1 = empty), counts[slots]; either may be NULL. */
+MOE_API int moe_cache_slots(const moe_cache_t *cache, int32_t *expert_of_slot, uint32_t *counts);
+MOE_API int moe_cache_stats(const moe_cache_t *cache, uint64_t *hits, uint64_t *misses,
+                    uint64_t *h2d_bytes);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H */

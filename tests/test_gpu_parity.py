@@ -1,0 +1,209 @@
+"""CUDA path vs the CPU oracle, element by element, through the C ABI.
+
+Bars: quantiser bytes and expert indices bit-exact; fp32 outputs within
+max|gpu - oracle| <= 2e-3 * (1 + |oracle|).  Inputs are the seeded synthetic
+workloads (weights N(0, 0.02) quantised 4-bit g64 / router 8-bit g64, tokens
+N(0, 1)); the tiny layer runs whole, the full-size layer is checked on every
+output of the sampled tokens.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from layers import OracleLayer, gpu_layer, topk_margin, within_tol
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+TOL = 2e-3
+
+
+@pytest.fixture(scope="module")
+def moe():
+    import bit_affine_quantised_affine4_b300 as m
+    return m
+
+
+def _cuda(a, dtype=None):
+    t = torch.as_tensor(np.ascontiguousarray(a))
+    if dtype is not None:
+        t = t.to(dtype)
+    return t.cuda()
+
+
+# ------------------------------------------------------------------ quantiser
+
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("N,K", [(7, 64), (33, 2816), (1408, 704)])
+def test_quantiser_bit_exact(moe, bits, N, K):
+    w = synth.normal(synth.key(1, N, K, bits), (N, K), 0.02)
+    w[0, :64] = 0.5  # constant group: scale 0
+    w[-1, -64:] = np.linspace(-3, 3, 64, dtype=np.float32)
+    q, s, b = moe.affine_quantise(_cuda(w), bits)
+    oq, os_, ob = oracle.quantise(w, bits)
+    assert np.array_equal(q.cpu().numpy().view(np.uint32), oq)
+    assert np.array_equal(s.cpu().numpy().view(np.uint16), os_)
+    assert np.array_equal(b.cpu().numpy().view(np.uint16), ob)
+
+
+# ------------------------------------------------------------------ qgemv
+
+@pytest.mark.parametrize("N,K", [(4, 64), (100, 320), (4224, 2816), (2816, 704), (2816, 2112)])
+def test_qgemv_affine4(moe, N, K):
+    w = synth.normal(synth.key(2, N, K), (N, K), 0.02)
+    x = synth.normal(synth.key(3, N, K), (K,), 1.0)
+    q, s, b = oracle.quantise(w, 4)
+    y = moe.qgemv_affine4(_cuda(q.view(np.int32)), _cuda(s.view(np.int16)), _cuda(b.view(np.int16)),
+                          K, _cuda(x))
+    ref = oracle.qgemv(q, s, b, K, 4, x)
+    ok, worst = within_tol(y.cpu().numpy(), ref, TOL)
+    assert ok, worst
+
+
+# ------------------------------------------------------------------ layers
+
+@pytest.fixture(scope="module")
+def tiny(moe):
+    s = synth.TINY
+    return s, gpu_layer(s, seed=0), OracleLayer(s, seed=0)
+
+
+@pytest.fixture(scope="module")
+def full_zipf(moe):
+    s = synth.FULL
+    bias = synth.popularity_bias(s, seed=0)
+    return s, gpu_layer(s, seed=0, bias=bias), OracleLayer(s, seed=0, bias=bias)
+
+
+@pytest.fixture(scope="module")
+def full_uniform(moe):
+    s = synth.FULL
+    return s, gpu_layer(s, seed=0), OracleLayer(s, seed=0)
+
+
+def _blobs_match(gl, ol, experts):
+    rq, rs, rb = gl.router_host()
+    assert np.array_equal(rq, ol.router[0]) and np.array_equal(rs, ol.router[1])
+    assert np.array_equal(rb, ol.router[2])
+    assert np.array_equal(gl.shared_blob_host(), ol.shared)
+    for e in experts:
+        assert np.array_equal(gl.expert_blob_host(int(e)), ol.expert(int(e))), e
+
+
+def _route_check(moe, shape, gl, ol, T, stream_id):
+    x = synth.tokens(shape, T, seed=0, stream=stream_id)
+    layer = gl.view()
+    ws = moe.new_workspace(layer, T)
+    logits = torch.empty((T, shape.E), dtype=torch.float32, device="cuda")
+    idx, gate = moe.moe_route(layer, _cuda(x), ws, logits=logits)
+    rlog, ridx, rgate = ol.route(x)
+    # a near-tie within the fp32 error bound would make an index flip legitimate;
+    # at these seeds there is none, and the test says so if one appears
+    bound = 1e-5 * np.max(np.abs(rlog)) + 1e-6
+    assert np.all(topk_margin(rlog, shape.topk) > bound), "near-tie at the top-k boundary"
+    assert np.array_equal(idx.cpu().numpy(), ridx)
+    assert within_tol(gate.cpu().numpy(), rgate, TOL)[0]
+    assert within_tol(logits.cpu().numpy(), rlog, TOL)[0]
+    return x
+
+
+def test_route_tiny(moe, tiny):
+    s, gl, ol = tiny
+    _blobs_match(gl, ol, [])
+    for T in (1, 5, 16, 128):
+        _route_check(moe, s, gl, ol, T, 10 + T)
+
+
+def test_route_full(moe, full_zipf):
+    s, gl, ol = full_zipf
+    _blobs_match(gl, ol, [])
+    for T in (1, 16, 128):
+        _route_check(moe, s, gl, ol, T, 20 + T)
+
+
+def _layer_check(moe, shape, gl, ol, T, stream_id, prefill=False, residual=False, check_tokens=None):
+    x = synth.tokens(shape, T, seed=0, stream=stream_id)
+    layer = gl.view()
+    ws = moe.new_workspace(layer, T)
+    idx = torch.empty((T, shape.topk), dtype=torch.int32, device="cuda")
+    gate = torch.empty((T, shape.topk), dtype=torch.float32, device="cuda")
+    fn = moe.moe_layer_prefill_chunk if prefill else moe.moe_layer_decode
+    flags = moe.MOE_RESIDUAL if residual else 0
+    y = fn(layer, _cuda(x), ws, flags=flags, idx=idx, gate=gate)
+    torch.cuda.synchronize()
+    assert moe.moe_workspace_status(ws) == moe.MOE_OK
+    toks = list(range(T)) if check_tokens is None else check_tokens
+    ry, ridx, rgate = ol.layer(x[toks], residual=residual)
+    _blobs_match(gl, ol, np.unique(ridx))
+    assert np.array_equal(idx.cpu().numpy()[toks], ridx)
+    assert within_tol(gate.cpu().numpy()[toks], rgate, TOL)[0]
+    ok, worst = within_tol(y.cpu().numpy()[toks], ry, TOL)
+    assert ok, "worst err/bound %.3f" % worst
+    return worst
+
+
+@pytest.mark.parametrize("T", [1, 2, 3, 8, 16])
+def test_decode_tiny(moe, tiny, T):
+    s, gl, ol = tiny
+    _layer_check(moe, s, gl, ol, T, 100 + T)
+
+
+def test_decode_tiny_residual(moe, tiny):
+    s, gl, ol = tiny
+    _layer_check(moe, s, gl, ol, 4, 150, residual=True)
+
+
+def test_decode_full_uniform_T1(moe, full_uniform):
+    s, gl, ol = full_uniform
+    for sid in range(3):
+        _layer_check(moe, s, gl, ol, 1, 200 + sid)
+
+
+@pytest.mark.parametrize("T", [1, 2, 4, 8, 16])
+def test_decode_full_zipf_batch(moe, full_zipf, T):
+    s, gl, ol = full_zipf
+    _layer_check(moe, s, gl, ol, T, 300 + T)
+
+
+@pytest.mark.parametrize("T", [1, 37, 128])
+def test_prefill_tiny(moe, tiny, T):
+    s, gl, ol = tiny
+    _layer_check(moe, s, gl, ol, T, 400 + T, prefill=True)
+
+
+def test_prefill_full_zipf_128(moe, full_zipf):
+    s, gl, ol = full_zipf
+    _layer_check(moe, s, gl, ol, 128, 500, prefill=True,
+                 check_tokens=[0, 1, 2, 31, 63, 64, 100, 126, 127])
+
+
+def test_odd_shapes(moe):
+    """A small layer whose sizes are not powers of two: H 384, I 192, Is 320, E 13, top-5."""
+    s = synth.Shape("odd", 384, 13, 5, 192, 320)
+    gl, ol = gpu_layer(s, seed=3), OracleLayer(s, seed=3)
+    for T in (1, 7):
+        _layer_check(moe, s, gl, ol, T, 600 + T)
+    _layer_check(moe, s, gl, ol, 29, 650, prefill=True)
+
+
+def test_many_experts_topk1(moe):
+    s = synth.Shape("wide", 256, 256, 1, 64, 64)
+    gl, ol = gpu_layer(s, seed=4), OracleLayer(s, seed=4)
+    _layer_check(moe, s, gl, ol, 16, 700)
+
+
+def test_rejects_bad_calls(moe, tiny):
+    s, gl, ol = tiny
+    layer = gl.view()
+    ws = moe.new_workspace(layer, 4)
+    x = torch.zeros((8, s.H), device="cuda")
+    with pytest.raises(moe.MoeError) as e:
+        moe.moe_layer_decode(layer, x, ws)  # 8 tokens > workspace T_max 4
+    assert e.value.status == moe.MOE_EWORKSPACE
+    with pytest.raises(moe.MoeError) as e:
+        moe.moe_layer_decode(layer, torch.zeros((17, s.H), device="cuda"), moe.new_workspace(layer, 17))
+    assert e.value.status == moe.MOE_EINVAL
+    with pytest.raises(moe.MoeError) as e:
+        moe.moe_layer_decode(layer, x[:2], ws, y=x[:2])  # y aliases x
+    assert e.value.status == moe.MOE_EINVAL
