@@ -60,26 +60,43 @@ struct LayerDev {
     BlobLayout L, Ls;
 };
 
-// Workspace (see moe_workspace_bytes).  ctrl words: [0] error flag, [1] router
-// ticket, [2] number of distinct routed experts U; then one ticket per 16-row
-// output tile of the down projection.
+// Workspace (see moe_workspace_bytes).  Control words live at the start:
+enum CtrlWord {
+    kErr = 0,        // a bounded wait gave up (sticky until moe_workspace_status)
+    kRouteTicket,    // router items finished (the last one runs top-k)
+    kU,              // number of distinct routed experts of this call
+    kQueue0,         // work queue: router, shared gate/up, shared down items
+    kQueue1,         // work queue: routed gate/up items
+    kQueue2,         // work queue: routed down items
+    kXPrep,          // router items whose slice of x is converted
+    kRouted,         // 1 once idx/gate/schedule are published
+    kSharedUp,       // shared gate/up items finished
+    kExit,           // CTAs finished (the last one resets the control words)
+    kCtrlWords = 16
+};
+
 struct Ws {
     unsigned *ctrl;
-    unsigned *tile_cnt;
-    float *logits;   // [Tmax][E]
-    int *idx;        // [Tmax][topk]
-    float *gate;     // [Tmax][topk]
-    int *uexp;       // [Umax] expert id of distinct expert u (ascending ids)
-    int *ucount;     // [Umax] tokens using u
-    int *ulist;      // [Umax][Tmax] pair ids p = t*topk + k, ascending
-    float *h;        // [Tmax*topk][I]  routed GeGLU activations per pair
-    float *hs;       // [Tmax][Is]      shared-expert activations
-    float *partial;  // [Tmax*topk + Tmax][H] per-pair down outputs, then shared
+    unsigned *tile_cnt;  // [H/16] tickets of the down combine (16-row tiles)
+    unsigned *up_done;   // [Umax] gate/up items finished per distinct expert
+    float *logits;       // [Tmax][E]
+    int *idx;            // [Tmax][topk]
+    float *gate;         // [Tmax][topk]
+    int *uexp;           // [Umax] expert id of distinct expert u (ascending ids)
+    int *ucount;         // [Umax] tokens using u
+    int *ulist;          // [Umax][Tmax] pair ids p = t*topk + k, ascending
+    float *h;            // [Tmax*topk][I]  routed activations (fp32 path)
+    float *hs;           // [Tmax][Is]      shared activations (fp32 path)
+    float *partial;      // [Tmax*topk + Tmax][H] per-pair down outputs, then shared
+    __half *x16;         // [Tmax][H]   tokens in fp16, fragment order
+    float *xsum;         // [Tmax][H/64] group sums of the fp16 tokens
+    __half *h16;         // [Tmax*topk][I] routed activations, fp16 fragment order
+    __half *hs16;        // [Tmax][Is]     shared activations, fp16 fragment order
     int Tmax, Umax;
 };
 
 struct WsLayout {
-    size_t ctrl, logits, idx, gate, uexp, ucount, ulist, h, hs, partial, total;
+    size_t ctrl, logits, idx, gate, uexp, ucount, ulist, h, hs, partial, x16, xsum, h16, hs16, total;
     int Tmax, Umax;
 };
 
@@ -88,7 +105,7 @@ inline WsLayout ws_layout(const moe_layer_t &l, int Tmax) {
     W.Tmax = Tmax;
     W.Umax = Tmax * l.topk < l.E ? Tmax * l.topk : l.E;
     size_t off = 0;
-    W.ctrl = off;    off = up256(off + sizeof(unsigned) * (16 + l.H / 16));
+    W.ctrl = off;    off = up256(off + sizeof(unsigned) * (kCtrlWords + l.H / 16 + W.Umax));
     W.logits = off;  off = up256(off + sizeof(float) * Tmax * l.E);
     W.idx = off;     off = up256(off + sizeof(int) * Tmax * l.topk);
     W.gate = off;    off = up256(off + sizeof(float) * Tmax * l.topk);
@@ -98,15 +115,20 @@ inline WsLayout ws_layout(const moe_layer_t &l, int Tmax) {
     W.h = off;       off = up256(off + sizeof(float) * size_t(Tmax) * l.topk * l.I);
     W.hs = off;      off = up256(off + sizeof(float) * size_t(Tmax) * l.Is);
     W.partial = off; off = up256(off + sizeof(float) * size_t(Tmax) * (l.topk + 1) * l.H);
+    W.x16 = off;     off = up256(off + sizeof(__half) * size_t(Tmax) * l.H);
+    W.xsum = off;    off = up256(off + sizeof(float) * size_t(Tmax) * (l.H / kGroup));
+    W.h16 = off;     off = up256(off + sizeof(__half) * size_t(Tmax) * l.topk * l.I);
+    W.hs16 = off;    off = up256(off + sizeof(__half) * size_t(Tmax) * l.Is);
     W.total = off;
     return W;
 }
 
-inline Ws ws_bind(void *base, const WsLayout &W) {
+inline Ws ws_bind(void *base, const WsLayout &W, const moe_layer_t &l) {
     uint8_t *p = (uint8_t *)base;
     Ws w;
     w.ctrl = (unsigned *)(p + W.ctrl);
-    w.tile_cnt = w.ctrl + 16;
+    w.tile_cnt = w.ctrl + kCtrlWords;
+    w.up_done = w.tile_cnt + l.H / 16;
     w.logits = (float *)(p + W.logits);
     w.idx = (int *)(p + W.idx);
     w.gate = (float *)(p + W.gate);
@@ -116,6 +138,10 @@ inline Ws ws_bind(void *base, const WsLayout &W) {
     w.h = (float *)(p + W.h);
     w.hs = (float *)(p + W.hs);
     w.partial = (float *)(p + W.partial);
+    w.x16 = (__half *)(p + W.x16);
+    w.xsum = (float *)(p + W.xsum);
+    w.h16 = (__half *)(p + W.h16);
+    w.hs16 = (__half *)(p + W.hs16);
     w.Tmax = W.Tmax;
     w.Umax = W.Umax;
     return w;

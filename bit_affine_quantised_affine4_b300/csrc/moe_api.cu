@@ -8,6 +8,8 @@
 #include "common.cuh"
 #include "route.cuh"
 #include "simple_kernels.cuh"
+#include "decode.cuh"
+#include "gemv.cuh"
 
 using namespace moe;
 
@@ -25,7 +27,9 @@ bool layer_ok(const moe_layer_t *l) {
         l->topk > l->E)
         return false;
     if (!l->r_q || !l->r_s || !l->r_b || !l->shared) return false;
-    if (!aligned(l->r_q, 16) || !aligned(l->shared, 256)) return false;
+    if (!aligned(l->r_q, 16) || !aligned(l->r_s, 16) || !aligned(l->r_b, 16) ||
+        !aligned(l->shared, 256))
+        return false;
     return true;
 }
 
@@ -80,7 +84,7 @@ int bind_ws(const moe_layer_t *l, int T, void *d_ws, size_t ws_bytes, Ws *out) {
     if (!d_ws || !aligned(d_ws, 256)) return MOE_EWORKSPACE;
     WsLayout W = ws_fit(l, ws_bytes);
     if (W.total > ws_bytes || W.Tmax < T) return MOE_EWORKSPACE;
-    *out = ws_bind(d_ws, W);
+    *out = ws_bind(d_ws, W, *l);
     return MOE_OK;
 }
 
@@ -94,11 +98,18 @@ int launch_route(const moe_layer_t *l, const LayerDev &ly, const float *x, int T
     return cuda_status();
 }
 
-int run_layer(const moe_layer_t *l, const float *x, int T, int Tlimit, int flags, float *y,
-              int32_t *idx_out, float *gate_out, void *d_ws, size_t ws_bytes, void *stream) {
+int check_layer_call(const moe_layer_t *l, const float *x, int T, int Tlimit, int flags,
+                     const float *y) {
     if (!layer_ok(l) || !experts_ok(l) || !x || !y || T < 1 || T > Tlimit) return MOE_EINVAL;
     if (flags & ~MOE_RESIDUAL) return MOE_EINVAL;
     if (!aligned(x, 16) || !aligned(y, 16) || x == y) return MOE_EINVAL;
+    return MOE_OK;
+}
+
+// Prefill chunk (and any T beyond the decode kernel): router + gather + expert
+// kernels launched in sequence.
+int run_layer_chunk(const moe_layer_t *l, const float *x, int T, int flags, float *y,
+                    int32_t *idx_out, float *gate_out, void *d_ws, size_t ws_bytes, void *stream) {
     Ws ws;
     int rc = bind_ws(l, T, d_ws, ws_bytes, &ws);
     if (rc) return rc;
@@ -111,6 +122,69 @@ int run_layer(const moe_layer_t *l, const float *x, int T, int Tlimit, int flags
     if ((rc = cuda_status())) return rc;
     const int down_items = (ws.Umax + 1) * (l->H / 16);
     k_expert_down_simple<<<down_items, 128, 0, st>>>(ly, x, T, flags, y, ws);
+    return cuda_status();
+}
+
+struct DecodeLaunch {
+    int device = -1;
+    int sms = 0;
+    int occ[2] = {0, 0};
+    size_t smem[2] = {0, 0};
+};
+
+// Grid of the persistent decode kernel: every SM times the CTAs that fit.
+int decode_grid(const moe_layer_t *l, int nch, size_t smem, int *grid) {
+    static thread_local DecodeLaunch cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cuda_status();
+    if (cache.device != dev) {
+        cache = DecodeLaunch();
+        cache.device = dev;
+        if (cudaDeviceGetAttribute(&cache.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return cuda_status();
+    }
+    int k = nch - 1;
+    if (cache.smem[k] != smem || cache.occ[k] == 0) {
+        int occ = 0;
+        auto fn = nch == 1 ? k_decode<1> : k_decode<2>;
+        if (smem > 48 * 1024 &&
+            cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+            return cuda_status();
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, kDecThreads, smem) != cudaSuccess)
+            return cuda_status();
+        if (occ < 1) return MOE_EINVAL;
+        cache.occ[k] = occ;
+        cache.smem[k] = smem;
+    }
+    (void)l;
+    *grid = cache.sms * cache.occ[k];
+    return MOE_OK;
+}
+
+int run_decode(const moe_layer_t *l, const float *x, int T, int flags, float *y, int32_t *idx_out,
+               float *gate_out, void *d_ws, size_t ws_bytes, void *stream) {
+    Ws ws;
+    int rc = bind_ws(l, T, d_ws, ws_bytes, &ws);
+    if (rc) return rc;
+    DecodeArgs a;
+    a.ly = layer_dev(l);
+    a.x = x;
+    a.T = T;
+    a.flags = flags;
+    a.y = y;
+    a.idx_out = idx_out;
+    a.gate_out = gate_out;
+    a.ws = ws;
+    a.R = (l->E + kRouterRows - 1) / kRouterRows;
+    const int nch = T > 8 ? 2 : 1;
+    const size_t smem = decode_smem_bytes(*l, nch);
+    int grid = 0;
+    if ((rc = decode_grid(l, nch, smem, &grid))) return rc;
+    cudaStream_t st = as_stream(stream);
+    if (nch == 1)
+        k_decode<1><<<grid, kDecThreads, smem, st>>>(a);
+    else
+        k_decode<2><<<grid, kDecThreads, smem, st>>>(a);
     return cuda_status();
 }
 
@@ -192,7 +266,7 @@ int qgemv_affine4(const uint32_t *q, const uint16_t *s, const uint16_t *b, int N
     if (!q || !s || !b || !x || !y || N < 1 || K < kGroup || K % kGroup) return MOE_EINVAL;
     if (!aligned(q, 16) || !aligned(x, 16)) return MOE_EINVAL;
     QMat m{q, (const __half *)s, (const __half *)b, N, K};
-    k_qgemv4_simple<<<(N + 3) / 4, 128, 0, as_stream(stream)>>>(m, x, y);
+    k_qgemv4_mma<<<(N + 15) / 16, kGemvWarps * 32, 0, as_stream(stream)>>>(m, x, y);
     return cuda_status();
 }
 
@@ -212,15 +286,17 @@ int moe_layer_decode(const moe_layer_t *layer, const float *x, int T, int flags,
                      int32_t *idx_out, float *gate_out, moe_cache_t *cache, void *d_ws,
                      size_t ws_bytes, void *stream) {
     if (cache) return MOE_ENOTREADY;
-    return run_layer(layer, x, T, MOE_MAX_DECODE_TOKENS, flags, y, idx_out, gate_out, d_ws,
-                     ws_bytes, stream);
+    int rc = check_layer_call(layer, x, T, MOE_MAX_DECODE_TOKENS, flags, y);
+    if (rc) return rc;
+    return run_decode(layer, x, T, flags, y, idx_out, gate_out, d_ws, ws_bytes, stream);
 }
 
 int moe_layer_prefill_chunk(const moe_layer_t *layer, const float *x, int T, int flags, float *y,
                             int32_t *idx_out, float *gate_out, void *d_ws, size_t ws_bytes,
                             void *stream) {
-    return run_layer(layer, x, T, MOE_MAX_PREFILL_TOKENS, flags, y, idx_out, gate_out, d_ws,
-                     ws_bytes, stream);
+    int rc = check_layer_call(layer, x, T, MOE_MAX_PREFILL_TOKENS, flags, y);
+    if (rc) return rc;
+    return run_layer_chunk(layer, x, T, flags, y, idx_out, gate_out, d_ws, ws_bytes, stream);
 }
 
 int moe_cache_create(moe_cache_t **out, int H, int E, int I, const void *h_experts,

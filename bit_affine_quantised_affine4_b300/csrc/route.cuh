@@ -103,7 +103,7 @@ __device__ void build_schedule(const LayerDev &ly, int T, Ws ws) {
                 uid[e] = -1;
             }
         }
-        ws.ctrl[2] = (unsigned)U;
+        ws.ctrl[kU] = (unsigned)U;
     }
     __syncthreads();
     if (threadIdx.x < 32) {
@@ -174,7 +174,7 @@ k_route(LayerDev ly, const float *__restrict__ x, int T, Ws ws, int32_t *idx_out
     __syncthreads();
     if (threadIdx.x == 0) {
         __threadfence();
-        unsigned tk = atomicAdd(&ws.ctrl[1], 1u);
+        unsigned tk = atomicAdd(&ws.ctrl[kRouteTicket], 1u);
         is_last = (tk == gridDim.x - 1);
     }
     __syncthreads();
@@ -184,7 +184,7 @@ k_route(LayerDev ly, const float *__restrict__ x, int T, Ws ws, int32_t *idx_out
         warp_topk_softmax(ws.logits, ly.E, ly.topk, t, ws.idx, ws.gate, idx_out, gate_out);
     __syncthreads();
     build_schedule(ly, T, ws);
-    if (threadIdx.x == 0) ws.ctrl[1] = 0u;
+    if (threadIdx.x == 0) ws.ctrl[kRouteTicket] = 0u;
 }
 
 }  // namespace moe

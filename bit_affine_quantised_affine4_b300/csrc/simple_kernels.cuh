@@ -92,7 +92,7 @@ __global__ void __launch_bounds__(128) k_expert_up_simple(LayerDev ly, const flo
                                                           int T, Ws ws) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tilesR = ly.I / 16;
-    const unsigned U = __ldcg(&ws.ctrl[2]);
+    const unsigned U = __ldcg(&ws.ctrl[kU]);
     int item = blockIdx.x;
     const bool shared = item >= ws.Umax * tilesR;
     QMat m;
@@ -168,7 +168,7 @@ __global__ void __launch_bounds__(128) k_expert_down_simple(LayerDev ly, const f
                                                             Ws ws) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tiles = ly.H / 16;
-    const unsigned U = __ldcg(&ws.ctrl[2]);
+    const unsigned U = __ldcg(&ws.ctrl[kU]);
     int item = blockIdx.x;
     const bool shared = item >= ws.Umax * tiles;
     QMat m;
