@@ -28,7 +28,7 @@ ENTRY_POINTS = (
     "moe_workspace_bytes", "moe_workspace_init", "moe_workspace_status",
     "affine_quantise", "qgemv_affine4", "moe_route", "moe_layer_decode",
     "moe_layer_prefill_chunk", "moe_cache_create", "moe_cache_destroy",
-    "moe_cache_slots", "moe_cache_stats",
+    "moe_cache_slots", "moe_cache_stats", "moe_layer_decode_noalloc",
 )
 
 
@@ -69,6 +69,7 @@ def _load():
     L.moe_route.argtypes = [p, p, i, p, p, p, p, sz, p]
     L.moe_layer_decode.argtypes = [p, p, i, i, p, p, p, p, p, sz, p]
     L.moe_layer_prefill_chunk.argtypes = [p, p, i, i, p, p, p, p, sz, p]
+    L.moe_layer_decode_noalloc.argtypes = [p, p, i, i, p, p, p, p]
     L.moe_cache_create.argtypes = [p, i, i, i, p, sz, i]
     L.moe_cache_destroy.argtypes = [p]
     L.moe_cache_slots.argtypes = [p, p, p]
@@ -173,6 +174,16 @@ def moe_layer_decode(layer: moe_layer_t, x, ws, y=None, flags: int = 0, idx=None
     _check(lib.moe_layer_decode(C.byref(layer), _ptr(x), T, flags, _ptr(y), _ptr(idx), _ptr(gate),
                                 None if cache is None else cache.handle, _ptr(ws), ws.numel(),
                                 _stream(stream)), "moe_layer_decode")
+    return y
+
+
+def moe_layer_decode_noalloc(layer: moe_layer_t, x, y=None, flags: int = 0, idx=None, gate=None,
+                             stream=None):
+    """moe_layer_decode with the library's own static scratch (no workspace argument)."""
+    T = x.shape[0]
+    y = torch.empty_like(x) if y is None else y
+    _check(lib.moe_layer_decode_noalloc(C.byref(layer), _ptr(x), T, flags, _ptr(y), _ptr(idx),
+                                        _ptr(gate), _stream(stream)), "moe_layer_decode_noalloc")
     return y
 
 

@@ -4,6 +4,7 @@
 
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 
 #include "common.cuh"
 #include "route.cuh"
@@ -188,6 +189,34 @@ int run_decode(const moe_layer_t *l, const float *x, int T, int flags, float *y,
     return cuda_status();
 }
 
+// ------------------------------------------------------------------ allocation-free decode
+// Scratch of moe_layer_decode_noalloc.  In host code this name is only a stand-in
+// for the device array, so the host looks up its device address once per device
+// and hands that address to the kernel like any workspace.
+__device__ __align__(256) unsigned char g_noalloc_scratch[MOE_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the current device's scratch array; the first call on a device
+// looks it up and zeroes the array (then waits for the device).
+int noalloc_scratch(void **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cuda_status();
+    if (dev < 0 || dev >= kMaxDevices) return MOE_EINVAL;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return cuda_status();
+        if (cudaMemset(p, 0, MOE_NOALLOC_SCRATCH_BYTES) != cudaSuccess) return cuda_status();
+        if (cudaDeviceSynchronize() != cudaSuccess) return cuda_status();
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return MOE_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -308,5 +337,20 @@ int moe_cache_create(moe_cache_t **out, int H, int E, int I, const void *h_exper
 int moe_cache_destroy(moe_cache_t *cache) { return cache ? MOE_ENOTREADY : MOE_OK; }
 int moe_cache_slots(const moe_cache_t *, int32_t *, uint32_t *) { return MOE_ENOTREADY; }
 int moe_cache_stats(const moe_cache_t *, uint64_t *, uint64_t *, uint64_t *) { return MOE_ENOTREADY; }
+
+int moe_layer_decode_noalloc(const moe_layer_t *layer, const float *x, int T, int flags, float *y,
+                             int32_t *idx_out, float *gate_out, void *stream) {
+    int rc = check_layer_call(layer, x, T, MOE_MAX_DECODE_TOKENS, flags, y);
+    if (rc) return rc;
+    if (ws_layout(*layer, T).total > MOE_NOALLOC_SCRATCH_BYTES) {
+        if (getenv("MOE_DEBUG"))
+            fprintf(stderr, "libmoe: layer needs %zu bytes of scratch at T=%d, more than %u\n",
+                    ws_layout(*layer, T).total, T, MOE_NOALLOC_SCRATCH_BYTES);
+        return MOE_EWORKSPACE;
+    }
+    void *ws = nullptr;
+    if ((rc = noalloc_scratch(&ws))) return rc;
+    return run_decode(layer, x, T, flags, y, idx_out, gate_out, ws, MOE_NOALLOC_SCRATCH_BYTES, stream);
+}
 
 }  // extern "C"

@@ -191,6 +191,34 @@ MOE_API int moe_layer_prefill_chunk(const moe_layer_t *layer, const float *x, in
                             int32_t *idx_out, float *gate_out, void *d_ws, size_t ws_bytes,
                             void *stream);
 
+/*
+ * moe_layer_decode_noalloc -- the same decode step as moe_layer_decode (no cache),
+ * for callers that cannot allocate device memory: for example a plug-in running
+ * inside a host framework that reserves the GPU's memory through its own allocator
+ * and forbids other cudaMalloc calls, or a latency-critical loop that may not
+ * risk cudaMalloc's implicit device synchronisation.  The pages have no
+ * counterpart to this call; it only changes where the scratch memory lives.
+ *
+ * It allocates nothing: its scratch is one file-scope device array of
+ * MOE_NOALLOC_SCRATCH_BYTES inside libmoe, present on every GPU that loads the
+ * library until the process exits.  The caller still supplies x, y and the
+ * optional idx/gate outputs (device pointers, as in moe_layer_decode).
+ *   - The first call on a device does a one-time set-up with that device
+ *     current: it looks up the array's device address and zeroes the array
+ *     (this synchronises the device).  Make that first call before any stream
+ *     capture.
+ *   - Every call shares the one array, so calls that overlap on the GPU (two
+ *     streams, or two host threads) race and give wrong results; serialise them.
+ *     Each call leaves the control words at zero for the next one; after a
+ *     MOE_ETIMEOUT from a device-side wait, later results are undefined.
+ *   - Returns MOE_EWORKSPACE when the layer at T tokens needs more scratch than
+ *     MOE_NOALLOC_SCRATCH_BYTES (the full-size layer, hidden 2816 with 128
+ *     experts, needs about 2.5 MB at T = 16); other errors as moe_layer_decode.
+ */
+#define MOE_NOALLOC_SCRATCH_BYTES (4u << 20)
+MOE_API int moe_layer_decode_noalloc(const moe_layer_t *layer, const float *x, int T, int flags,
+                                     float *y, int32_t *idx_out, float *gate_out, void *stream);
+
 /* ---------------------------------------------------------------- LFU cache */
 
 /*
