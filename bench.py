@@ -182,7 +182,7 @@ def run_ours(args):
     l2 = getattr(props, "L2_cache_size", 126 * 2**20)
 
     # enough distinct layer copies that a step never finds its weights in L2
-    copies = max(4, int(np.ceil(4 * l2 / DECODE_BYTES)))
+    copies = args.copies or max(4, int(np.ceil(4 * l2 / DECODE_BYTES)))
     layer = build_layer(moe, copies)
     views = [layer.view(c) for c in range(copies)]
     NX = 64
@@ -253,7 +253,7 @@ def run_ours(args):
                 "h2d_bytes_per_step": H * 4, "d2h_bytes_per_step": H * 4,
                 "note": "eager calls through the Python binding of the C ABI, pinned host x/y, "
                         "H2D + decode + D2H per step"},
-        "gpu_launches": args.steps * 3,
+        "gpu_launches": args.steps,  # one persistent k_decode launch per step
         "clocks": clocks,
     }
     line.update(extra)
@@ -344,6 +344,8 @@ def main():
     ap.add_argument("--quick", action="store_true", help="headline only, no side measurements")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle timing")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--copies", type=int, default=0,
+                    help="distinct layer copies to rotate over (default: enough to exceed 4x L2)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
