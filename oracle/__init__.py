@@ -66,6 +66,9 @@ def _declare(L):
     L.orc_expert_blob_bytes.argtypes = [C.c_int, C.c_int]
     L.orc_expert_blob_bytes.restype = C.c_size_t
     L.orc_expert_blob_offsets.argtypes = [C.c_int, C.c_int, _p]
+    L.orc_tile_blob_bytes.argtypes = [C.c_int, C.c_int]
+    L.orc_tile_blob_bytes.restype = C.c_size_t
+    L.orc_untile_expert.argtypes = [_p, C.c_int, C.c_int, _p]
     L.orc_expert.argtypes = [_p, C.c_int, C.c_int, _p, _p, _p]
     L.orc_moe_layer.argtypes = [C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, _p, _p, _p, _p, _p,
                                 _p, C.c_int, _p, C.c_int, _p, _p, _p]
@@ -175,6 +178,20 @@ def pack_expert(H: int, I: int, gu, d) -> np.ndarray:
         a = np.ascontiguousarray(a)
         raw = a.view(np.uint8).reshape(-1)
         blob[o:o + raw.size] = raw
+    return blob
+
+
+def tile_blob_bytes(H: int, I: int) -> int:
+    return int(lib().orc_tile_blob_bytes(H, I))
+
+
+def untile_expert(tiled, H: int, I: int) -> np.ndarray:
+    """The library's tile-layout blob of one expert -> the MLX-layout blob (uint8)."""
+    tiled = _c(tiled, np.uint8)
+    if tiled.size != tile_blob_bytes(H, I):
+        raise ValueError("tile blob of %d bytes, expected %d" % (tiled.size, tile_blob_bytes(H, I)))
+    blob = np.zeros(expert_blob_bytes(H, I), np.uint8)
+    _check(lib().orc_untile_expert(_ptr(tiled), H, I, _ptr(blob)), "untile_expert")
     return blob
 
 

@@ -259,6 +259,83 @@ void orc_expert_blob_offsets(int H, int I, size_t *off6) {
     off6[3] = L.d_q;  off6[4] = L.d_s;  off6[5] = L.d_b;
 }
 
+/*
+ * The library's tile layout of an expert (a storage order of the same codes,
+ * scales and biases; the pages give no layout, this one is the library's own).
+ * A tile is 16 matrix rows (an "a" row and a "b" row for each r = 0..7) by one
+ * group of 64 columns, 576 bytes:
+ *   bytes 16L..16L+15 (lane L = 4r + c, r = 0..7, c = 0..3): four 32-bit words,
+ *     words 2c and 2c+1 of the group in row a(r), then the same two words of
+ *     row b(r)  (word w of a group holds columns 8w..8w+7, MLX nibble order);
+ *   bytes 512 + 8r .. 512 + 8r + 7: four fp16 values, scale and bias of row a(r)
+ *     for this group, then scale and bias of row b(r).
+ * Gate/up part, at byte 0: tile (it, g), it = 0..I/8-1, g = 0..H/64-1, at
+ *   576 (it (H/64) + g), with a(r) = gate row 8 it + r and b(r) = up row 8 it + r
+ *   (row I + 8 it + r of the [2I][H] gate/up matrix).
+ * Down part, at byte 576 (I/8)(H/64): tile (rt, g), rt = 0..H/16-1,
+ *   g = 0..I/64-1, at 576 (rt (I/64) + g) from the part's start, with
+ *   a(r) = row 16 rt + r and b(r) = row 16 rt + 8 + r of the [H][I] down matrix.
+ */
+#define TILE_BYTES 576
+
+size_t orc_tile_blob_bytes(int H, int I) {
+    if (H <= 0 || I <= 0 || H % 128 || I % GROUP) return 0;
+    return (size_t)TILE_BYTES * ((size_t)(I / 8) * (H / GROUP) + (size_t)(H / 16) * (I / GROUP));
+}
+
+/* Copies one tile's words and scale/bias pairs back to MLX row-major arrays. */
+static void untile_one(const uint8_t *tile, int g, const int rows_a[8], const int rows_b[8],
+                       uint32_t *q, uint16_t *s, uint16_t *b, int words_per_row, int groups) {
+    for (int L = 0; L < 32; L++) {
+        const int r = L / 4, c = L % 4;
+        const uint32_t *w = (const uint32_t *)(tile + 16 * L);
+        q[(size_t)rows_a[r] * words_per_row + 8 * g + 2 * c] = w[0];
+        q[(size_t)rows_a[r] * words_per_row + 8 * g + 2 * c + 1] = w[1];
+        q[(size_t)rows_b[r] * words_per_row + 8 * g + 2 * c] = w[2];
+        q[(size_t)rows_b[r] * words_per_row + 8 * g + 2 * c + 1] = w[3];
+    }
+    for (int r = 0; r < 8; r++) {
+        const uint16_t *h = (const uint16_t *)(tile + 512 + 8 * r);
+        s[(size_t)rows_a[r] * groups + g] = h[0];
+        b[(size_t)rows_a[r] * groups + g] = h[1];
+        s[(size_t)rows_b[r] * groups + g] = h[2];
+        b[(size_t)rows_b[r] * groups + g] = h[3];
+    }
+}
+
+/* Tile-layout blob -> MLX-layout blob (orc_expert_blob_bytes(H, I) bytes). */
+int orc_untile_expert(const uint8_t *tiled, int H, int I, uint8_t *blob) {
+    if (!orc_tile_blob_bytes(H, I)) return ORC_EINVAL;
+    blob_layout L = layout_of(H, I);
+    memset(blob, 0, L.total);
+    const int G = H / GROUP, Gi = I / GROUP;
+    uint32_t *guq = (uint32_t *)(blob + L.gu_q);
+    uint16_t *gus = (uint16_t *)(blob + L.gu_s), *gub = (uint16_t *)(blob + L.gu_b);
+    uint32_t *dq = (uint32_t *)(blob + L.d_q);
+    uint16_t *ds = (uint16_t *)(blob + L.d_s), *db = (uint16_t *)(blob + L.d_b);
+    int ra[8], rb[8];
+    for (int it = 0; it < I / 8; it++)
+        for (int g = 0; g < G; g++) {
+            for (int r = 0; r < 8; r++) {
+                ra[r] = 8 * it + r;
+                rb[r] = I + 8 * it + r;
+            }
+            untile_one(tiled + (size_t)TILE_BYTES * ((size_t)it * G + g), g, ra, rb, guq, gus, gub,
+                       H / 8, G);
+        }
+    const uint8_t *down = tiled + (size_t)TILE_BYTES * (I / 8) * G;
+    for (int rt = 0; rt < H / 16; rt++)
+        for (int g = 0; g < Gi; g++) {
+            for (int r = 0; r < 8; r++) {
+                ra[r] = 16 * rt + r;
+                rb[r] = 16 * rt + 8 + r;
+            }
+            untile_one(down + (size_t)TILE_BYTES * ((size_t)rt * Gi + g), g, ra, rb, dq, ds, db,
+                       I / 8, Gi);
+        }
+    return ORC_OK;
+}
+
 /* GELU, tanh form: 0.5 z (1 + tanh(sqrt(2/pi) (z + 0.044715 z^3))). */
 double orc_gelu_tanh(double z) {
     const double c = sqrt(2.0 / 3.14159265358979323846);

@@ -413,3 +413,42 @@ def test_lfu_rejects_bad_requests_without_change():
     after = lfu.state()
     for a, b in zip(before, after):
         assert np.array_equal(a, b)
+
+
+# ----------------------------------------------------------------- tile layout
+
+def _mlx_parts(blob, H, I):
+    off = oracle.expert_blob_offsets(H, I)
+    sizes = [2 * I * H // 2, 2 * I * (H // 64) * 2, 2 * I * (H // 64) * 2, H * I // 2,
+             H * (I // 64) * 2, H * (I // 64) * 2]
+    shapes = [(2 * I, H // 8), (2 * I, H // 64), (2 * I, H // 64), (H, I // 8), (H, I // 64), (H, I // 64)]
+    dt = [np.uint32, np.uint16, np.uint16, np.uint32, np.uint16, np.uint16]
+    names = ["gu_q", "gu_s", "gu_b", "d_q", "d_s", "d_b"]
+    return {n: blob[o:o + sz].view(d).reshape(sh) for n, o, sz, sh, d in zip(names, off, sizes, shapes, dt)}
+
+
+def test_untile_hand_worked_positions():
+    g = _load("tile_layout.json")
+    H, I = g["H"], g["I"]
+    n = oracle.tile_blob_bytes(H, I)
+    assert n == 24 * 576
+    tiled = np.arange(n // 2, dtype=np.uint16).view(np.uint8)
+    parts = _mlx_parts(oracle.untile_expert(tiled, H, I), H, I)
+    words = tiled.view(np.uint32)
+    for e in g["words"]:
+        assert parts[e["part"]][e["row"], e["word"]] == words[e["tiled_word"]], e["why"]
+    for e in g["halves"]:
+        assert parts[e["part"]][e["row"], e["group"]] == e["tiled_half"], e["why"]
+
+
+@pytest.mark.parametrize("H,I", [(128, 64), (256, 128), (384, 192)])
+def test_untile_is_a_permutation(H, I):
+    """Every halfword of the tile blob lands in exactly one MLX position and the
+    sizes agree (no padding in either form at these shapes)."""
+    n = oracle.tile_blob_bytes(H, I)
+    assert n == oracle.expert_blob_bytes(H, I) == 3 * I * H * 36 // 64
+    tiled = np.arange(n // 2, dtype=np.uint32).astype(np.uint16).view(np.uint8)
+    if n // 2 > 65536:  # make halfwords unique with a second pass on the high part
+        pytest.skip("shape too large for unique 16-bit tags")
+    out = oracle.untile_expert(tiled, H, I).view(np.uint16)
+    assert np.array_equal(np.sort(out), np.arange(n // 2, dtype=np.uint16))
