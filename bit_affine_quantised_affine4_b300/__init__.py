@@ -21,14 +21,17 @@ MOE_MAX_TOPK = 8
 MOE_MAX_EXPERTS = 256
 MOE_MAX_DECODE_TOKENS = 16
 MOE_MAX_PREFILL_TOKENS = 128
+MOE_MAX_CACHE_SLOTS = 64
 
 # Every function the header declares (checked against include/moe.h by the tests).
 ENTRY_POINTS = (
     "moe_status_string", "moe_expert_blob_bytes", "moe_expert_blob_offsets",
+    "moe_tile_blob_bytes", "moe_expert_tile",
     "moe_workspace_bytes", "moe_workspace_init", "moe_workspace_status",
     "affine_quantise", "qgemv_affine4", "moe_route", "moe_layer_decode",
     "moe_layer_prefill_chunk", "moe_cache_create", "moe_cache_destroy",
     "moe_cache_slots", "moe_cache_stats", "moe_layer_decode_noalloc",
+    "moe_lfu_create", "moe_lfu_destroy", "moe_lfu_step", "moe_lfu_state",
 )
 
 
@@ -60,6 +63,9 @@ def _load():
     L.moe_expert_blob_bytes.argtypes = [i, i]
     L.moe_expert_blob_bytes.restype = sz
     L.moe_expert_blob_offsets.argtypes = [i, i, p]
+    L.moe_tile_blob_bytes.argtypes = [i, i]
+    L.moe_tile_blob_bytes.restype = sz
+    L.moe_expert_tile.argtypes = [p, i, i, p, p]
     L.moe_workspace_bytes.argtypes = [p, i]
     L.moe_workspace_bytes.restype = sz
     L.moe_workspace_init.argtypes = [p, sz, p]
@@ -74,8 +80,13 @@ def _load():
     L.moe_cache_destroy.argtypes = [p]
     L.moe_cache_slots.argtypes = [p, p, p]
     L.moe_cache_stats.argtypes = [p, p, p, p]
+    L.moe_lfu_create.argtypes = [p, i, i]
+    L.moe_lfu_destroy.argtypes = [p]
+    L.moe_lfu_step.argtypes = [p, p, i, p, p]
+    L.moe_lfu_state.argtypes = [p, p, p, p, p, p]
     for name in ENTRY_POINTS:
-        if name not in ("moe_status_string", "moe_expert_blob_bytes", "moe_workspace_bytes"):
+        if name not in ("moe_status_string", "moe_expert_blob_bytes", "moe_workspace_bytes",
+                        "moe_tile_blob_bytes"):
             getattr(L, name).restype = i
     return L
 
@@ -111,6 +122,16 @@ def moe_expert_blob_offsets(H: int, I: int):
     off = (C.c_size_t * 6)()
     _check(lib.moe_expert_blob_offsets(H, I, off), "moe_expert_blob_offsets")
     return list(off)
+
+
+def moe_tile_blob_bytes(H: int, I: int) -> int:
+    return int(lib.moe_tile_blob_bytes(H, I))
+
+
+def moe_expert_tile(mlx_blob: torch.Tensor, H: int, I: int, tile_blob: torch.Tensor, stream=None):
+    """MLX-layout expert blob -> tile-layout blob (both uint8 CUDA tensors)."""
+    _check(lib.moe_expert_tile(_ptr(mlx_blob), H, I, _ptr(tile_blob), _stream(stream)), "moe_expert_tile")
+    return tile_blob
 
 
 # ------------------------------------------------------------------ kernels
@@ -197,4 +218,80 @@ def moe_layer_prefill_chunk(layer: moe_layer_t, x, ws, y=None, flags: int = 0, i
     return y
 
 
-from .weights import Layer, make_layer, pack_expert_blob  # noqa: E402
+# ------------------------------------------------------------------ LFU policy and cache
+
+class LFU:
+    """The cache policy on the host (moe_lfu_*), for inspection and tests."""
+
+    def __init__(self, slots: int = 16, E: int = 128):
+        self.slots, self.E = slots, E
+        h = C.c_void_p()
+        _check(lib.moe_lfu_create(C.byref(h), slots, E), "moe_lfu_create")
+        self.handle = h
+
+    def __del__(self):
+        if getattr(self, "handle", None):
+            lib.moe_lfu_destroy(self.handle)
+            self.handle = None
+
+    def step(self, request):
+        import numpy as np
+        req = np.ascontiguousarray(request, dtype=np.int32)
+        n = req.size
+        slot = np.full(max(n, 1), -1, np.int32)
+        hit = np.zeros(max(n, 1), np.uint8)
+        _check(lib.moe_lfu_step(self.handle, req.ctypes.data if n else None, n, slot.ctypes.data,
+                                hit.ctypes.data), "moe_lfu_step")
+        return slot[:n], hit[:n].astype(bool)
+
+    def state(self):
+        import numpy as np
+        eos = np.empty(self.slots, np.int32)
+        cnt = np.empty(self.slots, np.uint32)
+        last = np.empty(self.slots, np.int64)
+        h, m = C.c_uint64(0), C.c_uint64(0)
+        _check(lib.moe_lfu_state(self.handle, eos.ctypes.data, cnt.ctypes.data, last.ctypes.data,
+                                 C.byref(h), C.byref(m)), "moe_lfu_state")
+        return eos, cnt, last, h.value, m.value
+
+
+class Cache:
+    """A per-layer expert cache (moe_cache_*) over tile-layout expert blobs held in
+    host memory: `host_experts` is a uint8 CPU tensor [E, stride] (pin it for the
+    copies to overlap compute); it must outlive the cache."""
+
+    def __init__(self, H: int, E: int, I: int, host_experts: torch.Tensor, slots: int = 16):
+        assert host_experts.device.type == "cpu" and host_experts.dtype == torch.uint8
+        assert host_experts.dim() == 2 and host_experts.shape[0] == E and host_experts.is_contiguous()
+        self.H, self.E, self.I, self.slots = H, E, I, slots
+        self.host_experts = host_experts
+        h = C.c_void_p()
+        _check(lib.moe_cache_create(C.byref(h), H, E, I, C.c_void_p(host_experts.data_ptr()),
+                                    host_experts.stride(0), slots), "moe_cache_create")
+        self.handle = h
+
+    def close(self):
+        if getattr(self, "handle", None):
+            _check(lib.moe_cache_destroy(self.handle), "moe_cache_destroy")
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def slots_state(self):
+        import numpy as np
+        eos = np.empty(self.slots, np.int32)
+        cnt = np.empty(self.slots, np.uint32)
+        _check(lib.moe_cache_slots(self.handle, eos.ctypes.data, cnt.ctypes.data), "moe_cache_slots")
+        return eos, cnt
+
+    def stats(self):
+        h, m, b = C.c_uint64(0), C.c_uint64(0), C.c_uint64(0)
+        _check(lib.moe_cache_stats(self.handle, C.byref(h), C.byref(m), C.byref(b)), "moe_cache_stats")
+        return h.value, m.value, b.value
+
+
+from .weights import Layer, make_layer, pack_expert_blob, pack_expert_tiles  # noqa: E402

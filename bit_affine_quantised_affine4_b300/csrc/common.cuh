@@ -62,63 +62,57 @@ struct LayerDev {
 
 // Workspace (see moe_workspace_bytes).  Control words live at the start:
 enum CtrlWord {
-    kErr = 0,        // a bounded wait gave up (sticky until moe_workspace_status)
-    kRouteTicket,    // router items finished (the last one runs top-k)
-    kU,              // number of distinct routed experts of this call
-    kQueue0,         // work queue: router, shared gate/up, shared down items
-    kQueue1,         // work queue: routed gate/up items
-    kQueue2,         // work queue: routed down items
-    kXPrep,          // router items whose slice of x is converted
-    kRouted,         // 1 once idx/gate/schedule are published
-    kSharedUp,       // shared gate/up items finished
-    kExit,           // CTAs finished (the last one resets the control words)
+    kErr = 0,         // a bounded wait gave up (sticky until moe_workspace_status)
+    kRouteTicket,     // standalone router: CTAs finished (the last one runs top-k)
+    kRouteCnt,        // decode: router rows published
+    kGuDone,          // decode: gate/up tiles finished
+    kExit,            // decode: CTAs finished (the last one resets the words above)
     kCtrlWords = 16
 };
 
+// Parts of the shared expert's down matrix (K = Is) cut to the routed experts'
+// K = I, so that every down unit has at most I/64 groups.
+__host__ __device__ inline int shared_parts(int I, int Is) { return (Is / kGroup + I / kGroup - 1) / (I / kGroup); }
+
 struct Ws {
     unsigned *ctrl;
-    unsigned *tile_cnt;  // [H/16] tickets of the down combine (16-row tiles)
-    unsigned *up_done;   // [Umax] gate/up items finished per distinct expert
-    float *logits;       // [Tmax][E]
-    int *idx;            // [Tmax][topk]
-    float *gate;         // [Tmax][topk]
-    int *uexp;           // [Umax] expert id of distinct expert u (ascending ids)
-    int *ucount;         // [Umax] tokens using u
-    int *ulist;          // [Umax][Tmax] pair ids p = t*topk + k, ascending
-    float *h;            // [Tmax*topk][I]  routed activations (fp32 path)
-    float *hs;           // [Tmax][Is]      shared activations (fp32 path)
-    float *partial;      // [Tmax*topk + Tmax][H] per-pair down outputs, then shared
-    __half *x16;         // [Tmax][H]   tokens in fp16, fragment order
-    float *xsum;         // [Tmax][H/64] group sums of the fp16 tokens
-    __half *h16;         // [Tmax*topk][I] routed activations, fp16 fragment order
-    __half *hs16;        // [Tmax][Is]     shared activations, fp16 fragment order
-    int Tmax, Umax;
+    unsigned *ticket;  // [H/16] tickets of the 16-row output tiles
+    float *logits;     // [Tmax][E]
+    int *idx;          // [Tmax][topk] routing of a separate router launch (cached decode)
+    float *gate;       // [Tmax][topk]
+    __half *h16;       // [Tmax*topk][I]  routed activations (compact slots)
+    __half *hs16;      // [Tmax][Is]      shared activations
+    float *pr;         // [Tmax*topk][H]  routed down partials
+    float *ps;         // [P][Tmax][H]    shared down partials
+    int Tmax;
 };
 
+// The control words and the 16-row-tile tickets sit in a header of fixed size
+// (enough tickets for the largest hidden size the layer calls accept), so one
+// workspace can serve layers of different shapes in turn: every call leaves the
+// header zeroed for the next one whatever the layer.
+constexpr int kMaxHiddenLayer = 4096;
+constexpr int kMaxTickets = kMaxHiddenLayer / 16;
+constexpr size_t kWsHeaderBytes = (kCtrlWords + kMaxTickets) * sizeof(unsigned);
+
 struct WsLayout {
-    size_t ctrl, logits, idx, gate, uexp, ucount, ulist, h, hs, partial, x16, xsum, h16, hs16, total;
-    int Tmax, Umax;
+    size_t ctrl, logits, idx, gate, h16, hs16, pr, ps, total;
+    int Tmax;
 };
 
 inline WsLayout ws_layout(const moe_layer_t &l, int Tmax) {
     WsLayout W;
     W.Tmax = Tmax;
-    W.Umax = Tmax * l.topk < l.E ? Tmax * l.topk : l.E;
+    const int P = shared_parts(l.I, l.Is);
     size_t off = 0;
-    W.ctrl = off;    off = up256(off + sizeof(unsigned) * (kCtrlWords + l.H / 16 + W.Umax));
-    W.logits = off;  off = up256(off + sizeof(float) * Tmax * l.E);
-    W.idx = off;     off = up256(off + sizeof(int) * Tmax * l.topk);
-    W.gate = off;    off = up256(off + sizeof(float) * Tmax * l.topk);
-    W.uexp = off;    off = up256(off + sizeof(int) * W.Umax);
-    W.ucount = off;  off = up256(off + sizeof(int) * W.Umax);
-    W.ulist = off;   off = up256(off + sizeof(int) * size_t(W.Umax) * Tmax);
-    W.h = off;       off = up256(off + sizeof(float) * size_t(Tmax) * l.topk * l.I);
-    W.hs = off;      off = up256(off + sizeof(float) * size_t(Tmax) * l.Is);
-    W.partial = off; off = up256(off + sizeof(float) * size_t(Tmax) * (l.topk + 1) * l.H);
-    W.x16 = off;     off = up256(off + sizeof(__half) * size_t(Tmax) * l.H);
-    W.xsum = off;    off = up256(off + sizeof(float) * size_t(Tmax) * (l.H / kGroup));
-    W.h16 = off;     off = up256(off + sizeof(__half) * size_t(Tmax) * l.topk * l.I);
-    W.hs16 = off;    off = up256(off + sizeof(__half) * size_t(Tmax) * l.Is);
+    W.ctrl = off;   off = up256(off + kWsHeaderBytes);
+    W.logits = off; off = up256(off + sizeof(float) * Tmax * l.E);
+    W.idx = off;    off = up256(off + sizeof(int) * Tmax * l.topk);
+    W.gate = off;   off = up256(off + sizeof(float) * Tmax * l.topk);
+    W.h16 = off;    off = up256(off + sizeof(__half) * size_t(Tmax) * l.topk * l.I);
+    W.hs16 = off;   off = up256(off + sizeof(__half) * size_t(Tmax) * l.Is);
+    W.pr = off;     off = up256(off + sizeof(float) * size_t(Tmax) * l.topk * l.H);
+    W.ps = off;     off = up256(off + sizeof(float) * size_t(P) * Tmax * l.H);
     W.total = off;
     return W;
 }
@@ -127,23 +121,16 @@ inline Ws ws_bind(void *base, const WsLayout &W, const moe_layer_t &l) {
     uint8_t *p = (uint8_t *)base;
     Ws w;
     w.ctrl = (unsigned *)(p + W.ctrl);
-    w.tile_cnt = w.ctrl + kCtrlWords;
-    w.up_done = w.tile_cnt + l.H / 16;
+    w.ticket = w.ctrl + kCtrlWords;
     w.logits = (float *)(p + W.logits);
     w.idx = (int *)(p + W.idx);
     w.gate = (float *)(p + W.gate);
-    w.uexp = (int *)(p + W.uexp);
-    w.ucount = (int *)(p + W.ucount);
-    w.ulist = (int *)(p + W.ulist);
-    w.h = (float *)(p + W.h);
-    w.hs = (float *)(p + W.hs);
-    w.partial = (float *)(p + W.partial);
-    w.x16 = (__half *)(p + W.x16);
-    w.xsum = (float *)(p + W.xsum);
     w.h16 = (__half *)(p + W.h16);
     w.hs16 = (__half *)(p + W.hs16);
+    w.pr = (float *)(p + W.pr);
+    w.ps = (float *)(p + W.ps);
     w.Tmax = W.Tmax;
-    w.Umax = W.Umax;
+    (void)l;
     return w;
 }
 

@@ -1,544 +1,626 @@
-// decode.cuh -- the whole MoE layer for 1..16 decode tokens in one persistent kernel.
+// decode.cuh -- the whole MoE layer for 1..16 decode tokens in one persistent,
+// cooperative kernel (one CTA per SM).
 //
 // The layer (devtrends page, section "Qual e il trucco principale dell'architettura";
 // remio.ai page, sections "Mac Gemma 4 26B entra nello spazio disponibile..." and
-// "L'affermazione dei 2 GB..."): an 8-bit router picks 8 experts per token, the
-// routed experts and an always-on shared expert run GeGLU FFNs on 4-bit affine
-// weights, and the outputs are combined with the softmax gates.
+// "L'affermazione dei 2 GB..."): an 8-bit router picks the top-8 experts per
+// token, the routed experts and an always-on shared expert run GeGLU FFNs on
+// 4-bit affine weights, and the outputs are combined with the softmax gates.
 //
-// Work is cut into items taken from three queues in order; an item only ever waits
-// for items of earlier queues or earlier positions, which running CTAs hold, so the
-// schedule cannot deadlock whatever the number of resident CTAs.
-//   queue 0: router items (convert a slice of the tokens to fp16 fragment order,
-//            then 8 router rows; the last one runs top-k/softmax and publishes the
-//            schedule), shared gate/up items (16 gate + 16 up rows), shared down
-//            items (64 output rows; they prefetch their weights to L2, then wait
-//            for the shared activations)
-//   queue 1: routed gate/up items, (distinct expert, 16 rows) -- after routing
-//   queue 2: routed down items, (distinct expert, 64 rows); they prefetch, wait for
-//            their expert's activations, and the last item of each 64-row tile
-//            combines y = sum_k g_k * routed_k + shared (+ x) in fixed order.
-// Every wait is bounded: on expiry the kernel raises the workspace error flag and
-// all CTAs drain without further work.  The last CTA to leave resets the control
-// words so the workspace is ready for the next call.
+// Each CTA has 16 compute warps and one producer warp.  Weights arrive through a
+// ring of shared-memory stages filled by bulk copies (TMA) and guarded by
+// mbarriers; every weight byte that is known is also prefetched into L2 as early
+// as possible, so HBM streams continuously while the SMs compute.
+//
+//   phase A  producer: copies this CTA's shared-expert gate/up tiles, prefetches
+//            a slice of the shared down matrix, computes its router rows (CUDA
+//            cores, 8-bit), publishes them, waits until all E rows are in.
+//            compute warps: shared gate/up tiles (below).
+//   routing  every CTA ranks the logits itself (identical results everywhere),
+//            and builds the schedule: distinct experts U in ascending id, the
+//            tokens using each, and a compact slot per (token, choice).
+//   phase B  gate/up: the CTA's tiles j = b, b+nC, ... of [shared | routed u=0..U-1]
+//            (one tile = 8 gate rows + the 8 matching up rows, full K).  The 16
+//            warps split K; partial sums meet in shared memory, GeGLU is applied,
+//            and h is written in fp16 (compact slots for routed experts).
+//            down: units (matrix, 16 output rows) in matrix-major order, a
+//            contiguous range per CTA, one unit per warp with full K; h of the
+//            CTA's matrices is copied to shared memory once every CTA's gate/up
+//            tiles are done.  Each unit writes fp32 partial rows; the last unit to
+//            finish a 16-row tile (a ticket) sums the tile's partials in a fixed
+//            order: y = sum_k gate_k * routed_k + sum_parts shared (+ x).
+// All cross-CTA waits are bounded (sync.cuh); results do not depend on timing.
 #pragma once
 
 #include "common.cuh"
 #include "mma_core.cuh"
 #include "route.cuh"
+#include "sync.cuh"
+#include "tile.cuh"
 
 namespace moe {
 
-constexpr int kDecWarps = 8;
-constexpr int kDecThreads = kDecWarps * 32;
-constexpr int kRouterRows = kDecWarps;  // router rows per router item
-constexpr int kDownRows = 64;           // output rows per down item
-constexpr long long kSpinLimit = 1ll << 22;  // polls of ~128 ns: about half a second
+constexpr int kCW = 16;                       // compute warps
+constexpr int kCThreads = kCW * 32;           // compute threads
+constexpr int kDecThreads = kCThreads + 32;   // + producer warp
+constexpr int kMaxStages = 4;
+constexpr int kMaxUnitsPerCta = 512;
+constexpr int kMaxPairs = MOE_MAX_DECODE_TOKENS * MOE_MAX_TOPK;
+
+// What one launch does: the shared expert, the routed experts, or both; and
+// whether the routing comes from an earlier router launch (idx_pre/gate_pre)
+// instead of the kernel's own router.  A launch with the routed experts also
+// combines the output tiles (reading the shared partials an earlier launch may
+// have written).
+constexpr int kModeShared = 1, kModeRouted = 2, kModePre = 4;
 
 struct DecodeArgs {
-    LayerDev ly;
+    // layer
+    int H, E, topk, I, Is;
+    const uint32_t *rq;
+    const __half *rs, *rb;
+    const float *bias;
+    const uint8_t *experts;
+    size_t stride;
+    const uint8_t *shared;
+    TileLayout Lr, Ls;  // routed and shared expert tile layouts
+    int P;              // shared down matrix split in P parts of <= Lr.Gi groups
+    // call
     const float *x;
-    int T;
-    int flags;
+    int T, flags;
     float *y;
     int32_t *idx_out;
     float *gate_out;
-    Ws ws;
-    int R;  // router items
+    // workspace
+    unsigned *ctrl, *ticket;
+    float *logits;
+    __half *h16;   // routed h: per distinct expert u a block [Gi][n_u][64] at slot base * I
+    __half *hs16;  // shared h: [Gs][T][64]
+    float *pr;     // routed partials [T*topk][H]
+    float *ps;     // shared partials [P][T][H]
+    // launch
+    int stages, SB, UPS, red_off, hsm_off, hsm_mat_bytes;
+    int mode;
+    const int *idx_pre;      // [T][topk] routing of an earlier router launch (kModePre)
+    const float *gate_pre;   // [T][topk]
+    int use_map;             // expert e's blob is experts + slot_map[e] * stride (cache slots)
+    short slot_map[MOE_MAX_EXPERTS];
 };
 
-__device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
+// fp16 pair (lo, hi) of a 32-bit word -> floats
+__device__ __forceinline__ float lo_half(uint32_t w) { return __half2float(__ushort_as_half((unsigned short)(w & 0xFFFFu))); }
+__device__ __forceinline__ float hi_half(uint32_t w) { return __half2float(__ushort_as_half((unsigned short)(w >> 16))); }
+
+// acc += s*2^24*D + b*S with S given per token column (2c, 2c+1).
+__device__ __forceinline__ void affine_acc(float (&acc)[4], const float (&d)[4], float S0, float S1,
+                                           float sa, float ba, float sb, float bb) {
+    acc[0] = fmaf(sa, d[0], fmaf(ba, S0, acc[0]));
+    acc[1] = fmaf(sa, d[1], fmaf(ba, S1, acc[1]));
+    acc[2] = fmaf(sb, d[2], fmaf(bb, S0, acc[2]));
+    acc[3] = fmaf(sb, d[3], fmaf(bb, S1, acc[3]));
 }
 
-// One thread waits until *p >= target; false if the wait gave up or another CTA did.
-__device__ bool wait_geq(const unsigned *p, unsigned target, unsigned *err) {
-    for (long long it = 0; it < kSpinLimit; it++) {
-        if (ld_acquire(p) >= target) return true;
-        if (*(volatile unsigned *)err) return false;
-        __nanosleep(128);
-    }
-    atomicExch(err, 1u);
-    return false;
-}
+// Position of column k of a group (fragment order) in a 128-byte h row of slot j:
+// the row's 16-byte chunks are swapped pairwise for odd slots, which makes the
+// B-fragment loads of 8 consecutive lanes hit 8 distinct bank groups.
+__host__ __device__ __forceinline__ int h_pos(int k, int j) { return frag_pos(k) ^ ((j & 1) << 3); }
 
-// CTA-wide wait; returns false (for every thread) on timeout/abort.
-__device__ bool cta_wait(const unsigned *p, unsigned target, unsigned *err, int *s_flag) {
-    if (threadIdx.x == 0) {
-        *s_flag = wait_geq(p, target, err) ? 1 : 0;
-        __threadfence();
+struct DecodeSmem {
+    uint64_t full[kMaxStages], empty[kMaxStages], hbar;
+    int idx[kMaxPairs];
+    float gate[kMaxPairs];
+    int pidx[kMaxPairs];
+    unsigned mask[MOE_MAX_EXPERTS];
+    short uid[MOE_MAX_EXPERTS];
+    int uexp[kMaxPairs], ubase[kMaxPairs], ucnt[kMaxPairs], uslot[kMaxPairs];
+    unsigned char last[kMaxUnitsPerCta];
+    int U;
+    int err;
+};
+
+template <int NCH, int GPW>
+__global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
+    extern __shared__ __align__(128) uint8_t dsm[];
+    __shared__ DecodeSmem S;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gl = lane >> 2, c = lane & 3;
+    const int b = blockIdx.x, nC = gridDim.x;
+    const bool producer = warp == kCW;
+    const int T = a.T, H = a.H;
+    const int Ti = a.Lr.Ti, G = a.Lr.G, Gi = a.Lr.Gi, Gs = a.Ls.Gi, R = a.Lr.R;
+    const bool do_shared = a.mode & kModeShared, do_routed = a.mode & kModeRouted, pre = a.mode & kModePre;
+    const int Ts = do_shared ? a.Ls.Ti : 0;  // shared gate/up tiles of this launch
+    const int Pe = do_shared ? a.P : 0;      // shared down parts of this launch
+    uint8_t *ring = dsm;
+    float *red = reinterpret_cast<float *>(dsm + a.red_off);
+    uint8_t *hsm = dsm + a.hsm_off;
+    volatile int *err = &S.err;
+
+    if (tid == 0) {
+        for (int s = 0; s < a.stages; s++) {
+            mbar_init(&S.full[s], 1);
+            mbar_init(&S.empty[s], kCW);
+        }
+        mbar_init(&S.hbar, 1);
+        S.err = 0;
+        mbar_fence_init();
     }
     __syncthreads();
-    bool ok = *s_flag != 0;
-    __syncthreads();
-    return ok;
-}
 
-__device__ __forceinline__ void l2_prefetch(const void *p, unsigned bytes) {
-    // bulk prefetch of a 16-byte aligned range into L2
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
+    // ---- ring bookkeeping (the producer and the consumers count fills alike)
+    int fill = 0;
+    int last_fill[kMaxStages] = {-1, -1, -1, -1};
+    auto producer_slot = [&](int k) -> int {  // lane 0 of the producer
+        const int s = k % a.stages;
+        if (k >= a.stages && !*err) {
+            if (!mbar_wait(&S.empty[s], ((k / a.stages) - 1) & 1, err)) {
+                *err = 1;
+                atomicExch(&a.ctrl[kErr], 1u);
+            }
+        }
+        return s;
+    };
+    auto consumer_wait = [&](int k) -> int {
+        const int s = k % a.stages;
+        if (!*err && !mbar_wait(&S.full[s], (k / a.stages) & 1, err)) {
+            *err = 1;
+            atomicExch(&a.ctrl[kErr], 1u);
+        }
+        return s;
+    };
+    auto consumer_release = [&](int s) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.empty[s]);
+    };
 
-// ------------------------------------------------------------------ router item
-__device__ void router_item(const DecodeArgs &a, int r, int *s_flag) {
-    const LayerDev &ly = a.ly;
-    const Ws &ws = a.ws;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int G = ly.H / kGroup;
-    // 1. tokens -> fp16 fragment order, groups [g0, g1) of every token
-    {
-        const int g0 = r * G / a.R, g1 = (r + 1) * G / a.R;
-        const int n = (g1 - g0) * a.T * 32;  // (token, group, pair of columns)
-        for (int i = threadIdx.x; i < n; i += kDecThreads) {
-            const int l = i & 31, tg = i >> 5;
-            const int t = tg / (g1 - g0), g = g0 + tg % (g1 - g0);
-            const int k = g * kGroup + 2 * l;
-            const float2 v = __ldg(reinterpret_cast<const float2 *>(a.x + (size_t)t * ly.H + k));
-            __half *row = ws.x16 + (size_t)t * ly.H;
-            row[frag_pos(k)] = __float2half_rn(v.x);
-            row[frag_pos(k + 1)] = __float2half_rn(v.y);
-        }
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            __threadfence();
-            atomicAdd(&ws.ctrl[kXPrep], 1u);
-        }
+    // gate/up tile t of the global list: shared tiles first, then routed (u, it).
+    auto gu_src = [&](int j) -> const uint8_t * {
+        if (j < Ts) return a.shared + (size_t)kTileBytes * G * j;
+        const int u = (j - Ts) / Ti, it = (j - Ts) % Ti;
+        return a.experts + (size_t)S.uslot[u] * a.stride + (size_t)kTileBytes * G * it;
+    };
+    const unsigned gu_bytes = (unsigned)(kTileBytes * G);
+    const int n_shared_mine = b < Ts ? (Ts - 1 - b) / nC + 1 : 0;
+
+    // ---- compute warps: x fragments for this warp's K slice, and their group sums
+    const int g0w = warp * G / kCW, g1w = (warp + 1) * G / kCW;
+    uint32_t xb[GPW][NCH][8];
+    float xs[GPW][NCH][2];
+    if (!producer) {
+#pragma unroll
+        for (int gi = 0; gi < GPW; gi++)
+#pragma unroll
+            for (int ch = 0; ch < NCH; ch++) {
+                const int g = g0w + gi, t = 8 * ch + gl;
+                if (g < g1w && t < T)
+                    load_b_f32(xb[gi][ch], a.x + (size_t)t * H + g * kGroup + 16 * c);
+                else
+                    zero_b(xb[gi][ch]);
+                float d[4] = {0.f, 0.f, 0.f, 0.f};
+                mma_group_sums(d, xb[gi][ch]);
+                xs[gi][ch][0] = d[0];
+                xs[gi][ch][1] = d[1];
+            }
     }
-    // 2. router rows: one per warp, all tokens
-    const int e = r * kRouterRows + warp;
-    if (e < ly.E) {
-        const int wpr = ly.H / 4;
-        const uint32_t *row = ly.rq + (size_t)e * wpr;
-        float acc[MOE_MAX_DECODE_TOKENS];
+
+    // One gate/up tile by the compute warps: K split over warps, reduction in
+    // shared memory, GeGLU, fp16 store of h.  `u` < 0 marks the shared expert.
+    int rbuf = 0;
+    auto gateup_tile = [&](int s, int u, int it) {
+        float acc[NCH][4];
 #pragma unroll
-        for (int t = 0; t < MOE_MAX_DECODE_TOKENS; t++) acc[t] = 0.f;
-        for (int w0 = 2 * lane; w0 < wpr; w0 += 64) {
-            const uint2 wd = ldg_u2(row + w0);
-            const int g = w0 >> 4;  // 16 words per group of 64 bytes
-            const float s = __half2float(ly.rs[(size_t)e * G + g]);
-            const float b = __half2float(ly.rb[(size_t)e * G + g]);
-            float wv[8];
+        for (int ch = 0; ch < NCH; ch++)
 #pragma unroll
-            for (int i = 0; i < 4; i++) {
-                wv[i] = fmaf(s, (float)((wd.x >> (8 * i)) & 0xFFu), b);
-                wv[4 + i] = fmaf(s, (float)((wd.y >> (8 * i)) & 0xFFu), b);
+            for (int i = 0; i < 4; i++) acc[ch][i] = 0.f;
+        if (!*err) {
+            const uint8_t *st = ring + (size_t)s * a.SB;
+#pragma unroll
+            for (int gi = 0; gi < GPW; gi++) {
+                const int g = g0w + gi;
+                if (g < g1w) {
+                    const uint4 q = *reinterpret_cast<const uint4 *>(st + g * kTileBytes + 16 * lane);
+                    const uint2 e = *reinterpret_cast<const uint2 *>(st + g * kTileBytes + 512 + 8 * gl);
+                    const float sa = lo_half(e.x) * kTwo24, ba = hi_half(e.x);
+                    const float sb = lo_half(e.y) * kTwo24, bb = hi_half(e.y);
+#pragma unroll
+                    for (int ch = 0; ch < NCH; ch++) {
+                        float d[4] = {0.f, 0.f, 0.f, 0.f};
+                        mma_group_codes(d, make_uint2(q.x, q.y), make_uint2(q.z, q.w), xb[gi][ch]);
+                        affine_acc(acc[ch], d, xs[gi][ch][0], xs[gi][ch][1], sa, ba, sb, bb);
+                    }
+                }
+            }
+        }
+        consumer_release(s);
+        float *rw = red + (size_t)((rbuf * kCW + warp) * NCH) * 128;
+#pragma unroll
+        for (int ch = 0; ch < NCH; ch++)
+            reinterpret_cast<float4 *>(rw + ch * 128)[lane] = make_float4(acc[ch][0], acc[ch][1], acc[ch][2], acc[ch][3]);
+        named_sync(1, kCThreads);
+        // reduce: output o = (ch, lane L, column i) uses slots i (gate) and i+2 (up)
+        constexpr int SPLIT = 8 / NCH, WPT = kCW / SPLIT;
+        const int o = tid / SPLIT, q = tid % SPLIT;
+        const int ch = o / 64, L = (o % 64) >> 1, i = o & 1;
+        float gs = 0.f, us = 0.f;
+        const float *rr = red + (size_t)(rbuf * kCW) * NCH * 128;
+#pragma unroll
+        for (int w = 0; w < WPT; w++) {
+            const float *p = rr + (size_t)((q * WPT + w) * NCH + ch) * 128 + L * 4;
+            gs += p[i];
+            us += p[i + 2];
+        }
+#pragma unroll
+        for (int off = SPLIT / 2; off > 0; off >>= 1) {
+            gs += __shfl_xor_sync(0xffffffffu, gs, off);
+            us += __shfl_xor_sync(0xffffffffu, us, off);
+        }
+        rbuf ^= 1;
+        if (q != 0 || *err) return;
+        const int row = 8 * it + (L >> 2), t = 8 * ch + 2 * (L & 3) + i;
+        if (t >= T) return;
+        const __half hv = __float2half_rn(gelu_tanh(gs) * us);
+        const int g = row / kGroup, k = row % kGroup;
+        if (u < 0) {
+            a.hs16[((size_t)g * T + t) * kGroup + h_pos(k, t)] = hv;
+        } else {
+            const unsigned m = S.mask[S.uexp[u]];
+            if ((m >> t) & 1u) {
+                const int slot = __popc(m & ((1u << t) - 1u)), n = S.ucnt[u];
+                a.h16[(size_t)S.ubase[u] * a.I + ((size_t)g * n + slot) * kGroup + h_pos(k, slot)] = hv;
+            }
+        }
+    };
+
+    // =========================== phase A ===========================
+    if (producer) {
+        if (lane == 0) {
+            // this CTA's shared gate/up tiles (as many as the ring holds now)
+            for (int k = 0; k < n_shared_mine && k < a.stages; k++) {
+                const int s = producer_slot(fill);
+                mbar_arrive_expect_tx(&S.full[s], gu_bytes);
+                bulk_g2s(ring + (size_t)s * a.SB, gu_src(b + k * nC), gu_bytes, &S.full[s]);
+                last_fill[s] = fill++;
+            }
+            // a slice of the shared down matrix, into L2
+            for (int r = b; r < R && do_shared; r += nC)
+                prefetch_l2(a.shared + a.Ls.gu_bytes + (size_t)kTileBytes * Gs * r, kTileBytes * Gs);
+        }
+        // router rows e = b, b + nC, ... (8-bit affine, fp32 FMA)
+        int nrows = 0;
+        const int wpr = H / 4, Gr = H / kGroup;
+        for (int e = b; e < a.E && !pre; e += nC) {
+            nrows++;
+            const uint32_t *row = a.rq + (size_t)e * wpr;
+            float acc[MOE_MAX_DECODE_TOKENS];
+#pragma unroll
+            for (int t = 0; t < MOE_MAX_DECODE_TOKENS; t++) acc[t] = 0.f;
+            for (int w0 = 2 * lane; w0 < wpr; w0 += 64) {
+                const uint2 wd = __ldg(reinterpret_cast<const uint2 *>(row + w0));
+                const int g = w0 >> 4;
+                const float s = __half2float(a.rs[(size_t)e * Gr + g]);
+                const float bb = __half2float(a.rb[(size_t)e * Gr + g]);
+                float wv[8];
+#pragma unroll
+                for (int i = 0; i < 4; i++) {
+                    wv[i] = fmaf(s, (float)((wd.x >> (8 * i)) & 0xFFu), bb);
+                    wv[4 + i] = fmaf(s, (float)((wd.y >> (8 * i)) & 0xFFu), bb);
+                }
+#pragma unroll
+                for (int t = 0; t < MOE_MAX_DECODE_TOKENS; t++) {
+                    if (t < T) {
+                        const float4 *xv = reinterpret_cast<const float4 *>(a.x + (size_t)t * H + 4 * w0);
+                        const float4 x0 = __ldg(xv), x1 = __ldg(xv + 1);
+                        float v = acc[t];
+                        v = fmaf(wv[0], x0.x, v); v = fmaf(wv[1], x0.y, v);
+                        v = fmaf(wv[2], x0.z, v); v = fmaf(wv[3], x0.w, v);
+                        v = fmaf(wv[4], x1.x, v); v = fmaf(wv[5], x1.y, v);
+                        v = fmaf(wv[6], x1.z, v); v = fmaf(wv[7], x1.w, v);
+                        acc[t] = v;
+                    }
+                }
             }
 #pragma unroll
             for (int t = 0; t < MOE_MAX_DECODE_TOKENS; t++) {
-                if (t < a.T) {
-                    const float4 *xv = reinterpret_cast<const float4 *>(a.x + (size_t)t * ly.H + 4 * w0);
-                    const float4 x0 = __ldg(xv), x1 = __ldg(xv + 1);
-                    float v = acc[t];
-                    v = fmaf(wv[0], x0.x, v); v = fmaf(wv[1], x0.y, v);
-                    v = fmaf(wv[2], x0.z, v); v = fmaf(wv[3], x0.w, v);
-                    v = fmaf(wv[4], x1.x, v); v = fmaf(wv[5], x1.y, v);
-                    v = fmaf(wv[6], x1.z, v); v = fmaf(wv[7], x1.w, v);
-                    acc[t] = v;
+                if (t < T) {
+                    const float v = warp_sum(acc[t]);
+                    if (lane == 0) a.logits[(size_t)t * a.E + e] = v + (a.bias ? a.bias[e] : 0.f);
                 }
             }
         }
-#pragma unroll
-        for (int t = 0; t < MOE_MAX_DECODE_TOKENS; t++) {
-            if (t < a.T) {
-                float v = warp_sum(acc[t]);
-                if (lane == 0) ws.logits[(size_t)t * ly.E + e] = v + (ly.bias ? ly.bias[e] : 0.f);
+        if (lane == 0) {
+            if (nrows) {
+                __threadfence();
+                atomicAdd(&a.ctrl[kRouteCnt], (unsigned)nrows);
             }
+            for (int k = a.stages; k < n_shared_mine; k++) {
+                const int s = producer_slot(fill);
+                if (!*err) {
+                    mbar_arrive_expect_tx(&S.full[s], gu_bytes);
+                    bulk_g2s(ring + (size_t)s * a.SB, gu_src(b + k * nC), gu_bytes, &S.full[s]);
+                    last_fill[s] = fill;
+                }
+                fill++;
+            }
+            if (!pre && !spin_geq(&a.ctrl[kRouteCnt], (unsigned)a.E, &a.ctrl[kErr])) *err = 1;
+        }
+        __syncwarp();
+    } else {
+        for (int k = 0; k < n_shared_mine; k++) {
+            const int s = consumer_wait(fill++);
+            gateup_tile(s, -1, b + k * nC);
         }
     }
-    // 3. the last router item ranks the experts and publishes the schedule
     __syncthreads();
-    if (threadIdx.x == 0) {
-        __threadfence();
-        *s_flag = atomicAdd(&ws.ctrl[kRouteTicket], 1u) == (unsigned)(a.R - 1);
-    }
-    __syncthreads();
-    const bool last = *s_flag;
-    __syncthreads();
-    if (!last) return;
-    __threadfence();
-    for (int t = warp; t < a.T; t += kDecWarps)
-        warp_topk_softmax(ws.logits, ly.E, ly.topk, t, ws.idx, ws.gate, a.idx_out, a.gate_out);
-    __syncthreads();
-    build_schedule(ly, a.T, ws);
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        __threadfence();
-        atomicExch(&ws.ctrl[kRouted], 1u);
-    }
-}
 
-// ------------------------------------------------------------------ token slots
-// Up to 16 token slots per item: slot j reads B row brow[j] and writes output row
-// orow[j].
-struct Slots {
-    int n;
-    int brow[MOE_MAX_DECODE_TOKENS];
-    int orow[MOE_MAX_DECODE_TOKENS];
-};
-
-// ------------------------------------------------------------------ gate/up item
-// 16 gate rows [i0, i0+16) and the up rows [Ie+i0, ...) of one expert matrix; the
-// CTA's 8 warps split the K groups, then reduce through shared memory and apply
-// GeGLU.  Output: fp16 activations in fragment order.
-template <int NCH>
-__device__ void gateup_item(const DecodeArgs &a, QMat m, int Ie, int i0, const Slots &sl,
-                            __half *hout, unsigned *done, float *smem) {
-    const LayerDev &ly = a.ly;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gl = lane >> 2, c = lane & 3;
-    const int G = ly.H / kGroup, wpr = ly.H / 8;
-    // stage scales and biases of the 32 rows: [4][16][G] halves
-    __half *sb = reinterpret_cast<__half *>(smem);
-    {
-        const int per = 16 * G * 2 / 16;  // 16-byte chunks per (part, 16 rows)
-        for (int i = threadIdx.x; i < 4 * per; i += kDecThreads) {
-            const int part = i / per, ch = i % per;
-            const __half *src = ((part & 1) ? m.b : m.s) + (size_t)(i0 + ((part >> 1) ? Ie : 0)) * G;
-            reinterpret_cast<uint4 *>(sb + part * 16 * G)[ch] = __ldg(reinterpret_cast<const uint4 *>(src) + ch);
+    // =========================== routing ===========================
+    if (pre) {
+        for (int p = tid; p < T * a.topk; p += kDecThreads) {
+            S.idx[p] = a.idx_pre[p];
+            S.gate[p] = a.gate_pre[p];
+            if (b == 0 && a.idx_out) a.idx_out[p] = S.idx[p];
+            if (b == 0 && a.gate_out) a.gate_out[p] = S.gate[p];
         }
+    } else if (!*err) {
+        for (int t = warp; t < T; t += kCW + 1)
+            warp_topk_softmax(a.logits + (size_t)t * a.E, a.E, a.topk, S.idx + t * a.topk,
+                              S.gate + t * a.topk, b == 0 ? a.idx_out + (a.idx_out ? t * a.topk : 0) : nullptr,
+                              b == 0 ? a.gate_out + (a.gate_out ? t * a.topk : 0) : nullptr);
     }
-    const uint32_t *qg_a = m.q + (size_t)(i0 + gl) * wpr + 2 * c;
-    const uint32_t *qg_b = qg_a + 8 * (size_t)wpr;
-    const uint32_t *qu_a = qg_a + (size_t)Ie * wpr;
-    const uint32_t *qu_b = qu_a + 8 * (size_t)wpr;
-    const int g0 = warp * G / kDecWarps, g1 = (warp + 1) * G / kDecWarps;
-    float accg[NCH][4], accu[NCH][4];
-#pragma unroll
-    for (int ch = 0; ch < NCH; ch++)
-#pragma unroll
-        for (int i = 0; i < 4; i++) accg[ch][i] = accu[ch][i] = 0.f;
+    for (int e = tid; e < a.E; e += kDecThreads) S.mask[e] = 0u;
     __syncthreads();
-    // two groups per step, the next step's weights loaded before this step's math
-    uint2 cur[2][4], nxt[2][4];
-    auto load = [&](uint2 (&dst)[2][4], int g) {
+    const int P2 = T * a.topk;
+    if (!*err)
+        for (int p = tid; p < P2; p += kDecThreads) atomicOr(&S.mask[S.idx[p]], 1u << (p / a.topk));
+    __syncthreads();
+    if (warp == 0) {
+        int ubase = 0, sbase = 0;
+        for (int e0 = 0; e0 < a.E; e0 += 32) {
+            const int e = e0 + lane;
+            const unsigned m = e < a.E ? S.mask[e] : 0u;
+            const unsigned bal = __ballot_sync(0xffffffffu, m != 0u);
+            const int rank = __popc(bal & ((1u << lane) - 1u));
+            const int cnt = __popc(m);
+            int incl = cnt;
 #pragma unroll
-        for (int k = 0; k < 2; k++) {
-            const int gg = (g + k < g1) ? g + k : g;
-            dst[k][0] = ldg_u2(qg_a + gg * 8);
-            dst[k][1] = ldg_u2(qg_b + gg * 8);
-            dst[k][2] = ldg_u2(qu_a + gg * 8);
-            dst[k][3] = ldg_u2(qu_b + gg * 8);
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += v;
+            }
+            if (m) {
+                const int u = ubase + rank;
+                S.uid[e] = (short)u;
+                S.uexp[u] = e;
+                S.ucnt[u] = cnt;
+                S.ubase[u] = sbase + incl - cnt;
+                S.uslot[u] = a.use_map ? a.slot_map[e] : e;
+            }
+            ubase += __popc(bal);
+            sbase += __shfl_sync(0xffffffffu, incl, 31);
         }
+        if (lane == 0) S.U = *err ? 0 : ubase;
+    }
+    __syncthreads();
+    for (int p = tid; p < P2 && !*err; p += kDecThreads) {
+        const int t = p / a.topk, e = S.idx[p];
+        S.pidx[p] = S.ubase[S.uid[e]] + __popc(S.mask[e] & ((1u << t) - 1u));
+    }
+    __syncthreads();
+
+    const int U = do_routed ? S.U : 0;  // routed experts of this launch
+    const int NGU = Ts + U * Ti;
+    const int NDN = (Pe + U) * R;
+    const int ulo = (int)((long long)NDN * b / nC), uhi = (int)((long long)NDN * (b + 1) / nC);
+    const int nunits = uhi - ulo;
+    const int nstg = (nunits + a.UPS - 1) / a.UPS;
+    const int m_first = ulo / R;
+    auto unit_src = [&](int gunit, int *ng) -> const uint8_t * {
+        const int m = gunit / R, r = gunit % R;
+        if (m < Pe) {
+            const int g0 = m * Gi;
+            *ng = min(Gi, Gs - g0);
+            return a.shared + a.Ls.gu_bytes + (size_t)kTileBytes * ((size_t)r * Gs + g0);
+        }
+        *ng = Gi;
+        return a.experts + (size_t)S.uslot[m - Pe] * a.stride + a.Lr.gu_bytes + (size_t)kTileBytes * Gi * r;
     };
-    if (g0 < g1) load(cur, g0);
-    for (int g = g0; g < g1; g += 2) {
-        if (g + 2 < g1) load(nxt, g + 2);
-#pragma unroll
-        for (int k = 0; k < 2; k++) {
-            const int gg = g + k;
-            if (gg < g1) {
-                const float sga = __half2float(sb[0 * 16 * G + gl * G + gg]) * kTwo24;
-                const float bga = __half2float(sb[1 * 16 * G + gl * G + gg]);
-                const float sgb = __half2float(sb[0 * 16 * G + (gl + 8) * G + gg]) * kTwo24;
-                const float bgb = __half2float(sb[1 * 16 * G + (gl + 8) * G + gg]);
-                const float sua = __half2float(sb[2 * 16 * G + gl * G + gg]) * kTwo24;
-                const float bua = __half2float(sb[3 * 16 * G + gl * G + gg]);
-                const float sub = __half2float(sb[2 * 16 * G + (gl + 8) * G + gg]) * kTwo24;
-                const float bub = __half2float(sb[3 * 16 * G + (gl + 8) * G + gg]);
-#pragma unroll
-                for (int ch = 0; ch < NCH; ch++) {
-                    uint32_t xb[8];
-                    const int slot = ch * 8 + gl;
-                    if (slot < sl.n)
-                        load_b(xb, a.ws.x16 + (size_t)sl.brow[slot] * ly.H + gg * kGroup + 16 * c);
-                    else
-                        zero_b(xb);
-                    float dsum[4] = {0.f, 0.f, 0.f, 0.f};
-                    mma_group_sums(dsum, xb);
-                    float dg[4] = {0.f, 0.f, 0.f, 0.f}, du[4] = {0.f, 0.f, 0.f, 0.f};
-                    mma_group_codes(dg, cur[k][0], cur[k][1], xb);
-                    mma_group_codes(du, cur[k][2], cur[k][3], xb);
-                    apply_affine(accg[ch], dg, dsum, sga, bga, sgb, bgb);
-                    apply_affine(accu[ch], du, dsum, sua, bua, sub, bub);
-                }
-            }
-        }
-#pragma unroll
-        for (int k = 0; k < 2; k++)
-#pragma unroll
-            for (int r = 0; r < 4; r++) cur[k][r] = nxt[k][r];
-    }
-    // reduce the 8 warps' partial sums: red[warp][ch][2][32 lanes][4]
-    __syncthreads();  // sb no longer needed; reuse the buffer
-    float *red = smem;
-#pragma unroll
-    for (int ch = 0; ch < NCH; ch++)
-#pragma unroll
-        for (int i = 0; i < 4; i++) {
-            red[(((warp * NCH + ch) * 2 + 0) * 32 + lane) * 4 + i] = accg[ch][i];
-            red[(((warp * NCH + ch) * 2 + 1) * 32 + lane) * 4 + i] = accu[ch][i];
-        }
-    __syncthreads();
-    for (int v = threadIdx.x; v < NCH * 32 * 4; v += kDecThreads) {
-        const int ch = v / 128, ln = (v / 4) % 32, i = v % 4;
-        float gsum = 0.f, usum = 0.f;
-#pragma unroll
-        for (int w = 0; w < kDecWarps; w++) {
-            gsum += red[(((w * NCH + ch) * 2 + 0) * 32 + ln) * 4 + i];
-            usum += red[(((w * NCH + ch) * 2 + 1) * 32 + ln) * 4 + i];
-        }
-        const int row = (ln >> 2) + ((i & 2) ? 8 : 0);
-        const int slot = ch * 8 + 2 * (ln & 3) + (i & 1);
-        if (slot < sl.n) {
-            const float hval = gelu_tanh(gsum) * usum;
-            hout[(size_t)sl.orow[slot] * Ie + frag_pos(i0 + row)] = __float2half_rn(hval);
-        }
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        __threadfence();
-        atomicAdd(done, 1u);
-    }
-}
+    // first gate/up tile index of this CTA among the routed ones
+    const int j_first = b + n_shared_mine * nC;
+    const int n_routed_mine = j_first < NGU ? (NGU - 1 - j_first) / nC + 1 : 0;
 
-// ------------------------------------------------------------------ down item
-// 64 output rows [n0, n0+64) of one down matrix (K = Ie): warps = 4 row tiles x 2
-// K halves.  Writes per-slot partial rows, then takes the tile's ticket; the last
-// contributor of the tile combines y.
-template <int NCH>
-__device__ void down_item(const DecodeArgs &a, QMat m, int n0, const Slots &sl, const __half *hin,
-                          unsigned target, float *smem, int *s_flag) {
-    const LayerDev &ly = a.ly;
-    const Ws &ws = a.ws;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gl = lane >> 2, c = lane & 3;
-    const int Ke = m.K, G = Ke / kGroup, wpr = Ke / 8;
-    __half *sb = reinterpret_cast<__half *>(smem);
-    {
-        const int per = kDownRows * G * 2 / 16;
-        for (int i = threadIdx.x; i < 2 * per; i += kDecThreads) {
-            const int part = i / per, ch = i % per;
-            const __half *src = (part ? m.b : m.s) + (size_t)n0 * G;
-            reinterpret_cast<uint4 *>(sb + part * kDownRows * G)[ch] =
-                __ldg(reinterpret_cast<const uint4 *>(src) + ch);
+    // =========================== phase B ===========================
+    if (producer) {
+        if (lane == 0 && !*err) {
+            // everything this CTA will read, into L2, in the order it is needed
+            for (int k = 0; k < n_routed_mine; k++) prefetch_l2(gu_src(j_first + k * nC), gu_bytes);
+            for (int k = 0; k < nunits; k++) {
+                int ng;
+                const uint8_t *src = unit_src(ulo + k, &ng);
+                prefetch_l2(src, kTileBytes * ng);
+            }
         }
-    }
-    const int rt = warp & 3, kh = warp >> 2;
-    const int ra = rt * 16 + gl;  // row within the 64-row tile
-    const uint32_t *qa = m.q + (size_t)(n0 + ra) * wpr + 2 * c;
-    const uint32_t *qb = qa + 8 * (size_t)wpr;
-    const int g0 = kh * G / 2, g1 = (kh + 1) * G / 2;
-    float acc[NCH][4];
-#pragma unroll
-    for (int ch = 0; ch < NCH; ch++)
-#pragma unroll
-        for (int i = 0; i < 4; i++) acc[ch][i] = 0.f;
-    __syncthreads();
-    uint2 cur[4][2], nxt[4][2];
-    auto load = [&](uint2 (&dst)[4][2], int g) {
-#pragma unroll
-        for (int k = 0; k < 4; k++) {
-            const int gg = (g + k < g1) ? g + k : g;
-            dst[k][0] = ldg_u2(qa + gg * 8);
-            dst[k][1] = ldg_u2(qb + gg * 8);
-        }
-    };
-    if (g0 < g1) load(cur, g0);
-    for (int g = g0; g < g1; g += 4) {
-        if (g + 4 < g1) load(nxt, g + 4);
-#pragma unroll
-        for (int k = 0; k < 4; k++) {
-            const int gg = g + k;
-            if (gg < g1) {
-                const float sa = __half2float(sb[ra * G + gg]) * kTwo24;
-                const float ba = __half2float(sb[kDownRows * G + ra * G + gg]);
-                const float sbb = __half2float(sb[(ra + 8) * G + gg]) * kTwo24;
-                const float bb = __half2float(sb[kDownRows * G + (ra + 8) * G + gg]);
-#pragma unroll
-                for (int ch = 0; ch < NCH; ch++) {
-                    uint32_t xb[8];
-                    const int slot = ch * 8 + gl;
-                    if (slot < sl.n)
-                        load_b(xb, hin + (size_t)sl.brow[slot] * Ke + gg * kGroup + 16 * c);
+        if (lane == 0) {
+            for (int k = 0; k < n_routed_mine; k++) {
+                const int s = producer_slot(fill);
+                if (!*err) {
+                    mbar_arrive_expect_tx(&S.full[s], gu_bytes);
+                    bulk_g2s(ring + (size_t)s * a.SB, gu_src(j_first + k * nC), gu_bytes, &S.full[s]);
+                    last_fill[s] = fill;
+                }
+                fill++;
+            }
+            auto down_fill = [&](int k) {
+                const int s = producer_slot(fill);
+                if (!*err) {
+                    const int u0 = k * a.UPS, u1 = min(nunits, u0 + a.UPS);
+                    unsigned bytes = 0;
+                    for (int i = u0; i < u1; i++) {
+                        int ng;
+                        unit_src(ulo + i, &ng);
+                        bytes += kTileBytes * ng;
+                    }
+                    mbar_arrive_expect_tx(&S.full[s], bytes);
+                    for (int i = u0; i < u1; i++) {
+                        int ng;
+                        const uint8_t *src = unit_src(ulo + i, &ng);
+                        bulk_g2s(ring + (size_t)s * a.SB + (size_t)(i - u0) * Gi * kTileBytes, src,
+                                 kTileBytes * ng, &S.full[s]);
+                    }
+                    last_fill[s] = fill;
+                }
+                fill++;
+            };
+            const int early = min(nstg, a.stages);
+            for (int k = 0; k < early; k++) down_fill(k);
+            // h of this CTA's matrices, once every gate/up tile of the layer is done
+            if (!*err && !spin_geq(&a.ctrl[kGuDone], (unsigned)NGU, &a.ctrl[kErr])) *err = 1;
+            if (!*err && nunits > 0) {
+                const int m_last = (uhi - 1) / R;
+                unsigned bytes = 0;
+                for (int m = m_first; m <= m_last; m++)
+                    bytes += m < Pe ? (unsigned)(min(Gi, Gs - m * Gi) * T * 128)
+                                    : (unsigned)(Gi * S.ucnt[m - Pe] * 128);
+                mbar_arrive_expect_tx(&S.hbar, bytes);
+                for (int m = m_first; m <= m_last; m++) {
+                    uint8_t *dst = hsm + (size_t)(m - m_first) * a.hsm_mat_bytes;
+                    if (m < Pe)
+                        bulk_g2s(dst, a.hs16 + (size_t)m * Gi * T * kGroup,
+                                 (unsigned)(min(Gi, Gs - m * Gi) * T * 128), &S.hbar);
                     else
-                        zero_b(xb);
-                    float dsum[4] = {0.f, 0.f, 0.f, 0.f}, d[4] = {0.f, 0.f, 0.f, 0.f};
-                    mma_group_sums(dsum, xb);
-                    mma_group_codes(d, cur[k][0], cur[k][1], xb);
-                    apply_affine(acc[ch], d, dsum, sa, ba, sbb, bb);
+                        bulk_g2s(dst, a.h16 + (size_t)S.ubase[m - Pe] * a.I,
+                                 (unsigned)(Gi * S.ucnt[m - Pe] * 128), &S.hbar);
                 }
             }
+            for (int k = early; k < nstg; k++) down_fill(k);
+            // drain: every copy this CTA issued has landed before the CTA exits
+            volatile int never = 0;
+            for (int s = 0; s < a.stages; s++)
+                if (last_fill[s] >= 0) mbar_wait(&S.full[s], (last_fill[s] / a.stages) & 1, &never);
+            if (nunits > 0) mbar_wait(&S.hbar, 0, &never);
         }
-#pragma unroll
-        for (int k = 0; k < 4; k++) {
-            cur[k][0] = nxt[k][0];
-            cur[k][1] = nxt[k][1];
+        __syncwarp();
+    } else {
+        // ---- routed gate/up tiles
+        for (int k = 0; k < n_routed_mine; k++) {
+            const int s = consumer_wait(fill++);
+            const int j = j_first + k * nC;
+            gateup_tile(s, (j - Ts) / Ti, (j - Ts) % Ti);
         }
-    }
-    // reduce the two K halves; write partial rows (fp32) of every slot
-    __syncthreads();
-    float *red = smem;  // [2 halves][4 tiles][NCH][32][4]
-#pragma unroll
-    for (int ch = 0; ch < NCH; ch++)
-#pragma unroll
-        for (int i = 0; i < 4; i++) red[((((kh * 4 + rt) * NCH + ch) * 32) + lane) * 4 + i] = acc[ch][i];
-    __syncthreads();
-    for (int v = threadIdx.x; v < 4 * NCH * 128; v += kDecThreads) {
-        const int t4 = v / (NCH * 128), ch = (v / 128) % NCH, ln = (v / 4) % 32, i = v % 4;
-        const float val = red[((((0 * 4 + t4) * NCH + ch) * 32) + ln) * 4 + i] +
-                          red[((((1 * 4 + t4) * NCH + ch) * 32) + ln) * 4 + i];
-        const int row = t4 * 16 + (ln >> 2) + ((i & 2) ? 8 : 0);
-        const int slot = ch * 8 + 2 * (ln & 3) + (i & 1);
-        if (slot < sl.n) ws.partial[(size_t)sl.orow[slot] * ly.H + n0 + row] = val;
-    }
-    // ticket of this 64-row tile: U routed contributions + 1 shared
-    __syncthreads();
-    const int tile = n0 / kDownRows;
-    if (threadIdx.x == 0) {
         __threadfence();
-        *s_flag = atomicAdd(&ws.tile_cnt[tile], 1u) == target;
-    }
-    __syncthreads();
-    const bool last = *s_flag;
-    __syncthreads();
-    if (!last) return;
-    __threadfence();
-    const size_t shared_base = (size_t)ws.Tmax * ly.topk;
-    for (int v = threadIdx.x; v < kDownRows * a.T; v += kDecThreads) {
-        const int t = v / kDownRows, n = n0 + v % kDownRows;
-        float acc2 = 0.f;
-        for (int k = 0; k < ly.topk; k++)
-            acc2 = fmaf(__ldcg(&ws.gate[t * ly.topk + k]),
-                        __ldcg(&ws.partial[(size_t)(t * ly.topk + k) * ly.H + n]), acc2);
-        acc2 += __ldcg(&ws.partial[(shared_base + t) * ly.H + n]);
-        if (a.flags & MOE_RESIDUAL) acc2 += __ldg(&a.x[(size_t)t * ly.H + n]);
-        a.y[(size_t)t * ly.H + n] = acc2;
-    }
-    if (threadIdx.x == 0) ws.tile_cnt[tile] = 0u;
-}
-
-// ------------------------------------------------------------------ the kernel
-template <int NCH>
-__global__ void __launch_bounds__(kDecThreads) k_decode(DecodeArgs a) {
-    extern __shared__ __align__(16) float smem[];
-    __shared__ int s_item, s_flag, s_abort;
-    __shared__ Slots sl;
-    const LayerDev &ly = a.ly;
-    const Ws &ws = a.ws;
-    const int tilesS = ly.Is / 16, downS = ly.H / kDownRows, tilesR = ly.I / 16;
-    const int n0 = a.R + tilesS + downS;
-    if (threadIdx.x == 0) s_abort = 0;
-    __syncthreads();
-    unsigned U = 0;
-    for (int q = 0; q < 3 && !s_abort; q++) {
-        if (q == 1) {
-            if (!cta_wait(&ws.ctrl[kRouted], 1u, &ws.ctrl[kErr], &s_flag)) {
-                s_abort = 1;
-                break;
-            }
-            U = __ldcg(&ws.ctrl[kU]);
+        named_sync(1, kCThreads);
+        if (tid == 0) atomicAdd(&a.ctrl[kGuDone], (unsigned)(n_shared_mine + n_routed_mine));
+        // ---- down units
+        if (nunits > 0 && !*err && !mbar_wait(&S.hbar, 0, err)) {
+            *err = 1;
+            atomicExch(&a.ctrl[kErr], 1u);
         }
-        const int count = q == 0 ? n0 : (q == 1 ? (int)U * tilesR : (int)U * downS);
-        while (true) {
-            if (threadIdx.x == 0) s_item = (int)atomicAdd(&ws.ctrl[kQueue0 + q], 1u);
-            __syncthreads();
-            const int it = s_item;
-            __syncthreads();
-            if (it >= count) break;
-            if (q == 0 && it < a.R) {
-                router_item(a, it, &s_flag);
-            } else if (q == 0 && it < a.R + tilesS) {
-                const int k = it - a.R;
-                if (threadIdx.x < MOE_MAX_DECODE_TOKENS) {
-                    sl.brow[threadIdx.x] = sl.orow[threadIdx.x] = threadIdx.x;
-                    if (threadIdx.x == 0) sl.n = a.T;
-                }
-                if (!cta_wait(&ws.ctrl[kXPrep], (unsigned)a.R, &ws.ctrl[kErr], &s_flag)) {
-                    s_abort = 1;
-                    break;
-                }
-                gateup_item<NCH>(a, gu_view(ly.shared, ly.Ls, ly.H, ly.Is), ly.Is, 16 * k, sl, ws.hs16,
-                                 &ws.ctrl[kSharedUp], smem);
-            } else if (q == 0) {
-                const int m = it - a.R - tilesS;
-                QMat d = down_view(ly.shared, ly.Ls, ly.H, ly.Is);
-                if (threadIdx.x == 0) {
-                    const int G = d.K / kGroup;
-                    l2_prefetch(d.q + (size_t)m * kDownRows * (d.K / 8), kDownRows * d.K / 2);
-                    l2_prefetch(d.s + (size_t)m * kDownRows * G, kDownRows * G * 2);
-                    l2_prefetch(d.b + (size_t)m * kDownRows * G, kDownRows * G * 2);
-                }
-                if (threadIdx.x < MOE_MAX_DECODE_TOKENS) {
-                    sl.brow[threadIdx.x] = threadIdx.x;
-                    sl.orow[threadIdx.x] = ws.Tmax * ly.topk + threadIdx.x;
-                    if (threadIdx.x == 0) sl.n = a.T;
-                }
-                if (!cta_wait(&ws.ctrl[kSharedUp], (unsigned)tilesS, &ws.ctrl[kErr], &s_flag)) {
-                    s_abort = 1;
-                    break;
-                }
-                // the tile ticket target (U) is only known after routing
-                if (!cta_wait(&ws.ctrl[kRouted], 1u, &ws.ctrl[kErr], &s_flag)) {
-                    s_abort = 1;
-                    break;
-                }
-                const unsigned Ucur = __ldcg(&ws.ctrl[kU]);
-                down_item<NCH>(a, d, m * kDownRows, sl, ws.hs16, Ucur, smem, &s_flag);
-            } else {
-                const int u = q == 1 ? it / tilesR : it / downS;
-                const int e = __ldcg(&ws.uexp[u]);
-                const uint8_t *blob = ly.experts + (size_t)e * ly.stride;
-                if (threadIdx.x < MOE_MAX_DECODE_TOKENS) {
-                    const int cnt = __ldcg(&ws.ucount[u]);
-                    const int p = threadIdx.x < cnt ? __ldcg(&ws.ulist[(size_t)u * ws.Tmax + threadIdx.x]) : 0;
-                    sl.brow[threadIdx.x] = q == 1 ? p / ly.topk : p;
-                    sl.orow[threadIdx.x] = p;
-                    if (threadIdx.x == 0) sl.n = cnt;
-                }
-                if (q == 1) {
-                    __syncthreads();
-                    gateup_item<NCH>(a, gu_view(blob, ly.L, ly.H, ly.I), ly.I, 16 * (it % tilesR), sl,
-                                     ws.h16, &ws.up_done[u], smem);
+        for (int k = 0; k < nstg; k++) {
+            const int s = consumer_wait(fill++);
+            for (int i = 0; i < a.UPS; i++) {
+                const int lu = k * a.UPS + i;
+                if (lu >= nunits || (lu % kCW) != warp || *err) continue;
+                const int gu = ulo + lu, m = gu / R, r = gu % R;
+                int ng, nsl;
+                float *dst;
+                size_t dstride;
+                if (m < Pe) {
+                    ng = min(Gi, Gs - m * Gi);
+                    nsl = T;
+                    dst = a.ps + (size_t)m * T * H;
                 } else {
-                    const int m = it % downS;
-                    QMat d = down_view(blob, ly.L, ly.H, ly.I);
-                    if (threadIdx.x == 0) {
-                        const int G = d.K / kGroup;
-                        l2_prefetch(d.q + (size_t)m * kDownRows * (d.K / 8), kDownRows * d.K / 2);
-                        l2_prefetch(d.s + (size_t)m * kDownRows * G, kDownRows * G * 2);
-                        l2_prefetch(d.b + (size_t)m * kDownRows * G, kDownRows * G * 2);
+                    ng = Gi;
+                    nsl = S.ucnt[m - Pe];
+                    dst = a.pr + (size_t)S.ubase[m - Pe] * H;
+                }
+                dstride = H;
+                const uint8_t *wst = ring + (size_t)s * a.SB + (size_t)i * Gi * kTileBytes;
+                const uint8_t *hm = hsm + (size_t)(m - m_first) * a.hsm_mat_bytes;
+                float acc[NCH][4];
+#pragma unroll
+                for (int ch = 0; ch < NCH; ch++)
+#pragma unroll
+                    for (int v = 0; v < 4; v++) acc[ch][v] = 0.f;
+                for (int g = 0; g < ng; g++) {
+                    const uint4 q = *reinterpret_cast<const uint4 *>(wst + g * kTileBytes + 16 * lane);
+                    const uint2 e = *reinterpret_cast<const uint2 *>(wst + g * kTileBytes + 512 + 8 * gl);
+                    const float sa = lo_half(e.x) * kTwo24, ba = hi_half(e.x);
+                    const float sb = lo_half(e.y) * kTwo24, bb = hi_half(e.y);
+#pragma unroll
+                    for (int ch = 0; ch < NCH; ch++) {
+                        if (8 * ch < nsl) {
+                            uint32_t hb[8];
+                            const int j = 8 * ch + gl;
+                            if (j < nsl) {
+                                const uint8_t *hr = hm + ((size_t)g * nsl + j) * 128;
+                                const int sw = (j & 1);
+                                const uint4 v0 = *reinterpret_cast<const uint4 *>(hr + 16 * ((2 * c) ^ sw));
+                                const uint4 v1 = *reinterpret_cast<const uint4 *>(hr + 16 * ((2 * c + 1) ^ sw));
+                                hb[0] = v0.x; hb[1] = v0.y; hb[2] = v0.z; hb[3] = v0.w;
+                                hb[4] = v1.x; hb[5] = v1.y; hb[6] = v1.z; hb[7] = v1.w;
+                            } else {
+                                zero_b(hb);
+                            }
+                            float d[4] = {0.f, 0.f, 0.f, 0.f}, sm[4] = {0.f, 0.f, 0.f, 0.f};
+                            mma_group_sums(sm, hb);
+                            mma_group_codes(d, make_uint2(q.x, q.y), make_uint2(q.z, q.w), hb);
+                            affine_acc(acc[ch], d, sm[0], sm[1], sa, ba, sb, bb);
+                        }
                     }
-                    if (!cta_wait(&ws.up_done[u], (unsigned)tilesR, &ws.ctrl[kErr], &s_flag)) {
-                        s_abort = 1;
-                        break;
+                }
+#pragma unroll
+                for (int ch = 0; ch < NCH; ch++) {
+                    const int j0 = 8 * ch + 2 * c, na = 16 * r + gl;
+                    if (j0 < nsl) {
+                        dst[(size_t)j0 * dstride + na] = acc[ch][0];
+                        dst[(size_t)j0 * dstride + na + 8] = acc[ch][2];
                     }
-                    down_item<NCH>(a, d, m * kDownRows, sl, ws.h16, U, smem, &s_flag);
+                    if (j0 + 1 < nsl) {
+                        dst[(size_t)(j0 + 1) * dstride + na] = acc[ch][1];
+                        dst[(size_t)(j0 + 1) * dstride + na + 8] = acc[ch][3];
+                    }
                 }
             }
+            consumer_release(s);
+        }
+        // ---- tickets of the 16-row tiles; the last contributor combines
+        __threadfence();
+        named_sync(1, kCThreads);
+        const unsigned target = (unsigned)(Pe + U);
+        for (int lu = tid; lu < nunits; lu += kCThreads) {
+            unsigned char last = 0;
+            if (!*err && do_routed) {
+                const int r = (ulo + lu) % R;
+                last = atomicAdd(&a.ticket[r], 1u) == target - 1u;
+                if (last) __threadfence();
+            }
+            S.last[lu] = last;
+        }
+        named_sync(1, kCThreads);
+        for (int lu = 0; lu < nunits; lu++) {
+            if (!S.last[lu]) continue;
+            const int r = (ulo + lu) % R;
+            for (int v = tid; v < 16 * T; v += kCThreads) {
+                const int t = v >> 4, n = 16 * r + (v & 15);
+                float acc = 0.f;
+                for (int k = 0; k < a.topk; k++)
+                    acc = fmaf(S.gate[t * a.topk + k], __ldcg(a.pr + (size_t)S.pidx[t * a.topk + k] * H + n), acc);
+                for (int p = 0; p < a.P; p++) acc += __ldcg(a.ps + ((size_t)p * T + t) * H + n);
+                if (a.flags & MOE_RESIDUAL) acc += __ldg(a.x + (size_t)t * H + n);
+                a.y[(size_t)t * H + n] = acc;
+            }
+            if (tid == 0) a.ticket[r] = 0u;
         }
     }
-    // leave; the last CTA resets the control words for the next call
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        __threadfence();
-        s_flag = atomicAdd(&ws.ctrl[kExit], 1u) == gridDim.x - 1;
-    }
-    __syncthreads();
-    if (s_flag) {
-        __threadfence();
-        const unsigned Umax = (unsigned)ws.Umax;
-        for (unsigned i = threadIdx.x; i < Umax; i += kDecThreads) ws.up_done[i] = 0u;
-        if (threadIdx.x == 0) {
-            ws.ctrl[kRouteTicket] = 0u;
-            ws.ctrl[kQueue0] = ws.ctrl[kQueue1] = ws.ctrl[kQueue2] = 0u;
-            ws.ctrl[kXPrep] = ws.ctrl[kRouted] = ws.ctrl[kSharedUp] = 0u;
-            ws.ctrl[kExit] = 0u;
-        }
-    }
-}
 
-// Dynamic shared memory of k_decode: the larger of the staged scales/biases and the
-// reduction buffers.
-inline size_t decode_smem_bytes(const moe_layer_t &l, int nch) {
-    const size_t G = l.H / kGroup, Gd = (l.I > l.Is ? l.I : l.Is) / kGroup;
-    size_t sb_up = 4 * 16 * G * 2, sb_down = 2 * kDownRows * Gd * 2;
-    size_t red_up = (size_t)kDecWarps * nch * 2 * 32 * 4 * 4;
-    size_t red_down = (size_t)2 * 4 * nch * 32 * 4 * 4;
-    size_t m = sb_up;
-    if (sb_down > m) m = sb_down;
-    if (red_up > m) m = red_up;
-    if (red_down > m) m = red_down;
-    return m;
+    // ---- leave; the last CTA resets the control words for the next call
+    __syncthreads();
+    if (tid == 0) {
+        __threadfence();
+        if (atomicAdd(&a.ctrl[kExit], 1u) == (unsigned)nC - 1u) {
+            a.ctrl[kRouteCnt] = 0u;
+            a.ctrl[kGuDone] = 0u;
+            __threadfence();
+            a.ctrl[kExit] = 0u;
+        }
+    }
 }
 
 }  // namespace moe

@@ -8,9 +8,11 @@
 
 #include "common.cuh"
 #include "route.cuh"
-#include "simple_kernels.cuh"
+#include "quantise.cuh"
+#include "tile.cuh"
 #include "decode.cuh"
 #include "gemv.cuh"
+#include "lfu.h"
 
 using namespace moe;
 
@@ -36,7 +38,7 @@ bool layer_ok(const moe_layer_t *l) {
 
 bool experts_ok(const moe_layer_t *l) {
     return l->experts && aligned(l->experts, 256) && l->expert_stride % 256 == 0 &&
-           l->expert_stride >= blob_layout(l->H, l->I).total;
+           l->expert_stride >= tile_layout(l->H, l->I).total;
 }
 
 LayerDev layer_dev(const moe_layer_t *l) {
@@ -107,59 +109,107 @@ int check_layer_call(const moe_layer_t *l, const float *x, int T, int Tlimit, in
     return MOE_OK;
 }
 
-// Prefill chunk (and any T beyond the decode kernel): router + gather + expert
-// kernels launched in sequence.
-int run_layer_chunk(const moe_layer_t *l, const float *x, int T, int flags, float *y,
-                    int32_t *idx_out, float *gate_out, void *d_ws, size_t ws_bytes, void *stream) {
-    Ws ws;
-    int rc = bind_ws(l, T, d_ws, ws_bytes, &ws);
-    if (rc) return rc;
-    LayerDev ly = layer_dev(l);
-    cudaStream_t st = as_stream(stream);
-    rc = launch_route(l, ly, x, T, ws, idx_out, gate_out, nullptr, st);
-    if (rc) return rc;
-    const int up_items = ws.Umax * (l->I / 16) + l->Is / 16;
-    k_expert_up_simple<<<up_items, 128, 0, st>>>(ly, x, T, ws);
-    if ((rc = cuda_status())) return rc;
-    const int down_items = (ws.Umax + 1) * (l->H / 16);
-    k_expert_down_simple<<<down_items, 128, 0, st>>>(ly, x, T, flags, y, ws);
-    return cuda_status();
-}
-
-struct DecodeLaunch {
-    int device = -1;
-    int sms = 0;
-    int occ[2] = {0, 0};
-    size_t smem[2] = {0, 0};
+struct DecodeCfg {
+    int device = -1, sms = 0, smem_optin = 0;
+    size_t static_smem[2][4] = {};
+    bool attr_set[2][4] = {};
+    int attr_smem[2][4] = {};
 };
 
-// Grid of the persistent decode kernel: every SM times the CTAs that fit.
-int decode_grid(const moe_layer_t *l, int nch, size_t smem, int *grid) {
-    static thread_local DecodeLaunch cache;
+template <int NCH, int GPW>
+void *decode_fn() { return (void *)k_decode<NCH, GPW>; }
+
+void *decode_kernel(int nch, int gpw) {
+    static void *const table[2][4] = {
+        {decode_fn<1, 1>(), decode_fn<1, 2>(), decode_fn<1, 3>(), decode_fn<1, 4>()},
+        {decode_fn<2, 1>(), decode_fn<2, 2>(), decode_fn<2, 3>(), decode_fn<2, 4>()}};
+    return table[nch - 1][gpw - 1];
+}
+
+struct DecodePlan {
+    DecodeArgs a;
+    void *fn = nullptr;
+    long long smem = 0;
+    int nC = 0;
+};
+
+// Arguments and launch shape of the decode kernel for one call (experts from
+// the layer; a cache replaces them before the launch).
+int decode_plan(const moe_layer_t *l, const float *x, int T, int flags, float *y, int32_t *idx_out,
+                float *gate_out, const Ws &ws, DecodePlan *plan) {
+    static thread_local DecodeCfg cfg;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return cuda_status();
-    if (cache.device != dev) {
-        cache = DecodeLaunch();
-        cache.device = dev;
-        if (cudaDeviceGetAttribute(&cache.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    if (cfg.device != dev) {
+        cfg = DecodeCfg();
+        cfg.device = dev;
+        if (cudaDeviceGetAttribute(&cfg.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&cfg.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
             return cuda_status();
     }
-    int k = nch - 1;
-    if (cache.smem[k] != smem || cache.occ[k] == 0) {
-        int occ = 0;
-        auto fn = nch == 1 ? k_decode<1> : k_decode<2>;
-        if (smem > 48 * 1024 &&
-            cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-            return cuda_status();
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, kDecThreads, smem) != cudaSuccess)
-            return cuda_status();
-        if (occ < 1) return MOE_EINVAL;
-        cache.occ[k] = occ;
-        cache.smem[k] = smem;
+    DecodeArgs &a = plan->a;
+    memset(&a, 0, sizeof(a));
+    a.H = l->H; a.E = l->E; a.topk = l->topk; a.I = l->I; a.Is = l->Is;
+    a.rq = l->r_q; a.rs = (const __half *)l->r_s; a.rb = (const __half *)l->r_b; a.bias = l->logit_bias;
+    a.experts = (const uint8_t *)l->experts; a.stride = l->expert_stride; a.shared = (const uint8_t *)l->shared;
+    a.Lr = tile_layout(l->H, l->I);
+    a.Ls = tile_layout(l->H, l->Is);
+    a.P = shared_parts(l->I, l->Is);
+    a.x = x; a.T = T; a.flags = flags; a.y = y; a.idx_out = idx_out; a.gate_out = gate_out;
+    a.ctrl = ws.ctrl; a.ticket = ws.ticket; a.logits = ws.logits; a.h16 = ws.h16; a.hs16 = ws.hs16;
+    a.pr = ws.pr; a.ps = ws.ps;
+    a.mode = kModeShared | kModeRouted;
+    const int nch = T > 8 ? 2 : 1;
+    const int gpw = (a.Lr.G + kCW - 1) / kCW;
+    if (gpw > 4 || l->H > kMaxHiddenLayer) return MOE_EINVAL;  // hidden size above 4096
+    const int nC = cfg.sms;
+    const int R = a.Lr.R, Gi = a.Lr.Gi;
+    const int Umax = T * l->topk < l->E ? T * l->topk : l->E;
+    const long long units_cta = ((long long)(a.P + Umax) * R + nC - 1) / nC;
+    if (units_cta > kMaxUnitsPerCta) return MOE_EINVAL;
+    const int hsm_mats = (int)((units_cta + R - 1) / R) + 1;
+    a.SB = (int)(((size_t)(a.Lr.G > Gi ? a.Lr.G : Gi) * kTileBytes + 127) / 128 * 128);
+    a.UPS = a.SB / (Gi * kTileBytes);
+    a.hsm_mat_bytes = Gi * T * 128;
+    const int red = 2 * kCW * nch * 512;
+    void *fn = decode_kernel(nch, gpw);
+    size_t &st = cfg.static_smem[nch - 1][gpw - 1];
+    if (st == 0) {
+        cudaFuncAttributes fa;
+        if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess) return cuda_status();
+        st = fa.sharedSizeBytes + 1;  // +1: computed
     }
-    (void)l;
-    *grid = cache.sms * cache.occ[k];
+    const long long budget = (long long)cfg.smem_optin - (long long)(st - 1);
+    int stages = kMaxStages;
+    long long smem = 0;
+    for (; stages >= 2; stages--) {
+        smem = (long long)stages * a.SB + red + (long long)hsm_mats * a.hsm_mat_bytes;
+        if (smem <= budget) break;
+    }
+    if (stages < 2) return MOE_EINVAL;
+    a.stages = stages;
+    a.red_off = stages * a.SB;
+    a.hsm_off = a.red_off + red;
+    if (cfg.attr_smem[nch - 1][gpw - 1] < smem) {
+        if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+            return cuda_status();
+        cfg.attr_smem[nch - 1][gpw - 1] = (int)smem;
+    }
+    plan->fn = fn;
+    plan->smem = smem;
+    plan->nC = nC;
     return MOE_OK;
+}
+
+// One CTA per SM, launched cooperatively so that every CTA is resident and the
+// cross-CTA waits can always complete.
+int decode_launch(DecodePlan &plan, int mode, void *stream) {
+    plan.a.mode = mode;
+    void *args[] = {&plan.a};
+    if (cudaLaunchCooperativeKernel(plan.fn, dim3(plan.nC), dim3(kDecThreads), args, (size_t)plan.smem,
+                                    as_stream(stream)) != cudaSuccess)
+        return cuda_status();
+    return cuda_status();
 }
 
 int run_decode(const moe_layer_t *l, const float *x, int T, int flags, float *y, int32_t *idx_out,
@@ -167,26 +217,111 @@ int run_decode(const moe_layer_t *l, const float *x, int T, int flags, float *y,
     Ws ws;
     int rc = bind_ws(l, T, d_ws, ws_bytes, &ws);
     if (rc) return rc;
-    DecodeArgs a;
-    a.ly = layer_dev(l);
-    a.x = x;
-    a.T = T;
-    a.flags = flags;
-    a.y = y;
-    a.idx_out = idx_out;
-    a.gate_out = gate_out;
-    a.ws = ws;
-    a.R = (l->E + kRouterRows - 1) / kRouterRows;
-    const int nch = T > 8 ? 2 : 1;
-    const size_t smem = decode_smem_bytes(*l, nch);
-    int grid = 0;
-    if ((rc = decode_grid(l, nch, smem, &grid))) return rc;
+    DecodePlan plan;
+    if ((rc = decode_plan(l, x, T, flags, y, idx_out, gate_out, ws, &plan))) return rc;
+    return decode_launch(plan, kModeShared | kModeRouted, stream);
+}
+
+// Prefill chunk: the chunk's tokens in groups of up to MOE_MAX_DECODE_TOKENS.
+int run_layer_chunk(const moe_layer_t *l, const float *x, int T, int flags, float *y,
+                    int32_t *idx_out, float *gate_out, void *d_ws, size_t ws_bytes, void *stream) {
+    for (int t0 = 0; t0 < T; t0 += MOE_MAX_DECODE_TOKENS) {
+        const int tc = T - t0 < MOE_MAX_DECODE_TOKENS ? T - t0 : MOE_MAX_DECODE_TOKENS;
+        int rc = run_decode(l, x + (size_t)t0 * l->H, tc, flags, y + (size_t)t0 * l->H,
+                            idx_out ? idx_out + (size_t)t0 * l->topk : nullptr,
+                            gate_out ? gate_out + (size_t)t0 * l->topk : nullptr, d_ws, ws_bytes, stream);
+        if (rc) return rc;
+    }
+    return MOE_OK;
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ LFU policy and cache
+struct moe_lfu {
+    moe::LfuPolicy policy;
+    moe_lfu(int slots, int E) : policy(slots, E) {}
+};
+
+struct moe_cache {
+    int H, E, I, slots, device;
+    size_t blob, host_stride;
+    const uint8_t *h_experts;
+    uint8_t *d_slots = nullptr;
+    int32_t *h_idx = nullptr;  // page-locked copy of the step's routing
+    cudaStream_t side = nullptr;
+    cudaEvent_t ev_idx = nullptr, ev_copies = nullptr;
+    moe::LfuPolicy policy;
+    uint64_t h2d_bytes = 0;
+    moe_cache(int slots_, int E_) : policy(slots_, E_) {}
+};
+
+namespace {
+
+void cache_free(moe_cache *c) {
+    if (!c) return;
+    if (c->d_slots) cudaFree(c->d_slots);
+    if (c->h_idx) cudaFreeHost(c->h_idx);
+    if (c->ev_idx) cudaEventDestroy(c->ev_idx);
+    if (c->ev_copies) cudaEventDestroy(c->ev_copies);
+    if (c->side) cudaStreamDestroy(c->side);
+    delete c;
+}
+
+// Decode through a cache: router launch, host copy of the routing (the host
+// waits for it), LFU step, copies of the missing experts on the side stream,
+// then the shared expert (overlapping the copies) and the routed experts.
+int run_decode_cached(const moe_layer_t *l, const float *x, int T, int flags, float *y, int32_t *idx_out,
+                      float *gate_out, moe_cache *c, void *d_ws, size_t ws_bytes, void *stream) {
+    if (c->H != l->H || c->E != l->E || c->I != l->I) return MOE_EINVAL;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cuda_status();
+    if (dev != c->device) return MOE_EINVAL;
+    Ws ws;
+    int rc = bind_ws(l, T, d_ws, ws_bytes, &ws);
+    if (rc) return rc;
     cudaStream_t st = as_stream(stream);
-    if (nch == 1)
-        k_decode<1><<<grid, kDecThreads, smem, st>>>(a);
-    else
-        k_decode<2><<<grid, kDecThreads, smem, st>>>(a);
-    return cuda_status();
+    LayerDev ly = layer_dev(l);
+    if ((rc = launch_route(l, ly, x, T, ws, ws.idx, ws.gate, nullptr, st))) return rc;
+    const int P2 = T * l->topk;
+    if (cudaMemcpyAsync(c->h_idx, ws.idx, sizeof(int32_t) * P2, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaEventRecord(c->ev_idx, st) != cudaSuccess || cudaEventSynchronize(c->ev_idx) != cudaSuccess)
+        return cuda_status();
+    int32_t req[kMaxPairs], slot[kMaxPairs];
+    uint8_t hit[kMaxPairs];
+    int n = 0;
+    for (int p = 0; p < P2; p++) {
+        bool seen = false;
+        for (int i = 0; i < n && !seen; i++) seen = req[i] == c->h_idx[p];
+        if (!seen) req[n++] = c->h_idx[p];
+    }
+    rc = c->policy.step(req, n, slot, hit);
+    if (rc == 3) return MOE_ECAPACITY;
+    if (rc) return MOE_EINVAL;
+    DecodePlan plan;
+    if ((rc = decode_plan(l, x, T, flags, y, idx_out, gate_out, ws, &plan))) return rc;
+    plan.a.experts = c->d_slots;
+    plan.a.stride = c->blob;
+    plan.a.use_map = 1;
+    plan.a.idx_pre = ws.idx;
+    plan.a.gate_pre = ws.gate;
+    for (int e = 0; e < l->E; e++) plan.a.slot_map[e] = (short)c->policy.slot_of(e);
+    int misses = 0;
+    for (int i = 0; i < n; i++) {
+        if (hit[i]) continue;
+        // The slot's previous expert was last read by work that precedes the
+        // router launch on `stream`, which the host has just waited for.
+        if (cudaMemcpyAsync(c->d_slots + (size_t)slot[i] * c->blob, c->h_experts + (size_t)req[i] * c->host_stride,
+                            c->blob, cudaMemcpyHostToDevice, c->side) != cudaSuccess)
+            return cuda_status();
+        c->h2d_bytes += c->blob;
+        misses++;
+    }
+    if (misses == 0) return decode_launch(plan, kModeShared | kModeRouted | kModePre, stream);
+    if (cudaEventRecord(c->ev_copies, c->side) != cudaSuccess) return cuda_status();
+    if ((rc = decode_launch(plan, kModeShared | kModePre, stream))) return rc;
+    if (cudaStreamWaitEvent(st, c->ev_copies, 0) != cudaSuccess) return cuda_status();
+    return decode_launch(plan, kModeRouted | kModePre, stream);
 }
 
 // ------------------------------------------------------------------ allocation-free decode
@@ -249,6 +384,22 @@ int moe_expert_blob_offsets(int H, int I, size_t offsets_out[6]) {
     offsets_out[4] = L.d_s;
     offsets_out[5] = L.d_b;
     return MOE_OK;
+}
+
+size_t moe_tile_blob_bytes(int H, int I) {
+    if (H <= 0 || I <= 0 || H % 128 || I % kGroup) return 0;
+    return tile_layout(H, I).total;
+}
+
+int moe_expert_tile(const void *mlx_blob, int H, int I, void *tile_blob, void *stream) {
+    if (!mlx_blob || !tile_blob || !moe_tile_blob_bytes(H, I) || mlx_blob == tile_blob) return MOE_EINVAL;
+    if (!aligned(mlx_blob, 16) || !aligned(tile_blob, 16)) return MOE_EINVAL;
+    const TileLayout T = tile_layout(H, I);
+    const long long threads = 32ll * ((long long)T.Ti * T.G + (long long)T.R * T.Gi);
+    const int block = 256;
+    k_tile_expert<<<(unsigned)((threads + block - 1) / block), block, 0, as_stream(stream)>>>(
+        (const uint8_t *)mlx_blob, (uint8_t *)tile_blob, H, I);
+    return cuda_status();
 }
 
 size_t moe_workspace_bytes(const moe_layer_t *layer, int T_max) {
@@ -314,7 +465,12 @@ int moe_route(const moe_layer_t *layer, const float *x, int T, int32_t *idx, flo
 int moe_layer_decode(const moe_layer_t *layer, const float *x, int T, int flags, float *y,
                      int32_t *idx_out, float *gate_out, moe_cache_t *cache, void *d_ws,
                      size_t ws_bytes, void *stream) {
-    if (cache) return MOE_ENOTREADY;
+    if (cache) {
+        if (!layer_ok(layer) || !x || !y || T < 1 || T > MOE_MAX_DECODE_TOKENS || (flags & ~MOE_RESIDUAL) ||
+            !aligned(x, 16) || !aligned(y, 16) || x == y)
+            return MOE_EINVAL;
+        return run_decode_cached(layer, x, T, flags, y, idx_out, gate_out, cache, d_ws, ws_bytes, stream);
+    }
     int rc = check_layer_call(layer, x, T, MOE_MAX_DECODE_TOKENS, flags, y);
     if (rc) return rc;
     return run_decode(layer, x, T, flags, y, idx_out, gate_out, d_ws, ws_bytes, stream);
@@ -328,15 +484,89 @@ int moe_layer_prefill_chunk(const moe_layer_t *layer, const float *x, int T, int
     return run_layer_chunk(layer, x, T, flags, y, idx_out, gate_out, d_ws, ws_bytes, stream);
 }
 
+int moe_lfu_create(moe_lfu_t **out, int slots, int E) {
+    if (!out) return MOE_EINVAL;
+    *out = nullptr;
+    if (slots < 1 || slots > MOE_MAX_CACHE_SLOTS || E < 1 || E > MOE_MAX_EXPERTS) return MOE_EINVAL;
+    *out = new (std::nothrow) moe_lfu(slots, E);
+    return *out ? MOE_OK : MOE_EINVAL;
+}
+
+int moe_lfu_destroy(moe_lfu_t *lfu) {
+    delete lfu;
+    return MOE_OK;
+}
+
+int moe_lfu_step(moe_lfu_t *lfu, const int32_t *req, int n, int32_t *slot_out, uint8_t *hit_out) {
+    if (!lfu) return MOE_EINVAL;
+    const int rc = lfu->policy.step(req, n, slot_out, hit_out);
+    return rc == 3 ? MOE_ECAPACITY : rc ? MOE_EINVAL : MOE_OK;
+}
+
+static void policy_state(const moe::LfuPolicy &p, int32_t *expert_of_slot, uint32_t *counts, int64_t *last) {
+    for (int s = 0; s < p.slots(); s++) {
+        if (expert_of_slot) expert_of_slot[s] = p.expert_in(s);
+        if (counts) counts[s] = p.count_of(s);
+        if (last) last[s] = p.last_of(s);
+    }
+}
+
+int moe_lfu_state(const moe_lfu_t *lfu, int32_t *expert_of_slot, uint32_t *counts, int64_t *last,
+                  uint64_t *hits, uint64_t *misses) {
+    if (!lfu) return MOE_EINVAL;
+    policy_state(lfu->policy, expert_of_slot, counts, last);
+    if (hits) *hits = lfu->policy.hits();
+    if (misses) *misses = lfu->policy.misses();
+    return MOE_OK;
+}
+
 int moe_cache_create(moe_cache_t **out, int H, int E, int I, const void *h_experts,
                      size_t host_stride, int slots) {
-    (void)H; (void)E; (void)I; (void)h_experts; (void)host_stride; (void)slots;
-    if (out) *out = nullptr;
-    return MOE_ENOTREADY;
+    if (!out) return MOE_EINVAL;
+    *out = nullptr;
+    const size_t blob = moe_tile_blob_bytes(H, I);
+    if (!blob || !h_experts || E < 1 || E > MOE_MAX_EXPERTS || slots < 1 || slots > MOE_MAX_CACHE_SLOTS ||
+        host_stride < blob)
+        return MOE_EINVAL;
+    moe_cache *c = new (std::nothrow) moe_cache(slots, E);
+    if (!c) return MOE_EINVAL;
+    c->H = H; c->E = E; c->I = I; c->slots = slots;
+    c->blob = blob;
+    c->host_stride = host_stride;
+    c->h_experts = (const uint8_t *)h_experts;
+    if (cudaGetDevice(&c->device) != cudaSuccess ||
+        cudaMalloc((void **)&c->d_slots, blob * (size_t)slots) != cudaSuccess ||
+        cudaMallocHost((void **)&c->h_idx, sizeof(int32_t) * kMaxPairs) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&c->side, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&c->ev_idx, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&c->ev_copies, cudaEventDisableTiming) != cudaSuccess) {
+        cache_free(c);
+        return cuda_status() ? MOE_ECUDA : MOE_ECUDA;
+    }
+    *out = c;
+    return MOE_OK;
 }
-int moe_cache_destroy(moe_cache_t *cache) { return cache ? MOE_ENOTREADY : MOE_OK; }
-int moe_cache_slots(const moe_cache_t *, int32_t *, uint32_t *) { return MOE_ENOTREADY; }
-int moe_cache_stats(const moe_cache_t *, uint64_t *, uint64_t *, uint64_t *) { return MOE_ENOTREADY; }
+
+int moe_cache_destroy(moe_cache_t *cache) {
+    if (!cache) return MOE_OK;
+    cudaStreamSynchronize(cache->side);
+    cache_free(cache);
+    return cuda_status();
+}
+
+int moe_cache_slots(const moe_cache_t *cache, int32_t *expert_of_slot, uint32_t *counts) {
+    if (!cache) return MOE_EINVAL;
+    policy_state(cache->policy, expert_of_slot, counts, nullptr);
+    return MOE_OK;
+}
+
+int moe_cache_stats(const moe_cache_t *cache, uint64_t *hits, uint64_t *misses, uint64_t *h2d_bytes) {
+    if (!cache) return MOE_EINVAL;
+    if (hits) *hits = cache->policy.hits();
+    if (misses) *misses = cache->policy.misses();
+    if (h2d_bytes) *h2d_bytes = cache->h2d_bytes;
+    return MOE_OK;
+}
 
 int moe_layer_decode_noalloc(const moe_layer_t *layer, const float *x, int T, int flags, float *y,
                              int32_t *idx_out, float *gate_out, void *stream) {

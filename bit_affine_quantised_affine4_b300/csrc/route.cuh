@@ -1,5 +1,4 @@
-// route.cuh -- router GEMV (8-bit affine), top-k with softmax gates, and the
-// per-call schedule of distinct experts.
+// route.cuh -- router GEMV (8-bit affine) and top-k with softmax gates.
 //
 // Router: logits[t][e] = sum_j (s q + b)[e][j] x[t][j] (+ bias[e]); the 8-bit
 // router and the top-8 choice per token per layer are the devtrends page's
@@ -19,17 +18,18 @@ __device__ __forceinline__ bool ranks_before(float va, int ia, float vb, int ib)
     return va > vb || (va == vb && ia < ib);
 }
 
-// Top-k of token t's E logits by one warp; writes idx/gate (workspace + optional
-// caller outputs).
-__device__ void warp_topk_softmax(const float *logits, int E, int topk, int t, int *ws_idx,
-                                  float *ws_gate, int32_t *idx_out, float *gate_out) {
+// Top-k of one token's E logits by one warp, then softmax over the chosen ones.
+// lrow: the token's logits (read through L2: other CTAs may have written them).
+// Writes idx_dst/gate_dst (any memory) and, when non-null, idx_out/gate_out.
+__device__ void warp_topk_softmax(const float *lrow, int E, int topk, int *idx_dst, float *gate_dst,
+                                  int32_t *idx_out, float *gate_out) {
     const int lane = threadIdx.x & 31;
     float v[MOE_MAX_EXPERTS / 32];
     unsigned taken = 0;
 #pragma unroll
     for (int i = 0; i < MOE_MAX_EXPERTS / 32; i++) {
         int e = lane + 32 * i;
-        float x = e < E ? __ldcg(logits + (size_t)t * E + e) : -INFINITY;
+        float x = e < E ? __ldcg(lrow + e) : -INFINITY;
         v[i] = (x != x) ? -INFINITY : x;  // NaN ranks last
     }
     float sel_v[MOE_MAX_TOPK];
@@ -68,64 +68,16 @@ __device__ void warp_topk_softmax(const float *logits, int E, int topk, int t, i
         }
         for (int k = 0; k < topk; k++) {
             float g = ex[k] / z;
-            ws_idx[t * topk + k] = sel_i[k];
-            ws_gate[t * topk + k] = g;
-            if (idx_out) idx_out[t * topk + k] = sel_i[k];
-            if (gate_out) gate_out[t * topk + k] = g;
-        }
-    }
-}
-
-// Distinct experts of the call in ascending id order, and for each the pairs
-// p = t*topk + k that chose it, ascending (a stable counting sort).  Run by one
-// CTA after all idx are written.
-__device__ void build_schedule(const LayerDev &ly, int T, Ws ws) {
-    __shared__ int cnt[MOE_MAX_EXPERTS];
-    __shared__ int uid[MOE_MAX_EXPERTS];
-    __shared__ int fill[MOE_MAX_EXPERTS];
-    const int P = T * ly.topk;
-    for (int e = threadIdx.x; e < ly.E; e += blockDim.x) {
-        cnt[e] = 0;
-        fill[e] = 0;
-    }
-    __syncthreads();
-    for (int p = threadIdx.x; p < P; p += blockDim.x) atomicAdd(&cnt[ws.idx[p]], 1);
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        int U = 0;
-        for (int e = 0; e < ly.E; e++) {
-            if (cnt[e] > 0) {
-                uid[e] = U;
-                ws.uexp[U] = e;
-                ws.ucount[U] = cnt[e];
-                U++;
-            } else {
-                uid[e] = -1;
-            }
-        }
-        ws.ctrl[kU] = (unsigned)U;
-    }
-    __syncthreads();
-    if (threadIdx.x < 32) {
-        const int lane = threadIdx.x;
-        for (int base = 0; base < P; base += 32) {
-            int p = base + lane;
-            int e = p < P ? ws.idx[p] : -1 - lane;
-            unsigned same = __match_any_sync(0xffffffffu, e);
-            int rank = __popc(same & ((1u << lane) - 1u));
-            if (p < P) {
-                int u = uid[e];
-                ws.ulist[(size_t)u * ws.Tmax + fill[u] + rank] = p;
-            }
-            __syncwarp();
-            if (p < P && rank == 0) fill[uid[e]] += __popc(same);
-            __syncwarp();
+            idx_dst[k] = sel_i[k];
+            gate_dst[k] = g;
+            if (idx_out) idx_out[k] = sel_i[k];
+            if (gate_out) gate_out[k] = g;
         }
     }
 }
 
 // logits for router rows e (one per warp) for all T tokens; the last CTA to finish
-// runs top-k + softmax for every token and builds the schedule.
+// runs top-k + softmax for every token.
 template <int TCH>
 __global__ void __launch_bounds__(kRouteWarps * 32)
 k_route(LayerDev ly, const float *__restrict__ x, int T, Ws ws, int32_t *idx_out, float *gate_out,
@@ -181,9 +133,8 @@ k_route(LayerDev ly, const float *__restrict__ x, int T, Ws ws, int32_t *idx_out
     if (!is_last) return;
     __threadfence();
     for (int t = warp; t < T; t += kRouteWarps)
-        warp_topk_softmax(ws.logits, ly.E, ly.topk, t, ws.idx, ws.gate, idx_out, gate_out);
-    __syncthreads();
-    build_schedule(ly, T, ws);
+        warp_topk_softmax(ws.logits + (size_t)t * ly.E, ly.E, ly.topk, idx_out + t * ly.topk,
+                          gate_out + t * ly.topk, nullptr, nullptr);
     if (threadIdx.x == 0) ws.ctrl[kRouteTicket] = 0u;
 }
 

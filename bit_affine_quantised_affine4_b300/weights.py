@@ -1,7 +1,8 @@
-"""Device-side layer weights in the blob layout of include/moe.h.
+"""Device-side layer weights in the tile layout of include/moe.h.
 
-Packing fp32 weights runs the library's own quantiser kernel (affine_quantise) on
-the GPU, writing straight into the expert blobs.
+Packing fp32 weights runs the library's own kernels on the GPU: the quantiser
+(affine_quantise) writes an MLX-layout blob, which moe_expert_tile reorders into
+the tile layout the layer kernels read.
 """
 from __future__ import annotations
 
@@ -9,7 +10,8 @@ import ctypes as C
 
 import torch
 
-from . import affine_quantise, moe_expert_blob_bytes, moe_expert_blob_offsets, moe_layer_t
+from . import (affine_quantise, moe_expert_blob_bytes, moe_expert_blob_offsets, moe_expert_tile,
+               moe_layer_t, moe_tile_blob_bytes)
 
 
 def _part(blob: torch.Tensor, off: int, nbytes: int, dtype) -> torch.Tensor:
@@ -18,7 +20,7 @@ def _part(blob: torch.Tensor, off: int, nbytes: int, dtype) -> torch.Tensor:
 
 def pack_expert_blob(gu_w: torch.Tensor, d_w: torch.Tensor, blob: torch.Tensor, stream=None):
     """Quantise one expert (gate/up [2I, H] gate rows first, down [H, I]; fp32 on the GPU)
-    into `blob` (uint8 CUDA tensor of at least moe_expert_blob_bytes(H, I) bytes)."""
+    into `blob` in the MLX layout (uint8 CUDA tensor of at least moe_expert_blob_bytes(H, I) bytes)."""
     I2, H = gu_w.shape
     I = I2 // 2
     assert d_w.shape == (H, I)
@@ -34,6 +36,16 @@ def pack_expert_blob(gu_w: torch.Tensor, d_w: torch.Tensor, blob: torch.Tensor, 
     return blob
 
 
+def pack_expert_tiles(gu_w: torch.Tensor, d_w: torch.Tensor, tiles: torch.Tensor, stream=None):
+    """Quantise one expert into `tiles` (uint8 CUDA tensor of at least
+    moe_tile_blob_bytes(H, I) bytes) in the tile layout."""
+    I2, H = gu_w.shape
+    mlx = torch.empty(moe_expert_blob_bytes(H, I2 // 2), dtype=torch.uint8, device=tiles.device)
+    pack_expert_blob(gu_w, d_w, mlx, stream)
+    moe_expert_tile(mlx, H, I2 // 2, tiles, stream)
+    return tiles
+
+
 class Layer:
     """One MoE layer resident on the GPU: router (8-bit), E expert blobs, shared blob.
 
@@ -45,8 +57,8 @@ class Layer:
     def __init__(self, H, E, topk, I, Is, device="cuda", copies=1):
         self.H, self.E, self.topk, self.I, self.Is = H, E, topk, I, Is
         self.device = torch.device(device)
-        self.stride = moe_expert_blob_bytes(H, I)
-        self.sstride = moe_expert_blob_bytes(H, Is)
+        self.stride = moe_tile_blob_bytes(H, I)
+        self.sstride = moe_tile_blob_bytes(H, Is)
         self.copies = copies
         self.r_q = torch.empty((copies, E, H // 4), dtype=torch.int32, device=self.device)
         self.r_s = torch.empty((copies, E, H // 64), dtype=torch.int16, device=self.device)
@@ -61,12 +73,12 @@ class Layer:
                         self.r_b[0])
 
     def set_expert(self, e: int, gu_w: torch.Tensor, d_w: torch.Tensor):
-        pack_expert_blob(gu_w.to(self.device, torch.float32), d_w.to(self.device, torch.float32),
-                         self.experts[0, e])
+        pack_expert_tiles(gu_w.to(self.device, torch.float32), d_w.to(self.device, torch.float32),
+                          self.experts[0, e])
 
     def set_shared(self, gu_w: torch.Tensor, d_w: torch.Tensor):
-        pack_expert_blob(gu_w.to(self.device, torch.float32), d_w.to(self.device, torch.float32),
-                         self.shared[0])
+        pack_expert_tiles(gu_w.to(self.device, torch.float32), d_w.to(self.device, torch.float32),
+                          self.shared[0])
 
     def set_bias(self, bias):
         self.bias = None if bias is None else torch.as_tensor(bias, dtype=torch.float32).to(self.device)
@@ -87,7 +99,7 @@ class Layer:
             logit_bias=None if self.bias is None else self.bias.data_ptr(),
         )
 
-    # ---- host copies (for comparison with the oracle)
+    # ---- host copies of the tile-layout blobs
     def expert_blob_host(self, e: int, c: int = 0):
         return self.experts[c, e].cpu().numpy()
 

@@ -71,11 +71,13 @@ MOE_API const char *moe_status_string(int status);
 #define MOE_MAX_EXPERTS 256
 #define MOE_MAX_DECODE_TOKENS 16
 #define MOE_MAX_PREFILL_TOKENS 128
+#define MOE_MAX_CACHE_SLOTS 64
 
 /* ---------------------------------------------------------------- layout */
 
 /*
- * One expert is one contiguous blob (the unit the cache copies):
+ * MLX layout of one expert (the interchange form; what affine_quantise writes):
+ * one contiguous blob
  *   gu_q [2I][H/8] u32 | gu_s [2I][H/64] f16 | gu_b [2I][H/64] f16 |
  *   d_q  [H][I/8]  u32 | d_s  [H][I/64]  f16 | d_b  [H][I/64]  f16
  * The gate/up matrix holds the I gate rows first, then the I up rows.  Every
@@ -86,15 +88,37 @@ MOE_API size_t moe_expert_blob_bytes(int H, int I);
 MOE_API int moe_expert_blob_offsets(int H, int I, size_t offsets_out[6]);
 
 /*
+ * Tile layout of one expert (the form the layer kernels read, and the unit a
+ * cache slot holds).  The same codes, scales and biases in another order; the
+ * pages give no storage layout, this one is the library's own.  A tile is 16
+ * matrix rows by one group of 64 columns, 576 bytes (4.5 bits per weight):
+ *   bytes 16L..16L+15, lane L = 4r + c (r = 0..7, c = 0..3): words 2c and 2c+1
+ *     of the group in row a(r), then the same two words of row b(r);
+ *   bytes 512+8r..512+8r+7: fp16 scale, bias of row a(r), scale, bias of row b(r).
+ * Gate/up part at byte 0: tile (it, g) at 576 (it H/64 + g) for it < I/8,
+ *   g < H/64, with a(r) = gate row 8it + r and b(r) = up row 8it + r.
+ * Down part at byte 576 (I/8)(H/64): tile (rt, g) at 576 (rt I/64 + g) from
+ *   its start, rt < H/16, g < I/64, with a(r) = row 16rt + r, b(r) = row 16rt+8+r.
+ * moe_tile_blob_bytes: the blob size (a multiple of 256), 0 for bad shapes
+ * (H must be a multiple of 128, I of 64).
+ * moe_expert_tile: converts one expert from the MLX layout (device, at least
+ * moe_expert_blob_bytes(H, I) bytes) to the tile layout (device, at least
+ * moe_tile_blob_bytes(H, I) bytes, not overlapping the source); stream-ordered.
+ */
+MOE_API size_t moe_tile_blob_bytes(int H, int I);
+MOE_API int moe_expert_tile(const void *mlx_blob, int H, int I, void *tile_blob, void *stream);
+
+/*
  * A layer.  All pointers are device pointers owned by the caller.
  *   H hidden size, E experts (<= MOE_MAX_EXPERTS), topk (1..MOE_MAX_TOPK),
  *   I routed-expert intermediate size, Is shared-expert intermediate size;
- *   H, I and Is multiples of 64 (H also a multiple of 128).
- *   r_q/r_s/r_b: 8-bit router matrix [E][H].
- *   experts: E blobs of shape (H, I), blob e at experts + e * expert_stride
- *     (expert_stride a multiple of 256 and >= moe_expert_blob_bytes(H, I)).
+ *   H a multiple of 128 (at most 4096 for the layer calls), I and Is multiples
+ *   of 64.
+ *   r_q/r_s/r_b: 8-bit router matrix [E][H] (MLX layout, 16-byte aligned).
+ *   experts: E tile-layout blobs of shape (H, I), blob e at experts + e * expert_stride
+ *     (256-byte aligned; expert_stride a multiple of 256 and >= moe_tile_blob_bytes(H, I)).
  *     May be NULL when a cache supplies the experts.
- *   shared: one blob of shape (H, Is).
+ *   shared: one tile-layout blob of shape (H, Is), 256-byte aligned.
  *   logit_bias: optional fp32 [E] added to the router logits (NULL = none).
  */
 typedef struct moe_layer {
@@ -113,9 +137,10 @@ typedef struct moe_layer {
  * Scratch for moe_route / moe_layer_decode / moe_layer_prefill_chunk on up to
  * T_max tokens (T_max <= MOE_MAX_PREFILL_TOKENS).  The caller allocates it on the
  * device (256-byte aligned) and must zero it once with moe_workspace_init before
- * first use; every call leaves it ready for the next one.  One workspace serves
- * one call at a time: calls that overlap on the GPU must use different
- * workspaces.  Returns 0 for an invalid layer or T_max.
+ * first use; every call leaves it ready for the next one, whatever the layer, so
+ * one workspace sized for the largest layer and T_max can serve several layers
+ * in turn.  One workspace serves one call at a time: calls that overlap on the
+ * GPU must use different workspaces.  Returns 0 for an invalid layer or T_max.
  */
 MOE_API size_t moe_workspace_bytes(const moe_layer_t *layer, int T_max);
 MOE_API int moe_workspace_init(void *d_ws, size_t ws_bytes, void *stream);
@@ -222,26 +247,49 @@ MOE_API int moe_layer_decode_noalloc(const moe_layer_t *layer, const float *x, i
 /* ---------------------------------------------------------------- LFU cache */
 
 /*
- * Per-layer expert cache: `slots` device slots (<= 64) of blob size for (H, I),
- * filled from the E expert blobs held by the caller in host memory at
- * h_experts + e * host_stride (page-locked memory is required for the copies to
- * overlap compute; it is not copied or freed by the library).  The library
- * allocates the slot pool, a non-blocking side stream and its events; all are
- * released by moe_cache_destroy.
+ * The cache policy (the pages give "16 slots, LFU, per layer": devtrends page,
+ * section "Qual e il trucco principale dell'architettura"; remio.ai page,
+ * section "Mac Gemma 4 26B entra nello spazio disponibile..."; the tie rules are
+ * this library's reading).  A step brings a request list R: the distinct
+ * experts of the step in first-appearance order (token-major over the router's
+ * choices).  Every resident expert in R is a hit (use count += 1, last use =
+ * step).  Then every missing expert of R, in order, takes the lowest empty slot,
+ * or else evicts the slot not holding a member of R with the smallest
+ * (count, last use, slot); it starts at count 1, last use = step.  Counts are
+ * forgotten on eviction.  More distinct experts than slots: MOE_ECAPACITY and no
+ * change.  A repeated or out-of-range expert in R: MOE_EINVAL and no change.
  *
- * Policy (the pages give "16 slots, LFU, per layer"; the tie rules are this
- * library's reading): per step with request list R (the tokens' choices, first
- * appearance order) every resident expert in R is a hit (count += 1, last = step);
- * every missing one, in order, takes the lowest empty slot, else evicts the slot
- * not in R with the smallest (count, last, slot), and starts at count 1.
+ * moe_lfu_*: the policy alone, on the host (no GPU needed).  slots <= 64,
+ * E <= MOE_MAX_EXPERTS.  moe_lfu_step writes, per request, the slot now holding
+ * it (slot_out) and whether it was a hit (hit_out); either may be NULL.
+ * moe_lfu_state: expert per slot (-1 = empty), use counts, last-use steps,
+ * running hit and miss totals; any output may be NULL.
+ */
+typedef struct moe_lfu moe_lfu_t;
+MOE_API int moe_lfu_create(moe_lfu_t **out, int slots, int E);
+MOE_API int moe_lfu_destroy(moe_lfu_t *lfu);
+MOE_API int moe_lfu_step(moe_lfu_t *lfu, const int32_t *req, int n, int32_t *slot_out, uint8_t *hit_out);
+MOE_API int moe_lfu_state(const moe_lfu_t *lfu, int32_t *expert_of_slot, uint32_t *counts, int64_t *last,
+                          uint64_t *hits, uint64_t *misses);
+
+/*
+ * Per-layer expert cache on the current device: `slots` (<= 64) device slots of
+ * moe_tile_blob_bytes(H, I) bytes, run by the policy above, filled from the E
+ * tile-layout expert blobs the caller keeps in host memory at
+ * h_experts + e * host_stride (page-locked memory is needed for the copies to
+ * overlap compute; the library neither copies nor frees it).  The library
+ * allocates the slot pool, a non-blocking side stream and two events, all
+ * released by moe_cache_destroy (which first waits for the side stream).
+ * Use one cache with calls issued in order on one stream.
+ * moe_cache_slots: expert per slot (-1 = empty) and use counts.
+ * moe_cache_stats: hits, misses and bytes copied host -> device so far.
  */
 MOE_API int moe_cache_create(moe_cache_t **out, int H, int E, int I, const void *h_experts,
-                     size_t host_stride, int slots);
+                             size_t host_stride, int slots);
 MOE_API int moe_cache_destroy(moe_cache_t *cache);
-/* expert_of_slot[slots] (-1 = empty), counts[slots]; either may be NULL. */
 MOE_API int moe_cache_slots(const moe_cache_t *cache, int32_t *expert_of_slot, uint32_t *counts);
 MOE_API int moe_cache_stats(const moe_cache_t *cache, uint64_t *hits, uint64_t *misses,
-                    uint64_t *h2d_bytes);
+                            uint64_t *h2d_bytes);
 
 #ifdef __cplusplus
 }

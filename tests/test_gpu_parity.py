@@ -47,6 +47,28 @@ def test_quantiser_bit_exact(moe, bits, N, K):
     assert np.array_equal(b.cpu().numpy().view(np.uint16), ob)
 
 
+# ------------------------------------------------------------------ tile layout
+
+@pytest.mark.parametrize("H,I", [(128, 64), (384, 192), (2816, 704), (2816, 2112)])
+def test_expert_tile_bit_exact(moe, H, I):
+    """moe_expert_tile on random bytes: the oracle's untile gives back the input."""
+    n = oracle.expert_blob_bytes(H, I)
+    rng = np.random.default_rng(H + I)
+    mlx = rng.integers(0, 256, n, dtype=np.uint8)
+    # padding between the MLX parts is not part of the expert: keep it zero
+    off = oracle.expert_blob_offsets(H, I)
+    sizes = [I * H, 2 * I * (H // 64) * 2, 2 * I * (H // 64) * 2, H * I // 2, H * (I // 64) * 2,
+             H * (I // 64) * 2]
+    keep = np.zeros(n, bool)
+    for o, sz in zip(off, sizes):
+        keep[o:o + sz] = True
+    mlx[~keep] = 0
+    tiles = torch.empty(moe.moe_tile_blob_bytes(H, I), dtype=torch.uint8, device="cuda")
+    moe.moe_expert_tile(_cuda(mlx), H, I, tiles)
+    back = oracle.untile_expert(tiles.cpu().numpy(), H, I)
+    assert np.array_equal(back, mlx)
+
+
 # ------------------------------------------------------------------ qgemv
 
 @pytest.mark.parametrize("N,K", [(4, 64), (100, 320), (4224, 2816), (2816, 704), (2816, 2112)])
@@ -83,12 +105,15 @@ def full_uniform(moe):
 
 
 def _blobs_match(gl, ol, experts):
+    """The GPU's quantised weights (tile layout, read back through the oracle's
+    untile) equal the oracle's own quantisation, bit for bit."""
     rq, rs, rb = gl.router_host()
     assert np.array_equal(rq, ol.router[0]) and np.array_equal(rs, ol.router[1])
     assert np.array_equal(rb, ol.router[2])
-    assert np.array_equal(gl.shared_blob_host(), ol.shared)
+    assert np.array_equal(oracle.untile_expert(gl.shared_blob_host(), gl.H, gl.Is), ol.shared)
     for e in experts:
-        assert np.array_equal(gl.expert_blob_host(int(e)), ol.expert(int(e))), e
+        assert np.array_equal(oracle.untile_expert(gl.expert_blob_host(int(e)), gl.H, gl.I),
+                              ol.expert(int(e))), e
 
 
 def _route_check(moe, shape, gl, ol, T, stream_id):
