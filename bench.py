@@ -231,6 +231,10 @@ def run_ours(args):
     extra = {}
     if not args.quick and rank == 0:
         extra = side_measurements(torch, moe, layer, copies, ws, args)
+    if args.stack and rank == 0:
+        del layer, views
+        torch.cuda.empty_cache()
+        extra["stack_decode_lfu"] = stack_measurement(torch, moe, args)
 
     line = {
         "metric": "MoE decode tokens/s (one full-size layer, T=1) and % of B300 HBM roofline; prefill-chunk tok/s",
@@ -315,6 +319,77 @@ def side_measurements(torch, moe, layer, copies, ws, args):
     return out
 
 
+def stack_measurement(torch, moe, args, n_layers=30, steps=256, slots=16):
+    """30-layer MoE stack decode (MoE part only: attention is the identity, each
+    layer adds its output to the residual stream), one token per step, experts in
+    page-locked host memory behind a 16-slot LFU cache per layer.  Routing follows
+    Zipf(1.1) popularity (a per-layer logit bias) and the step inputs are an AR(1)
+    sequence (rho 0.9), so consecutive steps route alike.  Weights come from the
+    GPU's seeded normal generator (N(0, 0.02)), quantised and tiled by the library."""
+    s = synth.FULL
+    dev = torch.device("cuda")
+    blob = moe.moe_tile_blob_bytes(H, I)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(0)
+    layers, hosts, caches, views = [], [], [], []
+    n_host = 0
+    for l in range(n_layers):
+        L = moe.Layer(H, E, TOPK, I, IS, device=dev, copies=1)
+        L.set_router(torch.randn(E, H, generator=gen, device=dev) * 0.02)
+        for e in range(E):
+            L.set_expert(e, torch.randn(2 * I, H, generator=gen, device=dev) * 0.02,
+                         torch.randn(H, I, generator=gen, device=dev) * 0.02)
+        L.set_shared(torch.randn(2 * IS, H, generator=gen, device=dev) * 0.02,
+                     torch.randn(H, IS, generator=gen, device=dev) * 0.02)
+        L.set_bias(synth.popularity_bias(s, seed=0, layer=l))
+        try:
+            host = torch.empty((E, blob), dtype=torch.uint8).pin_memory()
+            host.copy_(L.experts[0])
+            n_host += 1
+        except RuntimeError:
+            host = hosts[l % max(n_host, 1)]  # host memory ran short: reuse a layer's experts
+        L.experts = None
+        layers.append(L)
+        hosts.append(host)
+        views.append(L.view(experts=False))
+        caches.append(moe.Cache(H, E, I, host, slots=slots))
+    torch.cuda.synchronize()
+    X = torch.from_numpy(synth.token_sequence(s, steps, seed=0)).to(dev)
+    h = [torch.empty((1, H), device=dev), torch.empty((1, H), device=dev)]
+    ws = moe.new_workspace(views[0], 1)
+    warm = 8
+
+    def run(first, n):
+        for st in range(first, first + n):
+            cur = X[st:st + 1]
+            for l in range(n_layers):
+                moe.moe_layer_decode(views[l], cur, ws, y=h[l & 1], flags=moe.MOE_RESIDUAL, cache=caches[l])
+                cur = h[l & 1]
+
+    run(0, warm)
+    torch.cuda.synchronize()
+    st0 = [c.stats() for c in caches]
+    t0 = time.perf_counter()
+    run(warm, steps - warm)
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    st1 = [c.stats() for c in caches]
+    hits = sum(b[0] - a[0] for a, b in zip(st0, st1))
+    misses = sum(b[1] - a[1] for a, b in zip(st0, st1))
+    h2d = sum(b[2] - a[2] for a, b in zip(st0, st1))
+    n = steps - warm
+    out = {"layers": n_layers, "steps_timed": n, "slots_per_layer": slots, "tok_s": n / dt,
+           "ms_per_token": dt / n * 1e3, "hit_rate": hits / max(hits + misses, 1),
+           "misses_per_token": misses / n, "h2d_GB_s": h2d / dt / 1e9,
+           "host_layers_distinct": n_host,
+           "device_bytes_per_token": n_layers * DECODE_BYTES,
+           "note": "host-synchronous per layer (routing copied to the host for the LFU policy); "
+                   "misses copied on a side stream while the shared expert runs"}
+    for c in caches:
+        c.close()
+    return out
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -344,6 +419,8 @@ def main():
     ap.add_argument("--quick", action="store_true", help="headline only, no side measurements")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle timing")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--stack", action=argparse.BooleanOptionalAction, default=True,
+                    help="also run the 30-layer stack decode with per-layer LFU caches")
     ap.add_argument("--copies", type=int, default=0,
                     help="distinct layer copies to rotate over (default: enough to exceed 4x L2)")
     args = ap.parse_args()

@@ -84,8 +84,20 @@ struct Ws {
     __half *hs16;      // [Tmax][Is]      shared activations
     float *pr;         // [Tmax*topk][H]  routed down partials
     float *ps;         // [P][Tmax][H]    shared down partials
+    // prefill chunk (grouped GEMMs)
+    int *plan;         // U, rows used, uexp[256], urow[256], ucnt[256], rowtok[Rmax], rowpair[Rmax]
+    uint8_t *Br, *Bs;  // token operand tiles: [H/64][Rmax][128 B], [H/64][T16][128 B]
+    uint8_t *Hr, *Hs;  // h operand tiles:     [I/64][Rmax][128 B], [Is/64][T16][128 B]
+    float *Yr, *Ys;    // down rows: [Tmax*topk][H], [T16][H]
     int Tmax;
 };
+
+// Rows of the prefill's per-expert segments (each expert's token count rounded
+// up to 16) for T tokens: at most T*topk tokens plus 15 padding rows per expert.
+inline int prefill_rows(const moe_layer_t &l, int T) {
+    const int p = T * l.topk, u = p < l.E ? p : l.E;
+    return (p + 15 * u + 15) & ~15;
+}
 
 // The control words and the 16-row-tile tickets sit in a header of fixed size
 // (enough tickets for the largest hidden size the layer calls accept), so one
@@ -96,7 +108,8 @@ constexpr int kMaxTickets = kMaxHiddenLayer / 16;
 constexpr size_t kWsHeaderBytes = (kCtrlWords + kMaxTickets) * sizeof(unsigned);
 
 struct WsLayout {
-    size_t ctrl, logits, idx, gate, h16, hs16, pr, ps, total;
+    size_t ctrl, logits, idx, gate, h16, hs16, pr, ps, decode_total;
+    size_t plan, Br, Bs, Hr, Hs, Yr, Ys, total;
     int Tmax;
 };
 
@@ -113,6 +126,15 @@ inline WsLayout ws_layout(const moe_layer_t &l, int Tmax) {
     W.hs16 = off;   off = up256(off + sizeof(__half) * size_t(Tmax) * l.Is);
     W.pr = off;     off = up256(off + sizeof(float) * size_t(Tmax) * l.topk * l.H);
     W.ps = off;     off = up256(off + sizeof(float) * size_t(P) * Tmax * l.H);
+    W.decode_total = off;
+    const int Rmax = prefill_rows(l, Tmax), T16 = (Tmax + 15) & ~15;
+    W.plan = off;   off = up256(off + sizeof(int) * (2 + 3 * MOE_MAX_EXPERTS + 2 * size_t(Rmax)));
+    W.Br = off;     off = up256(off + size_t(l.H / kGroup) * Rmax * 128);
+    W.Bs = off;     off = up256(off + size_t(l.H / kGroup) * T16 * 128);
+    W.Hr = off;     off = up256(off + size_t(l.I / kGroup) * Rmax * 128);
+    W.Hs = off;     off = up256(off + size_t(l.Is / kGroup) * T16 * 128);
+    W.Yr = off;     off = up256(off + sizeof(float) * size_t(Tmax) * l.topk * l.H);
+    W.Ys = off;     off = up256(off + sizeof(float) * size_t(T16) * l.H);
     W.total = off;
     return W;
 }
@@ -129,6 +151,13 @@ inline Ws ws_bind(void *base, const WsLayout &W, const moe_layer_t &l) {
     w.hs16 = (__half *)(p + W.hs16);
     w.pr = (float *)(p + W.pr);
     w.ps = (float *)(p + W.ps);
+    w.plan = (int *)(p + W.plan);
+    w.Br = p + W.Br;
+    w.Bs = p + W.Bs;
+    w.Hr = p + W.Hr;
+    w.Hs = p + W.Hs;
+    w.Yr = (float *)(p + W.Yr);
+    w.Ys = (float *)(p + W.Ys);
     w.Tmax = W.Tmax;
     (void)l;
     return w;

@@ -13,9 +13,9 @@
 // as possible, so HBM streams continuously while the SMs compute.
 //
 //   phase A  producer: copies this CTA's shared-expert gate/up tiles, prefetches
-//            a slice of the shared down matrix, computes its router rows (CUDA
-//            cores, 8-bit), publishes them, waits until all E rows are in.
-//            compute warps: shared gate/up tiles (below).
+//            a slice of the shared down matrix, waits until all E router rows
+//            are published.  compute warps: this CTA's router rows (CUDA cores,
+//            8-bit; each row split over the warps), then its shared gate/up tiles.
 //   routing  every CTA ranks the logits itself (identical results everywhere),
 //            and builds the schedule: distinct experts U in ascending id, the
 //            tokens using each, and a compact slot per (token, choice).
@@ -46,6 +46,7 @@ constexpr int kDecThreads = kCThreads + 32;   // + producer warp
 constexpr int kMaxStages = 4;
 constexpr int kMaxUnitsPerCta = 512;
 constexpr int kMaxPairs = MOE_MAX_DECODE_TOKENS * MOE_MAX_TOPK;
+constexpr int kMaxRouterRows = 4;  // router rows per CTA (E <= 4 x grid size)
 
 // What one launch does: the shared expert, the routed experts, or both; and
 // whether the routing comes from an earlier router launch (idx_pre/gate_pre)
@@ -105,6 +106,31 @@ __device__ __forceinline__ void affine_acc(float (&acc)[4], const float (&d)[4],
 // B-fragment loads of 8 consecutive lanes hit 8 distinct bank groups.
 __host__ __device__ __forceinline__ int h_pos(int k, int j) { return frag_pos(k) ^ ((j & 1) << 3); }
 
+// Partial router logit of row e for token t over the word pairs [p0, p1) of the
+// 8-bit row (pair p holds columns 8p..8p+7), summed over the warp.
+__device__ __forceinline__ float router_partial(const DecodeArgs &a, int e, int t, int p0, int p1) {
+    const int lane = threadIdx.x & 31, G = a.H / kGroup;
+    const uint2 *row = reinterpret_cast<const uint2 *>(a.rq + (size_t)e * (a.H / 4));
+    const float4 *xt = reinterpret_cast<const float4 *>(a.x + (size_t)t * a.H);
+    const __half *sr = a.rs + (size_t)e * G, *br = a.rb + (size_t)e * G;
+    float acc = 0.f;
+#pragma unroll 4
+    for (int p = p0 + lane; p < p1; p += 32) {
+        const uint2 w = __ldg(row + p);
+        const float s = __half2float(sr[p >> 3]), bb = __half2float(br[p >> 3]);
+        const float4 x0 = __ldg(xt + 2 * p), x1 = __ldg(xt + 2 * p + 1);
+        acc = fmaf(fmaf(s, (float)(w.x & 0xFFu), bb), x0.x, acc);
+        acc = fmaf(fmaf(s, (float)((w.x >> 8) & 0xFFu), bb), x0.y, acc);
+        acc = fmaf(fmaf(s, (float)((w.x >> 16) & 0xFFu), bb), x0.z, acc);
+        acc = fmaf(fmaf(s, (float)(w.x >> 24), bb), x0.w, acc);
+        acc = fmaf(fmaf(s, (float)(w.y & 0xFFu), bb), x1.x, acc);
+        acc = fmaf(fmaf(s, (float)((w.y >> 8) & 0xFFu), bb), x1.y, acc);
+        acc = fmaf(fmaf(s, (float)((w.y >> 16) & 0xFFu), bb), x1.z, acc);
+        acc = fmaf(fmaf(s, (float)(w.y >> 24), bb), x1.w, acc);
+    }
+    return warp_sum(acc);
+}
+
 struct DecodeSmem {
     uint64_t full[kMaxStages], empty[kMaxStages], hbar;
     int idx[kMaxPairs];
@@ -114,6 +140,7 @@ struct DecodeSmem {
     short uid[MOE_MAX_EXPERTS];
     int uexp[kMaxPairs], ubase[kMaxPairs], ucnt[kMaxPairs], uslot[kMaxPairs];
     unsigned char last[kMaxUnitsPerCta];
+    float rpart[kMaxRouterRows][kCW];
     int U;
     int err;
 };
@@ -185,7 +212,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
     const int g0w = warp * G / kCW, g1w = (warp + 1) * G / kCW;
     uint32_t xb[GPW][NCH][8];
     float xs[GPW][NCH][2];
-    if (!producer) {
+    auto load_x = [&]() {
 #pragma unroll
         for (int gi = 0; gi < GPW; gi++)
 #pragma unroll
@@ -200,72 +227,78 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
                 xs[gi][ch][0] = d[0];
                 xs[gi][ch][1] = d[1];
             }
-    }
+    };
 
-    // One gate/up tile by the compute warps: K split over warps, reduction in
-    // shared memory, GeGLU, fp16 store of h.  `u` < 0 marks the shared expert.
+    // One or two gate/up tiles by the compute warps: K split over warps, partial
+    // sums meet in shared memory (one barrier per pair of tiles), GeGLU, fp16 store
+    // of h.  Tile j of the pair sits in ring stage s[j]; u[j] < 0 marks the shared
+    // expert, it[j] is the tile's row block.
     int rbuf = 0;
-    auto gateup_tile = [&](int s, int u, int it) {
-        float acc[NCH][4];
+    auto gateup_tiles = [&](int n, const int (&s)[2], const int (&u)[2], const int (&it)[2]) {
+        float *rw = red + (size_t)rbuf * 2 * kCW * NCH * 128;
 #pragma unroll
-        for (int ch = 0; ch < NCH; ch++)
+        for (int j = 0; j < 2; j++) {
+            if (j >= n) break;
+            float acc[NCH][4];
 #pragma unroll
-            for (int i = 0; i < 4; i++) acc[ch][i] = 0.f;
-        if (!*err) {
-            const uint8_t *st = ring + (size_t)s * a.SB;
+            for (int ch = 0; ch < NCH; ch++)
 #pragma unroll
-            for (int gi = 0; gi < GPW; gi++) {
-                const int g = g0w + gi;
-                if (g < g1w) {
-                    const uint4 q = *reinterpret_cast<const uint4 *>(st + g * kTileBytes + 16 * lane);
-                    const uint2 e = *reinterpret_cast<const uint2 *>(st + g * kTileBytes + 512 + 8 * gl);
-                    const float sa = lo_half(e.x) * kTwo24, ba = hi_half(e.x);
-                    const float sb = lo_half(e.y) * kTwo24, bb = hi_half(e.y);
+                for (int i = 0; i < 4; i++) acc[ch][i] = 0.f;
+            if (!*err) {
+                const uint8_t *st = ring + (size_t)s[j] * a.SB;
 #pragma unroll
-                    for (int ch = 0; ch < NCH; ch++) {
-                        float d[4] = {0.f, 0.f, 0.f, 0.f};
-                        mma_group_codes(d, make_uint2(q.x, q.y), make_uint2(q.z, q.w), xb[gi][ch]);
-                        affine_acc(acc[ch], d, xs[gi][ch][0], xs[gi][ch][1], sa, ba, sb, bb);
+                for (int gi = 0; gi < GPW; gi++) {
+                    const int g = g0w + gi;
+                    if (g < g1w) {
+                        const uint4 q = *reinterpret_cast<const uint4 *>(st + g * kTileBytes + 16 * lane);
+                        const uint2 e = *reinterpret_cast<const uint2 *>(st + g * kTileBytes + 512 + 8 * gl);
+                        const float sa = lo_half(e.x) * kTwo24, ba = hi_half(e.x);
+                        const float sb = lo_half(e.y) * kTwo24, bb = hi_half(e.y);
+#pragma unroll
+                        for (int ch = 0; ch < NCH; ch++) {
+                            float d[4] = {0.f, 0.f, 0.f, 0.f};
+                            mma_group_codes(d, make_uint2(q.x, q.y), make_uint2(q.z, q.w), xb[gi][ch]);
+                            affine_acc(acc[ch], d, xs[gi][ch][0], xs[gi][ch][1], sa, ba, sb, bb);
+                        }
                     }
                 }
             }
+            consumer_release(s[j]);
+#pragma unroll
+            for (int ch = 0; ch < NCH; ch++)
+                reinterpret_cast<float4 *>(rw + (size_t)((j * kCW + warp) * NCH + ch) * 128)[lane] =
+                    make_float4(acc[ch][0], acc[ch][1], acc[ch][2], acc[ch][3]);
         }
-        consumer_release(s);
-        float *rw = red + (size_t)((rbuf * kCW + warp) * NCH) * 128;
-#pragma unroll
-        for (int ch = 0; ch < NCH; ch++)
-            reinterpret_cast<float4 *>(rw + ch * 128)[lane] = make_float4(acc[ch][0], acc[ch][1], acc[ch][2], acc[ch][3]);
         named_sync(1, kCThreads);
-        // reduce: output o = (ch, lane L, column i) uses slots i (gate) and i+2 (up)
-        constexpr int SPLIT = 8 / NCH, WPT = kCW / SPLIT;
-        const int o = tid / SPLIT, q = tid % SPLIT;
-        const int ch = o / 64, L = (o % 64) >> 1, i = o & 1;
+        // reduce: output o = (tile j, ch, lane L, column i) uses slots i (gate) and
+        // i+2 (up) of the 16 warps' partials
+        const int outs = n * NCH * 64;
+        const int split = kCThreads / outs, wpt = kCW / split;
+        const int o = tid / split, q = tid % split;
+        const int j = o / (NCH * 64), ch = (o / 64) % NCH, L = (o % 64) >> 1, i = o & 1;
         float gs = 0.f, us = 0.f;
-        const float *rr = red + (size_t)(rbuf * kCW) * NCH * 128;
-#pragma unroll
-        for (int w = 0; w < WPT; w++) {
-            const float *p = rr + (size_t)((q * WPT + w) * NCH + ch) * 128 + L * 4;
+        for (int w = 0; w < wpt; w++) {
+            const float *p = rw + (size_t)((j * kCW + q * wpt + w) * NCH + ch) * 128 + L * 4;
             gs += p[i];
             us += p[i + 2];
         }
-#pragma unroll
-        for (int off = SPLIT / 2; off > 0; off >>= 1) {
+        for (int off = split / 2; off > 0; off >>= 1) {
             gs += __shfl_xor_sync(0xffffffffu, gs, off);
             us += __shfl_xor_sync(0xffffffffu, us, off);
         }
         rbuf ^= 1;
         if (q != 0 || *err) return;
-        const int row = 8 * it + (L >> 2), t = 8 * ch + 2 * (L & 3) + i;
+        const int row = 8 * it[j] + (L >> 2), t = 8 * ch + 2 * (L & 3) + i;
         if (t >= T) return;
         const __half hv = __float2half_rn(gelu_tanh(gs) * us);
         const int g = row / kGroup, k = row % kGroup;
-        if (u < 0) {
+        if (u[j] < 0) {
             a.hs16[((size_t)g * T + t) * kGroup + h_pos(k, t)] = hv;
         } else {
-            const unsigned m = S.mask[S.uexp[u]];
+            const unsigned m = S.mask[S.uexp[u[j]]];
             if ((m >> t) & 1u) {
-                const int slot = __popc(m & ((1u << t) - 1u)), n = S.ucnt[u];
-                a.h16[(size_t)S.ubase[u] * a.I + ((size_t)g * n + slot) * kGroup + h_pos(k, slot)] = hv;
+                const int slot = __popc(m & ((1u << t) - 1u)), nu = S.ucnt[u[j]];
+                a.h16[(size_t)S.ubase[u[j]] * a.I + ((size_t)g * nu + slot) * kGroup + h_pos(k, slot)] = hv;
             }
         }
     };
@@ -273,64 +306,35 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
     // =========================== phase A ===========================
     if (producer) {
         if (lane == 0) {
-            // this CTA's shared gate/up tiles (as many as the ring holds now)
+            // this CTA's shared gate/up tiles, and a slice of the shared down matrix into L2
             for (int k = 0; k < n_shared_mine && k < a.stages; k++) {
                 const int s = producer_slot(fill);
                 mbar_arrive_expect_tx(&S.full[s], gu_bytes);
                 bulk_g2s(ring + (size_t)s * a.SB, gu_src(b + k * nC), gu_bytes, &S.full[s]);
                 last_fill[s] = fill++;
             }
-            // a slice of the shared down matrix, into L2
             for (int r = b; r < R && do_shared; r += nC)
                 prefetch_l2(a.shared + a.Ls.gu_bytes + (size_t)kTileBytes * Gs * r, kTileBytes * Gs);
         }
-        // router rows e = b, b + nC, ... (8-bit affine, fp32 FMA)
-        int nrows = 0;
-        const int wpr = H / 4, Gr = H / kGroup;
-        for (int e = b; e < a.E && !pre; e += nC) {
-            nrows++;
-            const uint32_t *row = a.rq + (size_t)e * wpr;
-            float acc[MOE_MAX_DECODE_TOKENS];
-#pragma unroll
-            for (int t = 0; t < MOE_MAX_DECODE_TOKENS; t++) acc[t] = 0.f;
-            for (int w0 = 2 * lane; w0 < wpr; w0 += 64) {
-                const uint2 wd = __ldg(reinterpret_cast<const uint2 *>(row + w0));
-                const int g = w0 >> 4;
-                const float s = __half2float(a.rs[(size_t)e * Gr + g]);
-                const float bb = __half2float(a.rb[(size_t)e * Gr + g]);
-                float wv[8];
-#pragma unroll
-                for (int i = 0; i < 4; i++) {
-                    wv[i] = fmaf(s, (float)((wd.x >> (8 * i)) & 0xFFu), bb);
-                    wv[4 + i] = fmaf(s, (float)((wd.y >> (8 * i)) & 0xFFu), bb);
-                }
-#pragma unroll
-                for (int t = 0; t < MOE_MAX_DECODE_TOKENS; t++) {
-                    if (t < T) {
-                        const float4 *xv = reinterpret_cast<const float4 *>(a.x + (size_t)t * H + 4 * w0);
-                        const float4 x0 = __ldg(xv), x1 = __ldg(xv + 1);
-                        float v = acc[t];
-                        v = fmaf(wv[0], x0.x, v); v = fmaf(wv[1], x0.y, v);
-                        v = fmaf(wv[2], x0.z, v); v = fmaf(wv[3], x0.w, v);
-                        v = fmaf(wv[4], x1.x, v); v = fmaf(wv[5], x1.y, v);
-                        v = fmaf(wv[6], x1.z, v); v = fmaf(wv[7], x1.w, v);
-                        acc[t] = v;
-                    }
+        if (!pre) {
+            // this CTA's router logits from the compute warps' partial sums
+            named_sync(2, kDecThreads);
+            const int nchk = T >= kCW ? 1 : kCW / T;
+            int j = 0;
+            for (int e = b; e < a.E; e += nC, j++) {
+                if (lane < T) {
+                    float acc = 0.f;
+                    for (int k = 0; k < nchk; k++) acc += S.rpart[j][lane * nchk + k];
+                    a.logits[(size_t)lane * a.E + e] = acc + (a.bias ? a.bias[e] : 0.f);
                 }
             }
-#pragma unroll
-            for (int t = 0; t < MOE_MAX_DECODE_TOKENS; t++) {
-                if (t < T) {
-                    const float v = warp_sum(acc[t]);
-                    if (lane == 0) a.logits[(size_t)t * a.E + e] = v + (a.bias ? a.bias[e] : 0.f);
-                }
+            if (j > 0) {
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) atomicAdd(&a.ctrl[kRouteCnt], (unsigned)j);
             }
         }
         if (lane == 0) {
-            if (nrows) {
-                __threadfence();
-                atomicAdd(&a.ctrl[kRouteCnt], (unsigned)nrows);
-            }
             for (int k = a.stages; k < n_shared_mine; k++) {
                 const int s = producer_slot(fill);
                 if (!*err) {
@@ -344,9 +348,30 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
         }
         __syncwarp();
     } else {
-        for (int k = 0; k < n_shared_mine; k++) {
-            const int s = consumer_wait(fill++);
-            gateup_tile(s, -1, b + k * nC);
+        if (!pre) {
+            // router rows e = b, b + nC, ...: warp w takes token w / nchk and chunk
+            // w % nchk of the row, so every lane issues its few loads at once; the
+            // producer warp adds the partial sums up and publishes the logits
+            const int nchk = T >= kCW ? 1 : kCW / T;
+            const int np = H / 8;  // 8-code word pairs per row
+            const int t = warp / nchk, ck = warp % nchk;
+            int j = 0;
+            for (int e = b; e < a.E; e += nC, j++) {
+                float v = 0.f;
+                if (t < T) v = router_partial(a, e, t, ck * np / nchk, (ck + 1) * np / nchk);
+                if (lane == 0) S.rpart[j][warp] = v;
+            }
+            named_arrive(2, kDecThreads);
+        }
+        load_x();
+        for (int k = 0; k < n_shared_mine; k += 2) {
+            const int n = min(2, n_shared_mine - k);
+            int s[2] = {0, 0}, u[2] = {-1, -1}, it[2] = {0, 0};
+            for (int j = 0; j < n; j++) {
+                s[j] = consumer_wait(fill++);
+                it[j] = b + (k + j) * nC;
+            }
+            gateup_tiles(n, s, u, it);
         }
     }
     __syncthreads();
@@ -365,13 +390,15 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
                               S.gate + t * a.topk, b == 0 ? a.idx_out + (a.idx_out ? t * a.topk : 0) : nullptr,
                               b == 0 ? a.gate_out + (a.gate_out ? t * a.topk : 0) : nullptr);
     }
-    for (int e = tid; e < a.E; e += kDecThreads) S.mask[e] = 0u;
     __syncthreads();
+    // the schedule, built by warp 0 alone
     const int P2 = T * a.topk;
-    if (!*err)
-        for (int p = tid; p < P2; p += kDecThreads) atomicOr(&S.mask[S.idx[p]], 1u << (p / a.topk));
-    __syncthreads();
     if (warp == 0) {
+        for (int e = lane; e < a.E; e += 32) S.mask[e] = 0u;
+        __syncwarp();
+        if (!*err)
+            for (int p = lane; p < P2; p += 32) atomicOr(&S.mask[S.idx[p]], 1u << (p / a.topk));
+        __syncwarp();
         int ubase = 0, sbase = 0;
         for (int e0 = 0; e0 < a.E; e0 += 32) {
             const int e = e0 + lane;
@@ -397,11 +424,11 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
             sbase += __shfl_sync(0xffffffffu, incl, 31);
         }
         if (lane == 0) S.U = *err ? 0 : ubase;
-    }
-    __syncthreads();
-    for (int p = tid; p < P2 && !*err; p += kDecThreads) {
-        const int t = p / a.topk, e = S.idx[p];
-        S.pidx[p] = S.ubase[S.uid[e]] + __popc(S.mask[e] & ((1u << t) - 1u));
+        __syncwarp();
+        for (int p = lane; p < P2 && !*err; p += 32) {
+            const int t = p / a.topk, e = S.idx[p];
+            S.pidx[p] = S.ubase[S.uid[e]] + __popc(S.mask[e] & ((1u << t) - 1u));
+        }
     }
     __syncthreads();
 
@@ -428,17 +455,20 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
 
     // =========================== phase B ===========================
     if (producer) {
-        if (lane == 0 && !*err) {
-            // everything this CTA will read, into L2, in the order it is needed
-            for (int k = 0; k < n_routed_mine; k++) prefetch_l2(gu_src(j_first + k * nC), gu_bytes);
-            for (int k = 0; k < nunits; k++) {
-                int ng;
-                const uint8_t *src = unit_src(ulo + k, &ng);
-                prefetch_l2(src, kTileBytes * ng);
-            }
-        }
         if (lane == 0) {
-            for (int k = 0; k < n_routed_mine; k++) {
+            // the routed gate/up tiles through the ring (bulk copies stream better
+            // on their own than behind L2 prefetches of the same data)
+            const int first = min(n_routed_mine, a.stages);
+            for (int k = 0; k < first; k++) {
+                const int s = producer_slot(fill);
+                if (!*err) {
+                    mbar_arrive_expect_tx(&S.full[s], gu_bytes);
+                    bulk_g2s(ring + (size_t)s * a.SB, gu_src(j_first + k * nC), gu_bytes, &S.full[s]);
+                    last_fill[s] = fill;
+                }
+                fill++;
+            }
+            for (int k = first; k < n_routed_mine; k++) {
                 const int s = producer_slot(fill);
                 if (!*err) {
                     mbar_arrive_expect_tx(&S.full[s], gu_bytes);
@@ -499,10 +529,16 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
         __syncwarp();
     } else {
         // ---- routed gate/up tiles
-        for (int k = 0; k < n_routed_mine; k++) {
-            const int s = consumer_wait(fill++);
-            const int j = j_first + k * nC;
-            gateup_tile(s, (j - Ts) / Ti, (j - Ts) % Ti);
+        for (int k = 0; k < n_routed_mine; k += 2) {
+            const int n = min(2, n_routed_mine - k);
+            int s[2] = {0, 0}, u[2] = {0, 0}, it[2] = {0, 0};
+            for (int j = 0; j < n; j++) {
+                s[j] = consumer_wait(fill++);
+                const int jj = j_first + (k + j) * nC;
+                u[j] = (jj - Ts) / Ti;
+                it[j] = (jj - Ts) % Ti;
+            }
+            gateup_tiles(n, s, u, it);
         }
         __threadfence();
         named_sync(1, kCThreads);
@@ -538,6 +574,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
                 for (int ch = 0; ch < NCH; ch++)
 #pragma unroll
                     for (int v = 0; v < 4; v++) acc[ch][v] = 0.f;
+#pragma unroll 4
                 for (int g = 0; g < ng; g++) {
                     const uint4 q = *reinterpret_cast<const uint4 *>(wst + g * kTileBytes + 16 * lane);
                     const uint2 e = *reinterpret_cast<const uint2 *>(wst + g * kTileBytes + 512 + 8 * gl);
@@ -589,24 +626,26 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
             if (!*err && do_routed) {
                 const int r = (ulo + lu) % R;
                 last = atomicAdd(&a.ticket[r], 1u) == target - 1u;
-                if (last) __threadfence();
+                if (last) {
+                    a.ticket[r] = 0u;  // every contribution to this tile is in
+                    __threadfence();
+                }
             }
             S.last[lu] = last;
         }
         named_sync(1, kCThreads);
-        for (int lu = 0; lu < nunits; lu++) {
+        // all the tiles this CTA closes, combined together
+        for (int v = tid; v < nunits * 16 * T; v += kCThreads) {
+            const int lu = v / (16 * T);
             if (!S.last[lu]) continue;
-            const int r = (ulo + lu) % R;
-            for (int v = tid; v < 16 * T; v += kCThreads) {
-                const int t = v >> 4, n = 16 * r + (v & 15);
-                float acc = 0.f;
-                for (int k = 0; k < a.topk; k++)
-                    acc = fmaf(S.gate[t * a.topk + k], __ldcg(a.pr + (size_t)S.pidx[t * a.topk + k] * H + n), acc);
-                for (int p = 0; p < a.P; p++) acc += __ldcg(a.ps + ((size_t)p * T + t) * H + n);
-                if (a.flags & MOE_RESIDUAL) acc += __ldg(a.x + (size_t)t * H + n);
-                a.y[(size_t)t * H + n] = acc;
-            }
-            if (tid == 0) a.ticket[r] = 0u;
+            const int w = v % (16 * T), t = w >> 4;
+            const int n = 16 * ((ulo + lu) % R) + (w & 15);
+            float acc = 0.f;
+            for (int k = 0; k < a.topk; k++)
+                acc = fmaf(S.gate[t * a.topk + k], __ldcg(a.pr + (size_t)S.pidx[t * a.topk + k] * H + n), acc);
+            for (int p = 0; p < a.P; p++) acc += __ldcg(a.ps + ((size_t)p * T + t) * H + n);
+            if (a.flags & MOE_RESIDUAL) acc += __ldg(a.x + (size_t)t * H + n);
+            a.y[(size_t)t * H + n] = acc;
         }
     }
 

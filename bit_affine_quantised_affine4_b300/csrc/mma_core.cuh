@@ -39,6 +39,8 @@ __host__ __device__ __forceinline__ int frag_pos(int k) {
 // of rows g and g+8; xb = the lane's 8 B registers (two 16-byte loads).
 __device__ __forceinline__ void mma_group_codes(float (&d)[4], uint2 qa, uint2 qb,
                                                 const uint32_t (&xb)[8]) {
+    // two independent accumulator chains (words 2c and 2c+1), added at the end
+    float e[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int j = 0; j < 2; j++) {
         const uint32_t wa = j ? qa.y : qa.x, wb = j ? qb.y : qb.x;
@@ -49,9 +51,14 @@ __device__ __forceinline__ void mma_group_codes(float (&d)[4], uint2 qa, uint2 q
             a[1] = (wb >> (8 * h)) & 0x000F000Fu;
             a[2] = (wa >> (8 * h + 4)) & 0x000F000Fu;
             a[3] = (wb >> (8 * h + 4)) & 0x000F000Fu;
-            mma16816(d, a, xb[4 * j + 2 * h], xb[4 * j + 2 * h + 1]);
+            if (j == 0)
+                mma16816(d, a, xb[4 * j + 2 * h], xb[4 * j + 2 * h + 1]);
+            else
+                mma16816(e, a, xb[4 * j + 2 * h], xb[4 * j + 2 * h + 1]);
         }
     }
+#pragma unroll
+    for (int i = 0; i < 4; i++) d[i] += e[i];
 }
 
 // S += sum of the group's 64 token values, for token columns (2c, 2c+1) in d[0], d[1]
@@ -59,10 +66,14 @@ __device__ __forceinline__ void mma_group_codes(float (&d)[4], uint2 qa, uint2 q
 __device__ __forceinline__ void mma_group_sums(float (&d)[4], const uint32_t (&xb)[8]) {
     const uint32_t one2 = 0x3C003C00u;  // fp16x2 (1, 1)
     const uint32_t a[4] = {one2, one2, one2, one2};
+    float e[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int j = 0; j < 2; j++)
+    for (int h = 0; h < 2; h++) {
+        mma16816(d, a, xb[2 * h], xb[2 * h + 1]);
+        mma16816(e, a, xb[4 + 2 * h], xb[4 + 2 * h + 1]);
+    }
 #pragma unroll
-        for (int h = 0; h < 2; h++) mma16816(d, a, xb[4 * j + 2 * h], xb[4 * j + 2 * h + 1]);
+    for (int i = 0; i < 4; i++) d[i] += e[i];
 }
 
 // acc += s * 2^24 * D + b * S for the lane's four accumulator slots.

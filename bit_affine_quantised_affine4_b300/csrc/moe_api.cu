@@ -11,6 +11,7 @@
 #include "quantise.cuh"
 #include "tile.cuh"
 #include "decode.cuh"
+#include "prefill.cuh"
 #include "gemv.cuh"
 #include "lfu.h"
 
@@ -70,12 +71,14 @@ int cuda_status() {
 }
 
 // The workspace layout depends on T_max; recover the largest T_max whose layout
-// fits in ws_bytes (it is what the caller sized it for, or larger).
-WsLayout ws_fit(const moe_layer_t *l, size_t ws_bytes) {
+// fits in ws_bytes (it is what the caller sized it for, or larger).  Decode uses
+// only the layout's prefix (decode_total); the prefill chunk needs all of it.
+// Only the header is carried from call to call, and it sits at a fixed place.
+WsLayout ws_fit(const moe_layer_t *l, size_t ws_bytes, bool full) {
     WsLayout best = ws_layout(*l, 1);
     for (int t = 2; t <= MOE_MAX_PREFILL_TOKENS; t++) {
         WsLayout w = ws_layout(*l, t);
-        if (w.total > ws_bytes) break;
+        if ((full ? w.total : w.decode_total) > ws_bytes) break;
         best = w;
     }
     return best;
@@ -83,10 +86,10 @@ WsLayout ws_fit(const moe_layer_t *l, size_t ws_bytes) {
 
 // Binds the caller's workspace: the layout is the one for the largest T_max whose
 // size fits ws_bytes (what moe_workspace_bytes was asked for, or more).
-int bind_ws(const moe_layer_t *l, int T, void *d_ws, size_t ws_bytes, Ws *out) {
+int bind_ws(const moe_layer_t *l, int T, void *d_ws, size_t ws_bytes, Ws *out, bool full = false) {
     if (!d_ws || !aligned(d_ws, 256)) return MOE_EWORKSPACE;
-    WsLayout W = ws_fit(l, ws_bytes);
-    if (W.total > ws_bytes || W.Tmax < T) return MOE_EWORKSPACE;
+    WsLayout W = ws_fit(l, ws_bytes, full);
+    if ((full ? W.total : W.decode_total) > ws_bytes || W.Tmax < T) return MOE_EWORKSPACE;
     *out = ws_bind(d_ws, W, *l);
     return MOE_OK;
 }
@@ -163,6 +166,7 @@ int decode_plan(const moe_layer_t *l, const float *x, int T, int flags, float *y
     const int gpw = (a.Lr.G + kCW - 1) / kCW;
     if (gpw > 4 || l->H > kMaxHiddenLayer) return MOE_EINVAL;  // hidden size above 4096
     const int nC = cfg.sms;
+    if ((l->E + nC - 1) / nC > kMaxRouterRows) return MOE_EINVAL;
     const int R = a.Lr.R, Gi = a.Lr.Gi;
     const int Umax = T * l->topk < l->E ? T * l->topk : l->E;
     const long long units_cta = ((long long)(a.P + Umax) * R + nC - 1) / nC;
@@ -171,7 +175,7 @@ int decode_plan(const moe_layer_t *l, const float *x, int T, int flags, float *y
     a.SB = (int)(((size_t)(a.Lr.G > Gi ? a.Lr.G : Gi) * kTileBytes + 127) / 128 * 128);
     a.UPS = a.SB / (Gi * kTileBytes);
     a.hsm_mat_bytes = Gi * T * 128;
-    const int red = 2 * kCW * nch * 512;
+    const int red = 2 * 2 * kCW * nch * 512;  // two buffers of two tiles' partial sums
     void *fn = decode_kernel(nch, gpw);
     size_t &st = cfg.static_smem[nch - 1][gpw - 1];
     if (st == 0) {
@@ -222,17 +226,66 @@ int run_decode(const moe_layer_t *l, const float *x, int T, int flags, float *y,
     return decode_launch(plan, kModeShared | kModeRouted, stream);
 }
 
-// Prefill chunk: the chunk's tokens in groups of up to MOE_MAX_DECODE_TOKENS.
+// Prefill chunk: router, plan, gather, the two grouped GEMMs on the tensor
+// cores, combine (prefill.cuh).
 int run_layer_chunk(const moe_layer_t *l, const float *x, int T, int flags, float *y,
                     int32_t *idx_out, float *gate_out, void *d_ws, size_t ws_bytes, void *stream) {
-    for (int t0 = 0; t0 < T; t0 += MOE_MAX_DECODE_TOKENS) {
-        const int tc = T - t0 < MOE_MAX_DECODE_TOKENS ? T - t0 : MOE_MAX_DECODE_TOKENS;
-        int rc = run_decode(l, x + (size_t)t0 * l->H, tc, flags, y + (size_t)t0 * l->H,
-                            idx_out ? idx_out + (size_t)t0 * l->topk : nullptr,
-                            gate_out ? gate_out + (size_t)t0 * l->topk : nullptr, d_ws, ws_bytes, stream);
-        if (rc) return rc;
+    Ws ws;
+    int rc = bind_ws(l, T, d_ws, ws_bytes, &ws, true);
+    if (rc) return rc;
+    static thread_local int sms = 0, dev_seen = -1, smem_set = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cuda_status();
+    if (dev != dev_seen) {
+        dev_seen = dev;
+        smem_set = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return cuda_status();
     }
-    return MOE_OK;
+    if (!smem_set) {
+        if (cudaFuncSetAttribute(k_prefill_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)prefill_gemm_smem()) != cudaSuccess)
+            return cuda_status();
+        smem_set = 1;
+    }
+    cudaStream_t st = as_stream(stream);
+    LayerDev ly = layer_dev(l);
+    if ((rc = launch_route(l, ly, x, T, ws, ws.idx, ws.gate, nullptr, st))) return rc;
+    const int P2 = T * l->topk;
+    if (idx_out && cudaMemcpyAsync(idx_out, ws.idx, sizeof(int32_t) * P2, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+        return cuda_status();
+    if (gate_out && cudaMemcpyAsync(gate_out, ws.gate, sizeof(float) * P2, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+        return cuda_status();
+    const int Rmax = prefill_rows(*l, T), T16 = (T + 15) & ~15;
+    PfPlan plan;
+    plan.U = ws.plan;
+    plan.uexp = ws.plan + 2;
+    plan.urow = plan.uexp + MOE_MAX_EXPERTS;
+    plan.ucnt = plan.urow + MOE_MAX_EXPERTS;
+    plan.rowtok = plan.ucnt + MOE_MAX_EXPERTS;
+    plan.rowpair = plan.rowtok + Rmax;
+    k_prefill_plan<<<1, 256, 0, st>>>(ws.idx, T, l->E, l->topk, Rmax, plan);
+    if ((rc = cuda_status())) return rc;
+    const long long gthreads = (long long)(Rmax + T16) * (l->H / kGroup) * 8;
+    k_prefill_gather<<<(unsigned)((gthreads + 255) / 256), 256, 0, st>>>(x, T, l->H, Rmax, T16, plan.rowtok,
+                                                                         plan.U, ws.Br, ws.Bs);
+    if ((rc = cuda_status())) return rc;
+    PrefillGemmArgs g;
+    g.H = l->H; g.I = l->I; g.Is = l->Is; g.T = T; g.T16 = T16; g.Rmax = Rmax;
+    g.U = plan.U; g.uexp = plan.uexp; g.urow = plan.urow; g.ucnt = plan.ucnt; g.rowpair = plan.rowpair;
+    g.experts = (const uint8_t *)l->experts; g.stride = l->expert_stride; g.shared = (const uint8_t *)l->shared;
+    g.Lr = tile_layout(l->H, l->I);
+    g.Ls = tile_layout(l->H, l->Is);
+    g.Br = ws.Br; g.Bs = ws.Bs; g.Hr = ws.Hr; g.Hs = ws.Hs; g.Yr = ws.Yr; g.Ys = ws.Ys;
+    g.err = &ws.ctrl[kErr];
+    for (int kind = 0; kind < 2; kind++) {
+        g.kind = kind;
+        k_prefill_gemm<<<sms, kPfThreads, prefill_gemm_smem(), st>>>(g);
+        if ((rc = cuda_status())) return rc;
+    }
+    const long long cthreads = (long long)T * l->H;
+    k_prefill_combine<<<(unsigned)((cthreads + 255) / 256), 256, 0, st>>>(x, T, l->H, l->topk, flags, ws.gate,
+                                                                         ws.Yr, ws.Ys, y);
+    return cuda_status();
 }
 
 }  // namespace
@@ -572,10 +625,10 @@ int moe_layer_decode_noalloc(const moe_layer_t *layer, const float *x, int T, in
                              int32_t *idx_out, float *gate_out, void *stream) {
     int rc = check_layer_call(layer, x, T, MOE_MAX_DECODE_TOKENS, flags, y);
     if (rc) return rc;
-    if (ws_layout(*layer, T).total > MOE_NOALLOC_SCRATCH_BYTES) {
+    if (ws_layout(*layer, T).decode_total > MOE_NOALLOC_SCRATCH_BYTES) {
         if (getenv("MOE_DEBUG"))
             fprintf(stderr, "libmoe: layer needs %zu bytes of scratch at T=%d, more than %u\n",
-                    ws_layout(*layer, T).total, T, MOE_NOALLOC_SCRATCH_BYTES);
+                    ws_layout(*layer, T).decode_total, T, MOE_NOALLOC_SCRATCH_BYTES);
         return MOE_EWORKSPACE;
     }
     void *ws = nullptr;

@@ -13,65 +13,81 @@ namespace moe {
 
 constexpr int kRouteWarps = 8;  // one router row per warp
 
-// Ranking used by top-k: larger value first, equal values -> lower index.
-__device__ __forceinline__ bool ranks_before(float va, int ia, float vb, int ib) {
-    return va > vb || (va == vb && ia < ib);
+// Order-preserving key of a logit for the top-k: a larger value gives a larger
+// key; -0 and +0 are equal; NaN gets 1, below every number; 0 marks an entry
+// that is out of range or already taken.
+__device__ __forceinline__ unsigned topk_key(float v) {
+    if (v != v) return 1u;
+    if (v == 0.f) v = 0.f;
+    const unsigned u = __float_as_uint(v);
+    const unsigned k = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    return k > 1u ? k : 2u;
 }
 
 // Top-k of one token's E logits by one warp, then softmax over the chosen ones.
-// lrow: the token's logits (read through L2: other CTAs may have written them).
-// Writes idx_dst/gate_dst (any memory) and, when non-null, idx_out/gate_out.
+// Larger logit first, equal logits -> lower expert index.  Each round takes the
+// warp maximum of the keys (__reduce_max_sync) and the lowest index holding it
+// (__reduce_min_sync).  lrow: the token's logits (read through L2: other CTAs
+// may have written them).  Writes idx_dst/gate_dst (any memory) and, when
+// non-null, idx_out/gate_out.
 __device__ void warp_topk_softmax(const float *lrow, int E, int topk, int *idx_dst, float *gate_dst,
                                   int32_t *idx_out, float *gate_out) {
     const int lane = threadIdx.x & 31;
-    float v[MOE_MAX_EXPERTS / 32];
-    unsigned taken = 0;
+    constexpr int NV = MOE_MAX_EXPERTS / 32;
+    unsigned key[NV];
+    float val[NV];
 #pragma unroll
-    for (int i = 0; i < MOE_MAX_EXPERTS / 32; i++) {
-        int e = lane + 32 * i;
-        float x = e < E ? __ldcg(lrow + e) : -INFINITY;
-        v[i] = (x != x) ? -INFINITY : x;  // NaN ranks last
+    for (int i = 0; i < NV; i++) {
+        const int e = lane + 32 * i;
+        val[i] = e < E ? __ldcg(lrow + e) : 0.f;
+        key[i] = e < E ? topk_key(val[i]) : 0u;
     }
     float sel_v[MOE_MAX_TOPK];
     int sel_i[MOE_MAX_TOPK];
-    for (int k = 0; k < topk; k++) {
-        float bv = -INFINITY;
-        int bi = 0x7fffffff;
 #pragma unroll
-        for (int i = 0; i < MOE_MAX_EXPERTS / 32; i++) {
-            int e = lane + 32 * i;
-            if (e < E && !((taken >> i) & 1u) && ranks_before(v[i], e, bv, bi)) {
-                bv = v[i];
-                bi = e;
-            }
-        }
+    for (int k = 0; k < MOE_MAX_TOPK; k++) {
+        sel_v[k] = 0.f;
+        sel_i[k] = 0;
+        if (k < topk) {
+            unsigned best = key[0];
+            int bi = lane;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            if (ranks_before(ov, oi, bv, bi)) {
-                bv = ov;
-                bi = oi;
-            }
+            for (int i = 1; i < NV; i++)
+                if (key[i] > best) {
+                    best = key[i];
+                    bi = lane + 32 * i;
+                }
+            const unsigned m = __reduce_max_sync(0xffffffffu, best);
+            const int win = __reduce_min_sync(0xffffffffu, best == m ? bi : 0x7fffffff);
+            float v = 0.f;
+#pragma unroll
+            for (int i = 0; i < NV; i++)
+                if (win == lane + 32 * i) {
+                    v = val[i];
+                    key[i] = 0u;
+                }
+            sel_v[k] = __shfl_sync(0xffffffffu, v, win & 31);
+            sel_i[k] = win;
         }
-        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-        sel_v[k] = bv;
-        sel_i[k] = bi;
     }
     if (lane == 0) {
-        float m = sel_v[0];
+        const float m = sel_v[0];
         float ex[MOE_MAX_TOPK];
         float z = 0.f;
-        for (int k = 0; k < topk; k++) {
-            ex[k] = expf(sel_v[k] - m);
+#pragma unroll
+        for (int k = 0; k < MOE_MAX_TOPK; k++) {
+            ex[k] = k < topk ? expf(sel_v[k] - m) : 0.f;
             z += ex[k];
         }
-        for (int k = 0; k < topk; k++) {
-            float g = ex[k] / z;
-            idx_dst[k] = sel_i[k];
-            gate_dst[k] = g;
-            if (idx_out) idx_out[k] = sel_i[k];
-            if (gate_out) gate_out[k] = g;
+#pragma unroll
+        for (int k = 0; k < MOE_MAX_TOPK; k++) {
+            if (k < topk) {
+                const float g = ex[k] / z;
+                idx_dst[k] = sel_i[k];
+                gate_dst[k] = g;
+                if (idx_out) idx_out[k] = sel_i[k];
+                if (gate_out) gate_out[k] = g;
+            }
         }
     }
 }

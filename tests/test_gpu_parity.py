@@ -224,7 +224,11 @@ def test_rejects_bad_calls(moe, tiny):
     ws = moe.new_workspace(layer, 4)
     x = torch.zeros((8, s.H), device="cuda")
     with pytest.raises(moe.MoeError) as e:
-        moe.moe_layer_decode(layer, x, ws)  # 8 tokens > workspace T_max 4
+        moe.moe_layer_prefill_chunk(layer, x, ws)  # 8 tokens > workspace T_max 4
+    assert e.value.status == moe.MOE_EWORKSPACE
+    small = torch.zeros(4096, dtype=torch.uint8, device="cuda")
+    with pytest.raises(moe.MoeError) as e:
+        moe.moe_layer_decode(layer, x, small)  # far too small for 8 decode tokens
     assert e.value.status == moe.MOE_EWORKSPACE
     with pytest.raises(moe.MoeError) as e:
         moe.moe_layer_decode(layer, torch.zeros((17, s.H), device="cuda"), moe.new_workspace(layer, 17))
