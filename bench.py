@@ -390,6 +390,30 @@ def stack_measurement(torch, moe, args, n_layers=30, steps=256, slots=16):
     return out
 
 
+def run_prefill_only(args):
+    """The 128-token prefill chunk of one full-size layer with Zipf(1.1) routing,
+    run K times after W warm-ups (a short, single-layer case for profilers)."""
+    import torch
+    import bit_affine_quantised_affine4_b300 as moe
+    s = synth.FULL
+    layer = build_layer(moe, 1, bias=synth.popularity_bias(s, seed=0))
+    view = layer.view()
+    x = torch.from_numpy(synth.tokens(s, 128, seed=0, stream=2000)).cuda()
+    ws = moe.new_workspace(view, 128)
+    for _ in range(args.warmup):
+        moe.moe_layer_prefill_chunk(view, x, ws)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        moe.moe_layer_prefill_chunk(view, x, ws)
+    e1.record()
+    e1.synchronize()
+    us = e0.elapsed_time(e1) * 1000 / args.steps
+    print(json.dumps({"workload": "prefill chunk, 128 tokens, full-size layer, Zipf(1.1)",
+                      "us_per_chunk": us, "tok_s": 128e6 / us, "note": "single layer, weights may sit in L2"}))
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -419,6 +443,8 @@ def main():
     ap.add_argument("--quick", action="store_true", help="headline only, no side measurements")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle timing")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--prefill-only", action="store_true",
+                    help="only the 128-token prefill chunk of one layer (for profilers)")
     ap.add_argument("--stack", action=argparse.BooleanOptionalAction, default=True,
                     help="also run the 30-layer stack decode with per-layer LFU caches")
     ap.add_argument("--copies", type=int, default=0,
@@ -426,7 +452,9 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.impl == "reference":
+    if args.prefill_only:
+        run_prefill_only(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

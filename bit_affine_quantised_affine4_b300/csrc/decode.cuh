@@ -80,7 +80,7 @@ struct DecodeArgs {
     float *pr;     // routed partials [T*topk][H]
     float *ps;     // shared partials [P][T][H]
     // launch
-    int stages, SB, UPS, red_off, hsm_off, hsm_mat_bytes;
+    int stages, SB, UPS, red_off, hsm_off, hsm_mat_bytes, hsum_off;
     int mode;
     const int *idx_pre;      // [T][topk] routing of an earlier router launch (kModePre)
     const float *gate_pre;   // [T][topk]
@@ -105,31 +105,6 @@ __device__ __forceinline__ void affine_acc(float (&acc)[4], const float (&d)[4],
 // the row's 16-byte chunks are swapped pairwise for odd slots, which makes the
 // B-fragment loads of 8 consecutive lanes hit 8 distinct bank groups.
 __host__ __device__ __forceinline__ int h_pos(int k, int j) { return frag_pos(k) ^ ((j & 1) << 3); }
-
-// Partial router logit of row e for token t over the word pairs [p0, p1) of the
-// 8-bit row (pair p holds columns 8p..8p+7), summed over the warp.
-__device__ __forceinline__ float router_partial(const DecodeArgs &a, int e, int t, int p0, int p1) {
-    const int lane = threadIdx.x & 31, G = a.H / kGroup;
-    const uint2 *row = reinterpret_cast<const uint2 *>(a.rq + (size_t)e * (a.H / 4));
-    const float4 *xt = reinterpret_cast<const float4 *>(a.x + (size_t)t * a.H);
-    const __half *sr = a.rs + (size_t)e * G, *br = a.rb + (size_t)e * G;
-    float acc = 0.f;
-#pragma unroll 4
-    for (int p = p0 + lane; p < p1; p += 32) {
-        const uint2 w = __ldg(row + p);
-        const float s = __half2float(sr[p >> 3]), bb = __half2float(br[p >> 3]);
-        const float4 x0 = __ldg(xt + 2 * p), x1 = __ldg(xt + 2 * p + 1);
-        acc = fmaf(fmaf(s, (float)(w.x & 0xFFu), bb), x0.x, acc);
-        acc = fmaf(fmaf(s, (float)((w.x >> 8) & 0xFFu), bb), x0.y, acc);
-        acc = fmaf(fmaf(s, (float)((w.x >> 16) & 0xFFu), bb), x0.z, acc);
-        acc = fmaf(fmaf(s, (float)(w.x >> 24), bb), x0.w, acc);
-        acc = fmaf(fmaf(s, (float)(w.y & 0xFFu), bb), x1.x, acc);
-        acc = fmaf(fmaf(s, (float)((w.y >> 8) & 0xFFu), bb), x1.y, acc);
-        acc = fmaf(fmaf(s, (float)((w.y >> 16) & 0xFFu), bb), x1.z, acc);
-        acc = fmaf(fmaf(s, (float)(w.y >> 24), bb), x1.w, acc);
-    }
-    return warp_sum(acc);
-}
 
 struct DecodeSmem {
     uint64_t full[kMaxStages], empty[kMaxStages], hbar;
@@ -236,7 +211,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
     int rbuf = 0;
     auto gateup_tiles = [&](int n, const int (&s)[2], const int (&u)[2], const int (&it)[2]) {
         float *rw = red + (size_t)rbuf * 2 * kCW * NCH * 128;
-#pragma unroll
+#pragma unroll 1
         for (int j = 0; j < 2; j++) {
             if (j >= n) break;
             float acc[NCH][4];
@@ -303,6 +278,54 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
         }
     };
 
+    // ---- routing helpers (one warp): rank token t from the logits staged in
+    // shared memory; build the schedule from S.idx
+    auto rank_token = [&](int t) {
+        const float *lg = reinterpret_cast<const float *>(hsm);
+        warp_topk_softmax<true>(lg + (size_t)t * a.E, a.E, a.topk, S.idx + t * a.topk, S.gate + t * a.topk,
+                                b == 0 ? a.idx_out + (a.idx_out ? t * a.topk : 0) : nullptr,
+                                b == 0 ? a.gate_out + (a.gate_out ? t * a.topk : 0) : nullptr);
+    };
+    auto build_schedule = [&]() {
+        const int P2 = T * a.topk;
+        for (int e = lane; e < a.E; e += 32) S.mask[e] = 0u;
+        __syncwarp();
+        if (!*err)
+            for (int p = lane; p < P2; p += 32) atomicOr(&S.mask[S.idx[p]], 1u << (p / a.topk));
+        __syncwarp();
+        int ubase = 0, sbase = 0;
+#pragma unroll 1
+        for (int e0 = 0; e0 < a.E; e0 += 32) {
+            const int e = e0 + lane;
+            const unsigned m = e < a.E ? S.mask[e] : 0u;
+            const unsigned bal = __ballot_sync(0xffffffffu, m != 0u);
+            const int rank = __popc(bal & ((1u << lane) - 1u));
+            const int cnt = __popc(m);
+            int incl = cnt;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += v;
+            }
+            if (m) {
+                const int u = ubase + rank;
+                S.uid[e] = (short)u;
+                S.uexp[u] = e;
+                S.ucnt[u] = cnt;
+                S.ubase[u] = sbase + incl - cnt;
+                S.uslot[u] = a.use_map ? a.slot_map[e] : e;
+            }
+            ubase += __popc(bal);
+            sbase += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) S.U = *err ? 0 : ubase;
+        __syncwarp();
+        for (int p = lane; p < P2 && !*err; p += 32) {
+            const int t = p / a.topk, e = S.idx[p];
+            S.pidx[p] = S.ubase[S.uid[e]] + __popc(S.mask[e] & ((1u << t) - 1u));
+        }
+    };
+
     // =========================== phase A ===========================
     if (producer) {
         if (lane == 0) {
@@ -347,6 +370,22 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
             if (!pre && !spin_geq(&a.ctrl[kRouteCnt], (unsigned)a.E, &a.ctrl[kErr])) *err = 1;
         }
         __syncwarp();
+        // while the compute warps finish the shared tiles: the routing (an earlier
+        // launch's choices, or every token's logits) into shared memory
+        if (pre) {
+            for (int p = lane; p < T * a.topk; p += 32) {
+                S.idx[p] = a.idx_pre[p];
+                S.gate[p] = a.gate_pre[p];
+                if (b == 0 && a.idx_out) a.idx_out[p] = S.idx[p];
+                if (b == 0 && a.gate_out) a.gate_out[p] = S.gate[p];
+            }
+        } else if (!*err) {
+            float *lg = reinterpret_cast<float *>(hsm);
+            const int n = T * a.E;
+            for (int i = lane; i < n / 4; i += 32)
+                reinterpret_cast<float4 *>(lg)[i] = __ldcg(reinterpret_cast<const float4 *>(a.logits) + i);
+            for (int i = (n & ~3) + lane; i < n; i += 32) lg[i] = __ldcg(a.logits + i);
+        }
     } else {
         if (!pre) {
             // router rows e = b, b + nC, ...: warp w takes token w / nchk and chunk
@@ -358,7 +397,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
             int j = 0;
             for (int e = b; e < a.E; e += nC, j++) {
                 float v = 0.f;
-                if (t < T) v = router_partial(a, e, t, ck * np / nchk, (ck + 1) * np / nchk);
+                if (t < T) v = router_dot(a.rq, a.rs, a.rb, H, a.x, e, t, ck * np / nchk, (ck + 1) * np / nchk);
                 if (lane == 0) S.rpart[j][warp] = v;
             }
             named_arrive(2, kDecThreads);
@@ -375,61 +414,12 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
         }
     }
     __syncthreads();
-
-    // =========================== routing ===========================
-    if (pre) {
-        for (int p = tid; p < T * a.topk; p += kDecThreads) {
-            S.idx[p] = a.idx_pre[p];
-            S.gate[p] = a.gate_pre[p];
-            if (b == 0 && a.idx_out) a.idx_out[p] = S.idx[p];
-            if (b == 0 && a.gate_out) a.gate_out[p] = S.gate[p];
-        }
-    } else if (!*err) {
-        for (int t = warp; t < T; t += kCW + 1)
-            warp_topk_softmax(a.logits + (size_t)t * a.E, a.E, a.topk, S.idx + t * a.topk,
-                              S.gate + t * a.topk, b == 0 ? a.idx_out + (a.idx_out ? t * a.topk : 0) : nullptr,
-                              b == 0 ? a.gate_out + (a.gate_out ? t * a.topk : 0) : nullptr);
-    }
+    // one warp per token ranks the staged logits, then the producer warp builds
+    // the schedule
+    if (!pre && !*err)
+        for (int t = warp; t < T; t += kCW + 1) rank_token(t);
     __syncthreads();
-    // the schedule, built by warp 0 alone
-    const int P2 = T * a.topk;
-    if (warp == 0) {
-        for (int e = lane; e < a.E; e += 32) S.mask[e] = 0u;
-        __syncwarp();
-        if (!*err)
-            for (int p = lane; p < P2; p += 32) atomicOr(&S.mask[S.idx[p]], 1u << (p / a.topk));
-        __syncwarp();
-        int ubase = 0, sbase = 0;
-        for (int e0 = 0; e0 < a.E; e0 += 32) {
-            const int e = e0 + lane;
-            const unsigned m = e < a.E ? S.mask[e] : 0u;
-            const unsigned bal = __ballot_sync(0xffffffffu, m != 0u);
-            const int rank = __popc(bal & ((1u << lane) - 1u));
-            const int cnt = __popc(m);
-            int incl = cnt;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int v = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += v;
-            }
-            if (m) {
-                const int u = ubase + rank;
-                S.uid[e] = (short)u;
-                S.uexp[u] = e;
-                S.ucnt[u] = cnt;
-                S.ubase[u] = sbase + incl - cnt;
-                S.uslot[u] = a.use_map ? a.slot_map[e] : e;
-            }
-            ubase += __popc(bal);
-            sbase += __shfl_sync(0xffffffffu, incl, 31);
-        }
-        if (lane == 0) S.U = *err ? 0 : ubase;
-        __syncwarp();
-        for (int p = lane; p < P2 && !*err; p += 32) {
-            const int t = p / a.topk, e = S.idx[p];
-            S.pidx[p] = S.ubase[S.uid[e]] + __popc(S.mask[e] & ((1u << t) - 1u));
-        }
-    }
+    if (producer) build_schedule();
     __syncthreads();
 
     const int U = do_routed ? S.U : 0;  // routed experts of this launch
@@ -477,49 +467,48 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
                 }
                 fill++;
             }
-            auto down_fill = [&](int k) {
+            // down units: the first `stages` stages now; h of this CTA's matrices once
+            // every gate/up tile of the layer is done; then the remaining stages
+            const int early = min(nstg, a.stages);
+#pragma unroll 1
+            for (int k = 0; k <= nstg; k++) {
+                if (k == early) {
+                    if (!*err && !spin_geq(&a.ctrl[kGuDone], (unsigned)NGU, &a.ctrl[kErr])) *err = 1;
+                    if (!*err && nunits > 0) {
+                        unsigned bytes = 0;
+#pragma unroll 1
+                        for (int m = m_first; m <= (uhi - 1) / R; m++) {
+                            const bool sh = m < Pe;
+                            const unsigned nb = sh ? (unsigned)(min(Gi, Gs - m * Gi) * T * 128)
+                                                   : (unsigned)(Gi * S.ucnt[m - Pe] * 128);
+                            const __half *src = sh ? a.hs16 + (size_t)m * Gi * T * kGroup
+                                                   : a.h16 + (size_t)S.ubase[m - Pe] * a.I;
+                            bulk_g2s(hsm + (size_t)(m - m_first) * a.hsm_mat_bytes, src, nb, &S.hbar);
+                            bytes += nb;
+                        }
+                        // the arrival (with the byte count) comes after the copies: the
+                        // phase cannot complete before it
+                        mbar_arrive_expect_tx(&S.hbar, bytes);
+                    }
+                }
+                if (k == nstg) break;
                 const int s = producer_slot(fill);
                 if (!*err) {
                     const int u0 = k * a.UPS, u1 = min(nunits, u0 + a.UPS);
                     unsigned bytes = 0;
-                    for (int i = u0; i < u1; i++) {
-                        int ng;
-                        unit_src(ulo + i, &ng);
-                        bytes += kTileBytes * ng;
-                    }
-                    mbar_arrive_expect_tx(&S.full[s], bytes);
+#pragma unroll 1
                     for (int i = u0; i < u1; i++) {
                         int ng;
                         const uint8_t *src = unit_src(ulo + i, &ng);
                         bulk_g2s(ring + (size_t)s * a.SB + (size_t)(i - u0) * Gi * kTileBytes, src,
                                  kTileBytes * ng, &S.full[s]);
+                        bytes += kTileBytes * ng;
                     }
+                    mbar_arrive_expect_tx(&S.full[s], bytes);
                     last_fill[s] = fill;
                 }
                 fill++;
-            };
-            const int early = min(nstg, a.stages);
-            for (int k = 0; k < early; k++) down_fill(k);
-            // h of this CTA's matrices, once every gate/up tile of the layer is done
-            if (!*err && !spin_geq(&a.ctrl[kGuDone], (unsigned)NGU, &a.ctrl[kErr])) *err = 1;
-            if (!*err && nunits > 0) {
-                const int m_last = (uhi - 1) / R;
-                unsigned bytes = 0;
-                for (int m = m_first; m <= m_last; m++)
-                    bytes += m < Pe ? (unsigned)(min(Gi, Gs - m * Gi) * T * 128)
-                                    : (unsigned)(Gi * S.ucnt[m - Pe] * 128);
-                mbar_arrive_expect_tx(&S.hbar, bytes);
-                for (int m = m_first; m <= m_last; m++) {
-                    uint8_t *dst = hsm + (size_t)(m - m_first) * a.hsm_mat_bytes;
-                    if (m < Pe)
-                        bulk_g2s(dst, a.hs16 + (size_t)m * Gi * T * kGroup,
-                                 (unsigned)(min(Gi, Gs - m * Gi) * T * 128), &S.hbar);
-                    else
-                        bulk_g2s(dst, a.h16 + (size_t)S.ubase[m - Pe] * a.I,
-                                 (unsigned)(Gi * S.ucnt[m - Pe] * 128), &S.hbar);
-                }
             }
-            for (int k = early; k < nstg; k++) down_fill(k);
             // drain: every copy this CTA issued has landed before the CTA exits
             volatile int never = 0;
             for (int s = 0; s < a.stages; s++)
@@ -548,6 +537,30 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
             *err = 1;
             atomicExch(&a.ctrl[kErr], 1u);
         }
+        // sum of the (fp16) h values of every group and slot of this CTA's
+        // matrices, once: the bias term b * sum(h) of every unit of the matrix
+        float *hsum = reinterpret_cast<float *>(dsm + a.hsum_off);  // [matrix][Gi][T]
+        if (nunits > 0 && !*err) {
+            const int nm = (uhi - 1) / R - m_first + 1;
+            for (int v = tid; v < nm * Gi * T; v += kCThreads) {
+                const int mi = v / (Gi * T), g = (v / T) % Gi, j = v % T, m = m_first + mi;
+                const int ng = m < Pe ? min(Gi, Gs - m * Gi) : Gi;
+                const int nsl = m < Pe ? T : S.ucnt[m - Pe];
+                float acc = 0.f;
+                if (g < ng && j < nsl) {
+                    const __half2 *hr = reinterpret_cast<const __half2 *>(
+                        hsm + (size_t)mi * a.hsm_mat_bytes + ((size_t)g * nsl + j) * 128);
+#pragma unroll 8
+                    for (int k = 0; k < 32; k++) {
+                        const float2 f = __half22float2(hr[k]);
+                        acc += f.x;
+                        acc += f.y;
+                    }
+                }
+                hsum[v] = acc;
+            }
+        }
+        named_sync(1, kCThreads);
         for (int k = 0; k < nstg; k++) {
             const int s = consumer_wait(fill++);
             for (int i = 0; i < a.UPS; i++) {
@@ -569,12 +582,13 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
                 dstride = H;
                 const uint8_t *wst = ring + (size_t)s * a.SB + (size_t)i * Gi * kTileBytes;
                 const uint8_t *hm = hsm + (size_t)(m - m_first) * a.hsm_mat_bytes;
+                const float *hsg = hsum + (size_t)(m - m_first) * Gi * T;
                 float acc[NCH][4];
 #pragma unroll
                 for (int ch = 0; ch < NCH; ch++)
 #pragma unroll
                     for (int v = 0; v < 4; v++) acc[ch][v] = 0.f;
-#pragma unroll 4
+#pragma unroll 2
                 for (int g = 0; g < ng; g++) {
                     const uint4 q = *reinterpret_cast<const uint4 *>(wst + g * kTileBytes + 16 * lane);
                     const uint2 e = *reinterpret_cast<const uint2 *>(wst + g * kTileBytes + 512 + 8 * gl);
@@ -595,10 +609,12 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
                             } else {
                                 zero_b(hb);
                             }
-                            float d[4] = {0.f, 0.f, 0.f, 0.f}, sm[4] = {0.f, 0.f, 0.f, 0.f};
-                            mma_group_sums(sm, hb);
+                            const int j0 = 8 * ch + 2 * c;
+                            const float s0 = j0 < nsl ? hsg[g * T + j0] : 0.f;
+                            const float s1 = j0 + 1 < nsl ? hsg[g * T + j0 + 1] : 0.f;
+                            float d[4] = {0.f, 0.f, 0.f, 0.f};
                             mma_group_codes(d, make_uint2(q.x, q.y), make_uint2(q.z, q.w), hb);
-                            affine_acc(acc[ch], d, sm[0], sm[1], sa, ba, sb, bb);
+                            affine_acc(acc[ch], d, s0, s1, sa, ba, sb, bb);
                         }
                     }
                 }

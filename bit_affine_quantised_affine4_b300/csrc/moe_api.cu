@@ -96,11 +96,8 @@ int bind_ws(const moe_layer_t *l, int T, void *d_ws, size_t ws_bytes, Ws *out, b
 
 int launch_route(const moe_layer_t *l, const LayerDev &ly, const float *x, int T, Ws ws,
                  int32_t *idx, float *gate, float *logits, cudaStream_t st) {
-    const int grid = (l->E + kRouteWarps - 1) / kRouteWarps;
-    if (T == 1)
-        k_route<1><<<grid, kRouteWarps * 32, 0, st>>>(ly, x, T, ws, idx, gate, logits);
-    else
-        k_route<4><<<grid, kRouteWarps * 32, 0, st>>>(ly, x, T, ws, idx, gate, logits);
+    const dim3 grid(l->E, (T + kRouteTok - 1) / kRouteTok);
+    k_route<<<grid, kRouteTok * 32, 0, st>>>(ly, x, T, ws, idx, gate, logits);
     return cuda_status();
 }
 
@@ -184,16 +181,22 @@ int decode_plan(const moe_layer_t *l, const float *x, int T, int flags, float *y
         st = fa.sharedSizeBytes + 1;  // +1: computed
     }
     const long long budget = (long long)cfg.smem_optin - (long long)(st - 1);
+    // the h region also stages the T x E router logits while the routing is built
+    long long hsm = (long long)hsm_mats * a.hsm_mat_bytes;
+    const long long lg = ((long long)T * l->E * 4 + 127) / 128 * 128;
+    if (hsm < lg) hsm = lg;
+    const long long hsum = ((long long)hsm_mats * Gi * T * 4 + 127) / 128 * 128;  // per-group sums of h
     int stages = kMaxStages;
     long long smem = 0;
     for (; stages >= 2; stages--) {
-        smem = (long long)stages * a.SB + red + (long long)hsm_mats * a.hsm_mat_bytes;
+        smem = (long long)stages * a.SB + red + hsm + hsum;
         if (smem <= budget) break;
     }
     if (stages < 2) return MOE_EINVAL;
     a.stages = stages;
     a.red_off = stages * a.SB;
     a.hsm_off = a.red_off + red;
+    a.hsum_off = (int)(a.hsm_off + hsm);
     if (cfg.attr_smem[nch - 1][gpw - 1] < smem) {
         if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
             return cuda_status();

@@ -19,13 +19,14 @@
 //   combine  (grid)   y_t = sum_k gate_tk * routed_(t,k) + shared_t (+ x_t), in a
 //                     fixed order.
 //
-// Inside a GEMM CTA: warp 4 copies each K step's eight packed weight tiles and the
-// token tile with bulk copies (TMA) into a ring; warps 0-3 dequantise the weights
-// (w = s*q + b, exact, rounded once to fp16) into the swizzled operand layout;
-// one thread of warp 5 issues the MMAs (fp16 x fp16 -> fp32 in tensor memory)
-// and commits them to the stage's barrier; warps 0-3 then read the accumulator
-// out of tensor memory for the epilogue (two accumulators alternate so the next
-// item's MMAs overlap the epilogue).  Columns of both operands are stored in the
+// Inside a GEMM CTA: warp 8 prefetches the next item's weight block into L2 and
+// copies each K step's eight packed weight tiles and the token tile with bulk
+// copies (TMA) into a ring; warps 0-7 dequantise one weight tile each (w = s*q +
+// b, exact, rounded once to fp16) into the swizzled operand layout; one thread of
+// warp 9 issues the MMAs (fp16 x fp16 -> fp32 in tensor memory) and commits them
+// to the stage's barrier; warps 0-7 then read the accumulator out of tensor
+// memory for the epilogue (warps w and w+4 share a lane quarter and split the
+// columns; two accumulators alternate so the next item's MMAs overlap it).  Columns of both operands are stored in the
 // same permuted order within each run of 8 (see mma_core.cuh): a K permutation
 // applied to both operands leaves the product unchanged, and it lets one 32-bit
 // mask extract two codes into an fp16 pair.
@@ -40,7 +41,9 @@
 namespace moe {
 
 constexpr int kPfStages = 4;
-constexpr int kPfThreads = 192;      // warps 0-3 dequant + epilogue, warp 4 copies, warp 5 MMA
+constexpr int kPfDq = 8;             // dequant + epilogue warps (one weight tile each per K step)
+constexpr int kPfProducer = kPfDq, kPfMmaWarp = kPfDq + 1;
+constexpr int kPfThreads = (kPfDq + 2) * 32;
 constexpr int kPfRawA = 5120;        // eight 576-byte tiles, padded to 1024
 constexpr int kPfMaxN = 128;         // token rows of one item (<= MOE_MAX_PREFILL_TOKENS)
 constexpr int kPfRaw = kPfRawA + kPfMaxN * 128;
@@ -265,11 +268,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill_gemm(const PrefillGem
         for (int s = 0; s < kPfStages; s++) {
             mbar_init(&S.raw_full[s], 1);
             mbar_init(&S.stage_free[s], 1);
-            mbar_init(&S.a_full[s], 4);
+            mbar_init(&S.a_full[s], kPfDq);
         }
         for (int j = 0; j < 2; j++) {
             mbar_init(&S.acc_full[j], 1);
-            mbar_init(&S.acc_empty[j], 4);
+            mbar_init(&S.acc_empty[j], kPfDq);
         }
         S.err = 0;
         mbar_fence_init();
@@ -289,7 +292,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill_gemm(const PrefillGem
         atomicExch(a.err, 1u);
     };
 
-    if (warp == 4) {
+    if (warp == kPfProducer) {
         // ---------------- copies
         if (lane == 0) {
             int f = 0;
@@ -297,6 +300,12 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill_gemm(const PrefillGem
             for (int s = 0; s < kPfStages; s++) last[s] = -1;
             for (int i = b; i < NI; i += nC) {
                 const PfItem it = pf_item(a, i);
+                // this item's weight block (first item only) and the next one's, into L2
+                if (i == b) prefetch_l2(it.a, (unsigned)(8 * it.a_row));
+                if (i + nC < NI) {
+                    const PfItem nx = pf_item(a, i + nC);
+                    prefetch_l2(nx.a, (unsigned)(8 * nx.a_row));
+                }
                 for (int kb = 0; kb < it.nkb; kb++, f++) {
                     const int s = f % kPfStages;
                     if (f >= kPfStages && !*err &&
@@ -318,7 +327,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill_gemm(const PrefillGem
                 if (last[s] >= 0) mbar_wait(&S.raw_full[s], (last[s] / kPfStages) & 1, &never);
         }
         __syncwarp();
-    } else if (warp == 5) {
+    } else if (warp == kPfMmaWarp) {
         // ---------------- MMA issue
         if (lane == 0) {
             int f = 0, n_it = 0;
@@ -353,8 +362,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill_gemm(const PrefillGem
         }
         __syncwarp();
     } else {
-        // ---------------- dequantise + epilogue (warps 0-3, 128 threads)
+        // ---------------- dequantise + epilogue (warps 0-7)
         const int r = lane >> 2, c = lane & 3;
+        const int quad = warp & 3, half = warp >> 2;  // tensor-memory lane quarter, column half
         int f = 0, n_it = 0;
         for (int i = b; i < NI; i += nC, n_it++) {
             const PfItem it = pf_item(a, i);
@@ -364,9 +374,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill_gemm(const PrefillGem
                 if (!*err) {
                     const uint8_t *rs = raw + (size_t)s * kPfRaw;
                     uint8_t *as = sA + (size_t)s * kPfTileA;
-#pragma unroll
-                    for (int jj = 0; jj < 2; jj++) {
-                        const int j = 2 * warp + jj;
+                    {
+                        const int j = warp;
                         const uint4 q = *reinterpret_cast<const uint4 *>(rs + j * kTileBytes + 16 * lane);
                         const uint2 e = *reinterpret_cast<const uint2 *>(rs + j * kTileBytes + 512 + 8 * r);
                         const __half2 sa2 = __half2half2(__ushort_as_half((unsigned short)(e.x & 0xFFFFu)));
@@ -389,21 +398,22 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill_gemm(const PrefillGem
             const int ab = n_it & 1;
             if (!*err && !mbar_wait(&S.acc_full[ab], (n_it >> 1) & 1, err)) fail();
             tc_fence_after();
-            const uint32_t trow = tmem + ab * 128 + ((uint32_t)(32 * warp) << 16);
-            const int row = 32 * warp + lane;  // accumulator row of this thread
+            const uint32_t trow = tmem + ab * 128 + ((uint32_t)(32 * quad) << 16);
+            const int row = 32 * quad + lane;  // accumulator row of this thread
+            const int c_first = 16 * half;     // this warp takes every other 16-column chunk
             if (a.kind == 0) {
                 // rows 0-63 gate, 64-127 up (intermediate index 64 mb + row % 64)
-                if (warp >= 2 && !*err)
-                    for (int c0 = 0; c0 < it.N; c0 += 16) {
+                if (quad >= 2 && !*err)
+                    for (int c0 = c_first; c0 < it.N; c0 += 32) {
                         float v[16];
                         tmem_ld16(trow + c0, v);
 #pragma unroll
                         for (int q = 0; q < 16; q++) ebuf[(c0 + q) * 64 + row - 64] = v[q];
                     }
-                named_sync(1, 128);
-                if (warp < 2 && !*err) {
+                named_sync(1, kPfDq * 32);
+                if (quad < 2 && !*err) {
                     const int pos = frag_pos(row);  // operand position of column `row` of the K step
-                    for (int c0 = 0; c0 < it.N; c0 += 16) {
+                    for (int c0 = c_first; c0 < it.N; c0 += 32) {
                         float v[16];
                         tmem_ld16(trow + c0, v);
 #pragma unroll
@@ -415,17 +425,17 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill_gemm(const PrefillGem
                         }
                     }
                 }
-                named_sync(1, 128);
+                named_sync(1, kPfDq * 32);
                 // the item's h rows: one K step (kb = mb) of the down operand
                 uint8_t *dst = (it.u < 0 ? a.Hs + (size_t)it.mb * a.T16 * 128
                                          : a.Hr + ((size_t)it.mb * a.Rmax + a.urow[it.u]) * 128);
                 if (!*err)
-                    for (int v = tid; v < it.N * 8; v += 128)
+                    for (int v = tid; v < it.N * 8; v += kPfDq * 32)
                         reinterpret_cast<uint4 *>(dst)[v] = reinterpret_cast<const uint4 *>(hst)[v];
             } else if (!*err) {
                 // output row 128 mb + row, token column j
                 const int n = 128 * it.mb + row;
-                for (int c0 = 0; c0 < it.N; c0 += 16) {
+                for (int c0 = c_first; c0 < it.N; c0 += 32) {
                     float v[16];
                     tmem_ld16(trow + c0, v);
 #pragma unroll
@@ -441,7 +451,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill_gemm(const PrefillGem
                 }
             }
             tc_fence_before();
-            named_sync(1, 128);
+            named_sync(1, kPfDq * 32);
             if (lane == 0) mbar_arrive(&S.acc_empty[ab]);
         }
     }

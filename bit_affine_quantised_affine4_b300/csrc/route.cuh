@@ -11,7 +11,6 @@
 
 namespace moe {
 
-constexpr int kRouteWarps = 8;  // one router row per warp
 
 // Order-preserving key of a logit for the top-k: a larger value gives a larger
 // key; -0 and +0 are equal; NaN gets 1, below every number; 0 marks an entry
@@ -30,6 +29,8 @@ __device__ __forceinline__ unsigned topk_key(float v) {
 // (__reduce_min_sync).  lrow: the token's logits (read through L2: other CTAs
 // may have written them).  Writes idx_dst/gate_dst (any memory) and, when
 // non-null, idx_out/gate_out.
+// With SMEM set, lrow is in shared memory.
+template <bool SMEM = false>
 __device__ void warp_topk_softmax(const float *lrow, int E, int topk, int *idx_dst, float *gate_dst,
                                   int32_t *idx_out, float *gate_out) {
     const int lane = threadIdx.x & 31;
@@ -39,119 +40,111 @@ __device__ void warp_topk_softmax(const float *lrow, int E, int topk, int *idx_d
 #pragma unroll
     for (int i = 0; i < NV; i++) {
         const int e = lane + 32 * i;
-        val[i] = e < E ? __ldcg(lrow + e) : 0.f;
+        val[i] = e < E ? (SMEM ? lrow[e] : __ldcg(lrow + e)) : 0.f;
         key[i] = e < E ? topk_key(val[i]) : 0u;
     }
+    // rounds are not unrolled (compact code); lane 0 keeps the choices
     float sel_v[MOE_MAX_TOPK];
     int sel_i[MOE_MAX_TOPK];
+#pragma unroll 1
+    for (int k = 0; k < topk; k++) {
+        unsigned best = key[0];
+        int bi = lane;
 #pragma unroll
-    for (int k = 0; k < MOE_MAX_TOPK; k++) {
-        sel_v[k] = 0.f;
-        sel_i[k] = 0;
-        if (k < topk) {
-            unsigned best = key[0];
-            int bi = lane;
+        for (int i = 1; i < NV; i++)
+            if (key[i] > best) {
+                best = key[i];
+                bi = lane + 32 * i;
+            }
+        const unsigned m = __reduce_max_sync(0xffffffffu, best);
+        const int win = __reduce_min_sync(0xffffffffu, best == m ? bi : 0x7fffffff);
+        float v = 0.f;
 #pragma unroll
-            for (int i = 1; i < NV; i++)
-                if (key[i] > best) {
-                    best = key[i];
-                    bi = lane + 32 * i;
-                }
-            const unsigned m = __reduce_max_sync(0xffffffffu, best);
-            const int win = __reduce_min_sync(0xffffffffu, best == m ? bi : 0x7fffffff);
-            float v = 0.f;
-#pragma unroll
-            for (int i = 0; i < NV; i++)
-                if (win == lane + 32 * i) {
-                    v = val[i];
-                    key[i] = 0u;
-                }
-            sel_v[k] = __shfl_sync(0xffffffffu, v, win & 31);
+        for (int i = 0; i < NV; i++)
+            if (win == lane + 32 * i) {
+                v = val[i];
+                key[i] = 0u;
+            }
+        v = __shfl_sync(0xffffffffu, v, win & 31);
+        if (lane == 0) {
+            sel_v[k] = v;
             sel_i[k] = win;
         }
     }
     if (lane == 0) {
         const float m = sel_v[0];
-        float ex[MOE_MAX_TOPK];
         float z = 0.f;
-#pragma unroll
-        for (int k = 0; k < MOE_MAX_TOPK; k++) {
-            ex[k] = k < topk ? expf(sel_v[k] - m) : 0.f;
-            z += ex[k];
-        }
-#pragma unroll
-        for (int k = 0; k < MOE_MAX_TOPK; k++) {
-            if (k < topk) {
-                const float g = ex[k] / z;
-                idx_dst[k] = sel_i[k];
-                gate_dst[k] = g;
-                if (idx_out) idx_out[k] = sel_i[k];
-                if (gate_out) gate_out[k] = g;
-            }
+#pragma unroll 1
+        for (int k = 0; k < topk; k++) z += expf(sel_v[k] - m);
+#pragma unroll 1
+        for (int k = 0; k < topk; k++) {
+            const float g = expf(sel_v[k] - m) / z;
+            idx_dst[k] = sel_i[k];
+            gate_dst[k] = g;
+            if (idx_out) idx_out[k] = sel_i[k];
+            if (gate_out) gate_out[k] = g;
         }
     }
 }
 
-// logits for router rows e (one per warp) for all T tokens; the last CTA to finish
-// runs top-k + softmax for every token.
-template <int TCH>
-__global__ void __launch_bounds__(kRouteWarps * 32)
+// Partial router logit of row e for token t over the word pairs [p0, p1) of the
+// 8-bit row (pair p holds columns 8p..8p+7), summed over the warp.
+__device__ __forceinline__ float router_dot(const uint32_t *rq, const __half *rs, const __half *rb, int H,
+                                            const float *x, int e, int t, int p0, int p1) {
+    const int lane = threadIdx.x & 31, G = H / kGroup;
+    const uint2 *row = reinterpret_cast<const uint2 *>(rq + (size_t)e * (H / 4));
+    const float4 *xt = reinterpret_cast<const float4 *>(x + (size_t)t * H);
+    const __half *sr = rs + (size_t)e * G, *br = rb + (size_t)e * G;
+    float acc = 0.f;
+#pragma unroll 4
+    for (int p = p0 + lane; p < p1; p += 32) {
+        const uint2 w = __ldg(row + p);
+        const float s = __half2float(sr[p >> 3]), bb = __half2float(br[p >> 3]);
+        const float4 x0 = __ldg(xt + 2 * p), x1 = __ldg(xt + 2 * p + 1);
+        acc = fmaf(fmaf(s, (float)(w.x & 0xFFu), bb), x0.x, acc);
+        acc = fmaf(fmaf(s, (float)((w.x >> 8) & 0xFFu), bb), x0.y, acc);
+        acc = fmaf(fmaf(s, (float)((w.x >> 16) & 0xFFu), bb), x0.z, acc);
+        acc = fmaf(fmaf(s, (float)(w.x >> 24), bb), x0.w, acc);
+        acc = fmaf(fmaf(s, (float)(w.y & 0xFFu), bb), x1.x, acc);
+        acc = fmaf(fmaf(s, (float)((w.y >> 8) & 0xFFu), bb), x1.y, acc);
+        acc = fmaf(fmaf(s, (float)((w.y >> 16) & 0xFFu), bb), x1.z, acc);
+        acc = fmaf(fmaf(s, (float)(w.y >> 24), bb), x1.w, acc);
+    }
+    return warp_sum(acc);
+}
+
+constexpr int kRouteTok = 16;  // tokens per router CTA (one warp each)
+
+// CTA (e, g): router row e for tokens 16g..16g+15, one warp per token over the
+// whole row.  The last CTA of token group g (a ticket per group) ranks the group's
+// tokens, one warp per token.
+__global__ void __launch_bounds__(kRouteTok * 32)
 k_route(LayerDev ly, const float *__restrict__ x, int T, Ws ws, int32_t *idx_out, float *gate_out,
         float *logits_out) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int e = blockIdx.x * kRouteWarps + warp;
-    const int wpr = ly.H / 4;
-    const int G = ly.H / kGroup;
-    if (e < ly.E) {
-        const uint32_t *row = ly.rq + (size_t)e * wpr;
-        for (int t0 = 0; t0 < T; t0 += TCH) {
-            float acc[TCH];
-#pragma unroll
-            for (int i = 0; i < TCH; i++) acc[i] = 0.f;
-            for (int w = lane; w < wpr; w += 32) {
-                uint32_t word = __ldg(row + w);
-                int g = w >> 4;
-                float s = __half2float(ly.rs[(size_t)e * G + g]);
-                float b = __half2float(ly.rb[(size_t)e * G + g]);
-                float wv[4];
-#pragma unroll
-                for (int i = 0; i < 4; i++) wv[i] = fmaf(s, (float)((word >> (8 * i)) & 0xFFu), b);
-#pragma unroll
-                for (int tt = 0; tt < TCH; tt++) {
-                    if (t0 + tt < T) {
-                        float4 xv = __ldg((const float4 *)(x + (size_t)(t0 + tt) * ly.H) + w);
-                        acc[tt] = fmaf(wv[0], xv.x, acc[tt]);
-                        acc[tt] = fmaf(wv[1], xv.y, acc[tt]);
-                        acc[tt] = fmaf(wv[2], xv.z, acc[tt]);
-                        acc[tt] = fmaf(wv[3], xv.w, acc[tt]);
-                    }
-                }
-            }
-#pragma unroll
-            for (int tt = 0; tt < TCH; tt++) {
-                float v = warp_sum(acc[tt]);
-                if (lane == 0 && t0 + tt < T) {
-                    if (ly.bias) v += ly.bias[e];
-                    ws.logits[(size_t)(t0 + tt) * ly.E + e] = v;
-                    if (logits_out) logits_out[(size_t)(t0 + tt) * ly.E + e] = v;
-                }
-            }
+    const int e = blockIdx.x, t = blockIdx.y * kRouteTok + warp;
+    if (t < T) {
+        float v = router_dot(ly.rq, ly.rs, ly.rb, ly.H, x, e, t, 0, ly.H / 8);
+        if (lane == 0) {
+            if (ly.bias) v += ly.bias[e];
+            ws.logits[(size_t)t * ly.E + e] = v;
+            if (logits_out) logits_out[(size_t)t * ly.E + e] = v;
         }
     }
     __shared__ int is_last;
     __syncthreads();
     if (threadIdx.x == 0) {
         __threadfence();
-        unsigned tk = atomicAdd(&ws.ctrl[kRouteTicket], 1u);
+        unsigned tk = atomicAdd(&ws.ticket[blockIdx.y], 1u);
         is_last = (tk == gridDim.x - 1);
     }
     __syncthreads();
     if (!is_last) return;
     __threadfence();
-    for (int t = warp; t < T; t += kRouteWarps)
+    if (t < T)
         warp_topk_softmax(ws.logits + (size_t)t * ly.E, ly.E, ly.topk, idx_out + t * ly.topk,
                           gate_out + t * ly.topk, nullptr, nullptr);
-    if (threadIdx.x == 0) ws.ctrl[kRouteTicket] = 0u;
+    if (threadIdx.x == 0) ws.ticket[blockIdx.y] = 0u;
 }
 
 }  // namespace moe
