@@ -88,6 +88,13 @@ struct DecodeArgs {
     short slot_map[MOE_MAX_EXPERTS];
 };
 
+// x / d for x < 2^24 and 1 <= d <= 256: magic = 0xFFFFFFFF / d + 1 (d > 1), exact
+// in that range; d == 1 is passed through.
+__device__ __forceinline__ int udiv_small(int x, int d, unsigned magic) {
+    return d == 1 ? x : (int)__umulhi((unsigned)x, magic);
+}
+__device__ __forceinline__ unsigned udiv_magic(int d) { return d > 1 ? 0xFFFFFFFFu / (unsigned)d + 1u : 0u; }
+
 // fp16 pair (lo, hi) of a 32-bit word -> floats
 __device__ __forceinline__ float lo_half(uint32_t w) { return __half2float(__ushort_as_half((unsigned short)(w & 0xFFFFu))); }
 __device__ __forceinline__ float hi_half(uint32_t w) { return __half2float(__ushort_as_half((unsigned short)(w >> 16))); }
@@ -114,9 +121,10 @@ struct DecodeSmem {
     unsigned mask[MOE_MAX_EXPERTS];
     short uid[MOE_MAX_EXPERTS];
     int uexp[kMaxPairs], ubase[kMaxPairs], ucnt[kMaxPairs], uslot[kMaxPairs];
-    unsigned char last[kMaxUnitsPerCta];
+    short closed[kMaxUnitsPerCta];  // row tiles this CTA closes (tile index r)
     float rpart[kMaxRouterRows][kCW];
-    int U;
+    unsigned wsum[MOE_MAX_EXPERTS / 32];  // schedule: experts << 16 | slots of 32 experts
+    int U, nclosed;
     int err;
 };
 
@@ -246,10 +254,11 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
         }
         named_sync(1, kCThreads);
         // reduce: output o = (tile j, ch, lane L, column i) uses slots i (gate) and
-        // i+2 (up) of the 16 warps' partials
-        const int outs = n * NCH * 64;
-        const int split = kCThreads / outs, wpt = kCW / split;
-        const int o = tid / split, q = tid % split;
+        // i+2 (up) of the 16 warps' partials; 2^sh threads share an output
+        // (n * NCH * 64 outputs, n * NCH in {1, 2, 4})
+        const int sh = 3 - ((n * NCH) >> 1);
+        const int wpt = kCW >> sh;
+        const int o = tid >> sh, q = tid & ((1 << sh) - 1);
         const int j = o / (NCH * 64), ch = (o / 64) % NCH, L = (o % 64) >> 1, i = o & 1;
         float gs = 0.f, us = 0.f;
         for (int w = 0; w < wpt; w++) {
@@ -257,7 +266,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
             gs += p[i];
             us += p[i + 2];
         }
-        for (int off = split / 2; off > 0; off >>= 1) {
+        for (int off = (1 << sh) >> 1; off > 0; off >>= 1) {
             gs += __shfl_xor_sync(0xffffffffu, gs, off);
             us += __shfl_xor_sync(0xffffffffu, us, off);
         }
@@ -286,42 +295,57 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
                                 b == 0 ? a.idx_out + (a.idx_out ? t * a.topk : 0) : nullptr,
                                 b == 0 ? a.gate_out + (a.gate_out ? t * a.topk : 0) : nullptr);
     };
+    // The schedule, by every thread of the CTA (called between barriers): the
+    // distinct experts U in ascending id, the tokens using each (mask), a compact
+    // slot per (token, choice).
+    const unsigned topk_magic = udiv_magic(a.topk);
     auto build_schedule = [&]() {
         const int P2 = T * a.topk;
-        for (int e = lane; e < a.E; e += 32) S.mask[e] = 0u;
-        __syncwarp();
+        for (int e = tid; e < a.E; e += kDecThreads) S.mask[e] = 0u;
+        __syncthreads();
         if (!*err)
-            for (int p = lane; p < P2; p += 32) atomicOr(&S.mask[S.idx[p]], 1u << (p / a.topk));
-        __syncwarp();
-        int ubase = 0, sbase = 0;
-#pragma unroll 1
-        for (int e0 = 0; e0 < a.E; e0 += 32) {
-            const int e = e0 + lane;
-            const unsigned m = e < a.E ? S.mask[e] : 0u;
-            const unsigned bal = __ballot_sync(0xffffffffu, m != 0u);
-            const int rank = __popc(bal & ((1u << lane) - 1u));
-            const int cnt = __popc(m);
-            int incl = cnt;
+            for (int p = tid; p < P2; p += kDecThreads)
+                atomicOr(&S.mask[S.idx[p]], 1u << udiv_small(p, a.topk, topk_magic));
+        __syncthreads();
+        // warp w < nw scans experts 32w..32w+31
+        const int nw = (a.E + 31) >> 5;
+        unsigned m = 0u, bal = 0u;
+        int cnt = 0, incl = 0;
+        if (warp < nw) {
+            const int e = warp * 32 + lane;
+            m = e < a.E ? S.mask[e] : 0u;
+            bal = __ballot_sync(0xffffffffu, m != 0u);
+            cnt = __popc(m);
+            incl = cnt;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const int v = __shfl_up_sync(0xffffffffu, incl, o);
                 if (lane >= o) incl += v;
             }
+            if (lane == 31) S.wsum[warp] = ((unsigned)__popc(bal) << 16) | (unsigned)incl;
+        }
+        __syncthreads();
+        if (warp < nw) {
+            int ub = 0, sb = 0;
+            for (int w = 0; w < warp; w++) {
+                const unsigned v = S.wsum[w];
+                ub += (int)(v >> 16);
+                sb += (int)(v & 0xFFFFu);
+            }
+            const int e = warp * 32 + lane;
             if (m) {
-                const int u = ubase + rank;
+                const int u = ub + __popc(bal & ((1u << lane) - 1u));
                 S.uid[e] = (short)u;
                 S.uexp[u] = e;
                 S.ucnt[u] = cnt;
-                S.ubase[u] = sbase + incl - cnt;
+                S.ubase[u] = sb + incl - cnt;
                 S.uslot[u] = a.use_map ? a.slot_map[e] : e;
             }
-            ubase += __popc(bal);
-            sbase += __shfl_sync(0xffffffffu, incl, 31);
+            if (warp == nw - 1 && lane == 31) S.U = *err ? 0 : ub + __popc(bal);
         }
-        if (lane == 0) S.U = *err ? 0 : ubase;
-        __syncwarp();
-        for (int p = lane; p < P2 && !*err; p += 32) {
-            const int t = p / a.topk, e = S.idx[p];
+        __syncthreads();
+        for (int p = tid; p < P2 && !*err; p += kDecThreads) {
+            const int t = udiv_small(p, a.topk, topk_magic), e = S.idx[p];
             S.pidx[p] = S.ubase[S.uid[e]] + __popc(S.mask[e] & ((1u << t) - 1u));
         }
     };
@@ -385,6 +409,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
             for (int i = lane; i < n / 4; i += 32)
                 reinterpret_cast<float4 *>(lg)[i] = __ldcg(reinterpret_cast<const float4 *>(a.logits) + i);
             for (int i = (n & ~3) + lane; i < n; i += 32) lg[i] = __ldcg(a.logits + i);
+            __syncwarp();
+            rank_token(0);
         }
     } else {
         if (!pre) {
@@ -414,12 +440,14 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
         }
     }
     __syncthreads();
-    // one warp per token ranks the staged logits, then the producer warp builds
-    // the schedule
-    if (!pre && !*err)
-        for (int t = warp; t < T; t += kCW + 1) rank_token(t);
-    __syncthreads();
-    if (producer) build_schedule();
+    // the producer ranked token 0; one warp per token ranks the others, then the
+    // whole CTA builds the schedule
+    if (T > 1) {
+        if (!pre && !*err)
+            for (int t = 1 + warp; t < T; t += kCW + 1) rank_token(t);
+        __syncthreads();
+    }
+    build_schedule();
     __syncthreads();
 
     const int U = do_routed ? S.U : 0;  // routed experts of this launch
@@ -429,8 +457,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
     const int nunits = uhi - ulo;
     const int nstg = (nunits + a.UPS - 1) / a.UPS;
     const int m_first = ulo / R;
-    auto unit_src = [&](int gunit, int *ng) -> const uint8_t * {
-        const int m = gunit / R, r = gunit % R;
+    auto unit_src = [&](int m, int r, int *ng) -> const uint8_t * {
         if (m < Pe) {
             const int g0 = m * Gi;
             *ng = min(Gi, Gs - g0);
@@ -470,6 +497,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
             // down units: the first `stages` stages now; h of this CTA's matrices once
             // every gate/up tile of the layer is done; then the remaining stages
             const int early = min(nstg, a.stages);
+            int um = m_first, ur = ulo - m_first * R;  // (matrix, row tile) of the next unit
 #pragma unroll 1
             for (int k = 0; k <= nstg; k++) {
                 if (k == early) {
@@ -499,7 +527,11 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
 #pragma unroll 1
                     for (int i = u0; i < u1; i++) {
                         int ng;
-                        const uint8_t *src = unit_src(ulo + i, &ng);
+                        const uint8_t *src = unit_src(um, ur, &ng);
+                        if (++ur == R) {
+                            ur = 0;
+                            um++;
+                        }
                         bulk_g2s(ring + (size_t)s * a.SB + (size_t)(i - u0) * Gi * kTileBytes, src,
                                  kTileBytes * ng, &S.full[s]);
                         bytes += kTileBytes * ng;
@@ -561,12 +593,18 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
             }
         }
         named_sync(1, kCThreads);
+        int wm = (ulo + warp) / R, wr = ulo + warp - wm * R;  // this warp's next unit
         for (int k = 0; k < nstg; k++) {
             const int s = consumer_wait(fill++);
             for (int i = 0; i < a.UPS; i++) {
                 const int lu = k * a.UPS + i;
                 if (lu >= nunits || (lu % kCW) != warp || *err) continue;
-                const int gu = ulo + lu, m = gu / R, r = gu % R;
+                const int m = wm, r = wr;
+                wr += kCW;
+                while (wr >= R) {
+                    wr -= R;
+                    wm++;
+                }
                 int ng, nsl;
                 float *dst;
                 size_t dstride;
@@ -637,25 +675,25 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
         __threadfence();
         named_sync(1, kCThreads);
         const unsigned target = (unsigned)(Pe + U);
+        if (tid == 0) S.nclosed = 0;
+        named_sync(1, kCThreads);
         for (int lu = tid; lu < nunits; lu += kCThreads) {
-            unsigned char last = 0;
             if (!*err && do_routed) {
                 const int r = (ulo + lu) % R;
-                last = atomicAdd(&a.ticket[r], 1u) == target - 1u;
-                if (last) {
+                if (atomicAdd(&a.ticket[r], 1u) == target - 1u) {
                     a.ticket[r] = 0u;  // every contribution to this tile is in
                     __threadfence();
+                    S.closed[atomicAdd(&S.nclosed, 1)] = (short)r;
                 }
             }
-            S.last[lu] = last;
         }
         named_sync(1, kCThreads);
-        // all the tiles this CTA closes, combined together
-        for (int v = tid; v < nunits * 16 * T; v += kCThreads) {
-            const int lu = v / (16 * T);
-            if (!S.last[lu]) continue;
-            const int w = v % (16 * T), t = w >> 4;
-            const int n = 16 * ((ulo + lu) % R) + (w & 15);
+        // all the tiles this CTA closes, combined together: element v = (closed
+        // tile c, token t, row n % 16), v >> 4 = c * T + t
+        const unsigned T_magic = udiv_magic(T);
+        for (int v = tid; v < S.nclosed * 16 * T; v += kCThreads) {
+            const int ct = v >> 4, c = udiv_small(ct, T, T_magic), t = ct - c * T;
+            const int n = 16 * S.closed[c] + (v & 15);
             float acc = 0.f;
             for (int k = 0; k < a.topk; k++)
                 acc = fmaf(S.gate[t * a.topk + k], __ldcg(a.pr + (size_t)S.pidx[t * a.topk + k] * H + n), acc);

@@ -24,17 +24,17 @@ __device__ __forceinline__ unsigned topk_key(float v) {
 }
 
 // Top-k of one token's E logits by one warp, then softmax over the chosen ones.
-// Larger logit first, equal logits -> lower expert index.  Each round takes the
-// warp maximum of the keys (__reduce_max_sync) and the lowest index holding it
-// (__reduce_min_sync).  lrow: the token's logits (read through L2: other CTAs
-// may have written them).  Writes idx_dst/gate_dst (any memory) and, when
-// non-null, idx_out/gate_out.
-// With SMEM set, lrow is in shared memory.
-template <bool SMEM = false>
-__device__ void warp_topk_softmax(const float *lrow, int E, int topk, int *idx_dst, float *gate_dst,
-                                  int32_t *idx_out, float *gate_out) {
+// Larger logit first, equal logits -> lower expert index.  Each lane holds NV
+// keys (experts lane, lane + 32, ...); each round takes the warp maximum of the
+// keys (__reduce_max_sync) and the lowest index holding it (__reduce_min_sync),
+// and lane k keeps the k-th choice.  The gates are then computed by lanes
+// 0..topk-1 together.  lrow: the token's logits (read through L2 when SMEM is
+// false: other CTAs may have written them).  Writes idx_dst/gate_dst (any
+// memory) and, when non-null, idx_out/gate_out.
+template <bool SMEM, int NV>
+__device__ void warp_topk_softmax_nv(const float *lrow, int E, int topk, int *idx_dst, float *gate_dst,
+                                     int32_t *idx_out, float *gate_out) {
     const int lane = threadIdx.x & 31;
-    constexpr int NV = MOE_MAX_EXPERTS / 32;
     unsigned key[NV];
     float val[NV];
 #pragma unroll
@@ -43,9 +43,8 @@ __device__ void warp_topk_softmax(const float *lrow, int E, int topk, int *idx_d
         val[i] = e < E ? (SMEM ? lrow[e] : __ldcg(lrow + e)) : 0.f;
         key[i] = e < E ? topk_key(val[i]) : 0u;
     }
-    // rounds are not unrolled (compact code); lane 0 keeps the choices
-    float sel_v[MOE_MAX_TOPK];
-    int sel_i[MOE_MAX_TOPK];
+    float my_v = 0.f;
+    int my_i = 0;
 #pragma unroll 1
     for (int k = 0; k < topk; k++) {
         unsigned best = key[0];
@@ -66,25 +65,31 @@ __device__ void warp_topk_softmax(const float *lrow, int E, int topk, int *idx_d
                 key[i] = 0u;
             }
         v = __shfl_sync(0xffffffffu, v, win & 31);
-        if (lane == 0) {
-            sel_v[k] = v;
-            sel_i[k] = win;
+        if (lane == k) {
+            my_v = v;
+            my_i = win;
         }
     }
-    if (lane == 0) {
-        const float m = sel_v[0];
-        float z = 0.f;
-#pragma unroll 1
-        for (int k = 0; k < topk; k++) z += expf(sel_v[k] - m);
-#pragma unroll 1
-        for (int k = 0; k < topk; k++) {
-            const float g = expf(sel_v[k] - m) / z;
-            idx_dst[k] = sel_i[k];
-            gate_dst[k] = g;
-            if (idx_out) idx_out[k] = sel_i[k];
-            if (gate_out) gate_out[k] = g;
-        }
+    // softmax over the chosen logits (the first is the largest)
+    const float m0 = __shfl_sync(0xffffffffu, my_v, 0);
+    const float ex = lane < topk ? expf(my_v - m0) : 0.f;
+    const float z = warp_sum(ex);
+    if (lane < topk) {
+        const float g = ex / z;
+        idx_dst[lane] = my_i;
+        gate_dst[lane] = g;
+        if (idx_out) idx_out[lane] = my_i;
+        if (gate_out) gate_out[lane] = g;
     }
+}
+
+template <bool SMEM = false>
+__device__ __forceinline__ void warp_topk_softmax(const float *lrow, int E, int topk, int *idx_dst, float *gate_dst,
+                                                  int32_t *idx_out, float *gate_out) {
+    if (E <= 128)
+        warp_topk_softmax_nv<SMEM, 4>(lrow, E, topk, idx_dst, gate_dst, idx_out, gate_out);
+    else
+        warp_topk_softmax_nv<SMEM, MOE_MAX_EXPERTS / 32>(lrow, E, topk, idx_dst, gate_dst, idx_out, gate_out);
 }
 
 // Partial router logit of row e for token t over the word pairs [p0, p1) of the
