@@ -26,8 +26,10 @@
 //            down: units (matrix, 16 output rows) in matrix-major order, a
 //            contiguous range per CTA, one unit per warp with full K; h of the
 //            CTA's matrices is copied to shared memory once every CTA's gate/up
-//            tiles are done.  Each unit writes fp32 partial rows; the last unit to
-//            finish a 16-row tile (a ticket) sums the tile's partials in a fixed
+//            tiles are done.  Each unit writes fp32 partial rows and counts itself
+//            into its 16-row tile's ticket.
+//   combine  CTA b owns the 16-row tiles b, b + nC, ...; once a tile's ticket
+//            shows every contribution, the owner sums the partials in a fixed
 //            order: y = sum_k gate_k * routed_k + sum_parts shared (+ x).
 // All cross-CTA waits are bounded (sync.cuh); results do not depend on timing.
 #pragma once
@@ -80,7 +82,7 @@ struct DecodeArgs {
     float *pr;     // routed partials [T*topk][H]
     float *ps;     // shared partials [P][T][H]
     // launch
-    int stages, SB, UPS, red_off, hsm_off, hsm_mat_bytes, hsum_off;
+    int stages, SB, UPS, red_off, hsm_off, hsm_mat_bytes;
     int mode;
     const int *idx_pre;      // [T][topk] routing of an earlier router launch (kModePre)
     const float *gate_pre;   // [T][topk]
@@ -121,10 +123,9 @@ struct DecodeSmem {
     unsigned mask[MOE_MAX_EXPERTS];
     short uid[MOE_MAX_EXPERTS];
     int uexp[kMaxPairs], ubase[kMaxPairs], ucnt[kMaxPairs], uslot[kMaxPairs];
-    short closed[kMaxUnitsPerCta];  // row tiles this CTA closes (tile index r)
     float rpart[kMaxRouterRows][kCW];
     unsigned wsum[MOE_MAX_EXPERTS / 32];  // schedule: experts << 16 | slots of 32 experts
-    int U, nclosed;
+    int U;
     int err;
 };
 
@@ -569,30 +570,6 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
             *err = 1;
             atomicExch(&a.ctrl[kErr], 1u);
         }
-        // sum of the (fp16) h values of every group and slot of this CTA's
-        // matrices, once: the bias term b * sum(h) of every unit of the matrix
-        float *hsum = reinterpret_cast<float *>(dsm + a.hsum_off);  // [matrix][Gi][T]
-        if (nunits > 0 && !*err) {
-            const int nm = (uhi - 1) / R - m_first + 1;
-            for (int v = tid; v < nm * Gi * T; v += kCThreads) {
-                const int mi = v / (Gi * T), g = (v / T) % Gi, j = v % T, m = m_first + mi;
-                const int ng = m < Pe ? min(Gi, Gs - m * Gi) : Gi;
-                const int nsl = m < Pe ? T : S.ucnt[m - Pe];
-                float acc = 0.f;
-                if (g < ng && j < nsl) {
-                    const __half2 *hr = reinterpret_cast<const __half2 *>(
-                        hsm + (size_t)mi * a.hsm_mat_bytes + ((size_t)g * nsl + j) * 128);
-#pragma unroll 8
-                    for (int k = 0; k < 32; k++) {
-                        const float2 f = __half22float2(hr[k]);
-                        acc += f.x;
-                        acc += f.y;
-                    }
-                }
-                hsum[v] = acc;
-            }
-        }
-        named_sync(1, kCThreads);
         int wm = (ulo + warp) / R, wr = ulo + warp - wm * R;  // this warp's next unit
         for (int k = 0; k < nstg; k++) {
             const int s = consumer_wait(fill++);
@@ -620,7 +597,6 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
                 dstride = H;
                 const uint8_t *wst = ring + (size_t)s * a.SB + (size_t)i * Gi * kTileBytes;
                 const uint8_t *hm = hsm + (size_t)(m - m_first) * a.hsm_mat_bytes;
-                const float *hsg = hsum + (size_t)(m - m_first) * Gi * T;
                 float acc[NCH][4];
 #pragma unroll
                 for (int ch = 0; ch < NCH; ch++)
@@ -647,9 +623,19 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
                             } else {
                                 zero_b(hb);
                             }
-                            const int j0 = 8 * ch + 2 * c;
-                            const float s0 = j0 < nsl ? hsg[g * T + j0] : 0.f;
-                            const float s1 = j0 + 1 < nsl ? hsg[g * T + j0 + 1] : 0.f;
+                            // the group sum of h for slot 8ch + gl (the bias term b * sum h):
+                            // the lane's 16 values, then the 4 lanes of the slot; token
+                            // columns 2c, 2c+1 take it from lanes 8c and 8c + 4
+                            float hs = 0.f;
+#pragma unroll
+                            for (int w = 0; w < 8; w++) {
+                                const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&hb[w]));
+                                hs += f.x + f.y;
+                            }
+                            hs += __shfl_xor_sync(0xffffffffu, hs, 1);
+                            hs += __shfl_xor_sync(0xffffffffu, hs, 2);
+                            const float s0 = __shfl_sync(0xffffffffu, hs, 8 * c);
+                            const float s1 = __shfl_sync(0xffffffffu, hs, 8 * c + 4);
                             float d[4] = {0.f, 0.f, 0.f, 0.f};
                             mma_group_codes(d, make_uint2(q.x, q.y), make_uint2(q.z, q.w), hb);
                             affine_acc(acc[ch], d, s0, s1, sa, ba, sb, bb);
@@ -671,35 +657,34 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
             }
             consumer_release(s);
         }
-        // ---- tickets of the 16-row tiles; the last contributor combines
+        // ---- tickets: this CTA's down units are counted into their 16-row tiles
         __threadfence();
         named_sync(1, kCThreads);
-        const unsigned target = (unsigned)(Pe + U);
-        if (tid == 0) S.nclosed = 0;
-        named_sync(1, kCThreads);
-        for (int lu = tid; lu < nunits; lu += kCThreads) {
-            if (!*err && do_routed) {
-                const int r = (ulo + lu) % R;
-                if (atomicAdd(&a.ticket[r], 1u) == target - 1u) {
-                    a.ticket[r] = 0u;  // every contribution to this tile is in
-                    __threadfence();
-                    S.closed[atomicAdd(&S.nclosed, 1)] = (short)r;
+        if (do_routed && !*err)
+            for (int lu = tid; lu < nunits; lu += kCThreads) atomicAdd(&a.ticket[(ulo + lu) % R], 1u);
+        // ---- combine the tiles this CTA owns (r = b, b + nC, ...) once every
+        // contribution to them is in: y = sum_k gate_k * routed_k + sum_parts shared (+ x)
+        if (do_routed) {
+            const unsigned target = (unsigned)(Pe + U);
+            if (tid == 0)
+                for (int r = b; r < R && !*err; r += nC) {
+                    if (!spin_geq(&a.ticket[r], target, &a.ctrl[kErr])) *err = 1;
+                    a.ticket[r] = 0u;  // every contribution is in: ready for the next call
                 }
+            named_sync(1, kCThreads);
+            const int nown = b < R ? (R - 1 - b) / nC + 1 : 0;
+            const unsigned T_magic = udiv_magic(T);
+            // element v = (owned tile c, token t, row n % 16), v >> 4 = c * T + t
+            for (int v = tid; v < nown * 16 * T && !*err; v += kCThreads) {
+                const int ct = v >> 4, c = udiv_small(ct, T, T_magic), t = ct - c * T;
+                const int n = 16 * (b + c * nC) + (v & 15);
+                float acc = 0.f;
+                for (int k = 0; k < a.topk; k++)
+                    acc = fmaf(S.gate[t * a.topk + k], __ldcg(a.pr + (size_t)S.pidx[t * a.topk + k] * H + n), acc);
+                for (int p = 0; p < a.P; p++) acc += __ldcg(a.ps + ((size_t)p * T + t) * H + n);
+                if (a.flags & MOE_RESIDUAL) acc += __ldg(a.x + (size_t)t * H + n);
+                a.y[(size_t)t * H + n] = acc;
             }
-        }
-        named_sync(1, kCThreads);
-        // all the tiles this CTA closes, combined together: element v = (closed
-        // tile c, token t, row n % 16), v >> 4 = c * T + t
-        const unsigned T_magic = udiv_magic(T);
-        for (int v = tid; v < S.nclosed * 16 * T; v += kCThreads) {
-            const int ct = v >> 4, c = udiv_small(ct, T, T_magic), t = ct - c * T;
-            const int n = 16 * S.closed[c] + (v & 15);
-            float acc = 0.f;
-            for (int k = 0; k < a.topk; k++)
-                acc = fmaf(S.gate[t * a.topk + k], __ldcg(a.pr + (size_t)S.pidx[t * a.topk + k] * H + n), acc);
-            for (int p = 0; p < a.P; p++) acc += __ldcg(a.ps + ((size_t)p * T + t) * H + n);
-            if (a.flags & MOE_RESIDUAL) acc += __ldg(a.x + (size_t)t * H + n);
-            a.y[(size_t)t * H + n] = acc;
         }
     }
 

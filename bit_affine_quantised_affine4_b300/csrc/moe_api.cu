@@ -185,18 +185,16 @@ int decode_plan(const moe_layer_t *l, const float *x, int T, int flags, float *y
     long long hsm = (long long)hsm_mats * a.hsm_mat_bytes;
     const long long lg = ((long long)T * l->E * 4 + 127) / 128 * 128;
     if (hsm < lg) hsm = lg;
-    const long long hsum = ((long long)hsm_mats * Gi * T * 4 + 127) / 128 * 128;  // per-group sums of h
     int stages = kMaxStages;
     long long smem = 0;
     for (; stages >= 2; stages--) {
-        smem = (long long)stages * a.SB + red + hsm + hsum;
+        smem = (long long)stages * a.SB + red + hsm;
         if (smem <= budget) break;
     }
     if (stages < 2) return MOE_EINVAL;
     a.stages = stages;
     a.red_off = stages * a.SB;
     a.hsm_off = a.red_off + red;
-    a.hsum_off = (int)(a.hsm_off + hsm);
     if (cfg.attr_smem[nch - 1][gpw - 1] < smem) {
         if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
             return cuda_status();
