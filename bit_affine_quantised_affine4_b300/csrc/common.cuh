@@ -64,9 +64,10 @@ struct LayerDev {
 enum CtrlWord {
     kErr = 0,         // a bounded wait gave up (sticky until moe_workspace_status)
     kRouteTicket,     // standalone router: CTAs finished (the last one runs top-k)
-    kRouteCnt,        // decode: router rows published
-    kGuDone,          // decode: gate/up tiles finished
-    kExit,            // decode: CTAs finished (the last one resets the words above)
+    kRouteCnt,        // decode: router rows published (cumulative over calls)
+    kGuDone,          // decode: gate/up tiles finished (cumulative over calls)
+    kRouteBase,       // decode: kRouteCnt at the start of the next call (8-byte aligned pair
+    kGuBase,          //   with kGuBase, the same for kGuDone); written by CTA 0 at its end
     kCtrlWords = 16
 };
 

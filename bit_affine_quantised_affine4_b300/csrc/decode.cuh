@@ -351,9 +351,14 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
         }
     };
 
+    // the counters' values at the start of this call (cumulative counters: no
+    // reset between calls)
+    uint2 base = make_uint2(0u, 0u);
     // =========================== phase A ===========================
     if (producer) {
         if (lane == 0) {
+            base = __ldcg(reinterpret_cast<const uint2 *>(a.ctrl + kRouteBase));
+            if (base.x == 0xFFFFFFFFu && base.y == 0xFFFFFFFFu) __nanosleep(0);  // the load has landed
             // this CTA's shared gate/up tiles, and a slice of the shared down matrix into L2
             for (int k = 0; k < n_shared_mine && k < a.stages; k++) {
                 const int s = producer_slot(fill);
@@ -392,7 +397,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
                 }
                 fill++;
             }
-            if (!pre && !spin_geq(&a.ctrl[kRouteCnt], (unsigned)a.E, &a.ctrl[kErr])) *err = 1;
+            if (!pre && !spin_reach(&a.ctrl[kRouteCnt], base.x, (unsigned)a.E, &a.ctrl[kErr])) *err = 1;
         }
         __syncwarp();
         // while the compute warps finish the shared tiles: the routing (an earlier
@@ -502,7 +507,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
 #pragma unroll 1
             for (int k = 0; k <= nstg; k++) {
                 if (k == early) {
-                    if (!*err && !spin_geq(&a.ctrl[kGuDone], (unsigned)NGU, &a.ctrl[kErr])) *err = 1;
+                    if (!*err && !spin_reach(&a.ctrl[kGuDone], base.y, (unsigned)NGU, &a.ctrl[kErr])) *err = 1;
                     if (!*err && nunits > 0) {
                         unsigned bytes = 0;
 #pragma unroll 1
@@ -547,6 +552,12 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
             for (int s = 0; s < a.stages; s++)
                 if (last_fill[s] >= 0) mbar_wait(&S.full[s], (last_fill[s] / a.stages) & 1, &never);
             if (nunits > 0) mbar_wait(&S.hbar, 0, &never);
+            // every CTA has read the bases (all gate/up tiles are counted): the next
+            // call's bases
+            if (b == 0) {
+                a.ctrl[kRouteBase] = base.x + (pre ? 0u : (unsigned)a.E);
+                a.ctrl[kGuBase] = base.y + (unsigned)NGU;
+            }
         }
         __syncwarp();
     } else {
@@ -666,39 +677,39 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
         // contribution to them is in: y = sum_k gate_k * routed_k + sum_parts shared (+ x)
         if (do_routed) {
             const unsigned target = (unsigned)(Pe + U);
-            if (tid == 0)
-                for (int r = b; r < R && !*err; r += nC) {
-                    if (!spin_geq(&a.ticket[r], target, &a.ctrl[kErr])) *err = 1;
-                    a.ticket[r] = 0u;  // every contribution is in: ready for the next call
-                }
-            named_sync(1, kCThreads);
             const int nown = b < R ? (R - 1 - b) / nC + 1 : 0;
+            for (int c = tid; c < nown && !*err; c += kCThreads) {
+                const int r = b + c * nC;
+                if (!spin_geq(&a.ticket[r], target, &a.ctrl[kErr])) *err = 1;
+                a.ticket[r] = 0u;  // every contribution is in: ready for the next call
+            }
+            named_sync(1, kCThreads);
             const unsigned T_magic = udiv_magic(T);
             // element v = (owned tile c, token t, row n % 16), v >> 4 = c * T + t
             for (int v = tid; v < nown * 16 * T && !*err; v += kCThreads) {
                 const int ct = v >> 4, c = udiv_small(ct, T, T_magic), t = ct - c * T;
                 const int n = 16 * (b + c * nC) + (v & 15);
+                float pv[MOE_MAX_TOPK];
+#pragma unroll
+                for (int k = 0; k < MOE_MAX_TOPK; k++)
+                    pv[k] = k < a.topk ? __ldcg(a.pr + (size_t)S.pidx[t * a.topk + k] * H + n) : 0.f;
                 float acc = 0.f;
-                for (int k = 0; k < a.topk; k++)
-                    acc = fmaf(S.gate[t * a.topk + k], __ldcg(a.pr + (size_t)S.pidx[t * a.topk + k] * H + n), acc);
-                for (int p = 0; p < a.P; p++) acc += __ldcg(a.ps + ((size_t)p * T + t) * H + n);
+#pragma unroll
+                for (int k = 0; k < MOE_MAX_TOPK; k++)
+                    if (k < a.topk) acc = fmaf(S.gate[t * a.topk + k], pv[k], acc);
+                for (int p0 = 0; p0 < a.P; p0 += 4) {
+                    float sv[4];
+#pragma unroll
+                    for (int q = 0; q < 4; q++) sv[q] = p0 + q < a.P ? __ldcg(a.ps + ((size_t)(p0 + q) * T + t) * H + n) : 0.f;
+#pragma unroll
+                    for (int q = 0; q < 4; q++) acc += sv[q];
+                }
                 if (a.flags & MOE_RESIDUAL) acc += __ldg(a.x + (size_t)t * H + n);
                 a.y[(size_t)t * H + n] = acc;
             }
         }
     }
 
-    // ---- leave; the last CTA resets the control words for the next call
-    __syncthreads();
-    if (tid == 0) {
-        __threadfence();
-        if (atomicAdd(&a.ctrl[kExit], 1u) == (unsigned)nC - 1u) {
-            a.ctrl[kRouteCnt] = 0u;
-            a.ctrl[kGuDone] = 0u;
-            __threadfence();
-            a.ctrl[kExit] = 0u;
-        }
-    }
 }
 
 }  // namespace moe

@@ -99,6 +99,22 @@ __device__ __forceinline__ bool spin_geq(const unsigned *p, unsigned target, uns
     }
 }
 
+// One thread waits until the cumulative counter *p has advanced by `delta`
+// past `base` (modulo 2^32; bounded, no sleep); on expiry it raises *err.
+// Returns false on expiry or when another CTA already raised *err.
+__device__ __forceinline__ bool spin_reach(const unsigned *p, unsigned base, unsigned delta, unsigned *err) {
+    if (ld_acquire_gpu(p) - base >= delta) return true;
+    const unsigned long long t0 = global_ns();
+    while (true) {
+        if (ld_acquire_gpu(p) - base >= delta) return true;
+        if (*(volatile unsigned *)err) return false;
+        if (global_ns() - t0 > kWaitNs) {
+            atomicExch(err, 1u);
+            return false;
+        }
+    }
+}
+
 // Named barrier over `threads` threads (a multiple of 32).
 __device__ __forceinline__ void named_sync(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
