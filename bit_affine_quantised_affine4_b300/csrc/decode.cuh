@@ -146,6 +146,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
     uint8_t *hsm = dsm + a.hsm_off;
     volatile int *err = &S.err;
 
+    // the next decode kernel on the stream may start on SMs this one leaves; it
+    // waits for this one (pdl_wait) before it touches the workspace or x
+    pdl_launch_dependents();
     if (tid == 0) {
         for (int s = 0; s < a.stages; s++) {
             mbar_init(&S.full[s], 1);
@@ -357,9 +360,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
     // =========================== phase A ===========================
     if (producer) {
         if (lane == 0) {
-            base = __ldcg(reinterpret_cast<const uint2 *>(a.ctrl + kRouteBase));
-            if (base.x == 0xFFFFFFFFu && base.y == 0xFFFFFFFFu) __nanosleep(0);  // the load has landed
-            // this CTA's shared gate/up tiles, and a slice of the shared down matrix into L2
+            // this CTA's shared gate/up tiles, and a slice of the shared down matrix into
+            // L2 (weights only: this may run before the previous kernel has finished)
             for (int k = 0; k < n_shared_mine && k < a.stages; k++) {
                 const int s = producer_slot(fill);
                 mbar_arrive_expect_tx(&S.full[s], gu_bytes);
@@ -368,6 +370,12 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
             }
             for (int r = b; r < R && do_shared; r += nC)
                 prefetch_l2(a.shared + a.Ls.gu_bytes + (size_t)kTileBytes * Gs * r, kTileBytes * Gs);
+        }
+        __syncwarp();
+        pdl_wait();
+        if (lane == 0) {
+            base = __ldcg(reinterpret_cast<const uint2 *>(a.ctrl + kRouteBase));
+            if (base.x == 0xFFFFFFFFu && base.y == 0xFFFFFFFFu) __nanosleep(0);  // the load has landed
         }
         if (!pre) {
             // this CTA's router logits from the compute warps' partial sums
@@ -422,10 +430,23 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
         if (!pre) {
             // router rows e = b, b + nC, ...: warp w takes token w / nchk and chunk
             // w % nchk of the row, so every lane issues its few loads at once; the
-            // producer warp adds the partial sums up and publishes the logits
+            // producer warp adds the partial sums up and publishes the logits.  The
+            // chunk's weight lines are prefetched into L2 before the wait for the
+            // previous kernel.
             const int nchk = T >= kCW ? 1 : kCW / T;
             const int np = H / 8;  // 8-code word pairs per row
             const int t = warp / nchk, ck = warp % nchk;
+            if (t < T)
+                for (int e = b; e < a.E; e += nC) {
+                    const uint8_t *row = reinterpret_cast<const uint8_t *>(a.rq) + (size_t)e * H;
+                    const int l0 = (8 * (ck * np / nchk)) >> 7, l1 = (8 * ((ck + 1) * np / nchk) + 127) >> 7;
+                    if (l0 + lane < l1) prefetch_line_l2(row + (size_t)(l0 + lane) * 128);
+                    if (lane == 31 && ck == 0) {
+                        prefetch_line_l2(a.rs + (size_t)e * (H / kGroup));
+                        prefetch_line_l2(a.rb + (size_t)e * (H / kGroup));
+                    }
+                }
+            pdl_wait();
             int j = 0;
             for (int e = b; e < a.E; e += nC, j++) {
                 float v = 0.f;
@@ -433,6 +454,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
                 if (lane == 0) S.rpart[j][warp] = v;
             }
             named_arrive(2, kDecThreads);
+        } else {
+            pdl_wait();
         }
         load_x();
         for (int k = 0; k < n_shared_mine; k += 2) {

@@ -207,10 +207,35 @@ int decode_plan(const moe_layer_t *l, const float *x, int T, int flags, float *y
 }
 
 // One CTA per SM, launched cooperatively so that every CTA is resident and the
-// cross-CTA waits can always complete.
+// cross-CTA waits can always complete.  The launch also allows programmatic
+// dependent launch: when the previous operation on the stream is a decode
+// kernel, this one may start on the SMs it leaves while it finishes, and runs
+// its prologue (barrier set-up, weight copies and prefetches) before waiting
+// for it (griddepcontrol.wait).  If the runtime refuses the combination, the
+// plain cooperative launch is used from then on.
 int decode_launch(DecodePlan &plan, int mode, void *stream) {
+    static int pdl_ok = 1;
     plan.a.mode = mode;
     void *args[] = {&plan.a};
+    if (pdl_ok) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(plan.nC);
+        cfg.blockDim = dim3(kDecThreads);
+        cfg.dynamicSmemBytes = (size_t)plan.smem;
+        cfg.stream = as_stream(stream);
+        cudaLaunchAttribute attr[2];
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 2;
+        const cudaError_t e = cudaLaunchKernelExC(&cfg, plan.fn, args);
+        if (e == cudaSuccess) return MOE_OK;
+        if (e != cudaErrorInvalidValue && e != cudaErrorNotSupported) return cuda_status();
+        (void)cudaGetLastError();
+        pdl_ok = 0;
+    }
     if (cudaLaunchCooperativeKernel(plan.fn, dim3(plan.nC), dim3(kDecThreads), args, (size_t)plan.smem,
                                     as_stream(stream)) != cudaSuccess)
         return cuda_status();

@@ -115,6 +115,17 @@ __device__ __forceinline__ bool spin_reach(const unsigned *p, unsigned base, uns
     }
 }
 
+// Programmatic dependent launch: let the next kernel on the stream start early;
+// wait until the previous one has completed and its memory is visible (both are
+// no-ops when the launch did not ask for it).
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Prefetch of the 128-byte line holding p into L2.
+__device__ __forceinline__ void prefetch_line_l2(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // Named barrier over `threads` threads (a multiple of 32).
 __device__ __forceinline__ void named_sync(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
