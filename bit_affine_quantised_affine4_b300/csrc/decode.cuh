@@ -42,7 +42,9 @@
 
 namespace moe {
 
-constexpr int kCW = 16;                       // compute warps
+// 15 compute warps + the producer warp: 16 warps, 4 per SM sub-partition, so a
+// thread may hold up to 128 registers
+constexpr int kCW = 15;                       // compute warps
 constexpr int kCThreads = kCW * 32;           // compute threads
 constexpr int kDecThreads = kCThreads + 32;   // + producer warp
 constexpr int kMaxStages = 4;
@@ -123,8 +125,9 @@ struct DecodeSmem {
     unsigned mask[MOE_MAX_EXPERTS];
     short uid[MOE_MAX_EXPERTS];
     int uexp[kMaxPairs], ubase[kMaxPairs], ucnt[kMaxPairs], uslot[kMaxPairs];
-    float rpart[kMaxRouterRows][kCW];
+    float rpart[kMaxRouterRows][kCW > MOE_MAX_DECODE_TOKENS ? kCW : MOE_MAX_DECODE_TOKENS];
     unsigned wsum[MOE_MAX_EXPERTS / 32];  // schedule: experts << 16 | slots of 32 experts
+    unsigned tcnt[kMaxStages + 1];         // gate/up partial-sum slots: warps arrived
     int U;
     int err;
 };
@@ -155,6 +158,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
             mbar_init(&S.empty[s], kCW);
         }
         mbar_init(&S.hbar, 1);
+        for (int i = 0; i <= kMaxStages; i++) S.tcnt[i] = 0u;
         S.err = 0;
         mbar_fence_init();
     }
@@ -216,79 +220,88 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
             }
     };
 
-    // One or two gate/up tiles by the compute warps: K split over warps, partial
-    // sums meet in shared memory (one barrier per pair of tiles), GeGLU, fp16 store
-    // of h.  Tile j of the pair sits in ring stage s[j]; u[j] < 0 marks the shared
-    // expert, it[j] is the tile's row block.
-    int rbuf = 0;
-    auto gateup_tiles = [&](int n, const int (&s)[2], const int (&u)[2], const int (&it)[2]) {
-        float *rw = red + (size_t)rbuf * 2 * kCW * NCH * 128;
-#pragma unroll 1
-        for (int j = 0; j < 2; j++) {
-            if (j >= n) break;
-            float acc[NCH][4];
+    // One gate/up tile by the compute warps: each warp takes its K slice and puts
+    // its partial sums in one of stages + 1 slots of shared memory; the last warp
+    // to arrive (a counter per slot) adds the 16 partials up in warp order, applies
+    // GeGLU and stores h in fp16, while the others go on to their next tile.  A
+    // slot is not reused too early: a warp reaches tile k + stages + 1 only after
+    // every warp has released tile k + 1's stage, which the reducer of tile k does
+    // after its reduction.  u < 0 marks the shared expert, it is the tile's row block.
+    int slot = 0;
+    const int nslot = a.stages + 1;
+    auto gateup_tile = [&](int s, int u, int it) {
+        float acc[NCH][4];
 #pragma unroll
-            for (int ch = 0; ch < NCH; ch++)
+        for (int ch = 0; ch < NCH; ch++)
 #pragma unroll
-                for (int i = 0; i < 4; i++) acc[ch][i] = 0.f;
-            if (!*err) {
-                const uint8_t *st = ring + (size_t)s[j] * a.SB;
+            for (int i = 0; i < 4; i++) acc[ch][i] = 0.f;
+        if (!*err) {
+            const uint8_t *st = ring + (size_t)s * a.SB;
 #pragma unroll
-                for (int gi = 0; gi < GPW; gi++) {
-                    const int g = g0w + gi;
-                    if (g < g1w) {
-                        const uint4 q = *reinterpret_cast<const uint4 *>(st + g * kTileBytes + 16 * lane);
-                        const uint2 e = *reinterpret_cast<const uint2 *>(st + g * kTileBytes + 512 + 8 * gl);
-                        const float sa = lo_half(e.x) * kTwo24, ba = hi_half(e.x);
-                        const float sb = lo_half(e.y) * kTwo24, bb = hi_half(e.y);
+            for (int gi = 0; gi < GPW; gi++) {
+                const int g = g0w + gi;
+                if (g < g1w) {
+                    const uint4 q = *reinterpret_cast<const uint4 *>(st + g * kTileBytes + 16 * lane);
+                    const uint2 e = *reinterpret_cast<const uint2 *>(st + g * kTileBytes + 512 + 8 * gl);
+                    const float sa = lo_half(e.x) * kTwo24, ba = hi_half(e.x);
+                    const float sb = lo_half(e.y) * kTwo24, bb = hi_half(e.y);
 #pragma unroll
-                        for (int ch = 0; ch < NCH; ch++) {
-                            float d[4] = {0.f, 0.f, 0.f, 0.f};
-                            mma_group_codes(d, make_uint2(q.x, q.y), make_uint2(q.z, q.w), xb[gi][ch]);
-                            affine_acc(acc[ch], d, xs[gi][ch][0], xs[gi][ch][1], sa, ba, sb, bb);
-                        }
+                    for (int ch = 0; ch < NCH; ch++) {
+                        float d[4] = {0.f, 0.f, 0.f, 0.f};
+                        mma_group_codes(d, make_uint2(q.x, q.y), make_uint2(q.z, q.w), xb[gi][ch]);
+                        affine_acc(acc[ch], d, xs[gi][ch][0], xs[gi][ch][1], sa, ba, sb, bb);
                     }
                 }
             }
-            consumer_release(s[j]);
+        }
+        consumer_release(s);
+        float *rw = red + (size_t)slot * kCW * NCH * 128;
+        unsigned *cnt = &S.tcnt[slot];
+        if (++slot == nslot) slot = 0;
 #pragma unroll
-            for (int ch = 0; ch < NCH; ch++)
-                reinterpret_cast<float4 *>(rw + (size_t)((j * kCW + warp) * NCH + ch) * 128)[lane] =
-                    make_float4(acc[ch][0], acc[ch][1], acc[ch][2], acc[ch][3]);
+        for (int ch = 0; ch < NCH; ch++)
+            reinterpret_cast<float4 *>(rw + (size_t)(warp * NCH + ch) * 128)[lane] =
+                make_float4(acc[ch][0], acc[ch][1], acc[ch][2], acc[ch][3]);
+        __syncwarp();
+        unsigned last = 0;
+        if (lane == 0) {
+            __threadfence_block();
+            last = atomicAdd(cnt, 1u) == (unsigned)(kCW - 1);
         }
-        named_sync(1, kCThreads);
-        // reduce: output o = (tile j, ch, lane L, column i) uses slots i (gate) and
-        // i+2 (up) of the 16 warps' partials; 2^sh threads share an output
-        // (n * NCH * 64 outputs, n * NCH in {1, 2, 4})
-        const int sh = 3 - ((n * NCH) >> 1);
-        const int wpt = kCW >> sh;
-        const int o = tid >> sh, q = tid & ((1 << sh) - 1);
-        const int j = o / (NCH * 64), ch = (o / 64) % NCH, L = (o % 64) >> 1, i = o & 1;
-        float gs = 0.f, us = 0.f;
-        for (int w = 0; w < wpt; w++) {
-            const float *p = rw + (size_t)((j * kCW + q * wpt + w) * NCH + ch) * 128 + L * 4;
-            gs += p[i];
-            us += p[i + 2];
-        }
-        for (int off = (1 << sh) >> 1; off > 0; off >>= 1) {
-            gs += __shfl_xor_sync(0xffffffffu, gs, off);
-            us += __shfl_xor_sync(0xffffffffu, us, off);
-        }
-        rbuf ^= 1;
-        if (q != 0 || *err) return;
-        const int row = 8 * it[j] + (L >> 2), t = 8 * ch + 2 * (L & 3) + i;
-        if (t >= T) return;
-        const __half hv = __float2half_rn(gelu_tanh(gs) * us);
-        const int g = row / kGroup, k = row % kGroup;
-        if (u[j] < 0) {
-            a.hs16[((size_t)g * T + t) * kGroup + h_pos(k, t)] = hv;
-        } else {
-            const unsigned m = S.mask[S.uexp[u[j]]];
-            if ((m >> t) & 1u) {
-                const int slot = __popc(m & ((1u << t) - 1u)), nu = S.ucnt[u[j]];
-                a.h16[(size_t)S.ubase[u[j]] * a.I + ((size_t)g * nu + slot) * kGroup + h_pos(k, slot)] = hv;
+        if (!__shfl_sync(0xffffffffu, last, 0)) return;
+        __threadfence_block();
+        // lane L holds rows (L / 4, L / 4 + 8) = (gate, up) of row block it, token
+        // columns 2(L % 4), 2(L % 4) + 1 of each chunk
+        const int row = 8 * it + gl, g = row / kGroup, k = row % kGroup;
+#pragma unroll
+        for (int ch = 0; ch < NCH; ch++) {
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+            for (int w = 0; w < kCW; w++) {
+                const float4 p = reinterpret_cast<const float4 *>(rw + (size_t)(w * NCH + ch) * 128)[lane];
+                v.x += p.x;
+                v.y += p.y;
+                v.z += p.z;
+                v.w += p.w;
+            }
+#pragma unroll
+            for (int i = 0; i < 2; i++) {
+                const int t = 8 * ch + 2 * c + i;
+                if (t >= T || *err) continue;
+                const __half hv = __float2half_rn(gelu_tanh(i ? v.y : v.x) * (i ? v.w : v.z));
+                if (u < 0) {
+                    a.hs16[((size_t)g * T + t) * kGroup + h_pos(k, t)] = hv;
+                } else {
+                    const unsigned m = S.mask[S.uexp[u]];
+                    if ((m >> t) & 1u) {
+                        const int sl = __popc(m & ((1u << t) - 1u)), nu = S.ucnt[u];
+                        a.h16[(size_t)S.ubase[u] * a.I + ((size_t)g * nu + sl) * kGroup + h_pos(k, sl)] = hv;
+                    }
+                }
             }
         }
+        __syncwarp();
+        if (lane == 0) *cnt = 0u;
     };
 
     // ---- routing helpers (one warp): rank token t from the logits staged in
@@ -428,18 +441,19 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
         }
     } else {
         if (!pre) {
-            // router rows e = b, b + nC, ...: warp w takes token w / nchk and chunk
-            // w % nchk of the row, so every lane issues its few loads at once; the
-            // producer warp adds the partial sums up and publishes the logits.  The
-            // chunk's weight lines are prefetched into L2 before the wait for the
-            // previous kernel.
+            // router rows e = b, b + nC, ...: warp w takes chunk w % nchk of the row
+            // for tokens w / nchk, w / nchk + kCW / nchk, ..., so every lane issues
+            // its few loads at once; the producer warp adds the partial sums up and
+            // publishes the logits.  The chunk's weight lines are prefetched into L2
+            // before the wait for the previous kernel.
             const int nchk = T >= kCW ? 1 : kCW / T;
             const int np = H / 8;  // 8-code word pairs per row
-            const int t = warp / nchk, ck = warp % nchk;
-            if (t < T)
+            const int t0 = warp / nchk, ck = warp % nchk, tstep = kCW / nchk;
+            const int p0 = ck * np / nchk, p1 = (ck + 1) * np / nchk;
+            if (t0 < T)
                 for (int e = b; e < a.E; e += nC) {
                     const uint8_t *row = reinterpret_cast<const uint8_t *>(a.rq) + (size_t)e * H;
-                    const int l0 = (8 * (ck * np / nchk)) >> 7, l1 = (8 * ((ck + 1) * np / nchk) + 127) >> 7;
+                    const int l0 = (8 * p0) >> 7, l1 = (8 * p1 + 127) >> 7;
                     if (l0 + lane < l1) prefetch_line_l2(row + (size_t)(l0 + lane) * 128);
                     if (lane == 31 && ck == 0) {
                         prefetch_line_l2(a.rs + (size_t)e * (H / kGroup));
@@ -448,24 +462,19 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
                 }
             pdl_wait();
             int j = 0;
-            for (int e = b; e < a.E; e += nC, j++) {
-                float v = 0.f;
-                if (t < T) v = router_dot(a.rq, a.rs, a.rb, H, a.x, e, t, ck * np / nchk, (ck + 1) * np / nchk);
-                if (lane == 0) S.rpart[j][warp] = v;
-            }
+            for (int e = b; e < a.E; e += nC, j++)
+                for (int t = t0; t < T; t += tstep) {
+                    const float v = router_dot(a.rq, a.rs, a.rb, H, a.x, e, t, p0, p1);
+                    if (lane == 0) S.rpart[j][t * nchk + ck] = v;
+                }
             named_arrive(2, kDecThreads);
         } else {
             pdl_wait();
         }
         load_x();
-        for (int k = 0; k < n_shared_mine; k += 2) {
-            const int n = min(2, n_shared_mine - k);
-            int s[2] = {0, 0}, u[2] = {-1, -1}, it[2] = {0, 0};
-            for (int j = 0; j < n; j++) {
-                s[j] = consumer_wait(fill++);
-                it[j] = b + (k + j) * nC;
-            }
-            gateup_tiles(n, s, u, it);
+        for (int k = 0; k < n_shared_mine; k++) {
+            const int s = consumer_wait(fill++);
+            gateup_tile(s, -1, b + k * nC);
         }
     }
     __syncthreads();
@@ -584,17 +593,16 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
         }
         __syncwarp();
     } else {
-        // ---- routed gate/up tiles
-        for (int k = 0; k < n_routed_mine; k += 2) {
-            const int n = min(2, n_routed_mine - k);
-            int s[2] = {0, 0}, u[2] = {0, 0}, it[2] = {0, 0};
-            for (int j = 0; j < n; j++) {
-                s[j] = consumer_wait(fill++);
-                const int jj = j_first + (k + j) * nC;
-                u[j] = (jj - Ts) / Ti;
-                it[j] = (jj - Ts) % Ti;
+        // ---- routed gate/up tiles: (expert u, row block it) of tile j_first + k nC
+        int gu_u = (j_first - Ts) / Ti, gu_it = j_first - Ts - gu_u * Ti;
+        for (int k = 0; k < n_routed_mine; k++) {
+            const int s = consumer_wait(fill++);
+            gateup_tile(s, gu_u, gu_it);
+            gu_it += nC;
+            while (gu_it >= Ti) {
+                gu_it -= Ti;
+                gu_u++;
             }
-            gateup_tiles(n, s, u, it);
         }
         __threadfence();
         named_sync(1, kCThreads);

@@ -111,18 +111,18 @@ int check_layer_call(const moe_layer_t *l, const float *x, int T, int Tlimit, in
 
 struct DecodeCfg {
     int device = -1, sms = 0, smem_optin = 0;
-    size_t static_smem[2][4] = {};
-    bool attr_set[2][4] = {};
-    int attr_smem[2][4] = {};
+    size_t static_smem[2][5] = {};
+    bool attr_set[2][5] = {};
+    int attr_smem[2][5] = {};
 };
 
 template <int NCH, int GPW>
 void *decode_fn() { return (void *)k_decode<NCH, GPW>; }
 
 void *decode_kernel(int nch, int gpw) {
-    static void *const table[2][4] = {
-        {decode_fn<1, 1>(), decode_fn<1, 2>(), decode_fn<1, 3>(), decode_fn<1, 4>()},
-        {decode_fn<2, 1>(), decode_fn<2, 2>(), decode_fn<2, 3>(), decode_fn<2, 4>()}};
+    static void *const table[2][5] = {
+        {decode_fn<1, 1>(), decode_fn<1, 2>(), decode_fn<1, 3>(), decode_fn<1, 4>(), decode_fn<1, 5>()},
+        {decode_fn<2, 1>(), decode_fn<2, 2>(), decode_fn<2, 3>(), decode_fn<2, 4>(), decode_fn<2, 5>()}};
     return table[nch - 1][gpw - 1];
 }
 
@@ -161,7 +161,7 @@ int decode_plan(const moe_layer_t *l, const float *x, int T, int flags, float *y
     a.mode = kModeShared | kModeRouted;
     const int nch = T > 8 ? 2 : 1;
     const int gpw = (a.Lr.G + kCW - 1) / kCW;
-    if (gpw > 4 || l->H > kMaxHiddenLayer) return MOE_EINVAL;  // hidden size above 4096
+    if (gpw > 5 || l->H > kMaxHiddenLayer) return MOE_EINVAL;  // hidden size above 4096
     const int nC = cfg.sms;
     if ((l->E + nC - 1) / nC > kMaxRouterRows) return MOE_EINVAL;
     const int R = a.Lr.R, Gi = a.Lr.Gi;
@@ -172,7 +172,6 @@ int decode_plan(const moe_layer_t *l, const float *x, int T, int flags, float *y
     a.SB = (int)(((size_t)(a.Lr.G > Gi ? a.Lr.G : Gi) * kTileBytes + 127) / 128 * 128);
     a.UPS = a.SB / (Gi * kTileBytes);
     a.hsm_mat_bytes = Gi * T * 128;
-    const int red = 2 * 2 * kCW * nch * 512;  // two buffers of two tiles' partial sums
     void *fn = decode_kernel(nch, gpw);
     size_t &st = cfg.static_smem[nch - 1][gpw - 1];
     if (st == 0) {
@@ -188,13 +187,14 @@ int decode_plan(const moe_layer_t *l, const float *x, int T, int flags, float *y
     int stages = kMaxStages;
     long long smem = 0;
     for (; stages >= 2; stages--) {
+        const long long red = (long long)(stages + 1) * kCW * nch * 512;  // gate/up partial-sum slots
         smem = (long long)stages * a.SB + red + hsm;
         if (smem <= budget) break;
     }
     if (stages < 2) return MOE_EINVAL;
     a.stages = stages;
     a.red_off = stages * a.SB;
-    a.hsm_off = a.red_off + red;
+    a.hsm_off = a.red_off + (stages + 1) * kCW * nch * 512;
     if (cfg.attr_smem[nch - 1][gpw - 1] < smem) {
         if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
             return cuda_status();
