@@ -7,22 +7,26 @@
 // token, the routed experts and an always-on shared expert run GeGLU FFNs on
 // 4-bit affine weights, and the outputs are combined with the softmax gates.
 //
-// Each CTA has 16 compute warps and one producer warp.  Weights arrive through a
+// Each CTA has 15 compute warps and one producer warp.  Weights arrive through a
 // ring of shared-memory stages filled by bulk copies (TMA) and guarded by
-// mbarriers; every weight byte that is known is also prefetched into L2 as early
-// as possible, so HBM streams continuously while the SMs compute.
+// mbarriers.
 //
-//   phase A  producer: copies this CTA's shared-expert gate/up tiles, prefetches
-//            a slice of the shared down matrix, waits until all E router rows
-//            are published.  compute warps: this CTA's router rows (CUDA cores,
-//            8-bit; each row split over the warps), then its shared gate/up tiles.
-//   routing  every CTA ranks the logits itself (identical results everywhere),
-//            and builds the schedule: distinct experts U in ascending id, the
-//            tokens using each, and a compact slot per (token, choice).
+//   phase A  producer: copies this CTA's first shared-expert gate/up tiles,
+//            prefetches a slice of the shared down matrix into L2, then (after the
+//            previous kernel: programmatic dependent launch) publishes the CTA's
+//            router logits and waits until all E rows are published.  compute
+//            warps: this CTA's router rows (CUDA cores, 8-bit; each row split over
+//            the warps), then the token vectors' MMA fragments.
+//   routing  every CTA ranks the logits itself, one warp per token (identical
+//            results everywhere), and builds the schedule: distinct experts U in
+//            ascending id, the tokens using each, and a compact slot per (token,
+//            choice).  Nothing else competes for the SM meanwhile.
 //   phase B  gate/up: the CTA's tiles j = b, b+nC, ... of [shared | routed u=0..U-1]
-//            (one tile = 8 gate rows + the 8 matching up rows, full K).  The 16
-//            warps split K; partial sums meet in shared memory, GeGLU is applied,
-//            and h is written in fp16 (compact slots for routed experts).
+//            (one tile = 8 gate rows + the 8 matching up rows, full K); the shared
+//            ones are already in the ring while the routed ones are copied.  The
+//            warps split K; the last warp to finish a tile adds the partial sums
+//            up, applies GeGLU and writes h in fp16 (compact slots for routed
+//            experts).
 //            down: units (matrix, 16 output rows) in matrix-major order, a
 //            contiguous range per CTA, one unit per warp with full K; h of the
 //            CTA's matrices is copied to shared memory once every CTA's gate/up
@@ -408,21 +412,11 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
                 if (lane == 0) atomicAdd(&a.ctrl[kRouteCnt], (unsigned)j);
             }
         }
-        if (lane == 0) {
-            for (int k = a.stages; k < n_shared_mine; k++) {
-                const int s = producer_slot(fill);
-                if (!*err) {
-                    mbar_arrive_expect_tx(&S.full[s], gu_bytes);
-                    bulk_g2s(ring + (size_t)s * a.SB, gu_src(b + k * nC), gu_bytes, &S.full[s]);
-                    last_fill[s] = fill;
-                }
-                fill++;
-            }
-            if (!pre && !spin_reach(&a.ctrl[kRouteCnt], base.x, (unsigned)a.E, &a.ctrl[kErr])) *err = 1;
-        }
+        if (lane == 0 && !pre && !spin_reach(&a.ctrl[kRouteCnt], base.x, (unsigned)a.E, &a.ctrl[kErr]))
+            *err = 1;
         __syncwarp();
-        // while the compute warps finish the shared tiles: the routing (an earlier
-        // launch's choices, or every token's logits) into shared memory
+        // the routing (an earlier launch's choices, or every token's logits) into
+        // shared memory
         if (pre) {
             for (int p = lane; p < T * a.topk; p += 32) {
                 S.idx[p] = a.idx_pre[p];
@@ -436,8 +430,6 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
             for (int i = lane; i < n / 4; i += 32)
                 reinterpret_cast<float4 *>(lg)[i] = __ldcg(reinterpret_cast<const float4 *>(a.logits) + i);
             for (int i = (n & ~3) + lane; i < n; i += 32) lg[i] = __ldcg(a.logits + i);
-            __syncwarp();
-            rank_token(0);
         }
     } else {
         if (!pre) {
@@ -472,19 +464,13 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
             pdl_wait();
         }
         load_x();
-        for (int k = 0; k < n_shared_mine; k++) {
-            const int s = consumer_wait(fill++);
-            gateup_tile(s, -1, b + k * nC);
-        }
     }
     __syncthreads();
-    // the producer ranked token 0; one warp per token ranks the others, then the
-    // whole CTA builds the schedule
-    if (T > 1) {
-        if (!pre && !*err)
-            for (int t = 1 + warp; t < T; t += kCW + 1) rank_token(t);
-        __syncthreads();
-    }
+    // routing with the whole CTA (nothing else runs meanwhile): one warp per token
+    // ranks the staged logits, then every thread helps to build the schedule
+    if (!pre && !*err)
+        for (int t = warp; t < T; t += kCW + 1) rank_token(t);
+    __syncthreads();
     build_schedule();
     __syncthreads();
 
@@ -511,19 +497,19 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
     // =========================== phase B ===========================
     if (producer) {
         if (lane == 0) {
-            // the routed gate/up tiles through the ring (bulk copies stream better
-            // on their own than behind L2 prefetches of the same data)
-            const int first = min(n_routed_mine, a.stages);
-            for (int k = 0; k < first; k++) {
+            // the shared gate/up tiles that did not fit the ring at the start, then the
+            // routed ones (bulk copies stream better on their own than behind L2
+            // prefetches of the same data)
+            for (int k = a.stages; k < n_shared_mine; k++) {
                 const int s = producer_slot(fill);
                 if (!*err) {
                     mbar_arrive_expect_tx(&S.full[s], gu_bytes);
-                    bulk_g2s(ring + (size_t)s * a.SB, gu_src(j_first + k * nC), gu_bytes, &S.full[s]);
+                    bulk_g2s(ring + (size_t)s * a.SB, gu_src(b + k * nC), gu_bytes, &S.full[s]);
                     last_fill[s] = fill;
                 }
                 fill++;
             }
-            for (int k = first; k < n_routed_mine; k++) {
+            for (int k = 0; k < n_routed_mine; k++) {
                 const int s = producer_slot(fill);
                 if (!*err) {
                     mbar_arrive_expect_tx(&S.full[s], gu_bytes);
@@ -593,6 +579,12 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
         }
         __syncwarp();
     } else {
+        // ---- the shared gate/up tiles (in the ring since the start) while the routed
+        // ones are on their way
+        for (int k = 0; k < n_shared_mine; k++) {
+            const int s = consumer_wait(fill++);
+            gateup_tile(s, -1, b + k * nC);
+        }
         // ---- routed gate/up tiles: (expert u, row block it) of tile j_first + k nC
         int gu_u = (j_first - Ts) / Ti, gu_it = j_first - Ts - gu_u * Ti;
         for (int k = 0; k < n_routed_mine; k++) {
