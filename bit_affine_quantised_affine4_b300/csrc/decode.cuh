@@ -657,19 +657,11 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
                             } else {
                                 zero_b(hb);
                             }
-                            // the group sum of h for slot 8ch + gl (the bias term b * sum h):
-                            // the lane's 16 values, then the 4 lanes of the slot; token
-                            // columns 2c, 2c+1 take it from lanes 8c and 8c + 4
-                            float hs = 0.f;
-#pragma unroll
-                            for (int w = 0; w < 8; w++) {
-                                const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&hb[w]));
-                                hs += f.x + f.y;
-                            }
-                            hs += __shfl_xor_sync(0xffffffffu, hs, 1);
-                            hs += __shfl_xor_sync(0xffffffffu, hs, 2);
-                            const float s0 = __shfl_sync(0xffffffffu, hs, 8 * c);
-                            const float s1 = __shfl_sync(0xffffffffu, hs, 8 * c + 4);
+                            // the group sums of h for token columns 2c, 2c+1 (the bias term
+                            // b * sum h), on the tensor cores like those of x
+                            float hsum[4] = {0.f, 0.f, 0.f, 0.f};
+                            mma_group_sums(hsum, hb);
+                            const float s0 = hsum[0], s1 = hsum[1];
                             float d[4] = {0.f, 0.f, 0.f, 0.f};
                             mma_group_codes(d, make_uint2(q.x, q.y), make_uint2(q.z, q.w), hb);
                             affine_acc(acc[ch], d, s0, s1, sa, ba, sb, bb);
