@@ -30,7 +30,7 @@ ENTRY_POINTS = (
     "moe_workspace_bytes", "moe_workspace_init", "moe_workspace_status",
     "affine_quantise", "qgemv_affine4", "moe_route", "moe_layer_decode",
     "moe_layer_prefill_chunk", "moe_cache_create", "moe_cache_destroy",
-    "moe_cache_slots", "moe_cache_stats", "moe_layer_decode_noalloc",
+    "moe_cache_slots", "moe_cache_stats", "moe_layer_decode_noalloc", "moe_layer_decode_host",
     "moe_lfu_create", "moe_lfu_destroy", "moe_lfu_step", "moe_lfu_state",
 )
 
@@ -76,6 +76,7 @@ def _load():
     L.moe_layer_decode.argtypes = [p, p, i, i, p, p, p, p, p, sz, p]
     L.moe_layer_prefill_chunk.argtypes = [p, p, i, i, p, p, p, p, sz, p]
     L.moe_layer_decode_noalloc.argtypes = [p, p, i, i, p, p, p, p]
+    L.moe_layer_decode_host.argtypes = [p, p, i, i, p, p, p, p, p, sz, p]
     L.moe_cache_create.argtypes = [p, i, i, i, p, sz, i]
     L.moe_cache_destroy.argtypes = [p]
     L.moe_cache_slots.argtypes = [p, p, p]
@@ -195,6 +196,21 @@ def moe_layer_decode(layer: moe_layer_t, x, ws, y=None, flags: int = 0, idx=None
     _check(lib.moe_layer_decode(C.byref(layer), _ptr(x), T, flags, _ptr(y), _ptr(idx), _ptr(gate),
                                 None if cache is None else cache.handle, _ptr(ws), ws.numel(),
                                 _stream(stream)), "moe_layer_decode")
+    return y
+
+
+def moe_layer_decode_host(layer: moe_layer_t, x, ws, y=None, flags: int = 0, idx=None, gate=None,
+                          cache=None, stream=None):
+    """moe_layer_decode on host (CPU) tensors: x, y, idx, gate live in host memory
+    (pinned for asynchronous copies); returns once y is filled."""
+    T = x.shape[0]
+    y = torch.empty_like(x) if y is None else y
+    for t in (x, y, idx, gate):
+        if t is not None and t.is_cuda:
+            raise ValueError("moe_layer_decode_host takes host tensors")
+    _check(lib.moe_layer_decode_host(C.byref(layer), _ptr(x), T, flags, _ptr(y), _ptr(idx), _ptr(gate),
+                                     None if cache is None else cache.handle, _ptr(ws), ws.numel(),
+                                     _stream(stream)), "moe_layer_decode_host")
     return y
 
 

@@ -85,6 +85,9 @@ struct Ws {
     __half *hs16;      // [Tmax][Is]      shared activations
     float *pr;         // [Tmax*topk][H]  routed down partials
     float *ps;         // [P][Tmax][H]    shared down partials
+    float *xh, *yh;    // [Tmax][H]       device copies of a host call's x and y
+    int *ih;           // [Tmax][topk]    and of its routing outputs
+    float *gh;         // [Tmax][topk]
     // prefill chunk (grouped GEMMs)
     int *plan;         // U, rows used, uexp[256], urow[256], ucnt[256], rowtok[Rmax], rowpair[Rmax]
     uint8_t *Br, *Bs;  // token operand tiles: [H/64][Rmax][128 B], [H/64][T16][128 B]
@@ -109,7 +112,7 @@ constexpr int kMaxTickets = kMaxHiddenLayer / 16;
 constexpr size_t kWsHeaderBytes = (kCtrlWords + kMaxTickets) * sizeof(unsigned);
 
 struct WsLayout {
-    size_t ctrl, logits, idx, gate, h16, hs16, pr, ps, decode_total;
+    size_t ctrl, logits, idx, gate, h16, hs16, pr, ps, xh, yh, ih, gh, decode_total;
     size_t plan, Br, Bs, Hr, Hs, Yr, Ys, total;
     int Tmax;
 };
@@ -127,6 +130,10 @@ inline WsLayout ws_layout(const moe_layer_t &l, int Tmax) {
     W.hs16 = off;   off = up256(off + sizeof(__half) * size_t(Tmax) * l.Is);
     W.pr = off;     off = up256(off + sizeof(float) * size_t(Tmax) * l.topk * l.H);
     W.ps = off;     off = up256(off + sizeof(float) * size_t(P) * Tmax * l.H);
+    W.xh = off;     off = up256(off + sizeof(float) * size_t(Tmax) * l.H);
+    W.yh = off;     off = up256(off + sizeof(float) * size_t(Tmax) * l.H);
+    W.ih = off;     off = up256(off + sizeof(int) * size_t(Tmax) * l.topk);
+    W.gh = off;     off = up256(off + sizeof(float) * size_t(Tmax) * l.topk);
     W.decode_total = off;
     const int Rmax = prefill_rows(l, Tmax), T16 = (Tmax + 15) & ~15;
     W.plan = off;   off = up256(off + sizeof(int) * (2 + 3 * MOE_MAX_EXPERTS + 2 * size_t(Rmax)));
@@ -152,6 +159,10 @@ inline Ws ws_bind(void *base, const WsLayout &W, const moe_layer_t &l) {
     w.hs16 = (__half *)(p + W.hs16);
     w.pr = (float *)(p + W.pr);
     w.ps = (float *)(p + W.ps);
+    w.xh = (float *)(p + W.xh);
+    w.yh = (float *)(p + W.yh);
+    w.ih = (int *)(p + W.ih);
+    w.gh = (float *)(p + W.gh);
     w.plan = (int *)(p + W.plan);
     w.Br = p + W.Br;
     w.Bs = p + W.Bs;

@@ -96,7 +96,7 @@ int bind_ws(const moe_layer_t *l, int T, void *d_ws, size_t ws_bytes, Ws *out, b
 
 int launch_route(const moe_layer_t *l, const LayerDev &ly, const float *x, int T, Ws ws,
                  int32_t *idx, float *gate, float *logits, cudaStream_t st) {
-    const dim3 grid(l->E, (T + kRouteTok - 1) / kRouteTok);
+    const dim3 grid((l->E + kRouteExp - 1) / kRouteExp, (T + kRouteTok - 1) / kRouteTok);
     k_route<<<grid, kRouteTok * 32, 0, st>>>(ly, x, T, ws, idx, gate, logits);
     return cuda_status();
 }
@@ -553,6 +553,31 @@ int moe_layer_decode(const moe_layer_t *layer, const float *x, int T, int flags,
     int rc = check_layer_call(layer, x, T, MOE_MAX_DECODE_TOKENS, flags, y);
     if (rc) return rc;
     return run_decode(layer, x, T, flags, y, idx_out, gate_out, d_ws, ws_bytes, stream);
+}
+
+// Host buffers: x is staged in the workspace, the decode step runs on the stream,
+// y (and the routing) come back; the call returns once the stream is idle.
+int moe_layer_decode_host(const moe_layer_t *layer, const float *x_host, int T, int flags, float *y_host,
+                          int32_t *idx_host, float *gate_host, moe_cache_t *cache, void *d_ws, size_t ws_bytes,
+                          void *stream) {
+    if (!layer_ok(layer) || !x_host || !y_host || T < 1 || T > MOE_MAX_DECODE_TOKENS || (flags & ~MOE_RESIDUAL))
+        return MOE_EINVAL;
+    Ws ws;
+    int rc = bind_ws(layer, T, d_ws, ws_bytes, &ws);
+    if (rc) return rc;
+    cudaStream_t st = as_stream(stream);
+    const size_t xb = sizeof(float) * (size_t)T * layer->H, rb = (size_t)T * layer->topk;
+    if (cudaMemcpyAsync(ws.xh, x_host, xb, cudaMemcpyHostToDevice, st) != cudaSuccess) return cuda_status();
+    rc = moe_layer_decode(layer, ws.xh, T, flags, ws.yh, idx_host ? ws.ih : nullptr, gate_host ? ws.gh : nullptr,
+                          cache, d_ws, ws_bytes, stream);
+    if (rc) return rc;
+    if (cudaMemcpyAsync(y_host, ws.yh, xb, cudaMemcpyDeviceToHost, st) != cudaSuccess) return cuda_status();
+    if (idx_host && cudaMemcpyAsync(idx_host, ws.ih, sizeof(int32_t) * rb, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return cuda_status();
+    if (gate_host && cudaMemcpyAsync(gate_host, ws.gh, sizeof(float) * rb, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return cuda_status();
+    if (cudaStreamSynchronize(st) != cudaSuccess) return cuda_status();
+    return MOE_OK;
 }
 
 int moe_layer_prefill_chunk(const moe_layer_t *layer, const float *x, int T, int flags, float *y,

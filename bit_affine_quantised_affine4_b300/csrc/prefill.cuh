@@ -76,24 +76,52 @@ __global__ void __launch_bounds__(256) k_prefill_plan(const int *__restrict__ id
         atomicOr(&mask[e][t >> 5], 1u << (t & 31));
     }
     __syncthreads();
-    if (tid == 0) {
-        int U = 0, row = 0;
-        for (int e = 0; e < E; e++) {
-            const int cnt = __popc(mask[e][0]) + __popc(mask[e][1]) + __popc(mask[e][2]) + __popc(mask[e][3]);
-            uid[e] = -1;
-            if (cnt) {
-                uid[e] = U;
-                p.uexp[U] = e;
-                p.ucnt[U] = cnt;
-                p.urow[U] = row;
-                urow_s[U] = row;
-                row += round16(cnt);
-                U++;
-            }
+    // distinct experts in ascending id and their 16-padded row segments: warp w
+    // scans experts 32w..32w+31 (ballot + shuffle scan), then adds the totals of the
+    // warps before it
+    __shared__ unsigned wsum[MOE_MAX_EXPERTS / 32];  // experts << 16 | rows of the warp's 32 experts
+    __shared__ int ucnt_s[MOE_MAX_EXPERTS];
+    __shared__ int U_s;
+    const int warp = tid >> 5, lane = tid & 31, nw = (E + 31) >> 5;
+    int cnt = 0, incl = 0;
+    unsigned bal = 0u;
+    if (warp < nw) {
+        const int e = 32 * warp + lane;
+        cnt = e < E ? __popc(mask[e][0]) + __popc(mask[e][1]) + __popc(mask[e][2]) + __popc(mask[e][3]) : 0;
+        bal = __ballot_sync(0xffffffffu, cnt > 0);
+        incl = round16(cnt);
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
         }
-        urow_s[U] = row;
-        p.U[0] = U;
-        p.U[1] = row;
+        if (lane == 31) wsum[warp] = ((unsigned)__popc(bal) << 16) | (unsigned)incl;
+    }
+    __syncthreads();
+    if (warp < nw) {
+        int ub = 0, rb = 0;
+        for (int w = 0; w < warp; w++) {
+            ub += (int)(wsum[w] >> 16);
+            rb += (int)(wsum[w] & 0xFFFFu);
+        }
+        const int e = 32 * warp + lane;
+        if (e < E) uid[e] = -1;
+        if (cnt) {
+            const int u = ub + __popc(bal & ((1u << lane) - 1u)), row = rb + incl - round16(cnt);
+            uid[e] = u;
+            p.uexp[u] = e;
+            p.ucnt[u] = cnt;
+            p.urow[u] = row;
+            urow_s[u] = row;
+            ucnt_s[u] = cnt;
+        }
+        if (warp == nw - 1 && lane == 31) {
+            const int U = ub + __popc(bal), rows = rb + incl;
+            urow_s[U] = rows;
+            p.U[0] = U;
+            p.U[1] = rows;
+            U_s = U;
+        }
     }
     __syncthreads();
     for (int q = tid; q < P2; q += blockDim.x) {
@@ -105,7 +133,7 @@ __global__ void __launch_bounds__(256) k_prefill_plan(const int *__restrict__ id
         p.rowpair[urow_s[u] + rank] = q;
     }
     // padding rows of each segment, and unused rows up to Rmax
-    const int U = p.U[0], used = urow_s[U];
+    const int U = U_s, used = urow_s[U];
     for (int r = tid; r < Rmax; r += blockDim.x) {
         if (r >= used) {
             p.rowtok[r] = -1;
@@ -116,7 +144,7 @@ __global__ void __launch_bounds__(256) k_prefill_plan(const int *__restrict__ id
             const int mid = (lo + hi + 1) >> 1;
             if (urow_s[mid] <= r) lo = mid; else hi = mid - 1;
         }
-        if (r - urow_s[lo] >= p.ucnt[lo]) p.rowtok[r] = -1;
+        if (r - urow_s[lo] >= ucnt_s[lo]) p.rowtok[r] = -1;
     }
 }
 

@@ -119,22 +119,62 @@ __device__ __forceinline__ float router_dot(const uint32_t *rq, const __half *rs
 }
 
 constexpr int kRouteTok = 16;  // tokens per router CTA (one warp each)
+constexpr int kRouteExp = 4;   // router rows per CTA (each token vector read once for all of them)
 
-// CTA (e, g): router row e for tokens 16g..16g+15, one warp per token over the
-// whole row.  The last CTA of token group g (a ticket per group) ranks the group's
-// tokens, one warp per token.
+// Router rows e0 .. e0 + NE - 1 (those < E) for token t, over the whole row:
+// router_dot's arithmetic for each row, with each x element loaded once for all.
+template <int NE>
+__device__ __forceinline__ void router_dot_rows(const uint32_t *rq, const __half *rs, const __half *rb, int H,
+                                                int E, const float *x, int e0, int t, float (&out)[NE]) {
+    const int lane = threadIdx.x & 31, G = H / kGroup, np = H / 8;
+    const float4 *xt = reinterpret_cast<const float4 *>(x + (size_t)t * H);
+    float acc[NE];
+#pragma unroll
+    for (int j = 0; j < NE; j++) acc[j] = 0.f;
+#pragma unroll 2
+    for (int p = lane; p < np; p += 32) {
+        const float4 x0 = __ldg(xt + 2 * p), x1 = __ldg(xt + 2 * p + 1);
+#pragma unroll
+        for (int j = 0; j < NE; j++) {
+            const int e = e0 + j < E ? e0 + j : E - 1;
+            const uint2 w = __ldg(reinterpret_cast<const uint2 *>(rq + (size_t)e * (H / 4)) + p);
+            const float sc = __half2float(rs[(size_t)e * G + (p >> 3)]), bb = __half2float(rb[(size_t)e * G + (p >> 3)]);
+            float a = acc[j];
+            a = fmaf(fmaf(sc, (float)(w.x & 0xFFu), bb), x0.x, a);
+            a = fmaf(fmaf(sc, (float)((w.x >> 8) & 0xFFu), bb), x0.y, a);
+            a = fmaf(fmaf(sc, (float)((w.x >> 16) & 0xFFu), bb), x0.z, a);
+            a = fmaf(fmaf(sc, (float)(w.x >> 24), bb), x0.w, a);
+            a = fmaf(fmaf(sc, (float)(w.y & 0xFFu), bb), x1.x, a);
+            a = fmaf(fmaf(sc, (float)((w.y >> 8) & 0xFFu), bb), x1.y, a);
+            a = fmaf(fmaf(sc, (float)((w.y >> 16) & 0xFFu), bb), x1.z, a);
+            a = fmaf(fmaf(sc, (float)(w.y >> 24), bb), x1.w, a);
+            acc[j] = a;
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < NE; j++) out[j] = warp_sum(acc[j]);
+}
+
+// CTA (r, g): router rows 4r..4r+3 for tokens 16g..16g+15, one warp per token
+// over the whole rows.  The last CTA of token group g (a ticket per group) ranks
+// the group's tokens, one warp per token.
 __global__ void __launch_bounds__(kRouteTok * 32)
 k_route(LayerDev ly, const float *__restrict__ x, int T, Ws ws, int32_t *idx_out, float *gate_out,
         float *logits_out) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int e = blockIdx.x, t = blockIdx.y * kRouteTok + warp;
+    const int e0 = blockIdx.x * kRouteExp, t = blockIdx.y * kRouteTok + warp;
     if (t < T) {
-        float v = router_dot(ly.rq, ly.rs, ly.rb, ly.H, x, e, t, 0, ly.H / 8);
-        if (lane == 0) {
-            if (ly.bias) v += ly.bias[e];
-            ws.logits[(size_t)t * ly.E + e] = v;
-            if (logits_out) logits_out[(size_t)t * ly.E + e] = v;
-        }
+        float v[kRouteExp];
+        router_dot_rows<kRouteExp>(ly.rq, ly.rs, ly.rb, ly.H, ly.E, x, e0, t, v);
+        if (lane == 0)
+#pragma unroll
+            for (int j = 0; j < kRouteExp; j++) {
+                const int e = e0 + j;
+                if (e >= ly.E) break;
+                const float lv = v[j] + (ly.bias ? ly.bias[e] : 0.f);
+                ws.logits[(size_t)t * ly.E + e] = lv;
+                if (logits_out) logits_out[(size_t)t * ly.E + e] = lv;
+            }
     }
     __shared__ int is_last;
     __syncthreads();

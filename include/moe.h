@@ -217,6 +217,21 @@ MOE_API int moe_layer_prefill_chunk(const moe_layer_t *layer, const float *x, in
                             void *stream);
 
 /*
+ * moe_layer_decode_host -- moe_layer_decode on HOST buffers: x_host (T x H fp32),
+ * y_host (T x H fp32) and the optional idx_host / gate_host (T x topk) are host
+ * memory; page-locked memory makes the copies asynchronous, pageable memory also
+ * works.  The call copies x into the workspace (which holds device staging for x,
+ * y and the routing), runs the decode step on `stream` (through `cache` when it is
+ * non-null), copies y and the requested routing back, and waits for `stream`
+ * before it returns: the outputs are ready on return.  x_host and y_host must not
+ * overlap.  Same workspace (moe_workspace_bytes) and error codes as
+ * moe_layer_decode; MOE_ECUDA if a copy or the stream wait fails.
+ */
+MOE_API int moe_layer_decode_host(const moe_layer_t *layer, const float *x_host, int T, int flags,
+                                  float *y_host, int32_t *idx_host, float *gate_host, moe_cache_t *cache,
+                                  void *d_ws, size_t ws_bytes, void *stream);
+
+/*
  * moe_layer_decode_noalloc -- the same decode step as moe_layer_decode (no cache),
  * for callers that cannot allocate device memory: for example a plug-in running
  * inside a host framework that reserves the GPU's memory through its own allocator

@@ -191,6 +191,33 @@ def test_decode_full_zipf_batch(moe, full_zipf, T):
     _layer_check(moe, s, gl, ol, T, 300 + T)
 
 
+@pytest.mark.parametrize("T", [1, 5, 16])
+def test_decode_host_buffers(moe, tiny, T):
+    # moe_layer_decode_host: host x/y/idx/gate, copies and the stream wait inside the
+    # call; the result equals the device-pointer call's and is within the oracle's
+    # tolerance
+    s, gl, ol = tiny
+    x = synth.tokens(s, T, seed=0, stream=700 + T)
+    layer = gl.view()
+    ws = moe.new_workspace(layer, T)
+    xh = torch.from_numpy(x).pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+    ih = torch.empty((T, s.topk), dtype=torch.int32).pin_memory()
+    gh = torch.empty((T, s.topk), dtype=torch.float32).pin_memory()
+    moe.moe_layer_decode_host(layer, xh, ws, y=yh, flags=moe.MOE_RESIDUAL, idx=ih, gate=gh)
+    assert moe.moe_workspace_status(ws) == moe.MOE_OK
+    yd = moe.moe_layer_decode(layer, _cuda(x), ws, flags=moe.MOE_RESIDUAL)
+    torch.cuda.synchronize()
+    assert np.array_equal(yh.numpy(), yd.cpu().numpy())
+    ry, ridx, rgate = ol.layer(x, residual=True)
+    assert np.array_equal(ih.numpy(), ridx)
+    assert within_tol(gh.numpy(), rgate, TOL)[0]
+    ok, worst = within_tol(yh.numpy(), ry, TOL)
+    assert ok, "worst err/bound %.3f" % worst
+    with pytest.raises(ValueError):
+        moe.moe_layer_decode_host(layer, _cuda(x), ws)
+
+
 @pytest.mark.parametrize("T", [1, 37, 128])
 def test_prefill_tiny(moe, tiny, T):
     s, gl, ol = tiny
