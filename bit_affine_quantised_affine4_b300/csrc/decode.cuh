@@ -407,7 +407,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
                 }
             }
             if (j > 0) {
-                __threadfence();
+                fence_acq_rel_gpu();
                 __syncwarp();
                 if (lane == 0) atomicAdd(&a.ctrl[kRouteCnt], (unsigned)j);
             }
@@ -596,7 +596,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
                 gu_u++;
             }
         }
-        __threadfence();
+        fence_acq_rel_gpu();
         named_sync(1, kCThreads);
         if (tid == 0) atomicAdd(&a.ctrl[kGuDone], (unsigned)(n_shared_mine + n_routed_mine));
         // ---- down units
@@ -684,7 +684,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
             consumer_release(s);
         }
         // ---- tickets: this CTA's down units are counted into their 16-row tiles
-        __threadfence();
+        fence_acq_rel_gpu();
         named_sync(1, kCThreads);
         if (do_routed && !*err)
             for (int lu = tid; lu < nunits; lu += kCThreads) atomicAdd(&a.ticket[(ulo + lu) % R], 1u);

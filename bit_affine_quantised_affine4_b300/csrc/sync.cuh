@@ -126,6 +126,10 @@ __device__ __forceinline__ void prefetch_line_l2(const void *p) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
+// Release/acquire fence at GPU scope: this thread's earlier writes become visible
+// before its later ones (with a relaxed counter update after it: a release).
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
 // Named barrier over `threads` threads (a multiple of 32).
 __device__ __forceinline__ void named_sync(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
