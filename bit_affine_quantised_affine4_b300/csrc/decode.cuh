@@ -131,7 +131,7 @@ struct DecodeSmem {
     int uexp[kMaxPairs], ubase[kMaxPairs], ucnt[kMaxPairs], uslot[kMaxPairs];
     float rpart[kMaxRouterRows][kCW > MOE_MAX_DECODE_TOKENS ? kCW : MOE_MAX_DECODE_TOKENS];
     unsigned wsum[MOE_MAX_EXPERTS / 32];  // schedule: experts << 16 | slots of 32 experts
-    unsigned tcnt[kMaxStages + 1];         // gate/up partial-sum slots: warps arrived
+    unsigned tcnt[kMaxStages + 2];         // gate/up partial-sum slots: warps arrived (+1: claimed)
     int U;
     int err;
 };
@@ -162,7 +162,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
             mbar_init(&S.empty[s], kCW);
         }
         mbar_init(&S.hbar, 1);
-        for (int i = 0; i <= kMaxStages; i++) S.tcnt[i] = 0u;
+        for (int i = 0; i < kMaxStages + 2; i++) S.tcnt[i] = 0u;
         S.err = 0;
         mbar_fence_init();
     }
@@ -225,15 +225,54 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
     };
 
     // One gate/up tile by the compute warps: each warp takes its K slice and puts
-    // its partial sums in one of stages + 1 slots of shared memory; the last warp
-    // to arrive (a counter per slot) adds the 16 partials up in warp order, applies
-    // GeGLU and stores h in fp16, while the others go on to their next tile.  A
-    // slot is not reused too early: a warp reaches tile k + stages + 1 only after
-    // every warp has released tile k + 1's stage, which the reducer of tile k does
-    // after its reduction.  u < 0 marks the shared expert, it is the tile's row block.
+    // its partial sums in one of stages + 2 slots of shared memory and counts
+    // itself in (a counter per slot).  A tile is reduced (the 15 partials added up
+    // in warp order, GeGLU, h stored in fp16) by the first warp that, having
+    // written its partial of the next tile, finds all 15 partials of this one in
+    // and claims it -- usually a fast warp, so no warp is both the slowest and the
+    // one that reduces.  The CTA's last tile is reduced by its last arriver.  A slot
+    // is reused only after the warp that reduced its previous tile has released a
+    // later ring stage.  u < 0 marks the shared expert, it is the tile's row block.
     int slot = 0;
-    const int nslot = a.stages + 1;
-    auto gateup_tile = [&](int s, int u, int it) {
+    const int nslot = a.stages + 2;
+    auto reduce_tile = [&](int sl, int u, int it) {
+        const float *rw = red + (size_t)sl * kCW * NCH * 128;
+        __threadfence_block();
+        // lane L holds rows (L / 4, L / 4 + 8) = (gate, up) of row block it, token
+        // columns 2(L % 4), 2(L % 4) + 1 of each chunk
+        const int row = 8 * it + gl, g = row / kGroup, k = row % kGroup;
+#pragma unroll
+        for (int ch = 0; ch < NCH; ch++) {
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 5
+            for (int w = 0; w < kCW; w++) {
+                const float4 p = reinterpret_cast<const float4 *>(rw + (size_t)(w * NCH + ch) * 128)[lane];
+                v.x += p.x;
+                v.y += p.y;
+                v.z += p.z;
+                v.w += p.w;
+            }
+#pragma unroll
+            for (int i = 0; i < 2; i++) {
+                const int t = 8 * ch + 2 * c + i;
+                if (t >= T || *err) continue;
+                const __half hv = __float2half_rn(gelu_tanh(i ? v.y : v.x) * (i ? v.w : v.z));
+                if (u < 0) {
+                    a.hs16[((size_t)g * T + t) * kGroup + h_pos(k, t)] = hv;
+                } else {
+                    const unsigned m = S.mask[S.uexp[u]];
+                    if ((m >> t) & 1u) {
+                        const int sl2 = __popc(m & ((1u << t) - 1u)), nu = S.ucnt[u];
+                        a.h16[(size_t)S.ubase[u] * a.I + ((size_t)g * nu + sl2) * kGroup + h_pos(k, sl2)] = hv;
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) S.tcnt[sl] = 0u;
+    };
+    int p_slot = -1, p_u = 0, p_it = 0;  // the previous tile (a reduction candidate)
+    auto gateup_tile = [&](int s, int u, int it, bool final_tile) {
         float acc[NCH][4];
 #pragma unroll
         for (int ch = 0; ch < NCH; ch++)
@@ -260,54 +299,27 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
         }
         consumer_release(s);
         float *rw = red + (size_t)slot * kCW * NCH * 128;
-        unsigned *cnt = &S.tcnt[slot];
-        if (++slot == nslot) slot = 0;
 #pragma unroll
         for (int ch = 0; ch < NCH; ch++)
             reinterpret_cast<float4 *>(rw + (size_t)(warp * NCH + ch) * 128)[lane] =
                 make_float4(acc[ch][0], acc[ch][1], acc[ch][2], acc[ch][3]);
         __syncwarp();
-        unsigned last = 0;
+        unsigned claim = 0;  // bit 0: reduce the previous tile; bit 1: reduce this one
         if (lane == 0) {
             __threadfence_block();
-            last = atomicAdd(cnt, 1u) == (unsigned)(kCW - 1);
+            const unsigned n = atomicAdd(&S.tcnt[slot], 1u) + 1u;
+            if (final_tile && n == (unsigned)kCW) claim |= 2u;
+            if (p_slot >= 0 && atomicCAS(&S.tcnt[p_slot], (unsigned)kCW, (unsigned)kCW + 1u) == (unsigned)kCW)
+                claim |= 1u;
         }
-        if (!__shfl_sync(0xffffffffu, last, 0)) return;
-        __threadfence_block();
-        // lane L holds rows (L / 4, L / 4 + 8) = (gate, up) of row block it, token
-        // columns 2(L % 4), 2(L % 4) + 1 of each chunk
-        const int row = 8 * it + gl, g = row / kGroup, k = row % kGroup;
-#pragma unroll
-        for (int ch = 0; ch < NCH; ch++) {
-            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-            for (int w = 0; w < kCW; w++) {
-                const float4 p = reinterpret_cast<const float4 *>(rw + (size_t)(w * NCH + ch) * 128)[lane];
-                v.x += p.x;
-                v.y += p.y;
-                v.z += p.z;
-                v.w += p.w;
-            }
-#pragma unroll
-            for (int i = 0; i < 2; i++) {
-                const int t = 8 * ch + 2 * c + i;
-                if (t >= T || *err) continue;
-                const __half hv = __float2half_rn(gelu_tanh(i ? v.y : v.x) * (i ? v.w : v.z));
-                if (u < 0) {
-                    a.hs16[((size_t)g * T + t) * kGroup + h_pos(k, t)] = hv;
-                } else {
-                    const unsigned m = S.mask[S.uexp[u]];
-                    if ((m >> t) & 1u) {
-                        const int sl = __popc(m & ((1u << t) - 1u)), nu = S.ucnt[u];
-                        a.h16[(size_t)S.ubase[u] * a.I + ((size_t)g * nu + sl) * kGroup + h_pos(k, sl)] = hv;
-                    }
-                }
-            }
-        }
-        __syncwarp();
-        if (lane == 0) *cnt = 0u;
+        claim = __shfl_sync(0xffffffffu, claim, 0);
+        if (claim & 1u) reduce_tile(p_slot, p_u, p_it);
+        if (claim & 2u) reduce_tile(slot, u, it);
+        p_slot = slot;
+        p_u = u;
+        p_it = it;
+        if (++slot == nslot) slot = 0;
     };
-
     // ---- routing helpers (one warp): rank token t from the logits staged in
     // shared memory; build the schedule from S.idx
     auto rank_token = [&](int t) {
@@ -583,13 +595,13 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
         // ones are on their way
         for (int k = 0; k < n_shared_mine; k++) {
             const int s = consumer_wait(fill++);
-            gateup_tile(s, -1, b + k * nC);
+            gateup_tile(s, -1, b + k * nC, n_routed_mine == 0 && k == n_shared_mine - 1);
         }
         // ---- routed gate/up tiles: (expert u, row block it) of tile j_first + k nC
         int gu_u = (j_first - Ts) / Ti, gu_it = j_first - Ts - gu_u * Ti;
         for (int k = 0; k < n_routed_mine; k++) {
             const int s = consumer_wait(fill++);
-            gateup_tile(s, gu_u, gu_it);
+            gateup_tile(s, gu_u, gu_it, k == n_routed_mine - 1);
             gu_it += nC;
             while (gu_it >= Ti) {
                 gu_it -= Ti;
