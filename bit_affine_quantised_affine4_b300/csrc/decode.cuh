@@ -88,7 +88,7 @@ struct DecodeArgs {
     float *pr;     // routed partials [T*topk][H]
     float *ps;     // shared partials [P][T][H]
     // launch
-    int stages, SB, UPS, red_off, hsm_off, hsm_mat_bytes;
+    int stages, SB, UPS, red_off, hsm_off, hsm_mat_bytes, hsum_off;
     int mode;
     const int *idx_pre;      // [T][topk] routing of an earlier router launch (kModePre)
     const float *gate_pre;   // [T][topk]
@@ -616,6 +616,38 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
             *err = 1;
             atomicExch(&a.ctrl[kErr], 1u);
         }
+        // T > 8: the group sums of h (the bias term b * sum h) once per (matrix,
+        // group, 8-token chunk) of this CTA's matrices, by an MMA with a ones matrix;
+        // at T <= 8 each unit computes its own (one chunk: cheaper than a barrier)
+        float *hsum = reinterpret_cast<float *>(dsm + a.hsum_off);  // [matrix][Gi][16]
+        if constexpr (NCH > 1) {
+            const int nm = nunits > 0 ? (uhi - 1) / R - m_first + 1 : 0;
+            for (int task = warp; task < nm * Gi * NCH && !*err; task += kCW) {
+                const int ch = task % NCH, mg = task / NCH, mi = mg / Gi, g = mg - mi * Gi, m = m_first + mi;
+                const int ng = m < Pe ? min(Gi, Gs - m * Gi) : Gi;
+                const int nsl = m < Pe ? T : S.ucnt[m - Pe];
+                if (g >= ng || 8 * ch >= nsl) continue;
+                uint32_t hb[8];
+                const int j = 8 * ch + gl;
+                if (j < nsl) {
+                    const uint8_t *hr = hsm + (size_t)mi * a.hsm_mat_bytes + ((size_t)g * nsl + j) * 128;
+                    const int sw = (j & 1);
+                    const uint4 v0 = *reinterpret_cast<const uint4 *>(hr + 16 * ((2 * c) ^ sw));
+                    const uint4 v1 = *reinterpret_cast<const uint4 *>(hr + 16 * ((2 * c + 1) ^ sw));
+                    hb[0] = v0.x; hb[1] = v0.y; hb[2] = v0.z; hb[3] = v0.w;
+                    hb[4] = v1.x; hb[5] = v1.y; hb[6] = v1.z; hb[7] = v1.w;
+                } else {
+                    zero_b(hb);
+                }
+                float d[4] = {0.f, 0.f, 0.f, 0.f};
+                mma_group_sums(d, hb);
+                if (gl == 0) {
+                    hsum[(size_t)mg * 16 + 8 * ch + 2 * c] = d[0];
+                    hsum[(size_t)mg * 16 + 8 * ch + 2 * c + 1] = d[1];
+                }
+            }
+            named_sync(1, kCThreads);
+        }
         int wm = (ulo + warp) / R, wr = ulo + warp - wm * R;  // this warp's next unit
         for (int k = 0; k < nstg; k++) {
             const int s = consumer_wait(fill++);
@@ -671,9 +703,17 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
                             }
                             // the group sums of h for token columns 2c, 2c+1 (the bias term
                             // b * sum h), on the tensor cores like those of x
-                            float hsum[4] = {0.f, 0.f, 0.f, 0.f};
-                            mma_group_sums(hsum, hb);
-                            const float s0 = hsum[0], s1 = hsum[1];
+                            float s0, s1;
+                            if constexpr (NCH > 1) {
+                                const float *hg = hsum + ((size_t)(m - m_first) * Gi + g) * 16 + 8 * ch + 2 * c;
+                                s0 = hg[0];
+                                s1 = hg[1];
+                            } else {
+                                float hq[4] = {0.f, 0.f, 0.f, 0.f};
+                                mma_group_sums(hq, hb);
+                                s0 = hq[0];
+                                s1 = hq[1];
+                            }
                             float d[4] = {0.f, 0.f, 0.f, 0.f};
                             mma_group_codes(d, make_uint2(q.x, q.y), make_uint2(q.z, q.w), hb);
                             affine_acc(acc[ch], d, s0, s1, sa, ba, sb, bb);

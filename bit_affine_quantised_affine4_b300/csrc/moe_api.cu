@@ -188,13 +188,14 @@ int decode_plan(const moe_layer_t *l, const float *x, int T, int flags, float *y
     long long smem = 0;
     for (; stages >= 2; stages--) {
         const long long red = (long long)(stages + 2) * kCW * nch * 512;  // gate/up partial-sum slots
-        smem = (long long)stages * a.SB + red + hsm;
+        smem = (long long)stages * a.SB + red + hsm + (long long)hsm_mats * Gi * 16 * 4;
         if (smem <= budget) break;
     }
     if (stages < 2) return MOE_EINVAL;
     a.stages = stages;
     a.red_off = stages * a.SB;
     a.hsm_off = a.red_off + (stages + 2) * kCW * nch * 512;
+    a.hsum_off = (int)(a.hsm_off + hsm);
     if (cfg.attr_smem[nch - 1][gpw - 1] < smem) {
         if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
             return cuda_status();
