@@ -38,6 +38,23 @@ SHARED_BYTES = 3 * IS * H * 36 // 64         # 10,036,224 B
 ROUTER_BYTES = E * H * 68 // 64              # 382,976 B at 8.5 bit/weight
 DECODE_BYTES = TOPK * EXPERT_BYTES + SHARED_BYTES + ROUTER_BYTES  # 37,182,464 B per token
 
+# DRAM traffic (read + write) of one k_decode launch at T = 1 from the ncu capture
+# summarised in profiles/k_decode_full_T1.md; reported only while the decode
+# kernel's sources are the ones it was taken on (their SHA-1 below)
+DECODE_NCU_TRAFFIC = {"sha1": "ad61ae78a5b85470ce5be571b92bc84656d36220", "bytes": 37_312_512}
+DECODE_SOURCES = ["bit_affine_quantised_affine4_b300/csrc/" + f for f in
+                  ("decode.cuh", "common.cuh", "mma_core.cuh", "route.cuh", "sync.cuh", "tile.cuh",
+                   "moe_api.cu")] + ["include/moe.h"]
+
+
+def decode_traffic():
+    import hashlib
+    h = hashlib.sha1()
+    for f in DECODE_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return DECODE_NCU_TRAFFIC["bytes"] if h.hexdigest() == DECODE_NCU_TRAFFIC["sha1"] else None
+
 
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -248,7 +265,7 @@ def run_ours(args):
                              "warm-up = W steps + one untimed replay of the timed graph",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": None,
+                     "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": decode_traffic(),
                      "peak_source": peaks["source"], "kernel": "moe_layer_decode (whole call)"},
         "e2e": {"value": world * args.steps / e2e_dt, "unit": "tok/s",
                 "h2d_bytes_per_step": H * 4, "d2h_bytes_per_step": H * 4,
