@@ -136,7 +136,7 @@ inline WsLayout ws_layout(const moe_layer_t &l, int Tmax) {
     W.gh = off;     off = up256(off + sizeof(float) * size_t(Tmax) * l.topk);
     W.decode_total = off;
     const int Rmax = prefill_rows(l, Tmax), T16 = (Tmax + 15) & ~15;
-    W.plan = off;   off = up256(off + sizeof(int) * (2 + 3 * MOE_MAX_EXPERTS + 2 * size_t(Rmax)));
+    W.plan = off;   off = up256(off + sizeof(int) * (2 + 3 * MOE_MAX_EXPERTS + 2 * size_t(Rmax) + MOE_MAX_EXPERTS + 1));
     W.Br = off;     off = up256(off + size_t(l.H / kGroup) * Rmax * 128);
     W.Bs = off;     off = up256(off + size_t(l.H / kGroup) * T16 * 128);
     W.Hr = off;     off = up256(off + size_t(l.I / kGroup) * Rmax * 128);

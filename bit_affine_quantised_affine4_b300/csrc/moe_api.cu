@@ -290,6 +290,7 @@ int run_layer_chunk(const moe_layer_t *l, const float *x, int T, int flags, floa
     plan.ucnt = plan.urow + MOE_MAX_EXPERTS;
     plan.rowtok = plan.ucnt + MOE_MAX_EXPERTS;
     plan.rowpair = plan.rowtok + Rmax;
+    plan.uslc = plan.rowpair + Rmax;
     k_prefill_plan<<<1, 256, 0, st>>>(ws.idx, T, l->E, l->topk, Rmax, plan);
     if ((rc = cuda_status())) return rc;
     const long long gthreads = (long long)(Rmax + T16) * (l->H / kGroup) * 8;
@@ -298,7 +299,7 @@ int run_layer_chunk(const moe_layer_t *l, const float *x, int T, int flags, floa
     if ((rc = cuda_status())) return rc;
     PrefillGemmArgs g;
     g.H = l->H; g.I = l->I; g.Is = l->Is; g.T = T; g.T16 = T16; g.Rmax = Rmax;
-    g.U = plan.U; g.uexp = plan.uexp; g.urow = plan.urow; g.ucnt = plan.ucnt; g.rowpair = plan.rowpair;
+    g.U = plan.U; g.uexp = plan.uexp; g.urow = plan.urow; g.ucnt = plan.ucnt; g.rowpair = plan.rowpair; g.uslc = plan.uslc;
     g.experts = (const uint8_t *)l->experts; g.stride = l->expert_stride; g.shared = (const uint8_t *)l->shared;
     g.Lr = tile_layout(l->H, l->I);
     g.Ls = tile_layout(l->H, l->Is);

@@ -45,7 +45,9 @@ constexpr int kPfDq = 8;             // dequant + epilogue warps (one weight til
 constexpr int kPfProducer = kPfDq, kPfMmaWarp = kPfDq + 1;
 constexpr int kPfThreads = (kPfDq + 2) * 32;
 constexpr int kPfRawA = 5120;        // eight 576-byte tiles, padded to 1024
-constexpr int kPfMaxN = 128;         // token rows of one item (<= MOE_MAX_PREFILL_TOKENS)
+constexpr int kPfMaxN = 128;         // token rows of one item (an expert with more tokens would be
+                                     // cut into slices of kPfMaxN rows; kPfMaxN-row slices with 8 stages
+                                     // measured slower: 358 vs 305 us per chunk)
 constexpr int kPfRaw = kPfRawA + kPfMaxN * 128;
 constexpr int kPfTileA = 128 * 128;  // dequantised A: 128 rows x 64 fp16
 constexpr int kPfTmemCols = 256;     // two fp32 accumulators of up to 128 columns
@@ -58,6 +60,8 @@ struct PfPlan {
     int *ucnt;     // [MOE_MAX_EXPERTS] tokens of the expert
     int *rowtok;   // [Rmax] token of each row, -1 = padding
     int *rowpair;  // [Rmax] pair t * topk + k of each row
+    int *uslc;     // [MOE_MAX_EXPERTS + 1] first kPfMaxN-token slice of each expert (prefix of
+                   // ceil(ucnt / kPfMaxN)); uslc[U] = all slices
 };
 
 __device__ __forceinline__ int round16(int n) { return (n + 15) & ~15; }
@@ -80,29 +84,39 @@ __global__ void __launch_bounds__(256) k_prefill_plan(const int *__restrict__ id
     // scans experts 32w..32w+31 (ballot + shuffle scan), then adds the totals of the
     // warps before it
     __shared__ unsigned wsum[MOE_MAX_EXPERTS / 32];  // experts << 16 | rows of the warp's 32 experts
+    __shared__ int wslc[MOE_MAX_EXPERTS / 32];       // kPfMaxN-token slices of the warp's experts
     __shared__ int ucnt_s[MOE_MAX_EXPERTS];
     __shared__ int U_s;
     const int warp = tid >> 5, lane = tid & 31, nw = (E + 31) >> 5;
-    int cnt = 0, incl = 0;
+    int cnt = 0, incl = 0, sincl = 0;
     unsigned bal = 0u;
     if (warp < nw) {
         const int e = 32 * warp + lane;
         cnt = e < E ? __popc(mask[e][0]) + __popc(mask[e][1]) + __popc(mask[e][2]) + __popc(mask[e][3]) : 0;
         bal = __ballot_sync(0xffffffffu, cnt > 0);
         incl = round16(cnt);
+        sincl = (cnt + kPfMaxN - 1) / kPfMaxN;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int v = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += v;
+            const int w = __shfl_up_sync(0xffffffffu, sincl, o);
+            if (lane >= o) {
+                incl += v;
+                sincl += w;
+            }
         }
-        if (lane == 31) wsum[warp] = ((unsigned)__popc(bal) << 16) | (unsigned)incl;
+        if (lane == 31) {
+            wsum[warp] = ((unsigned)__popc(bal) << 16) | (unsigned)incl;
+            wslc[warp] = sincl;
+        }
     }
     __syncthreads();
     if (warp < nw) {
-        int ub = 0, rb = 0;
+        int ub = 0, rb = 0, sb = 0;
         for (int w = 0; w < warp; w++) {
             ub += (int)(wsum[w] >> 16);
             rb += (int)(wsum[w] & 0xFFFFu);
+            sb += wslc[w];
         }
         const int e = 32 * warp + lane;
         if (e < E) uid[e] = -1;
@@ -112,6 +126,7 @@ __global__ void __launch_bounds__(256) k_prefill_plan(const int *__restrict__ id
             p.uexp[u] = e;
             p.ucnt[u] = cnt;
             p.urow[u] = row;
+            p.uslc[u] = sb + sincl - (cnt + kPfMaxN - 1) / kPfMaxN;
             urow_s[u] = row;
             ucnt_s[u] = cnt;
         }
@@ -120,6 +135,7 @@ __global__ void __launch_bounds__(256) k_prefill_plan(const int *__restrict__ id
             urow_s[U] = rows;
             p.U[0] = U;
             p.U[1] = rows;
+            p.uslc[U] = sb + sincl;
             U_s = U;
         }
     }
@@ -192,7 +208,7 @@ struct PrefillGemmArgs {
     int kind;  // 0: gate/up + GeGLU, 1: down
     int H, I, Is, T, T16, Rmax;
     const int *U;  // [0] distinct experts
-    const int *uexp, *urow, *ucnt, *rowpair;
+    const int *uexp, *urow, *ucnt, *rowpair, *uslc;
     const uint8_t *experts;
     size_t stride;
     const uint8_t *shared;
@@ -210,38 +226,58 @@ struct PfItem {
     int nkb;             // K steps (groups)
     const uint8_t *b;    // token tile rows of K step 0
     size_t b_kb;         // bytes between K steps of the token tiles
-    int n, N;            // valid token rows, padded (multiple of 16)
+    int n, N;            // valid token rows, padded (multiple of 16), of this kPfMaxN-row slice
+    int row0;            // first row of the slice (shared: token; routed: in the expert's segment)
     int mb;              // M block
     int u;               // routed expert, -1 = shared
 };
 
+// Items: [shared M block mb, slice sl] for mb < ms, sl < ceil(T / kPfMaxN); then per
+// distinct expert u, [M block mb, slice sl] for mb < mr, sl < its slices.
+__device__ __forceinline__ int pf_shared_slices(const PrefillGemmArgs &a) { return (a.T + kPfMaxN - 1) / kPfMaxN; }
+__device__ __forceinline__ int pf_items(const PrefillGemmArgs &a) {
+    const int ms = a.kind == 0 ? a.Is / 64 : a.H / 128, mr = a.kind == 0 ? a.I / 64 : a.H / 128;
+    return ms * pf_shared_slices(a) + mr * a.uslc[a.U[0]];
+}
 __device__ __forceinline__ PfItem pf_item(const PrefillGemmArgs &a, int i) {
     PfItem it;
     const int ms = a.kind == 0 ? a.Is / 64 : a.H / 128;  // shared M blocks
     const int mr = a.kind == 0 ? a.I / 64 : a.H / 128;   // routed M blocks per expert
-    if (i < ms) {
+    const int nss = pf_shared_slices(a);
+    if (i < ms * nss) {
+        const int mb = i / nss, sl = i - mb * nss;
         it.u = -1;
-        it.mb = i;
-        it.n = a.T;
-        it.N = a.T16;
-        it.b = a.kind == 0 ? a.Bs : a.Hs;
+        it.mb = mb;
+        it.row0 = sl * kPfMaxN;
+        it.n = min(kPfMaxN, a.T - it.row0);
+        it.N = round16(it.n);
+        it.b = (a.kind == 0 ? a.Bs : a.Hs) + (size_t)it.row0 * 128;
         it.b_kb = (size_t)a.T16 * 128;
         if (a.kind == 0) {
-            it.a = a.shared + (size_t)kTileBytes * (8 * i) * a.Ls.G;
+            it.a = a.shared + (size_t)kTileBytes * (8 * mb) * a.Ls.G;
             it.a_row = (size_t)kTileBytes * a.Ls.G;
             it.nkb = a.Ls.G;
         } else {
-            it.a = a.shared + a.Ls.gu_bytes + (size_t)kTileBytes * (8 * i) * a.Ls.Gi;
+            it.a = a.shared + a.Ls.gu_bytes + (size_t)kTileBytes * (8 * mb) * a.Ls.Gi;
             it.a_row = (size_t)kTileBytes * a.Ls.Gi;
             it.nkb = a.Ls.Gi;
         }
     } else {
-        const int u = (i - ms) / mr, mb = (i - ms) % mr;
+        // expert u: the last one with mr * uslc[u] <= j
+        const int j = i - ms * nss;
+        int lo = 0, hi = a.U[0] - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (mr * a.uslc[mid] <= j) lo = mid; else hi = mid - 1;
+        }
+        const int u = lo, ns = a.uslc[u + 1] - a.uslc[u], r = j - mr * a.uslc[u];
+        const int mb = r / ns, sl = r - mb * ns;
         it.u = u;
         it.mb = mb;
-        it.n = a.ucnt[u];
+        it.row0 = sl * kPfMaxN;
+        it.n = min(kPfMaxN, a.ucnt[u] - it.row0);
         it.N = round16(it.n);
-        it.b = (a.kind == 0 ? a.Br : a.Hr) + (size_t)a.urow[u] * 128;
+        it.b = (a.kind == 0 ? a.Br : a.Hr) + (size_t)(a.urow[u] + it.row0) * 128;
         it.b_kb = (size_t)a.Rmax * 128;
         const uint8_t *blob = a.experts + (size_t)a.uexp[u] * a.stride;
         if (a.kind == 0) {
@@ -257,8 +293,6 @@ __device__ __forceinline__ PfItem pf_item(const PrefillGemmArgs &a, int i) {
     return it;
 }
 
-// Dequantise 8 code nibbles (one word) into 4 fp16 pairs in operand order:
-// pair k holds columns (k, k+4) of the word's 8; w = s*q + b with one rounding.
 __device__ __forceinline__ uint4 deq_word(uint32_t w, __half2 s2, __half2 b2) {
     const uint32_t magic = 0x64006400u;  // fp16 1024 in both halves
     const __half2 k1024 = __halves2half2(__ushort_as_half((unsigned short)0x6400), __ushort_as_half((unsigned short)0x6400));
@@ -280,9 +314,30 @@ struct PfSmem {
     int err;
 };
 
-__global__ void __launch_bounds__(kPfThreads, 1) k_prefill_gemm(const PrefillGemmArgs a) {
+__global__ void __launch_bounds__(kPfThreads, 1) k_prefill_gemm(const PrefillGemmArgs ga) {
     extern __shared__ __align__(1024) uint8_t psm_raw[];
     __shared__ PfSmem S;
+    // the plan in shared memory: every item lookup reads it
+    __shared__ int pl_U[2], pl_uslc[MOE_MAX_EXPERTS + 1], pl_ucnt[MOE_MAX_EXPERTS], pl_urow[MOE_MAX_EXPERTS],
+        pl_uexp[MOE_MAX_EXPERTS];
+    {
+        const int U = ga.U[0];
+        if (threadIdx.x == 0) pl_U[0] = U;
+        for (int u = threadIdx.x; u <= U; u += blockDim.x) {
+            pl_uslc[u] = ga.uslc[u];
+            if (u < U) {
+                pl_ucnt[u] = ga.ucnt[u];
+                pl_urow[u] = ga.urow[u];
+                pl_uexp[u] = ga.uexp[u];
+            }
+        }
+    }
+    PrefillGemmArgs a = ga;
+    a.U = pl_U;
+    a.uslc = pl_uslc;
+    a.ucnt = pl_ucnt;
+    a.urow = pl_urow;
+    a.uexp = pl_uexp;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // 1024-aligned carve-up: raw stages | dequantised A stages | epilogue buffers
     uint8_t *base = psm_raw + ((1024u - (smem_addr(psm_raw) & 1023u)) & 1023u);
@@ -311,9 +366,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill_gemm(const PrefillGem
     tc_fence_after();
     const uint32_t tmem = S.tmem;
 
-    const int ms = a.kind == 0 ? a.Is / 64 : a.H / 128;
-    const int mr = a.kind == 0 ? a.I / 64 : a.H / 128;
-    const int NI = ms + a.U[0] * mr;
+    const int NI = pf_items(a);
     const int b = blockIdx.x, nC = gridDim.x;
     auto fail = [&]() {
         *err = 1;
@@ -455,8 +508,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill_gemm(const PrefillGem
                 }
                 named_sync(1, kPfDq * 32);
                 // the item's h rows: one K step (kb = mb) of the down operand
-                uint8_t *dst = (it.u < 0 ? a.Hs + (size_t)it.mb * a.T16 * 128
-                                         : a.Hr + ((size_t)it.mb * a.Rmax + a.urow[it.u]) * 128);
+                uint8_t *dst = (it.u < 0 ? a.Hs + ((size_t)it.mb * a.T16 + it.row0) * 128
+                                         : a.Hr + ((size_t)it.mb * a.Rmax + a.urow[it.u] + it.row0) * 128);
                 if (!*err)
                     for (int v = tid; v < it.N * 8; v += kPfDq * 32)
                         reinterpret_cast<uint4 *>(dst)[v] = reinterpret_cast<const uint4 *>(hst)[v];
@@ -471,9 +524,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill_gemm(const PrefillGem
                         const int jt = c0 + q;
                         if (jt < it.n) {
                             if (it.u < 0)
-                                a.Ys[(size_t)jt * a.H + n] = v[q];
+                                a.Ys[(size_t)(it.row0 + jt) * a.H + n] = v[q];
                             else
-                                a.Yr[(size_t)a.rowpair[a.urow[it.u] + jt] * a.H + n] = v[q];
+                                a.Yr[(size_t)a.rowpair[a.urow[it.u] + it.row0 + jt] * a.H + n] = v[q];
                         }
                     }
                 }
