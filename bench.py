@@ -41,7 +41,7 @@ DECODE_BYTES = TOPK * EXPERT_BYTES + SHARED_BYTES + ROUTER_BYTES  # 37,182,464 B
 # DRAM traffic (read + write) of one k_decode launch at T = 1 from the ncu capture
 # summarised in profiles/k_decode_full_T1.md; reported only while the decode
 # kernel's sources are the ones it was taken on (their SHA-1 below)
-DECODE_NCU_TRAFFIC = {"sha1": "ad61ae78a5b85470ce5be571b92bc84656d36220", "bytes": 37_312_512}
+DECODE_NCU_TRAFFIC = {"sha1": "72f7b28e717e7f96b8e2b1a63c84c52aae480d77", "bytes": 37_305_344}
 DECODE_SOURCES = ["bit_affine_quantised_affine4_b300/csrc/" + f for f in
                   ("decode.cuh", "common.cuh", "mma_core.cuh", "route.cuh", "sync.cuh", "tile.cuh",
                    "moe_api.cu")] + ["include/moe.h"]
@@ -78,8 +78,9 @@ class ClockSampler:
 
     def __enter__(self):
         try:
-            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
-            self.path = os.path.join(ROOT, "gpurun_out", "clocks_%d.csv" % os.getpid())
+            import tempfile
+            self.path = os.path.join(os.environ.get("MOE_BENCH_CLOCKS_DIR", tempfile.gettempdir()),
+                                     "moe_bench_clocks_%d.csv" % os.getpid())
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.dev), "--query-gpu=" + self.FIELDS,

@@ -578,7 +578,12 @@ int moe_layer_decode_host(const moe_layer_t *layer, const float *x_host, int T, 
         return cuda_status();
     if (gate_host && cudaMemcpyAsync(gate_host, ws.gh, sizeof(float) * rb, cudaMemcpyDeviceToHost, st) != cudaSuccess)
         return cuda_status();
-    if (cudaStreamSynchronize(st) != cudaSuccess) return cuda_status();
+    // wait for the stream by polling it: a decode step is a few tens of
+    // microseconds, shorter than the wake-up of a blocking wait
+    cudaError_t q;
+    while ((q = cudaStreamQuery(st)) == cudaErrorNotReady) {
+    }
+    if (q != cudaSuccess) return cuda_status();
     return MOE_OK;
 }
 

@@ -223,7 +223,8 @@ MOE_API int moe_layer_prefill_chunk(const moe_layer_t *layer, const float *x, in
  * works.  The call copies x into the workspace (which holds device staging for x,
  * y and the routing), runs the decode step on `stream` (through `cache` when it is
  * non-null), copies y and the requested routing back, and waits for `stream`
- * before it returns: the outputs are ready on return.  x_host and y_host must not
+ * (polling it, so the calling thread stays busy meanwhile) before it returns: the
+ * outputs are ready on return.  x_host and y_host must not
  * overlap.  Same workspace (moe_workspace_bytes) and error codes as
  * moe_layer_decode; MOE_ECUDA if a copy or the stream wait fails.
  */
