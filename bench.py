@@ -400,9 +400,37 @@ def stack_measurement(torch, moe, args, n_layers=30, steps=256, slots=16):
            "device_bytes_per_token": n_layers * DECODE_BYTES,
            "note": "host-synchronous per layer (routing copied to the host for the LFU policy); "
                    "misses copied on a side stream while the shared expert runs"}
+    out["h2d_link_probe_GB_s"] = h2d_link_probe(torch, caches[0].host_experts)
+    out["h2d_link_use"] = out["h2d_GB_s"] / max(out["h2d_link_probe_GB_s"]["expert_copies"], 1e-9)
     for c in caches:
         c.close()
     return out
+
+
+def h2d_link_probe(torch, host):
+    """Host -> device copy rate of this box's link, measured here: back-to-back
+    cudaMemcpyAsync copies from page-locked memory, (a) of one expert blob at a time
+    (what a cache miss copies), (b) of 64 MB at a time."""
+    blob = host.shape[1]
+    st = torch.cuda.Stream()
+    res = {}
+    for name, nbytes, reps in (("expert_copies", blob, 32), ("copies_64MB", 64 << 20, 8)):
+        src = host.view(-1)[:min(nbytes, host.numel())] if nbytes <= host.numel() else None
+        if src is None:
+            big = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+            src = big
+        dst = torch.empty(src.numel(), dtype=torch.uint8, device="cuda")
+        with torch.cuda.stream(st):
+            for _ in range(2):
+                dst.copy_(src, non_blocking=True)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            for _ in range(reps):
+                dst.copy_(src, non_blocking=True)
+            e1.record(st)
+        e1.synchronize()
+        res[name] = src.numel() * reps / (e0.elapsed_time(e1) * 1e-3) / 1e9
+    return res
 
 
 def run_prefill_only(args):
