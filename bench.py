@@ -398,8 +398,9 @@ def stack_measurement(torch, moe, args, n_layers=30, steps=256, slots=16):
            "misses_per_token": misses / n, "h2d_GB_s": h2d / dt / 1e9,
            "host_layers_distinct": n_host,
            "device_bytes_per_token": n_layers * DECODE_BYTES,
-           "note": "host-synchronous per layer (routing copied to the host for the LFU policy); "
-                   "misses copied on a side stream while the shared expert runs"}
+           "note": "per layer the router writes the routing into mapped host memory and a flag the "
+                   "host polls; the host runs the LFU policy; misses are copied on a side stream while "
+                   "the shared expert runs"}
     out["h2d_link_probe_GB_s"] = h2d_link_probe(torch, caches[0].host_experts)
     out["h2d_link_use"] = out["h2d_GB_s"] / max(out["h2d_link_probe_GB_s"]["expert_copies"], 1e-9)
     for c in caches:

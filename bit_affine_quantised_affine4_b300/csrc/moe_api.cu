@@ -4,6 +4,8 @@
 
 #include <cstdio>
 #include <cstring>
+#include <atomic>
+#include <chrono>
 #include <mutex>
 
 #include "common.cuh"
@@ -95,9 +97,10 @@ int bind_ws(const moe_layer_t *l, int T, void *d_ws, size_t ws_bytes, Ws *out, b
 }
 
 int launch_route(const moe_layer_t *l, const LayerDev &ly, const float *x, int T, Ws ws,
-                 int32_t *idx, float *gate, float *logits, cudaStream_t st) {
+                 int32_t *idx, float *gate, float *logits, cudaStream_t st, int32_t *idx_host = nullptr,
+                 unsigned *flag_host = nullptr, unsigned seq = 0) {
     const dim3 grid((l->E + kRouteExp - 1) / kRouteExp, (T + kRouteTok - 1) / kRouteTok);
-    k_route<<<grid, kRouteTok * 32, 0, st>>>(ly, x, T, ws, idx, gate, logits);
+    k_route<<<grid, kRouteTok * 32, 0, st>>>(ly, x, T, ws, idx, gate, logits, idx_host, flag_host, seq);
     return cuda_status();
 }
 
@@ -329,7 +332,10 @@ struct moe_cache {
     size_t blob, host_stride;
     const uint8_t *h_experts;
     uint8_t *d_slots = nullptr;
-    int32_t *h_idx = nullptr;  // page-locked copy of the step's routing
+    int32_t *h_idx = nullptr;  // page-locked, device-mapped: the step's routing (the router writes it)
+    int32_t *d_idx = nullptr;  // its device address
+    unsigned *h_flag = nullptr, *d_flag = nullptr;  // the router's per-call flag (after h_idx)
+    unsigned seq = 0;
     cudaStream_t side = nullptr;
     cudaEvent_t ev_idx = nullptr, ev_copies = nullptr;
     moe::LfuPolicy policy;
@@ -342,16 +348,17 @@ namespace {
 void cache_free(moe_cache *c) {
     if (!c) return;
     if (c->d_slots) cudaFree(c->d_slots);
-    if (c->h_idx) cudaFreeHost(c->h_idx);
+    if (c->h_idx) cudaFreeHost(c->h_idx);  // h_flag lives in the same allocation
     if (c->ev_idx) cudaEventDestroy(c->ev_idx);
     if (c->ev_copies) cudaEventDestroy(c->ev_copies);
     if (c->side) cudaStreamDestroy(c->side);
     delete c;
 }
 
-// Decode through a cache: router launch, host copy of the routing (the host
-// waits for it), LFU step, copies of the missing experts on the side stream,
-// then the shared expert (overlapping the copies) and the routed experts.
+// Decode through a cache: router launch (it writes the routing into mapped host
+// memory and then a per-call flag, which the host polls), LFU step, copies of the
+// missing experts on the side stream, then the shared expert (overlapping the
+// copies) and the routed experts.
 int run_decode_cached(const moe_layer_t *l, const float *x, int T, int flags, float *y, int32_t *idx_out,
                       float *gate_out, moe_cache *c, void *d_ws, size_t ws_bytes, void *stream) {
     if (c->H != l->H || c->E != l->E || c->I != l->I) return MOE_EINVAL;
@@ -363,11 +370,22 @@ int run_decode_cached(const moe_layer_t *l, const float *x, int T, int flags, fl
     if (rc) return rc;
     cudaStream_t st = as_stream(stream);
     LayerDev ly = layer_dev(l);
-    if ((rc = launch_route(l, ly, x, T, ws, ws.idx, ws.gate, nullptr, st))) return rc;
+    const unsigned seq = ++c->seq == 0 ? ++c->seq : c->seq;  // never 0 (the flag's initial value)
+    if ((rc = launch_route(l, ly, x, T, ws, ws.idx, ws.gate, nullptr, st, c->d_idx, c->d_flag, seq))) return rc;
     const int P2 = T * l->topk;
-    if (cudaMemcpyAsync(c->h_idx, ws.idx, sizeof(int32_t) * P2, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
-        cudaEventRecord(c->ev_idx, st) != cudaSuccess || cudaEventSynchronize(c->ev_idx) != cudaSuccess)
-        return cuda_status();
+    {
+        // the router's flag (bounded: 5 s; a failed stream ends the wait at once)
+        volatile unsigned *flag = c->h_flag;
+        const auto t0 = std::chrono::steady_clock::now();
+        for (unsigned spin = 0; *flag != seq; spin++) {
+            if ((spin & 1023u) == 1023u) {
+                const cudaError_t q = cudaStreamQuery(st);
+                if (q != cudaSuccess && q != cudaErrorNotReady) return cuda_status();
+                if (std::chrono::steady_clock::now() - t0 > std::chrono::seconds(5)) return MOE_ETIMEOUT;
+            }
+        }
+        std::atomic_thread_fence(std::memory_order_acquire);
+    }
     int32_t req[kMaxPairs], slot[kMaxPairs];
     uint8_t hit[kMaxPairs];
     int n = 0;
@@ -647,7 +665,10 @@ int moe_cache_create(moe_cache_t **out, int H, int E, int I, const void *h_exper
     c->h_experts = (const uint8_t *)h_experts;
     if (cudaGetDevice(&c->device) != cudaSuccess ||
         cudaMalloc((void **)&c->d_slots, blob * (size_t)slots) != cudaSuccess ||
-        cudaMallocHost((void **)&c->h_idx, sizeof(int32_t) * kMaxPairs) != cudaSuccess ||
+        cudaHostAlloc((void **)&c->h_idx, sizeof(int32_t) * kMaxPairs + 64, cudaHostAllocMapped) != cudaSuccess ||
+        (c->h_flag = reinterpret_cast<unsigned *>(c->h_idx + kMaxPairs), *c->h_flag = 0u, false) ||
+        cudaHostGetDevicePointer((void **)&c->d_idx, c->h_idx, 0) != cudaSuccess ||
+        (c->d_flag = reinterpret_cast<unsigned *>(c->d_idx + kMaxPairs), false) ||
         cudaStreamCreateWithFlags(&c->side, cudaStreamNonBlocking) != cudaSuccess ||
         cudaEventCreateWithFlags(&c->ev_idx, cudaEventDisableTiming) != cudaSuccess ||
         cudaEventCreateWithFlags(&c->ev_copies, cudaEventDisableTiming) != cudaSuccess) {

@@ -157,10 +157,12 @@ __device__ __forceinline__ void router_dot_rows(const uint32_t *rq, const __half
 
 // CTA (r, g): router rows 4r..4r+3 for tokens 16g..16g+15, one warp per token
 // over the whole rows.  The last CTA of token group g (a ticket per group) ranks
-// the group's tokens, one warp per token.
+// the group's tokens, one warp per token.  When idx_host is set (page-locked host
+// memory mapped into the device's address space) the group's choices also go
+// there, followed by flag_host[g] = seq once they are visible to the host.
 __global__ void __launch_bounds__(kRouteTok * 32)
 k_route(LayerDev ly, const float *__restrict__ x, int T, Ws ws, int32_t *idx_out, float *gate_out,
-        float *logits_out) {
+        float *logits_out, int32_t *idx_host, unsigned *flag_host, unsigned seq) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int e0 = blockIdx.x * kRouteExp, t = blockIdx.y * kRouteTok + warp;
     if (t < T) {
@@ -188,8 +190,16 @@ k_route(LayerDev ly, const float *__restrict__ x, int T, Ws ws, int32_t *idx_out
     __threadfence();
     if (t < T)
         warp_topk_softmax(ws.logits + (size_t)t * ly.E, ly.E, ly.topk, idx_out + t * ly.topk,
-                          gate_out + t * ly.topk, nullptr, nullptr);
+                          gate_out + t * ly.topk, idx_host ? idx_host + t * ly.topk : nullptr, nullptr);
     if (threadIdx.x == 0) ws.ticket[blockIdx.y] = 0u;
+    if (idx_host) {
+        __threadfence_system();
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            __threadfence_system();
+            *(volatile unsigned *)(flag_host + blockIdx.y) = seq;
+        }
+    }
 }
 
 }  // namespace moe
