@@ -337,7 +337,7 @@ struct moe_cache {
     unsigned *h_flag = nullptr, *d_flag = nullptr;  // the router's per-call flag (after h_idx)
     unsigned seq = 0;
     cudaStream_t side = nullptr;
-    cudaEvent_t ev_idx = nullptr, ev_copies = nullptr;
+    cudaEvent_t ev_copies = nullptr;
     moe::LfuPolicy policy;
     uint64_t h2d_bytes = 0;
     moe_cache(int slots_, int E_) : policy(slots_, E_) {}
@@ -349,7 +349,6 @@ void cache_free(moe_cache *c) {
     if (!c) return;
     if (c->d_slots) cudaFree(c->d_slots);
     if (c->h_idx) cudaFreeHost(c->h_idx);  // h_flag lives in the same allocation
-    if (c->ev_idx) cudaEventDestroy(c->ev_idx);
     if (c->ev_copies) cudaEventDestroy(c->ev_copies);
     if (c->side) cudaStreamDestroy(c->side);
     delete c;
@@ -663,18 +662,22 @@ int moe_cache_create(moe_cache_t **out, int H, int E, int I, const void *h_exper
     c->blob = blob;
     c->host_stride = host_stride;
     c->h_experts = (const uint8_t *)h_experts;
-    if (cudaGetDevice(&c->device) != cudaSuccess ||
-        cudaMalloc((void **)&c->d_slots, blob * (size_t)slots) != cudaSuccess ||
-        cudaHostAlloc((void **)&c->h_idx, sizeof(int32_t) * kMaxPairs + 64, cudaHostAllocMapped) != cudaSuccess ||
-        (c->h_flag = reinterpret_cast<unsigned *>(c->h_idx + kMaxPairs), *c->h_flag = 0u, false) ||
-        cudaHostGetDevicePointer((void **)&c->d_idx, c->h_idx, 0) != cudaSuccess ||
-        (c->d_flag = reinterpret_cast<unsigned *>(c->d_idx + kMaxPairs), false) ||
-        cudaStreamCreateWithFlags(&c->side, cudaStreamNonBlocking) != cudaSuccess ||
-        cudaEventCreateWithFlags(&c->ev_idx, cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventCreateWithFlags(&c->ev_copies, cudaEventDisableTiming) != cudaSuccess) {
+    // the routing buffer and, after it, the router's flag: page-locked, mapped
+    const size_t idx_bytes = sizeof(int32_t) * kMaxPairs + 64;
+    bool ok = cudaGetDevice(&c->device) == cudaSuccess &&
+              cudaMalloc((void **)&c->d_slots, blob * (size_t)slots) == cudaSuccess &&
+              cudaHostAlloc((void **)&c->h_idx, idx_bytes, cudaHostAllocMapped) == cudaSuccess &&
+              cudaHostGetDevicePointer((void **)&c->d_idx, c->h_idx, 0) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&c->side, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaEventCreateWithFlags(&c->ev_copies, cudaEventDisableTiming) == cudaSuccess;
+    if (!ok) {
         cache_free(c);
-        return cuda_status() ? MOE_ECUDA : MOE_ECUDA;
+        (void)cudaGetLastError();
+        return MOE_ECUDA;
     }
+    c->h_flag = reinterpret_cast<unsigned *>(c->h_idx + kMaxPairs);
+    c->d_flag = reinterpret_cast<unsigned *>(c->d_idx + kMaxPairs);
+    *c->h_flag = 0u;
     *out = c;
     return MOE_OK;
 }
