@@ -194,8 +194,9 @@ typedef struct moe_cache moe_cache_t;
  * for all the tokens that chose it.  x, y: device fp32 [T][H] (y must not alias
  * x).  idx_out / gate_out: optional device outputs [T][topk].
  * cache == NULL: experts come from layer->experts; the call does not synchronise.
- * cache != NULL: experts come from the cache's device slots; the call copies the
- *   routing to the host, synchronises on it, runs the LFU policy, issues the
+ * cache != NULL: experts come from the cache's device slots; the router writes the
+ *   routing into page-locked host memory mapped for the device and the call waits
+ *   for it (polling; MOE_ETIMEOUT after 5 s), runs the LFU policy, issues the
  *   missing experts' host->device copies on the cache's side stream while the
  *   shared expert runs on `stream`, and then computes the routed experts.  It
  *   returns once all work is enqueued (not finished).  MOE_ECAPACITY if the
