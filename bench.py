@@ -166,9 +166,31 @@ def build_layer(moe, copies, bias=None):
                           bias=bias, copies=copies)
 
 
+def ranks_barrier(torch):
+    """Barrier over the ranks of the process group (no-op without one)."""
+    import torch.distributed as td
+    if td.is_available() and td.is_initialized():
+        td.barrier()
+
+
+def max_over_ranks(torch, value, device="cpu"):
+    """The largest of every rank's value (the value itself without a process group)."""
+    import torch.distributed as td
+    if not (td.is_available() and td.is_initialized()):
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    td.all_reduce(t, op=td.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world, steps, seconds):
+    """Whole-job throughput: every rank processes `steps` units in at most `seconds`."""
+    return world * steps / seconds
+
+
 def time_graph(torch, fn_steps, K, W):
     """Capture K steps (and W warm-up steps) as CUDA graphs; time the K-step replay
-    with CUDA events on the capturing stream."""
+    with CUDA events on the capturing stream, between barriers over the ranks."""
     st = torch.cuda.Stream()
     torch.cuda.synchronize()
     gW, gK = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
@@ -183,6 +205,7 @@ def time_graph(torch, fn_steps, K, W):
         gW.replay()
         gK.replay()  # untimed replay: uploads the timed graph
     torch.cuda.synchronize()
+    ranks_barrier(torch)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(st):
         ev0.record(st)
@@ -190,6 +213,7 @@ def time_graph(torch, fn_steps, K, W):
         ev1.record(st)
     ev1.synchronize()
     torch.cuda.synchronize()
+    ranks_barrier(torch)
     return ev0.elapsed_time(ev1) / 1e3
 
 
@@ -227,12 +251,9 @@ def run_ours(args):
     with ClockSampler(torch.cuda.current_device()) as clk:
         dt = time_graph(torch, decode_steps, args.steps, args.warmup)
     clocks = clk.summary()
-    if dist:
-        t = torch.tensor([dt], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        dt = float(t.item())
+    dt = max_over_ranks(torch, dt, dev)
     per_step = dt / args.steps
-    value = world * args.steps / dt  # tokens/s over all ranks (one token per step per rank)
+    value = job_rate(world, args.steps, dt)  # tokens/s over all ranks (one token per step per rank)
     achieved_gbs = DECODE_BYTES / per_step / 1e9
 
     # ---- end to end through the public API with host buffers: one
@@ -249,9 +270,13 @@ def run_ours(args):
 
     e2e_steps(args.warmup, 0)
     torch.cuda.synchronize()
+    ranks_barrier(torch)
     t0 = time.perf_counter()
     e2e_steps(args.steps, args.warmup)
+    torch.cuda.synchronize()
     e2e_dt = time.perf_counter() - t0
+    ranks_barrier(torch)
+    e2e_dt = max_over_ranks(torch, e2e_dt, dev)
 
     extra = {}
     if not args.quick and rank == 0:
@@ -278,7 +303,7 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": decode_traffic(),
                      "peak_source": peaks["source"], "kernel": "moe_layer_decode (whole call)"},
-        "e2e": {"value": world * args.steps / e2e_dt, "unit": "tok/s",
+        "e2e": {"value": job_rate(world, args.steps, e2e_dt), "unit": "tok/s",
                 "h2d_bytes_per_step": H * 4, "d2h_bytes_per_step": H * 4,
                 "note": "moe_layer_decode_host through the Python binding, one call per step: "
                         "H2D of x from pinned memory + decode + D2H of y + stream wait"},
