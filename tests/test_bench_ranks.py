@@ -60,3 +60,18 @@ def test_helpers_without_process_group():
     bench.ranks_barrier(torch)  # no-op
     assert bench.max_over_ranks(torch, 2.5) == 2.5
     assert bench.job_rate(1, 10, 0.5) == 20.0
+
+
+def test_traffic_hash_ignores_comments_only(tmp_path, monkeypatch):
+    # the captured DRAM traffic is reported only while the decode sources match the
+    # capture: a comment or blank-space edit keeps the hash, a code edit changes it
+    import bench
+    src = tmp_path / "k.cuh"
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "DECODE_SOURCES", ["k.cuh"])
+    src.write_text("int f(int x) { return x + 1; }  // one\n")
+    h0 = bench.decode_sources_sha1()
+    src.write_text("/* doc */\nint f(int x)  {\n  return x + 1;\n}  // two\n")
+    assert bench.decode_sources_sha1() == h0
+    src.write_text("int f(int x) { return x + 2; }\n")
+    assert bench.decode_sources_sha1() != h0
