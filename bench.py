@@ -493,6 +493,31 @@ def run_prefill_only(args):
                       "us_per_chunk": us, "tok_s": 128e6 / us, "note": "single layer, weights may sit in L2"}))
 
 
+def run_decode_only(args):
+    """Decode steps of T tokens on the full-size layer with Zipf(1.1) routing,
+    rotating over 2 layer copies, K times after W warm-ups (a short case for
+    profilers: the batch sweep's configuration at one T)."""
+    import torch
+    import bit_affine_quantised_affine4_b300 as moe
+    s, T = synth.FULL, args.decode_only
+    layer = build_layer(moe, 2, bias=synth.popularity_bias(s, seed=0))
+    views = [layer.view(c) for c in range(2)]
+    x = torch.from_numpy(synth.tokens(s, T, seed=0, stream=3000 + T)).cuda()
+    ws = moe.new_workspace(views[0], T)
+    for i in range(args.warmup):
+        moe.moe_layer_decode(views[i % 2], x, ws)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(args.steps):
+        moe.moe_layer_decode(views[i % 2], x, ws)
+    e1.record()
+    e1.synchronize()
+    us = e0.elapsed_time(e1) * 1000 / args.steps
+    print(json.dumps({"workload": "decode, %d tokens, full-size layer, Zipf(1.1)" % T, "us_per_step": us,
+                      "note": "eager launches, 2 layer copies (weights may sit in L2)"}))
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -524,6 +549,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--prefill-only", action="store_true",
                     help="only the 128-token prefill chunk of one layer (for profilers)")
+    ap.add_argument("--decode-only", type=int, default=0, metavar="T",
+                    help="only decode steps of T tokens with Zipf routing on one layer (for profilers)")
     ap.add_argument("--stack", action=argparse.BooleanOptionalAction, default=True,
                     help="also run the 30-layer stack decode with per-layer LFU caches")
     ap.add_argument("--copies", type=int, default=0,
@@ -531,8 +558,12 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.decode_only and not 1 <= args.decode_only <= 16:
+        ap.error("--decode-only takes 1..16 tokens")
     if args.prefill_only:
         run_prefill_only(args)
+    elif args.decode_only:
+        run_decode_only(args)
     elif args.impl == "reference":
         run_reference(args)
     else:
