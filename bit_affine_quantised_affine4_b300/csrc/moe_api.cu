@@ -218,7 +218,7 @@ int decode_plan(const moe_layer_t *l, const float *x, int T, int flags, float *y
 // for it (griddepcontrol.wait).  If the runtime refuses the combination, the
 // plain cooperative launch is used from then on.
 int decode_launch(DecodePlan &plan, int mode, void *stream) {
-    static int pdl_ok = 1;
+    static std::atomic<int> pdl_ok{1};  // shared by every calling thread
     plan.a.mode = mode;
     void *args[] = {&plan.a};
     if (pdl_ok) {
@@ -238,7 +238,7 @@ int decode_launch(DecodePlan &plan, int mode, void *stream) {
         if (e == cudaSuccess) return MOE_OK;
         if (e != cudaErrorInvalidValue && e != cudaErrorNotSupported) return cuda_status();
         (void)cudaGetLastError();
-        pdl_ok = 0;
+        pdl_ok.store(0);
     }
     if (cudaLaunchCooperativeKernel(plan.fn, dim3(plan.nC), dim3(kDecThreads), args, (size_t)plan.smem,
                                     as_stream(stream)) != cudaSuccess)
