@@ -24,9 +24,10 @@
 //   phase B  gate/up: the CTA's tiles j = b, b+nC, ... of [shared | routed u=0..U-1]
 //            (one tile = 8 gate rows + the 8 matching up rows, full K); the shared
 //            ones are already in the ring while the routed ones are copied.  The
-//            warps split K; the last warp to finish a tile adds the partial sums
-//            up, applies GeGLU and writes h in fp16 (compact slots for routed
-//            experts).
+//            warps split K and leave their partial sums in shared memory; a tile
+//            is reduced (GeGLU, h written in fp16, compact slots for routed
+//            experts) by the first warp that finds it complete after its next
+//            tile, the CTA's last tile by its last arriver.
 //            down: units (matrix, 16 output rows) in matrix-major order, a
 //            contiguous range per CTA, one unit per warp with full K; h of the
 //            CTA's matrices is copied to shared memory once every CTA's gate/up
