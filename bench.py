@@ -38,9 +38,10 @@ SHARED_BYTES = 3 * IS * H * 36 // 64         # 10,036,224 B
 ROUTER_BYTES = E * H * 68 // 64              # 382,976 B at 8.5 bit/weight
 DECODE_BYTES = TOPK * EXPERT_BYTES + SHARED_BYTES + ROUTER_BYTES  # 37,182,464 B per token
 
-# DRAM traffic (read + write) of one k_decode launch at T = 1 from the ncu capture
-# summarised in profiles/k_decode_full_T1.md; reported only while the decode
-# kernel's sources are the ones it was taken on (their SHA-1 without comments)
+# DRAM traffic (read + write) of one decode launch at T = 1 from an ncu capture of
+# `bench.py --quick` (dram__bytes_read.sum + dram__bytes_write.sum); reported only
+# while the decode kernel's sources are the ones it was taken on (their SHA-1
+# without comments)
 DECODE_NCU_TRAFFIC = {"sha1": "5d0fe9df0ac397459068a5379ca49695c60c5d89", "bytes": 37_345_792}
 DECODE_SOURCES = ["bit_affine_quantised_affine4_b300/csrc/" + f for f in
                   ("decode.cuh", "common.cuh", "mma_core.cuh", "route.cuh", "sync.cuh", "tile.cuh",
@@ -141,28 +142,65 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- oracle (CPU) leg
-def oracle_decode_rate(seconds=15.0, max_tokens=64):
+def cpu_model():
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def _omp():
+    """The OpenMP runtime the oracle library runs on (to set its thread count)."""
+    import ctypes
+    try:
+        return ctypes.CDLL("libgomp.so.1")
+    except OSError:
+        return None
+
+
+def oracle_decode_rate(seconds=15.0, max_tokens=64, single_tokens=3):
     """The oracle as it stands: full-size layer, one token per call, timed on the
-    host cores over a bounded sample of tokens."""
+    host cores over a bounded sample of tokens (each call timed on its own; the
+    rate is 1 / median).  A single-thread figure comes from a few more calls with
+    the OpenMP runtime set to one thread."""
     sys.path.insert(0, os.path.join(ROOT, "tests"))
     from layers import OracleLayer  # test-side builder around the oracle
     s = synth.FULL
     ol = OracleLayer(s, seed=0)
-    x = synth.tokens(s, max_tokens, seed=0, stream=9000)
+    n_all = max_tokens + single_tokens
+    x = synth.tokens(s, n_all, seed=0, stream=9000)
     # route everything first so expert quantisation (data preparation) is untimed
-    for t in range(max_tokens):
+    for t in range(n_all):
         _, idx, _ = ol.route(x[t:t + 1])
         for e in np.unique(idx):
             ol.expert(int(e))
-    n = 0
+    omp = _omp()
+    cores = omp.omp_get_max_threads() if omp else int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    times = []
     t0 = time.perf_counter()
-    while n < max_tokens and time.perf_counter() - t0 < seconds:
-        ol.layer(x[n:n + 1])
-        n += 1
-    dt = time.perf_counter() - t0
-    cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
-    return {"value": n / dt, "unit": "tok/s", "cores": cores, "kind": "oracle",
-            "sample": "%d decode tokens of the full-size layer (uniform routing), %.1f s" % (n, dt)}
+    while len(times) < max_tokens and (len(times) < 3 or time.perf_counter() - t0 < seconds):
+        t1 = time.perf_counter()
+        ol.layer(x[len(times):len(times) + 1])
+        times.append(time.perf_counter() - t1)
+    single = None
+    if omp:
+        omp.omp_set_num_threads(1)
+        st = []
+        for t in range(single_tokens):
+            t1 = time.perf_counter()
+            ol.layer(x[max_tokens + t:max_tokens + t + 1])
+            st.append(time.perf_counter() - t1)
+        omp.omp_set_num_threads(cores)
+        single = 1.0 / statistics.median(st)
+    med = statistics.median(times)
+    return {"value": 1.0 / med, "unit": "tok/s", "cores": cores, "kind": "oracle",
+            "cpu_model": cpu_model(), "single_thread_tok_s": single,
+            "sample": "%d decode tokens of the full-size layer (uniform routing), each timed alone, "
+                      "rate = 1 / median (%.1f ms); single thread: median of %d more tokens"
+                      % (len(times), med * 1e3, single_tokens)}
 
 
 # ---------------------------------------------------------------- GPU leg
@@ -297,7 +335,9 @@ def run_ours(args):
         "metric": "MoE decode tokens/s (one full-size layer, T=1) and % of B300 HBM roofline; prefill-chunk tok/s",
         "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": per_step * 1e3, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "u4 weights (affine g64), f32 accumulate",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "u4 weights (affine g64, fp16 scale/bias), u8 router; fp16 activations (x, h) "
+                 "as tensor-core operands, f32 accumulate",
         "data": "synthetic: weights N(0,0.02) quantised 4-bit g64 (router 8-bit g64), tokens N(0,1), seed 0",
         "config": {"workload": "moe_layer_decode, hidden 2816, 128 experts top-8, inter 704, shared 2112, "
                                "GeGLU, T=1, uniform router logits",
@@ -327,6 +367,14 @@ def run_ours(args):
         torch.distributed.destroy_process_group()
 
 
+def unique_experts(idx, written):
+    """Mean number of distinct experts per step over the routing rows the steps
+    wrote (row i % NX for steps i = 0 .. written - 1; the others were never run)."""
+    rows = idx[:min(idx.shape[0], written)].cpu().numpy()
+    assert (rows >= 0).all(), "a routing row the steps should have written is unset"
+    return float(np.mean([len(np.unique(r)) for r in rows]))
+
+
 def side_measurements(torch, moe, layer, copies, ws, args):
     """Decode batch sweep and the 128-token prefill chunk, both with Zipf(1.1)
     popularity (router logit bias), timed the same way as the headline."""
@@ -340,7 +388,7 @@ def side_measurements(torch, moe, layer, copies, ws, args):
         NX = 32
         X = torch.from_numpy(synth.tokens(s, NX * T, seed=0, stream=1000 + T)).to(dev).view(NX, T, H)
         Y = torch.empty_like(X)
-        idx = torch.empty((NX, T, TOPK), dtype=torch.int32, device=dev)
+        idx = torch.full((NX, T, TOPK), -1, dtype=torch.int32, device=dev)
 
         def steps(n, first):
             for i in range(first, first + n):
@@ -348,7 +396,7 @@ def side_measurements(torch, moe, layer, copies, ws, args):
 
         K = max(20, args.steps // 4)
         dt = time_graph(torch, steps, K, args.warmup)
-        U = float(np.mean([len(np.unique(idx[j].cpu().numpy())) for j in range(NX)]))
+        U = unique_experts(idx, args.warmup + K)
         bytes_step = U * EXPERT_BYTES + SHARED_BYTES + ROUTER_BYTES
         sweep.append({"T": T, "tok_s": K * T / dt, "us_per_step": dt / K * 1e6, "unique_experts": U,
                       "GB_s": bytes_step / (dt / K) / 1e9})
@@ -358,7 +406,7 @@ def side_measurements(torch, moe, layer, copies, ws, args):
     NX = 4
     X = torch.from_numpy(synth.tokens(s, NX * T, seed=0, stream=2000)).to(dev).view(NX, T, H)
     Y = torch.empty_like(X)
-    idx = torch.empty((NX, T, TOPK), dtype=torch.int32, device=dev)
+    idx = torch.full((NX, T, TOPK), -1, dtype=torch.int32, device=dev)
 
     def psteps(n, first):
         for i in range(first, first + n):
@@ -366,7 +414,7 @@ def side_measurements(torch, moe, layer, copies, ws, args):
 
     K = 10
     dt = time_graph(torch, psteps, K, args.warmup)
-    U = float(np.mean([len(np.unique(idx[j].cpu().numpy())) for j in range(NX)]))
+    U = unique_experts(idx, args.warmup + K)
     bytes_step = U * EXPERT_BYTES + SHARED_BYTES + ROUTER_BYTES
     flops = 2 * T * (TOPK * 3 * I * H + 3 * IS * H + E * H)
     out["prefill_chunk_zipf"] = {"T": T, "tok_s": K * T / dt, "us_per_chunk": dt / K * 1e6,

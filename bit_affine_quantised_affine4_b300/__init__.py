@@ -17,6 +17,8 @@ from . import build as _build
 
 MOE_OK, MOE_EINVAL, MOE_ECUDA, MOE_ECAPACITY, MOE_ETIMEOUT, MOE_EWORKSPACE, MOE_ENOTREADY = range(7)
 MOE_RESIDUAL = 1
+MOE_INJECT_NONE, MOE_INJECT_WAIT, MOE_INJECT_COPY = range(3)
+MOE_NOALLOC_SCRATCH_BYTES = 4 << 20
 MOE_MAX_TOPK = 8
 MOE_MAX_EXPERTS = 256
 MOE_MAX_DECODE_TOKENS = 16
@@ -32,6 +34,7 @@ ENTRY_POINTS = (
     "moe_layer_prefill_chunk", "moe_cache_create", "moe_cache_destroy",
     "moe_cache_slots", "moe_cache_stats", "moe_layer_decode_noalloc", "moe_layer_decode_host",
     "moe_lfu_create", "moe_lfu_destroy", "moe_lfu_step", "moe_lfu_state",
+    "moe_decode_workspace_bytes", "moe_noalloc_status", "moe_debug_inject",
 )
 
 
@@ -85,9 +88,13 @@ def _load():
     L.moe_lfu_destroy.argtypes = [p]
     L.moe_lfu_step.argtypes = [p, p, i, p, p]
     L.moe_lfu_state.argtypes = [p, p, p, p, p, p]
+    L.moe_decode_workspace_bytes.argtypes = [p, i]
+    L.moe_decode_workspace_bytes.restype = sz
+    L.moe_noalloc_status.argtypes = [p]
+    L.moe_debug_inject.argtypes = [i]
     for name in ENTRY_POINTS:
         if name not in ("moe_status_string", "moe_expert_blob_bytes", "moe_workspace_bytes",
-                        "moe_tile_blob_bytes"):
+                        "moe_tile_blob_bytes", "moe_decode_workspace_bytes"):
             getattr(L, name).restype = i
     return L
 
@@ -160,6 +167,18 @@ def qgemv_affine4(q, s, b, K: int, x, y=None, stream=None):
 
 def moe_workspace_bytes(layer: moe_layer_t, T_max: int) -> int:
     return int(lib.moe_workspace_bytes(C.byref(layer), T_max))
+
+
+def moe_decode_workspace_bytes(layer: moe_layer_t, T_max: int) -> int:
+    return int(lib.moe_decode_workspace_bytes(C.byref(layer), T_max))
+
+
+def moe_noalloc_status(stream=None) -> int:
+    return int(lib.moe_noalloc_status(_stream(stream)))
+
+
+def moe_debug_inject(what: int):
+    _check(lib.moe_debug_inject(int(what)), "moe_debug_inject")
 
 
 def moe_workspace_init(ws: torch.Tensor, stream=None):

@@ -95,6 +95,10 @@ struct DecodeArgs {
     const float *gate_pre;   // [T][topk]
     int use_map;             // expert e's blob is experts + slot_map[e] * stride (cache slots)
     short slot_map[MOE_MAX_EXPERTS];
+    // fault injection (tests of the error path): extra router rows the routing
+    // wait expects (0 normally; > 0 makes it unreachable) and that wait's limit
+    unsigned route_extra;
+    unsigned long long route_wait_ns;
 };
 
 // x / d for x < 2^24 and 1 <= d <= 256: magic = 0xFFFFFFFF / d + 1 (d > 1), exact
@@ -425,7 +429,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
                 if (lane == 0) atomicAdd(&a.ctrl[kRouteCnt], (unsigned)j);
             }
         }
-        if (lane == 0 && !pre && !spin_reach(&a.ctrl[kRouteCnt], base.x, (unsigned)a.E, &a.ctrl[kErr]))
+        if (lane == 0 && !pre &&
+            !spin_reach(&a.ctrl[kRouteCnt], base.x, (unsigned)a.E + a.route_extra, &a.ctrl[kErr], a.route_wait_ns))
             *err = 1;
         __syncwarp();
         // the routing (an earlier launch's choices, or every token's logits) into
@@ -534,6 +539,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
             // down units: the first `stages` stages now; h of this CTA's matrices once
             // every gate/up tile of the layer is done; then the remaining stages
             const int early = min(nstg, a.stages);
+            bool h_armed = false;                      // the h copies were issued
             int um = m_first, ur = ulo - m_first * R;  // (matrix, row tile) of the next unit
 #pragma unroll 1
             for (int k = 0; k <= nstg; k++) {
@@ -554,6 +560,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
                         // the arrival (with the byte count) comes after the copies: the
                         // phase cannot complete before it
                         mbar_arrive_expect_tx(&S.hbar, bytes);
+                        h_armed = true;
                     }
                 }
                 if (k == nstg) break;
@@ -582,7 +589,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
             volatile int never = 0;
             for (int s = 0; s < a.stages; s++)
                 if (last_fill[s] >= 0) mbar_wait(&S.full[s], (last_fill[s] / a.stages) & 1, &never);
-            if (nunits > 0) mbar_wait(&S.hbar, 0, &never);
+            if (h_armed) mbar_wait(&S.hbar, 0, &never);
             // every CTA has read the bases (all gate/up tiles are counted): the next
             // call's bases
             if (b == 0) {

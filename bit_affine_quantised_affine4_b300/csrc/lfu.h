@@ -80,6 +80,16 @@ public:
         return 0;
     }
 
+    // Marks slot s empty (its contents are no longer known): the expert it held,
+    // if any, is no longer resident.  Counts and totals are otherwise unchanged.
+    void invalidate(int s) {
+        if (s < 0 || s >= slots_ || expert_[s] < 0) return;
+        where_[expert_[s]] = -1;
+        expert_[s] = -1;
+        count_[s] = 0;
+        last_[s] = 0;
+    }
+
 private:
     int victim() const {
         for (int s = 0; s < slots_; s++)

@@ -23,6 +23,16 @@ namespace {
 
 cudaStream_t as_stream(void *s) { return (cudaStream_t)s; }
 
+// Fault injection for tests of the error paths (moe_debug_inject): the next
+// eligible call consumes it.
+std::atomic<int> g_inject{MOE_INJECT_NONE};
+constexpr unsigned long long kInjectWaitNs = 2ull * 1000 * 1000;  // 2 ms
+
+bool take_inject(int what) {
+    int v = what;
+    return g_inject.compare_exchange_strong(v, MOE_INJECT_NONE);
+}
+
 bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
 bool layer_ok(const moe_layer_t *l) {
@@ -162,6 +172,8 @@ int decode_plan(const moe_layer_t *l, const float *x, int T, int flags, float *y
     a.ctrl = ws.ctrl; a.ticket = ws.ticket; a.logits = ws.logits; a.h16 = ws.h16; a.hs16 = ws.hs16;
     a.pr = ws.pr; a.ps = ws.ps;
     a.mode = kModeShared | kModeRouted;
+    a.route_extra = 0;
+    a.route_wait_ns = kWaitNs;
     const int nch = T > 8 ? 2 : 1;
     const int gpw = (a.Lr.G + kCW - 1) / kCW;
     if (gpw > 5 || l->H > kMaxHiddenLayer) return MOE_EINVAL;  // hidden size above 4096
@@ -253,6 +265,11 @@ int run_decode(const moe_layer_t *l, const float *x, int T, int flags, float *y,
     if (rc) return rc;
     DecodePlan plan;
     if ((rc = decode_plan(l, x, T, flags, y, idx_out, gate_out, ws, &plan))) return rc;
+    if (take_inject(MOE_INJECT_WAIT)) {
+        // the routing wait expects one router row more than there are: it runs out
+        plan.a.route_extra = 1;
+        plan.a.route_wait_ns = kInjectWaitNs;
+    }
     return decode_launch(plan, kModeShared | kModeRouted, stream);
 }
 
@@ -393,11 +410,21 @@ int run_decode_cached(const moe_layer_t *l, const float *x, int T, int flags, fl
         for (int i = 0; i < n && !seen; i++) seen = req[i] == c->h_idx[p];
         if (!seen) req[n++] = c->h_idx[p];
     }
+    const moe::LfuPolicy before = c->policy;  // restored if the step cannot be carried out
     rc = c->policy.step(req, n, slot, hit);
     if (rc == 3) return MOE_ECAPACITY;
     if (rc) return MOE_EINVAL;
+    // A failure from here on leaves the policy as it was before the step, except
+    // that the slots whose copies were already issued are marked empty (their
+    // contents are no longer the experts the policy had there).
+    int issued[kMaxPairs], n_issued = 0;
+    auto fail = [&](int status) {
+        c->policy = before;
+        for (int i = 0; i < n_issued; i++) c->policy.invalidate(issued[i]);
+        return status;
+    };
     DecodePlan plan;
-    if ((rc = decode_plan(l, x, T, flags, y, idx_out, gate_out, ws, &plan))) return rc;
+    if ((rc = decode_plan(l, x, T, flags, y, idx_out, gate_out, ws, &plan))) return fail(rc);
     plan.a.experts = c->d_slots;
     plan.a.stride = c->blob;
     plan.a.use_map = 1;
@@ -407,19 +434,25 @@ int run_decode_cached(const moe_layer_t *l, const float *x, int T, int flags, fl
     int misses = 0;
     for (int i = 0; i < n; i++) {
         if (hit[i]) continue;
+        if (take_inject(MOE_INJECT_COPY)) return fail(MOE_ECUDA);  // as if the copy had failed
         // The slot's previous expert was last read by work that precedes the
         // router launch on `stream`, which the host has just waited for.
         if (cudaMemcpyAsync(c->d_slots + (size_t)slot[i] * c->blob, c->h_experts + (size_t)req[i] * c->host_stride,
                             c->blob, cudaMemcpyHostToDevice, c->side) != cudaSuccess)
-            return cuda_status();
+            return fail(cuda_status());
+        issued[n_issued++] = slot[i];
         c->h2d_bytes += c->blob;
         misses++;
     }
-    if (misses == 0) return decode_launch(plan, kModeShared | kModeRouted | kModePre, stream);
-    if (cudaEventRecord(c->ev_copies, c->side) != cudaSuccess) return cuda_status();
-    if ((rc = decode_launch(plan, kModeShared | kModePre, stream))) return rc;
-    if (cudaStreamWaitEvent(st, c->ev_copies, 0) != cudaSuccess) return cuda_status();
-    return decode_launch(plan, kModeRouted | kModePre, stream);
+    if (misses == 0) {
+        rc = decode_launch(plan, kModeShared | kModeRouted | kModePre, stream);
+        return rc ? fail(rc) : MOE_OK;
+    }
+    if (cudaEventRecord(c->ev_copies, c->side) != cudaSuccess) return fail(cuda_status());
+    if ((rc = decode_launch(plan, kModeShared | kModePre, stream))) return fail(rc);
+    if (cudaStreamWaitEvent(st, c->ev_copies, 0) != cudaSuccess) return fail(cuda_status());
+    rc = decode_launch(plan, kModeRouted | kModePre, stream);
+    return rc ? fail(rc) : MOE_OK;
 }
 
 // ------------------------------------------------------------------ allocation-free decode
@@ -447,6 +480,21 @@ int noalloc_scratch(void **out) {
         g_noalloc_ptr[dev] = p;
     }
     *out = g_noalloc_ptr[dev];
+    return MOE_OK;
+}
+
+// Reads the error word at the start of a scratch area after `stream` is idle and,
+// if a device-side wait gave up, zeroes the whole area (then waits for the
+// device): MOE_ETIMEOUT; MOE_OK otherwise.
+int scratch_status(void *d_ws, size_t ws_bytes, cudaStream_t st) {
+    if (cudaStreamSynchronize(st) != cudaSuccess) return cuda_status();
+    unsigned err = 0;
+    if (cudaMemcpy(&err, d_ws, sizeof(unsigned), cudaMemcpyDeviceToHost) != cudaSuccess) return cuda_status();
+    if (err) {
+        if (cudaMemset(d_ws, 0, ws_bytes) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess)
+            return cuda_status();
+        return MOE_ETIMEOUT;
+    }
     return MOE_OK;
 }
 
@@ -513,16 +561,17 @@ int moe_workspace_init(void *d_ws, size_t ws_bytes, void *stream) {
 
 int moe_workspace_status(void *d_ws, size_t ws_bytes, void *stream) {
     if (!d_ws || ws_bytes < 16) return MOE_EINVAL;
-    cudaStream_t st = as_stream(stream);
-    if (cudaStreamSynchronize(st) != cudaSuccess) return cuda_status();
-    unsigned err = 0;
-    if (cudaMemcpy(&err, d_ws, sizeof(unsigned), cudaMemcpyDeviceToHost) != cudaSuccess)
-        return cuda_status();
-    if (err) {
-        cudaMemset(d_ws, 0, ws_bytes);
-        cudaDeviceSynchronize();
-        return MOE_ETIMEOUT;
-    }
+    return scratch_status(d_ws, ws_bytes, as_stream(stream));
+}
+
+size_t moe_decode_workspace_bytes(const moe_layer_t *layer, int T_max) {
+    if (!layer_ok(layer) || T_max < 1 || T_max > MOE_MAX_DECODE_TOKENS) return 0;
+    return ws_layout(*layer, T_max).decode_total;
+}
+
+int moe_debug_inject(int what) {
+    if (what != MOE_INJECT_NONE && what != MOE_INJECT_WAIT && what != MOE_INJECT_COPY) return MOE_EINVAL;
+    g_inject.store(what);
     return MOE_OK;
 }
 
@@ -716,6 +765,13 @@ int moe_layer_decode_noalloc(const moe_layer_t *layer, const float *x, int T, in
     void *ws = nullptr;
     if ((rc = noalloc_scratch(&ws))) return rc;
     return run_decode(layer, x, T, flags, y, idx_out, gate_out, ws, MOE_NOALLOC_SCRATCH_BYTES, stream);
+}
+
+int moe_noalloc_status(void *stream) {
+    void *ws = nullptr;
+    const int rc = noalloc_scratch(&ws);
+    if (rc) return rc;
+    return scratch_status(ws, MOE_NOALLOC_SCRATCH_BYTES, as_stream(stream));
 }
 
 }  // extern "C"

@@ -52,14 +52,16 @@ __device__ __forceinline__ bool mbar_test(uint64_t *bar, unsigned parity) {
 }
 
 // Waits for the phase of `bar` with the given parity to complete; false if the
-// wait ran out of time or `abort` (a CTA-wide error word) became non-zero.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, unsigned parity, volatile int *abort) {
+// wait ran out of time (`limit` ns) or `abort` (a CTA-wide error word) became
+// non-zero.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, unsigned parity, volatile int *abort,
+                                          unsigned long long limit = kWaitNs) {
     if (mbar_test(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
     while (true) {
         if (mbar_test(bar, parity)) return true;
         if (*abort) return false;
-        if (global_ns() - t0 > kWaitNs) return false;
+        if (global_ns() - t0 > limit) return false;
     }
 }
 
@@ -83,15 +85,16 @@ __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p) {
     return v;
 }
 
-// One thread waits until *p >= target (bounded); on expiry it raises *err.
-// Returns false on expiry or when another CTA already raised *err.
-__device__ __forceinline__ bool spin_geq(const unsigned *p, unsigned target, unsigned *err) {
+// One thread waits until *p >= target (bounded by `limit` ns); on expiry it
+// raises *err.  Returns false on expiry or when another CTA already raised *err.
+__device__ __forceinline__ bool spin_geq(const unsigned *p, unsigned target, unsigned *err,
+                                         unsigned long long limit = kWaitNs) {
     if (ld_acquire_gpu(p) >= target) return true;
     const unsigned long long t0 = global_ns();
     while (true) {
         if (ld_acquire_gpu(p) >= target) return true;
         if (*(volatile unsigned *)err) return false;
-        if (global_ns() - t0 > kWaitNs) {
+        if (global_ns() - t0 > limit) {
             atomicExch(err, 1u);
             return false;
         }
@@ -100,15 +103,16 @@ __device__ __forceinline__ bool spin_geq(const unsigned *p, unsigned target, uns
 }
 
 // One thread waits until the cumulative counter *p has advanced by `delta`
-// past `base` (modulo 2^32; bounded, no sleep); on expiry it raises *err.
-// Returns false on expiry or when another CTA already raised *err.
-__device__ __forceinline__ bool spin_reach(const unsigned *p, unsigned base, unsigned delta, unsigned *err) {
+// past `base` (modulo 2^32; bounded by `limit` ns, no sleep); on expiry it
+// raises *err.  Returns false on expiry or when another CTA already raised *err.
+__device__ __forceinline__ bool spin_reach(const unsigned *p, unsigned base, unsigned delta, unsigned *err,
+                                           unsigned long long limit = kWaitNs) {
     if (ld_acquire_gpu(p) - base >= delta) return true;
     const unsigned long long t0 = global_ns();
     while (true) {
         if (ld_acquire_gpu(p) - base >= delta) return true;
         if (*(volatile unsigned *)err) return false;
-        if (global_ns() - t0 > kWaitNs) {
+        if (global_ns() - t0 > limit) {
             atomicExch(err, 1u);
             return false;
         }

@@ -148,9 +148,18 @@ MOE_API int moe_workspace_init(void *d_ws, size_t ws_bytes, void *stream);
 /*
  * Synchronises `stream`, then reports whether a device-side wait of an earlier
  * call on this workspace gave up (MOE_ETIMEOUT) and re-initialises the workspace
- * in that case.  MOE_OK otherwise.
+ * in that case (zeroes it and waits for the device).  MOE_OK otherwise.  Outputs
+ * of a call whose wait gave up are undefined.
  */
 MOE_API int moe_workspace_status(void *d_ws, size_t ws_bytes, void *stream);
+
+/*
+ * The part of the workspace that moe_route and moe_layer_decode use for up to
+ * T_max tokens (1..MOE_MAX_DECODE_TOKENS): a caller that never runs a prefill
+ * chunk may allocate only this many bytes.  Returns 0 for an invalid layer or
+ * T_max.  (moe_workspace_bytes covers the prefill chunk as well.)
+ */
+MOE_API size_t moe_decode_workspace_bytes(const moe_layer_t *layer, int T_max);
 
 /* ---------------------------------------------------------------- kernels */
 
@@ -188,7 +197,15 @@ MOE_API int moe_route(const moe_layer_t *layer, const float *x, int T, int32_t *
 typedef struct moe_cache moe_cache_t;
 
 /*
- * Decode step on T = 1..MOE_MAX_DECODE_TOKENS independent tokens:
+ * Decode step on T = 1..MOE_MAX_DECODE_TOKENS independent tokens (the per-token
+ * MoE layer the pages describe: an 8-bit router choosing 8 experts per token, an
+ * always-on shared expert, both branches summed -- devtrends page "Come eseguire
+ * un modello da 26 miliardi...", section "Qual e il trucco principale
+ * dell'architettura"; remio.ai page "TurboFieldfare esegue Mac Gemma 4 26B in
+ * 2 GB...", sections "Mac Gemma 4 26B entra nello spazio disponibile..." and
+ * "L'affermazione dei 2 GB trasforma la larghezza di banda dell'SSD nel nuovo
+ * vincolo"; 4-bit affine group-64 weights per elsolitario.org "Correr un modelo
+ * de 26.000 millones...", section "Detalles tecnicos y rendimiento"):
  *   y_t = sum_k gate_tk * expert_{idx_tk}(x_t) + shared(x_t)   (+ x_t with MOE_RESIDUAL)
  * expert(x) = Wd (gelu_tanh(Wg x) * (Wu x)).  Every distinct expert is read once
  * for all the tokens that chose it.  x, y: device fp32 [T][H] (y must not alias
@@ -207,7 +224,11 @@ MOE_API int moe_layer_decode(const moe_layer_t *layer, const float *x, int T, in
                      size_t ws_bytes, void *stream);
 
 /*
- * Prefill chunk of T = 1..MOE_MAX_PREFILL_TOKENS tokens: the same result as T
+ * Prefill chunk of T = 1..MOE_MAX_PREFILL_TOKENS tokens (the pages' prefill in
+ * chunks of 128 tokens, so that one loaded expert serves many rows: devtrends
+ * page "Come eseguire un modello da 26 miliardi...", section "Prestazioni nel
+ * mondo reale"; remio.ai page, section "L'affermazione dei 2 GB..."; iitog.ru
+ * page "TurboFieldfare: движок с открытым кодом..."): the same result as T
  * independent decodes (chunking only lets one expert load serve many rows).  The
  * tokens routed to each expert are gathered, multiplied on the tensor cores with
  * fp16 operands and fp32 accumulation, and scattered back through the gates.
@@ -248,18 +269,30 @@ MOE_API int moe_layer_decode_host(const moe_layer_t *layer, const float *x_host,
  *   - The first call on a device does a one-time set-up with that device
  *     current: it looks up the array's device address and zeroes the array
  *     (this synchronises the device).  Make that first call before any stream
- *     capture.
+ *     capture.  The set-up belongs to the device's primary context: it does not
+ *     survive a reset of that context (cudaDeviceReset), after which this call
+ *     must not be used again in the process.
  *   - Every call shares the one array, so calls that overlap on the GPU (two
  *     streams, or two host threads) race and give wrong results; serialise them.
- *     Each call leaves the control words at zero for the next one; after a
- *     MOE_ETIMEOUT from a device-side wait, later results are undefined.
+ *     The array carries state from call to call: the decode's cumulative
+ *     counters (each call starts from the values the previous call left) and
+ *     the output-tile tickets, which each call returns to zero.
+ *   - A device-side wait that gives up (a lost signal) raises an error word in
+ *     the array; that call's outputs, and those of every later call, are
+ *     undefined until moe_noalloc_status has seen it.  moe_noalloc_status
+ *     synchronises `stream`, returns MOE_ETIMEOUT and zeroes the array if a wait
+ *     gave up, and MOE_OK otherwise.  A caller that must know its result is good
+ *     checks it after the call.
  *   - Returns MOE_EWORKSPACE when the layer at T tokens needs more scratch than
- *     MOE_NOALLOC_SCRATCH_BYTES (the full-size layer, hidden 2816 with 128
- *     experts, needs about 2.5 MB at T = 16); other errors as moe_layer_decode.
+ *     MOE_NOALLOC_SCRATCH_BYTES; moe_decode_workspace_bytes tells how much it
+ *     needs (the full-size layer, hidden 2816 with 128 experts, top-8, expert
+ *     inter 704, shared inter 2112, needs 2,602,240 bytes at T = 16).  Other
+ *     errors as moe_layer_decode.
  */
 #define MOE_NOALLOC_SCRATCH_BYTES (4u << 20)
 MOE_API int moe_layer_decode_noalloc(const moe_layer_t *layer, const float *x, int T, int flags,
                                      float *y, int32_t *idx_out, float *gate_out, void *stream);
+MOE_API int moe_noalloc_status(void *stream);
 
 /* ---------------------------------------------------------------- LFU cache */
 
@@ -307,6 +340,27 @@ MOE_API int moe_cache_destroy(moe_cache_t *cache);
 MOE_API int moe_cache_slots(const moe_cache_t *cache, int32_t *expert_of_slot, uint32_t *counts);
 MOE_API int moe_cache_stats(const moe_cache_t *cache, uint64_t *hits, uint64_t *misses,
                             uint64_t *h2d_bytes);
+
+/* ---------------------------------------------------------------- tests */
+
+/*
+ * Fault injection for tests of the error paths (the pages have no counterpart).
+ * The next eligible call consumes the injection:
+ *   MOE_INJECT_WAIT  the next moe_layer_decode / moe_layer_decode_noalloc without
+ *                    a cache makes its routing wait expect one router row more
+ *                    than exist, with a 2 ms limit: the wait gives up, the kernel
+ *                    drains without computing, and moe_workspace_status (or
+ *                    moe_noalloc_status) reports MOE_ETIMEOUT.
+ *   MOE_INJECT_COPY  the next host -> device expert copy of a cached decode fails
+ *                    as if cudaMemcpyAsync had returned an error: the call returns
+ *                    MOE_ECUDA and the cache's policy state is as before the call.
+ *   MOE_INJECT_NONE  clears a pending injection.
+ * No GPU fault is involved.  Returns MOE_EINVAL for an unknown value.
+ */
+#define MOE_INJECT_NONE 0
+#define MOE_INJECT_WAIT 1
+#define MOE_INJECT_COPY 2
+MOE_API int moe_debug_inject(int what);
 
 #ifdef __cplusplus
 }

@@ -225,9 +225,9 @@ def test_prefill_tiny(moe, tiny, T):
 
 
 def test_prefill_full_zipf_128(moe, full_zipf):
+    # every one of the 128 tokens, outputs and routing
     s, gl, ol = full_zipf
-    _layer_check(moe, s, gl, ol, 128, 500, prefill=True,
-                 check_tokens=[0, 1, 2, 31, 63, 64, 100, 126, 127])
+    _layer_check(moe, s, gl, ol, 128, 500, prefill=True)
 
 
 def test_odd_shapes(moe):

@@ -1,5 +1,6 @@
 """A stack of MoE layers decoded through per-layer LFU caches (the 30-layer stack
-workload, scaled down), called through the C ABI.
+workload, scaled down in depth: the tiny layer, and 3 layers of the full-size
+layer with 16 slots each), called through the C ABI.
 
 Each layer has its own experts in page-locked host memory and its own device
 cache; attention is the identity, so a step is h <- h + MoE_l(h) for l = 1..L.
@@ -31,10 +32,11 @@ def _requests(idx):
     return seen
 
 
-@pytest.mark.parametrize("layers,slots,steps", [(3, 16, 10), (2, 10, 12)])
-def test_stack_teacher_forced(layers, slots, steps):
+@pytest.mark.parametrize("shape_name,layers,slots,steps", [("tiny", 3, 16, 10), ("tiny", 2, 10, 12),
+                                                            ("full", 3, 16, 6)])
+def test_stack_teacher_forced(shape_name, layers, slots, steps):
     import bit_affine_quantised_affine4_b300 as moe
-    s = synth.TINY
+    s = synth.SHAPES[shape_name]
     gls, ols, caches, views, policies = [], [], [], [], []
     for l in range(layers):
         bias = synth.popularity_bias(s, seed=0, layer=l)

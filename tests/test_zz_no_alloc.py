@@ -59,6 +59,42 @@ def test_noalloc_matches_workspace_decode_twice(shape, T):
         assert ok, "call %d: worst err/bound %.3f" % (call, worst)
 
 
+def test_noalloc_scratch_fits_full_layer():
+    # the full-size layer (hidden 2816, 128 experts, top-8, inter 704, shared
+    # inter 2112) at the largest decode batch needs 2,602,240 bytes of scratch,
+    # under the static array's 4 MiB
+    import bit_affine_quantised_affine4_b300 as moe
+    s = synth.FULL
+    layer = moe.moe_layer_t(H=s.H, E=s.E, topk=s.topk, I=s.I, Is=s.Is, r_q=256, r_s=256, r_b=256,
+                            experts=256, expert_stride=moe.moe_tile_blob_bytes(s.H, s.I), shared=256)
+    need = moe.moe_decode_workspace_bytes(layer, moe.MOE_MAX_DECODE_TOKENS)
+    assert need == 2_602_240
+    assert need <= moe.MOE_NOALLOC_SCRATCH_BYTES
+
+
+def test_noalloc_status_reports_a_wait_that_gave_up():
+    """A routing wait made unreachable (fault injection, 2 ms limit) gives up: the
+    kernel drains, moe_noalloc_status reports MOE_ETIMEOUT once and clears the
+    array, and the next call is correct again."""
+    import bit_affine_quantised_affine4_b300 as moe
+    shape = synth.TINY
+    gl = gpu_layer(shape, seed=0)
+    layer = gl.view()
+    x = torch.from_numpy(synth.tokens(shape, 1, seed=0, stream=990)).cuda()
+    _noalloc_call(moe, layer, x, 1)
+    assert moe.moe_noalloc_status() == moe.MOE_OK
+    moe.moe_debug_inject(moe.MOE_INJECT_WAIT)
+    _noalloc_call(moe, layer, x, 1)
+    assert moe.moe_noalloc_status() == moe.MOE_ETIMEOUT
+    assert moe.moe_noalloc_status() == moe.MOE_OK
+    y_na, idx_na, _ = _noalloc_call(moe, layer, x, 1)
+    y_ws, idx_ws, _ = _with_workspace(moe, layer, x, 1)
+    torch.cuda.synchronize()
+    assert moe.moe_noalloc_status() == moe.MOE_OK
+    assert np.array_equal(idx_na.cpu().numpy(), idx_ws.cpu().numpy())
+    assert within_tol(y_na.cpu().numpy(), y_ws.cpu().numpy(), TOL)[0]
+
+
 def test_noalloc_rejects_oversized_layer():
     import bit_affine_quantised_affine4_b300 as moe
     # 256 experts of a wide layer at T = 16 need more scratch than the static array
