@@ -222,13 +222,17 @@ int decode_plan(const moe_layer_t *l, const float *x, int T, int flags, float *y
     return MOE_OK;
 }
 
-// One CTA per SM, launched cooperatively so that every CTA is resident and the
-// cross-CTA waits can always complete.  The launch also allows programmatic
-// dependent launch: when the previous operation on the stream is a decode
-// kernel, this one may start on the SMs it leaves while it finishes, and runs
-// its prologue (barrier set-up, weight copies and prefetches) before waiting
-// for it (griddepcontrol.wait).  If the runtime refuses the combination, the
-// plain cooperative launch is used from then on.
+// One CTA per SM, launched with programmatic dependent launch: when the previous
+// operation on the stream is a decode kernel, this one starts on each SM as that
+// kernel leaves it, and runs its prologue there (barrier set-up, weight copies and
+// prefetches) before waiting for it (griddepcontrol.wait).  It is not a
+// cooperative launch -- a cooperative grid starts only once the whole GPU is
+// free -- but its CTAs are resident together all the same: the previous decode
+// kernel signals launch_dependents at its start, so all of its CTAs are resident
+// before this grid launches, and this grid's CTAs take SMs as those exit (any
+// other predecessor has finished before the launch).  Every cross-CTA wait is
+// bounded in any case.  If the runtime refuses programmatic dependent launch, a
+// cooperative launch is used from then on.
 int decode_launch(DecodePlan &plan, int mode, void *stream) {
     static std::atomic<int> pdl_ok{1};  // shared by every calling thread
     plan.a.mode = mode;
@@ -239,13 +243,11 @@ int decode_launch(DecodePlan &plan, int mode, void *stream) {
         cfg.blockDim = dim3(kDecThreads);
         cfg.dynamicSmemBytes = (size_t)plan.smem;
         cfg.stream = as_stream(stream);
-        cudaLaunchAttribute attr[2];
-        attr[0].id = cudaLaunchAttributeCooperative;
-        attr[0].val.cooperative = 1;
-        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
-        cfg.numAttrs = 2;
+        cfg.numAttrs = 1;
         const cudaError_t e = cudaLaunchKernelExC(&cfg, plan.fn, args);
         if (e == cudaSuccess) return MOE_OK;
         if (e != cudaErrorInvalidValue && e != cudaErrorNotSupported) return cuda_status();
