@@ -17,6 +17,7 @@ from . import build as _build
 
 MOE_OK, MOE_EINVAL, MOE_ECUDA, MOE_ECAPACITY, MOE_ETIMEOUT, MOE_EWORKSPACE, MOE_ENOTREADY = range(7)
 MOE_RESIDUAL = 1
+MOE_PRENORM = 2
 MOE_INJECT_NONE, MOE_INJECT_WAIT, MOE_INJECT_COPY = range(3)
 MOE_NOALLOC_SCRATCH_BYTES = 4 << 20
 MOE_MAX_TOPK = 8
@@ -34,7 +35,7 @@ ENTRY_POINTS = (
     "moe_layer_prefill_chunk", "moe_cache_create", "moe_cache_destroy",
     "moe_cache_slots", "moe_cache_stats", "moe_layer_decode_noalloc", "moe_layer_decode_host",
     "moe_lfu_create", "moe_lfu_destroy", "moe_lfu_step", "moe_lfu_state",
-    "moe_decode_workspace_bytes", "moe_noalloc_status", "moe_debug_inject",
+    "moe_decode_workspace_bytes", "moe_noalloc_status", "moe_debug_inject", "moe_rmsnorm",
 )
 
 
@@ -50,6 +51,7 @@ class moe_layer_t(C.Structure):
         ("r_q", C.c_void_p), ("r_s", C.c_void_p), ("r_b", C.c_void_p),
         ("experts", C.c_void_p), ("expert_stride", C.c_size_t),
         ("shared", C.c_void_p), ("logit_bias", C.c_void_p),
+        ("norm_w", C.c_void_p), ("norm_eps", C.c_float),
     ]
 
 
@@ -92,6 +94,7 @@ def _load():
     L.moe_decode_workspace_bytes.restype = sz
     L.moe_noalloc_status.argtypes = [p]
     L.moe_debug_inject.argtypes = [i]
+    L.moe_rmsnorm.argtypes = [p, p, C.c_float, i, i, p, p]
     for name in ENTRY_POINTS:
         if name not in ("moe_status_string", "moe_expert_blob_bytes", "moe_workspace_bytes",
                         "moe_tile_blob_bytes", "moe_decode_workspace_bytes"):
@@ -162,6 +165,14 @@ def qgemv_affine4(q, s, b, K: int, x, y=None, stream=None):
     y = torch.empty(N, dtype=torch.float32, device=x.device) if y is None else y
     _check(lib.qgemv_affine4(_ptr(q), _ptr(s), _ptr(b), N, K, _ptr(x), _ptr(y), _stream(stream)),
            "qgemv_affine4")
+    return y
+
+
+def moe_rmsnorm(x, w, eps: float, y=None, stream=None):
+    """RMSNorm of the rows of x (fp32 CUDA [T, H]) with weight w ([H])."""
+    T, H = x.shape
+    y = torch.empty_like(x) if y is None else y
+    _check(lib.moe_rmsnorm(_ptr(x), _ptr(w), float(eps), T, H, _ptr(y), _stream(stream)), "moe_rmsnorm")
     return y
 
 

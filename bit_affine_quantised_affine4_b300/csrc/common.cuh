@@ -57,6 +57,8 @@ struct LayerDev {
     size_t stride;
     const uint8_t *shared;
     const float *bias;
+    const float *norm_w;  // RMSNorm weight when the router reads RMSNorm(x) (else null)
+    float norm_eps;
     BlobLayout L, Ls;
 };
 
@@ -93,6 +95,7 @@ struct Ws {
     uint8_t *Br, *Bs;  // token operand tiles: [H/64][Rmax][128 B], [H/64][T16][128 B]
     uint8_t *Hr, *Hs;  // h operand tiles:     [I/64][Rmax][128 B], [Is/64][T16][128 B]
     float *Yr, *Ys;    // down rows: [Tmax*topk][H], [T16][H]
+    float *xn;         // [Tmax][H] RMSNorm(x) of a pre-norm prefill chunk
     int Tmax;
 };
 
@@ -113,7 +116,7 @@ constexpr size_t kWsHeaderBytes = (kCtrlWords + kMaxTickets) * sizeof(unsigned);
 
 struct WsLayout {
     size_t ctrl, logits, idx, gate, h16, hs16, pr, ps, xh, yh, ih, gh, decode_total;
-    size_t plan, Br, Bs, Hr, Hs, Yr, Ys, total;
+    size_t plan, Br, Bs, Hr, Hs, Yr, Ys, xn, total;
     int Tmax;
 };
 
@@ -143,6 +146,7 @@ inline WsLayout ws_layout(const moe_layer_t &l, int Tmax) {
     W.Hs = off;     off = up256(off + size_t(l.Is / kGroup) * T16 * 128);
     W.Yr = off;     off = up256(off + sizeof(float) * size_t(Tmax) * l.topk * l.H);
     W.Ys = off;     off = up256(off + sizeof(float) * size_t(T16) * l.H);
+    W.xn = off;     off = up256(off + sizeof(float) * size_t(Tmax) * l.H);
     W.total = off;
     return W;
 }
@@ -170,6 +174,7 @@ inline Ws ws_bind(void *base, const WsLayout &W, const moe_layer_t &l) {
     w.Hs = p + W.Hs;
     w.Yr = (float *)(p + W.Yr);
     w.Ys = (float *)(p + W.Ys);
+    w.xn = (float *)(p + W.xn);
     w.Tmax = W.Tmax;
     (void)l;
     return w;

@@ -99,6 +99,10 @@ struct DecodeArgs {
     // wait expects (0 normally; > 0 makes it unreachable) and that wait's limit
     unsigned route_extra;
     unsigned long long route_wait_ns;
+    // RMSNorm in front of the layer (flags & MOE_PRENORM): the router and the
+    // experts read x * norm_w / rms(x); 1 / rms is applied to their sums
+    const float *norm_w;
+    float norm_eps;
 };
 
 // x / d for x < 2^24 and 1 <= d <= 256: magic = 0xFFFFFFFF / d + 1 (d > 1), exact
@@ -137,6 +141,8 @@ struct DecodeSmem {
     float rpart[kMaxRouterRows][kCW > MOE_MAX_DECODE_TOKENS ? kCW : MOE_MAX_DECODE_TOKENS];
     unsigned wsum[MOE_MAX_EXPERTS / 32];  // schedule: experts << 16 | slots of 32 experts
     unsigned tcnt[kMaxStages + 2];         // gate/up partial-sum slots: warps arrived (+1: claimed)
+    float xss[kCW][MOE_MAX_DECODE_TOKENS];  // RMSNorm: partial sums of squares of x per warp
+    float inv_r[MOE_MAX_DECODE_TOKENS];     // RMSNorm: 1 / rms(x_t)
     int U;
     int err;
 };
@@ -209,6 +215,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
     const int n_shared_mine = b < Ts ? (Ts - 1 - b) / nC + 1 : 0;
 
     // ---- compute warps: x fragments for this warp's K slice, and their group sums
+    // (of x * norm_w with MOE_PRENORM)
+    const bool prenorm = a.flags & MOE_PRENORM;
     const int g0w = warp * G / kCW, g1w = (warp + 1) * G / kCW;
     uint32_t xb[GPW][NCH][8];
     float xs[GPW][NCH][2];
@@ -219,7 +227,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
             for (int ch = 0; ch < NCH; ch++) {
                 const int g = g0w + gi, t = 8 * ch + gl;
                 if (g < g1w && t < T)
-                    load_b_f32(xb[gi][ch], a.x + (size_t)t * H + g * kGroup + 16 * c);
+                    load_b_f32(xb[gi][ch], a.x + (size_t)t * H + g * kGroup + 16 * c,
+                               prenorm ? a.norm_w + g * kGroup + 16 * c : nullptr);
                 else
                     zero_b(xb[gi][ch]);
                 float d[4] = {0.f, 0.f, 0.f, 0.f};
@@ -261,7 +270,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
             for (int i = 0; i < 2; i++) {
                 const int t = 8 * ch + 2 * c + i;
                 if (t >= T || *err) continue;
-                const __half hv = __float2half_rn(gelu_tanh(i ? v.y : v.x) * (i ? v.w : v.z));
+                const float f = prenorm ? S.inv_r[t] : 1.f;
+                const __half hv = __float2half_rn(gelu_tanh(f * (i ? v.y : v.x)) * (f * (i ? v.w : v.z)));
                 if (u < 0) {
                     a.hs16[((size_t)g * T + t) * kGroup + h_pos(k, t)] = hv;
                 } else {
@@ -420,7 +430,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
                 if (lane < T) {
                     float acc = 0.f;
                     for (int k = 0; k < nchk; k++) acc += S.rpart[j][lane * nchk + k];
-                    a.logits[(size_t)lane * a.E + e] = acc + (a.bias ? a.bias[e] : 0.f);
+                    // with MOE_PRENORM the sum is of x * norm_w: every CTA applies
+                    // 1 / rms and the bias when it ranks
+                    a.logits[(size_t)lane * a.E + e] = prenorm ? acc : acc + (a.bias ? a.bias[e] : 0.f);
                 }
             }
             if (j > 0) {
@@ -474,16 +486,47 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
             int j = 0;
             for (int e = b; e < a.E; e += nC, j++)
                 for (int t = t0; t < T; t += tstep) {
-                    const float v = router_dot(a.rq, a.rs, a.rb, H, a.x, e, t, p0, p1);
+                    const float v = router_dot(a.rq, a.rs, a.rb, H, a.x, e, t, p0, p1, prenorm ? a.norm_w : nullptr);
                     if (lane == 0) S.rpart[j][t * nchk + ck] = v;
                 }
             named_arrive(2, kDecThreads);
         } else {
             pdl_wait();
         }
+        if (prenorm) {
+            // this warp's share of every token's sum of squares
+            for (int t = 0; t < T; t++) {
+                const float4 *xt = reinterpret_cast<const float4 *>(a.x + (size_t)t * H);
+                float sq = 0.f;
+                for (int i = warp * 32 + lane; i < H / 4; i += kCThreads) {
+                    const float4 v = __ldg(xt + i);
+                    sq += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+                }
+                sq = warp_sum(sq);
+                if (lane == 0) S.xss[warp][t] = sq;
+            }
+        }
         load_x();
     }
     __syncthreads();
+    if (prenorm) {
+        // 1 / rms(x_t) from the warps' partial sums (in warp order), then the staged
+        // logits become (1 / rms) sum + bias
+        if (tid < T) {
+            float sq = 0.f;
+            for (int w = 0; w < kCW; w++) sq += S.xss[w][tid];
+            S.inv_r[tid] = rms_inv(sq, H, a.norm_eps);
+        }
+        __syncthreads();
+        if (!pre && !*err) {
+            float *lg = reinterpret_cast<float *>(hsm);
+            for (int i = tid; i < T * a.E; i += kDecThreads) {
+                const int t = i / a.E, e = i - t * a.E;
+                lg[i] = lg[i] * S.inv_r[t] + (a.bias ? a.bias[e] : 0.f);
+            }
+        }
+        __syncthreads();
+    }
     // routing with the whole CTA (nothing else runs meanwhile): one warp per token
     // ranks the staged logits, then every thread helps to build the schedule
     if (!pre && !*err)

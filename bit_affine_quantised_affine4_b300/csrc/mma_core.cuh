@@ -106,12 +106,19 @@ __device__ __forceinline__ void zero_b(uint32_t (&xb)[8]) {
     for (int i = 0; i < 8; i++) xb[i] = 0u;
 }
 
-// Sixteen fp32 columns 16c..16c+15 of one group -> the lane's 8 B registers.
-__device__ __forceinline__ void load_b_f32(uint32_t (&xb)[8], const float *cols16) {
+// Sixteen fp32 columns 16c..16c+15 of one group -> the lane's 8 B registers;
+// scaled elementwise by the matching columns of w when w is non-null.
+__device__ __forceinline__ void load_b_f32(uint32_t (&xb)[8], const float *cols16, const float *w = nullptr) {
     const float4 *p = reinterpret_cast<const float4 *>(cols16);
+    const float4 *q = reinterpret_cast<const float4 *>(w);
 #pragma unroll
     for (int j = 0; j < 2; j++) {
         float4 lo = __ldg(p + 2 * j), hi = __ldg(p + 2 * j + 1);  // columns 8j..8j+3, 8j+4..8j+7
+        if (q) {
+            const float4 wl = __ldg(q + 2 * j), wh = __ldg(q + 2 * j + 1);
+            lo = make_float4(lo.x * wl.x, lo.y * wl.y, lo.z * wl.z, lo.w * wl.w);
+            hi = make_float4(hi.x * wh.x, hi.y * wh.y, hi.z * wh.z, hi.w * wh.w);
+        }
         __half2 r0 = __floats2half2_rn(lo.x, hi.x);
         __half2 r1 = __floats2half2_rn(lo.y, hi.y);
         __half2 r2 = __floats2half2_rn(lo.z, hi.z);

@@ -68,6 +68,8 @@ LayerDev layer_dev(const moe_layer_t *l) {
     d.stride = l->expert_stride;
     d.shared = (const uint8_t *)l->shared;
     d.bias = l->logit_bias;
+    d.norm_w = nullptr;
+    d.norm_eps = l->norm_eps;
     d.L = blob_layout(l->H, l->I);
     d.Ls = blob_layout(l->H, l->Is);
     return d;
@@ -108,18 +110,57 @@ int bind_ws(const moe_layer_t *l, int T, void *d_ws, size_t ws_bytes, Ws *out, b
 
 int launch_route(const moe_layer_t *l, const LayerDev &ly, const float *x, int T, Ws ws,
                  int32_t *idx, float *gate, float *logits, cudaStream_t st, int32_t *idx_host = nullptr,
-                 unsigned *flag_host = nullptr, unsigned seq = 0) {
+                 unsigned *flag_host = nullptr, unsigned seq = 0, bool prenorm = false) {
     const dim3 grid((l->E + kRouteExp - 1) / kRouteExp, (T + kRouteTok - 1) / kRouteTok);
-    k_route<<<grid, kRouteTok * 32, 0, st>>>(ly, x, T, ws, idx, gate, logits, idx_host, flag_host, seq);
+    LayerDev lr = ly;
+    lr.norm_w = prenorm ? l->norm_w : nullptr;
+    lr.norm_eps = l->norm_eps;
+    k_route<<<grid, kRouteTok * 32, 0, st>>>(lr, x, T, ws, idx, gate, logits, idx_host, flag_host, seq);
     return cuda_status();
+}
+
+// Flags a layer call accepts; MOE_PRENORM needs the layer's RMSNorm weight.
+bool flags_ok(const moe_layer_t *l, int flags) {
+    if (flags & ~(MOE_RESIDUAL | MOE_PRENORM)) return false;
+    if ((flags & MOE_PRENORM) && (!l->norm_w || !aligned(l->norm_w, 16) || !(l->norm_eps >= 0.f)))
+        return false;
+    return true;
 }
 
 int check_layer_call(const moe_layer_t *l, const float *x, int T, int Tlimit, int flags,
                      const float *y) {
     if (!layer_ok(l) || !experts_ok(l) || !x || !y || T < 1 || T > Tlimit) return MOE_EINVAL;
-    if (flags & ~MOE_RESIDUAL) return MOE_EINVAL;
+    if (!flags_ok(l, flags)) return MOE_EINVAL;
     if (!aligned(x, 16) || !aligned(y, 16) || x == y) return MOE_EINVAL;
     return MOE_OK;
+}
+
+// RMSNorm, one CTA per row: y = x * w / sqrt(mean(x^2) + eps).
+__global__ void __launch_bounds__(256) k_rmsnorm(const float *x, const float *__restrict__ w, float eps, int H,
+                                                 float *y) {
+    const float4 *xr = reinterpret_cast<const float4 *>(x + (size_t)blockIdx.x * H);
+    float4 *yr = reinterpret_cast<float4 *>(y + (size_t)blockIdx.x * H);
+    const float4 *w4 = reinterpret_cast<const float4 *>(w);
+    __shared__ float part[8];
+    __shared__ float inv;
+    float sq = 0.f;
+    for (int i = threadIdx.x; i < H / 4; i += blockDim.x) {
+        const float4 v = xr[i];
+        sq += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+    }
+    sq = warp_sum(sq);
+    if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = sq;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float s = 0.f;
+        for (int i = 0; i < (int)(blockDim.x >> 5); i++) s += part[i];
+        inv = rms_inv(s, H, eps);
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < H / 4; i += blockDim.x) {
+        const float4 v = xr[i], g = __ldg(w4 + i);
+        yr[i] = make_float4(v.x * g.x * inv, v.y * g.y * inv, v.z * g.z * inv, v.w * g.w * inv);
+    }
 }
 
 struct DecodeCfg {
@@ -174,6 +215,8 @@ int decode_plan(const moe_layer_t *l, const float *x, int T, int flags, float *y
     a.mode = kModeShared | kModeRouted;
     a.route_extra = 0;
     a.route_wait_ns = kWaitNs;
+    a.norm_w = l->norm_w;
+    a.norm_eps = l->norm_eps;
     const int nch = T > 8 ? 2 : 1;
     const int gpw = (a.Lr.G + kCW - 1) / kCW;
     if (gpw > 5 || l->H > kMaxHiddenLayer) return MOE_EINVAL;  // hidden size above 4096
@@ -298,7 +341,15 @@ int run_layer_chunk(const moe_layer_t *l, const float *x, int T, int flags, floa
     }
     cudaStream_t st = as_stream(stream);
     LayerDev ly = layer_dev(l);
-    if ((rc = launch_route(l, ly, x, T, ws, ws.idx, ws.gate, nullptr, st))) return rc;
+    // with MOE_PRENORM the chunk runs on RMSNorm(x) (a copy in the workspace); the
+    // residual below still adds the raw x
+    const float *xin = x;
+    if (flags & MOE_PRENORM) {
+        k_rmsnorm<<<T, 256, 0, st>>>(x, l->norm_w, l->norm_eps, l->H, ws.xn);
+        if ((rc = cuda_status())) return rc;
+        xin = ws.xn;
+    }
+    if ((rc = launch_route(l, ly, xin, T, ws, ws.idx, ws.gate, nullptr, st))) return rc;
     const int P2 = T * l->topk;
     if (idx_out && cudaMemcpyAsync(idx_out, ws.idx, sizeof(int32_t) * P2, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
         return cuda_status();
@@ -316,7 +367,7 @@ int run_layer_chunk(const moe_layer_t *l, const float *x, int T, int flags, floa
     k_prefill_plan<<<1, 256, 0, st>>>(ws.idx, T, l->E, l->topk, Rmax, plan);
     if ((rc = cuda_status())) return rc;
     const long long gthreads = (long long)(Rmax + T16) * (l->H / kGroup) * 8;
-    k_prefill_gather<<<(unsigned)((gthreads + 255) / 256), 256, 0, st>>>(x, T, l->H, Rmax, T16, plan.rowtok,
+    k_prefill_gather<<<(unsigned)((gthreads + 255) / 256), 256, 0, st>>>(xin, T, l->H, Rmax, T16, plan.rowtok,
                                                                          plan.U, ws.Br, ws.Bs);
     if ((rc = cuda_status())) return rc;
     PrefillGemmArgs g;
@@ -389,7 +440,9 @@ int run_decode_cached(const moe_layer_t *l, const float *x, int T, int flags, fl
     cudaStream_t st = as_stream(stream);
     LayerDev ly = layer_dev(l);
     const unsigned seq = ++c->seq == 0 ? ++c->seq : c->seq;  // never 0 (the flag's initial value)
-    if ((rc = launch_route(l, ly, x, T, ws, ws.idx, ws.gate, nullptr, st, c->d_idx, c->d_flag, seq))) return rc;
+    if ((rc = launch_route(l, ly, x, T, ws, ws.idx, ws.gate, nullptr, st, c->d_idx, c->d_flag, seq,
+                           flags & MOE_PRENORM)))
+        return rc;
     const int P2 = T * l->topk;
     {
         // the router's flag (bounded: 5 s; a failed stream ends the wait at once)
@@ -590,6 +643,13 @@ int affine_quantise(const float *w, int N, int K, int bits, uint32_t *q, uint16_
     return cuda_status();
 }
 
+int moe_rmsnorm(const float *x, const float *w, float eps, int T, int H, float *y, void *stream) {
+    if (!x || !w || !y || T < 1 || H < 4 || H % 4 || !(eps >= 0.f)) return MOE_EINVAL;
+    if (!aligned(x, 16) || !aligned(w, 16) || !aligned(y, 16)) return MOE_EINVAL;
+    k_rmsnorm<<<T, 256, 0, as_stream(stream)>>>(x, w, eps, H, y);
+    return cuda_status();
+}
+
 int qgemv_affine4(const uint32_t *q, const uint16_t *s, const uint16_t *b, int N, int K,
                   const float *x, float *y, void *stream) {
     if (!q || !s || !b || !x || !y || N < 1 || K < kGroup || K % kGroup) return MOE_EINVAL;
@@ -615,7 +675,7 @@ int moe_layer_decode(const moe_layer_t *layer, const float *x, int T, int flags,
                      int32_t *idx_out, float *gate_out, moe_cache_t *cache, void *d_ws,
                      size_t ws_bytes, void *stream) {
     if (cache) {
-        if (!layer_ok(layer) || !x || !y || T < 1 || T > MOE_MAX_DECODE_TOKENS || (flags & ~MOE_RESIDUAL) ||
+        if (!layer_ok(layer) || !x || !y || T < 1 || T > MOE_MAX_DECODE_TOKENS || !flags_ok(layer, flags) ||
             !aligned(x, 16) || !aligned(y, 16) || x == y)
             return MOE_EINVAL;
         return run_decode_cached(layer, x, T, flags, y, idx_out, gate_out, cache, d_ws, ws_bytes, stream);
@@ -630,7 +690,7 @@ int moe_layer_decode(const moe_layer_t *layer, const float *x, int T, int flags,
 int moe_layer_decode_host(const moe_layer_t *layer, const float *x_host, int T, int flags, float *y_host,
                           int32_t *idx_host, float *gate_host, moe_cache_t *cache, void *d_ws, size_t ws_bytes,
                           void *stream) {
-    if (!layer_ok(layer) || !x_host || !y_host || T < 1 || T > MOE_MAX_DECODE_TOKENS || (flags & ~MOE_RESIDUAL))
+    if (!layer_ok(layer) || !x_host || !y_host || T < 1 || T > MOE_MAX_DECODE_TOKENS || !flags_ok(layer, flags))
         return MOE_EINVAL;
     Ws ws;
     int rc = bind_ws(layer, T, d_ws, ws_bytes, &ws);

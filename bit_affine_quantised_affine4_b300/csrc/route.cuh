@@ -92,20 +92,36 @@ __device__ __forceinline__ void warp_topk_softmax(const float *lrow, int E, int 
         warp_topk_softmax_nv<SMEM, MOE_MAX_EXPERTS / 32>(lrow, E, topk, idx_dst, gate_dst, idx_out, gate_out);
 }
 
+// x columns 8p..8p+7 of a token row as two float4, multiplied elementwise by the
+// RMSNorm weight g when one is given (the 1 / rms factor is applied to the sums).
+__device__ __forceinline__ void load_x8(const float4 *xt, const float4 *g4, int p, float4 &x0, float4 &x1) {
+    x0 = __ldg(xt + 2 * p);
+    x1 = __ldg(xt + 2 * p + 1);
+    if (g4) {
+        const float4 g0 = __ldg(g4 + 2 * p), g1 = __ldg(g4 + 2 * p + 1);
+        x0 = make_float4(x0.x * g0.x, x0.y * g0.y, x0.z * g0.z, x0.w * g0.w);
+        x1 = make_float4(x1.x * g1.x, x1.y * g1.y, x1.z * g1.z, x1.w * g1.w);
+    }
+}
+
 // Partial router logit of row e for token t over the word pairs [p0, p1) of the
-// 8-bit row (pair p holds columns 8p..8p+7), summed over the warp.
+// 8-bit row (pair p holds columns 8p..8p+7), summed over the warp; x is scaled
+// elementwise by g when g is non-null.
 __device__ __forceinline__ float router_dot(const uint32_t *rq, const __half *rs, const __half *rb, int H,
-                                            const float *x, int e, int t, int p0, int p1) {
+                                            const float *x, int e, int t, int p0, int p1,
+                                            const float *g = nullptr) {
     const int lane = threadIdx.x & 31, G = H / kGroup;
     const uint2 *row = reinterpret_cast<const uint2 *>(rq + (size_t)e * (H / 4));
     const float4 *xt = reinterpret_cast<const float4 *>(x + (size_t)t * H);
+    const float4 *g4 = reinterpret_cast<const float4 *>(g);
     const __half *sr = rs + (size_t)e * G, *br = rb + (size_t)e * G;
     float acc = 0.f;
 #pragma unroll 4
     for (int p = p0 + lane; p < p1; p += 32) {
         const uint2 w = __ldg(row + p);
         const float s = __half2float(sr[p >> 3]), bb = __half2float(br[p >> 3]);
-        const float4 x0 = __ldg(xt + 2 * p), x1 = __ldg(xt + 2 * p + 1);
+        float4 x0, x1;
+        load_x8(xt, g4, p, x0, x1);
         acc = fmaf(fmaf(s, (float)(w.x & 0xFFu), bb), x0.x, acc);
         acc = fmaf(fmaf(s, (float)((w.x >> 8) & 0xFFu), bb), x0.y, acc);
         acc = fmaf(fmaf(s, (float)((w.x >> 16) & 0xFFu), bb), x0.z, acc);
@@ -123,17 +139,29 @@ constexpr int kRouteExp = 4;   // router rows per CTA (each token vector read on
 
 // Router rows e0 .. e0 + NE - 1 (those < E) for token t, over the whole row:
 // router_dot's arithmetic for each row, with each x element loaded once for all.
+// With a RMSNorm weight g, x is scaled by g and *ss receives the token's sum of
+// squares of x (the caller applies 1 / rms to the sums).
 template <int NE>
 __device__ __forceinline__ void router_dot_rows(const uint32_t *rq, const __half *rs, const __half *rb, int H,
-                                                int E, const float *x, int e0, int t, float (&out)[NE]) {
+                                                int E, const float *x, int e0, int t, float (&out)[NE],
+                                                const float *g = nullptr, float *ss = nullptr) {
     const int lane = threadIdx.x & 31, G = H / kGroup, np = H / 8;
     const float4 *xt = reinterpret_cast<const float4 *>(x + (size_t)t * H);
+    const float4 *g4 = reinterpret_cast<const float4 *>(g);
     float acc[NE];
+    float sq = 0.f;
 #pragma unroll
     for (int j = 0; j < NE; j++) acc[j] = 0.f;
 #pragma unroll 2
     for (int p = lane; p < np; p += 32) {
-        const float4 x0 = __ldg(xt + 2 * p), x1 = __ldg(xt + 2 * p + 1);
+        float4 x0 = __ldg(xt + 2 * p), x1 = __ldg(xt + 2 * p + 1);
+        if (g4) {
+            sq += x0.x * x0.x + x0.y * x0.y + x0.z * x0.z + x0.w * x0.w;
+            sq += x1.x * x1.x + x1.y * x1.y + x1.z * x1.z + x1.w * x1.w;
+            const float4 g0 = __ldg(g4 + 2 * p), g1 = __ldg(g4 + 2 * p + 1);
+            x0 = make_float4(x0.x * g0.x, x0.y * g0.y, x0.z * g0.z, x0.w * g0.w);
+            x1 = make_float4(x1.x * g1.x, x1.y * g1.y, x1.z * g1.z, x1.w * g1.w);
+        }
 #pragma unroll
         for (int j = 0; j < NE; j++) {
             const int e = e0 + j < E ? e0 + j : E - 1;
@@ -153,6 +181,12 @@ __device__ __forceinline__ void router_dot_rows(const uint32_t *rq, const __half
     }
 #pragma unroll
     for (int j = 0; j < NE; j++) out[j] = warp_sum(acc[j]);
+    if (ss) *ss = warp_sum(sq);
+}
+
+// 1 / sqrt(mean square + eps): the RMSNorm factor of a row from its sum of squares.
+__device__ __forceinline__ float rms_inv(float sumsq, int H, float eps) {
+    return rsqrtf(sumsq / (float)H + eps);
 }
 
 // CTA (r, g): router rows 4r..4r+3 for tokens 16g..16g+15, one warp per token
@@ -166,14 +200,16 @@ k_route(LayerDev ly, const float *__restrict__ x, int T, Ws ws, int32_t *idx_out
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int e0 = blockIdx.x * kRouteExp, t = blockIdx.y * kRouteTok + warp;
     if (t < T) {
-        float v[kRouteExp];
-        router_dot_rows<kRouteExp>(ly.rq, ly.rs, ly.rb, ly.H, ly.E, x, e0, t, v);
+        float v[kRouteExp], ss = 0.f;
+        router_dot_rows<kRouteExp>(ly.rq, ly.rs, ly.rb, ly.H, ly.E, x, e0, t, v, ly.norm_w,
+                                   ly.norm_w ? &ss : nullptr);
+        const float inv = ly.norm_w ? rms_inv(ss, ly.H, ly.norm_eps) : 1.f;
         if (lane == 0)
 #pragma unroll
             for (int j = 0; j < kRouteExp; j++) {
                 const int e = e0 + j;
                 if (e >= ly.E) break;
-                const float lv = v[j] + (ly.bias ? ly.bias[e] : 0.f);
+                const float lv = (ly.norm_w ? v[j] * inv : v[j]) + (ly.bias ? ly.bias[e] : 0.f);
                 ws.logits[(size_t)t * ly.E + e] = lv;
                 if (logits_out) logits_out[(size_t)t * ly.E + e] = lv;
             }

@@ -66,6 +66,7 @@ class Layer:
         self.experts = torch.empty((copies, E, self.stride), dtype=torch.uint8, device=self.device)
         self.shared = torch.empty((copies, self.sstride), dtype=torch.uint8, device=self.device)
         self.bias = None
+        self.norm_w, self.norm_eps = None, 0.0
 
     # ---- filling
     def set_router(self, w: torch.Tensor):
@@ -83,6 +84,11 @@ class Layer:
     def set_bias(self, bias):
         self.bias = None if bias is None else torch.as_tensor(bias, dtype=torch.float32).to(self.device)
 
+    def set_norm(self, w, eps: float = 1e-6):
+        """RMSNorm weight [H] and epsilon, read by the layer calls with MOE_PRENORM."""
+        self.norm_w = None if w is None else torch.as_tensor(w, dtype=torch.float32).to(self.device).contiguous()
+        self.norm_eps = float(eps)
+
     def replicate(self):
         for c in range(1, self.copies):
             self.r_q[c].copy_(self.r_q[0]); self.r_s[c].copy_(self.r_s[0]); self.r_b[c].copy_(self.r_b[0])
@@ -97,6 +103,8 @@ class Layer:
             expert_stride=self.stride,
             shared=self.shared[c].data_ptr(),
             logit_bias=None if self.bias is None else self.bias.data_ptr(),
+            norm_w=None if self.norm_w is None else self.norm_w.data_ptr(),
+            norm_eps=self.norm_eps,
         )
 
     # ---- host copies of the tile-layout blobs

@@ -65,6 +65,8 @@ MOE_API const char *moe_status_string(int status);
 
 /* flags for moe_layer_decode / moe_layer_prefill_chunk */
 #define MOE_RESIDUAL 1 /* y = x + MoE(x) instead of y = MoE(x) */
+#define MOE_PRENORM 2  /* the layer reads RMSNorm(x) (layer->norm_w, norm_eps) instead of x;
+                          with MOE_RESIDUAL: y = x + MoE(RMSNorm(x)), the pre-norm block */
 
 #define MOE_GROUP 64
 #define MOE_MAX_TOPK 8
@@ -120,6 +122,8 @@ MOE_API int moe_expert_tile(const void *mlx_blob, int H, int I, void *tile_blob,
  *     May be NULL when a cache supplies the experts.
  *   shared: one tile-layout blob of shape (H, Is), 256-byte aligned.
  *   logit_bias: optional fp32 [E] added to the router logits (NULL = none).
+ *   norm_w, norm_eps: the RMSNorm in front of the layer (used with MOE_PRENORM):
+ *     RMSNorm(x)[j] = x[j] * norm_w[j] / sqrt(mean over j of x[j]^2 + norm_eps).
  */
 typedef struct moe_layer {
     int H, E, topk, I, Is;
@@ -129,6 +133,8 @@ typedef struct moe_layer {
     size_t expert_stride;
     const void *shared;
     const float *logit_bias;
+    const float *norm_w; /* RMSNorm weight, fp32 [H], device; read with MOE_PRENORM only */
+    float norm_eps;      /* RMSNorm epsilon (>= 0) */
 } moe_layer_t;
 
 /* ---------------------------------------------------------------- workspace */
@@ -184,6 +190,18 @@ MOE_API int qgemv_affine4(const uint32_t *q, const uint16_t *s, const uint16_t *
                   const float *x, float *y, void *stream);
 
 /*
+ * RMSNorm of T rows (T >= 1) of H values (H a multiple of 4):
+ *   y[t][j] = x[t][j] * w[j] / sqrt(mean over j of x[t][j]^2 + eps)
+ * The pages list an RMSNorm kernel among the engine's own kernels (devtrends page
+ * "Come eseguire un modello da 26 miliardi...", section "Senza dipendenze da
+ * llama.cpp e MLX"; iitog.ru page "TurboFieldfare: движок с открытым кодом...");
+ * this is the plain root-mean-square normalisation.  x, w, y: device fp32 (x and y
+ * [T][H], w [H]); y may alias x.  fp32 arithmetic.  The layer calls apply the same
+ * normalisation inside their kernels with the MOE_PRENORM flag.
+ */
+MOE_API int moe_rmsnorm(const float *x, const float *w, float eps, int T, int H, float *y, void *stream);
+
+/*
  * Router on T tokens (1..MOE_MAX_PREFILL_TOKENS): logits = deq(Wr) x (+ bias),
  * idx = the topk largest logits, larger first, equal -> lower expert index;
  * gate = softmax over the chosen logits.  x device fp32 [T][H]; idx device int32
@@ -207,7 +225,9 @@ typedef struct moe_cache moe_cache_t;
  * vincolo"; 4-bit affine group-64 weights per elsolitario.org "Correr un modelo
  * de 26.000 millones...", section "Detalles tecnicos y rendimiento"):
  *   y_t = sum_k gate_tk * expert_{idx_tk}(x_t) + shared(x_t)   (+ x_t with MOE_RESIDUAL)
- * expert(x) = Wd (gelu_tanh(Wg x) * (Wu x)).  Every distinct expert is read once
+ * expert(x) = Wd (gelu_tanh(Wg x) * (Wu x)).  With MOE_PRENORM the router and the
+ * experts read RMSNorm(x) (see moe_rmsnorm) while MOE_RESIDUAL adds the raw x.  Every
+ * distinct expert is read once
  * for all the tokens that chose it.  x, y: device fp32 [T][H] (y must not alias
  * x).  idx_out / gate_out: optional device outputs [T][topk].
  * cache == NULL: experts come from layer->experts; the call does not synchronise.

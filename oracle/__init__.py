@@ -72,6 +72,7 @@ def _declare(L):
     L.orc_expert.argtypes = [_p, C.c_int, C.c_int, _p, _p, _p]
     L.orc_moe_layer.argtypes = [C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, _p, _p, _p, _p, _p,
                                 _p, C.c_int, _p, C.c_int, _p, _p, _p]
+    L.orc_rmsnorm.argtypes = [_p, _p, C.c_double, C.c_int, C.c_int, _p]
     L.orc_lfu_create.argtypes = [C.c_int, C.c_int]
     L.orc_lfu_create.restype = _p
     L.orc_lfu_destroy.argtypes = [_p]
@@ -226,6 +227,24 @@ def moe_layer(H, E, topk, I, Is, router, experts, shared, x, logit_bias=None, re
                              1 if residual else 0, _ptr(y), _ptr(idx), _ptr(gate))
     _check(rc, "moe_layer")
     return y, idx, gate
+
+
+def rmsnorm(x, g, eps: float) -> np.ndarray:
+    """x [T, H] (or [H]) fp32, g [H] fp32 -> x * g / sqrt(mean(x^2) + eps), fp64."""
+    x2 = _c(np.atleast_2d(x), np.float32)
+    g = _c(g, np.float32)
+    T, H = x2.shape
+    out = np.empty((T, H), np.float64)
+    _check(lib().orc_rmsnorm(_ptr(x2), _ptr(g), float(eps), T, H, _ptr(out)), "rmsnorm")
+    return out if np.ndim(x) == 2 else out[0]
+
+
+def moe_block(H, E, topk, I, Is, router, experts, shared, x, norm_w, norm_eps, logit_bias=None):
+    """The pre-norm MoE block y = x + MoE(RMSNorm(x)).  The layer's input is the
+    normalised x rounded to fp32 (the layer's input type).  -> (y, idx, gate)."""
+    xn = rmsnorm(x, norm_w, norm_eps).astype(np.float32)
+    y, idx, gate = moe_layer(H, E, topk, I, Is, router, experts, shared, xn, logit_bias=logit_bias)
+    return y + np.atleast_2d(x).astype(np.float64), idx, gate
 
 
 def moe_prefill_chunk(*args, **kw):

@@ -422,6 +422,29 @@ done:
     return rc;
 }
 
+/*
+ * RMSNorm of T rows of H values:
+ *   out[t][j] = x[t][j] * g[j] / sqrt(mean over j of x[t][j]^2 + eps).
+ * The pages list an RMSNorm kernel among the engine's own kernels ("Come eseguire
+ * un modello da 26 miliardi...", section "Senza dipendenze da llama.cpp e MLX";
+ * "TurboFieldfare: движок с открытым кодом...", main technical paragraph) without
+ * its formula; this is the plain root-mean-square normalisation (Zhang and
+ * Sennrich, 2019): no mean subtraction, g applied as is.  The MoE block around it
+ * is y = x + MoE(RMSNorm(x)) (pre-norm with the residual).  fp64, the sum of
+ * squares in index order.
+ */
+int orc_rmsnorm(const float *x, const float *g, double eps, int T, int H, double *out) {
+    if (T < 0 || H <= 0 || eps < 0.0 || !x || !g || !out) return ORC_EINVAL;
+    for (int t = 0; t < T; t++) {
+        const float *xt = x + (size_t)t * H;
+        double ss = 0.0;
+        for (int j = 0; j < H; j++) ss += (double)xt[j] * (double)xt[j];
+        const double rms = sqrt(ss / (double)H + eps);
+        for (int j = 0; j < H; j++) out[(size_t)t * H + j] = rms > 0.0 ? (double)xt[j] * (double)g[j] / rms : 0.0;
+    }
+    return ORC_OK;
+}
+
 /* ---- per-layer LFU expert cache ----
  *
  * One call = one step with the request list R (router order; for a batch, the

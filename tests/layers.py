@@ -45,6 +45,20 @@ class OracleLayer:
         s = self.shape
         return oracle.route(*self.router, s.E, s.H, x, topk=s.topk, logit_bias=self.bias)
 
+    def block(self, x, norm_w, norm_eps):
+        """The pre-norm block y = x + MoE(RMSNorm(x)) -> (y, idx, gate)."""
+        s = self.shape
+        xn = oracle.rmsnorm(x, norm_w, norm_eps).astype(np.float32)
+        _, idx, _ = self.route(xn)
+        experts = [None] * s.E
+        for e in np.unique(idx):
+            experts[int(e)] = self.expert(int(e))
+        return oracle.moe_block(s.H, s.E, s.topk, s.I, s.Is, self.router, experts, self.shared, x, norm_w,
+                                norm_eps, logit_bias=self.bias)
+
+    def route_normed(self, x, norm_w, norm_eps):
+        return self.route(oracle.rmsnorm(x, norm_w, norm_eps).astype(np.float32))
+
     def layer(self, x, residual=False):
         s = self.shape
         _, idx, _ = self.route(x)
@@ -55,13 +69,22 @@ class OracleLayer:
                                 logit_bias=self.bias, residual=residual)
 
 
-def gpu_layer(shape, seed=0, layer=0, bias=None, copies=1, router_w=None, edit=None):
+def gpu_layer(shape, seed=0, layer=0, bias=None, copies=1, router_w=None, edit=None, norm=None):
+    """norm = (weight [H], eps) for the MOE_PRENORM calls, or None."""
     import bit_affine_quantised_affine4_b300 as moe
     rw = synth.router_weights(shape, seed, layer) if router_w is None else router_w
-    return moe.make_layer(shape.H, shape.E, shape.topk, shape.I, shape.Is,
-                          np.ascontiguousarray(rw, np.float32),
-                          lambda e: _expert_w(shape, e, seed, layer, edit),
-                          _shared_w(shape, seed, layer, edit), bias=bias, copies=copies)
+    L = moe.make_layer(shape.H, shape.E, shape.topk, shape.I, shape.Is,
+                       np.ascontiguousarray(rw, np.float32),
+                       lambda e: _expert_w(shape, e, seed, layer, edit),
+                       _shared_w(shape, seed, layer, edit), bias=bias, copies=copies)
+    if norm is not None:
+        L.set_norm(norm[0], norm[1])
+    return L
+
+
+def norm_weights(shape, seed=0, layer=0):
+    """A seeded RMSNorm weight: 1 + N(0, 0.1^2) per column."""
+    return (1.0 + synth.normal(synth.key(seed, layer, 99), (shape.H,), 0.1)).astype(np.float32)
 
 
 def within_tol(gpu, ref, rel=2e-3):

@@ -359,6 +359,55 @@ def test_layer_rejects_missing_routed_expert():
         oracle.moe_layer(H, E, 8, I, Is, router, holes, shared, x[:1])
 
 
+# ----------------------------------------------------------------- RMSNorm
+
+def test_rmsnorm_hand_worked_rows():
+    # x = (3, 4): mean of squares 12.5, rms = sqrt(12.5) = 5 / sqrt(2)
+    #   -> (3, 4) * sqrt(2) / 5 = (0.848528137..., 1.131370849...)
+    out = oracle.rmsnorm(np.array([3.0, 4.0], np.float32), np.ones(2, np.float32), 0.0)
+    assert np.allclose(out, [3 * math.sqrt(2) / 5, 4 * math.sqrt(2) / 5], rtol=1e-15, atol=0)
+    # one-hot 3 e_1 in H = 4: mean of squares 9/4, rms 1.5 -> 2 g_1 at index 1, 0 elsewhere
+    g = np.array([0.5, -1.25, 2.0, 3.0], np.float32)
+    out = oracle.rmsnorm(np.array([0.0, 3.0, 0.0, 0.0], np.float32), g, 0.0)
+    assert np.array_equal(out, [0.0, 2 * -1.25, 0.0, 0.0])
+    # a constant row c with eps: g c / sqrt(c^2 + eps) (c = 2, eps = 0.25 -> g 2 / sqrt(4.25))
+    out = oracle.rmsnorm(np.full(8, 2.0, np.float32), np.arange(8, dtype=np.float32), 0.25)
+    assert np.allclose(out, np.arange(8) * 2 / math.sqrt(4.25), rtol=1e-15, atol=0)
+    # a zero row stays zero (eps > 0: no division by zero)
+    assert np.array_equal(oracle.rmsnorm(np.zeros((2, 5), np.float32), np.ones(5, np.float32), 1e-6),
+                          np.zeros((2, 5)))
+
+
+def test_rmsnorm_invariants():
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((3, 96)).astype(np.float32)
+    g = np.ones(96, np.float32)
+    out = oracle.rmsnorm(x, g, 0.0)
+    # unit root mean square per row when g = 1 and eps = 0
+    assert np.allclose(np.sqrt(np.mean(out ** 2, axis=1)), 1.0, rtol=1e-14)
+    # scale invariance (eps = 0): a power-of-two scale is exact in fp32
+    assert np.allclose(oracle.rmsnorm(x * np.float32(8.0), g, 0.0), out, rtol=1e-14)
+    # rows are independent, and g multiplies elementwise
+    g2 = rng.standard_normal(96).astype(np.float32)
+    assert np.allclose(oracle.rmsnorm(x, g2, 0.0), out * g2.astype(np.float64), rtol=1e-14)
+    assert np.array_equal(oracle.rmsnorm(x[1], g2, 1e-5), oracle.rmsnorm(x, g2, 1e-5)[1])
+
+
+def test_prenorm_block_is_residual_plus_layer_of_normalised_input():
+    H, E, I, Is, router, experts, shared, x = _small_layer(seed=12)
+    g = np.linspace(0.5, 1.5, H).astype(np.float32)
+    yb, ib, gb = oracle.moe_block(H, E, 8, I, Is, router, experts, shared, x, g, 1e-6)
+    xn = oracle.rmsnorm(x, g, 1e-6).astype(np.float32)
+    yl, il, gl = oracle.moe_layer(H, E, 8, I, Is, router, experts, shared, xn)
+    assert np.array_equal(ib, il) and np.array_equal(gb, gl)
+    assert np.array_equal(yb, yl + x.astype(np.float64))
+    # the layer sees a normalised input: scaling x by 4 changes only the residual
+    y4, i4, _ = oracle.moe_block(H, E, 8, I, Is, router, experts, shared, x * np.float32(4.0), g, 0.0)
+    y1, i1, _ = oracle.moe_block(H, E, 8, I, Is, router, experts, shared, x, g, 0.0)
+    assert np.array_equal(i4, i1)
+    assert np.allclose(y4 - 4 * x.astype(np.float64), y1 - x.astype(np.float64), rtol=1e-6, atol=1e-9)
+
+
 # ----------------------------------------------------------------- LFU
 
 def _lfu_cases():

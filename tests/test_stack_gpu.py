@@ -16,7 +16,7 @@ import pytest
 
 import oracle
 import synth
-from layers import OracleLayer, gpu_layer, within_tol
+from layers import OracleLayer, gpu_layer, norm_weights, within_tol
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -32,15 +32,22 @@ def _requests(idx):
     return seen
 
 
-@pytest.mark.parametrize("shape_name,layers,slots,steps", [("tiny", 3, 16, 10), ("tiny", 2, 10, 12),
-                                                            ("full", 3, 16, 6)])
-def test_stack_teacher_forced(shape_name, layers, slots, steps):
+@pytest.mark.parametrize("shape_name,layers,slots,steps,prenorm", [("tiny", 3, 16, 10, False),
+                                                                    ("tiny", 2, 10, 12, False),
+                                                                    ("tiny", 3, 16, 8, True),
+                                                                    ("full", 3, 16, 6, True)])
+def test_stack_teacher_forced(shape_name, layers, slots, steps, prenorm):
+    """prenorm: each layer is the pre-norm block h <- h + MoE(RMSNorm(h)), which
+    keeps the activations of a deep stack bounded (the plain residual stack grows
+    layer over layer, GeGLU being quadratic)."""
     import bit_affine_quantised_affine4_b300 as moe
     s = synth.SHAPES[shape_name]
-    gls, ols, caches, views, policies = [], [], [], [], []
+    gls, ols, caches, views, policies, norms = [], [], [], [], [], []
     for l in range(layers):
         bias = synth.popularity_bias(s, seed=0, layer=l)
-        gl = gpu_layer(s, seed=0, layer=l, bias=bias)
+        norm = (norm_weights(s, 0, l), 1e-6) if prenorm else None
+        norms.append(norm)
+        gl = gpu_layer(s, seed=0, layer=l, bias=bias, norm=norm)
         gls.append(gl)
         ols.append(OracleLayer(s, seed=0, layer=l, bias=bias))
         caches.append(moe.Cache(s.H, s.E, s.I, gl.experts[0].cpu().pin_memory(), slots=slots))
@@ -56,10 +63,14 @@ def test_stack_teacher_forced(shape_name, layers, slots, steps):
         h_free = xs[k:k + 1].astype(np.float64)
         for l in range(layers):
             h_in = h.cpu().numpy()
-            y = moe.moe_layer_decode(views[l], h, ws, flags=moe.MOE_RESIDUAL, idx=idx, cache=caches[l])
+            flags = moe.MOE_RESIDUAL | (moe.MOE_PRENORM if prenorm else 0)
+            y = moe.moe_layer_decode(views[l], h, ws, flags=flags, idx=idx, cache=caches[l])
             torch.cuda.synchronize()
             gidx = idx.cpu().numpy()
-            ry, ridx, _ = ols[l].layer(h_in, residual=True)
+            if prenorm:
+                ry, ridx, _ = ols[l].block(h_in, *norms[l])
+            else:
+                ry, ridx, _ = ols[l].layer(h_in, residual=True)
             assert np.array_equal(gidx, ridx), (k, l)
             ok, worst = within_tol(y.cpu().numpy(), ry, TOL)
             assert ok, "step %d layer %d: worst err/bound %.3f" % (k, l, worst)
@@ -68,7 +79,10 @@ def test_stack_teacher_forced(shape_name, layers, slots, steps):
             reos, rcnt, _, _, _ = policies[l].state()
             assert np.array_equal(eos, reos) and np.array_equal(cnt, rcnt), (k, l)
             # the free-running oracle stack, for the report only
-            fy, fidx, _ = ols[l].layer(h_free.astype(np.float32), residual=True)
+            if prenorm:
+                fy, fidx, _ = ols[l].block(h_free.astype(np.float32), *norms[l])
+            else:
+                fy, fidx, _ = ols[l].layer(h_free.astype(np.float32), residual=True)
             if first_divergence is None and not np.array_equal(fidx, gidx):
                 first_divergence = (k, l)
             h_free = fy
