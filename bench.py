@@ -425,12 +425,14 @@ def side_measurements(torch, moe, layer, copies, ws, args):
 
 
 def stack_measurement(torch, moe, args, n_layers=30, steps=256, slots=16):
-    """30-layer MoE stack decode (MoE part only: attention is the identity, each
-    layer adds its output to the residual stream), one token per step, experts in
-    page-locked host memory behind a 16-slot LFU cache per layer.  Routing follows
-    Zipf(1.1) popularity (a per-layer logit bias) and the step inputs are an AR(1)
-    sequence (rho 0.9), so consecutive steps route alike.  Weights come from the
-    GPU's seeded normal generator (N(0, 0.02)), quantised and tiled by the library."""
+    """30-layer MoE stack decode (MoE part only: attention is the identity), one
+    token per step, experts in page-locked host memory behind a 16-slot LFU cache
+    per layer.  Each layer is the pre-norm block h <- h + MoE(RMSNorm(h)) (without
+    the norm the residual stream grows layer over layer).  Routing follows Zipf(1.1)
+    popularity (a per-layer logit bias) and the step inputs are an AR(1) sequence
+    (rho 0.9), so consecutive steps route alike.  Weights come from the GPU's seeded
+    normal generator (N(0, 0.02); RMSNorm weights 1 + N(0, 0.1^2)), quantised and
+    tiled by the library."""
     s = synth.FULL
     dev = torch.device("cuda")
     blob = moe.moe_tile_blob_bytes(H, I)
@@ -447,6 +449,7 @@ def stack_measurement(torch, moe, args, n_layers=30, steps=256, slots=16):
         L.set_shared(torch.randn(2 * IS, H, generator=gen, device=dev) * 0.02,
                      torch.randn(H, IS, generator=gen, device=dev) * 0.02)
         L.set_bias(synth.popularity_bias(s, seed=0, layer=l))
+        L.set_norm(1.0 + 0.1 * torch.randn(H, generator=gen, device=dev), 1e-6)
         try:
             host = torch.empty((E, blob), dtype=torch.uint8).pin_memory()
             host.copy_(L.experts[0])
@@ -468,7 +471,8 @@ def stack_measurement(torch, moe, args, n_layers=30, steps=256, slots=16):
         for st in range(first, first + n):
             cur = X[st:st + 1]
             for l in range(n_layers):
-                moe.moe_layer_decode(views[l], cur, ws, y=h[l & 1], flags=moe.MOE_RESIDUAL, cache=caches[l])
+                moe.moe_layer_decode(views[l], cur, ws, y=h[l & 1], flags=moe.MOE_RESIDUAL | moe.MOE_PRENORM,
+                                     cache=caches[l])
                 cur = h[l & 1]
 
     run(0, warm)
@@ -488,9 +492,9 @@ def stack_measurement(torch, moe, args, n_layers=30, steps=256, slots=16):
            "misses_per_token": misses / n, "h2d_GB_s": h2d / dt / 1e9,
            "host_layers_distinct": n_host,
            "device_bytes_per_token": n_layers * DECODE_BYTES,
-           "note": "per layer the router writes the routing into mapped host memory and a flag the "
-                   "host polls; the host runs the LFU policy; misses are copied on a side stream while "
-                   "the shared expert runs"}
+           "note": "pre-norm blocks h + MoE(RMSNorm(h)); per layer the router writes the routing into "
+                   "mapped host memory and a flag the host polls; the host runs the LFU policy; misses "
+                   "are copied on a side stream while the shared expert runs"}
     out["h2d_link_probe_GB_s"] = h2d_link_probe(torch, caches[0].host_experts)
     out["h2d_link_use"] = out["h2d_GB_s"] / max(out["h2d_link_probe_GB_s"]["expert_copies"], 1e-9)
     for c in caches:
