@@ -35,8 +35,9 @@ ENTRY_POINTS = (
     "moe_layer_prefill_chunk", "moe_cache_create", "moe_cache_destroy",
     "moe_cache_slots", "moe_cache_stats", "moe_layer_decode_noalloc", "moe_layer_decode_host",
     "moe_lfu_create", "moe_lfu_destroy", "moe_lfu_step", "moe_lfu_state",
-    "moe_decode_workspace_bytes", "moe_noalloc_status", "moe_debug_inject", "moe_rmsnorm",
+    "moe_decode_workspace_bytes", "moe_noalloc_status", "moe_debug_inject", "moe_rmsnorm", "moe_sample",
 )
+MOE_SAMPLE_MAX_K = 1024
 
 
 class MoeError(RuntimeError):
@@ -95,6 +96,7 @@ def _load():
     L.moe_noalloc_status.argtypes = [p]
     L.moe_debug_inject.argtypes = [i]
     L.moe_rmsnorm.argtypes = [p, p, C.c_float, i, i, p, p]
+    L.moe_sample.argtypes = [p, i, i, C.c_float, i, C.c_float, p, p, p]
     for name in ENTRY_POINTS:
         if name not in ("moe_status_string", "moe_expert_blob_bytes", "moe_workspace_bytes",
                         "moe_tile_blob_bytes", "moe_decode_workspace_bytes"):
@@ -174,6 +176,15 @@ def moe_rmsnorm(x, w, eps: float, y=None, stream=None):
     y = torch.empty_like(x) if y is None else y
     _check(lib.moe_rmsnorm(_ptr(x), _ptr(w), float(eps), T, H, _ptr(y), _stream(stream)), "moe_rmsnorm")
     return y
+
+
+def moe_sample(logits, temperature: float, top_k: int, top_p: float, u, tokens=None, stream=None):
+    """One token per row of logits (fp32 CUDA [T, V]) with the caller's uniforms u ([T])."""
+    T, V = logits.shape
+    tokens = torch.empty(T, dtype=torch.int32, device=logits.device) if tokens is None else tokens
+    _check(lib.moe_sample(_ptr(logits), T, V, float(temperature), int(top_k), float(top_p), _ptr(u),
+                          _ptr(tokens), _stream(stream)), "moe_sample")
+    return tokens
 
 
 def moe_workspace_bytes(layer: moe_layer_t, T_max: int) -> int:

@@ -15,6 +15,7 @@
 #include "decode.cuh"
 #include "prefill.cuh"
 #include "gemv.cuh"
+#include "sample.cuh"
 #include "lfu.h"
 
 using namespace moe;
@@ -640,6 +641,17 @@ int affine_quantise(const float *w, int N, int K, int bits, uint32_t *q, uint16_
     if (blocks > 0x7fffffffLL) return MOE_EINVAL;
     k_quantise<<<(unsigned)blocks, threads, 0, as_stream(stream)>>>(w, N, K, bits, q, (__half *)s,
                                                                     (__half *)b);
+    return cuda_status();
+}
+
+int moe_sample(const float *logits, int T, int V, float temperature, int top_k, float top_p, const float *u,
+               int32_t *tokens, void *stream) {
+    if (!logits || !u || !tokens || T < 1 || V < 1 || !(top_p > 0.f && top_p <= 1.f) || temperature != temperature)
+        return MOE_EINVAL;
+    if (!aligned(logits, 4) || !aligned(u, 4) || !aligned(tokens, 4)) return MOE_EINVAL;
+    const int K = (top_k <= 0 || top_k >= V) ? V : top_k;
+    if (temperature > 0.f && K > kSampleMaxK) return MOE_EINVAL;
+    k_sample<<<T, kSampleThreads, 0, as_stream(stream)>>>(logits, V, temperature, K, top_p, u, tokens);
     return cuda_status();
 }
 

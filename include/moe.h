@@ -202,6 +202,28 @@ MOE_API int qgemv_affine4(const uint32_t *q, const uint16_t *s, const uint16_t *
 MOE_API int moe_rmsnorm(const float *x, const float *w, float eps, int T, int H, float *y, void *stream);
 
 /*
+ * One token per row of vocabulary logits (the engine samples with temperature,
+ * top-K and top-P, defaults 0.2, 64 and 0.95: elsolitario.org "Correr un modelo de
+ * 26.000 millones...", section "Como empezar"; the pages give the parameters, the
+ * order of the steps is this library's plain reading):
+ *   1. keep the top_k largest logits, larger first, equal -> lower index (top_k <= 0
+ *      or >= V keeps all V);
+ *   2. softmax of the kept logits at the temperature;
+ *   3. keep the shortest prefix, in that order, whose probability reaches top_p
+ *      (at least one token; top_p = 1 keeps all);
+ *   4. return the first kept token whose cumulative weight exceeds u[t] times the
+ *      prefix's total.
+ * temperature <= 0 is greedy (the largest logit, equal -> lower index).
+ * logits: device fp32 [T][V]; u: device fp32 [T], uniform numbers in [0, 1) that
+ * the caller draws (the library has no random state); tokens: device int32 [T].
+ * T >= 1, V >= 1, 0 < top_p <= 1; with temperature > 0 at most 1024 tokens may
+ * survive top-K (MOE_EINVAL otherwise).  fp32 arithmetic, deterministic.
+ */
+#define MOE_SAMPLE_MAX_K 1024
+MOE_API int moe_sample(const float *logits, int T, int V, float temperature, int top_k, float top_p,
+                       const float *u, int32_t *tokens, void *stream);
+
+/*
  * Router on T tokens (1..MOE_MAX_PREFILL_TOKENS): logits = deq(Wr) x (+ bias),
  * idx = the topk largest logits, larger first, equal -> lower expert index;
  * gate = softmax over the chosen logits.  x device fp32 [T][H]; idx device int32

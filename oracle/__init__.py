@@ -73,6 +73,7 @@ def _declare(L):
     L.orc_moe_layer.argtypes = [C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, _p, _p, _p, _p, _p,
                                 _p, C.c_int, _p, C.c_int, _p, _p, _p]
     L.orc_rmsnorm.argtypes = [_p, _p, C.c_double, C.c_int, C.c_int, _p]
+    L.orc_sample.argtypes = [_p, C.c_int, C.c_double, C.c_int, C.c_double, C.c_double, _p, _p]
     L.orc_lfu_create.argtypes = [C.c_int, C.c_int]
     L.orc_lfu_create.restype = _p
     L.orc_lfu_destroy.argtypes = [_p]
@@ -237,6 +238,18 @@ def rmsnorm(x, g, eps: float) -> np.ndarray:
     out = np.empty((T, H), np.float64)
     _check(lib().orc_rmsnorm(_ptr(x2), _ptr(g), float(eps), T, H, _ptr(out)), "rmsnorm")
     return out if np.ndim(x) == 2 else out[0]
+
+
+def sample(logits, temperature: float, top_k: int, top_p: float, u: float):
+    """One token from a row of logits (temperature, top-K, top-P, uniform u).
+    -> (token, margin): margin is the smallest gap between a decision's two sides,
+    relative to the kept total (see orc_sample)."""
+    lg = _c(logits, np.float32)
+    tok = C.c_int32(0)
+    m = C.c_double(0.0)
+    _check(lib().orc_sample(_ptr(lg), lg.size, float(temperature), int(top_k), float(top_p), float(u),
+                            C.byref(tok), C.byref(m)), "sample")
+    return tok.value, m.value
 
 
 def moe_block(H, E, topk, I, Is, router, experts, shared, x, norm_w, norm_eps, logit_bias=None):

@@ -445,6 +445,94 @@ int orc_rmsnorm(const float *x, const float *g, double eps, int T, int H, double
     return ORC_OK;
 }
 
+/*
+ * Token sampling from one row of V logits (the engine's defaults are temperature
+ * 0.2, top-K 64, top-P 0.95: "Correr un modelo de 26.000 millones...", section
+ * "Como empezar"; the pages give the parameters, not the procedure).  The plain
+ * reading, in this order:
+ *   1. top-K: the K largest logits, larger first, equal -> lower index (K <= 0 or
+ *      K >= V keeps all V);
+ *   2. softmax of the kept logits at the temperature: p_i = exp((l_i - l_max) / temp)
+ *      / sum, in fp64;
+ *   3. top-P: the kept tokens in that order; keep the shortest prefix whose
+ *      cumulative probability reaches top_p (at least one token; top_p >= 1 keeps
+ *      all);
+ *   4. draw: with the caller's uniform u in [0, 1), the first kept token j whose
+ *      cumulative probability exceeds u times the prefix's total.
+ * temperature <= 0 is greedy: the largest logit, equal -> lower index.
+ * Writes the token; *margin (if non-null) receives the smallest distance, in
+ * units of the prefix total, between u * total and a cumulative sum, or between
+ * top_p and a cumulative probability -- the decisions a rounding could flip.
+ */
+typedef struct {
+    float v;
+    int i;
+} orc_vi;
+
+static int vi_desc(const void *a, const void *b) {
+    const orc_vi *x = (const orc_vi *)a, *y = (const orc_vi *)b;
+    if (x->v > y->v) return -1;
+    if (x->v < y->v) return 1;
+    return x->i < y->i ? -1 : (x->i > y->i);
+}
+
+int orc_sample(const float *logits, int V, double temperature, int top_k, double top_p, double u,
+               int32_t *token, double *margin) {
+    if (V <= 0 || !logits || !token || !(u >= 0.0 && u < 1.0)) return ORC_EINVAL;
+    orc_vi *s = (orc_vi *)malloc(sizeof(orc_vi) * (size_t)V);
+    double *c = (double *)malloc(sizeof(double) * (size_t)V);
+    if (!s || !c) {
+        free(s);
+        free(c);
+        return ORC_EINVAL;
+    }
+    for (int i = 0; i < V; i++) {
+        s[i].v = logits[i];
+        s[i].i = i;
+    }
+    qsort(s, (size_t)V, sizeof(orc_vi), vi_desc);
+    if (temperature <= 0.0) {
+        *token = s[0].i;
+        if (margin) *margin = 1.0;
+        free(s);
+        free(c);
+        return ORC_OK;
+    }
+    const int K = (top_k <= 0 || top_k >= V) ? V : top_k;
+    double total = 0.0;
+    for (int j = 0; j < K; j++) {
+        total += exp(((double)s[j].v - (double)s[0].v) / temperature);
+        c[j] = total;
+    }
+    int n = K;
+    double m = 1.0;
+    if (top_p < 1.0) {
+        for (int j = 0; j < K; j++) {
+            const double d = c[j] / total - top_p;
+            if (fabs(d) < m) m = fabs(d);
+            if (d >= 0.0) {
+                n = j + 1;
+                break;
+            }
+        }
+    }
+    const double thr = u * c[n - 1];
+    int pick = n - 1;
+    for (int j = 0; j < n; j++) {
+        const double d = (c[j] - thr) / c[n - 1];
+        if (fabs(d) < m) m = fabs(d);
+        if (c[j] > thr) {
+            pick = j;
+            break;
+        }
+    }
+    *token = s[pick].i;
+    if (margin) *margin = m;
+    free(s);
+    free(c);
+    return ORC_OK;
+}
+
 /* ---- per-layer LFU expert cache ----
  *
  * One call = one step with the request list R (router order; for a batch, the

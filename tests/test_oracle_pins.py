@@ -408,6 +408,54 @@ def test_prenorm_block_is_residual_plus_layer_of_normalised_input():
     assert np.allclose(y4 - 4 * x.astype(np.float64), y1 - x.astype(np.float64), rtol=1e-6, atol=1e-9)
 
 
+# ----------------------------------------------------------------- sampling
+
+def test_sample_hand_worked():
+    # logits (1, 3, 2, 3, 0.5), temperature 1, top-K 3: the kept tokens in order are
+    # 1, 3 (tie with 1: the lower index first), 2 with weights 1, 1, e^-1; totals
+    # 1, 2, 2 + e^-1 = 2.3679
+    lg = [1.0, 3.0, 2.0, 3.0, 0.5]
+    e1 = math.exp(-1.0)
+    total = 2.0 + e1
+    # top-P 0.9: the cumulative 1/total, 2/total (0.845) stay below, so all three stay
+    assert oracle.sample(lg, 1.0, 3, 0.9, 0.2)[0] == 1          # 0.2 * total < 1
+    assert oracle.sample(lg, 1.0, 3, 0.9, 0.5)[0] == 3          # 1 <= 0.5 * total < 2
+    assert oracle.sample(lg, 1.0, 3, 0.9, 0.9)[0] == 2          # 0.9 * total >= 2
+    # top-P 0.8: 2 / total = 0.845 reaches it, so tokens 1 and 3 remain (total 2)
+    assert oracle.sample(lg, 1.0, 3, 0.8, 0.9)[0] == 3          # 0.9 * 2 = 1.8 < 2
+    assert oracle.sample(lg, 1.0, 3, 0.8, 0.45)[0] == 1         # 0.9 < 1
+    # the margin of u = 0.5 with top-P 0.9 is the top-P decision: |2 / total - 0.9|
+    assert abs(oracle.sample(lg, 1.0, 3, 0.9, 0.5)[1] - abs(2 / total - 0.9)) < 1e-12
+
+
+def test_sample_greedy_and_degenerate_cuts():
+    rng = np.random.default_rng(7)
+    lg = rng.standard_normal(300).astype(np.float32)
+    lg[[17, 250]] = 9.0  # tied maximum: the lower index wins
+    for u in (0.0, 0.3, 0.999):
+        assert oracle.sample(lg, 0.0, 64, 0.95, u)[0] == 17     # greedy
+        assert oracle.sample(lg, 0.7, 1, 0.95, u)[0] == 17      # top-K 1
+        assert oracle.sample(lg, 0.7, 64, 1e-9, u)[0] == 17     # top-P keeps one token
+    # a power-of-two temperature is a power-of-two rescaling of the logits
+    for u in (0.1, 0.6, 0.95):
+        assert oracle.sample(lg, 2.0, 50, 0.9, u)[0] == oracle.sample(lg / np.float32(2.0), 1.0, 50, 0.9, u)[0]
+
+
+def test_sample_frequencies_are_the_softmax():
+    # no cuts: over a uniform grid of u, token j is drawn for a share of the grid equal
+    # to its softmax probability (to within one grid step per boundary)
+    lg = np.array([0.3, -1.2, 2.0, 0.0, 1.1, -0.4, 0.9], np.float32)
+    temp = 0.8
+    n = 20000
+    counts = np.zeros(lg.size)
+    for k in range(n):
+        counts[oracle.sample(lg, temp, 0, 1.0, (k + 0.5) / n)[0]] += 1
+    z = lg.astype(np.float64) / temp
+    p = np.exp(z - z.max())
+    p /= p.sum()
+    assert np.all(np.abs(counts / n - p) <= 2.0 / n)
+
+
 # ----------------------------------------------------------------- LFU
 
 def _lfu_cases():
