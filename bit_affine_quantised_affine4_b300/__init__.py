@@ -36,6 +36,7 @@ ENTRY_POINTS = (
     "moe_cache_slots", "moe_cache_stats", "moe_layer_decode_noalloc", "moe_layer_decode_host",
     "moe_lfu_create", "moe_lfu_destroy", "moe_lfu_step", "moe_lfu_state",
     "moe_decode_workspace_bytes", "moe_noalloc_status", "moe_debug_inject", "moe_rmsnorm", "moe_sample",
+    "moe_cache_set_device_policy",
 )
 MOE_SAMPLE_MAX_K = 1024
 
@@ -87,6 +88,7 @@ def _load():
     L.moe_cache_destroy.argtypes = [p]
     L.moe_cache_slots.argtypes = [p, p, p]
     L.moe_cache_stats.argtypes = [p, p, p, p]
+    L.moe_cache_set_device_policy.argtypes = [p, i]
     L.moe_lfu_create.argtypes = [p, i, i]
     L.moe_lfu_destroy.argtypes = [p]
     L.moe_lfu_step.argtypes = [p, p, i, p, p]
@@ -337,6 +339,10 @@ class Cache:
             self.close()
         except Exception:
             pass
+
+    def set_device_policy(self, enable: bool = True):
+        """Run the policy on the device: a cached decode then needs no host round trip."""
+        _check(lib.moe_cache_set_device_policy(self.handle, 1 if enable else 0), "moe_cache_set_device_policy")
 
     def slots_state(self):
         import numpy as np

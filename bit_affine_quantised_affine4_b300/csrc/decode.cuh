@@ -95,6 +95,7 @@ struct DecodeArgs {
     const float *gate_pre;   // [T][topk]
     int use_map;             // expert e's blob is experts + slot_map[e] * stride (cache slots)
     short slot_map[MOE_MAX_EXPERTS];
+    const short *slot_dev;   // or, when non-null, the slot of expert e in device memory
     // fault injection (tests of the error path): extra router rows the routing
     // wait expects (0 normally; > 0 makes it unreachable) and that wait's limit
     unsigned route_extra;
@@ -387,7 +388,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
                 S.uexp[u] = e;
                 S.ucnt[u] = cnt;
                 S.ubase[u] = sb + incl - cnt;
-                S.uslot[u] = a.use_map ? a.slot_map[e] : e;
+                S.uslot[u] = a.use_map ? (a.slot_dev ? a.slot_dev[e] : a.slot_map[e]) : e;
             }
             if (warp == nw - 1 && lane == 31) S.U = *err ? 0 : ub + __popc(bal);
         }

@@ -80,6 +80,22 @@ public:
         return 0;
     }
 
+    // Replaces the whole state (expert per slot with -1 = empty, counts, last uses,
+    // the step counter and the running totals).
+    void load(const int *expert_of, const uint32_t *count, const int64_t *last, int64_t step, uint64_t hits,
+              uint64_t misses) {
+        for (int e = 0; e < experts_; e++) where_[e] = -1;
+        for (int s = 0; s < slots_; s++) {
+            expert_[s] = expert_of[s];
+            count_[s] = count[s];
+            last_[s] = last[s];
+            if (expert_[s] >= 0) where_[expert_[s]] = s;
+        }
+        step_ = step;
+        hits_ = hits;
+        misses_ = misses;
+    }
+
     // Marks slot s empty (its contents are no longer known): the expert it held,
     // if any, is no longer resident.  Counts and totals are otherwise unchanged.
     void invalidate(int s) {

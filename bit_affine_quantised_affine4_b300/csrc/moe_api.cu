@@ -111,12 +111,12 @@ int bind_ws(const moe_layer_t *l, int T, void *d_ws, size_t ws_bytes, Ws *out, b
 
 int launch_route(const moe_layer_t *l, const LayerDev &ly, const float *x, int T, Ws ws,
                  int32_t *idx, float *gate, float *logits, cudaStream_t st, int32_t *idx_host = nullptr,
-                 unsigned *flag_host = nullptr, unsigned seq = 0, bool prenorm = false) {
+                 unsigned *flag_host = nullptr, unsigned seq = 0, bool prenorm = false, DevLfu *lfu = nullptr) {
     const dim3 grid((l->E + kRouteExp - 1) / kRouteExp, (T + kRouteTok - 1) / kRouteTok);
     LayerDev lr = ly;
     lr.norm_w = prenorm ? l->norm_w : nullptr;
     lr.norm_eps = l->norm_eps;
-    k_route<<<grid, kRouteTok * 32, 0, st>>>(lr, x, T, ws, idx, gate, logits, idx_host, flag_host, seq);
+    k_route<<<grid, kRouteTok * 32, 0, st>>>(lr, x, T, ws, idx, gate, logits, idx_host, flag_host, seq, lfu);
     return cuda_status();
 }
 
@@ -402,6 +402,11 @@ struct moe_cache {
     int H, E, I, slots, device;
     size_t blob, host_stride;
     const uint8_t *h_experts;
+    // device-resident policy (moe_cache_set_device_policy): the state in device
+    // memory and the device's address of the host blobs
+    int dev_policy = 0;
+    moe::DevLfu *d_lfu = nullptr;
+    const uint8_t *h_experts_dev = nullptr;
     uint8_t *d_slots = nullptr;
     int32_t *h_idx = nullptr;  // page-locked, device-mapped: the step's routing (the router writes it)
     int32_t *d_idx = nullptr;  // its device address
@@ -416,9 +421,47 @@ struct moe_cache {
 
 namespace {
 
+// The cache's policy state as the device keeps it.
+moe::DevLfu dev_state_of(const moe::LfuPolicy &p, uint64_t h2d_bytes) {
+    moe::DevLfu d;
+    memset(&d, 0, sizeof(d));
+    d.slots = p.slots();
+    d.E = p.experts();
+    d.step = p.steps();
+    d.hits = p.hits();
+    d.misses = p.misses();
+    d.h2d_bytes = h2d_bytes;
+    for (int s = 0; s < kDevLfuMaxSlots; s++) {
+        d.expert_of[s] = s < p.slots() ? p.expert_in(s) : -1;
+        d.count[s] = s < p.slots() ? p.count_of(s) : 0u;
+        d.last[s] = s < p.slots() ? p.last_of(s) : 0;
+    }
+    for (int e = 0; e < MOE_MAX_EXPERTS; e++) d.where[e] = (short)(e < p.experts() ? p.slot_of(e) : -1);
+    return d;
+}
+
+// Brings a device-resident policy's state back into the host policy (waits for
+// the device first).
+int cache_pull(moe_cache *c) {
+    if (!c->dev_policy) return MOE_OK;
+    moe::DevLfu d;
+    if (cudaDeviceSynchronize() != cudaSuccess || cudaMemcpy(&d, c->d_lfu, sizeof(d), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return cuda_status();
+    uint32_t cnt[kDevLfuMaxSlots];
+    int64_t last[kDevLfuMaxSlots];
+    for (int s = 0; s < kDevLfuMaxSlots; s++) {
+        cnt[s] = d.count[s];
+        last[s] = d.last[s];
+    }
+    c->policy.load(d.expert_of, cnt, last, d.step, d.hits, d.misses);
+    c->h2d_bytes = d.h2d_bytes;
+    return MOE_OK;
+}
+
 void cache_free(moe_cache *c) {
     if (!c) return;
     if (c->d_slots) cudaFree(c->d_slots);
+    if (c->d_lfu) cudaFree(c->d_lfu);
     if (c->h_idx) cudaFreeHost(c->h_idx);  // h_flag lives in the same allocation
     if (c->ev_copies) cudaEventDestroy(c->ev_copies);
     if (c->side) cudaStreamDestroy(c->side);
@@ -440,6 +483,28 @@ int run_decode_cached(const moe_layer_t *l, const float *x, int T, int flags, fl
     if (rc) return rc;
     cudaStream_t st = as_stream(stream);
     LayerDev ly = layer_dev(l);
+    if (c->dev_policy) {
+        // everything on `stream`, nothing waited for on the host: the router's ranking
+        // CTA runs the policy step, the fetch kernel copies the misses from host
+        // memory into their slots, the decode kernel reads the slot map on the device
+        if (T * l->topk > c->slots) return MOE_ECAPACITY;
+        if ((rc = launch_route(l, ly, x, T, ws, ws.idx, ws.gate, nullptr, st, nullptr, nullptr, 0,
+                               flags & MOE_PRENORM, c->d_lfu)))
+            return rc;
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return cuda_status();
+        k_cache_fetch<<<2 * sms, 256, 0, st>>>(c->d_lfu, c->h_experts_dev, c->host_stride, c->d_slots, c->blob);
+        if ((rc = cuda_status())) return rc;
+        DecodePlan plan;
+        if ((rc = decode_plan(l, x, T, flags, y, idx_out, gate_out, ws, &plan))) return rc;
+        plan.a.experts = c->d_slots;
+        plan.a.stride = c->blob;
+        plan.a.use_map = 1;
+        plan.a.slot_dev = c->d_lfu->where;
+        plan.a.idx_pre = ws.idx;
+        plan.a.gate_pre = ws.gate;
+        return decode_launch(plan, kModeShared | kModeRouted | kModePre, stream);
+    }
     const unsigned seq = ++c->seq == 0 ? ++c->seq : c->seq;  // never 0 (the flag's initial value)
     if ((rc = launch_route(l, ly, x, T, ws, ws.idx, ws.gate, nullptr, st, c->d_idx, c->d_flag, seq,
                            flags & MOE_PRENORM)))
@@ -808,21 +873,55 @@ int moe_cache_create(moe_cache_t **out, int H, int E, int I, const void *h_exper
 int moe_cache_destroy(moe_cache_t *cache) {
     if (!cache) return MOE_OK;
     cudaStreamSynchronize(cache->side);
+    if (cache->dev_policy) cudaDeviceSynchronize();
     cache_free(cache);
     return cuda_status();
 }
 
 int moe_cache_slots(const moe_cache_t *cache, int32_t *expert_of_slot, uint32_t *counts) {
     if (!cache) return MOE_EINVAL;
+    const int rc = cache_pull(const_cast<moe_cache *>(cache));
+    if (rc) return rc;
     policy_state(cache->policy, expert_of_slot, counts, nullptr);
     return MOE_OK;
 }
 
 int moe_cache_stats(const moe_cache_t *cache, uint64_t *hits, uint64_t *misses, uint64_t *h2d_bytes) {
     if (!cache) return MOE_EINVAL;
+    const int rc = cache_pull(const_cast<moe_cache *>(cache));
+    if (rc) return rc;
     if (hits) *hits = cache->policy.hits();
     if (misses) *misses = cache->policy.misses();
     if (h2d_bytes) *h2d_bytes = cache->h2d_bytes;
+    return MOE_OK;
+}
+
+int moe_cache_set_device_policy(moe_cache_t *cache, int enable) {
+    if (!cache) return MOE_EINVAL;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cuda_status();
+    if (dev != cache->device) return MOE_EINVAL;
+    if (!enable) {
+        const int rc = cache_pull(cache);
+        if (rc) return rc;
+        cache->dev_policy = 0;
+        return MOE_OK;
+    }
+    if (cache->dev_policy) return MOE_OK;
+    // the host blobs must be readable by the device (page-locked and mapped)
+    void *hd = nullptr;
+    if (cudaHostGetDevicePointer(&hd, const_cast<uint8_t *>(cache->h_experts), 0) != cudaSuccess || !hd) {
+        (void)cudaGetLastError();
+        return MOE_EINVAL;
+    }
+    if (!aligned(hd, 16) || cache->host_stride % 16) return MOE_EINVAL;
+    if (!cache->d_lfu && cudaMalloc((void **)&cache->d_lfu, sizeof(moe::DevLfu)) != cudaSuccess) return cuda_status();
+    const moe::DevLfu d = dev_state_of(cache->policy, cache->h2d_bytes);
+    if (cudaStreamSynchronize(cache->side) != cudaSuccess ||
+        cudaMemcpy(cache->d_lfu, &d, sizeof(d), cudaMemcpyHostToDevice) != cudaSuccess)
+        return cuda_status();
+    cache->h_experts_dev = (const uint8_t *)hd;
+    cache->dev_policy = 1;
     return MOE_OK;
 }
 

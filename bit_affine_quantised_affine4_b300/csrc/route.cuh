@@ -8,6 +8,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "lfu_dev.cuh"
 
 namespace moe {
 
@@ -191,12 +192,13 @@ __device__ __forceinline__ float rms_inv(float sumsq, int H, float eps) {
 
 // CTA (r, g): router rows 4r..4r+3 for tokens 16g..16g+15, one warp per token
 // over the whole rows.  The last CTA of token group g (a ticket per group) ranks
-// the group's tokens, one warp per token.  When idx_host is set (page-locked host
+// the group's tokens, one warp per token; with a device-resident cache policy
+// (lfu) it then runs the policy's step on the routing.  When idx_host is set (page-locked host
 // memory mapped into the device's address space) the group's choices also go
 // there, followed by flag_host[g] = seq once they are visible to the host.
 __global__ void __launch_bounds__(kRouteTok * 32)
 k_route(LayerDev ly, const float *__restrict__ x, int T, Ws ws, int32_t *idx_out, float *gate_out,
-        float *logits_out, int32_t *idx_host, unsigned *flag_host, unsigned seq) {
+        float *logits_out, int32_t *idx_host, unsigned *flag_host, unsigned seq, DevLfu *lfu) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int e0 = blockIdx.x * kRouteExp, t = blockIdx.y * kRouteTok + warp;
     if (t < T) {
@@ -228,6 +230,11 @@ k_route(LayerDev ly, const float *__restrict__ x, int T, Ws ws, int32_t *idx_out
         warp_topk_softmax(ws.logits + (size_t)t * ly.E, ly.E, ly.topk, idx_out + t * ly.topk,
                           gate_out + t * ly.topk, idx_host ? idx_host + t * ly.topk : nullptr, nullptr);
     if (threadIdx.x == 0) ws.ticket[blockIdx.y] = 0u;
+    if (lfu) {
+        // the cache policy's step on this call's routing (one token group: T <= 16)
+        __syncthreads();
+        if (threadIdx.x == 0) dev_lfu_step(lfu, idx_out, T * ly.topk);
+    }
     if (idx_host) {
         __threadfence_system();
         __syncthreads();

@@ -383,6 +383,26 @@ MOE_API int moe_cache_slots(const moe_cache_t *cache, int32_t *expert_of_slot, u
 MOE_API int moe_cache_stats(const moe_cache_t *cache, uint64_t *hits, uint64_t *misses,
                             uint64_t *h2d_bytes);
 
+/*
+ * Device-resident policy (enable = 1) or host policy (0, the default).  The pages
+ * have the CPU schedule the expert reads while the GPU computes; with the policy on
+ * the device a cached decode needs no host round trip:
+ *   - the router's ranking CTA runs the policy step above on the device;
+ *   - a fetch kernel copies the missing experts from the host blobs (read by the SMs
+ *     through the blobs' device mapping) into their slots;
+ *   - the decode kernel reads each expert's slot from device memory.
+ * The call then returns without waiting for the GPU, like an uncached decode.  The
+ * policy, its tie rules and its statistics are the same in both modes, and
+ * switching carries the state over.
+ * Enabling needs h_experts to be page-locked and mapped into the device's address
+ * space (cudaHostGetDevicePointer succeeds on it; memory from cudaHostAlloc or a
+ * pinned PyTorch tensor is), else MOE_EINVAL.  With the device policy a call needs
+ * T * topk <= slots (the request list then always fits; MOE_ECAPACITY otherwise).
+ * moe_cache_slots and moe_cache_stats wait for the device (cudaDeviceSynchronize)
+ * before they read a device-resident state.  Switching waits as well.
+ */
+MOE_API int moe_cache_set_device_policy(moe_cache_t *cache, int enable);
+
 /* ---------------------------------------------------------------- tests */
 
 /*

@@ -33,15 +33,20 @@ def _requests(idx):
     return seen
 
 
+@pytest.mark.parametrize("policy", ["host", "device"])
 @pytest.mark.parametrize("shape_name,slots,T,steps", [("tiny", 16, 1, 24), ("tiny", 10, 1, 30),
                                                       ("tiny", 16, 2, 12), ("full", 16, 1, 12)])
-def test_cached_decode_matches_oracle_and_policy(shape_name, slots, T, steps):
+def test_cached_decode_matches_oracle_and_policy(shape_name, slots, T, steps, policy):
+    """policy "device": the policy step runs on the GPU and the misses are fetched by
+    a kernel from the mapped host blobs; same slot tables, counts and outputs."""
     import bit_affine_quantised_affine4_b300 as moe
     s = synth.SHAPES[shape_name]
     bias = synth.popularity_bias(s, seed=0)
     gl = gpu_layer(s, seed=0, bias=bias)
     ol = OracleLayer(s, seed=0, bias=bias)
     cache = moe.Cache(s.H, s.E, s.I, _host_experts(gl), slots=slots)
+    if policy == "device":
+        cache.set_device_policy(True)
     policy = oracle.LFU(slots, s.E)
     layer = gl.view(experts=False)
     ws = moe.new_workspace(layer, T)
@@ -64,6 +69,51 @@ def test_cached_decode_matches_oracle_and_policy(shape_name, slots, T, steps):
     assert (hits, misses) == policy.state()[3:]
     assert h2d == misses * moe.moe_tile_blob_bytes(s.H, s.I)
     assert misses > 0 and hits > 0
+    cache.close()
+
+
+def test_policy_switch_keeps_state():
+    """Steps alternate between the host and the device policy; the slot table and the
+    counts follow the oracle's policy throughout."""
+    import bit_affine_quantised_affine4_b300 as moe
+    s = synth.TINY
+    bias = synth.popularity_bias(s, seed=0)
+    gl, ol = gpu_layer(s, seed=0, bias=bias), OracleLayer(s, seed=0, bias=bias)
+    cache = moe.Cache(s.H, s.E, s.I, _host_experts(gl), slots=12)
+    policy = oracle.LFU(12, s.E)
+    layer = gl.view(experts=False)
+    ws = moe.new_workspace(layer, 1)
+    xs = synth.token_sequence(s, 24, seed=1)
+    idx = torch.empty((1, s.topk), dtype=torch.int32, device="cuda")
+    for k in range(24):
+        cache.set_device_policy(k % 6 >= 3)
+        y = moe.moe_layer_decode(layer, torch.from_numpy(xs[k:k + 1]).cuda(), ws, idx=idx, cache=cache)
+        torch.cuda.synchronize()
+        ry, ridx, _ = ol.layer(xs[k:k + 1])
+        assert np.array_equal(idx.cpu().numpy(), ridx), k
+        assert within_tol(y.cpu().numpy(), ry, TOL)[0], k
+        policy.step(_requests(idx.cpu().numpy()))
+        eos, cnt = cache.slots_state()
+        reos, rcnt, _, rh, rm = policy.state()
+        assert np.array_equal(eos, reos) and np.array_equal(cnt, rcnt), k
+        assert cache.stats()[:2] == (rh, rm), k
+    assert cache.stats()[2] == cache.stats()[1] * moe.moe_tile_blob_bytes(s.H, s.I)
+    cache.close()
+
+
+def test_device_policy_capacity_error():
+    import bit_affine_quantised_affine4_b300 as moe
+    s = synth.TINY
+    gl = gpu_layer(s, seed=0)
+    cache = moe.Cache(s.H, s.E, s.I, _host_experts(gl), slots=12)
+    cache.set_device_policy(True)
+    layer = gl.view(experts=False)
+    ws = moe.new_workspace(layer, 2)
+    x = torch.from_numpy(synth.tokens(s, 2, seed=0, stream=3)).cuda()
+    with pytest.raises(moe.MoeError) as e:
+        moe.moe_layer_decode(layer, x, ws, cache=cache)  # 2 tokens x top-8 > 12 slots
+    assert e.value.status == moe.MOE_ECAPACITY
+    assert cache.stats() == (0, 0, 0)
     cache.close()
 
 

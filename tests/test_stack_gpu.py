@@ -32,11 +32,12 @@ def _requests(idx):
     return seen
 
 
-@pytest.mark.parametrize("shape_name,layers,slots,steps,prenorm", [("tiny", 3, 16, 10, False),
-                                                                    ("tiny", 2, 10, 12, False),
-                                                                    ("tiny", 3, 16, 8, True),
-                                                                    ("full", 3, 16, 6, True)])
-def test_stack_teacher_forced(shape_name, layers, slots, steps, prenorm):
+@pytest.mark.parametrize("shape_name,layers,slots,steps,prenorm,policy", [("tiny", 3, 16, 10, False, "host"),
+                                                                           ("tiny", 2, 10, 12, False, "device"),
+                                                                           ("tiny", 3, 16, 8, True, "device"),
+                                                                           ("full", 3, 16, 6, True, "host"),
+                                                                           ("full", 3, 16, 6, True, "device")])
+def test_stack_teacher_forced(shape_name, layers, slots, steps, prenorm, policy):
     """prenorm: each layer is the pre-norm block h <- h + MoE(RMSNorm(h)), which
     keeps the activations of a deep stack bounded (the plain residual stack grows
     layer over layer, GeGLU being quadratic)."""
@@ -51,6 +52,8 @@ def test_stack_teacher_forced(shape_name, layers, slots, steps, prenorm):
         gls.append(gl)
         ols.append(OracleLayer(s, seed=0, layer=l, bias=bias))
         caches.append(moe.Cache(s.H, s.E, s.I, gl.experts[0].cpu().pin_memory(), slots=slots))
+        if policy == "device":
+            caches[-1].set_device_policy(True)
         views.append(gl.view(experts=False))
         policies.append(oracle.LFU(slots, s.E))
     ws = moe.new_workspace(views[0], 1)
