@@ -475,26 +475,39 @@ def stack_measurement(torch, moe, args, n_layers=30, steps=256, slots=16):
                                      cache=caches[l])
                 cur = h[l & 1]
 
+    def timed(first, n):
+        torch.cuda.synchronize()
+        st0 = [c.stats() for c in caches]
+        t0 = time.perf_counter()
+        run(first, n)
+        torch.cuda.synchronize()
+        dt = time.perf_counter() - t0
+        st1 = [c.stats() for c in caches]
+        hits = sum(b[0] - a[0] for a, b in zip(st0, st1))
+        misses = sum(b[1] - a[1] for a, b in zip(st0, st1))
+        h2d = sum(b[2] - a[2] for a, b in zip(st0, st1))
+        return {"steps_timed": n, "tok_s": n / dt, "ms_per_token": dt / n * 1e3,
+                "hit_rate": hits / max(hits + misses, 1), "misses_per_token": misses / n,
+                "h2d_GB_s": h2d / dt / 1e9}
+
+    # the first half of the sequence with the host policy, the second half with the
+    # policy on the device (both on warm caches)
+    half = (steps - warm) // 2
     run(0, warm)
-    torch.cuda.synchronize()
-    st0 = [c.stats() for c in caches]
-    t0 = time.perf_counter()
-    run(warm, steps - warm)
-    torch.cuda.synchronize()
-    dt = time.perf_counter() - t0
-    st1 = [c.stats() for c in caches]
-    hits = sum(b[0] - a[0] for a, b in zip(st0, st1))
-    misses = sum(b[1] - a[1] for a, b in zip(st0, st1))
-    h2d = sum(b[2] - a[2] for a, b in zip(st0, st1))
-    n = steps - warm
-    out = {"layers": n_layers, "steps_timed": n, "slots_per_layer": slots, "tok_s": n / dt,
-           "ms_per_token": dt / n * 1e3, "hit_rate": hits / max(hits + misses, 1),
-           "misses_per_token": misses / n, "h2d_GB_s": h2d / dt / 1e9,
-           "host_layers_distinct": n_host,
-           "device_bytes_per_token": n_layers * DECODE_BYTES,
-           "note": "pre-norm blocks h + MoE(RMSNorm(h)); per layer the router writes the routing into "
-                   "mapped host memory and a flag the host polls; the host runs the LFU policy; misses "
-                   "are copied on a side stream while the shared expert runs"}
+    host = timed(warm, half)
+    for c in caches:
+        c.set_device_policy(True)
+    device = timed(warm + half, half)
+    out = {"layers": n_layers, "slots_per_layer": slots, "host_layers_distinct": n_host,
+           "device_bytes_per_token": n_layers * DECODE_BYTES}
+    out.update(device)
+    out["policy"] = "device"
+    out["host_policy"] = host
+    out["note"] = ("pre-norm blocks h + MoE(RMSNorm(h)).  Device policy: per layer the router's ranking CTA "
+                   "runs the LFU step on device state, a kernel copies the misses from the mapped host "
+                   "blobs, the decode reads the slot map on the device: no host round trip.  Host policy: "
+                   "the router writes the routing into mapped host memory, the host polls a flag, runs "
+                   "the policy and copies the misses on a side stream while the shared expert runs")
     out["h2d_link_probe_GB_s"] = h2d_link_probe(torch, caches[0].host_experts)
     out["h2d_link_use"] = out["h2d_GB_s"] / max(out["h2d_link_probe_GB_s"]["expert_copies"], 1e-9)
     for c in caches:
