@@ -42,7 +42,7 @@ DECODE_BYTES = TOPK * EXPERT_BYTES + SHARED_BYTES + ROUTER_BYTES  # 37,182,464 B
 # `bench.py --quick` (dram__bytes_read.sum + dram__bytes_write.sum); reported only
 # while the decode kernel's sources are the ones it was taken on (their SHA-1
 # without comments)
-DECODE_NCU_TRAFFIC = {"sha1": "5d0fe9df0ac397459068a5379ca49695c60c5d89", "bytes": 37_345_792}
+DECODE_NCU_TRAFFIC = {"sha1": "4b69c1ac4058ccc54de2bc33ac7ba8e2923f12e0", "bytes": 37_313_792}
 DECODE_SOURCES = ["bit_affine_quantised_affine4_b300/csrc/" + f for f in
                   ("decode.cuh", "common.cuh", "mma_core.cuh", "route.cuh", "sync.cuh", "tile.cuh",
                    "moe_api.cu")] + ["include/moe.h"]
@@ -475,11 +475,11 @@ def stack_measurement(torch, moe, args, n_layers=30, steps=256, slots=16):
                                      cache=caches[l])
                 cur = h[l & 1]
 
-    def timed(first, n):
+    def timed(first, n, fn=None):
         torch.cuda.synchronize()
         st0 = [c.stats() for c in caches]
         t0 = time.perf_counter()
-        run(first, n)
+        (fn or run)(first, n)
         torch.cuda.synchronize()
         dt = time.perf_counter() - t0
         st1 = [c.stats() for c in caches]
@@ -490,18 +490,32 @@ def stack_measurement(torch, moe, args, n_layers=30, steps=256, slots=16):
                 "hit_rate": hits / max(hits + misses, 1), "misses_per_token": misses / n,
                 "h2d_GB_s": h2d / dt / 1e9}
 
-    # the first half of the sequence with the host policy, the second half with the
-    # policy on the device (both on warm caches)
-    half = (steps - warm) // 2
+    # a third of the sequence with the host policy, a third with the policy on the
+    # device, the last third with the device policy replayed from a CUDA graph (a
+    # layer call then needs no host involvement at all); all on warm caches
+    third = (steps - warm) // 3
     run(0, warm)
-    host = timed(warm, half)
+    host = timed(warm, third)
     for c in caches:
         c.set_device_policy(True)
-    device = timed(warm + half, half)
+    device = timed(warm + third, third)
+    first = warm + 2 * third
+    st = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=st):
+        run(first, third)
+
+    def replay(first_, n_):
+        with torch.cuda.stream(st):
+            g.replay()
+
+    graph = timed(first, third, replay)
     out = {"layers": n_layers, "slots_per_layer": slots, "host_layers_distinct": n_host,
            "device_bytes_per_token": n_layers * DECODE_BYTES}
-    out.update(device)
-    out["policy"] = "device"
+    out.update(graph)
+    out["policy"] = "device, CUDA graph of the steps"
+    out["device_policy_eager"] = device
     out["host_policy"] = host
     out["note"] = ("pre-norm blocks h + MoE(RMSNorm(h)).  Device policy: per layer the router's ranking CTA "
                    "runs the LFU step on device state, a kernel copies the misses from the mapped host "
