@@ -136,6 +136,25 @@ int check_layer_call(const moe_layer_t *l, const float *x, int T, int Tlimit, in
     return MOE_OK;
 }
 
+// The device's address of a page-locked host buffer mapped into its address space
+// (null when p is null or not such a buffer).
+template <typename T>
+T *mapped_alias(T *p) {
+    if (!p) return nullptr;
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    if (at.type != cudaMemoryTypeHost || !at.devicePointer) return nullptr;
+    return reinterpret_cast<T *>(at.devicePointer);
+}
+
+__global__ void __launch_bounds__(256) k_copy16(const uint4 *__restrict__ src, uint4 *__restrict__ dst, size_t n) {
+    const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n) dst[i] = src[i];
+}
+
 // RMSNorm, one CTA per row: y = x * w / sqrt(mean(x^2) + eps).
 __global__ void __launch_bounds__(256) k_rmsnorm(const float *x, const float *__restrict__ w, float eps, int H,
                                                  float *y) {
@@ -763,7 +782,11 @@ int moe_layer_decode(const moe_layer_t *layer, const float *x, int T, int flags,
 }
 
 // Host buffers: x is staged in the workspace, the decode step runs on the stream,
-// y (and the routing) come back; the call returns once the stream is idle.
+// y (and the routing) come back; the call returns once the stream is idle.  Where a
+// host buffer is page-locked and mapped into the device's address space, the copies
+// are kernels' plain accesses instead of DMA transfers (whose set-up dominates at
+// these sizes): a small kernel reads x into the workspace, and the decode kernel
+// writes y, idx and gate straight into host memory.
 int moe_layer_decode_host(const moe_layer_t *layer, const float *x_host, int T, int flags, float *y_host,
                           int32_t *idx_host, float *gate_host, moe_cache_t *cache, void *d_ws, size_t ws_bytes,
                           void *stream) {
@@ -774,14 +797,29 @@ int moe_layer_decode_host(const moe_layer_t *layer, const float *x_host, int T, 
     if (rc) return rc;
     cudaStream_t st = as_stream(stream);
     const size_t xb = sizeof(float) * (size_t)T * layer->H, rb = (size_t)T * layer->topk;
-    if (cudaMemcpyAsync(ws.xh, x_host, xb, cudaMemcpyHostToDevice, st) != cudaSuccess) return cuda_status();
-    rc = moe_layer_decode(layer, ws.xh, T, flags, ws.yh, idx_host ? ws.ih : nullptr, gate_host ? ws.gh : nullptr,
+    const float *xd = mapped_alias(x_host);
+    float *yd = mapped_alias(y_host), *gd = mapped_alias(gate_host);
+    int32_t *id = mapped_alias(idx_host);
+    if (xd && aligned(xd, 16)) {
+        k_copy16<<<(unsigned)((xb / 16 + 255) / 256), 256, 0, st>>>(reinterpret_cast<const uint4 *>(xd),
+                                                                  reinterpret_cast<uint4 *>(ws.xh), xb / 16);
+        if ((rc = cuda_status())) return rc;
+    } else if (cudaMemcpyAsync(ws.xh, x_host, xb, cudaMemcpyHostToDevice, st) != cudaSuccess) {
+        return cuda_status();
+    }
+    const bool y_direct = yd && aligned(yd, 16) && !cache;
+    const bool i_direct = id && !cache, g_direct = gd && !cache;
+    rc = moe_layer_decode(layer, ws.xh, T, flags, y_direct ? yd : ws.yh,
+                          idx_host ? (i_direct ? id : ws.ih) : nullptr, gate_host ? (g_direct ? gd : ws.gh) : nullptr,
                           cache, d_ws, ws_bytes, stream);
     if (rc) return rc;
-    if (cudaMemcpyAsync(y_host, ws.yh, xb, cudaMemcpyDeviceToHost, st) != cudaSuccess) return cuda_status();
-    if (idx_host && cudaMemcpyAsync(idx_host, ws.ih, sizeof(int32_t) * rb, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    if (!y_direct && cudaMemcpyAsync(y_host, ws.yh, xb, cudaMemcpyDeviceToHost, st) != cudaSuccess)
         return cuda_status();
-    if (gate_host && cudaMemcpyAsync(gate_host, ws.gh, sizeof(float) * rb, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    if (idx_host && !i_direct &&
+        cudaMemcpyAsync(idx_host, ws.ih, sizeof(int32_t) * rb, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return cuda_status();
+    if (gate_host && !g_direct &&
+        cudaMemcpyAsync(gate_host, ws.gh, sizeof(float) * rb, cudaMemcpyDeviceToHost, st) != cudaSuccess)
         return cuda_status();
     // wait for the stream by polling it: a decode step is a few tens of
     // microseconds, shorter than the wake-up of a blocking wait

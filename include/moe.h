@@ -288,8 +288,11 @@ MOE_API int moe_layer_prefill_chunk(const moe_layer_t *layer, const float *x, in
  * y and the routing), runs the decode step on `stream` (through `cache` when it is
  * non-null), copies y and the requested routing back, and waits for `stream`
  * (polling it, so the calling thread stays busy meanwhile) before it returns: the
- * outputs are ready on return.  x_host and y_host must not
- * overlap.  Same workspace (moe_workspace_bytes) and error codes as
+ * outputs are ready on return.  Page-locked buffers that are mapped into the
+ * device's address space (cudaHostAlloc memory, a pinned PyTorch tensor) skip the
+ * DMA copies: a small kernel reads x from host memory and, without a cache, the
+ * decode kernel writes y and the routing straight into host memory.  x_host and
+ * y_host must not overlap.  Same workspace (moe_workspace_bytes) and error codes as
  * moe_layer_decode; MOE_ECUDA if a copy or the stream wait fails.
  */
 MOE_API int moe_layer_decode_host(const moe_layer_t *layer, const float *x_host, int T, int flags,

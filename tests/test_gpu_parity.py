@@ -191,19 +191,22 @@ def test_decode_full_zipf_batch(moe, full_zipf, T):
     _layer_check(moe, s, gl, ol, T, 300 + T)
 
 
+@pytest.mark.parametrize("pinned", [True, False], ids=["pinned", "pageable"])
 @pytest.mark.parametrize("T", [1, 5, 16])
-def test_decode_host_buffers(moe, tiny, T):
+def test_decode_host_buffers(moe, tiny, T, pinned):
     # moe_layer_decode_host: host x/y/idx/gate, copies and the stream wait inside the
-    # call; the result equals the device-pointer call's and is within the oracle's
-    # tolerance
+    # call (pinned, mapped buffers: kernels read and write host memory directly;
+    # pageable ones: DMA copies through the workspace); the result equals the
+    # device-pointer call's and is within the oracle's tolerance
     s, gl, ol = tiny
     x = synth.tokens(s, T, seed=0, stream=700 + T)
     layer = gl.view()
     ws = moe.new_workspace(layer, T)
-    xh = torch.from_numpy(x).pin_memory()
-    yh = torch.empty_like(xh).pin_memory()
-    ih = torch.empty((T, s.topk), dtype=torch.int32).pin_memory()
-    gh = torch.empty((T, s.topk), dtype=torch.float32).pin_memory()
+    pin = (lambda t: t.pin_memory()) if pinned else (lambda t: t)
+    xh = pin(torch.from_numpy(x))
+    yh = pin(torch.full_like(xh, float("nan")))
+    ih = pin(torch.full((T, s.topk), -1, dtype=torch.int32))
+    gh = pin(torch.empty((T, s.topk), dtype=torch.float32))
     moe.moe_layer_decode_host(layer, xh, ws, y=yh, flags=moe.MOE_RESIDUAL, idx=ih, gate=gh)
     assert moe.moe_workspace_status(ws) == moe.MOE_OK
     yd = moe.moe_layer_decode(layer, _cuda(x), ws, flags=moe.MOE_RESIDUAL)
