@@ -307,11 +307,12 @@ def run_ours(args):
     xh = torch.from_numpy(synth.tokens(synth.FULL, NX, seed=0, stream=rank)).pin_memory()
     yh = torch.empty((NX, H)).pin_memory()
     st = torch.cuda.Stream()
+    xrows = [xh[i:i + 1] for i in range(NX)]  # a caller's per-token host buffers
+    yrows = [yh[i:i + 1] for i in range(NX)]
 
     def e2e_steps(n, first):
         for i in range(first, first + n):
-            moe.moe_layer_decode_host(views[i % copies], xh[i % NX:i % NX + 1], ws, y=yh[i % NX:i % NX + 1],
-                                      stream=st)
+            moe.moe_layer_decode_host(views[i % copies], xrows[i % NX], ws, y=yrows[i % NX], stream=st)
 
     e2e_steps(args.warmup, 0)
     torch.cuda.synchronize()
@@ -352,8 +353,9 @@ def run_ours(args):
                      "peak_source": peaks["source"], "kernel": "moe_layer_decode (whole call)"},
         "e2e": {"value": job_rate(world, args.steps, e2e_dt), "unit": "tok/s",
                 "h2d_bytes_per_step": H * 4, "d2h_bytes_per_step": H * 4,
-                "note": "moe_layer_decode_host through the Python binding, one call per step: "
-                        "H2D of x from pinned memory + decode + D2H of y + stream wait"},
+                "note": "moe_layer_decode_host through the Python binding, one call per step on pinned "
+                        "host rows: x read and y written by the kernels through the rows' device "
+                        "mapping, then the call polls the stream until y is in host memory"},
         "gpu_launches": args.steps,  # one persistent k_decode launch per step
         "clocks": clocks,
     }

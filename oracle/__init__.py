@@ -74,6 +74,9 @@ def _declare(L):
                                 _p, C.c_int, _p, C.c_int, _p, _p, _p]
     L.orc_rmsnorm.argtypes = [_p, _p, C.c_double, C.c_int, C.c_int, _p]
     L.orc_sample.argtypes = [_p, C.c_int, C.c_double, C.c_int, C.c_double, C.c_double, _p, _p]
+    L.orc_attn_step.argtypes = [C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, C.c_double, C.c_double,
+                                _p, _p, _p, _p, _p, _p, _p, C.c_double, C.c_int, _p, _p, _p, C.c_int, C.c_int,
+                                _p, _p]
     L.orc_lfu_create.argtypes = [C.c_int, C.c_int]
     L.orc_lfu_create.restype = _p
     L.orc_lfu_destroy.argtypes = [_p]
@@ -258,6 +261,33 @@ def moe_block(H, E, topk, I, Is, router, experts, shared, x, norm_w, norm_eps, l
     xn = rmsnorm(x, norm_w, norm_eps).astype(np.float32)
     y, idx, gate = moe_layer(H, E, topk, I, Is, router, experts, shared, xn, logit_bias=logit_bias)
     return y + np.atleast_2d(x).astype(np.float64), idx, gate
+
+
+def attn_step(H: int, nq: int, nkv: int, d: int, window: int, kv_len: int, theta: float, scale: float,
+              wqkv, wo, k_cache, v_cache, x, pos: int, residual: bool = True, norm_w=None,
+              norm_eps: float = 1e-6):
+    """One attention block over the tokens x [T, H] at positions pos .. pos+T-1.
+
+    wqkv / wo = (q, s, b) 4-bit affine of [(nq + 2 nkv) d, H] / [H, nq d].  k_cache,
+    v_cache: uint16 (binary16 bits) [nkv, kv_len, d], updated in place.
+    -> (y fp64 [T, H], o fp64 [T, nq d] the attention output before Wo)."""
+    for c in (k_cache, v_cache):
+        if c.dtype != np.uint16 or not c.flags.c_contiguous or c.shape != (nkv, kv_len, d):
+            raise ValueError("caches must be C-contiguous uint16 [nkv, kv_len, d]")
+    qq, qs, qb = (_c(a, t) for a, t in zip(wqkv, (np.uint32, np.uint16, np.uint16)))
+    oq, os_, ob = (_c(a, t) for a, t in zip(wo, (np.uint32, np.uint16, np.uint16)))
+    x2 = _c(np.atleast_2d(x), np.float32)
+    T = x2.shape[0]
+    nw = None if norm_w is None else _c(norm_w, np.float32)
+    y = np.empty((T, H), np.float64)
+    o = np.empty((T, nq * d), np.float64)
+    rc = lib().orc_attn_step(H, nq, nkv, d, window, kv_len, theta, scale, _ptr(qq), _ptr(qs), _ptr(qb),
+                             _ptr(oq), _ptr(os_), _ptr(ob), _ptr(nw), norm_eps, int(bool(residual)),
+                             _ptr(k_cache), _ptr(v_cache), _ptr(x2), T, pos, _ptr(y), _ptr(o))
+    if rc == ORC_ECAPACITY:
+        raise ValueError("oracle attn_step: positions do not fit the cache")
+    _check(rc, "attn_step")
+    return y, o
 
 
 def moe_prefill_chunk(*args, **kw):

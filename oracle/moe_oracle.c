@@ -646,3 +646,132 @@ void orc_lfu_state(const orc_lfu *c, int32_t *expert_of_slot, uint32_t *count, i
     if (hits) *hits = c->hits;
     if (misses) *misses = c->misses;
 }
+
+/* ---- attention block with an FP16 key/value cache ---- */
+
+/*
+ * One attention block over T consecutive tokens of one sequence, at positions
+ * pos .. pos+T-1.  The pages name the pieces: the engine's own kernels compute a
+ * quantised GEMV, attention, RMSNorm and RoPE; the projections are 4-bit MLX affine
+ * weights; the key/value cache is FP16, a bounded ring for the 25 sliding-window
+ * layers and a linear store for the 5 full-attention layers, 4096 tokens in the
+ * measured setup ("TurboFieldfare: движок с открытым кодом...", main technical
+ * paragraph; "TurboFieldfare esegue Mac Gemma 4 26B in 2 GB...", section "Mac Gemma 4
+ * 26B entra nello spazio disponibile...").  They give no shapes or formulas, so the
+ * plain readings (each listed in the design notes) are:
+ *   - tokens are taken one after another; each is written into the cache before
+ *     it attends, so it sees itself;
+ *   - xn = RMSNorm(x) when norm_w is given (pre-norm), else x;
+ *   - [q; k; v] = Wqkv xn, Wqkv [(nq + 2 nkv) d][H] with the nq query heads, then
+ *     the nkv key heads, then the nkv value heads, d rows each;
+ *   - RoPE, rotate-half pairing: for i < d/2 and angle a = p * theta^(-2i/d),
+ *     (u_i, u_{i+d/2}) -> (u_i cos a - u_{i+d/2} sin a, u_{i+d/2} cos a + u_i sin a),
+ *     applied to every query and key head at the token's own position p;
+ *   - the cache holds the rotated keys and the values rounded to binary16, laid
+ *     out [nkv][kv_len][d]; a sliding layer (window > 0) keeps position j in slot
+ *     j mod kv_len and attends to positions max(0, p - window + 1) .. p; a full
+ *     layer (window == 0) keeps j in slot j and attends to 0 .. p;
+ *   - query head h reads key/value head h / (nq / nkv) (grouped queries);
+ *     scores s_j = scale * q_h . k_j, weights softmax(s) over the attended
+ *     positions, o_h = sum_j w_j v_j;
+ *   - y = Wo o (+ x when residual), Wo [H][nq d].
+ * Everything in fp64 except the cache, which is binary16 as the pages state.
+ * The cache arrays are read and updated in place; attn_out (optional) receives
+ * o [T][nq d].
+ */
+static double pow_neg(double theta, int i2, int d) { return pow(theta, -(double)i2 / (double)d); }
+
+static void rope_fp64(double *u, int d, int p, double theta) {
+    for (int i = 0; i < d / 2; i++) {
+        const double a = (double)p * pow_neg(theta, 2 * i, d);
+        const double c = cos(a), s = sin(a);
+        const double lo = u[i], hi = u[i + d / 2];
+        u[i] = lo * c - hi * s;
+        u[i + d / 2] = hi * c + lo * s;
+    }
+}
+
+static uint16_t double_to_half(double v) {
+    _Float16 h = (_Float16)v;
+    uint16_t r;
+    memcpy(&r, &h, 2);
+    return r;
+}
+
+int orc_attn_step(int H, int nq, int nkv, int d, int window, int kv_len, double theta, double scale,
+                  const uint32_t *wqkv_q, const uint16_t *wqkv_s, const uint16_t *wqkv_b,
+                  const uint32_t *wo_q, const uint16_t *wo_s, const uint16_t *wo_b,
+                  const float *norm_w, double eps, int residual, uint16_t *k_cache, uint16_t *v_cache,
+                  const float *x, int T, int pos, double *y, double *attn_out) {
+    if (H <= 0 || H % GROUP || nq <= 0 || nkv <= 0 || nq % nkv || d <= 0 || d % 2 || (nq * d) % GROUP ||
+        window < 0 || kv_len <= 0 || T < 0 || pos < 0 || !k_cache || !v_cache || !x || !y || theta <= 0.0)
+        return ORC_EINVAL;
+    if (window > 0 ? kv_len < window : pos + T > kv_len) return ORC_ECAPACITY;
+    const int G = nq / nkv, nqkv = (nq + 2 * nkv) * d, no = nq * d;
+    double *xn = malloc(sizeof(double) * H), *qkv = malloc(sizeof(double) * nqkv);
+    double *o = malloc(sizeof(double) * no), *sc = malloc(sizeof(double) * (size_t)(pos + T));
+    if (!xn || !qkv || !o || !sc) {
+        free(xn); free(qkv); free(o); free(sc);
+        return ORC_EINVAL;
+    }
+    for (int t = 0; t < T; t++) {
+        const int p = pos + t;
+        const float *xt = x + (size_t)t * H;
+        if (norm_w) {
+            double ss = 0.0;
+            for (int j = 0; j < H; j++) ss += (double)xt[j] * (double)xt[j];
+            const double rms = sqrt(ss / (double)H + eps);
+            for (int j = 0; j < H; j++) xn[j] = rms > 0.0 ? (double)xt[j] * (double)norm_w[j] / rms : 0.0;
+        } else {
+            for (int j = 0; j < H; j++) xn[j] = (double)xt[j];
+        }
+#pragma omp parallel for schedule(static)
+        for (int n = 0; n < nqkv; n++) {
+            double acc = 0.0;
+            for (int j = 0; j < H; j++) acc += deq_at(wqkv_q, wqkv_s, wqkv_b, H, 4, n, j) * xn[j];
+            qkv[n] = acc;
+        }
+        for (int h = 0; h < nq + nkv; h++) rope_fp64(qkv + (size_t)h * d, d, p, theta);
+        const int slot = window > 0 ? p % kv_len : p;
+        for (int g = 0; g < nkv; g++)
+            for (int i = 0; i < d; i++) {
+                const size_t at = ((size_t)g * kv_len + slot) * d + i;
+                k_cache[at] = double_to_half(qkv[(size_t)(nq + g) * d + i]);
+                v_cache[at] = double_to_half(qkv[(size_t)(nq + nkv + g) * d + i]);
+            }
+        const int lo = window > 0 ? (p - window + 1 > 0 ? p - window + 1 : 0) : 0;
+        for (int h = 0; h < nq; h++) {
+            const int g = h / G;
+            const double *qh = qkv + (size_t)h * d;
+            double m = -INFINITY;
+            for (int j = lo; j <= p; j++) {
+                const int sl = window > 0 ? j % kv_len : j;
+                const uint16_t *kj = k_cache + ((size_t)g * kv_len + sl) * d;
+                double s = 0.0;
+                for (int i = 0; i < d; i++) s += qh[i] * orc_half_to_double(kj[i]);
+                sc[j] = scale * s;
+                if (sc[j] > m) m = sc[j];
+            }
+            double den = 0.0;
+            for (int j = lo; j <= p; j++) den += exp(sc[j] - m);
+            double *oh = o + (size_t)h * d;
+            for (int i = 0; i < d; i++) oh[i] = 0.0;
+            for (int j = lo; j <= p; j++) {
+                const int sl = window > 0 ? j % kv_len : j;
+                const uint16_t *vj = v_cache + ((size_t)g * kv_len + sl) * d;
+                const double w = exp(sc[j] - m) / den;
+                for (int i = 0; i < d; i++) oh[i] += w * orc_half_to_double(vj[i]);
+            }
+        }
+        if (attn_out)
+            for (int i = 0; i < no; i++) attn_out[(size_t)t * no + i] = o[i];
+#pragma omp parallel for schedule(static)
+        for (int n = 0; n < H; n++) {
+            double acc = residual ? (double)xt[n] : 0.0;
+            for (int i = 0; i < no; i++) acc += deq_at(wo_q, wo_s, wo_b, no, 4, n, i) * o[i];
+            y[(size_t)t * H + n] = acc;
+        }
+    }
+    free(xn); free(qkv); free(o); free(sc);
+    return ORC_OK;
+}

@@ -10,6 +10,13 @@ Workloads (weights N(0, 0.02) before quantisation, tokens N(0, 1)):
 * ``tiny``   hidden 512, 32 experts, top-8, expert inter 256, shared inter 512
 * ``full``   hidden 2816, 128 experts, top-8, expert inter 704, shared inter 2112
   (uniform router logits, or Zipf(1.1) popularity through a logit bias)
+
+Attention blocks (``AttnShape``; weights N(0, 0.02), cached keys/values N(0, 1)):
+
+* ``attn-tiny-sliding`` / ``attn-tiny-full``  hidden 512, 4 query heads, 2 key/value
+  heads of 64, window 16 in a ring of 23 / linear store of 96
+* ``attn-full-sliding`` / ``attn-full-global`` hidden 2816, 16 query heads, 8
+  key/value heads of 256, window 1024 in a ring of 1151 / linear store of 4096
 """
 from __future__ import annotations
 
@@ -25,7 +32,8 @@ _SRC = os.path.join(_HERE, "synth.c")
 _LIB = os.path.join(_HERE, "libsynth.so")
 
 # sub-stream ids
-T_ROUTER, T_EXPERT_GU, T_EXPERT_D, T_SHARED_GU, T_SHARED_D, T_TOKENS, T_ZIPF, T_AR1 = range(8)
+(T_ROUTER, T_EXPERT_GU, T_EXPERT_D, T_SHARED_GU, T_SHARED_D, T_TOKENS, T_ZIPF, T_AR1, T_ATTN_QKV, T_ATTN_O,
+ T_KV, T_NORM) = range(12)
 
 
 @dataclass(frozen=True)
@@ -41,6 +49,34 @@ class Shape:
 TINY = Shape("tiny", 512, 32, 8, 256, 512)
 FULL = Shape("full", 2816, 128, 8, 704, 2112)
 SHAPES = {"tiny": TINY, "full": FULL}
+
+@dataclass(frozen=True)
+class AttnShape:
+    """One attention block: window > 0 is a sliding-window layer whose cache is a ring
+    of kv_len entries; window == 0 is a full layer with a linear store of kv_len."""
+    name: str
+    H: int
+    nq: int
+    nkv: int
+    d: int
+    window: int
+    kv_len: int
+    theta: float
+
+    @property
+    def scale(self) -> float:
+        return self.d ** -0.5
+
+    @property
+    def n_qkv(self) -> int:
+        return (self.nq + 2 * self.nkv) * self.d
+
+
+ATTN_TINY_SLIDING = AttnShape("attn-tiny-sliding", 512, 4, 2, 64, 16, 23, 10000.0)
+ATTN_TINY_FULL = AttnShape("attn-tiny-full", 512, 4, 2, 64, 0, 96, 1000000.0)
+ATTN_FULL_SLIDING = AttnShape("attn-full-sliding", 2816, 16, 8, 256, 1024, 1151, 10000.0)
+ATTN_FULL_GLOBAL = AttnShape("attn-full-global", 2816, 16, 8, 256, 0, 4096, 1000000.0)
+ATTN_SHAPES = {a.name: a for a in (ATTN_TINY_SLIDING, ATTN_TINY_FULL, ATTN_FULL_SLIDING, ATTN_FULL_GLOBAL)}
 
 WEIGHT_SIGMA = 0.02
 ZIPF_S = 1.1
@@ -147,3 +183,21 @@ def popularity_bias(shape: Shape, seed: int = 0, layer: int = 0, s: float = ZIPF
 
 def token_sequence(shape: Shape, steps: int, seed: int = 0, rho: float = AR1_RHO) -> np.ndarray:
     return ar1(key(seed, 0, T_AR1), steps, shape.H, rho)
+
+
+def attn_weights(shape: AttnShape, seed: int = 0, layer: int = 0):
+    """-> (Wqkv [(nq + 2 nkv) d, H]: query heads, key heads, value heads; Wo [H, nq d]) fp32."""
+    wqkv = normal(key(seed, layer, T_ATTN_QKV), (shape.n_qkv, shape.H), WEIGHT_SIGMA)
+    wo = normal(key(seed, layer, T_ATTN_O), (shape.H, shape.nq * shape.d), WEIGHT_SIGMA)
+    return wqkv, wo
+
+
+def kv_history(shape: AttnShape, seed: int = 0, layer: int = 0):
+    """Stand-in for the keys and values of earlier tokens: fp32 N(0, 1), [2][nkv][kv_len][d]
+    (keys, then values); the caller stores them at the cache's precision."""
+    return normal(key(seed, layer, T_KV), (2, shape.nkv, shape.kv_len, shape.d), 1.0)
+
+
+def norm_weights(H: int, seed: int = 0, layer: int = 0) -> np.ndarray:
+    """RMSNorm gains around 1: 1 + 0.1 N(0, 1)."""
+    return (1.0 + normal(key(seed, layer, T_NORM), (H,), 0.1)).astype(np.float32)
