@@ -36,7 +36,7 @@ ENTRY_POINTS = (
     "moe_cache_slots", "moe_cache_stats", "moe_layer_decode_noalloc", "moe_layer_decode_host",
     "moe_lfu_create", "moe_lfu_destroy", "moe_lfu_step", "moe_lfu_state",
     "moe_decode_workspace_bytes", "moe_noalloc_status", "moe_debug_inject", "moe_rmsnorm", "moe_sample",
-    "moe_cache_set_device_policy",
+    "moe_cache_set_device_policy", "moe_attn_workspace_bytes", "moe_attn_step", "moe_attn_workspace_status",
 )
 MOE_SAMPLE_MAX_K = 1024
 
@@ -54,6 +54,17 @@ class moe_layer_t(C.Structure):
         ("experts", C.c_void_p), ("expert_stride", C.c_size_t),
         ("shared", C.c_void_p), ("logit_bias", C.c_void_p),
         ("norm_w", C.c_void_p), ("norm_eps", C.c_float),
+    ]
+
+
+class moe_attn_t(C.Structure):
+    _fields_ = [
+        ("H", C.c_int), ("nq", C.c_int), ("nkv", C.c_int), ("d", C.c_int),
+        ("window", C.c_int), ("kv_len", C.c_int), ("theta", C.c_float), ("scale", C.c_float),
+        ("wqkv_q", C.c_void_p), ("wqkv_s", C.c_void_p), ("wqkv_b", C.c_void_p),
+        ("wo_q", C.c_void_p), ("wo_s", C.c_void_p), ("wo_b", C.c_void_p),
+        ("norm_w", C.c_void_p), ("norm_eps", C.c_float),
+        ("k_cache", C.c_void_p), ("v_cache", C.c_void_p),
     ]
 
 
@@ -99,9 +110,13 @@ def _load():
     L.moe_debug_inject.argtypes = [i]
     L.moe_rmsnorm.argtypes = [p, p, C.c_float, i, i, p, p]
     L.moe_sample.argtypes = [p, i, i, C.c_float, i, C.c_float, p, p, p]
+    L.moe_attn_workspace_bytes.argtypes = [p, i]
+    L.moe_attn_workspace_bytes.restype = sz
+    L.moe_attn_step.argtypes = [p, p, i, i, i, p, p, p, sz, p]
+    L.moe_attn_workspace_status.argtypes = [p, sz, p]
     for name in ENTRY_POINTS:
         if name not in ("moe_status_string", "moe_expert_blob_bytes", "moe_workspace_bytes",
-                        "moe_tile_blob_bytes", "moe_decode_workspace_bytes"):
+                        "moe_tile_blob_bytes", "moe_decode_workspace_bytes", "moe_attn_workspace_bytes"):
             getattr(L, name).restype = i
     return L
 
@@ -178,6 +193,34 @@ def moe_rmsnorm(x, w, eps: float, y=None, stream=None):
     y = torch.empty_like(x) if y is None else y
     _check(lib.moe_rmsnorm(_ptr(x), _ptr(w), float(eps), T, H, _ptr(y), _stream(stream)), "moe_rmsnorm")
     return y
+
+
+def moe_attn_workspace_bytes(attn: moe_attn_t, T_max: int) -> int:
+    return int(lib.moe_attn_workspace_bytes(C.byref(attn), int(T_max)))
+
+
+def new_attn_workspace(attn: moe_attn_t, T_max: int, device="cuda") -> torch.Tensor:
+    """A zero-filled workspace for moe_attn_step calls of up to T_max tokens."""
+    n = moe_attn_workspace_bytes(attn, T_max)
+    if n == 0:
+        raise MoeError(MOE_EINVAL, "moe_attn_workspace_bytes")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def moe_attn_step(attn: moe_attn_t, x, ws, pos: int, y=None, flags: int = 0, attn_out=None, stream=None):
+    """One attention block on the T tokens x [T, H] (device fp32) at positions pos .. pos+T-1;
+    updates the layer's key/value cache and returns y [T, H]."""
+    T = x.shape[0]
+    y = torch.empty_like(x) if y is None else y
+    _check(lib.moe_attn_step(C.byref(attn), _ptr(x), T, int(pos), flags, _ptr(y), _ptr(attn_out), _ptr(ws),
+                             ws.numel(), _stream(stream)), "moe_attn_step")
+    return y
+
+
+def moe_attn_workspace_status(ws, stream=None) -> int:
+    """MOE_ETIMEOUT if a bounded wait of an attention call on `ws` gave up since the last
+    status call (and clears it), else MOE_OK; synchronises the stream."""
+    return int(lib.moe_attn_workspace_status(_ptr(ws), ws.numel(), _stream(stream)))
 
 
 def moe_sample(logits, temperature: float, top_k: int, top_p: float, u, tokens=None, stream=None):
@@ -357,4 +400,4 @@ class Cache:
         return h.value, m.value, b.value
 
 
-from .weights import Layer, make_layer, pack_expert_blob, pack_expert_tiles  # noqa: E402
+from .weights import AttnLayer, Layer, make_layer, pack_expert_blob, pack_expert_tiles  # noqa: E402

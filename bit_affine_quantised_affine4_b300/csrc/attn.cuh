@@ -1,0 +1,658 @@
+// attn.cuh -- one attention block over a binary16 key/value cache: the 4-bit
+// query/key/value projection with RoPE and the cache store, attention over split
+// position ranges with an in-kernel combine, and the 4-bit output projection.
+//
+// The pages list attention, RoPE, RMSNorm and the quantised GEMV among the engine's
+// own kernels, keep the key/value cache in FP16 -- a bounded ring for the 25
+// sliding-window layers, a linear store for the 5 full layers -- and quantise the
+// attention weights in the same 4-bit affine format as the experts ("TurboFieldfare:
+// движок с открытым кодом...", main technical paragraph; "TurboFieldfare esegue Mac
+// Gemma 4 26B in 2 GB...", section "Mac Gemma 4 26B entra nello spazio
+// disponibile...").  The formulas are the plain readings: rotate-half RoPE at the
+// token's position, softmax(scale q.k) over the attended positions, grouped
+// key/value heads.
+//
+// Three launches per call:
+//   k_attn_proj<kProjQKV>  [q;k;v] = Wqkv xn on the tensor cores (mma_core.cuh's
+//       nibble-as-subnormal trick); a CTA owns 16 rows at dimension i and the 16
+//       rows at i + d/2 of one head, so the rotation of each pair happens in its
+//       epilogue; queries go to the workspace (rotated, times the score scale),
+//       keys and values to their cache slots in binary16.
+//   k_attn<D>  a CTA takes one key/value head, up to 8 (token, query head) rows and
+//       one slice of the attended positions, in blocks of 64 with a running
+//       maximum; its partial (max, sum, unnormalised output) goes to the
+//       workspace and the last CTA of the slice set merges them in slice order.
+//   k_attn_proj<kProjPlain>  y = Wo o (+ x).
+// A sliding-window call with T tokens needs kv_len >= window + T - 1: then the T
+// new entries, written before anything is read, overwrite no position that any of
+// the T tokens attends to.
+#pragma once
+
+#include "common.cuh"
+#include "mma_core.cuh"
+#include "sync.cuh"
+
+namespace moe {
+
+constexpr int kAttnThreads = 256;
+constexpr int kAttnWarps = kAttnThreads / 32;
+constexpr int kAttnRows = 8;       // most (token, query head) rows of one attention tile
+constexpr int kAttnMaxSlices = 256;
+constexpr int kProjTokens = 8;     // token columns per projection CTA (the MMA's n)
+constexpr int kProjQKV = 0, kProjPlain = 1;
+// Warps of a projection CTA (they split the K groups) and the groups of weights a
+// warp holds in flight: the query/key/value projection (K = hidden; one batch
+// covers hidden 3072) and the output projection (K = nq d; one batch covers 4096).
+template <int MODE> struct ProjCfg;
+template <> struct ProjCfg<kProjQKV> { static constexpr int warps = 4, batch = 12; };
+template <> struct ProjCfg<kProjPlain> { static constexpr int warps = 8, batch = 8; };
+template <int MODE> constexpr int proj_threads() { return 32 * ProjCfg<MODE>::warps; }
+
+struct ProjArgs {
+    const uint32_t *q;  // weights [N][K], 4-bit affine, MLX layout
+    const __half *s, *b;
+    int N, K;
+    const float *x;  // [T][K]
+    int T;
+    const float *norm_w;  // RMSNorm gain (QKV mode) or null
+    float norm_eps;
+    // QKV mode
+    int nq, nkv, d, window, kv_len, p0;
+    float scale;
+    double freq[256];  // RoPE frequencies theta^(-2i/d), i < d/2 (fp64, from the host)
+    float *qr;  // [T][nq][d] rotated queries times the score scale
+    __half *kc, *vc;  // [nkv][kv_len][d]
+    // plain mode
+    float *y;            // [T][N]
+    const float *resid;  // [T][N] or null
+};
+
+__host__ __device__ inline int attn_slot(int p, int window, int kv_len) { return window > 0 ? p % kv_len : p; }
+
+// Row stride (halves) of the staged fp16 tokens: K plus 16 bytes, so that the
+// lanes of consecutive token columns start in different banks.
+__host__ __device__ inline int proj_xs_stride(int K) { return K + 8; }
+
+// Shared memory of a projection CTA: the staged tokens, their per-group sums and
+// the cross-warp reduction.
+template <int MODE>
+inline size_t proj_smem_bytes(int K, int T) {
+    const int rows = T < kProjTokens ? T : kProjTokens;
+    return sizeof(__half) * rows * proj_xs_stride(K) + sizeof(float) * rows * (K / kGroup) +
+           sizeof(float) * ProjCfg<MODE>::warps * 16 * 8;
+}
+
+// One CTA computes 16 output rows for up to 8 tokens.  The rows of the MMA tile
+// are rowA(g) = ra0 + g and rowB(g) = rb0 + g (g < 8).  In QKV mode a query or key
+// tile takes 8 dimensions i..i+7 of one head as rowA and their RoPE partners
+// i+d/2.. as rowB, so both halves of every rotated pair end in the same CTA; value
+// tiles and the plain mode take 16 consecutive rows.
+//
+// Launched with programmatic dependent launch: the weights (never written by the
+// kernels of a step) and the rotation angles are loaded before griddepcontrol.wait,
+// the tokens (the previous kernel's output) after it; the CTA lets its dependents
+// start only after its own wait (the attention kernel relies on that).
+template <int MODE>
+__global__ void __launch_bounds__(proj_threads<MODE>(), MODE == kProjQKV ? 4 : 2) k_attn_proj(const ProjArgs a) {
+    constexpr int kWarps = ProjCfg<MODE>::warps, kBatch = ProjCfg<MODE>::batch, kThreads = 32 * kWarps;
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int XS = proj_xs_stride(a.K);
+    const int G = a.K / kGroup;
+    const int t0 = blockIdx.y * kProjTokens, Tc = min(kProjTokens, a.T - t0), Tr = min(a.T, kProjTokens);
+    __half *xs = reinterpret_cast<__half *>(smem);
+    float *gsum = reinterpret_cast<float *>(smem + sizeof(__half) * Tr * XS);  // [token][group] sums of xs
+    float *red = gsum + Tr * G;                                                 // [warp][16][8]
+    __shared__ float inv_r[kProjTokens];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gl = lane >> 2, c = lane & 3;
+
+    int ra0, rb0, head = 0, i0 = 0;
+    bool pair = false;
+    if constexpr (MODE == kProjQKV) {
+        const int per = a.d / 16, npair = (a.nq + a.nkv) * per;
+        if ((int)blockIdx.x < npair) {
+            head = blockIdx.x / per;
+            i0 = 8 * (blockIdx.x % per);
+            pair = true;
+            ra0 = head * a.d + i0;
+            rb0 = ra0 + a.d / 2;
+        } else {
+            ra0 = (a.nq + a.nkv) * a.d + 16 * (blockIdx.x - npair);
+            rb0 = ra0 + 8;
+        }
+    } else {
+        ra0 = 16 * blockIdx.x;
+        rb0 = ra0 + 8;
+    }
+
+    // this warp's groups; their weights are loaded kBatch at a time, the first
+    // batch before the wait
+    const int g0 = warp * G / kWarps, g1 = (warp + 1) * G / kWarps;
+    const int wpr = a.K / 8;
+    const uint32_t *qa = a.q + (size_t)(ra0 + gl) * wpr + 2 * c, *qb = a.q + (size_t)(rb0 + gl) * wpr + 2 * c;
+    const __half *sa = a.s + (size_t)(ra0 + gl) * G, *sb = a.s + (size_t)(rb0 + gl) * G;
+    const __half *ba = a.b + (size_t)(ra0 + gl) * G, *bb = a.b + (size_t)(rb0 + gl) * G;
+    uint2 wa[kBatch], wb[kBatch];
+    __half2 sba[kBatch], sbb[kBatch];  // (scale, bias) of rowA and rowB
+    auto load_batch = [&](int gb) {
+#pragma unroll
+        for (int u = 0; u < kBatch; u++) {
+            const int g = gb + u;
+            if (g < g1) {
+                wa[u] = ldg_u2(qa + g * 8);
+                wb[u] = ldg_u2(qb + g * 8);
+                sba[u] = __halves2half2(__ldg(sa + g), __ldg(ba + g));
+                sbb[u] = __halves2half2(__ldg(sb + g), __ldg(bb + g));
+            }
+        }
+    };
+    load_batch(g0);
+
+    // rotation of the pair tile for epilogue thread (r = tid & 7, t = tid >> 3): the
+    // angle p * f in fp64, reduced to [-pi, pi] before the fp32 sine and cosine
+    float rc = 1.f, rs = 0.f;
+    if (MODE == kProjQKV && pair && tid < 64) {
+        const int r = tid & 7, t = tid >> 3;
+        if (t < Tc) {
+            const double ang = (double)(a.p0 + t0 + t) * a.freq[i0 + r];
+            const double twopi = 6.283185307179586476925286766559, inv2pi = 0.15915494309189533576888376337251;
+            sincosf((float)fma(-rint(ang * inv2pi), twopi, ang), &rs, &rc);
+        }
+    }
+    pdl_wait();
+    pdl_launch_dependents();
+
+    // RMSNorm of the CTA's tokens (QKV mode with a gain): warp w sums tokens w, w + kWarps
+    if (MODE == kProjQKV && a.norm_w) {
+        for (int t = warp; t < Tc; t += kWarps) {
+            const float4 *xr = reinterpret_cast<const float4 *>(a.x + (size_t)(t0 + t) * a.K);
+            float ss = 0.f;
+            for (int j = lane; j < a.K / 4; j += 32) {
+                const float4 v = __ldg(xr + j);
+                ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+            if (lane == 0) inv_r[t] = rsqrtf(ss / (float)a.K + a.norm_eps);
+        }
+        __syncthreads();
+    }
+    // stage the tokens as fp16 in fragment order, 8 columns per thread and step,
+    // and the sum of each group of 64 staged values (eight consecutive threads hold
+    // one group: K/8 is a multiple of 8 and kThreads of 32); the loads of SU steps
+    // are issued before any of them is used
+    constexpr int SU = 4;
+    const int nst = Tc * (a.K / 8);
+    for (int u0 = 0; u0 < nst; u0 += SU * kThreads) {
+        float4 lo[SU], hi[SU];
+#pragma unroll
+        for (int k = 0; k < SU; k++) {
+            const int u = u0 + k * kThreads + tid;
+            if (u < nst) {
+                const int t = u / (a.K / 8), j = (u % (a.K / 8)) * 8;
+                const float4 *xp = reinterpret_cast<const float4 *>(a.x + (size_t)(t0 + t) * a.K + j);
+                lo[k] = __ldg(xp);
+                hi[k] = __ldg(xp + 1);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < SU; k++) {
+            const int u = u0 + k * kThreads + tid;
+            float part = 0.f;
+            if (u < nst) {
+                const int t = u / (a.K / 8), j = (u % (a.K / 8)) * 8;
+                float4 l4 = lo[k], h4 = hi[k];
+                if (MODE == kProjQKV && a.norm_w) {
+                    const float4 *wp = reinterpret_cast<const float4 *>(a.norm_w + j);
+                    const float4 wl = __ldg(wp), wh = __ldg(wp + 1);
+                    const float ir = inv_r[t];
+                    l4 = make_float4(l4.x * wl.x * ir, l4.y * wl.y * ir, l4.z * wl.z * ir, l4.w * wl.w * ir);
+                    h4 = make_float4(h4.x * wh.x * ir, h4.y * wh.y * ir, h4.z * wh.z * ir, h4.w * wh.w * ir);
+                }
+                // fragment order within the run of 8: (0,4, 1,5, 2,6, 3,7)
+                __half2 h0 = __floats2half2_rn(l4.x, h4.x), h1 = __floats2half2_rn(l4.y, h4.y);
+                __half2 h2 = __floats2half2_rn(l4.z, h4.z), h3 = __floats2half2_rn(l4.w, h4.w);
+                *reinterpret_cast<uint4 *>(xs + (size_t)t * XS + j) =
+                    make_uint4(*reinterpret_cast<uint32_t *>(&h0), *reinterpret_cast<uint32_t *>(&h1),
+                               *reinterpret_cast<uint32_t *>(&h2), *reinterpret_cast<uint32_t *>(&h3));
+                const float2 f0 = __half22float2(h0), f1 = __half22float2(h1), f2 = __half22float2(h2),
+                             f3 = __half22float2(h3);
+                part = ((f0.x + f0.y) + (f1.x + f1.y)) + ((f2.x + f2.y) + (f3.x + f3.y));
+            }
+            part += __shfl_xor_sync(0xffffffffu, part, 1);
+            part += __shfl_xor_sync(0xffffffffu, part, 2);
+            part += __shfl_xor_sync(0xffffffffu, part, 4);
+            if ((u & 7) == 0 && u < nst) gsum[(u / (a.K / 8)) * G + (u % (a.K / 8)) / 8] = part;
+        }
+    }
+    __syncthreads();
+
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    const int ta = 2 * c, tb = 2 * c + 1;  // the lane's token columns
+    for (int gb = g0; gb < g1; gb += kBatch) {
+        if (gb != g0) load_batch(gb);
+#pragma unroll
+        for (int u = 0; u < kBatch; u++) {
+            const int g = gb + u;
+            if (g < g1) {
+                uint32_t xb[8];
+                if (gl < Tc)
+                    load_b(xb, xs + (size_t)gl * XS + g * kGroup + 16 * c);
+                else
+                    zero_b(xb);
+                float dd[4] = {0.f, 0.f, 0.f, 0.f};
+                mma_group_codes(dd, wa[u], wb[u], xb);
+                const float sm[2] = {ta < Tc ? gsum[ta * G + g] : 0.f, tb < Tc ? gsum[tb * G + g] : 0.f};
+                const float2 fa = __half22float2(sba[u]), fb = __half22float2(sbb[u]);
+                acc[0] = fmaf(fa.x * kTwo24, dd[0], fmaf(fa.y, sm[0], acc[0]));
+                acc[1] = fmaf(fa.x * kTwo24, dd[1], fmaf(fa.y, sm[1], acc[1]));
+                acc[2] = fmaf(fb.x * kTwo24, dd[2], fmaf(fb.y, sm[0], acc[2]));
+                acc[3] = fmaf(fb.x * kTwo24, dd[3], fmaf(fb.y, sm[1], acc[3]));
+            }
+        }
+    }
+    // accumulator slots: [0] (rowA gl, token 2c), [1] (gl, 2c+1), [2] (rowB gl, 2c), [3] (rowB gl, 2c+1)
+    {
+        float *rw = red + (size_t)warp * 128;
+        rw[gl * 8 + 2 * c] = acc[0];
+        rw[gl * 8 + 2 * c + 1] = acc[1];
+        rw[(gl + 8) * 8 + 2 * c] = acc[2];
+        rw[(gl + 8) * 8 + 2 * c + 1] = acc[3];
+    }
+    __syncthreads();
+    auto total = [&](int r, int t) {  // r < 8: rowA gl = r; r >= 8: rowB gl = r - 8
+        float v = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; w++) v += red[w * 128 + r * 8 + t];
+        return v;
+    };
+    if constexpr (MODE == kProjPlain) {
+        const int r = tid >> 3, t = tid & 7;  // the first 128 threads: 16 rows x 8 tokens
+        if (tid < 128 && t < Tc) {
+            const int row = r < 8 ? ra0 + r : rb0 + (r - 8);
+            const size_t at = (size_t)(t0 + t) * a.N + row;
+            float v = total(r, t);
+            if (a.resid) v += a.resid[at];
+            a.y[at] = v;
+        }
+        return;
+    }
+    if (pair) {
+        if (tid < 64) {
+            const int r = tid & 7, t = tid >> 3;
+            if (t < Tc) {
+                const float lo = total(r, t), hi = total(r + 8, t);
+                const float nlo = lo * rc - hi * rs, nhi = hi * rc + lo * rs;
+                const int i = i0 + r, p = a.p0 + t0 + t;
+                if (head < a.nq) {
+                    float *qrow = a.qr + ((size_t)(t0 + t) * a.nq + head) * a.d;
+                    qrow[i] = nlo * a.scale;
+                    qrow[i + a.d / 2] = nhi * a.scale;
+                } else {
+                    __half *krow = a.kc + ((size_t)(head - a.nq) * a.kv_len + attn_slot(p, a.window, a.kv_len)) * a.d;
+                    krow[i] = __float2half_rn(nlo);
+                    krow[i + a.d / 2] = __float2half_rn(nhi);
+                }
+            }
+        }
+    } else {
+        const int r = tid >> 3, t = tid & 7;
+        if (tid < 128 && t < Tc) {
+            const int dim = (r < 8 ? ra0 + r : rb0 + (r - 8)) - (a.nq + a.nkv) * a.d, g = dim / a.d, i = dim % a.d;
+            const int p = a.p0 + t0 + t;
+            a.vc[((size_t)g * a.kv_len + attn_slot(p, a.window, a.kv_len)) * a.d + i] = __float2half_rn(total(r, t));
+        }
+    }
+}
+
+// ---------------------------------------------------------------- attention
+
+constexpr int kAttnSlice = 32;  // positions per shared-memory block of the attention CTA
+
+struct AttnArgs {
+    const float *qr;  // [T][nq][D] rotated queries times the score scale
+    const __half *kc, *vc;
+    int nq, nkv, G, kv_len, window, p0, T, S;
+    float *part_o;     // [nkv][tiles][S][RT][D] unnormalised outputs
+    float2 *part_ml;   // [nkv][tiles][S][RT] (running max, sum of weights)
+    unsigned *ticket;  // [nkv][tiles]
+    unsigned *err;     // raised when a bounded wait gives up
+    float *ao;         // [T][nq D]
+    float *ao_user;    // optional copy of ao
+};
+
+__device__ __forceinline__ int attn_lo(int p, int window) { return window > 0 ? max(0, p - window + 1) : 0; }
+
+// Dynamic shared memory of the attention CTA: one block of key rows and one of
+// value rows, binary16.
+__host__ __device__ constexpr size_t attn_smem_bytes(int D) { return (size_t)2 * kAttnSlice * D * sizeof(__half); }
+
+// Issues the bulk copies of positions [c0, c1] (cache rows of one key/value head)
+// into rows c0 - u0 .. of the block; a ring's wrap splits a run in two.
+template <int D>
+__device__ __forceinline__ void attn_copy_rows(const AttnArgs &a, const __half *kh, const __half *vh, __half *ks,
+                                               __half *vs, int u0, int c0, int c1, uint64_t *bar) {
+    while (c0 <= c1) {
+        const int s0 = attn_slot(c0, a.window, a.kv_len);
+        const int n = a.window > 0 ? min(c1 - c0 + 1, a.kv_len - s0) : c1 - c0 + 1;
+        const unsigned bytes = (unsigned)n * D * sizeof(__half);
+        bulk_g2s(ks + (size_t)(c0 - u0) * D, kh + (size_t)s0 * D, bytes, bar);
+        bulk_g2s(vs + (size_t)(c0 - u0) * D, vh + (size_t)s0 * D, bytes, bar);
+        c0 += n;
+    }
+}
+
+// RT: (token, query head) rows of a tile, 1, 2, 4 or 8 (the host picks the
+// smallest power of two that holds the call's rows, at most 8).
+//
+// Launched with programmatic dependent launch.  Before griddepcontrol.wait the
+// CTA starts the bulk copies of the cached rows of earlier tokens (positions below
+// this call's first): every kernel of the library signals its dependents only
+// after its own wait, so the kernel that wrote those rows has completed by the
+// time this one starts.  The rows of this call's own tokens are copied after the
+// wait.
+template <int D, int RT>
+__global__ void __launch_bounds__(kAttnThreads) k_attn(const AttnArgs a) {
+    constexpr int PL = kAttnThreads / (D / 2);  // position planes of the value pass (thread = 2 dims)
+    constexpr int DL = D / 32;                  // dimensions per lane in the score pass
+    extern __shared__ __align__(128) unsigned char dsm[];
+    __half *ks = reinterpret_cast<__half *>(dsm);  // [kAttnSlice][D]
+    __half *vs = ks + kAttnSlice * D;             // [kAttnSlice][D]
+    __shared__ __align__(16) float qs[RT][D];
+    __shared__ float sc[RT][kAttnSlice];
+    __shared__ __align__(16) float red[PL][RT][D];
+    __shared__ float m_run[RT], l_run[RT], alpha[RT], den[RT];
+    __shared__ float ew[RT][kAttnMaxSlices];  // combine: weight of each slice
+    __shared__ float4 part4[kAttnThreads];    // combine: [nph][kAttnThreads / nph] partial sums
+    __shared__ int row_p[RT], row_lo[RT];
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    __shared__ unsigned last;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int s = blockIdx.x, tile = blockIdx.y, h = blockIdx.z;
+    const int tiles = gridDim.y;
+    const int R = min(RT, a.T * a.G - tile * RT);  // live rows of this tile
+
+    // the tile's positions [A, B] and this slice of them, in blocks of kAttnSlice
+    const int t_first = tile * RT / a.G, t_last = (tile * RT + R - 1) / a.G;
+    const int A = attn_lo(a.p0 + t_first, a.window), B = a.p0 + t_last;
+    const int L = (B - A + a.S) / a.S;  // ceil((B - A + 1) / S)
+    const int j0 = A + s * L, j1 = min(B, j0 + L - 1);
+    const __half *kh = a.kc + (size_t)h * a.kv_len * D;
+    const __half *vh = a.vc + (size_t)h * a.kv_len * D;
+
+    if (tid == 0) {
+        mbar_init(&bar, 1);
+        mbar_fence_init();
+        abort_flag = 0;
+        if (j0 <= j1) {  // the first block: rows of earlier tokens now, the rest after the wait
+            const int u1 = min(j1, j0 + kAttnSlice - 1);
+            mbar_arrive_expect_tx(&bar, (unsigned)(2 * (u1 - j0 + 1) * D * sizeof(__half)));
+            attn_copy_rows<D>(a, kh, vh, ks, vs, j0, j0, min(u1, a.p0 - 1), &bar);
+        }
+    }
+    pdl_wait();
+    pdl_launch_dependents();
+    if (tid == 0 && j0 <= j1) {
+        const int u1 = min(j1, j0 + kAttnSlice - 1);
+        attn_copy_rows<D>(a, kh, vh, ks, vs, j0, max(j0, a.p0), u1, &bar);
+    }
+
+    // queries of the tile's rows (row r = token t, head h G + g)
+    for (int u = tid; u < RT * (D / 4); u += kAttnThreads) {
+        const int r = u / (D / 4), i = (u % (D / 4)) * 4, rg = tile * RT + r;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (r < R) {
+            const int t = rg / a.G, g = rg % a.G;
+            v = *reinterpret_cast<const float4 *>(a.qr + ((size_t)t * a.nq + h * a.G + g) * D + i);
+        }
+        *reinterpret_cast<float4 *>(&qs[r][i]) = v;
+    }
+    if (tid < RT) {
+        const int rg = tile * RT + tid;
+        const int p = tid < R ? a.p0 + rg / a.G : -1;
+        row_p[tid] = p;
+        row_lo[tid] = tid < R ? attn_lo(p, a.window) : 0;
+        m_run[tid] = -INFINITY;
+        l_run[tid] = 0.f;
+        alpha[tid] = 0.f;
+    }
+    __syncthreads();
+
+    const int slot_d = tid % (D / 2), plane = tid / (D / 2);
+    float acc[RT][2];
+#pragma unroll
+    for (int r = 0; r < RT; r++) acc[r][0] = acc[r][1] = 0.f;
+
+    unsigned phase = 0;
+    for (int u0 = j0; u0 <= j1; u0 += kAttnSlice, phase ^= 1u) {
+        const int nb = min(kAttnSlice, j1 - u0 + 1);
+        if (u0 != j0 && tid == 0) {  // a later block (slices longer than one block)
+            mbar_arrive_expect_tx(&bar, (unsigned)(2 * nb * D * sizeof(__half)));
+            attn_copy_rows<D>(a, kh, vh, ks, vs, u0, u0, u0 + nb - 1, &bar);
+        }
+        if (!mbar_wait(&bar, phase, &abort_flag)) {
+            abort_flag = 1;
+            atomicExch(a.err, 1u);
+        }
+        __syncthreads();
+        if (abort_flag) break;
+        // scores: warp w takes positions u0 + w + 8k
+#pragma unroll
+        for (int k = 0; k < kAttnSlice / kAttnWarps; k++) {
+            const int jj = warp + kAttnWarps * k;
+            if (jj < nb) {
+                float kf[DL];
+                if constexpr (DL >= 8) {
+#pragma unroll
+                    for (int c8 = 0; c8 < DL / 8; c8++) {
+                        const uint4 w = *reinterpret_cast<const uint4 *>(ks + (size_t)jj * D + lane * DL + 8 * c8);
+                        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                        for (int i = 0; i < 4; i++) {
+                            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&ww[i]));
+                            kf[8 * c8 + 2 * i] = f.x;
+                            kf[8 * c8 + 2 * i + 1] = f.y;
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < DL / 2; i++) {
+                        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(ks + (size_t)jj * D + lane * DL + 2 * i));
+                        kf[2 * i] = f.x;
+                        kf[2 * i + 1] = f.y;
+                    }
+                }
+                const int j = u0 + jj;
+#pragma unroll
+                for (int r = 0; r < RT; r++) {
+                    if (r < R) {
+                        float dot = 0.f;
+                        if constexpr (DL % 4 == 0) {
+                            const float4 *q4 = reinterpret_cast<const float4 *>(&qs[r][lane * DL]);
+#pragma unroll
+                            for (int i = 0; i < DL / 4; i++) {
+                                const float4 qv = q4[i];
+                                dot = fmaf(qv.x, kf[4 * i], dot);
+                                dot = fmaf(qv.y, kf[4 * i + 1], dot);
+                                dot = fmaf(qv.z, kf[4 * i + 2], dot);
+                                dot = fmaf(qv.w, kf[4 * i + 3], dot);
+                            }
+                        } else {
+                            const float2 qv = *reinterpret_cast<const float2 *>(&qs[r][lane * DL]);
+                            dot = fmaf(qv.x, kf[0], fmaf(qv.y, kf[1], dot));
+                        }
+#pragma unroll
+                        for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+                        if (lane == 0) sc[r][jj] = (j >= row_lo[r] && j <= row_p[r]) ? dot : -INFINITY;
+                    }
+                }
+            }
+        }
+        __syncthreads();
+        // running maximum and weights: warp r owns row r
+        if (warp < R) {
+            const float v = lane < nb ? sc[warp][lane] : -INFINITY;
+            float m = v;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            const float mo = m_run[warp], mn = fmaxf(mo, m);
+            const float e = (lane < nb && mn != -INFINITY) ? __expf(v - mn) : 0.f;
+            if (lane < nb) sc[warp][lane] = e;
+            float l = e;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+            if (lane == 0) {
+                const float al = mo == -INFINITY ? 0.f : __expf(mo - mn);
+                alpha[warp] = al;
+                l_run[warp] = l_run[warp] * al + l;
+                m_run[warp] = mn;
+            }
+        }
+        __syncthreads();
+        // values: thread (plane, dims 2 slot_d, 2 slot_d + 1) over positions jj = plane mod PL
+#pragma unroll
+        for (int r = 0; r < RT; r++) {
+            acc[r][0] *= alpha[r];
+            acc[r][1] *= alpha[r];
+        }
+#pragma unroll 4
+        for (int jj = plane; jj < nb; jj += PL) {
+            const float2 v = __half22float2(*reinterpret_cast<const __half2 *>(vs + (size_t)jj * D + 2 * slot_d));
+#pragma unroll
+            for (int r = 0; r < RT; r++) {
+                const float w = sc[r][jj];
+                acc[r][0] = fmaf(w, v.x, acc[r][0]);
+                acc[r][1] = fmaf(w, v.y, acc[r][1]);
+            }
+        }
+        __syncthreads();  // the block's rows and scores are rewritten by the next block
+    }
+    if (abort_flag) {
+        // a copy that never completed may still land: give it time (bounded) before
+        // the CTA's shared memory is released; the slice then counts as empty (the
+        // error word tells the caller that the outputs are not valid)
+        volatile int no_abort = 0;
+        if (tid == 0) mbar_wait(&bar, phase, &no_abort, kWaitNs / 4);
+#pragma unroll
+        for (int r = 0; r < RT; r++) acc[r][0] = acc[r][1] = 0.f;
+        if (tid < RT) {
+            m_run[tid] = -INFINITY;
+            l_run[tid] = 0.f;
+        }
+        __syncthreads();
+    }
+
+    // the slice's partial: planes summed in order
+#pragma unroll
+    for (int r = 0; r < RT; r++) {
+        red[plane][r][2 * slot_d] = acc[r][0];
+        red[plane][r][2 * slot_d + 1] = acc[r][1];
+    }
+    __syncthreads();
+    const size_t pbase = (((size_t)h * tiles + tile) * a.S + s) * RT;
+    for (int u = tid; u < R * (D / 4); u += kAttnThreads) {
+        const int r = u / (D / 4), i = (u % (D / 4)) * 4;
+        float4 v = *reinterpret_cast<const float4 *>(&red[0][r][i]);
+#pragma unroll
+        for (int pl = 1; pl < PL; pl++) {
+            const float4 w = *reinterpret_cast<const float4 *>(&red[pl][r][i]);
+            v.x += w.x; v.y += w.y; v.z += w.z; v.w += w.w;
+        }
+        *reinterpret_cast<float4 *>(a.part_o + (pbase + r) * D + i) = v;
+    }
+    if (tid < R) a.part_ml[pbase + tid] = make_float2(m_run[tid], l_run[tid]);
+
+    // the last slice of (head, tile) merges all of them, in slice order
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+        const unsigned prev = atomicAdd(&a.ticket[h * tiles + tile], 1u);
+        last = prev == (unsigned)a.S - 1u;
+    }
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    const size_t pb0 = ((size_t)h * tiles + tile) * a.S * RT;
+    // per row: the largest slice maximum M, each slice's weight exp(m_s - M) (0 for
+    // a slice without positions) and the total weight; warp r owns row r and reads
+    // every slice's (max, sum) once
+    if (warp < R) {
+        constexpr int PerLane = kAttnMaxSlices / 32;
+        float2 ml[PerLane];
+#pragma unroll
+        for (int k = 0; k < PerLane; k++) {
+            const int q = lane + 32 * k;
+            ml[k] = q < a.S ? __ldcg(a.part_ml + pb0 + (size_t)q * RT + warp) : make_float2(-INFINITY, 0.f);
+        }
+        float M = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < PerLane; k++)
+            if (ml[k].y > 0.f) M = fmaxf(M, ml[k].x);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        float l = 0.f;
+#pragma unroll
+        for (int k = 0; k < PerLane; k++) {
+            const int q = lane + 32 * k;
+            const float e = ml[k].y > 0.f ? __expf(ml[k].x - M) : 0.f;
+            if (q < a.S) ew[warp][q] = e;
+            l = fmaf(ml[k].y, e, l);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+        if (lane == 0) den[warp] = l;
+    }
+    __syncthreads();
+    // the weighted sum of the slices' outputs, four dimensions per item; the slices
+    // are split over nph phases when there are fewer items than threads
+    const int items = R * (D / 4);
+    const int nph = items >= kAttnThreads ? 1 : kAttnThreads / items;
+    const int per = kAttnThreads / nph;
+    for (int base = 0; base < items; base += per) {
+        const int it = base + tid % per, ph = tid / per;
+        const bool live = it < items && ph < nph;
+        float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (live) {
+            const int r = it / (D / 4), i = (it % (D / 4)) * 4;
+            const float4 *src = reinterpret_cast<const float4 *>(a.part_o + (pb0 + r) * D + i);
+            const size_t stride = (size_t)RT * D / 4;  // float4s from one slice to the next
+            for (int q = ph; q < a.S; q += 8 * nph) {
+                float4 v[8];
+#pragma unroll
+                for (int k = 0; k < 8; k++) {
+                    const int qq = q + k * nph;
+                    v[k] = qq < a.S ? __ldcg(src + (size_t)qq * stride) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+                for (int k = 0; k < 8; k++) {
+                    const int qq = q + k * nph;
+                    const float e = qq < a.S ? ew[r][qq] : 0.f;
+                    num.x = fmaf(v[k].x, e, num.x); num.y = fmaf(v[k].y, e, num.y);
+                    num.z = fmaf(v[k].z, e, num.z); num.w = fmaf(v[k].w, e, num.w);
+                }
+            }
+        }
+        if (nph > 1) {
+            __syncthreads();
+            if (live) part4[ph * per + (it - base)] = num;
+            __syncthreads();
+            if (ph != 0 || !live) continue;
+            for (int k = 1; k < nph; k++) {
+                const float4 w = part4[k * per + (it - base)];
+                num.x += w.x; num.y += w.y; num.z += w.z; num.w += w.w;
+            }
+        } else if (!live) {
+            continue;
+        }
+        const int r = it / (D / 4), i = (it % (D / 4)) * 4;
+        const int rg = tile * RT + r, t = rg / a.G, g = rg % a.G;
+        const float inv = 1.f / den[r];
+        const float4 o = make_float4(num.x * inv, num.y * inv, num.z * inv, num.w * inv);
+        const size_t at = (size_t)t * a.nq * D + (size_t)(h * a.G + g) * D + i;
+        *reinterpret_cast<float4 *>(a.ao + at) = o;
+        if (a.ao_user) *reinterpret_cast<float4 *>(a.ao_user + at) = o;
+    }
+    if (tid == 0) a.ticket[h * tiles + tile] = 0u;  // ready for the next call
+}
+
+}  // namespace moe

@@ -8,9 +8,10 @@ from __future__ import annotations
 
 import ctypes as C
 
+import numpy as np
 import torch
 
-from . import (affine_quantise, moe_expert_blob_bytes, moe_expert_blob_offsets, moe_expert_tile,
+from . import (affine_quantise, moe_attn_t, moe_expert_blob_bytes, moe_expert_blob_offsets, moe_expert_tile,
                moe_layer_t, moe_tile_blob_bytes)
 
 
@@ -132,3 +133,51 @@ def make_layer(H, E, topk, I, Is, router_w, expert_w, shared_w, bias=None, devic
     L.replicate()
     torch.cuda.synchronize(L.device)
     return L
+
+
+class AttnLayer:
+    """One attention block resident on the GPU: the 4-bit [q; k; v] and output
+    projections (MLX layout) and the binary16 key/value cache [nkv, kv_len, d]."""
+
+    def __init__(self, H, nq, nkv, d, window, kv_len, theta, scale=None, device="cuda"):
+        self.H, self.nq, self.nkv, self.d = H, nq, nkv, d
+        self.window, self.kv_len, self.theta = window, kv_len, float(theta)
+        self.scale = d ** -0.5 if scale is None else float(scale)
+        self.device = torch.device(device)
+        nqkv = (nq + 2 * nkv) * d
+        self.wqkv = (torch.zeros((nqkv, H // 8), dtype=torch.int32, device=self.device),
+                     torch.zeros((nqkv, H // 64), dtype=torch.int16, device=self.device),
+                     torch.zeros((nqkv, H // 64), dtype=torch.int16, device=self.device))
+        K = nq * d
+        self.wo = (torch.zeros((H, K // 8), dtype=torch.int32, device=self.device),
+                   torch.zeros((H, K // 64), dtype=torch.int16, device=self.device),
+                   torch.zeros((H, K // 64), dtype=torch.int16, device=self.device))
+        self.k_cache = torch.zeros((nkv, kv_len, d), dtype=torch.int16, device=self.device)
+        self.v_cache = torch.zeros((nkv, kv_len, d), dtype=torch.int16, device=self.device)
+        self.norm_w, self.norm_eps = None, 0.0
+
+    def set_weights(self, wqkv, wo):
+        """Quantise fp32 Wqkv [(nq + 2 nkv) d, H] and Wo [H, nq d] with the library's quantiser."""
+        affine_quantise(torch.as_tensor(wqkv).to(self.device, torch.float32).contiguous(), 4, *self.wqkv)
+        affine_quantise(torch.as_tensor(wo).to(self.device, torch.float32).contiguous(), 4, *self.wo)
+
+    def set_cache(self, k_bits, v_bits):
+        """Cache contents as binary16 bits: uint16 numpy arrays or int16 tensors [nkv, kv_len, d]."""
+        for dst, src in ((self.k_cache, k_bits), (self.v_cache, v_bits)):
+            if not torch.is_tensor(src):
+                src = torch.from_numpy(np.ascontiguousarray(src).view(np.int16))
+            dst.copy_(src.view(torch.int16))
+
+    def set_norm(self, w, eps: float = 1e-6):
+        self.norm_w = None if w is None else torch.as_tensor(w, dtype=torch.float32).to(self.device).contiguous()
+        self.norm_eps = float(eps)
+
+    def view(self) -> moe_attn_t:
+        return moe_attn_t(
+            H=self.H, nq=self.nq, nkv=self.nkv, d=self.d, window=self.window, kv_len=self.kv_len,
+            theta=self.theta, scale=self.scale,
+            wqkv_q=self.wqkv[0].data_ptr(), wqkv_s=self.wqkv[1].data_ptr(), wqkv_b=self.wqkv[2].data_ptr(),
+            wo_q=self.wo[0].data_ptr(), wo_s=self.wo[1].data_ptr(), wo_b=self.wo[2].data_ptr(),
+            norm_w=None if self.norm_w is None else self.norm_w.data_ptr(), norm_eps=self.norm_eps,
+            k_cache=self.k_cache.data_ptr(), v_cache=self.v_cache.data_ptr(),
+        )

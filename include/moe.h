@@ -427,6 +427,86 @@ MOE_API int moe_cache_set_device_policy(moe_cache_t *cache, int enable);
 #define MOE_INJECT_COPY 2
 MOE_API int moe_debug_inject(int what);
 
+/* ---------------------------------------------------------------- attention */
+
+/*
+ * One attention block of a decoder layer over a binary16 key/value cache.  The
+ * pages list attention and RoPE among the engine's own kernels, quantise the
+ * attention weights in the same 4-bit affine format as the experts and keep the
+ * key/value cache in FP16: a bounded ring for the 25 sliding-window layers, a
+ * linear store for the 5 full-attention layers, 4096 tokens in the measured setup
+ * (iitog.ru page "TurboFieldfare: движок с открытым кодом...", main technical
+ * paragraph; remio.ai page, section "Mac Gemma 4 26B entra nello spazio
+ * disponibile...").  They give no shapes or formulas; this library's readings:
+ *   xn = RMSNorm(x) with MOE_PRENORM (norm_w, norm_eps as in moe_layer_t), else x;
+ *   [q; k; v] = Wqkv xn: nq query heads, then nkv key heads, then nkv value heads,
+ *     d rows each;
+ *   RoPE on every query and key head at the token's position p, rotate-half
+ *     pairing: for i < d/2, a = p * theta^(-2i/d),
+ *     (u_i, u_{i+d/2}) -> (u_i cos a - u_{i+d/2} sin a, u_{i+d/2} cos a + u_i sin a);
+ *   the rotated key and the value are stored in binary16 at slot p mod kv_len (a
+ *     sliding-window layer, window > 0) or slot p (a full layer, window == 0);
+ *   query head h attends, with key/value head h / (nq / nkv), to positions
+ *     max(0, p - window + 1) .. p (sliding) or 0 .. p (full), the token's own
+ *     included: o_h = sum_j softmax_j(scale q_h . k_j) v_j;
+ *   y = Wo o, plus x with MOE_RESIDUAL.
+ * The shapes:
+ *   H hidden size, a multiple of 64, at most MOE_ATTN_MAX_HIDDEN;
+ *   nq query heads, nkv key/value heads, nq a multiple of nkv; d in {64, 128, 256,
+ *   512}; nq * d at most MOE_ATTN_MAX_HIDDEN;
+ *   window >= 0; kv_len entries per key/value head (1 .. MOE_ATTN_MAX_KV);
+ *   theta > 0 the RoPE base; scale the score scale (1/sqrt(d) is the usual one).
+ * All pointers are device pointers owned by the caller:
+ *   wqkv_q/s/b 4-bit [(nq + 2 nkv) d][H], wo_q/s/b 4-bit [H][nq d] (MLX layout);
+ *   k_cache, v_cache binary16 [nkv][kv_len][d], 16-byte aligned, read and updated.
+ */
+#define MOE_ATTN_MAX_HIDDEN 8192
+#define MOE_ATTN_MAX_KV 65536
+
+typedef struct moe_attn {
+    int H, nq, nkv, d;
+    int window, kv_len;
+    float theta, scale;
+    const uint32_t *wqkv_q;
+    const uint16_t *wqkv_s, *wqkv_b;
+    const uint32_t *wo_q;
+    const uint16_t *wo_s, *wo_b;
+    const float *norm_w;
+    float norm_eps;
+    uint16_t *k_cache, *v_cache;
+} moe_attn_t;
+
+/*
+ * Workspace for moe_attn_step calls of up to T tokens (0 for bad shapes or T out
+ * of 1..MOE_MAX_PREFILL_TOKENS).  The workspace is device memory the caller owns,
+ * 256-byte aligned, zero-filled once before its first use (cudaMemset); every call
+ * leaves its control words zero again.  One workspace serves one stream at a time.
+ */
+MOE_API size_t moe_attn_workspace_bytes(const moe_attn_t *attn, int T);
+
+/*
+ * T consecutive tokens (1..MOE_MAX_PREFILL_TOKENS) of one sequence at positions
+ * pos .. pos+T-1: their keys and values are written into the cache, then each
+ * token attends as above (so a chunk equals T one-token calls in order).
+ * x, y: device fp32 [T][H]; y may alias x.  attn_out: optional device fp32
+ * [T][nq d], the attention output o before Wo.  flags: MOE_RESIDUAL, MOE_PRENORM.
+ * MOE_ECAPACITY when the positions do not fit the cache: a full layer needs
+ * pos + T <= kv_len; a sliding layer needs kv_len >= window + T - 1, so that the new
+ * entries overwrite no position the chunk still attends to (window + 0 suffices for
+ * one token).  fp16 activations as tensor-core operands in the projections, fp32
+ * everywhere else; deterministic.  Three kernel launches, stream-ordered.
+ */
+MOE_API int moe_attn_step(const moe_attn_t *attn, const float *x, int T, int pos, int flags, float *y,
+                          float *attn_out, void *d_ws, size_t ws_bytes, void *stream);
+
+/*
+ * Synchronises `stream` and reports whether a bounded device-side wait of an
+ * attention call on this workspace gave up since the last status call
+ * (MOE_ETIMEOUT; the outputs of that call are not valid) and clears the report.
+ * MOE_OK otherwise.
+ */
+MOE_API int moe_attn_workspace_status(void *d_ws, size_t ws_bytes, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
