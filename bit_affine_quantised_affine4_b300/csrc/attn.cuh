@@ -40,12 +40,10 @@ constexpr int kAttnRows = 8;       // most (token, query head) rows of one atten
 constexpr int kAttnMaxSlices = 256;
 constexpr int kProjTokens = 8;     // token columns per projection CTA (the MMA's n)
 constexpr int kProjQKV = 0, kProjPlain = 1;
-// Warps of a projection CTA (they split the K groups) and the groups of weights a
-// warp holds in flight: the query/key/value projection (K = hidden; one batch
-// covers hidden 3072) and the output projection (K = nq d; one batch covers 4096).
+// Warps of a projection CTA; they split the K groups.
 template <int MODE> struct ProjCfg;
-template <> struct ProjCfg<kProjQKV> { static constexpr int warps = 4, batch = 12; };
-template <> struct ProjCfg<kProjPlain> { static constexpr int warps = 8, batch = 8; };
+template <> struct ProjCfg<kProjQKV> { static constexpr int warps = 4; };
+template <> struct ProjCfg<kProjPlain> { static constexpr int warps = 8; };
 template <int MODE> constexpr int proj_threads() { return 32 * ProjCfg<MODE>::warps; }
 
 struct ProjArgs {
@@ -65,6 +63,7 @@ struct ProjArgs {
     // plain mode
     float *y;            // [T][N]
     const float *resid;  // [T][N] or null
+    unsigned *err;       // raised when a bounded wait gives up
 };
 
 __host__ __device__ inline int attn_slot(int p, int window, int kv_len) { return window > 0 ? p % kv_len : p; }
@@ -73,12 +72,18 @@ __host__ __device__ inline int attn_slot(int p, int window, int kv_len) { return
 // lanes of consecutive token columns start in different banks.
 __host__ __device__ inline int proj_xs_stride(int K) { return K + 8; }
 
-// Shared memory of a projection CTA: the staged tokens, their per-group sums and
-// the cross-warp reduction.
+// Row stride (bytes) of the CTA's weight rows in shared memory: K/2 rounded so
+// that it is 32 modulo 128, which puts the 8-byte fragment loads of a half-warp
+// (4 rows x 4 lanes) in distinct banks.
+__host__ __device__ inline int proj_wrow(int K) { return K / 2 + ((32 - (K / 2) % 128) + 128) % 128; }
+
+// Shared memory of a projection CTA: the 16 weight rows, their scales and biases,
+// the staged tokens, their per-group sums and the cross-warp reduction.
 template <int MODE>
 inline size_t proj_smem_bytes(int K, int T) {
     const int rows = T < kProjTokens ? T : kProjTokens;
-    return sizeof(__half) * rows * proj_xs_stride(K) + sizeof(float) * rows * (K / kGroup) +
+    return (size_t)16 * proj_wrow(K) + (size_t)2 * 16 * (K / kGroup) * sizeof(__half) +
+           sizeof(__half) * rows * proj_xs_stride(K) + sizeof(float) * rows * (K / kGroup) +
            sizeof(float) * ProjCfg<MODE>::warps * 16 * 8;
 }
 
@@ -88,21 +93,26 @@ inline size_t proj_smem_bytes(int K, int T) {
 // i+d/2.. as rowB, so both halves of every rotated pair end in the same CTA; value
 // tiles and the plain mode take 16 consecutive rows.
 //
-// Launched with programmatic dependent launch: the weights (never written by the
-// kernels of a step) and the rotation angles are loaded before griddepcontrol.wait,
-// the tokens (the previous kernel's output) after it; the CTA lets its dependents
-// start only after its own wait (the attention kernel relies on that).
+// The weights arrive by bulk copy (one per row, plus the two 8-row blocks of
+// scales and of biases), issued at the start, before griddepcontrol.wait: the
+// kernels of a step never write them.  The tokens (the previous kernel's output)
+// are read after the wait.  The CTA lets its dependents start only after its own
+// wait (the attention kernel relies on that).
 template <int MODE>
 __global__ void __launch_bounds__(proj_threads<MODE>(), MODE == kProjQKV ? 4 : 2) k_attn_proj(const ProjArgs a) {
-    constexpr int kWarps = ProjCfg<MODE>::warps, kBatch = ProjCfg<MODE>::batch, kThreads = 32 * kWarps;
-    extern __shared__ __align__(16) unsigned char smem[];
-    const int XS = proj_xs_stride(a.K);
+    constexpr int kWarps = ProjCfg<MODE>::warps, kThreads = 32 * kWarps;
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int XS = proj_xs_stride(a.K), WR = proj_wrow(a.K);
     const int G = a.K / kGroup;
     const int t0 = blockIdx.y * kProjTokens, Tc = min(kProjTokens, a.T - t0), Tr = min(a.T, kProjTokens);
-    __half *xs = reinterpret_cast<__half *>(smem);
-    float *gsum = reinterpret_cast<float *>(smem + sizeof(__half) * Tr * XS);  // [token][group] sums of xs
-    float *red = gsum + Tr * G;                                                 // [warp][16][8]
+    uint8_t *wq = smem;                                                     // [16][WR] codes, rows A then B
+    __half *wsb = reinterpret_cast<__half *>(smem + (size_t)16 * WR);       // [2 (s, b)][16][G]
+    __half *xs = wsb + 2 * 16 * G;                                          // [Tr][XS] staged tokens
+    float *gsum = reinterpret_cast<float *>(xs + (size_t)Tr * XS);          // [Tr][G] sums of xs
+    float *red = gsum + Tr * G;                                             // [warp][16][8]
     __shared__ float inv_r[kProjTokens];
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gl = lane >> 2, c = lane & 3;
 
     int ra0, rb0, head = 0, i0 = 0;
@@ -124,28 +134,27 @@ __global__ void __launch_bounds__(proj_threads<MODE>(), MODE == kProjQKV ? 4 : 2
         rb0 = ra0 + 8;
     }
 
-    // this warp's groups; their weights are loaded kBatch at a time, the first
-    // batch before the wait
-    const int g0 = warp * G / kWarps, g1 = (warp + 1) * G / kWarps;
-    const int wpr = a.K / 8;
-    const uint32_t *qa = a.q + (size_t)(ra0 + gl) * wpr + 2 * c, *qb = a.q + (size_t)(rb0 + gl) * wpr + 2 * c;
-    const __half *sa = a.s + (size_t)(ra0 + gl) * G, *sb = a.s + (size_t)(rb0 + gl) * G;
-    const __half *ba = a.b + (size_t)(ra0 + gl) * G, *bb = a.b + (size_t)(rb0 + gl) * G;
-    uint2 wa[kBatch], wb[kBatch];
-    __half2 sba[kBatch], sbb[kBatch];  // (scale, bias) of rowA and rowB
-    auto load_batch = [&](int gb) {
-#pragma unroll
-        for (int u = 0; u < kBatch; u++) {
-            const int g = gb + u;
-            if (g < g1) {
-                wa[u] = ldg_u2(qa + g * 8);
-                wb[u] = ldg_u2(qb + g * 8);
-                sba[u] = __halves2half2(__ldg(sa + g), __ldg(ba + g));
-                sbb[u] = __halves2half2(__ldg(sb + g), __ldg(bb + g));
-            }
+    // the CTA's weights: 16 code rows, then scales and biases of rows A and B
+    if (warp == 0) {
+        const unsigned row_bytes = (unsigned)(a.K / 2), sb_bytes = (unsigned)(8 * G * sizeof(__half));
+        if (lane == 0) {
+            mbar_init(&bar, 1);
+            mbar_fence_init();
+            abort_flag = 0;
+            mbar_arrive_expect_tx(&bar, 16 * row_bytes + 4 * sb_bytes);
         }
-    };
-    load_batch(g0);
+        __syncwarp();
+        const uint8_t *qb = reinterpret_cast<const uint8_t *>(a.q);
+        if (lane < 16) {
+            const int row = lane < 8 ? ra0 + lane : rb0 + (lane - 8);
+            bulk_g2s(wq + (size_t)lane * WR, qb + (size_t)row * row_bytes, row_bytes, &bar);
+        } else if (lane < 20) {
+            const int k = lane - 16;  // (scale | bias) x (rows A | rows B)
+            const __half *src = ((k & 1) ? a.b : a.s) + (size_t)((k & 2) ? rb0 : ra0) * G;
+            bulk_g2s(wsb + (size_t)(k & 1) * 16 * G + ((k & 2) ? 8 * G : 0), src, sb_bytes, &bar);
+        }
+    }
+    const int g0 = warp * G / kWarps, g1 = (warp + 1) * G / kWarps;
 
     // rotation of the pair tile for epilogue thread (r = tid & 7, t = tid >> 3): the
     // angle p * f in fp64, reduced to [-pi, pi] before the fp32 sine and cosine
@@ -226,29 +235,44 @@ __global__ void __launch_bounds__(proj_threads<MODE>(), MODE == kProjQKV ? 4 : 2
     }
     __syncthreads();
 
+    if (!mbar_wait(&bar, 0, &abort_flag)) {
+        abort_flag = 1;
+        atomicExch(a.err, 1u);
+    }
+    __syncthreads();
+    if (abort_flag) {
+        // a copy that never completed may still land: give it time (bounded)
+        // before the CTA's shared memory is released; the error word tells the
+        // caller that the outputs are not valid
+        volatile int no_abort = 0;
+        if (tid == 0) mbar_wait(&bar, 0, &no_abort, kWaitNs / 4);
+        __syncthreads();
+        return;
+    }
+
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     const int ta = 2 * c, tb = 2 * c + 1;  // the lane's token columns
-    for (int gb = g0; gb < g1; gb += kBatch) {
-        if (gb != g0) load_batch(gb);
-#pragma unroll
-        for (int u = 0; u < kBatch; u++) {
-            const int g = gb + u;
-            if (g < g1) {
-                uint32_t xb[8];
-                if (gl < Tc)
-                    load_b(xb, xs + (size_t)gl * XS + g * kGroup + 16 * c);
-                else
-                    zero_b(xb);
-                float dd[4] = {0.f, 0.f, 0.f, 0.f};
-                mma_group_codes(dd, wa[u], wb[u], xb);
-                const float sm[2] = {ta < Tc ? gsum[ta * G + g] : 0.f, tb < Tc ? gsum[tb * G + g] : 0.f};
-                const float2 fa = __half22float2(sba[u]), fb = __half22float2(sbb[u]);
-                acc[0] = fmaf(fa.x * kTwo24, dd[0], fmaf(fa.y, sm[0], acc[0]));
-                acc[1] = fmaf(fa.x * kTwo24, dd[1], fmaf(fa.y, sm[1], acc[1]));
-                acc[2] = fmaf(fb.x * kTwo24, dd[2], fmaf(fb.y, sm[0], acc[2]));
-                acc[3] = fmaf(fb.x * kTwo24, dd[3], fmaf(fb.y, sm[1], acc[3]));
-            }
-        }
+    const uint8_t *wa_row = wq + (size_t)gl * WR + 8 * c, *wb_row = wq + (size_t)(gl + 8) * WR + 8 * c;
+    const __half *sA = wsb + gl * G, *sB = wsb + (gl + 8) * G, *bA = wsb + 16 * G + gl * G,
+                 *bB = wsb + 16 * G + (gl + 8) * G;
+#pragma unroll 4
+    for (int g = g0; g < g1; g++) {
+        uint32_t xb[8];
+        if (gl < Tc)
+            load_b(xb, xs + (size_t)gl * XS + g * kGroup + 16 * c);
+        else
+            zero_b(xb);
+        const uint2 wa = *reinterpret_cast<const uint2 *>(wa_row + 32 * g);
+        const uint2 wb = *reinterpret_cast<const uint2 *>(wb_row + 32 * g);
+        float dd[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_group_codes(dd, wa, wb, xb);
+        const float sm0 = ta < Tc ? gsum[ta * G + g] : 0.f, sm1 = tb < Tc ? gsum[tb * G + g] : 0.f;
+        const float sa = __half2float(sA[g]) * kTwo24, ba = __half2float(bA[g]);
+        const float sb = __half2float(sB[g]) * kTwo24, bb = __half2float(bB[g]);
+        acc[0] = fmaf(sa, dd[0], fmaf(ba, sm0, acc[0]));
+        acc[1] = fmaf(sa, dd[1], fmaf(ba, sm1, acc[1]));
+        acc[2] = fmaf(sb, dd[2], fmaf(bb, sm0, acc[2]));
+        acc[3] = fmaf(sb, dd[3], fmaf(bb, sm1, acc[3]));
     }
     // accumulator slots: [0] (rowA gl, token 2c), [1] (gl, 2c+1), [2] (rowB gl, 2c), [3] (rowB gl, 2c+1)
     {
@@ -322,23 +346,32 @@ struct AttnArgs {
 
 __device__ __forceinline__ int attn_lo(int p, int window) { return window > 0 ? max(0, p - window + 1) : 0; }
 
-// Dynamic shared memory of the attention CTA: one block of key rows and one of
-// value rows, binary16.
-__host__ __device__ constexpr size_t attn_smem_bytes(int D) { return (size_t)2 * kAttnSlice * D * sizeof(__half); }
+// Dynamic shared memory of the attention CTA: the tile's queries, one block of
+// key rows (each row padded by 16 bytes, so that 32 lanes reading 32 rows hit
+// distinct banks) and one block of value rows, binary16.
+__host__ __device__ constexpr int attn_kstride(int D) { return D + 8; }  // halves
+__host__ __device__ constexpr size_t attn_smem_bytes(int D, int RT) {
+    return (size_t)RT * D * sizeof(float) + (size_t)kAttnSlice * attn_kstride(D) * sizeof(__half) +
+           (size_t)kAttnSlice * D * sizeof(__half);
+}
 
 // Issues the bulk copies of positions [c0, c1] (cache rows of one key/value head)
-// into rows c0 - u0 .. of the block; a ring's wrap splits a run in two.
+// into rows c0 - u0 .. of the block: one copy per key row (padded rows), one per
+// contiguous run of value rows (a ring's wrap splits a run in two).  Lane `lane`
+// of the calling warp issues every 32nd key row; lane 0 the value runs.
 template <int D>
 __device__ __forceinline__ void attn_copy_rows(const AttnArgs &a, const __half *kh, const __half *vh, __half *ks,
-                                               __half *vs, int u0, int c0, int c1, uint64_t *bar) {
-    while (c0 <= c1) {
-        const int s0 = attn_slot(c0, a.window, a.kv_len);
-        const int n = a.window > 0 ? min(c1 - c0 + 1, a.kv_len - s0) : c1 - c0 + 1;
-        const unsigned bytes = (unsigned)n * D * sizeof(__half);
-        bulk_g2s(ks + (size_t)(c0 - u0) * D, kh + (size_t)s0 * D, bytes, bar);
-        bulk_g2s(vs + (size_t)(c0 - u0) * D, vh + (size_t)s0 * D, bytes, bar);
-        c0 += n;
-    }
+                                               __half *vs, int u0, int c0, int c1, uint64_t *bar, int lane) {
+    constexpr unsigned kRow = D * sizeof(__half);
+    for (int c = c0 + lane; c <= c1; c += 32)
+        bulk_g2s(ks + (size_t)(c - u0) * attn_kstride(D), kh + (size_t)attn_slot(c, a.window, a.kv_len) * D, kRow, bar);
+    if (lane == 0)
+        while (c0 <= c1) {
+            const int s0 = attn_slot(c0, a.window, a.kv_len);
+            const int n = a.window > 0 ? min(c1 - c0 + 1, a.kv_len - s0) : c1 - c0 + 1;
+            bulk_g2s(vs + (size_t)(c0 - u0) * D, vh + (size_t)s0 * D, (unsigned)n * kRow, bar);
+            c0 += n;
+        }
 }
 
 // RT: (token, query head) rows of a tile, 1, 2, 4 or 8 (the host picks the
@@ -348,16 +381,24 @@ __device__ __forceinline__ void attn_copy_rows(const AttnArgs &a, const __half *
 // CTA starts the bulk copies of the cached rows of earlier tokens (positions below
 // this call's first): every kernel of the library signals its dependents only
 // after its own wait, so the kernel that wrote those rows has completed by the
-// time this one starts.  The rows of this call's own tokens are copied after the
-// wait.
+// time this one starts.  The rows of this call's own tokens and the queries are
+// copied after the wait.
+//
+// Scores: lane p of every warp takes position p of the block, warp w the
+// dimensions [w D/8, (w+1) D/8); each lane forms its partial dot products with the
+// tile's queries (no shuffles), warp r then adds the eight partials of row r,
+// lane by lane, and runs the online-softmax step.  Values: thread (plane, dims
+// 2 slot_d, 2 slot_d + 1) over the positions of its plane.
 template <int D, int RT>
 __global__ void __launch_bounds__(kAttnThreads) k_attn(const AttnArgs a) {
-    constexpr int PL = kAttnThreads / (D / 2);  // position planes of the value pass (thread = 2 dims)
-    constexpr int DL = D / 32;                  // dimensions per lane in the score pass
+    constexpr int PL = kAttnThreads / (D / 2);  // position planes of the value pass
+    constexpr int DW = D / kAttnWarps;          // dimensions per warp in the score pass
+    constexpr int KS = attn_kstride(D);
     extern __shared__ __align__(128) unsigned char dsm[];
-    __half *ks = reinterpret_cast<__half *>(dsm);  // [kAttnSlice][D]
-    __half *vs = ks + kAttnSlice * D;             // [kAttnSlice][D]
-    __shared__ __align__(16) float qs[RT][D];
+    float *qs = reinterpret_cast<float *>(dsm);                          // [RT][D]
+    __half *ks = reinterpret_cast<__half *>(dsm + (size_t)RT * D * 4);   // [kAttnSlice][KS]
+    __half *vs = ks + (size_t)kAttnSlice * KS;                           // [kAttnSlice][D]
+    __shared__ float scp[kAttnWarps][RT][kAttnSlice];  // partial scores of each warp
     __shared__ float sc[RT][kAttnSlice];
     __shared__ __align__(16) float red[PL][RT][D];
     __shared__ float m_run[RT], l_run[RT], alpha[RT], den[RT];
@@ -379,33 +420,29 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(const AttnArgs a) {
     const int j0 = A + s * L, j1 = min(B, j0 + L - 1);
     const __half *kh = a.kc + (size_t)h * a.kv_len * D;
     const __half *vh = a.vc + (size_t)h * a.kv_len * D;
+    const int nb0 = j0 <= j1 ? min(kAttnSlice, j1 - j0 + 1) : 0;  // positions of the first block
 
-    if (tid == 0) {
-        mbar_init(&bar, 1);
-        mbar_fence_init();
-        abort_flag = 0;
-        if (j0 <= j1) {  // the first block: rows of earlier tokens now, the rest after the wait
-            const int u1 = min(j1, j0 + kAttnSlice - 1);
-            mbar_arrive_expect_tx(&bar, (unsigned)(2 * (u1 - j0 + 1) * D * sizeof(__half)));
-            attn_copy_rows<D>(a, kh, vh, ks, vs, j0, j0, min(u1, a.p0 - 1), &bar);
+    if (warp == 0) {
+        if (lane == 0) {
+            mbar_init(&bar, 1);
+            mbar_fence_init();
+            abort_flag = 0;
+            // the first block's rows and the queries (a slice without positions copies
+            // nothing and posts an empty partial)
+            if (nb0) mbar_arrive_expect_tx(&bar, (unsigned)(2 * nb0 * D * sizeof(__half) + R * D * sizeof(float)));
         }
+        __syncwarp();
+        if (nb0) attn_copy_rows<D>(a, kh, vh, ks, vs, j0, j0, min(j0 + nb0 - 1, a.p0 - 1), &bar, lane);
     }
     pdl_wait();
     pdl_launch_dependents();
-    if (tid == 0 && j0 <= j1) {
-        const int u1 = min(j1, j0 + kAttnSlice - 1);
-        attn_copy_rows<D>(a, kh, vh, ks, vs, j0, max(j0, a.p0), u1, &bar);
-    }
-
-    // queries of the tile's rows (row r = token t, head h G + g)
-    for (int u = tid; u < RT * (D / 4); u += kAttnThreads) {
-        const int r = u / (D / 4), i = (u % (D / 4)) * 4, rg = tile * RT + r;
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (r < R) {
-            const int t = rg / a.G, g = rg % a.G;
-            v = *reinterpret_cast<const float4 *>(a.qr + ((size_t)t * a.nq + h * a.G + g) * D + i);
+    if (warp == 0 && nb0) {
+        attn_copy_rows<D>(a, kh, vh, ks, vs, j0, max(j0, a.p0), j0 + nb0 - 1, &bar, lane);
+        // queries: row r is token t's head h G + g
+        for (int r = lane; r < R; r += 32) {
+            const int rg = tile * RT + r, t = rg / a.G, g = rg % a.G;
+            bulk_g2s(qs + (size_t)r * D, a.qr + ((size_t)t * a.nq + h * a.G + g) * D, D * sizeof(float), &bar);
         }
-        *reinterpret_cast<float4 *>(&qs[r][i]) = v;
     }
     if (tid < RT) {
         const int rg = tile * RT + tid;
@@ -426,9 +463,10 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(const AttnArgs a) {
     unsigned phase = 0;
     for (int u0 = j0; u0 <= j1; u0 += kAttnSlice, phase ^= 1u) {
         const int nb = min(kAttnSlice, j1 - u0 + 1);
-        if (u0 != j0 && tid == 0) {  // a later block (slices longer than one block)
-            mbar_arrive_expect_tx(&bar, (unsigned)(2 * nb * D * sizeof(__half)));
-            attn_copy_rows<D>(a, kh, vh, ks, vs, u0, u0, u0 + nb - 1, &bar);
+        if (u0 != j0 && warp == 0) {  // a later block (slices longer than one block)
+            if (lane == 0) mbar_arrive_expect_tx(&bar, (unsigned)(2 * nb * D * sizeof(__half)));
+            __syncwarp();
+            attn_copy_rows<D>(a, kh, vh, ks, vs, u0, u0, u0 + nb - 1, &bar, lane);
         }
         if (!mbar_wait(&bar, phase, &abort_flag)) {
             abort_flag = 1;
@@ -436,68 +474,57 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(const AttnArgs a) {
         }
         __syncthreads();
         if (abort_flag) break;
-        // scores: warp w takes positions u0 + w + 8k
+        // partial scores: lane = position, warp = dimensions [warp DW, warp DW + DW)
+        {
+            float part[RT];
 #pragma unroll
-        for (int k = 0; k < kAttnSlice / kAttnWarps; k++) {
-            const int jj = warp + kAttnWarps * k;
-            if (jj < nb) {
-                float kf[DL];
-                if constexpr (DL >= 8) {
+            for (int r = 0; r < RT; r++) part[r] = 0.f;
+            if (lane < nb) {
+                const __half *krow = ks + (size_t)lane * KS + warp * DW;
 #pragma unroll
-                    for (int c8 = 0; c8 < DL / 8; c8++) {
-                        const uint4 w = *reinterpret_cast<const uint4 *>(ks + (size_t)jj * D + lane * DL + 8 * c8);
-                        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+                for (int c8 = 0; c8 < DW / 8; c8++) {
+                    const uint4 w = *reinterpret_cast<const uint4 *>(krow + 8 * c8);
+                    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+                    float kf[8];
 #pragma unroll
-                        for (int i = 0; i < 4; i++) {
-                            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&ww[i]));
-                            kf[8 * c8 + 2 * i] = f.x;
-                            kf[8 * c8 + 2 * i + 1] = f.y;
-                        }
-                    }
-                } else {
-#pragma unroll
-                    for (int i = 0; i < DL / 2; i++) {
-                        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(ks + (size_t)jj * D + lane * DL + 2 * i));
+                    for (int i = 0; i < 4; i++) {
+                        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&ww[i]));
                         kf[2 * i] = f.x;
                         kf[2 * i + 1] = f.y;
                     }
-                }
-                const int j = u0 + jj;
 #pragma unroll
-                for (int r = 0; r < RT; r++) {
-                    if (r < R) {
-                        float dot = 0.f;
-                        if constexpr (DL % 4 == 0) {
-                            const float4 *q4 = reinterpret_cast<const float4 *>(&qs[r][lane * DL]);
-#pragma unroll
-                            for (int i = 0; i < DL / 4; i++) {
-                                const float4 qv = q4[i];
-                                dot = fmaf(qv.x, kf[4 * i], dot);
-                                dot = fmaf(qv.y, kf[4 * i + 1], dot);
-                                dot = fmaf(qv.z, kf[4 * i + 2], dot);
-                                dot = fmaf(qv.w, kf[4 * i + 3], dot);
-                            }
-                        } else {
-                            const float2 qv = *reinterpret_cast<const float2 *>(&qs[r][lane * DL]);
-                            dot = fmaf(qv.x, kf[0], fmaf(qv.y, kf[1], dot));
-                        }
-#pragma unroll
-                        for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-                        if (lane == 0) sc[r][jj] = (j >= row_lo[r] && j <= row_p[r]) ? dot : -INFINITY;
+                    for (int r = 0; r < RT; r++) {
+                        const float4 q0 = *reinterpret_cast<const float4 *>(qs + (size_t)r * D + warp * DW + 8 * c8);
+                        const float4 q1 = *reinterpret_cast<const float4 *>(qs + (size_t)r * D + warp * DW + 8 * c8 + 4);
+                        float v = part[r];
+                        v = fmaf(q0.x, kf[0], v); v = fmaf(q0.y, kf[1], v);
+                        v = fmaf(q0.z, kf[2], v); v = fmaf(q0.w, kf[3], v);
+                        v = fmaf(q1.x, kf[4], v); v = fmaf(q1.y, kf[5], v);
+                        v = fmaf(q1.z, kf[6], v); v = fmaf(q1.w, kf[7], v);
+                        part[r] = v;
                     }
                 }
             }
+#pragma unroll
+            for (int r = 0; r < RT; r++) scp[warp][r][lane] = part[r];
         }
         __syncthreads();
-        // running maximum and weights: warp r owns row r
+        // row r (warp r): the score of position lane, the running maximum and weights
         if (warp < R) {
-            const float v = lane < nb ? sc[warp][lane] : -INFINITY;
+            float v = -INFINITY;
+            if (lane < nb) {
+                float sum = 0.f;
+#pragma unroll
+                for (int w = 0; w < kAttnWarps; w++) sum += scp[w][warp][lane];
+                const int j = u0 + lane;
+                v = (j >= row_lo[warp] && j <= row_p[warp]) ? sum : -INFINITY;
+            }
             float m = v;
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
             const float mo = m_run[warp], mn = fmaxf(mo, m);
             const float e = (lane < nb && mn != -INFINITY) ? __expf(v - mn) : 0.f;
-            if (lane < nb) sc[warp][lane] = e;
+            sc[warp][lane] = e;
             float l = e;
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
@@ -509,7 +536,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(const AttnArgs a) {
             }
         }
         __syncthreads();
-        // values: thread (plane, dims 2 slot_d, 2 slot_d + 1) over positions jj = plane mod PL
+        // values
 #pragma unroll
         for (int r = 0; r < RT; r++) {
             acc[r][0] *= alpha[r];

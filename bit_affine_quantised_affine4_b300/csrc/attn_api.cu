@@ -39,8 +39,8 @@ bool shape_ok(const moe_attn_t *a) {
     if (a->window < 0 || a->kv_len < 1 || a->kv_len > MOE_ATTN_MAX_KV) return false;
     if (!(a->theta > 0.f) || !std::isfinite(a->theta) || !std::isfinite(a->scale)) return false;
     if (!a->wqkv_q || !a->wqkv_s || !a->wqkv_b || !a->wo_q || !a->wo_s || !a->wo_b) return false;
-    if (!al(a->wqkv_q, 8) || !al(a->wo_q, 8) || !al(a->wqkv_s, 2) || !al(a->wqkv_b, 2) || !al(a->wo_s, 2) ||
-        !al(a->wo_b, 2))
+    if (!al(a->wqkv_q, 16) || !al(a->wo_q, 16) || !al(a->wqkv_s, 16) || !al(a->wqkv_b, 16) || !al(a->wo_s, 16) ||
+        !al(a->wo_b, 16))
         return false;
     if (!a->k_cache || !a->v_cache || !al(a->k_cache, 16) || !al(a->v_cache, 16)) return false;
     return true;
@@ -175,12 +175,12 @@ template <int D, int RT>
 int launch_attn_rt(const AttnArgs &args, dim3 grid, cudaStream_t st) {
     static std::atomic<int> ready{0};
     if (!ready.load()) {
-        if (cudaFuncSetAttribute(k_attn<D, RT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)attn_smem_bytes(D)) !=
+        if (cudaFuncSetAttribute(k_attn<D, RT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)attn_smem_bytes(D, RT)) !=
             cudaSuccess)
             return attn_cuda_status();
         ready.store(1);
     }
-    return launch_pdl(k_attn<D, RT>, grid, dim3(kAttnThreads), attn_smem_bytes(D), st, args);
+    return launch_pdl(k_attn<D, RT>, grid, dim3(kAttnThreads), attn_smem_bytes(D, RT), st, args);
 }
 
 template <int D>
@@ -245,6 +245,7 @@ int moe_attn_step(const moe_attn_t *attn, const float *x, int T, int pos, int fl
     rope_freqs(a->theta, a->d, p.freq);
     p.scale = a->scale;
     p.qr = w.qr;
+    p.err = w.err;
     p.kc = reinterpret_cast<__half *>(a->k_cache);
     p.vc = reinterpret_cast<__half *>(a->v_cache);
     if ((rc = launch_pdl(k_attn_proj<kProjQKV>, dim3(p.N / 16, tok_groups), dim3(proj_threads<kProjQKV>()),
@@ -287,6 +288,7 @@ int moe_attn_step(const moe_attn_t *attn, const float *x, int T, int pos, int fl
     o.T = T;
     o.y = y;
     o.resid = (flags & MOE_RESIDUAL) ? x : nullptr;
+    o.err = w.err;
     return launch_pdl(k_attn_proj<kProjPlain>, dim3(a->H / 16, tok_groups), dim3(proj_threads<kProjPlain>()),
                       proj_smem_bytes<kProjPlain>(o.K, T), st, o);
 }

@@ -456,7 +456,7 @@ MOE_API int moe_debug_inject(int what);
  *   512}; nq * d at most MOE_ATTN_MAX_HIDDEN;
  *   window >= 0; kv_len entries per key/value head (1 .. MOE_ATTN_MAX_KV);
  *   theta > 0 the RoPE base; scale the score scale (1/sqrt(d) is the usual one).
- * All pointers are device pointers owned by the caller:
+ * All pointers are device pointers owned by the caller, 16-byte aligned:
  *   wqkv_q/s/b 4-bit [(nq + 2 nkv) d][H], wo_q/s/b 4-bit [H][nq d] (MLX layout);
  *   k_cache, v_cache binary16 [nkv][kv_len][d], 16-byte aligned, read and updated.
  */
