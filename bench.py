@@ -327,10 +327,15 @@ def run_ours(args):
     extra = {}
     if not args.quick and rank == 0:
         extra = side_measurements(torch, moe, layer, copies, ws, args)
+    if not args.quick and rank == 0:
+        extra["attention_block"] = attention_measurement(torch, moe, args, peaks)
     if args.stack and rank == 0:
         del layer, views
         torch.cuda.empty_cache()
-        extra["stack_decode_lfu"] = stack_measurement(torch, moe, args)
+        stack_layers = build_stack_layers(torch, moe)
+        extra["stack_decode_attention"] = stack_attn_measurement(torch, moe, args, stack_layers)
+        extra["stack_decode_lfu"] = stack_measurement(torch, moe, args, layers=stack_layers)
+        del stack_layers
 
     line = {
         "metric": "MoE decode tokens/s (one full-size layer, T=1) and % of B300 HBM roofline; prefill-chunk tok/s",
@@ -426,22 +431,80 @@ def side_measurements(torch, moe, layer, copies, ws, args):
     return out
 
 
-def stack_measurement(torch, moe, args, n_layers=30, steps=256, slots=16):
-    """30-layer MoE stack decode (MoE part only: attention is the identity), one
-    token per step, experts in page-locked host memory behind a 16-slot LFU cache
-    per layer.  Each layer is the pre-norm block h <- h + MoE(RMSNorm(h)) (without
-    the norm the residual stream grows layer over layer).  Routing follows Zipf(1.1)
-    popularity (a per-layer logit bias) and the step inputs are an AR(1) sequence
-    (rho 0.9), so consecutive steps route alike.  Weights come from the GPU's seeded
-    normal generator (N(0, 0.02); RMSNorm weights 1 + N(0, 0.1^2)), quantised and
-    tiled by the library."""
+ATTN_SLIDING, ATTN_GLOBAL = synth.ATTN_FULL_SLIDING, synth.ATTN_FULL_GLOBAL
+
+
+def attn_weight_bytes(a):
+    """4-bit weights (4.5 bits with scale and bias) of one attention block."""
+    return (a.n_qkv * a.H + a.H * a.nq * a.d) * 9 // 16
+
+
+def attn_call_bytes(a, attended):
+    """Algorithmic bytes of one T = 1 attention call that attends to `attended`
+    positions: the weights, the binary16 keys and values read, the new key and value
+    written, x read and y written."""
+    return attn_weight_bytes(a) + 2 * a.nkv * attended * a.d * 2 + 2 * a.nkv * a.d * 2 + 2 * a.H * 4
+
+
+def new_attn_layer(torch, moe, a, gen, dev):
+    L = moe.AttnLayer(a.H, a.nq, a.nkv, a.d, a.window, a.kv_len, a.theta, device=dev)
+    L.set_weights(torch.randn(a.n_qkv, a.H, generator=gen, device=dev) * 0.02,
+                  torch.randn(a.H, a.nq * a.d, generator=gen, device=dev) * 0.02)
+    L.set_cache(torch.randn(a.nkv, a.kv_len, a.d, generator=gen, device=dev).half().view(torch.int16),
+                torch.randn(a.nkv, a.kv_len, a.d, generator=gen, device=dev).half().view(torch.int16))
+    L.set_norm(1.0 + 0.1 * torch.randn(a.H, generator=gen, device=dev), 1e-6)
+    return L
+
+
+def attention_measurement(torch, moe, args, peaks):
+    """One attention block (pre-norm, residual), T = 1, for a sliding-window layer
+    (window 1024, ring of 1151) and a full layer (store of 4096, at its last
+    position), rotating over enough layer copies that weights and caches do not
+    fit in L2; CUDA-graph replay timed with events."""
+    dev = torch.device("cuda")
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1)
+    out = {}
+    for a, pos, attended in ((ATTN_SLIDING, 5000, ATTN_SLIDING.window), (ATTN_GLOBAL, ATTN_GLOBAL.kv_len - 1,
+                                                                         ATTN_GLOBAL.kv_len)):
+        per = attn_weight_bytes(a) + 2 * a.nkv * a.kv_len * a.d * 2
+        copies = max(4, int(np.ceil(3 * (128 << 20) / per)))
+        layers = [new_attn_layer(torch, moe, a, gen, dev) for _ in range(copies)]
+        views = [l.view() for l in layers]
+        ws = moe.new_attn_workspace(views[0], 1)
+        x = torch.randn(1, a.H, generator=gen, device=dev)
+        y = torch.empty_like(x)
+
+        def steps(n, first):
+            for i in range(first, first + n):
+                moe.moe_attn_step(views[i % copies], x, ws, pos, y=y, flags=moe.MOE_RESIDUAL | moe.MOE_PRENORM)
+
+        K = max(40, args.steps // 2)
+        dt = time_graph(torch, steps, K, args.warmup)
+        status = moe.moe_attn_workspace_status(ws)
+        b = attn_call_bytes(a, attended)
+        gbs = b / (dt / K) / 1e9
+        out[a.name] = {"us_per_call": dt / K * 1e6, "attended_positions": attended, "algorithmic_bytes": b,
+                       "GB_s": gbs, "frac_of_hbm": gbs / peaks["hbm_gbs"], "layer_copies": copies,
+                       "status": moe.status_string(status)}
+        del layers, views, ws
+        torch.cuda.empty_cache()
+    out["shape"] = ("hidden 2816, 16 query heads and 8 key/value heads of 256, 4-bit Wqkv [8192 x 2816] and "
+                    "Wo [2816 x 4096], binary16 cache; three kernels per call (QKV + RoPE + cache store, "
+                    "attention, output projection + residual) with programmatic dependent launch")
+    return out
+
+
+def build_stack_layers(torch, moe, n_layers=30):
+    """The 30 MoE layers of the decode stacks, experts resident on the device: router,
+    experts and shared expert from the GPU's seeded normal generator (N(0, 0.02)),
+    quantised and tiled by the library; Zipf(1.1) logit bias per layer; RMSNorm
+    weights 1 + N(0, 0.1^2)."""
     s = synth.FULL
     dev = torch.device("cuda")
-    blob = moe.moe_tile_blob_bytes(H, I)
     gen = torch.Generator(device=dev)
     gen.manual_seed(0)
-    layers, hosts, caches, views = [], [], [], []
-    n_host = 0
+    layers = []
     for l in range(n_layers):
         L = moe.Layer(H, E, TOPK, I, IS, device=dev, copies=1)
         L.set_router(torch.randn(E, H, generator=gen, device=dev) * 0.02)
@@ -452,6 +515,89 @@ def stack_measurement(torch, moe, args, n_layers=30, steps=256, slots=16):
                      torch.randn(H, IS, generator=gen, device=dev) * 0.02)
         L.set_bias(synth.popularity_bias(s, seed=0, layer=l))
         L.set_norm(1.0 + 0.1 * torch.randn(H, generator=gen, device=dev), 1e-6)
+        layers.append(L)
+    torch.cuda.synchronize()
+    return layers
+
+
+def stack_attn_measurement(torch, moe, args, layers, steps=64):
+    """The 30-layer decode step with attention: per layer the pre-norm attention
+    block h <- h + Attn(RMSNorm(h)) over a binary16 key/value cache, then the
+    pre-norm MoE block h <- h + MoE(RMSNorm(h)) with every expert resident.  Layers
+    6, 12, ..., 30 attend to the whole context (a linear store of 4096), the other 25
+    to a window of 1024 (a ring of 1151).  The context holds 4096 - 64 synthetic
+    tokens when the 64 timed steps start.  Each step is 30 x (3 attention kernels +
+    1 MoE decode kernel), replayed from a CUDA graph; the same steps are also
+    timed with the attention blocks alone and the MoE blocks alone."""
+    dev = torch.device("cuda")
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(2)
+    n_layers = len(layers)
+    attn = [new_attn_layer(torch, moe, ATTN_GLOBAL if l % 6 == 5 else ATTN_SLIDING, gen, dev) for l in range(n_layers)]
+    aviews = [a.view() for a in attn]
+    mviews = [L.view() for L in layers]
+    # one workspace for both layer kinds: the larger of their sizes
+    big = max((aviews[0], aviews[n_layers // 6 * 6 - 1]), key=lambda v: moe.moe_attn_workspace_bytes(v, 1))
+    aws = moe.new_attn_workspace(big, 1)
+    mws = moe.new_workspace(mviews[0], 1)
+    X = torch.from_numpy(synth.token_sequence(synth.FULL, steps, seed=0)).to(dev)
+    ha = torch.empty((1, H), device=dev)
+    hb = [torch.empty((1, H), device=dev), torch.empty((1, H), device=dev)]  # the decode's y must not alias x
+    pos0 = ATTN_GLOBAL.kv_len - steps
+    flags = moe.MOE_RESIDUAL | moe.MOE_PRENORM
+
+    def run(which):
+        def fn(n, first):
+            for st in range(first, first + n):
+                cur = X[st % steps:st % steps + 1]
+                for l in range(n_layers):
+                    if which != "moe":
+                        moe.moe_attn_step(aviews[l], cur, aws, pos0 + st % steps, y=ha, flags=flags)
+                        cur = ha
+                    if which != "attn":
+                        moe.moe_layer_decode(mviews[l], cur, mws, y=hb[l & 1], flags=flags)
+                        cur = hb[l & 1]
+        return fn
+
+    res = {}
+    for which in ("both", "attn", "moe"):
+        dt = time_graph(torch, run(which), steps, 2)
+        res[which] = dt / steps
+    status = moe.moe_attn_workspace_status(aws)
+    attended = sum((ATTN_GLOBAL.kv_len - steps // 2) if l % 6 == 5 else ATTN_SLIDING.window for l in range(n_layers))
+    attn_bytes = sum(attn_weight_bytes(ATTN_GLOBAL if l % 6 == 5 else ATTN_SLIDING) for l in range(n_layers)) + \
+        2 * ATTN_SLIDING.nkv * attended * ATTN_SLIDING.d * 2
+    moe_bytes = n_layers * DECODE_BYTES
+    out = {"layers": n_layers, "full_attention_layers": n_layers // 6, "context": ATTN_GLOBAL.kv_len,
+           "steps_timed": steps, "tok_s": 1.0 / res["both"], "ms_per_token": res["both"] * 1e3,
+           "attention_only_ms": res["attn"] * 1e3, "moe_only_ms": res["moe"] * 1e3,
+           "bytes_per_token": attn_bytes + moe_bytes,
+           "GB_s": (attn_bytes + moe_bytes) / res["both"] / 1e9, "attn_status": moe.status_string(status),
+           "note": "experts resident; the routing follows Zipf(1.1) with an AR(1) token sequence; "
+                   "bytes: 4-bit weights at 4.5 bits + binary16 keys/values attended (mean context of the "
+                   "timed steps for the full layers)"}
+    del attn, aviews, aws
+    torch.cuda.empty_cache()
+    return out
+
+
+def stack_measurement(torch, moe, args, layers=None, n_layers=30, steps=256, slots=16):
+    """30-layer MoE stack decode (MoE part only: attention is the identity), one
+    token per step, experts in page-locked host memory behind a 16-slot LFU cache
+    per layer.  Each layer is the pre-norm block h <- h + MoE(RMSNorm(h)) (without
+    the norm the residual stream grows layer over layer).  Routing follows Zipf(1.1)
+    popularity (a per-layer logit bias) and the step inputs are an AR(1) sequence
+    (rho 0.9), so consecutive steps route alike.  `layers`: the resident layers of
+    build_stack_layers, whose experts move to host memory here."""
+    s = synth.FULL
+    dev = torch.device("cuda")
+    blob = moe.moe_tile_blob_bytes(H, I)
+    if layers is None:
+        layers = build_stack_layers(torch, moe, n_layers)
+    n_layers = len(layers)
+    hosts, caches, views = [], [], []
+    n_host = 0
+    for l, L in enumerate(layers):
         try:
             host = torch.empty((E, blob), dtype=torch.uint8).pin_memory()
             host.copy_(L.experts[0])
@@ -459,11 +605,11 @@ def stack_measurement(torch, moe, args, n_layers=30, steps=256, slots=16):
         except RuntimeError:
             host = hosts[l % max(n_host, 1)]  # host memory ran short: reuse a layer's experts
         L.experts = None
-        layers.append(L)
         hosts.append(host)
         views.append(L.view(experts=False))
         caches.append(moe.Cache(H, E, I, host, slots=slots))
     torch.cuda.synchronize()
+    torch.cuda.empty_cache()
     X = torch.from_numpy(synth.token_sequence(s, steps, seed=0)).to(dev)
     h = [torch.empty((1, H), device=dev), torch.empty((1, H), device=dev)]
     ws = moe.new_workspace(views[0], 1)
