@@ -42,7 +42,7 @@ DECODE_BYTES = TOPK * EXPERT_BYTES + SHARED_BYTES + ROUTER_BYTES  # 37,182,464 B
 # `bench.py --quick` (dram__bytes_read.sum + dram__bytes_write.sum); reported only
 # while the decode kernel's sources are the ones it was taken on (their SHA-1
 # without comments)
-DECODE_NCU_TRAFFIC = {"sha1": "4b69c1ac4058ccc54de2bc33ac7ba8e2923f12e0", "bytes": 37_313_792}
+DECODE_NCU_TRAFFIC = {"sha1": "6921279d20da9c7fa6d079117324820ea31cf55a", "bytes": 37_343_488}
 DECODE_SOURCES = ["bit_affine_quantised_affine4_b300/csrc/" + f for f in
                   ("decode.cuh", "common.cuh", "mma_core.cuh", "route.cuh", "sync.cuh", "tile.cuh",
                    "moe_api.cu")] + ["include/moe.h"]
@@ -329,6 +329,7 @@ def run_ours(args):
         extra = side_measurements(torch, moe, layer, copies, ws, args)
     if not args.quick and rank == 0:
         extra["attention_block"] = attention_measurement(torch, moe, args, peaks)
+        extra["qgemv_affine4"] = qgemv_measurement(torch, moe, args, peaks)
     if args.stack and rank == 0:
         del layer, views
         torch.cuda.empty_cache()
@@ -492,6 +493,38 @@ def attention_measurement(torch, moe, args, peaks):
     out["shape"] = ("hidden 2816, 16 query heads and 8 key/value heads of 256, 4-bit Wqkv [8192 x 2816] and "
                     "Wo [2816 x 4096], binary16 cache; three kernels per call (QKV + RoPE + cache store, "
                     "attention, output projection + residual) with programmatic dependent launch")
+    return out
+
+
+def qgemv_measurement(torch, moe, args, peaks):
+    """qgemv_affine4 alone, one token: the attention block's two matrix shapes
+    ([8192 x 2816] and [2816 x 4096]), rotating over copies whose total exceeds L2;
+    CUDA-graph replay timed with events.  Bytes: the 4-bit weights at 4.5 bits plus
+    x and y."""
+    dev = torch.device("cuda")
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(3)
+    out = {}
+    for N, K in ((8192, 2816), (2816, 4096)):
+        wbytes = N * K * 9 // 16
+        copies = max(4, int(np.ceil(3 * (128 << 20) / wbytes)))
+        mats = [moe.affine_quantise(torch.randn(N, K, generator=gen, device=dev) * 0.02, 4) for _ in range(copies)]
+        x = torch.randn(K, generator=gen, device=dev)
+        y = torch.empty(N, device=dev)
+
+        def steps(n, first):
+            for i in range(first, first + n):
+                q, sc, b = mats[i % copies]
+                moe.qgemv_affine4(q, sc, b, K, x, y=y)
+
+        K_steps = max(40, args.steps // 2)
+        dt = time_graph(torch, steps, K_steps, args.warmup)
+        b = wbytes + K * 4 + N * 4
+        gbs = b / (dt / K_steps) / 1e9
+        out["%dx%d" % (N, K)] = {"us_per_call": dt / K_steps * 1e6, "algorithmic_bytes": b, "GB_s": gbs,
+                                 "frac_of_hbm": gbs / peaks["hbm_gbs"], "copies": copies}
+        del mats
+        torch.cuda.empty_cache()
     return out
 
 
@@ -752,6 +785,38 @@ def run_decode_only(args):
                       "note": "eager launches, 2 layer copies (weights may sit in L2)"}))
 
 
+def run_attention_only(args):
+    """Attention blocks alone (T = 1, pre-norm, residual) on the sliding-window shape
+    (window 1024, ring 1151) or the full shape (store of 4096, last position),
+    rotating over 2 layers, K times after W warm-ups (a short case for profilers)."""
+    import torch
+    import bit_affine_quantised_affine4_b300 as moe
+    a = ATTN_GLOBAL if args.attention_only == "global" else ATTN_SLIDING
+    pos = a.kv_len - 1 if a.window == 0 else 5000
+    dev = torch.device("cuda")
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1)
+    layers = [new_attn_layer(torch, moe, a, gen, dev) for _ in range(2)]
+    views = [l.view() for l in layers]
+    ws = moe.new_attn_workspace(views[0], 1)
+    x = torch.randn(1, a.H, generator=gen, device=dev)
+    y = torch.empty_like(x)
+    flags = moe.MOE_RESIDUAL | moe.MOE_PRENORM
+    for i in range(args.warmup):
+        moe.moe_attn_step(views[i % 2], x, ws, pos, y=y, flags=flags)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(args.steps):
+        moe.moe_attn_step(views[i % 2], x, ws, pos, y=y, flags=flags)
+    e1.record()
+    e1.synchronize()
+    status = moe.moe_attn_workspace_status(ws)
+    print(json.dumps({"workload": "attention block, T=1, %s" % a.name, "us_per_call": e0.elapsed_time(e1) * 1000 /
+                      args.steps, "status": moe.status_string(status),
+                      "note": "eager launches, 2 layers (weights and caches may sit in L2)"}))
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -781,6 +846,8 @@ def main():
     ap.add_argument("--quick", action="store_true", help="headline only, no side measurements")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle timing")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--attention-only", choices=["sliding", "global"], default=None,
+                    help="attention blocks alone (a short case for profilers)")
     ap.add_argument("--prefill-only", action="store_true",
                     help="only the 128-token prefill chunk of one layer (for profilers)")
     ap.add_argument("--decode-only", type=int, default=0, metavar="T",
@@ -794,7 +861,9 @@ def main():
         ap.error("--warmup must be >= 3")
     if args.decode_only and not 1 <= args.decode_only <= 16:
         ap.error("--decode-only takes 1..16 tokens")
-    if args.prefill_only:
+    if args.attention_only:
+        run_attention_only(args)
+    elif args.prefill_only:
         run_prefill_only(args)
     elif args.decode_only:
         run_decode_only(args)

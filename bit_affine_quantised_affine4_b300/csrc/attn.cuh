@@ -77,12 +77,23 @@ __host__ __device__ inline int proj_xs_stride(int K) { return K + 8; }
 // (4 rows x 4 lanes) in distinct banks.
 __host__ __device__ inline int proj_wrow(int K) { return K / 2 + ((32 - (K / 2) % 128) + 128) % 128; }
 
+// Row stride (bytes) of the CTA's scales and of its biases in shared memory.  When
+// a row of G fp16 values is a multiple of 16 bytes (G a multiple of 8) the rows
+// are copied one by one into a stride that is an odd multiple of 16 bytes, so
+// that the 8 rows a fragment reads at one group sit in distinct banks; otherwise
+// the 8-row blocks are copied whole and keep the stride 2G (G = 44: 88 bytes,
+// already conflict-free).
+__host__ __device__ inline int proj_srow(int K) {
+    const int G = K / kGroup;
+    return G % 8 ? 2 * G : 2 * G + ((2 * G) % 32 == 0 ? 16 : 0);
+}
+
 // Shared memory of a projection CTA: the 16 weight rows, their scales and biases,
 // the staged tokens, their per-group sums and the cross-warp reduction.
 template <int MODE>
 inline size_t proj_smem_bytes(int K, int T) {
     const int rows = T < kProjTokens ? T : kProjTokens;
-    return (size_t)16 * proj_wrow(K) + (size_t)2 * 16 * (K / kGroup) * sizeof(__half) +
+    return (size_t)16 * proj_wrow(K) + (size_t)2 * 16 * proj_srow(K) +
            sizeof(__half) * rows * proj_xs_stride(K) + sizeof(float) * rows * (K / kGroup) +
            sizeof(float) * ProjCfg<MODE>::warps * 16 * 8;
 }
@@ -102,12 +113,12 @@ template <int MODE>
 __global__ void __launch_bounds__(proj_threads<MODE>(), MODE == kProjQKV ? 4 : 2) k_attn_proj(const ProjArgs a) {
     constexpr int kWarps = ProjCfg<MODE>::warps, kThreads = 32 * kWarps;
     extern __shared__ __align__(128) unsigned char smem[];
-    const int XS = proj_xs_stride(a.K), WR = proj_wrow(a.K);
+    const int XS = proj_xs_stride(a.K), WR = proj_wrow(a.K), SR = proj_srow(a.K);
     const int G = a.K / kGroup;
     const int t0 = blockIdx.y * kProjTokens, Tc = min(kProjTokens, a.T - t0), Tr = min(a.T, kProjTokens);
     uint8_t *wq = smem;                                                     // [16][WR] codes, rows A then B
-    __half *wsb = reinterpret_cast<__half *>(smem + (size_t)16 * WR);       // [2 (s, b)][16][G]
-    __half *xs = wsb + 2 * 16 * G;                                          // [Tr][XS] staged tokens
+    uint8_t *wsb = smem + (size_t)16 * WR;                                  // [2 (s, b)][16][SR bytes]
+    __half *xs = reinterpret_cast<__half *>(wsb + (size_t)2 * 16 * SR);     // [Tr][XS] staged tokens
     float *gsum = reinterpret_cast<float *>(xs + (size_t)Tr * XS);          // [Tr][G] sums of xs
     float *red = gsum + Tr * G;                                             // [warp][16][8]
     __shared__ float inv_r[kProjTokens];
@@ -136,22 +147,27 @@ __global__ void __launch_bounds__(proj_threads<MODE>(), MODE == kProjQKV ? 4 : 2
 
     // the CTA's weights: 16 code rows, then scales and biases of rows A and B
     if (warp == 0) {
-        const unsigned row_bytes = (unsigned)(a.K / 2), sb_bytes = (unsigned)(8 * G * sizeof(__half));
+        const unsigned row_bytes = (unsigned)(a.K / 2), srow = (unsigned)(G * sizeof(__half));
         if (lane == 0) {
             mbar_init(&bar, 1);
             mbar_fence_init();
             abort_flag = 0;
-            mbar_arrive_expect_tx(&bar, 16 * row_bytes + 4 * sb_bytes);
+            mbar_arrive_expect_tx(&bar, 16 * row_bytes + 32 * srow);
         }
         __syncwarp();
         const uint8_t *qb = reinterpret_cast<const uint8_t *>(a.q);
         if (lane < 16) {
             const int row = lane < 8 ? ra0 + lane : rb0 + (lane - 8);
             bulk_g2s(wq + (size_t)lane * WR, qb + (size_t)row * row_bytes, row_bytes, &bar);
-        } else if (lane < 20) {
-            const int k = lane - 16;  // (scale | bias) x (rows A | rows B)
+        }
+        if (SR != 2 * G) {  // one copy per scale or bias row: lane = (s | b) x 16 rows
+            const int r = lane & 15, row = r < 8 ? ra0 + r : rb0 + (r - 8);
+            const __half *src = ((lane & 16) ? a.b : a.s) + (size_t)row * G;
+            bulk_g2s(wsb + (size_t)(lane >> 4) * 16 * SR + (size_t)r * SR, src, srow, &bar);
+        } else if (lane >= 16 && lane < 20) {  // the 8-row blocks: (scale | bias) x (rows A | rows B)
+            const int k = lane - 16;
             const __half *src = ((k & 1) ? a.b : a.s) + (size_t)((k & 2) ? rb0 : ra0) * G;
-            bulk_g2s(wsb + (size_t)(k & 1) * 16 * G + ((k & 2) ? 8 * G : 0), src, sb_bytes, &bar);
+            bulk_g2s(wsb + (size_t)(k & 1) * 16 * SR + ((k & 2) ? 8 * SR : 0), src, 8 * srow, &bar);
         }
     }
     const int g0 = warp * G / kWarps, g1 = (warp + 1) * G / kWarps;
@@ -253,8 +269,10 @@ __global__ void __launch_bounds__(proj_threads<MODE>(), MODE == kProjQKV ? 4 : 2
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     const int ta = 2 * c, tb = 2 * c + 1;  // the lane's token columns
     const uint8_t *wa_row = wq + (size_t)gl * WR + 8 * c, *wb_row = wq + (size_t)(gl + 8) * WR + 8 * c;
-    const __half *sA = wsb + gl * G, *sB = wsb + (gl + 8) * G, *bA = wsb + 16 * G + gl * G,
-                 *bB = wsb + 16 * G + (gl + 8) * G;
+    const __half *sA = reinterpret_cast<const __half *>(wsb + (size_t)gl * SR),
+                 *sB = reinterpret_cast<const __half *>(wsb + (size_t)(gl + 8) * SR),
+                 *bA = reinterpret_cast<const __half *>(wsb + (size_t)(16 + gl) * SR),
+                 *bB = reinterpret_cast<const __half *>(wsb + (size_t)(24 + gl) * SR);
 #pragma unroll 4
     for (int g = g0; g < g1; g++) {
         uint32_t xb[8];

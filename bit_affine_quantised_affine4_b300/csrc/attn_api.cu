@@ -194,7 +194,30 @@ int launch_attn(const AttnArgs &args, int rt, int tiles, int nkv, cudaStream_t s
     }
 }
 
+__device__ unsigned g_qgemv_err;  // bounded-wait report word of the standalone GEMV
+
 }  // namespace
+
+int moe::qgemv_rows16(const uint32_t *q, const __half *s, const __half *b, int N, int K, const float *x, float *y,
+                      cudaStream_t st) {
+    static unsigned *err = nullptr;
+    int rc;
+    if (!err && cudaGetSymbolAddress(reinterpret_cast<void **>(&err), g_qgemv_err) != cudaSuccess)
+        return attn_cuda_status();
+    if ((rc = proj_smem_optin<kProjPlain>())) return rc;
+    ProjArgs o{};
+    o.q = q;
+    o.s = s;
+    o.b = b;
+    o.N = N;
+    o.K = K;
+    o.x = x;
+    o.T = 1;
+    o.y = y;
+    o.err = err;
+    return launch_pdl(k_attn_proj<kProjPlain>, dim3(N / 16, 1), dim3(proj_threads<kProjPlain>()),
+                      proj_smem_bytes<kProjPlain>(K, 1), st, o);
+}
 
 extern "C" {
 

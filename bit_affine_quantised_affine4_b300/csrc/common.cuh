@@ -192,4 +192,10 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// y = W x for one token with the output-projection kernel of the attention block
+// (16-row tiles, weights by bulk copy into shared memory): N a multiple of 16,
+// K <= 8192, every operand 16-byte aligned.  Defined with that kernel.
+int qgemv_rows16(const uint32_t *q, const __half *s, const __half *b, int N, int K, const float *x, float *y,
+                 cudaStream_t st);
+
 }  // namespace moe

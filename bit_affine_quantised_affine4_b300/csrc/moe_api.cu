@@ -750,6 +750,8 @@ int qgemv_affine4(const uint32_t *q, const uint16_t *s, const uint16_t *b, int N
                   const float *x, float *y, void *stream) {
     if (!q || !s || !b || !x || !y || N < 1 || K < kGroup || K % kGroup) return MOE_EINVAL;
     if (!aligned(q, 16) || !aligned(x, 16)) return MOE_EINVAL;
+    if (N % 16 == 0 && K <= 8192 && aligned(s, 16) && aligned(b, 16) && aligned(y, 16))
+        return qgemv_rows16(q, (const __half *)s, (const __half *)b, N, K, x, y, as_stream(stream));
     QMat m{q, (const __half *)s, (const __half *)b, N, K};
     k_qgemv4_mma<<<(N + 15) / 16, kGemvWarps * 32, 0, as_stream(stream)>>>(m, x, y);
     return cuda_status();

@@ -184,7 +184,10 @@ MOE_API int affine_quantise(const float *w, int N, int K, int bits, uint32_t *q,
  * One 4-bit quantised GEMV, y[n] = sum_j (s[n][j/64] q[n][j] + b[n][j/64]) x[j]
  * (the "quantised GEMV" kernel of the devtrends page, section "Senza dipendenze
  * da llama.cpp e MLX").  q/s/b device [N][K] 4-bit; x device fp32 [K];
- * y device fp32 [N].  N >= 1, K a multiple of 64.
+ * y device fp32 [N].  N >= 1, K a multiple of 64; q and x 16-byte aligned.
+ * With N a multiple of 16, K <= 8192 and s, b, y 16-byte aligned as well, the
+ * rows are read by bulk copies into shared memory, 16 rows per CTA; otherwise by
+ * plain loads.  fp16 x as the tensor-core operand, fp32 accumulation.
  */
 MOE_API int qgemv_affine4(const uint32_t *q, const uint16_t *s, const uint16_t *b, int N, int K,
                   const float *x, float *y, void *stream);

@@ -71,7 +71,8 @@ def test_expert_tile_bit_exact(moe, H, I):
 
 # ------------------------------------------------------------------ qgemv
 
-@pytest.mark.parametrize("N,K", [(4, 64), (100, 320), (4224, 2816), (2816, 704), (2816, 2112)])
+@pytest.mark.parametrize("N,K", [(4, 64), (100, 320), (4224, 2816), (2816, 704), (2816, 2112), (16, 64),
+                                 (48, 8192), (8192, 2816), (2816, 4096)])
 def test_qgemv_affine4(moe, N, K):
     w = synth.normal(synth.key(2, N, K), (N, K), 0.02)
     x = synth.normal(synth.key(3, N, K), (K,), 1.0)
