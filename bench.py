@@ -330,6 +330,7 @@ def run_ours(args):
     if not args.quick and rank == 0:
         extra["attention_block"] = attention_measurement(torch, moe, args, peaks)
         extra["qgemv_affine4"] = qgemv_measurement(torch, moe, args, peaks)
+        extra["sampling_and_rmsnorm"] = sample_norm_measurement(torch, moe, args, peaks)
     if args.stack and rank == 0:
         del layer, views
         torch.cuda.empty_cache()
@@ -525,6 +526,51 @@ def qgemv_measurement(torch, moe, args, peaks):
                                  "frac_of_hbm": gbs / peaks["hbm_gbs"], "copies": copies}
         del mats
         torch.cuda.empty_cache()
+    return out
+
+
+def sample_norm_measurement(torch, moe, args, peaks):
+    """Token sampling (the engine's defaults: temperature 0.2, top-K 64, top-P 0.95)
+    over a 262,144-entry vocabulary for 1 and 16 rows, and RMSNorm of 1 and 16
+    rows of 2816, rotating over inputs larger than L2; CUDA-graph replay timed with
+    events.  Bytes: logits read (sampling), x read + y written + the gain (RMSNorm)."""
+    dev = torch.device("cuda")
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(4)
+    out = {}
+    V = 262144
+    for T in (1, 16):
+        n = max(4, int(np.ceil(3 * (128 << 20) / (T * V * 4))))
+        logits = [torch.randn(T, V, generator=gen, device=dev) * 3.0 for _ in range(n)]
+        u = torch.rand(T, generator=gen, device=dev)
+        tok = torch.empty(T, dtype=torch.int32, device=dev)
+
+        def steps(k, first):
+            for i in range(first, first + k):
+                moe.moe_sample(logits[i % n], 0.2, 64, 0.95, u, tokens=tok)
+
+        K = max(40, args.steps // 2)
+        dt = time_graph(torch, steps, K, args.warmup)
+        gbs = T * V * 4 / (dt / K) / 1e9
+        out["sample_V262144_T%d" % T] = {"us_per_call": dt / K * 1e6, "GB_s": gbs,
+                                         "frac_of_hbm": gbs / peaks["hbm_gbs"]}
+        del logits
+    w = 1.0 + 0.1 * torch.randn(H, generator=gen, device=dev)
+    for T in (1, 16):
+        n = max(4, int(np.ceil(3 * (128 << 20) / (T * H * 8))))
+        xs = [torch.randn(T, H, generator=gen, device=dev) for _ in range(n)]
+        ys = [torch.empty(T, H, device=dev) for _ in range(n)]
+
+        def nsteps(k, first):
+            for i in range(first, first + k):
+                moe.moe_rmsnorm(xs[i % n], w, 1e-6, y=ys[i % n])
+
+        K = max(40, args.steps // 2)
+        dt = time_graph(torch, nsteps, K, args.warmup)
+        b = 2 * T * H * 4 + H * 4
+        out["rmsnorm_H2816_T%d" % T] = {"us_per_call": dt / K * 1e6, "GB_s": b / (dt / K) / 1e9}
+        del xs, ys
+    torch.cuda.empty_cache()
     return out
 
 

@@ -18,7 +18,7 @@ from . import build as _build
 MOE_OK, MOE_EINVAL, MOE_ECUDA, MOE_ECAPACITY, MOE_ETIMEOUT, MOE_EWORKSPACE, MOE_ENOTREADY = range(7)
 MOE_RESIDUAL = 1
 MOE_PRENORM = 2
-MOE_INJECT_NONE, MOE_INJECT_WAIT, MOE_INJECT_COPY = range(3)
+MOE_INJECT_NONE, MOE_INJECT_WAIT, MOE_INJECT_COPY, MOE_INJECT_ATTN_WAIT = range(4)
 MOE_NOALLOC_SCRATCH_BYTES = 4 << 20
 MOE_MAX_TOPK = 8
 MOE_MAX_EXPERTS = 256

@@ -358,6 +358,8 @@ struct AttnArgs {
     float2 *part_ml;   // [nkv][tiles][S][RT] (running max, sum of weights)
     unsigned *ticket;  // [nkv][tiles]
     unsigned *err;     // raised when a bounded wait gives up
+    unsigned extra_tx;            // bytes the first block expects beyond its copies (0; fault injection)
+    unsigned long long wait_ns;   // limit of each wait on the block barrier
     float *ao;         // [T][nq D]
     float *ao_user;    // optional copy of ao
 };
@@ -447,7 +449,8 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(const AttnArgs a) {
             abort_flag = 0;
             // the first block's rows and the queries (a slice without positions copies
             // nothing and posts an empty partial)
-            if (nb0) mbar_arrive_expect_tx(&bar, (unsigned)(2 * nb0 * D * sizeof(__half) + R * D * sizeof(float)));
+            if (nb0)
+                mbar_arrive_expect_tx(&bar, (unsigned)(2 * nb0 * D * sizeof(__half) + R * D * sizeof(float)) + a.extra_tx);
         }
         __syncwarp();
         if (nb0) attn_copy_rows<D>(a, kh, vh, ks, vs, j0, j0, min(j0 + nb0 - 1, a.p0 - 1), &bar, lane);
@@ -486,7 +489,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(const AttnArgs a) {
             __syncwarp();
             attn_copy_rows<D>(a, kh, vh, ks, vs, u0, u0, u0 + nb - 1, &bar, lane);
         }
-        if (!mbar_wait(&bar, phase, &abort_flag)) {
+        if (!mbar_wait(&bar, phase, &abort_flag, a.wait_ns)) {
             abort_flag = 1;
             atomicExch(a.err, 1u);
         }
@@ -577,7 +580,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(const AttnArgs a) {
         // the CTA's shared memory is released; the slice then counts as empty (the
         // error word tells the caller that the outputs are not valid)
         volatile int no_abort = 0;
-        if (tid == 0) mbar_wait(&bar, phase, &no_abort, kWaitNs / 4);
+        if (tid == 0) mbar_wait(&bar, phase, &no_abort, a.wait_ns);
 #pragma unroll
         for (int r = 0; r < RT; r++) acc[r][0] = acc[r][1] = 0.f;
         if (tid < RT) {

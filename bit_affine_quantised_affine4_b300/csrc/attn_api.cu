@@ -289,6 +289,11 @@ int moe_attn_step(const moe_attn_t *attn, const float *x, int T, int pos, int fl
     g.part_ml = w.part_ml;
     g.ticket = w.ticket;
     g.err = w.err;
+    g.wait_ns = kWaitNs;
+    if (take_injection(MOE_INJECT_ATTN_WAIT)) {  // the blocks' barriers wait for 16 bytes that never come
+        g.extra_tx = 16;
+        g.wait_ns = 2ull * 1000 * 1000;
+    }
     g.ao = w.ao;
     g.ao_user = attn_out;
     const int rt = rows_of(a, T);

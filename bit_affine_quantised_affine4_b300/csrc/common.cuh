@@ -192,6 +192,9 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// Consumes a pending moe_debug_inject of kind `what` (true if there was one).
+bool take_injection(int what);
+
 // y = W x for one token with the output-projection kernel of the attention block
 // (16-row tiles, weights by bulk copy into shared memory): N a multiple of 16,
 // K <= 8192, every operand 16-byte aligned.  Defined with that kernel.

@@ -710,7 +710,8 @@ size_t moe_decode_workspace_bytes(const moe_layer_t *layer, int T_max) {
 }
 
 int moe_debug_inject(int what) {
-    if (what != MOE_INJECT_NONE && what != MOE_INJECT_WAIT && what != MOE_INJECT_COPY) return MOE_EINVAL;
+    if (what != MOE_INJECT_NONE && what != MOE_INJECT_WAIT && what != MOE_INJECT_COPY && what != MOE_INJECT_ATTN_WAIT)
+        return MOE_EINVAL;
     g_inject.store(what);
     return MOE_OK;
 }
@@ -735,7 +736,9 @@ int moe_sample(const float *logits, int T, int V, float temperature, int top_k, 
     if (!aligned(logits, 4) || !aligned(u, 4) || !aligned(tokens, 4)) return MOE_EINVAL;
     const int K = (top_k <= 0 || top_k >= V) ? V : top_k;
     if (temperature > 0.f && K > kSampleMaxK) return MOE_EINVAL;
-    k_sample<<<T, kSampleThreads, 0, as_stream(stream)>>>(logits, V, temperature, K, top_p, u, tokens);
+    // one cluster of kSampleCluster CTAs per row (the kernel's static cluster shape)
+    k_sample<<<T * kSampleCluster, kSampleThreads, 0, as_stream(stream)>>>(logits, V, temperature, K, top_p, u,
+                                                                        tokens);
     return cuda_status();
 }
 
@@ -988,3 +991,5 @@ int moe_noalloc_status(void *stream) {
 }
 
 }  // extern "C"
+
+bool moe::take_injection(int what) { return take_inject(what); }

@@ -422,12 +422,18 @@ MOE_API int moe_cache_set_device_policy(moe_cache_t *cache, int enable);
  *   MOE_INJECT_COPY  the next host -> device expert copy of a cached decode fails
  *                    as if cudaMemcpyAsync had returned an error: the call returns
  *                    MOE_ECUDA and the cache's policy state is as before the call.
+ *   MOE_INJECT_ATTN_WAIT  the next moe_attn_step makes its attention CTAs expect
+ *                    16 bytes more than their copies bring, with a 2 ms limit:
+ *                    the waits give up, the CTAs drain, and
+ *                    moe_attn_workspace_status reports MOE_ETIMEOUT (the keys
+ *                    and values of the call are stored; its outputs are not valid).
  *   MOE_INJECT_NONE  clears a pending injection.
  * No GPU fault is involved.  Returns MOE_EINVAL for an unknown value.
  */
 #define MOE_INJECT_NONE 0
 #define MOE_INJECT_WAIT 1
 #define MOE_INJECT_COPY 2
+#define MOE_INJECT_ATTN_WAIT 3
 MOE_API int moe_debug_inject(int what);
 
 /* ---------------------------------------------------------------- attention */

@@ -199,3 +199,26 @@ def test_refusals():
     assert rc(ws=p.ws.data_ptr() + 8) == moe.MOE_EWORKSPACE
     # nothing ran for the refused calls: the next call still matches the oracle, cache included
     p.step(_tokens(shape, 1, 1), 2)
+
+
+def test_attention_wait_times_out_and_recovers():
+    """Fault injection (no GPU fault): the next call's attention CTAs expect 16
+    bytes more than their copies bring, with a 2 ms limit.  The waits give up, the
+    workspace status reports MOE_ETIMEOUT once, and the next call matches the oracle
+    again (the timed-out call stored its keys and values, as the oracle's copy of the
+    call does, and its slices still took their tickets)."""
+    shape = synth.ATTN_TINY_SLIDING
+    p = Pair(shape, seed=8)
+    moe, torch = p.moe, p.torch
+    p.step(_tokens(shape, 1, 0), 30)
+    assert moe.moe_attn_workspace_status(p.ws) == moe.MOE_OK
+    moe.moe_debug_inject(moe.MOE_INJECT_ATTN_WAIT)
+    x = _tokens(shape, 2, 1)
+    xd = torch.from_numpy(x).cuda()
+    moe.moe_attn_step(p.view, xd, p.ws, 31, flags=moe.MOE_RESIDUAL)
+    s = shape
+    oracle.attn_step(s.H, s.nq, s.nkv, s.d, s.window, s.kv_len, s.theta, s.scale, p.wqkv, p.wo, p.k, p.v, x, 31)
+    assert moe.moe_attn_workspace_status(p.ws) == moe.MOE_ETIMEOUT
+    assert moe.moe_attn_workspace_status(p.ws) == moe.MOE_OK
+    p.step(_tokens(shape, 1, 2), 33)
+    p.step(_tokens(shape, 3, 3), 34)

@@ -75,3 +75,23 @@ def test_sample_rejects_bad_arguments():
         with pytest.raises(moe.MoeError) as e:
             moe.moe_sample(lg, temp, k, p, u)
         assert e.value.status == moe.MOE_EINVAL
+
+
+def test_sample_large_vocab_both_paths():
+    """262,144 logits: a row whose top bin holds 10,000 equal maxima (more than the
+    4096 packs the compacting path keeps: the radix-select path runs) beside plain
+    rows (the compacting path)."""
+    import bit_affine_quantised_affine4_b300 as moe
+    V, T = 262144, 3
+    rng = np.random.default_rng(7)
+    lg = (2.0 * rng.standard_normal((T, V))).astype(np.float32)
+    lg[0, rng.choice(V, 10000, replace=False)] = lg[0].max() + 0.5
+    u = rng.random(T).astype(np.float32)
+    for temp, k, p in ((0.2, 64, 0.95), (1.0, 1000, 1.0)):
+        tok = moe.moe_sample(torch.from_numpy(lg).cuda(), temp, k, p, torch.from_numpy(u).cuda())
+        torch.cuda.synchronize()
+        got = tok.cpu().numpy()
+        for t in range(T):
+            want, margin = oracle.sample(lg[t], temp, k, p, float(u[t]))
+            if margin >= 1e-5:
+                assert got[t] == want, (temp, k, p, t)
