@@ -222,3 +222,44 @@ def test_attention_wait_times_out_and_recovers():
     assert moe.moe_attn_workspace_status(p.ws) == moe.MOE_OK
     p.step(_tokens(shape, 1, 2), 33)
     p.step(_tokens(shape, 3, 3), 34)
+
+
+def test_decode_step_stack_teacher_forced():
+    """A decode step of a small stack as in the 30-layer workload: per layer the
+    pre-norm attention block, then the pre-norm MoE block; layers 0 and 1 attend
+    to a window (16 positions in a ring of 23, which wraps during the steps),
+    layer 2 to the whole context (a store of 96).  Teacher-forced per block: each
+    oracle block runs on the GPU's input to that block (the oracle keeps its own
+    key/value caches, which track the GPU's to binary16 rounding).  Checked every
+    step and block: outputs within 2e-3 (1 + |oracle|), expert indices bit-exact."""
+    import bit_affine_quantised_affine4_b300 as moe
+    from layers import OracleLayer, gpu_layer, norm_weights, within_tol
+    s = synth.TINY
+    eps = 1e-6
+    attn, moes, omoes, mnorms = [], [], [], []
+    for l in range(3):
+        a = synth.ATTN_TINY_FULL if l == 2 else synth.ATTN_TINY_SLIDING
+        attn.append(Pair(a, seed=20, layer=l, norm=(synth.norm_weights(a.H, seed=20, layer=l), eps)))
+        bias = synth.popularity_bias(s, seed=0, layer=l)
+        norm = (norm_weights(s, 0, l), eps)
+        mnorms.append(norm)
+        moes.append(gpu_layer(s, seed=0, layer=l, bias=bias, norm=norm))
+        omoes.append(OracleLayer(s, seed=0, layer=l, bias=bias))
+    mviews = [g.view() for g in moes]
+    ws = moe.new_workspace(mviews[0], 1)
+    import torch
+    idx = torch.empty((1, s.topk), dtype=torch.int32, device="cuda")
+    xs = synth.token_sequence(s, 8, seed=1)
+    pos0 = 60
+    for k in range(8):
+        h = xs[k:k + 1].astype(np.float32)
+        for l in range(3):
+            ha = attn[l].step(h, pos0 + k).cpu().numpy()  # checks y, o and the caches against the oracle
+            y = moe.moe_layer_decode(mviews[l], torch.from_numpy(ha).cuda(), ws,
+                                     flags=moe.MOE_RESIDUAL | moe.MOE_PRENORM, idx=idx)
+            torch.cuda.synchronize()
+            ry, ridx, _ = omoes[l].block(ha, *mnorms[l])
+            assert np.array_equal(idx.cpu().numpy(), ridx), (k, l)
+            ok, worst = within_tol(y.cpu().numpy(), ry, 2e-3)
+            assert ok, "step %d layer %d: worst err/bound %.3f" % (k, l, worst)
+            h = y.cpu().numpy()
