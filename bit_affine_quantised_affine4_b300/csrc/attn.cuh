@@ -28,6 +28,8 @@
 // the T tokens attends to.
 #pragma once
 
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "mma_core.cuh"
 #include "sync.cuh"
@@ -348,35 +350,41 @@ __global__ void __launch_bounds__(proj_threads<MODE>(), MODE == kProjQKV ? 4 : 2
 
 // ---------------------------------------------------------------- attention
 
-constexpr int kAttnSlice = 32;  // positions per shared-memory block of the attention CTA
+constexpr int kAttnSlice = 32;       // positions per shared-memory block
+constexpr int kAttnStages = 2;       // blocks of one CTA in flight at once
+constexpr int kAttnMaxCluster = 16;  // CTAs (slices) merged in distributed shared memory
 
 struct AttnArgs {
     const float *qr;  // [T][nq][D] rotated queries times the score scale
     const __half *kc, *vc;
-    int nq, nkv, G, kv_len, window, p0, T, S;
-    float *part_o;     // [nkv][tiles][S][RT][D] unnormalised outputs
-    float2 *part_ml;   // [nkv][tiles][S][RT] (running max, sum of weights)
+    int nq, nkv, G, kv_len, window, p0, T;
+    int S;             // slices of a tile's positions (gridDim.x), a multiple of the cluster size
+    int nst;           // shared-memory blocks of a CTA in flight (1 or kAttnStages)
+    float *part_o;     // [nkv][tiles][S / cluster][RT][D] unnormalised outputs of the clusters
+    float2 *part_ml;   // [nkv][tiles][S / cluster][RT] (running max, sum of weights)
     unsigned *ticket;  // [nkv][tiles]
     unsigned *err;     // raised when a bounded wait gives up
     unsigned extra_tx;            // bytes the first block expects beyond its copies (0; fault injection)
-    unsigned long long wait_ns;   // limit of each wait on the block barrier
+    unsigned long long wait_ns;   // limit of each wait on a block barrier
     float *ao;         // [T][nq D]
     float *ao_user;    // optional copy of ao
 };
 
 __device__ __forceinline__ int attn_lo(int p, int window) { return window > 0 ? max(0, p - window + 1) : 0; }
 
-// Dynamic shared memory of the attention CTA: the tile's queries, one block of
-// key rows (each row padded by 16 bytes, so that 32 lanes reading 32 rows hit
-// distinct banks) and one block of value rows, binary16.
+// Shared memory of the attention CTA (dynamic part): the tile's queries, then
+// kAttnStages blocks, each of key rows (padded by 16 bytes, so that 32 lanes
+// reading 32 rows hit distinct banks) and value rows, binary16.
 __host__ __device__ constexpr int attn_kstride(int D) { return D + 8; }  // halves
-__host__ __device__ constexpr size_t attn_smem_bytes(int D, int RT) {
-    return (size_t)RT * D * sizeof(float) + (size_t)kAttnSlice * attn_kstride(D) * sizeof(__half) +
-           (size_t)kAttnSlice * D * sizeof(__half);
+__host__ __device__ constexpr size_t attn_stage_bytes(int D) {
+    return (size_t)kAttnSlice * attn_kstride(D) * sizeof(__half) + (size_t)kAttnSlice * D * sizeof(__half);
+}
+__host__ __device__ constexpr size_t attn_smem_bytes(int D, int RT, int nst = kAttnStages) {
+    return (size_t)RT * D * sizeof(float) + nst * attn_stage_bytes(D);
 }
 
 // Issues the bulk copies of positions [c0, c1] (cache rows of one key/value head)
-// into rows c0 - u0 .. of the block: one copy per key row (padded rows), one per
+// into rows c0 - u0 .. of a block: one copy per key row (padded rows), one per
 // contiguous run of value rows (a ring's wrap splits a run in two).  Lane `lane`
 // of the calling warp issues every 32nd key row; lane 0 the value runs.
 template <int D>
@@ -397,6 +405,18 @@ __device__ __forceinline__ void attn_copy_rows(const AttnArgs &a, const __half *
 // RT: (token, query head) rows of a tile, 1, 2, 4 or 8 (the host picks the
 // smallest power of two that holds the call's rows, at most 8).
 //
+// Grid (S slices, tiles, key/value heads); the slices of one tile run as thread
+// block clusters of up to kAttnMaxCluster CTAs.  A CTA takes its slice's positions
+// in blocks of kAttnSlice, nst blocks in flight (bulk copies on one mbarrier per
+// stage), and keeps a running maximum and sum per row.  The host gives a slice
+// two blocks and makes the tile's slices one cluster when that covers the tile
+// (a window of up to 1024 positions); otherwise a slice has one block and its own
+// cluster of one.  The cluster
+// then merges its slices through distributed shared memory; when one cluster
+// covers the tile (a decode token's window or context up to kAttnMaxCluster x 64
+// positions) its leader writes the attention output directly, otherwise the
+// cluster leaders post partials and the last of them (a ticket) merges those.
+//
 // Launched with programmatic dependent launch.  Before griddepcontrol.wait the
 // CTA starts the bulk copies of the cached rows of earlier tokens (positions below
 // this call's first): every kernel of the library signals its dependents only
@@ -411,26 +431,31 @@ __device__ __forceinline__ void attn_copy_rows(const AttnArgs &a, const __half *
 // 2 slot_d, 2 slot_d + 1) over the positions of its plane.
 template <int D, int RT>
 __global__ void __launch_bounds__(kAttnThreads) k_attn(const AttnArgs a) {
+    namespace cg = cooperative_groups;
     constexpr int PL = kAttnThreads / (D / 2);  // position planes of the value pass
     constexpr int DW = D / kAttnWarps;          // dimensions per warp in the score pass
     constexpr int KS = attn_kstride(D);
     extern __shared__ __align__(128) unsigned char dsm[];
-    float *qs = reinterpret_cast<float *>(dsm);                          // [RT][D]
-    __half *ks = reinterpret_cast<__half *>(dsm + (size_t)RT * D * 4);   // [kAttnSlice][KS]
-    __half *vs = ks + (size_t)kAttnSlice * KS;                           // [kAttnSlice][D]
+    float *qs = reinterpret_cast<float *>(dsm);  // [RT][D]
+    auto kst = [&](int st) {
+        return reinterpret_cast<__half *>(dsm + (size_t)RT * D * sizeof(float) + st * attn_stage_bytes(D));
+    };
+    auto vst = [&](int st) { return kst(st) + (size_t)kAttnSlice * KS; };
     __shared__ float scp[kAttnWarps][RT][kAttnSlice];  // partial scores of each warp
     __shared__ float sc[RT][kAttnSlice];
-    __shared__ __align__(16) float red[PL][RT][D];
-    __shared__ float m_run[RT], l_run[RT], alpha[RT], den[RT];
-    __shared__ float ew[RT][kAttnMaxSlices];  // combine: weight of each slice
-    __shared__ float4 part4[kAttnThreads];    // combine: [nph][kAttnThreads / nph] partial sums
+    __shared__ __align__(16) float red[PL][RT][D];  // the slice's output ends in red[0]
+    __shared__ float m_run[RT], l_run[RT], alpha[RT], den[RT], cm[RT];
+    __shared__ float ew[RT][kAttnMaxSlices];  // merge: weight of each slice or cluster
+    __shared__ float4 part4[kAttnThreads];    // merge: [nph][kAttnThreads / nph] partial sums
     __shared__ int row_p[RT], row_lo[RT];
-    __shared__ __align__(8) uint64_t bar;
+    __shared__ __align__(8) uint64_t bar[kAttnStages];
     __shared__ int abort_flag;
     __shared__ unsigned last;
+    cg::cluster_group cl = cg::this_cluster();
+    const int CS = (int)cl.num_blocks(), crank = (int)cl.block_rank();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int s = blockIdx.x, tile = blockIdx.y, h = blockIdx.z;
-    const int tiles = gridDim.y;
+    const int tiles = gridDim.y, ncl = a.S / CS, cidx = s / CS;
     const int R = min(RT, a.T * a.G - tile * RT);  // live rows of this tile
 
     // the tile's positions [A, B] and this slice of them, in blocks of kAttnSlice
@@ -438,31 +463,39 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(const AttnArgs a) {
     const int A = attn_lo(a.p0 + t_first, a.window), B = a.p0 + t_last;
     const int L = (B - A + a.S) / a.S;  // ceil((B - A + 1) / S)
     const int j0 = A + s * L, j1 = min(B, j0 + L - 1);
+    const int nblk = j0 <= j1 ? (j1 - j0 + kAttnSlice) / kAttnSlice : 0;
+    auto block_n = [&](int bk) { return min(kAttnSlice, j1 - (j0 + bk * kAttnSlice) + 1); };
     const __half *kh = a.kc + (size_t)h * a.kv_len * D;
     const __half *vh = a.vc + (size_t)h * a.kv_len * D;
-    const int nb0 = j0 <= j1 ? min(kAttnSlice, j1 - j0 + 1) : 0;  // positions of the first block
+    const int first = min(nblk, a.nst);  // blocks copied at the start
 
     if (warp == 0) {
         if (lane == 0) {
-            mbar_init(&bar, 1);
+            for (int st = 0; st < kAttnStages; st++) mbar_init(&bar[st], 1);
             mbar_fence_init();
             abort_flag = 0;
-            // the first block's rows and the queries (a slice without positions copies
-            // nothing and posts an empty partial)
-            if (nb0)
-                mbar_arrive_expect_tx(&bar, (unsigned)(2 * nb0 * D * sizeof(__half) + R * D * sizeof(float)) + a.extra_tx);
+            // the first blocks' rows (and, on stage 0, the queries)
+            for (int bk = 0; bk < first; bk++)
+                mbar_arrive_expect_tx(&bar[bk], (unsigned)(2 * block_n(bk) * D * sizeof(__half)) +
+                                                    (bk == 0 ? (unsigned)(R * D * sizeof(float)) + a.extra_tx : 0u));
         }
         __syncwarp();
-        if (nb0) attn_copy_rows<D>(a, kh, vh, ks, vs, j0, j0, min(j0 + nb0 - 1, a.p0 - 1), &bar, lane);
+        for (int bk = 0; bk < first; bk++) {
+            const int u0 = j0 + bk * kAttnSlice;
+            attn_copy_rows<D>(a, kh, vh, kst(bk), vst(bk), u0, u0, min(u0 + block_n(bk) - 1, a.p0 - 1), &bar[bk], lane);
+        }
     }
     pdl_wait();
     pdl_launch_dependents();
-    if (warp == 0 && nb0) {
-        attn_copy_rows<D>(a, kh, vh, ks, vs, j0, max(j0, a.p0), j0 + nb0 - 1, &bar, lane);
+    if (warp == 0 && nblk) {
+        for (int bk = 0; bk < first; bk++) {
+            const int u0 = j0 + bk * kAttnSlice;
+            attn_copy_rows<D>(a, kh, vh, kst(bk), vst(bk), u0, max(u0, a.p0), u0 + block_n(bk) - 1, &bar[bk], lane);
+        }
         // queries: row r is token t's head h G + g
         for (int r = lane; r < R; r += 32) {
             const int rg = tile * RT + r, t = rg / a.G, g = rg % a.G;
-            bulk_g2s(qs + (size_t)r * D, a.qr + ((size_t)t * a.nq + h * a.G + g) * D, D * sizeof(float), &bar);
+            bulk_g2s(qs + (size_t)r * D, a.qr + ((size_t)t * a.nq + h * a.G + g) * D, D * sizeof(float), &bar[0]);
         }
     }
     if (tid < RT) {
@@ -481,15 +514,13 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(const AttnArgs a) {
 #pragma unroll
     for (int r = 0; r < RT; r++) acc[r][0] = acc[r][1] = 0.f;
 
-    unsigned phase = 0;
-    for (int u0 = j0; u0 <= j1; u0 += kAttnSlice, phase ^= 1u) {
-        const int nb = min(kAttnSlice, j1 - u0 + 1);
-        if (u0 != j0 && warp == 0) {  // a later block (slices longer than one block)
-            if (lane == 0) mbar_arrive_expect_tx(&bar, (unsigned)(2 * nb * D * sizeof(__half)));
-            __syncwarp();
-            attn_copy_rows<D>(a, kh, vh, ks, vs, u0, u0, u0 + nb - 1, &bar, lane);
-        }
-        if (!mbar_wait(&bar, phase, &abort_flag, a.wait_ns)) {
+    int issued = first, bk = 0;
+    for (; bk < nblk; bk++) {
+        const int st = bk % a.nst;
+        const unsigned phase = (unsigned)(bk / a.nst) & 1u;
+        const int u0 = j0 + bk * kAttnSlice, nb = block_n(bk);
+        const __half *ks = kst(st), *vs = vst(st);
+        if (!mbar_wait(&bar[st], phase, &abort_flag, a.wait_ns)) {
             abort_flag = 1;
             atomicExch(a.err, 1u);
         }
@@ -573,14 +604,23 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(const AttnArgs a) {
                 acc[r][1] = fmaf(w, v.y, acc[r][1]);
             }
         }
-        __syncthreads();  // the block's rows and scores are rewritten by the next block
+        __syncthreads();  // the stage's rows and the scores are free again
+        if (issued < nblk && warp == 0) {  // the next block into the freed stage
+            const int u2 = j0 + issued * kAttnSlice, n2 = block_n(issued);
+            if (lane == 0) mbar_arrive_expect_tx(&bar[st], (unsigned)(2 * n2 * D * sizeof(__half)));
+            __syncwarp();
+            attn_copy_rows<D>(a, kh, vh, kst(st), vst(st), u2, u2, u2 + n2 - 1, &bar[st], lane);
+        }
+        if (issued < nblk) issued++;
     }
     if (abort_flag) {
-        // a copy that never completed may still land: give it time (bounded) before
-        // the CTA's shared memory is released; the slice then counts as empty (the
-        // error word tells the caller that the outputs are not valid)
+        // copies that never completed may still land: give each stage in flight time
+        // (bounded) before the CTA's shared memory is released; the slice then counts
+        // as empty (the error word tells the caller that the outputs are not valid)
         volatile int no_abort = 0;
-        if (tid == 0) mbar_wait(&bar, phase, &no_abort, a.wait_ns);
+        if (tid == 0)
+            for (int k = bk; k < issued; k++)
+                mbar_wait(&bar[k % a.nst], (unsigned)(k / a.nst) & 1u, &no_abort, a.wait_ns);
 #pragma unroll
         for (int r = 0; r < RT; r++) acc[r][0] = acc[r][1] = 0.f;
         if (tid < RT) {
@@ -590,47 +630,99 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(const AttnArgs a) {
         __syncthreads();
     }
 
-    // the slice's partial: planes summed in order
+    // the slice's output (planes summed in order) into red[0]
 #pragma unroll
     for (int r = 0; r < RT; r++) {
         red[plane][r][2 * slot_d] = acc[r][0];
         red[plane][r][2 * slot_d + 1] = acc[r][1];
     }
     __syncthreads();
-    const size_t pbase = (((size_t)h * tiles + tile) * a.S + s) * RT;
-    for (int u = tid; u < R * (D / 4); u += kAttnThreads) {
-        const int r = u / (D / 4), i = (u % (D / 4)) * 4;
-        float4 v = *reinterpret_cast<const float4 *>(&red[0][r][i]);
+    if (PL > 1)
+        for (int u = tid; u < RT * (D / 4); u += kAttnThreads) {
+            const int r = u / (D / 4), i = (u % (D / 4)) * 4;
+            float4 v = *reinterpret_cast<const float4 *>(&red[0][r][i]);
 #pragma unroll
-        for (int pl = 1; pl < PL; pl++) {
-            const float4 w = *reinterpret_cast<const float4 *>(&red[pl][r][i]);
-            v.x += w.x; v.y += w.y; v.z += w.z; v.w += w.w;
+            for (int pl = 1; pl < PL; pl++) {
+                const float4 w = *reinterpret_cast<const float4 *>(&red[pl][r][i]);
+                v.x += w.x; v.y += w.y; v.z += w.z; v.w += w.w;
+            }
+            *reinterpret_cast<float4 *>(&red[0][r][i]) = v;
         }
-        *reinterpret_cast<float4 *>(a.part_o + (pbase + r) * D + i) = v;
-    }
-    if (tid < R) a.part_ml[pbase + tid] = make_float2(m_run[tid], l_run[tid]);
 
-    // the last slice of (head, tile) merges all of them, in slice order
+    // ---- the cluster's slices merged by its leader (distributed shared memory)
+    cl.sync();
+    if (crank == 0) {
+        if (warp < R) {  // row `warp`: the largest maximum, each slice's weight, the total
+            const float mk = lane < CS ? *cl.map_shared_rank(&m_run[warp], lane) : -INFINITY;
+            const float lk = lane < CS ? *cl.map_shared_rank(&l_run[warp], lane) : 0.f;
+            float M = lk > 0.f ? mk : -INFINITY;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+            const float e = lk > 0.f ? __expf(mk - M) : 0.f;
+            if (lane < CS) ew[warp][lane] = e;
+            float lt = lk * e;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) lt += __shfl_xor_sync(0xffffffffu, lt, o);
+            if (lane == 0) {
+                cm[warp] = M;
+                den[warp] = lt;
+            }
+        }
+        __syncthreads();
+        for (int u = tid; u < R * (D / 4); u += kAttnThreads) {
+            const int r = u / (D / 4), i = (u % (D / 4)) * 4;
+            float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int k0 = 0; k0 < CS; k0 += 4) {  // four CTAs' rows in flight at a time
+                float4 v[4];
+#pragma unroll
+                for (int k = 0; k < 4; k++)
+                    v[k] = k0 + k < CS ? *reinterpret_cast<const float4 *>(cl.map_shared_rank(&red[0][r][i], k0 + k))
+                                       : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int k = 0; k < 4; k++) {
+                    const float e = k0 + k < CS ? ew[r][k0 + k] : 0.f;
+                    o.x = fmaf(v[k].x, e, o.x); o.y = fmaf(v[k].y, e, o.y);
+                    o.z = fmaf(v[k].z, e, o.z); o.w = fmaf(v[k].w, e, o.w);
+                }
+            }
+            if (ncl == 1) {  // the whole tile: the attention output
+                const int rg = tile * RT + r, t = rg / a.G, g = rg % a.G;
+                const float inv = 1.f / den[r];
+                const float4 out = make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
+                const size_t at = (size_t)t * a.nq * D + (size_t)(h * a.G + g) * D + i;
+                *reinterpret_cast<float4 *>(a.ao + at) = out;
+                if (a.ao_user) *reinterpret_cast<float4 *>(a.ao_user + at) = out;
+            } else {
+                const size_t pbase = (((size_t)h * tiles + tile) * ncl + cidx) * RT;
+                *reinterpret_cast<float4 *>(a.part_o + (pbase + r) * D + i) = o;
+            }
+        }
+        if (ncl > 1 && tid < R) {
+            const size_t pbase = (((size_t)h * tiles + tile) * ncl + cidx) * RT;
+            a.part_ml[pbase + tid] = make_float2(cm[tid], den[tid]);
+        }
+    }
+    cl.sync();  // the leader has read every slice: the others may leave
+    if (crank != 0 || ncl == 1) return;
+
+    // ---- several clusters: the last leader of (head, tile) merges their partials
     __threadfence();
     __syncthreads();
     if (tid == 0) {
         const unsigned prev = atomicAdd(&a.ticket[h * tiles + tile], 1u);
-        last = prev == (unsigned)a.S - 1u;
+        last = prev == (unsigned)ncl - 1u;
     }
     __syncthreads();
     if (!last) return;
     __threadfence();
-    const size_t pb0 = ((size_t)h * tiles + tile) * a.S * RT;
-    // per row: the largest slice maximum M, each slice's weight exp(m_s - M) (0 for
-    // a slice without positions) and the total weight; warp r owns row r and reads
-    // every slice's (max, sum) once
+    const size_t pb0 = ((size_t)h * tiles + tile) * ncl * RT;
     if (warp < R) {
         constexpr int PerLane = kAttnMaxSlices / 32;
         float2 ml[PerLane];
 #pragma unroll
         for (int k = 0; k < PerLane; k++) {
             const int q = lane + 32 * k;
-            ml[k] = q < a.S ? __ldcg(a.part_ml + pb0 + (size_t)q * RT + warp) : make_float2(-INFINITY, 0.f);
+            ml[k] = q < ncl ? __ldcg(a.part_ml + pb0 + (size_t)q * RT + warp) : make_float2(-INFINITY, 0.f);
         }
         float M = -INFINITY;
 #pragma unroll
@@ -643,7 +735,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(const AttnArgs a) {
         for (int k = 0; k < PerLane; k++) {
             const int q = lane + 32 * k;
             const float e = ml[k].y > 0.f ? __expf(ml[k].x - M) : 0.f;
-            if (q < a.S) ew[warp][q] = e;
+            if (q < ncl) ew[warp][q] = e;
             l = fmaf(ml[k].y, e, l);
         }
 #pragma unroll
@@ -651,8 +743,8 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(const AttnArgs a) {
         if (lane == 0) den[warp] = l;
     }
     __syncthreads();
-    // the weighted sum of the slices' outputs, four dimensions per item; the slices
-    // are split over nph phases when there are fewer items than threads
+    // the weighted sum of the partials, four dimensions per item; the partials are
+    // split over nph phases when there are fewer items than threads
     const int items = R * (D / 4);
     const int nph = items >= kAttnThreads ? 1 : kAttnThreads / items;
     const int per = kAttnThreads / nph;
@@ -663,18 +755,18 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(const AttnArgs a) {
         if (live) {
             const int r = it / (D / 4), i = (it % (D / 4)) * 4;
             const float4 *src = reinterpret_cast<const float4 *>(a.part_o + (pb0 + r) * D + i);
-            const size_t stride = (size_t)RT * D / 4;  // float4s from one slice to the next
-            for (int q = ph; q < a.S; q += 8 * nph) {
+            const size_t stride = (size_t)RT * D / 4;  // float4s from one partial to the next
+            for (int q = ph; q < ncl; q += 8 * nph) {
                 float4 v[8];
 #pragma unroll
                 for (int k = 0; k < 8; k++) {
                     const int qq = q + k * nph;
-                    v[k] = qq < a.S ? __ldcg(src + (size_t)qq * stride) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    v[k] = qq < ncl ? __ldcg(src + (size_t)qq * stride) : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
 #pragma unroll
                 for (int k = 0; k < 8; k++) {
                     const int qq = q + k * nph;
-                    const float e = qq < a.S ? ew[r][qq] : 0.f;
+                    const float e = qq < ncl ? ew[r][qq] : 0.f;
                     num.x = fmaf(v[k].x, e, num.x); num.y = fmaf(v[k].y, e, num.y);
                     num.z = fmaf(v[k].z, e, num.z); num.w = fmaf(v[k].w, e, num.w);
                 }

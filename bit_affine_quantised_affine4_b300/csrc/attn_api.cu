@@ -121,27 +121,39 @@ int proj_smem_optin() {
 // that one finishes; each kernel waits (griddepcontrol.wait) before it reads the
 // predecessor's output.  If the runtime refuses the attribute, plain launches are
 // used from then on.
+// `cluster` > 1 launches thread block clusters of that many CTAs along x.
 template <typename Args>
-int launch_pdl(void (*fn)(Args), dim3 grid, dim3 block, size_t smem, cudaStream_t st, const Args &args) {
+int launch_pdl(void (*fn)(Args), dim3 grid, dim3 block, size_t smem, cudaStream_t st, const Args &args,
+               int cluster = 1) {
     static std::atomic<int> pdl_ok{1};
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    if (cluster > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = (unsigned)cluster;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        n++;
+    }
     if (pdl_ok.load()) {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = grid;
-        cfg.blockDim = block;
-        cfg.dynamicSmemBytes = smem;
-        cfg.stream = st;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        cfg.numAttrs = n + 1;
         const cudaError_t e = cudaLaunchKernelEx(&cfg, fn, args);
         if (e == cudaSuccess) return attn_cuda_status();
         if (e != cudaErrorInvalidValue && e != cudaErrorNotSupported) return attn_cuda_status();
         (void)cudaGetLastError();
         pdl_ok.store(0);
     }
-    fn<<<grid, block, smem, st>>>(args);
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    if (cudaLaunchKernelEx(&cfg, fn, args) != cudaSuccess) return attn_cuda_status();
     return attn_cuda_status();
 }
 
@@ -171,26 +183,80 @@ void rope_freqs(float theta, int d, double *out) {
     memcpy(out, n.f, sizeof(double) * (d / 2));
 }
 
+// The largest cluster of k_attn<D, RT> CTAs the device co-schedules: 16 (a
+// non-portable size) when it can, else 8; found once per kernel.
 template <int D, int RT>
-int launch_attn_rt(const AttnArgs &args, dim3 grid, cudaStream_t st) {
-    static std::atomic<int> ready{0};
-    if (!ready.load()) {
-        if (cudaFuncSetAttribute(k_attn<D, RT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)attn_smem_bytes(D, RT)) !=
-            cudaSuccess)
-            return attn_cuda_status();
-        ready.store(1);
+int attn_max_cluster() {
+    static std::atomic<int> cmax{0};
+    int c = cmax.load();
+    if (c) return c;
+    if (cudaFuncSetAttribute(k_attn<D, RT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)attn_smem_bytes(D, RT)) != cudaSuccess)
+        return -attn_cuda_status();
+    c = 8;
+    if (cudaFuncSetAttribute(k_attn<D, RT>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(kAttnMaxCluster, 1, 1);
+        cfg.blockDim = dim3(kAttnThreads);
+        cfg.dynamicSmemBytes = attn_smem_bytes(D, RT);
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = kAttnMaxCluster;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, k_attn<D, RT>, &cfg) == cudaSuccess && n > 0) c = kAttnMaxCluster;
     }
-    return launch_pdl(k_attn<D, RT>, grid, dim3(kAttnThreads), attn_smem_bytes(D, RT), st, args);
+    (void)cudaGetLastError();
+    cmax.store(c);
+    return c;
+}
+
+// Slices of a call whose tiles attend to at most `range` positions.  When two
+// shared-memory blocks per slice let one cluster (of up to cmax CTAs) cover a
+// tile, that is the launch (*nst = 2, *cluster = the slices rounded up to a power
+// of two): no partial leaves the cluster.  Otherwise one block per slice, at most
+// kAttnMaxSlices, each CTA its own cluster (*nst = 1, *cluster = 1) and the
+// partials merged through the workspace: larger clusters measured slower there
+// (co-scheduling 16 CTAs per GPC left SMs idle).
+int attn_slices(long long range, int cmax, int *cluster, int *nst) {
+    const long long two = (range + 2 * kAttnSlice - 1) / (2 * kAttnSlice);
+    if (two <= cmax) {
+        int cs = 1;
+        while (cs < two) cs *= 2;
+        *cluster = cs;
+        *nst = kAttnStages;
+        return cs;
+    }
+    *cluster = 1;
+    *nst = 1;
+    return (int)std::min((range + kAttnSlice - 1) / kAttnSlice, (long long)kAttnMaxSlices);
+}
+
+template <int D, int RT>
+int launch_attn_rt(AttnArgs args, long long range, int tiles, int nkv, int max_partials, cudaStream_t st) {
+    const int cmax = attn_max_cluster<D, RT>();
+    if (cmax < 0) return -cmax;
+    int cs, nst;
+    args.S = attn_slices(range, cmax, &cs, &nst);
+    args.nst = nst;
+    // a chunk's call range can exceed one tile's: fewer, longer slices then
+    if (cs == 1) args.S = std::min(args.S, max_partials);
+    if (args.S / cs > max_partials) return MOE_EWORKSPACE;  // cannot happen with moe_attn_workspace_bytes
+    return launch_pdl(k_attn<D, RT>, dim3(args.S, tiles, nkv), dim3(kAttnThreads), attn_smem_bytes(D, RT, nst), st,
+                      args, cs);
 }
 
 template <int D>
-int launch_attn(const AttnArgs &args, int rt, int tiles, int nkv, cudaStream_t st) {
-    const dim3 grid(args.S, tiles, nkv);
+int launch_attn(const AttnArgs &args, long long range, int rt, int tiles, int nkv, int max_partials,
+                cudaStream_t st) {
     switch (rt) {
-        case 1: return launch_attn_rt<D, 1>(args, grid, st);
-        case 2: return launch_attn_rt<D, 2>(args, grid, st);
-        case 4: return launch_attn_rt<D, 4>(args, grid, st);
-        default: return launch_attn_rt<D, 8>(args, grid, st);
+        case 1: return launch_attn_rt<D, 1>(args, range, tiles, nkv, max_partials, st);
+        case 2: return launch_attn_rt<D, 2>(args, range, tiles, nkv, max_partials, st);
+        case 4: return launch_attn_rt<D, 4>(args, range, tiles, nkv, max_partials, st);
+        default: return launch_attn_rt<D, 8>(args, range, tiles, nkv, max_partials, st);
     }
 }
 
@@ -284,7 +350,7 @@ int moe_attn_step(const moe_attn_t *attn, const float *x, int T, int pos, int fl
     g.kc = reinterpret_cast<const __half *>(a->k_cache);
     g.vc = reinterpret_cast<const __half *>(a->v_cache);
     g.nq = a->nq; g.nkv = a->nkv; g.G = G; g.kv_len = a->kv_len; g.window = a->window; g.p0 = pos; g.T = T;
-    g.S = std::min(slices_max(a, T), slices_for(range));
+    g.S = 0;  // set with the cluster size at the launch
     g.part_o = w.part_o;
     g.part_ml = w.part_ml;
     g.ticket = w.ticket;
@@ -297,11 +363,12 @@ int moe_attn_step(const moe_attn_t *attn, const float *x, int T, int pos, int fl
     g.ao = w.ao;
     g.ao_user = attn_out;
     const int rt = rows_of(a, T);
+    const int mp = slices_max(a, T);
     switch (a->d) {
-        case 64: rc = launch_attn<64>(g, rt, tiles, a->nkv, st); break;
-        case 128: rc = launch_attn<128>(g, rt, tiles, a->nkv, st); break;
-        case 256: rc = launch_attn<256>(g, rt, tiles, a->nkv, st); break;
-        default: rc = launch_attn<512>(g, rt, tiles, a->nkv, st); break;
+        case 64: rc = launch_attn<64>(g, range, rt, tiles, a->nkv, mp, st); break;
+        case 128: rc = launch_attn<128>(g, range, rt, tiles, a->nkv, mp, st); break;
+        case 256: rc = launch_attn<256>(g, range, rt, tiles, a->nkv, mp, st); break;
+        default: rc = launch_attn<512>(g, range, rt, tiles, a->nkv, mp, st); break;
     }
     if (rc) return rc;
 
