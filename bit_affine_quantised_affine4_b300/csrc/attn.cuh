@@ -44,7 +44,7 @@ constexpr int kProjTokens = 8;     // token columns per projection CTA (the MMA'
 constexpr int kProjQKV = 0, kProjPlain = 1;
 // Warps of a projection CTA; they split the K groups.
 template <int MODE> struct ProjCfg;
-template <> struct ProjCfg<kProjQKV> { static constexpr int warps = 4; };
+template <> struct ProjCfg<kProjQKV> { static constexpr int warps = 8; };
 template <> struct ProjCfg<kProjPlain> { static constexpr int warps = 8; };
 template <int MODE> constexpr int proj_threads() { return 32 * ProjCfg<MODE>::warps; }
 
