@@ -300,6 +300,29 @@ def moe_layer_decode_host(layer: moe_layer_t, x, ws, y=None, flags: int = 0, idx
     return y
 
 
+class DecodeHostCall:
+    """moe_layer_decode_host for repeated one-token calls on the same layer,
+    workspace and stream: the arguments are marshalled once, and each call passes
+    only the host rows (tensors or plain addresses) -- the per-call Python work of
+    a decode loop that feeds the library from host memory."""
+
+    def __init__(self, layer: moe_layer_t, ws, flags: int = 0, stream=None):
+        self._layer = layer  # kept alive for the pointer below
+        self._lref = C.byref(layer)
+        self._ws, self._nbytes = C.c_void_p(ws.data_ptr()), C.c_size_t(ws.numel())
+        self._keep = ws
+        self._flags = int(flags)
+        self._stream = _stream(stream)
+        self._fn = lib.moe_layer_decode_host
+
+    def __call__(self, x, y):
+        xp = x if isinstance(x, int) else x.data_ptr()
+        yp = y if isinstance(y, int) else y.data_ptr()
+        rc = self._fn(self._lref, xp, 1, self._flags, yp, None, None, None, self._ws, self._nbytes, self._stream)
+        if rc != MOE_OK:
+            raise MoeError(rc, "moe_layer_decode_host")
+
+
 def moe_layer_decode_noalloc(layer: moe_layer_t, x, y=None, flags: int = 0, idx=None, gate=None,
                              stream=None):
     """moe_layer_decode with the library's own static scratch (no workspace argument)."""

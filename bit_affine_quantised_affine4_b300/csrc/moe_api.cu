@@ -355,7 +355,9 @@ int run_layer_chunk(const moe_layer_t *l, const float *x, int T, int flags, floa
     }
     if (!smem_set) {
         if (cudaFuncSetAttribute(k_prefill_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)prefill_gemm_smem()) != cudaSuccess)
+                                 (int)prefill_gemm_smem()) != cudaSuccess ||
+            cudaFuncSetAttribute(k_prefill_route, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)prefill_route_smem()) != cudaSuccess)
             return cuda_status();
         smem_set = 1;
     }
@@ -369,7 +371,22 @@ int run_layer_chunk(const moe_layer_t *l, const float *x, int T, int flags, floa
         if ((rc = cuda_status())) return rc;
         xin = ws.xn;
     }
-    if ((rc = launch_route(l, ly, xin, T, ws, ws.idx, ws.gate, nullptr, st))) return rc;
+    // the router: tiled over (K slice, 64 experts, 32 tokens) when the slices' partial
+    // sums fit in the down GEMM's fp32 output rows (unused until that GEMM runs)
+    const int KS = prefill_route_slices(l->H), nEB = (l->E + kRtExp - 1) / kRtExp;
+    const int nTB = (T + kRtTok - 1) / kRtTok;
+    if ((size_t)KS * l->E <= (size_t)l->topk * l->H) {
+        RouteTiledArgs ra;
+        ra.rq = ly.rq; ra.rs = ly.rs; ra.rb = ly.rb; ra.bias = ly.bias;
+        ra.x = xin; ra.T = T; ra.H = l->H; ra.E = l->E; ra.topk = l->topk;
+        ra.part = ws.Yr; ra.idx = ws.idx; ra.gate = ws.gate;
+        k_prefill_route<<<dim3(KS, nEB, nTB), kRtThreads, prefill_route_smem(), st>>>(ra);
+        if ((rc = cuda_status())) return rc;
+        k_prefill_topk<<<(T + kRtTopkWarps - 1) / kRtTopkWarps, kRtTopkWarps * 32, 0, st>>>(ra, KS);
+        if ((rc = cuda_status())) return rc;
+    } else if ((rc = launch_route(l, ly, xin, T, ws, ws.idx, ws.gate, nullptr, st))) {
+        return rc;
+    }
     const int P2 = T * l->topk;
     if (idx_out && cudaMemcpyAsync(idx_out, ws.idx, sizeof(int32_t) * P2, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
         return cuda_status();

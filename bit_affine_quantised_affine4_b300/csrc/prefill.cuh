@@ -5,6 +5,8 @@
 // "Prestazioni nel mondo reale"; remio.ai page, section "L'affermazione dei 2
 // GB..."); by definition its output equals that many independent decodes.
 //
+//   route    (grid)   router logits as a small fp32 GEMM split over K slices,
+//                     then one warp per token sums the slices and ranks them.
 //   plan     (1 CTA)  from the router's choices: distinct experts U in ascending
 //                     id, the tokens of each in ascending order, a row segment per
 //                     expert (its token count rounded up to 16), the row of every
@@ -19,14 +21,18 @@
 //   combine  (grid)   y_t = sum_k gate_tk * routed_(t,k) + shared_t (+ x_t), in a
 //                     fixed order.
 //
-// Inside a GEMM CTA: warp 8 prefetches the next item's weight block into L2 and
-// copies each K step's eight packed weight tiles and the token tile with bulk
-// copies (TMA) into a ring; warps 0-7 dequantise one weight tile each (w = s*q +
-// b, exact, rounded once to fp16) into the swizzled operand layout; one thread of
-// warp 9 issues the MMAs (fp16 x fp16 -> fp32 in tensor memory) and commits them
-// to the stage's barrier; warps 0-7 then read the accumulator out of tensor
-// memory for the epilogue (warps w and w+4 share a lane quarter and split the
-// columns; two accumulators alternate so the next item's MMAs overlap it).  Columns of both operands are stored in the
+// Inside a GEMM CTA: one thread of the producer warp prefetches the next item's
+// weight block into L2 and fills two rings with bulk copies (TMA): a packed-weight
+// ring, one copy per tile row covering kPfKF K steps (a copy costs about the same
+// whatever its size, so fewer, larger copies), and an operand ring, one stage per K
+// step, into which it copies the token tile.  The eight dequantising warps turn one
+// weight tile each (w = s*q + b, exact, rounded once to fp16) into the swizzled A
+// operand of the same operand stage; the stage's barrier completes with the token
+// bytes and one arrival per dequantising thread.  One thread of the MMA warp issues
+// the MMAs (fp16 x fp16 -> fp32 in tensor memory) and commits them to the stage's
+// release barrier.  Eight epilogue warps read the accumulator out of tensor memory
+// (two per lane quarter, splitting the columns) while the next item's K steps run
+// into the other of two accumulators.  Columns of both operands are stored in the
 // same permuted order within each run of 8 (see mma_core.cuh): a K permutation
 // applied to both operands leaves the product unchanged, and it lets one 32-bit
 // mask extract two codes into an fp16 pair.
@@ -34,22 +40,31 @@
 
 #include "common.cuh"
 #include "mma_core.cuh"
+#include "route.cuh"
 #include "sync.cuh"
 #include "tile.cuh"
 #include "umma.cuh"
 
 namespace moe {
 
-constexpr int kPfStages = 4;
-constexpr int kPfDq = 8;             // dequant + epilogue warps (one weight tile each per K step)
-constexpr int kPfProducer = kPfDq, kPfMmaWarp = kPfDq + 1;
-constexpr int kPfThreads = (kPfDq + 2) * 32;
-constexpr int kPfRawA = 5120;        // eight 576-byte tiles, padded to 1024
-constexpr int kPfMaxN = 128;         // token rows of one item (an expert with more tokens would be
-                                     // cut into slices of kPfMaxN rows; kPfMaxN-row slices with 8 stages
-                                     // measured slower: 358 vs 305 us per chunk)
-constexpr int kPfRaw = kPfRawA + kPfMaxN * 128;
+constexpr int kPfKF = 4;             // K steps (groups) per packed-weight copy: one bulk copy per
+                                     // tile row moves kPfKF tiles (a copy costs the same whatever its size)
+constexpr int kPfWStages = 3;        // packed-weight ring: kPfKF K steps per stage
+constexpr int kPfQStages = 3;        // operand ring: dequantised A and the token tile of one K step
+constexpr int kPfDq = 8;             // dequantising warps of a group (one weight tile each per K step)
+constexpr int kPfDqGroups = 1;       // groups of dequantising warps, taking alternate K steps (two
+                                     // groups measured slower: 312 vs 302 us per chunk)
+constexpr int kPfProducer = kPfDqGroups * kPfDq, kPfMmaWarp = kPfProducer + 1;
+constexpr int kPfEpi0 = kPfProducer + 2;  // first epilogue warp
+constexpr int kPfEpi = 8;            // epilogue warps: each lane quarter of tensor memory twice
+constexpr int kPfThreads = (kPfEpi0 + kPfEpi) * 32;
+constexpr int kPfWRow = kPfKF * kTileBytes;  // one tile row's kPfKF tiles in a weight stage
+constexpr int kPfW = 8 * kPfWRow;            // a weight stage (18432 bytes, a multiple of 1024)
+constexpr int kPfMaxN = 128;         // token rows of one item: an expert with more tokens would be cut
+                                     // into slices of kPfMaxN rows, each its own item (64-row slices with
+                                     // five operand stages measured slower: 318 vs 303 us per chunk)
 constexpr int kPfTileA = 128 * 128;  // dequantised A: 128 rows x 64 fp16
+constexpr int kPfQ = kPfTileA + kPfMaxN * 128;  // an operand stage: A, then the token tile
 constexpr int kPfTmemCols = 256;     // two fp32 accumulators of up to 128 columns
 
 // Plan written by k_prefill_plan (ints in the workspace).
@@ -65,6 +80,139 @@ struct PfPlan {
 };
 
 __device__ __forceinline__ int round16(int n) { return (n + 15) & ~15; }
+
+// ------------------------------------------------------------------ router (tiled)
+// The chunk's router as a small fp32 GEMM on the CUDA cores.  Each dequantised
+// router weight w = s*q + b (rounded once to fp32, as in the decode router) is
+// formed once per CTA and reused by 32 tokens, instead of once per (token, row).
+// CTA (ks, eb, tb): tokens 32 tb .. +31, experts 64 eb .. +63, columns of K slice
+// ks (kRtSliceCols wide); thread (warp w, lane l) accumulates tokens tg + 8 i and
+// experts 16 w + eg + 4 j (tg = l % 8, eg = l / 8, i, j < 4) over the slice in
+// ascending column order.  Partial sums go to part[ks][t][e]; k_prefill_topk then
+// adds them per token in slice order.
+constexpr int kRtSliceCols = 128;               // K columns per slice (two groups)
+constexpr int kRtTok = 32, kRtExp = 64;         // CTA tile
+constexpr int kRtThreads = 128;
+constexpr int kRtPitch = kRtSliceCols + 4;      // padded smem row (floats): conflict-free float4 reads
+
+inline size_t prefill_route_smem() { return sizeof(float) * (size_t)(kRtTok + kRtExp) * kRtPitch; }
+inline int prefill_route_slices(int H) { return (H + kRtSliceCols - 1) / kRtSliceCols; }
+
+struct RouteTiledArgs {
+    const uint32_t *rq;           // [E][H/4] 8-bit codes
+    const __half *rs, *rb;        // [E][H/64]
+    const float *bias;            // [E] or null
+    const float *x;               // [T][H]
+    int T, H, E, topk;
+    float *part;                  // [KS][T][E] partial logits
+    int32_t *idx;                 // [T][topk]
+    float *gate;                  // [T][topk]
+};
+
+__global__ void __launch_bounds__(kRtThreads, 4) k_prefill_route(const RouteTiledArgs a) {
+    extern __shared__ __align__(16) float rt_sm[];
+    float *xs = rt_sm;                        // [kRtTok][kRtPitch]
+    float *wsm = rt_sm + kRtTok * kRtPitch;   // [kRtExp][kRtPitch]
+    const int ks = blockIdx.x, eb = blockIdx.y, tb = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int t0 = tb * kRtTok, e0 = eb * kRtExp, k0 = ks * kRtSliceCols;
+    const int kw = min(kRtSliceCols, a.H - k0);  // 64 or 128
+    const int G = a.H / kGroup, c4 = kw / 4;     // float4 columns of the slice
+    // x rows of the tile (zeros past T)
+    for (int v = tid; v < kRtTok * c4; v += kRtThreads) {
+        const int r = v / c4, c = v - r * c4, t = t0 + r;
+        float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (t < a.T) val = __ldg(reinterpret_cast<const float4 *>(a.x + (size_t)t * a.H + k0) + c);
+        *reinterpret_cast<float4 *>(xs + r * kRtPitch + 4 * c) = val;
+    }
+    // router rows of the tile, dequantised: 16 codes (one uint4) per step (zeros past E)
+    const int c16 = kw / 16;
+    for (int v = tid; v < kRtExp * c16; v += kRtThreads) {
+        const int r = v / c16, c = v - r * c16, e = e0 + r;
+        float *dst = wsm + r * kRtPitch + 16 * c;
+        if (e < a.E) {
+            const uint4 q = __ldg(reinterpret_cast<const uint4 *>(a.rq + (size_t)e * (a.H / 4) + k0 / 4) + c);
+            const int g = (k0 + 16 * c) / kGroup;
+            const float s = __half2float(a.rs[(size_t)e * G + g]), b = __half2float(a.rb[(size_t)e * G + g]);
+            const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int u = 0; u < 4; u++)
+                *reinterpret_cast<float4 *>(dst + 4 * u) =
+                    make_float4(fmaf(s, (float)(wd[u] & 0xFFu), b), fmaf(s, (float)((wd[u] >> 8) & 0xFFu), b),
+                                fmaf(s, (float)((wd[u] >> 16) & 0xFFu), b), fmaf(s, (float)(wd[u] >> 24), b));
+        } else {
+#pragma unroll
+            for (int u = 0; u < 4; u++) *reinterpret_cast<float4 *>(dst + 4 * u) = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+    __syncthreads();
+    const int tg = lane & 7, eg = lane >> 3;
+    float acc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; i++)
+#pragma unroll
+        for (int j = 0; j < 4; j++) acc[i][j] = 0.f;
+    const float *xr = xs + tg * kRtPitch;
+    const float *wr = wsm + (16 * warp + eg) * kRtPitch;
+#pragma unroll 2
+    for (int k = 0; k < kw; k += 4) {
+        float4 xv[4], wv[4];
+#pragma unroll
+        for (int i = 0; i < 4; i++) xv[i] = *reinterpret_cast<const float4 *>(xr + 8 * i * kRtPitch + k);
+#pragma unroll
+        for (int j = 0; j < 4; j++) wv[j] = *reinterpret_cast<const float4 *>(wr + 4 * j * kRtPitch + k);
+#pragma unroll
+        for (int i = 0; i < 4; i++)
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+                float s = acc[i][j];
+                s = fmaf(wv[j].x, xv[i].x, s);
+                s = fmaf(wv[j].y, xv[i].y, s);
+                s = fmaf(wv[j].z, xv[i].z, s);
+                s = fmaf(wv[j].w, xv[i].w, s);
+                acc[i][j] = s;
+            }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        const int t = t0 + tg + 8 * i;
+        if (t >= a.T) continue;
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            const int e = e0 + 16 * warp + eg + 4 * j;
+            if (e < a.E) a.part[((size_t)ks * a.T + t) * a.E + e] = acc[i][j];
+        }
+    }
+}
+
+// One warp per token: the token's logits as the sum of the slices' partials in
+// slice order plus the bias, then the router's top-k and softmax.
+constexpr int kRtTopkWarps = 8;
+__global__ void __launch_bounds__(kRtTopkWarps * 32) k_prefill_topk(const RouteTiledArgs a, int KS) {
+    __shared__ float lg[kRtTopkWarps][MOE_MAX_EXPERTS];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = blockIdx.x * kRtTopkWarps + warp;
+    if (t >= a.T) return;
+    constexpr int NV = MOE_MAX_EXPERTS / 32;
+    float acc[NV];
+#pragma unroll
+    for (int i = 0; i < NV; i++) acc[i] = 0.f;
+    for (int q = 0; q < KS; q++) {
+        const float *pr = a.part + ((size_t)q * a.T + t) * a.E;
+#pragma unroll
+        for (int i = 0; i < NV; i++) {
+            const int e = lane + 32 * i;
+            if (e < a.E) acc[i] += __ldcg(pr + e);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < NV; i++) {
+        const int e = lane + 32 * i;
+        if (e < a.E) lg[warp][e] = acc[i] + (a.bias ? a.bias[e] : 0.f);
+    }
+    __syncwarp();
+    warp_topk_softmax<true>(lg[warp], a.E, a.topk, a.idx + t * a.topk, a.gate + t * a.topk, nullptr, nullptr);
+}
 
 // ------------------------------------------------------------------ plan
 __global__ void __launch_bounds__(256) k_prefill_plan(const int *__restrict__ idx, int T, int E, int topk,
@@ -308,7 +456,8 @@ __device__ __forceinline__ uint4 deq_word(uint32_t w, __half2 s2, __half2 b2) {
 }
 
 struct PfSmem {
-    uint64_t raw_full[kPfStages], stage_free[kPfStages], a_full[kPfStages];
+    uint64_t w_full[kPfWStages], w_free[kPfWStages];                 // packed-weight ring
+    uint64_t q_full[kPfQStages], q_free[kPfQStages];  // operand ring
     uint64_t acc_full[2], acc_empty[2];
     uint32_t tmem;
     int err;
@@ -339,23 +488,28 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill_gemm(const PrefillGem
     a.urow = pl_urow;
     a.uexp = pl_uexp;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // 1024-aligned carve-up: raw stages | dequantised A stages | epilogue buffers
+    // 1024-aligned carve-up: weight stages | operand stages | epilogue buffers
     uint8_t *base = psm_raw + ((1024u - (smem_addr(psm_raw) & 1023u)) & 1023u);
-    uint8_t *raw = base;
-    uint8_t *sA = raw + (size_t)kPfStages * kPfRaw;
-    float *ebuf = reinterpret_cast<float *>(sA + (size_t)kPfStages * kPfTileA);  // [128 cols][64 rows]
+    uint8_t *wst = base;
+    uint8_t *qst = wst + (size_t)kPfWStages * kPfW;
+    float *ebuf = reinterpret_cast<float *>(qst + (size_t)kPfQStages * kPfQ);  // [128 cols][64 rows]
     uint8_t *hst = reinterpret_cast<uint8_t *>(ebuf + 64 * kPfMaxN);          // [128 rows][128 B]
     volatile int *err = &S.err;
 
     if (tid == 0) {
-        for (int s = 0; s < kPfStages; s++) {
-            mbar_init(&S.raw_full[s], 1);
-            mbar_init(&S.stage_free[s], 1);
-            mbar_init(&S.a_full[s], kPfDq);
+        for (int s = 0; s < kPfWStages; s++) {
+            mbar_init(&S.w_full[s], 1);
+            mbar_init(&S.w_free[s], kPfDqGroups * kPfDq);
+        }
+        for (int s = 0; s < kPfQStages; s++) {
+            // full: the producer's arrival with the token tile's bytes, then one arrival per
+            // thread of the dequantising group that writes the stage's A
+            mbar_init(&S.q_full[s], 1 + kPfDq * 32);
+            mbar_init(&S.q_free[s], 1);
         }
         for (int j = 0; j < 2; j++) {
             mbar_init(&S.acc_full[j], 1);
-            mbar_init(&S.acc_empty[j], kPfDq);
+            mbar_init(&S.acc_empty[j], kPfEpi);
         }
         S.err = 0;
         mbar_fence_init();
@@ -374,11 +528,13 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill_gemm(const PrefillGem
     };
 
     if (warp == kPfProducer) {
-        // ---------------- copies
+        // ---------------- copies (one thread): per kPfKF K steps of an item, one bulk copy
+        // per tile row into the weight ring; per K step, the token tile into the operand ring
         if (lane == 0) {
-            int f = 0;
-            int last[kPfStages];
-            for (int s = 0; s < kPfStages; s++) last[s] = -1;
+            int f = 0, wf = 0;
+            int wlast[kPfWStages], qlast[kPfQStages];
+            for (int s = 0; s < kPfWStages; s++) wlast[s] = -1;
+            for (int s = 0; s < kPfQStages; s++) qlast[s] = -1;
             for (int i = b; i < NI; i += nC) {
                 const PfItem it = pf_item(a, i);
                 // this item's weight block (first item only) and the next one's, into L2
@@ -388,24 +544,36 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill_gemm(const PrefillGem
                     prefetch_l2(nx.a, (unsigned)(8 * nx.a_row));
                 }
                 for (int kb = 0; kb < it.nkb; kb++, f++) {
-                    const int s = f % kPfStages;
-                    if (f >= kPfStages && !*err &&
-                        !mbar_wait(&S.stage_free[s], ((f / kPfStages) - 1) & 1, err))
+                    if (kb % kPfKF == 0) {
+                        const int w = wf % kPfWStages, nk = min(kPfKF, it.nkb - kb);
+                        if (wf >= kPfWStages && !*err &&
+                            !mbar_wait(&S.w_free[w], ((wf / kPfWStages) - 1) & 1, err))
+                            fail();
+                        if (!*err) {
+                            mbar_arrive_expect_tx(&S.w_full[w], 8 * nk * kTileBytes);
+                            uint8_t *dst = wst + (size_t)w * kPfW;
+                            for (int j = 0; j < 8; j++)
+                                bulk_g2s(dst + j * kPfWRow, it.a + j * it.a_row + (size_t)kb * kTileBytes,
+                                         nk * kTileBytes, &S.w_full[w]);
+                            wlast[w] = wf;
+                        }
+                        wf++;
+                    }
+                    const int q = f % kPfQStages;
+                    if (f >= kPfQStages && !*err && !mbar_wait(&S.q_free[q], ((f / kPfQStages) - 1) & 1, err))
                         fail();
                     if (*err) continue;
-                    uint8_t *dst = raw + (size_t)s * kPfRaw;
-                    mbar_arrive_expect_tx(&S.raw_full[s], 8 * kTileBytes + it.N * 128);
-                    for (int j = 0; j < 8; j++)
-                        bulk_g2s(dst + j * kTileBytes, it.a + j * it.a_row + (size_t)kb * kTileBytes, kTileBytes,
-                                 &S.raw_full[s]);
-                    bulk_g2s(dst + kPfRawA, it.b + (size_t)kb * it.b_kb, it.N * 128, &S.raw_full[s]);
-                    last[s] = f;
+                    mbar_arrive_expect_tx(&S.q_full[q], it.N * 128);
+                    bulk_g2s(qst + (size_t)q * kPfQ + kPfTileA, it.b + (size_t)kb * it.b_kb, it.N * 128, &S.q_full[q]);
+                    qlast[q] = f;
                 }
             }
             // drain: the last copies of every stage have landed
             volatile int never = 0;
-            for (int s = 0; s < kPfStages; s++)
-                if (last[s] >= 0) mbar_wait(&S.raw_full[s], (last[s] / kPfStages) & 1, &never);
+            for (int s = 0; s < kPfWStages; s++)
+                if (wlast[s] >= 0) mbar_wait(&S.w_full[s], (wlast[s] / kPfWStages) & 1, &never);
+            for (int s = 0; s < kPfQStages; s++)
+                if (qlast[s] >= 0) mbar_wait(&S.q_full[s], (qlast[s] / kPfQStages) & 1, &never);
         }
         __syncwarp();
     } else if (warp == kPfMmaWarp) {
@@ -419,63 +587,81 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill_gemm(const PrefillGem
                 tc_fence_after();
                 const uint32_t idesc = umma_idesc_f16(128, it.N);
                 for (int kb = 0; kb < it.nkb; kb++, f++) {
-                    const int s = f % kPfStages;
-                    if (!*err && !mbar_wait(&S.a_full[s], (f / kPfStages) & 1, err)) fail();
+                    const int q = f % kPfQStages;
+                    if (!mbar_wait(&S.q_full[q], (f / kPfQStages) & 1, err)) fail();
                     tc_fence_after();
-                    if (!*err) {
-                        const uint32_t sa = smem_addr(sA + (size_t)s * kPfTileA);
-                        const uint32_t sb = smem_addr(raw + (size_t)s * kPfRaw + kPfRawA);
+                    {
+                        const uint32_t sa = smem_addr(qst + (size_t)q * kPfQ);
+                        const uint32_t sb = sa + kPfTileA;
 #pragma unroll
                         for (int ks = 0; ks < 4; ks++)
                             umma_f16(tmem + ab * 128, umma_desc(sa + 32 * ks), umma_desc(sb + 32 * ks), idesc,
                                      kb > 0 || ks > 0);
                     }
-                    umma_commit(&S.stage_free[s]);
+                    umma_commit(&S.q_free[q]);
                 }
                 umma_commit(&S.acc_full[ab]);
             }
             // every MMA issued here has finished before tensor memory is released
             if (f > 0) {
                 volatile int never = 0;
-                const int s = (f - 1) % kPfStages;
-                mbar_wait(&S.stage_free[s], ((f - 1) / kPfStages) & 1, &never);
+                const int q = (f - 1) % kPfQStages;
+                mbar_wait(&S.q_free[q], ((f - 1) / kPfQStages) & 1, &never);
             }
         }
         __syncwarp();
-    } else {
-        // ---------------- dequantise + epilogue (warps 0-7)
+    } else if (warp < kPfProducer) {
+        // ---------------- dequantise: group g = warp / 8 takes the K steps f with f % kPfDqGroups == g,
+        // warp j = warp % 8 the tile row j of each; every warp of both groups releases each
+        // weight stage (after waiting for its copy, so that no release runs a phase ahead)
+        const int g = warp / kPfDq, j = warp % kPfDq;
         const int r = lane >> 2, c = lane & 3;
-        const int quad = warp & 3, half = warp >> 2;  // tensor-memory lane quarter, column half
-        int f = 0, n_it = 0;
-        for (int i = b; i < NI; i += nC, n_it++) {
-            const PfItem it = pf_item(a, i);
-            for (int kb = 0; kb < it.nkb; kb++, f++) {
-                const int s = f % kPfStages;
-                if (!*err && !mbar_wait(&S.raw_full[s], (f / kPfStages) & 1, err)) fail();
-                if (!*err) {
-                    const uint8_t *rs = raw + (size_t)s * kPfRaw;
-                    uint8_t *as = sA + (size_t)s * kPfTileA;
+        const int ra = a.kind == 0 ? 8 * j + r : 16 * j + r;
+        const int rb = a.kind == 0 ? 64 + 8 * j + r : 16 * j + 8 + r;
+        const uint32_t oa0 = sw128_chunk(ra, 2 * c), oa1 = sw128_chunk(ra, 2 * c + 1);
+        const uint32_t ob0 = sw128_chunk(rb, 2 * c), ob1 = sw128_chunk(rb, 2 * c + 1);
+        int f = 0, wf = 0;
+        for (int i = b; i < NI; i += nC) {
+            const int nkb = pf_item(a, i).nkb;
+            for (int kb = 0; kb < nkb; kb++, f++) {
+                const int w = wf % kPfWStages, q = f % kPfQStages;
+                // (the waits give up at once when another warp raised the error word)
+                if (kb % kPfKF == 0 && !mbar_wait(&S.w_full[w], (wf / kPfWStages) & 1, err)) fail();
+                if (f % kPfDqGroups == g) {
+                    // the packed tile is loaded before the wait for the operand stage
+                    const uint8_t *rs = wst + (size_t)w * kPfW + j * kPfWRow + (kb % kPfKF) * kTileBytes;
+                    const uint4 qv = *reinterpret_cast<const uint4 *>(rs + 16 * lane);
+                    const uint2 e = *reinterpret_cast<const uint2 *>(rs + 512 + 8 * r);
+                    if (f >= kPfQStages && !mbar_wait(&S.q_free[q], ((f / kPfQStages) - 1) & 1, err)) fail();
                     {
-                        const int j = warp;
-                        const uint4 q = *reinterpret_cast<const uint4 *>(rs + j * kTileBytes + 16 * lane);
-                        const uint2 e = *reinterpret_cast<const uint2 *>(rs + j * kTileBytes + 512 + 8 * r);
+                        uint8_t *as = qst + (size_t)q * kPfQ;
                         const __half2 sa2 = __half2half2(__ushort_as_half((unsigned short)(e.x & 0xFFFFu)));
                         const __half2 ba2 = __half2half2(__ushort_as_half((unsigned short)(e.x >> 16)));
                         const __half2 sb2 = __half2half2(__ushort_as_half((unsigned short)(e.y & 0xFFFFu)));
                         const __half2 bb2 = __half2half2(__ushort_as_half((unsigned short)(e.y >> 16)));
-                        const int ra = a.kind == 0 ? 8 * j + r : 16 * j + r;
-                        const int rb = a.kind == 0 ? 64 + 8 * j + r : 16 * j + 8 + r;
-                        *reinterpret_cast<uint4 *>(as + sw128_chunk(ra, 2 * c)) = deq_word(q.x, sa2, ba2);
-                        *reinterpret_cast<uint4 *>(as + sw128_chunk(ra, 2 * c + 1)) = deq_word(q.y, sa2, ba2);
-                        *reinterpret_cast<uint4 *>(as + sw128_chunk(rb, 2 * c)) = deq_word(q.z, sb2, bb2);
-                        *reinterpret_cast<uint4 *>(as + sw128_chunk(rb, 2 * c + 1)) = deq_word(q.w, sb2, bb2);
+                        *reinterpret_cast<uint4 *>(as + oa0) = deq_word(qv.x, sa2, ba2);
+                        *reinterpret_cast<uint4 *>(as + oa1) = deq_word(qv.y, sa2, ba2);
+                        *reinterpret_cast<uint4 *>(as + ob0) = deq_word(qv.z, sb2, bb2);
+                        *reinterpret_cast<uint4 *>(as + ob1) = deq_word(qv.w, sb2, bb2);
+                        fence_async_smem();
                     }
-                    fence_async_smem();
+                    mbar_arrive(&S.q_full[q]);  // each thread, after its own stores and fence
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&S.a_full[s]);
+                if (kb % kPfKF == kPfKF - 1 || kb == nkb - 1) {
+                    // the weight stage is consumed after its last K step
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&S.w_free[w]);
+                    wf++;
+                }
             }
-            // epilogue of item i
+        }
+    } else {
+        // ---------------- epilogue (warps 18-25), overlapping the next item's K steps
+        const int etid = tid - kPfEpi0 * 32;
+        const int quad = warp & 3, half = (warp - kPfEpi0) >> 2;  // tensor-memory lane quarter, column half
+        int n_it = 0;
+        for (int i = b; i < NI; i += nC, n_it++) {
+            const PfItem it = pf_item(a, i);
             const int ab = n_it & 1;
             if (!*err && !mbar_wait(&S.acc_full[ab], (n_it >> 1) & 1, err)) fail();
             tc_fence_after();
@@ -491,7 +677,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill_gemm(const PrefillGem
 #pragma unroll
                         for (int q = 0; q < 16; q++) ebuf[(c0 + q) * 64 + row - 64] = v[q];
                     }
-                named_sync(1, kPfDq * 32);
+                named_sync(1, kPfEpi * 32);
                 if (quad < 2 && !*err) {
                     const int pos = frag_pos(row);  // operand position of column `row` of the K step
                     for (int c0 = c_first; c0 < it.N; c0 += 32) {
@@ -506,12 +692,12 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill_gemm(const PrefillGem
                         }
                     }
                 }
-                named_sync(1, kPfDq * 32);
+                named_sync(1, kPfEpi * 32);
                 // the item's h rows: one K step (kb = mb) of the down operand
                 uint8_t *dst = (it.u < 0 ? a.Hs + ((size_t)it.mb * a.T16 + it.row0) * 128
                                          : a.Hr + ((size_t)it.mb * a.Rmax + a.urow[it.u] + it.row0) * 128);
                 if (!*err)
-                    for (int v = tid; v < it.N * 8; v += kPfDq * 32)
+                    for (int v = etid; v < it.N * 8; v += kPfEpi * 32)
                         reinterpret_cast<uint4 *>(dst)[v] = reinterpret_cast<const uint4 *>(hst)[v];
             } else if (!*err) {
                 // output row 128 mb + row, token column j
@@ -532,7 +718,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill_gemm(const PrefillGem
                 }
             }
             tc_fence_before();
-            named_sync(1, kPfDq * 32);
+            named_sync(1, kPfEpi * 32);
             if (lane == 0) mbar_arrive(&S.acc_empty[ab]);
         }
     }
@@ -545,7 +731,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill_gemm(const PrefillGem
 }
 
 inline size_t prefill_gemm_smem() {
-    return 1024 + (size_t)kPfStages * kPfRaw + (size_t)kPfStages * kPfTileA + 64 * kPfMaxN * 4 + kPfMaxN * 128;
+    return 1024 + (size_t)kPfWStages * kPfW + (size_t)kPfQStages * kPfQ + 64 * kPfMaxN * 4 + kPfMaxN * 128;
 }
 
 // ------------------------------------------------------------------ combine

@@ -220,6 +220,13 @@ def test_decode_host_buffers(moe, tiny, T, pinned):
     assert ok, "worst err/bound %.3f" % worst
     with pytest.raises(ValueError):
         moe.moe_layer_decode_host(layer, _cuda(x), ws)
+    if T == 1:  # the reusable call object: the same call, arguments marshalled once
+        call = moe.DecodeHostCall(layer, ws, flags=moe.MOE_RESIDUAL)
+        y2 = pin(torch.full_like(xh, float("nan")))
+        call(xh, y2)
+        assert np.array_equal(y2.numpy(), yh.numpy())
+        call(xh.data_ptr(), y2.data_ptr())  # plain addresses
+        assert np.array_equal(y2.numpy(), yh.numpy())
 
 
 @pytest.mark.parametrize("T", [1, 37, 128])
