@@ -49,12 +49,10 @@ namespace moe {
 
 constexpr int kPfKF = 4;             // K steps (groups) per packed-weight copy: one bulk copy per
                                      // tile row moves kPfKF tiles (a copy costs the same whatever its size)
-constexpr int kPfWStages = 3;        // packed-weight ring: kPfKF K steps per stage
-constexpr int kPfQStages = 3;        // operand ring: dequantised A and the token tile of one K step
-constexpr int kPfDq = 8;             // dequantising warps of a group (one weight tile each per K step)
-constexpr int kPfDqGroups = 1;       // groups of dequantising warps, taking alternate K steps (two
-                                     // groups measured slower: 312 vs 302 us per chunk)
-constexpr int kPfProducer = kPfDqGroups * kPfDq, kPfMmaWarp = kPfProducer + 1;
+constexpr int kPfWStages = 2;        // packed-weight ring: kPfKF K steps per stage
+constexpr int kPfQStages = 4;        // operand ring: dequantised A and the token tile of one K step
+constexpr int kPfDq = 8;             // dequantising warps (one weight tile row each per K step)
+constexpr int kPfProducer = kPfDq, kPfMmaWarp = kPfProducer + 1;
 constexpr int kPfEpi0 = kPfProducer + 2;  // first epilogue warp
 constexpr int kPfEpi = 8;            // epilogue warps: each lane quarter of tensor memory twice
 constexpr int kPfThreads = (kPfEpi0 + kPfEpi) * 32;
@@ -455,6 +453,20 @@ __device__ __forceinline__ uint4 deq_word(uint32_t w, __half2 s2, __half2 b2) {
     return make_uint4(r[0], r[1], r[2], r[3]);
 }
 
+// True when the phase of `bar` with the given parity has completed (a non-blocking
+// test, tried before the bounded waiting loop on the pipeline's hot paths).
+__device__ __forceinline__ bool pf_done(uint64_t *bar, unsigned parity) {
+    unsigned ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 struct PfSmem {
     uint64_t w_full[kPfWStages], w_free[kPfWStages];                 // packed-weight ring
     uint64_t q_full[kPfQStages], q_free[kPfQStages];  // operand ring
@@ -499,7 +511,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill_gemm(const PrefillGem
     if (tid == 0) {
         for (int s = 0; s < kPfWStages; s++) {
             mbar_init(&S.w_full[s], 1);
-            mbar_init(&S.w_free[s], kPfDqGroups * kPfDq);
+            mbar_init(&S.w_free[s], kPfDq);
         }
         for (int s = 0; s < kPfQStages; s++) {
             // full: the producer's arrival with the token tile's bytes, then one arrival per
@@ -588,7 +600,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill_gemm(const PrefillGem
                 const uint32_t idesc = umma_idesc_f16(128, it.N);
                 for (int kb = 0; kb < it.nkb; kb++, f++) {
                     const int q = f % kPfQStages;
-                    if (!mbar_wait(&S.q_full[q], (f / kPfQStages) & 1, err)) fail();
+                    if (!pf_done(&S.q_full[q], (f / kPfQStages) & 1) && !mbar_wait(&S.q_full[q], (f / kPfQStages) & 1, err))
+                        fail();
                     tc_fence_after();
                     {
                         const uint32_t sa = smem_addr(qst + (size_t)q * kPfQ);
@@ -611,10 +624,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill_gemm(const PrefillGem
         }
         __syncwarp();
     } else if (warp < kPfProducer) {
-        // ---------------- dequantise: group g = warp / 8 takes the K steps f with f % kPfDqGroups == g,
-        // warp j = warp % 8 the tile row j of each; every warp of both groups releases each
-        // weight stage (after waiting for its copy, so that no release runs a phase ahead)
-        const int g = warp / kPfDq, j = warp % kPfDq;
+        // ---------------- dequantise: warp j takes tile row j of every K step
+        const int j = warp;
         const int r = lane >> 2, c = lane & 3;
         const int ra = a.kind == 0 ? 8 * j + r : 16 * j + r;
         const int rb = a.kind == 0 ? 64 + 8 * j + r : 16 * j + 8 + r;
@@ -627,12 +638,14 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill_gemm(const PrefillGem
                 const int w = wf % kPfWStages, q = f % kPfQStages;
                 // (the waits give up at once when another warp raised the error word)
                 if (kb % kPfKF == 0 && !mbar_wait(&S.w_full[w], (wf / kPfWStages) & 1, err)) fail();
-                if (f % kPfDqGroups == g) {
+                {
                     // the packed tile is loaded before the wait for the operand stage
                     const uint8_t *rs = wst + (size_t)w * kPfW + j * kPfWRow + (kb % kPfKF) * kTileBytes;
                     const uint4 qv = *reinterpret_cast<const uint4 *>(rs + 16 * lane);
                     const uint2 e = *reinterpret_cast<const uint2 *>(rs + 512 + 8 * r);
-                    if (f >= kPfQStages && !mbar_wait(&S.q_free[q], ((f / kPfQStages) - 1) & 1, err)) fail();
+                    if (f >= kPfQStages && !pf_done(&S.q_free[q], ((f / kPfQStages) - 1) & 1) &&
+                        !mbar_wait(&S.q_free[q], ((f / kPfQStages) - 1) & 1, err))
+                        fail();
                     {
                         uint8_t *as = qst + (size_t)q * kPfQ;
                         const __half2 sa2 = __half2half2(__ushort_as_half((unsigned short)(e.x & 0xFFFFu)));
@@ -656,7 +669,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill_gemm(const PrefillGem
             }
         }
     } else {
-        // ---------------- epilogue (warps 18-25), overlapping the next item's K steps
+        // ---------------- epilogue (warps 10-17), overlapping the next item's K steps
         const int etid = tid - kPfEpi0 * 32;
         const int quad = warp & 3, half = (warp - kPfEpi0) >> 2;  // tensor-memory lane quarter, column half
         int n_it = 0;
