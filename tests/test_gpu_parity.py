@@ -256,6 +256,23 @@ def test_many_experts_topk1(moe):
     _layer_check(moe, s, gl, ol, 16, 700)
 
 
+def test_prefill_router_fallback(moe):
+    # 256 experts with top-1: the chunk router's slice partials would not fit the
+    # down GEMM's scratch (E * ceil(H/128) > topk * H), so the chunk takes the
+    # decode path's router; three 16-token groups of it
+    s = synth.Shape("wide", 256, 256, 1, 64, 64)
+    gl, ol = gpu_layer(s, seed=4), OracleLayer(s, seed=4)
+    _layer_check(moe, s, gl, ol, 40, 702, prefill=True)
+
+
+def test_prefill_ragged_router_tiles(moe):
+    # the chunk router's tiles with ragged edges: 100 experts (a partial second
+    # 64-row block), 77 tokens (a partial third 32-token block), three K slices
+    s = synth.Shape("ragged", 384, 100, 6, 128, 192)
+    gl, ol = gpu_layer(s, seed=6), OracleLayer(s, seed=6)
+    _layer_check(moe, s, gl, ol, 77, 703, prefill=True)
+
+
 def test_rejects_bad_calls(moe, tiny):
     s, gl, ol = tiny
     layer = gl.view()
