@@ -42,7 +42,7 @@ DECODE_BYTES = TOPK * EXPERT_BYTES + SHARED_BYTES + ROUTER_BYTES  # 37,182,464 B
 # `bench.py --quick` (dram__bytes_read.sum + dram__bytes_write.sum); reported only
 # while the decode kernel's sources are the ones it was taken on (their SHA-1
 # without comments)
-DECODE_NCU_TRAFFIC = {"sha1": "81ce90df28eca5268f3e0ec6c857d8f3377ee8c6", "bytes": 37_315_328}
+DECODE_NCU_TRAFFIC = {"sha1": "7ce637ff67689019675d75f66a302230625c2f94", "bytes": 37_318_144}
 DECODE_SOURCES = ["bit_affine_quantised_affine4_b300/csrc/" + f for f in
                   ("decode.cuh", "common.cuh", "mma_core.cuh", "route.cuh", "sync.cuh", "tile.cuh",
                    "moe_api.cu")] + ["include/moe.h"]
@@ -301,32 +301,40 @@ def run_ours(args):
     value = job_rate(world, args.steps, dt)  # tokens/s over all ranks (one token per step per rank)
     achieved_gbs = DECODE_BYTES / per_step / 1e9
 
-    # ---- end to end through the public API with host buffers: one
-    # moe_layer_decode_host call per step copies the token in (pinned host
-    # memory), runs the decode, copies y back and returns once it is there
+    # ---- end to end through the public API with host buffers: one call per step
+    # copies the token in (pinned host memory), runs the decode, copies y back and
+    # returns once it is there -- through the prepared host call (moe_host_call,
+    # a recorded graph per layer) and, for comparison, moe_layer_decode_host
     xh = torch.from_numpy(synth.tokens(synth.FULL, NX, seed=0, stream=rank)).pin_memory()
     yh = torch.empty((NX, H)).pin_memory()
     st = torch.cuda.Stream()
     xrows = [xh[i:i + 1] for i in range(NX)]  # a caller's per-token host buffers
     yrows = [yh[i:i + 1] for i in range(NX)]
 
-    calls = [moe.DecodeHostCall(v, ws, stream=st) for v in views]  # arguments marshalled once per layer
+    prepared = [moe.HostCall(v, ws, T=1, stream=st) for v in views]  # one per layer copy
+    unprepared = [moe.DecodeHostCall(v, ws, stream=st) for v in views]  # arguments marshalled once per layer
 
-    def e2e_steps(n, first):
-        for i in range(first, first + n):
-            calls[i % copies](xrows[i % NX], yrows[i % NX])
+    def e2e_time(calls):
+        def e2e_steps(n, first):
+            for i in range(first, first + n):
+                calls[i % copies](xrows[i % NX], yrows[i % NX])
 
-    e2e_steps(args.warmup, 0)
-    torch.cuda.synchronize()
-    passes = []
-    for _ in range(3):  # the host-bound call varies with the host: the median of three passes of K steps
-        ranks_barrier(torch)
-        t0 = time.perf_counter()
-        e2e_steps(args.steps, args.warmup)
+        e2e_steps(args.warmup, 0)
         torch.cuda.synchronize()
-        passes.append(time.perf_counter() - t0)
-    ranks_barrier(torch)
-    e2e_dt = max_over_ranks(torch, statistics.median(passes), dev)
+        passes = []
+        for _ in range(3):  # the host-bound call varies with the host: the median of three passes of K steps
+            ranks_barrier(torch)
+            t0 = time.perf_counter()
+            e2e_steps(args.steps, args.warmup)
+            torch.cuda.synchronize()
+            passes.append(time.perf_counter() - t0)
+        ranks_barrier(torch)
+        return max_over_ranks(torch, statistics.median(passes), dev)
+
+    e2e_dt = e2e_time(prepared)
+    e2e_host_dt = e2e_time(unprepared)
+    for c in prepared:
+        c.close()
 
     extra = {}
     if not args.quick and rank == 0:
@@ -364,10 +372,14 @@ def run_ours(args):
                      "peak_source": peaks["source"], "kernel": "moe_layer_decode (whole call)"},
         "e2e": {"value": job_rate(world, args.steps, e2e_dt), "unit": "tok/s",
                 "h2d_bytes_per_step": H * 4, "d2h_bytes_per_step": H * 4,
-                "note": "moe_layer_decode_host through the Python binding (DecodeHostCall), one call per step on pinned "
-                        "host rows: x read and y written by the kernels through the rows' device "
-                        "mapping, then the call polls the stream until y is in host memory; median of "
-                        "three passes of K steps"},
+                "note": "moe_host_call_run through the Python binding (HostCall, one prepared handle per "
+                        "layer copy), one call per step on pinned host rows: x copied into the handle's "
+                        "mapped staging row and read by the device, the step's recorded graph launched, "
+                        "y written by the decode kernel into the mapped row and copied out once the "
+                        "completion word arrives; median of three passes of K steps",
+                "moe_layer_decode_host": {"value": job_rate(world, args.steps, e2e_host_dt), "unit": "tok/s",
+                                          "note": "the unprepared host-buffer call (DecodeHostCall): mapped "
+                                                  "rows, two launches and a stream poll per step"}},
         "gpu_launches": args.steps,  # one persistent k_decode launch per step
         "clocks": clocks,
     }

@@ -37,6 +37,7 @@ ENTRY_POINTS = (
     "moe_lfu_create", "moe_lfu_destroy", "moe_lfu_step", "moe_lfu_state",
     "moe_decode_workspace_bytes", "moe_noalloc_status", "moe_debug_inject", "moe_rmsnorm", "moe_sample",
     "moe_cache_set_device_policy", "moe_attn_workspace_bytes", "moe_attn_step", "moe_attn_workspace_status",
+    "moe_host_call_create", "moe_host_call_run", "moe_host_call_rows", "moe_host_call_destroy",
 )
 MOE_SAMPLE_MAX_K = 1024
 
@@ -114,6 +115,10 @@ def _load():
     L.moe_attn_workspace_bytes.restype = sz
     L.moe_attn_step.argtypes = [p, p, i, i, i, p, p, p, sz, p]
     L.moe_attn_workspace_status.argtypes = [p, sz, p]
+    L.moe_host_call_create.argtypes = [p, p, i, i, p, sz, p]
+    L.moe_host_call_run.argtypes = [p, p, p]
+    L.moe_host_call_rows.argtypes = [p, p, p]
+    L.moe_host_call_destroy.argtypes = [p]
     for name in ENTRY_POINTS:
         if name not in ("moe_status_string", "moe_expert_blob_bytes", "moe_workspace_bytes",
                         "moe_tile_blob_bytes", "moe_decode_workspace_bytes", "moe_attn_workspace_bytes"):
@@ -321,6 +326,49 @@ class DecodeHostCall:
         rc = self._fn(self._lref, xp, 1, self._flags, yp, None, None, None, self._ws, self._nbytes, self._stream)
         if rc != MOE_OK:
             raise MoeError(rc, "moe_layer_decode_host")
+
+
+class HostCall:
+    """moe_host_call: the decode step on host rows, prepared once for one layer,
+    workspace, token count T, flags and stream (the step is a recorded CUDA graph;
+    each call copies x in, launches it, waits for its completion word in host memory
+    and copies y out).  `x_row` / `y_row` are the handle's page-locked staging rows
+    (T x H fp32 tensors); passing them to the call skips the copies."""
+
+    def __init__(self, layer: moe_layer_t, ws, T: int = 1, flags: int = 0, stream=None):
+        self._layer, self._ws = layer, ws  # kept alive for the handle's pointers
+        self.T, self.H = int(T), int(layer.H)
+        h = C.c_void_p()
+        _check(lib.moe_host_call_create(C.byref(h), C.byref(layer), self.T, int(flags), _ptr(ws), ws.numel(),
+                                        _stream(stream)), "moe_host_call_create")
+        self._h = h
+        xr, yr = C.POINTER(C.c_float)(), C.POINTER(C.c_float)()
+        _check(lib.moe_host_call_rows(h, C.byref(xr), C.byref(yr)), "moe_host_call_rows")
+        n = self.T * self.H
+        self.x_row = torch.frombuffer((C.c_float * n).from_address(C.addressof(xr.contents)),
+                                      dtype=torch.float32).view(self.T, self.H)
+        self.y_row = torch.frombuffer((C.c_float * n).from_address(C.addressof(yr.contents)),
+                                      dtype=torch.float32).view(self.T, self.H)
+        self._run = lib.moe_host_call_run
+
+    def __call__(self, x, y):
+        """x, y: host tensors (T x H fp32, contiguous) or plain addresses."""
+        xp = x if isinstance(x, int) else x.data_ptr()
+        yp = y if isinstance(y, int) else y.data_ptr()
+        rc = self._run(self._h, xp, yp)
+        if rc != MOE_OK:
+            raise MoeError(rc, "moe_host_call_run")
+
+    def close(self):
+        if self._h:
+            lib.moe_host_call_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def moe_layer_decode_noalloc(layer: moe_layer_t, x, y=None, flags: int = 0, idx=None, gate=None,

@@ -90,13 +90,32 @@ int cuda_status() {
 // only the layout's prefix (decode_total); the prefill chunk needs all of it.
 // Only the header is carried from call to call, and it sits at a fixed place.
 WsLayout ws_fit(const moe_layer_t *l, size_t ws_bytes, bool full) {
-    WsLayout best = ws_layout(*l, 1);
-    for (int t = 2; t <= MOE_MAX_PREFILL_TOKENS; t++) {
-        WsLayout w = ws_layout(*l, t);
-        if ((full ? w.total : w.decode_total) > ws_bytes) break;
-        best = w;
+    // the sizes grow with T_max: a binary search over 1..MOE_MAX_PREFILL_TOKENS, and the
+    // last answer is kept per thread (a decode loop binds the same workspace every call)
+    struct Key {
+        int H, E, topk, I, Is, full;
+        size_t bytes;
+        bool operator==(const Key &o) const {
+            return H == o.H && E == o.E && topk == o.topk && I == o.I && Is == o.Is && full == o.full &&
+                   bytes == o.bytes;
+        }
+    };
+    static thread_local Key last_key{-1, 0, 0, 0, 0, 0, 0};
+    static thread_local WsLayout last;
+    const Key key{l->H, l->E, l->topk, l->I, l->Is, full ? 1 : 0, ws_bytes};
+    if (key == last_key) return last;
+    auto size_of = [&](int t) {
+        const WsLayout w = ws_layout(*l, t);
+        return full ? w.total : w.decode_total;
+    };
+    int lo = 1, hi = MOE_MAX_PREFILL_TOKENS;  // the answer: the largest fitting T_max, else 1
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) / 2;
+        if (size_of(mid) <= ws_bytes) lo = mid; else hi = mid - 1;
     }
-    return best;
+    last = ws_layout(*l, lo);
+    last_key = key;
+    return last;
 }
 
 // Binds the caller's workspace: the layout is the one for the largest T_max whose
@@ -657,6 +676,45 @@ int scratch_status(void *d_ws, size_t ws_bytes, cudaStream_t st) {
 
 }  // namespace
 
+
+// ------------------------------------------------------------------ prepared host call
+struct moe_host_call {
+    moe_layer_t layer;
+    int T = 0, flags = 0;
+    void *ws = nullptr;
+    size_t ws_bytes = 0, xb = 0;
+    cudaStream_t st = nullptr, cap = nullptr;
+    float *x_h = nullptr, *y_h = nullptr;           // page-locked, mapped staging rows
+    unsigned *flag_h = nullptr;                      // completion word (page-locked, mapped)
+    unsigned *count_d = nullptr;                     // steps completed (device memory)
+    unsigned seq = 0;
+    cudaGraph_t graph = nullptr;
+    cudaGraphExec_t exec = nullptr;
+};
+
+namespace {
+
+// After the step: counts it and publishes the count to the host's completion word.
+__global__ void k_host_signal(unsigned *count, volatile unsigned *flag) {
+    const unsigned v = *count + 1u;
+    *count = v;
+    __threadfence_system();
+    *flag = v;
+}
+
+void host_call_free(moe_host_call *c) {
+    if (c->exec) cudaGraphExecDestroy(c->exec);
+    if (c->graph) cudaGraphDestroy(c->graph);
+    if (c->cap) cudaStreamDestroy(c->cap);
+    if (c->x_h) cudaFreeHost(c->x_h);
+    if (c->y_h) cudaFreeHost(c->y_h);
+    if (c->flag_h) cudaFreeHost(c->flag_h);
+    if (c->count_d) cudaFree(c->count_d);
+    delete c;
+}
+
+}  // namespace
+
 extern "C" {
 
 const char *moe_status_string(int status) {
@@ -1005,6 +1063,104 @@ int moe_noalloc_status(void *stream) {
     const int rc = noalloc_scratch(&ws);
     if (rc) return rc;
     return scratch_status(ws, MOE_NOALLOC_SCRATCH_BYTES, as_stream(stream));
+}
+
+
+int moe_host_call_create(moe_host_call_t **out, const moe_layer_t *layer, int T, int flags, void *d_ws,
+                         size_t ws_bytes, void *stream) {
+    if (!out) return MOE_EINVAL;
+    *out = nullptr;
+    if (!layer_ok(layer) || T < 1 || T > MOE_MAX_DECODE_TOKENS || !flags_ok(layer, flags)) return MOE_EINVAL;
+    Ws w;
+    int rc = bind_ws(layer, T, d_ws, ws_bytes, &w);
+    if (rc) return rc;
+    moe_host_call *c = new (std::nothrow) moe_host_call();
+    if (!c) return MOE_EINVAL;
+    c->layer = *layer;
+    c->T = T;
+    c->flags = flags;
+    c->ws = d_ws;
+    c->ws_bytes = ws_bytes;
+    c->xb = sizeof(float) * (size_t)T * layer->H;
+    c->st = as_stream(stream);
+    void *xd = nullptr, *yd = nullptr, *fd = nullptr;
+    if (cudaHostAlloc(&c->x_h, c->xb, cudaHostAllocMapped) != cudaSuccess ||
+        cudaHostAlloc(&c->y_h, c->xb, cudaHostAllocMapped) != cudaSuccess ||
+        cudaHostAlloc(&c->flag_h, 256, cudaHostAllocMapped) != cudaSuccess ||
+        cudaHostGetDevicePointer(&xd, c->x_h, 0) != cudaSuccess ||
+        cudaHostGetDevicePointer(&yd, c->y_h, 0) != cudaSuccess ||
+        cudaHostGetDevicePointer(&fd, c->flag_h, 0) != cudaSuccess || cudaMalloc(&c->count_d, 256) != cudaSuccess ||
+        cudaMemset(c->count_d, 0, 256) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&c->cap, cudaStreamNonBlocking) != cudaSuccess) {
+        rc = cuda_status();
+        host_call_free(c);
+        return rc ? rc : MOE_ECUDA;
+    }
+    memset(c->x_h, 0, c->xb);
+    *(volatile unsigned *)c->flag_h = 0u;
+    // the step, recorded once: x from its staging row into the workspace, the decode
+    // kernel writing y into its staging row, the completion word
+    if (cudaStreamBeginCapture(c->cap, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+        rc = cuda_status();
+        host_call_free(c);
+        return rc ? rc : MOE_ECUDA;
+    }
+    k_copy16<<<(unsigned)((c->xb / 16 + 255) / 256), 256, 0, c->cap>>>(reinterpret_cast<const uint4 *>(xd),
+                                                                      reinterpret_cast<uint4 *>(w.xh), c->xb / 16);
+    rc = cuda_status();
+    if (!rc)
+        rc = moe_layer_decode(layer, w.xh, T, flags, static_cast<float *>(yd), nullptr, nullptr, nullptr, d_ws,
+                              ws_bytes, c->cap);
+    if (!rc) {
+        k_host_signal<<<1, 1, 0, c->cap>>>(c->count_d, static_cast<volatile unsigned *>(fd));
+        rc = cuda_status();
+    }
+    const cudaError_t ec = cudaStreamEndCapture(c->cap, &c->graph);
+    if (!rc && (ec != cudaSuccess || cudaGraphInstantiate(&c->exec, c->graph, 0) != cudaSuccess)) rc = MOE_ECUDA;
+    if (rc) {
+        (void)cudaGetLastError();
+        host_call_free(c);
+        return rc;
+    }
+    *out = c;
+    return MOE_OK;
+}
+
+int moe_host_call_run(moe_host_call_t *c, const float *x_host, float *y_host) {
+    if (!c || !x_host || !y_host) return MOE_EINVAL;
+    if (x_host != c->x_h) memcpy(c->x_h, x_host, c->xb);
+    if (cudaGraphLaunch(c->exec, c->st) != cudaSuccess) return cuda_status();
+    const unsigned want = ++c->seq;
+    volatile unsigned *flag = c->flag_h;
+    // wait for the completion word: host memory, no driver call per test; the stream
+    // is asked now and then so that a failed step ends the wait
+    const auto t0 = std::chrono::steady_clock::now();
+    for (unsigned spins = 1;; spins++) {
+        if (*flag == want) break;
+        if ((spins & 1023u) == 0) {
+            const cudaError_t q = cudaStreamQuery(c->st);
+            if (q != cudaSuccess && q != cudaErrorNotReady) return cuda_status();
+            if (q == cudaSuccess && *flag != want) return MOE_ECUDA;  // the step ended without its signal
+            if (std::chrono::steady_clock::now() - t0 > std::chrono::seconds(5)) return MOE_ETIMEOUT;
+        }
+    }
+    std::atomic_thread_fence(std::memory_order_acquire);
+    if (y_host != c->y_h) memcpy(y_host, c->y_h, c->xb);
+    return MOE_OK;
+}
+
+int moe_host_call_rows(moe_host_call_t *c, float **x_row, float **y_row) {
+    if (!c) return MOE_EINVAL;
+    if (x_row) *x_row = c->x_h;
+    if (y_row) *y_row = c->y_h;
+    return MOE_OK;
+}
+
+int moe_host_call_destroy(moe_host_call_t *c) {
+    if (!c) return MOE_OK;
+    if (cudaStreamSynchronize(c->st) != cudaSuccess) (void)cudaGetLastError();
+    host_call_free(c);
+    return MOE_OK;
 }
 
 }  // extern "C"

@@ -303,6 +303,38 @@ MOE_API int moe_layer_decode_host(const moe_layer_t *layer, const float *x_host,
                                   void *d_ws, size_t ws_bytes, void *stream);
 
 /*
+ * moe_host_call -- a prepared moe_layer_decode_host for a decode loop: the same
+ * decode step (the routed MoE layer of moe_layer_decode; devtrends page, section
+ * "Qual è il trucco principale dell'architettura") for one layer, workspace,
+ * token count T (1..MOE_MAX_DECODE_TOKENS), flags and stream, all fixed when the
+ * handle is created.  Creation allocates page-locked, device-mapped staging rows
+ * for x and y (T x H fp32 each) and a completion word, and records the step -- x
+ * read from its staging row into the workspace, the decode kernel writing y into
+ * its staging row, the completion word set -- as a CUDA graph.
+ *
+ * moe_host_call_run copies x_host (T x H fp32, host memory) into the x row,
+ * launches the graph on the stream, waits for the completion word (polling host
+ * memory, the calling thread stays busy) and copies the y row to y_host: one
+ * driver call per step.  moe_host_call_rows returns the two staging rows; a caller
+ * may write x into the x row and read y from the y row and pass those rows to
+ * moe_host_call_run, which then skips the copies.  Outputs are ready on return.
+ *
+ * The layer's weights, the workspace and the stream must stay valid while the
+ * handle lives; a handle serves one thread at a time; a failed device wait is
+ * reported by moe_workspace_status as for moe_layer_decode.  Errors: MOE_EINVAL
+ * (arguments as moe_layer_decode, NULL handle or buffers), MOE_EWORKSPACE,
+ * MOE_ECUDA (allocation, capture or launch failed, or the step ended without its
+ * completion word), MOE_ETIMEOUT (no completion within 5 s).
+ * moe_host_call_destroy waits for the stream and frees the handle (NULL is fine).
+ */
+typedef struct moe_host_call moe_host_call_t;
+MOE_API int moe_host_call_create(moe_host_call_t **out, const moe_layer_t *layer, int T, int flags, void *d_ws,
+                                 size_t ws_bytes, void *stream);
+MOE_API int moe_host_call_run(moe_host_call_t *c, const float *x_host, float *y_host);
+MOE_API int moe_host_call_rows(moe_host_call_t *c, float **x_row, float **y_row);
+MOE_API int moe_host_call_destroy(moe_host_call_t *c);
+
+/*
  * moe_layer_decode_noalloc -- the same decode step as moe_layer_decode (no cache),
  * for callers that cannot allocate device memory: for example a plug-in running
  * inside a host framework that reserves the GPU's memory through its own allocator

@@ -229,6 +229,37 @@ def test_decode_host_buffers(moe, tiny, T, pinned):
         assert np.array_equal(y2.numpy(), yh.numpy())
 
 
+@pytest.mark.parametrize("T", [1, 5])
+def test_host_call(moe, tiny, T):
+    # the prepared host call (a recorded graph per layer, workspace, T and flags):
+    # consecutive steps on one handle equal the device-pointer call bit for bit,
+    # from pinned and from pageable rows and from the handle's own staging rows
+    s, gl, ol = tiny
+    x = synth.tokens(s, 4 * T, seed=0, stream=720 + T)
+    layer = gl.view()
+    ws = moe.new_workspace(layer, 16)
+    hc = moe.HostCall(layer, ws, T=T, flags=moe.MOE_RESIDUAL)
+    for k in range(3):
+        xk = torch.from_numpy(x[k * T:(k + 1) * T].copy())
+        if k != 1:
+            xk = xk.pin_memory()
+        yk = torch.full_like(xk, float("nan"))
+        hc(xk, yk)
+        yd = moe.moe_layer_decode(layer, _cuda(xk.numpy()), ws, flags=moe.MOE_RESIDUAL)
+        torch.cuda.synchronize()
+        assert np.array_equal(yk.numpy(), yd.cpu().numpy())
+    hc.x_row.copy_(torch.from_numpy(x[3 * T:]))
+    hc(hc.x_row, hc.y_row)
+    ry, _, _ = ol.layer(x[3 * T:], residual=True)
+    ok, worst = within_tol(hc.y_row.numpy(), ry, TOL)
+    assert ok, "worst err/bound %.3f" % worst
+    assert moe.moe_workspace_status(ws) == moe.MOE_OK
+    hc.close()
+    for bad_T in (0, moe.MOE_MAX_DECODE_TOKENS + 1):
+        with pytest.raises(moe.MoeError):
+            moe.HostCall(layer, ws, T=bad_T)
+
+
 @pytest.mark.parametrize("T", [1, 37, 128])
 def test_prefill_tiny(moe, tiny, T):
     s, gl, ol = tiny
