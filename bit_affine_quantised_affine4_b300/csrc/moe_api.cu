@@ -433,15 +433,24 @@ int run_layer_chunk(const moe_layer_t *l, const float *x, int T, int flags, floa
     g.Lr = tile_layout(l->H, l->I);
     g.Ls = tile_layout(l->H, l->Is);
     g.Br = ws.Br; g.Bs = ws.Bs; g.Hr = ws.Hr; g.Hs = ws.Hs; g.Yr = ws.Yr; g.Ys = ws.Ys;
+    // the down GEMM cuts the shared expert's K = Is into parts of the routed experts'
+    // K = I (equal items over the CTAs); parts 1.. go to the gate/up token tiles' area,
+    // free once the gate/up GEMM has run
+    const int sp = shared_parts(l->I, l->Is);
+    const size_t br_bytes = (size_t)(l->H / kGroup) * Rmax * 128;
+    g.sparts = (sp > 1 && (size_t)(sp - 1) * T16 * l->H * sizeof(float) <= br_bytes) ? sp : 1;
+    g.Ys_more = reinterpret_cast<float *>(ws.Br);
     g.err = &ws.ctrl[kErr];
+    const int sparts = g.sparts;
     for (int kind = 0; kind < 2; kind++) {
         g.kind = kind;
+        g.sparts = kind == 0 ? 1 : sparts;  // (the gate/up GEMM has no K parts)
         k_prefill_gemm<<<sms, kPfThreads, prefill_gemm_smem(), st>>>(g);
         if ((rc = cuda_status())) return rc;
     }
-    const long long cthreads = (long long)T * l->H;
-    k_prefill_combine<<<(unsigned)((cthreads + 255) / 256), 256, 0, st>>>(x, T, l->H, l->topk, flags, ws.gate,
-                                                                         ws.Yr, ws.Ys, y);
+    const long long cthreads = (long long)T * (l->H / 4);
+    k_prefill_combine<<<(unsigned)((cthreads + 255) / 256), 256, 0, st>>>(
+        x, T, l->H, l->topk, flags, ws.gate, ws.Yr, ws.Ys, sparts, g.Ys_more, T16, y);
     return cuda_status();
 }
 

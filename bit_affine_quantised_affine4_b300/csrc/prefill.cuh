@@ -362,6 +362,8 @@ struct PrefillGemmArgs {
     const uint8_t *Br, *Bs;  // token operand tiles [kb][rows][128 B] (routed Rmax rows, shared T16 rows)
     uint8_t *Hr, *Hs;        // kind 0 output: h operand tiles for the down
     float *Yr, *Ys;          // kind 1 output: fp32 rows [pair][H], [t][H]
+    int sparts;              // kind 1: the shared down matrix in sparts K parts of at most I/64 groups
+    float *Ys_more;          // kind 1: parts 1.. of the shared rows, [sparts - 1][T16][H]
     unsigned *err;
 };
 
@@ -376,24 +378,28 @@ struct PfItem {
     int row0;            // first row of the slice (shared: token; routed: in the expert's segment)
     int mb;              // M block
     int u;               // routed expert, -1 = shared
+    int part;            // shared down: K part
 };
 
 // Items: [shared M block mb, slice sl] for mb < ms, sl < ceil(T / kPfMaxN); then per
 // distinct expert u, [M block mb, slice sl] for mb < mr, sl < its slices.
 __device__ __forceinline__ int pf_shared_slices(const PrefillGemmArgs &a) { return (a.T + kPfMaxN - 1) / kPfMaxN; }
 __device__ __forceinline__ int pf_items(const PrefillGemmArgs &a) {
-    const int ms = a.kind == 0 ? a.Is / 64 : a.H / 128, mr = a.kind == 0 ? a.I / 64 : a.H / 128;
+    const int ms = a.kind == 0 ? a.Is / 64 : (a.H / 128) * a.sparts, mr = a.kind == 0 ? a.I / 64 : a.H / 128;
     return ms * pf_shared_slices(a) + mr * a.uslc[a.U[0]];
 }
 __device__ __forceinline__ PfItem pf_item(const PrefillGemmArgs &a, int i) {
     PfItem it;
-    const int ms = a.kind == 0 ? a.Is / 64 : a.H / 128;  // shared M blocks
-    const int mr = a.kind == 0 ? a.I / 64 : a.H / 128;   // routed M blocks per expert
+    const int ms = a.kind == 0 ? a.Is / 64 : (a.H / 128) * a.sparts;  // shared (M block, K part) items
+    const int mr = a.kind == 0 ? a.I / 64 : a.H / 128;                 // routed M blocks per expert
     const int nss = pf_shared_slices(a);
+    it.part = 0;
     if (i < ms * nss) {
-        const int mb = i / nss, sl = i - mb * nss;
+        const int mp = i / nss, sl = i - mp * nss;
+        const int mb = a.kind == 0 ? mp : mp / a.sparts;
         it.u = -1;
         it.mb = mb;
+        it.part = a.kind == 0 ? 0 : mp - mb * a.sparts;
         it.row0 = sl * kPfMaxN;
         it.n = min(kPfMaxN, a.T - it.row0);
         it.N = round16(it.n);
@@ -404,9 +410,12 @@ __device__ __forceinline__ PfItem pf_item(const PrefillGemmArgs &a, int i) {
             it.a_row = (size_t)kTileBytes * a.Ls.G;
             it.nkb = a.Ls.G;
         } else {
-            it.a = a.shared + a.Ls.gu_bytes + (size_t)kTileBytes * (8 * mb) * a.Ls.Gi;
+            // K part p: groups [p Gi, min((p + 1) Gi, Gis)) of the shared down rows
+            const int k0 = it.part * a.Lr.Gi;
+            it.a = a.shared + a.Ls.gu_bytes + (size_t)kTileBytes * ((size_t)(8 * mb) * a.Ls.Gi + k0);
             it.a_row = (size_t)kTileBytes * a.Ls.Gi;
-            it.nkb = a.Ls.Gi;
+            it.nkb = a.sparts > 1 ? min(a.Lr.Gi, a.Ls.Gi - k0) : a.Ls.Gi;
+            it.b += (size_t)k0 * it.b_kb;
         }
     } else {
         // expert u: the last one with mr * uslc[u] <= j
@@ -723,7 +732,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill_gemm(const PrefillGem
                         const int jt = c0 + q;
                         if (jt < it.n) {
                             if (it.u < 0)
-                                a.Ys[(size_t)(it.row0 + jt) * a.H + n] = v[q];
+                                (it.part ? a.Ys_more + (size_t)(it.part - 1) * a.T16 * a.H : a.Ys)
+                                    [(size_t)(it.row0 + jt) * a.H + n] = v[q];
                             else
                                 a.Yr[(size_t)a.rowpair[a.urow[it.u] + it.row0 + jt] * a.H + n] = v[q];
                         }
@@ -748,18 +758,34 @@ inline size_t prefill_gemm_smem() {
 }
 
 // ------------------------------------------------------------------ combine
+// One thread per 4 consecutive outputs (H is a multiple of 4): the same fixed order
+// of additions per element as one thread per output, with 16-byte loads.
 __global__ void __launch_bounds__(256) k_prefill_combine(const float *__restrict__ x, int T, int H, int topk,
                                                          int flags, const float *__restrict__ gate,
                                                          const float *__restrict__ Yr,
-                                                         const float *__restrict__ Ys, float *__restrict__ y) {
-    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= (long long)T * H) return;
-    const int t = (int)(i / H), n = (int)(i % H);
-    float acc = 0.f;
-    for (int k = 0; k < topk; k++) acc = fmaf(gate[t * topk + k], Yr[(size_t)(t * topk + k) * H + n], acc);
-    acc += Ys[(size_t)t * H + n];
-    if (flags & MOE_RESIDUAL) acc += x[(size_t)t * H + n];
-    y[i] = acc;
+                                                         const float *__restrict__ Ys, int sparts,
+                                                         const float *__restrict__ Ys_more, int T16,
+                                                         float *__restrict__ y) {
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;  // float4 index
+    const int H4 = H / 4;
+    if (i >= (long long)T * H4) return;
+    const int t = (int)(i / H4), n4 = (int)(i % H4);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < topk; k++) {
+        const float g = gate[t * topk + k];
+        const float4 v = __ldg(reinterpret_cast<const float4 *>(Yr + (size_t)(t * topk + k) * H) + n4);
+        acc = make_float4(fmaf(g, v.x, acc.x), fmaf(g, v.y, acc.y), fmaf(g, v.z, acc.z), fmaf(g, v.w, acc.w));
+    }
+    for (int p = 0; p < sparts; p++) {  // the shared expert's K parts, in order
+        const float *ys = p ? Ys_more + (size_t)(p - 1) * T16 * H : Ys;
+        const float4 sv = __ldg(reinterpret_cast<const float4 *>(ys + (size_t)t * H) + n4);
+        acc = make_float4(acc.x + sv.x, acc.y + sv.y, acc.z + sv.z, acc.w + sv.w);
+    }
+    if (flags & MOE_RESIDUAL) {
+        const float4 xv = __ldg(reinterpret_cast<const float4 *>(x + (size_t)t * H) + n4);
+        acc = make_float4(acc.x + xv.x, acc.y + xv.y, acc.z + xv.z, acc.w + xv.w);
+    }
+    reinterpret_cast<float4 *>(y)[i] = acc;
 }
 
 }  // namespace moe
