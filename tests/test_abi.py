@@ -59,3 +59,15 @@ def test_host_side_argument_checks():
         == moe.MOE_EWORKSPACE
     assert L.moe_layer_decode(C.byref(good), 256, 17, 0, 512, None, None, None, 256, 1 << 30, None) \
         == moe.MOE_EINVAL
+    # the prepared host call: refused before any allocation, capture or launch
+    h = C.c_void_p(0)
+    assert L.moe_host_call_create(None, C.byref(good), 1, 0, 256, 1 << 30, None) == moe.MOE_EINVAL
+    assert L.moe_host_call_create(C.byref(h), C.byref(bad), 1, 0, 256, 1 << 30, None) == moe.MOE_EINVAL
+    assert L.moe_host_call_create(C.byref(h), C.byref(good), 0, 0, 256, 1 << 30, None) == moe.MOE_EINVAL
+    assert L.moe_host_call_create(C.byref(h), C.byref(good), 17, 0, 256, 1 << 30, None) == moe.MOE_EINVAL
+    assert L.moe_host_call_create(C.byref(h), C.byref(good), 1, 0x100, 256, 1 << 30, None) == moe.MOE_EINVAL
+    assert L.moe_host_call_create(C.byref(h), C.byref(good), 1, 0, 256, 16, None) == moe.MOE_EWORKSPACE
+    assert h.value is None  # no handle on a refusal
+    assert L.moe_host_call_run(None, 256, 256) == moe.MOE_EINVAL
+    assert L.moe_host_call_rows(None, None, None) == moe.MOE_EINVAL
+    assert L.moe_host_call_destroy(None) == moe.MOE_OK
