@@ -399,10 +399,11 @@ int run_layer_chunk(const moe_layer_t *l, const float *x, int T, int flags, floa
         ra.rq = ly.rq; ra.rs = ly.rs; ra.rb = ly.rb; ra.bias = ly.bias;
         ra.x = xin; ra.T = T; ra.H = l->H; ra.E = l->E; ra.topk = l->topk;
         ra.part = ws.Yr; ra.idx = ws.idx; ra.gate = ws.gate;
-        k_prefill_route<<<dim3(KS, nEB, nTB), kRtThreads, prefill_route_smem(), st>>>(ra);
-        if ((rc = cuda_status())) return rc;
-        k_prefill_topk<<<(T + kRtTopkWarps - 1) / kRtTopkWarps, kRtTopkWarps * 32, 0, st>>>(ra, KS);
-        if ((rc = cuda_status())) return rc;
+        if (pf_launch(k_prefill_route, dim3(KS, nEB, nTB), dim3(kRtThreads), prefill_route_smem(), st, ra) !=
+                cudaSuccess ||
+            pf_launch(k_prefill_topk, dim3((T + kRtTopkWarps - 1) / kRtTopkWarps), dim3(kRtTopkWarps * 32), 0, st,
+                      ra, KS) != cudaSuccess)
+            return cuda_status();
     } else if ((rc = launch_route(l, ly, xin, T, ws, ws.idx, ws.gate, nullptr, st))) {
         return rc;
     }
@@ -420,12 +421,13 @@ int run_layer_chunk(const moe_layer_t *l, const float *x, int T, int flags, floa
     plan.rowtok = plan.ucnt + MOE_MAX_EXPERTS;
     plan.rowpair = plan.rowtok + Rmax;
     plan.uslc = plan.rowpair + Rmax;
-    k_prefill_plan<<<1, 256, 0, st>>>(ws.idx, T, l->E, l->topk, Rmax, plan);
-    if ((rc = cuda_status())) return rc;
+    if (pf_launch(k_prefill_plan, dim3(1), dim3(256), 0, st, (const int *)ws.idx, T, l->E, l->topk, Rmax, plan) !=
+        cudaSuccess)
+        return cuda_status();
     const long long gthreads = (long long)(Rmax + T16) * (l->H / kGroup) * 8;
-    k_prefill_gather<<<(unsigned)((gthreads + 255) / 256), 256, 0, st>>>(xin, T, l->H, Rmax, T16, plan.rowtok,
-                                                                         plan.U, ws.Br, ws.Bs);
-    if ((rc = cuda_status())) return rc;
+    if (pf_launch(k_prefill_gather, dim3((unsigned)((gthreads + 255) / 256)), dim3(256), 0, st, xin, T, l->H, Rmax,
+                  T16, (const int *)plan.rowtok, (const int *)plan.U, ws.Br, ws.Bs) != cudaSuccess)
+        return cuda_status();
     PrefillGemmArgs g;
     g.H = l->H; g.I = l->I; g.Is = l->Is; g.T = T; g.T16 = T16; g.Rmax = Rmax;
     g.U = plan.U; g.uexp = plan.uexp; g.urow = plan.urow; g.ucnt = plan.ucnt; g.rowpair = plan.rowpair; g.uslc = plan.uslc;
@@ -445,13 +447,15 @@ int run_layer_chunk(const moe_layer_t *l, const float *x, int T, int flags, floa
     for (int kind = 0; kind < 2; kind++) {
         g.kind = kind;
         g.sparts = kind == 0 ? 1 : sparts;  // (the gate/up GEMM has no K parts)
-        k_prefill_gemm<<<sms, kPfThreads, prefill_gemm_smem(), st>>>(g);
-        if ((rc = cuda_status())) return rc;
+        if (pf_launch(k_prefill_gemm, dim3(sms), dim3(kPfThreads), prefill_gemm_smem(), st, g) != cudaSuccess)
+            return cuda_status();
     }
     const long long cthreads = (long long)T * (l->H / 4);
-    k_prefill_combine<<<(unsigned)((cthreads + 255) / 256), 256, 0, st>>>(
-        x, T, l->H, l->topk, flags, ws.gate, ws.Yr, ws.Ys, sparts, g.Ys_more, T16, y);
-    return cuda_status();
+    if (pf_launch(k_prefill_combine, dim3((unsigned)((cthreads + 255) / 256)), dim3(256), 0, st, x, T, l->H,
+                  l->topk, flags, (const float *)ws.gate, (const float *)ws.Yr, (const float *)ws.Ys, sparts,
+                  (const float *)g.Ys_more, T16, y) != cudaSuccess)
+        return cuda_status();
+    return MOE_OK;
 }
 
 }  // namespace

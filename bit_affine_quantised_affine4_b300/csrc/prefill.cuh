@@ -38,6 +38,8 @@
 // mask extract two codes into an fp16 pair.
 #pragma once
 
+#include <atomic>
+
 #include "common.cuh"
 #include "mma_core.cuh"
 #include "route.cuh"
@@ -116,13 +118,6 @@ __global__ void __launch_bounds__(kRtThreads, 4) k_prefill_route(const RouteTile
     const int t0 = tb * kRtTok, e0 = eb * kRtExp, k0 = ks * kRtSliceCols;
     const int kw = min(kRtSliceCols, a.H - k0);  // 64 or 128
     const int G = a.H / kGroup, c4 = kw / 4;     // float4 columns of the slice
-    // x rows of the tile (zeros past T)
-    for (int v = tid; v < kRtTok * c4; v += kRtThreads) {
-        const int r = v / c4, c = v - r * c4, t = t0 + r;
-        float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (t < a.T) val = __ldg(reinterpret_cast<const float4 *>(a.x + (size_t)t * a.H + k0) + c);
-        *reinterpret_cast<float4 *>(xs + r * kRtPitch + 4 * c) = val;
-    }
     // router rows of the tile, dequantised: 16 codes (one uint4) per step (zeros past E)
     const int c16 = kw / 16;
     for (int v = tid; v < kRtExp * c16; v += kRtThreads) {
@@ -142,6 +137,17 @@ __global__ void __launch_bounds__(kRtThreads, 4) k_prefill_route(const RouteTile
 #pragma unroll
             for (int u = 0; u < 4; u++) *reinterpret_cast<float4 *>(dst + 4 * u) = make_float4(0.f, 0.f, 0.f, 0.f);
         }
+    }
+    // the tokens (the previous kernel's output) and the partial sums' area (which the
+    // previous chunk's combine reads) only after the previous kernel has finished
+    pdl_wait();
+    pdl_launch_dependents();
+    // x rows of the tile (zeros past T)
+    for (int v = tid; v < kRtTok * c4; v += kRtThreads) {
+        const int r = v / c4, c = v - r * c4, t = t0 + r;
+        float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (t < a.T) val = __ldg(reinterpret_cast<const float4 *>(a.x + (size_t)t * a.H + k0) + c);
+        *reinterpret_cast<float4 *>(xs + r * kRtPitch + 4 * c) = val;
     }
     __syncthreads();
     const int tg = lane & 7, eg = lane >> 3;
@@ -190,6 +196,8 @@ __global__ void __launch_bounds__(kRtTopkWarps * 32) k_prefill_topk(const RouteT
     __shared__ float lg[kRtTopkWarps][MOE_MAX_EXPERTS];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = blockIdx.x * kRtTopkWarps + warp;
+    pdl_wait();
+    pdl_launch_dependents();
     if (t >= a.T) return;
     constexpr int NV = MOE_MAX_EXPERTS / 32;
     float acc[NV];
@@ -218,6 +226,8 @@ __global__ void __launch_bounds__(256) k_prefill_plan(const int *__restrict__ id
     __shared__ unsigned mask[MOE_MAX_EXPERTS][4];  // token bit masks (T <= 128)
     __shared__ int urow_s[MOE_MAX_EXPERTS + 1], uid[MOE_MAX_EXPERTS];
     const int tid = threadIdx.x;
+    pdl_wait();
+    pdl_launch_dependents();
     for (int i = tid; i < MOE_MAX_EXPERTS * 4; i += blockDim.x) (&mask[0][0])[i] = 0u;
     __syncthreads();
     const int P2 = T * topk;
@@ -320,6 +330,8 @@ __global__ void __launch_bounds__(256) k_prefill_gather(const float *__restrict_
     const int G = H / kGroup;
     const long long n = (long long)(Rmax + T16) * G * 8;
     const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    pdl_wait();
+    pdl_launch_dependents();
     if (i >= n) return;
     const int ch = (int)(i & 7);
     const long long rk = i >> 3;
@@ -490,18 +502,6 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill_gemm(const PrefillGem
     // the plan in shared memory: every item lookup reads it
     __shared__ int pl_U[2], pl_uslc[MOE_MAX_EXPERTS + 1], pl_ucnt[MOE_MAX_EXPERTS], pl_urow[MOE_MAX_EXPERTS],
         pl_uexp[MOE_MAX_EXPERTS];
-    {
-        const int U = ga.U[0];
-        if (threadIdx.x == 0) pl_U[0] = U;
-        for (int u = threadIdx.x; u <= U; u += blockDim.x) {
-            pl_uslc[u] = ga.uslc[u];
-            if (u < U) {
-                pl_ucnt[u] = ga.ucnt[u];
-                pl_urow[u] = ga.urow[u];
-                pl_uexp[u] = ga.uexp[u];
-            }
-        }
-    }
     PrefillGemmArgs a = ga;
     a.U = pl_U;
     a.uslc = pl_uslc;
@@ -536,6 +536,21 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill_gemm(const PrefillGem
         mbar_fence_init();
     }
     if (warp == 0) tmem_alloc(&S.tmem, kPfTmemCols);
+    // the plan and the operands are the previous kernels' outputs
+    pdl_wait();
+    pdl_launch_dependents();
+    {
+        const int U = ga.U[0];
+        if (threadIdx.x == 0) pl_U[0] = U;
+        for (int u = threadIdx.x; u <= U; u += blockDim.x) {
+            pl_uslc[u] = ga.uslc[u];
+            if (u < U) {
+                pl_ucnt[u] = ga.ucnt[u];
+                pl_urow[u] = ga.urow[u];
+                pl_uexp[u] = ga.uexp[u];
+            }
+        }
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -753,6 +768,34 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill_gemm(const PrefillGem
     }
 }
 
+// Launches a kernel of the chunk with programmatic dependent launch (each kernel
+// waits for its predecessor with griddepcontrol.wait before it reads that one's
+// output, and lets its own dependents start right after); a runtime that refuses
+// the attribute gets plain launches from then on.
+template <typename... KArgs, typename... Args>
+inline cudaError_t pf_launch(void (*fn)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                             Args... args) {
+    static std::atomic<int> pdl_ok{1};
+    if (pdl_ok.load()) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = grid;
+        cfg.blockDim = block;
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        const cudaError_t e = cudaLaunchKernelEx(&cfg, fn, args...);
+        if (e != cudaErrorInvalidValue && e != cudaErrorNotSupported) return e;
+        (void)cudaGetLastError();
+        pdl_ok.store(0);
+    }
+    fn<<<grid, block, smem, st>>>(args...);
+    return cudaGetLastError();
+}
+
 inline size_t prefill_gemm_smem() {
     return 1024 + (size_t)kPfWStages * kPfW + (size_t)kPfQStages * kPfQ + 64 * kPfMaxN * 4 + kPfMaxN * 128;
 }
@@ -768,6 +811,8 @@ __global__ void __launch_bounds__(256) k_prefill_combine(const float *__restrict
                                                          float *__restrict__ y) {
     const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;  // float4 index
     const int H4 = H / 4;
+    pdl_wait();
+    pdl_launch_dependents();
     if (i >= (long long)T * H4) return;
     const int t = (int)(i / H4), n4 = (int)(i % H4);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
