@@ -169,7 +169,10 @@ T *mapped_alias(T *p) {
     return reinterpret_cast<T *>(at.devicePointer);
 }
 
+// x staging ahead of a decode launch: the decode (programmatic dependent launch) may
+// start its weight-only prologue at once and waits for this kernel before it reads x.
 __global__ void __launch_bounds__(256) k_copy16(const uint4 *__restrict__ src, uint4 *__restrict__ dst, size_t n) {
+    pdl_launch_dependents();
     const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i < n) dst[i] = src[i];
 }
