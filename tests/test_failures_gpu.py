@@ -10,6 +10,8 @@
   returns MOE_ECUDA, the cache's slot table, counts and statistics are those of
   before the call, and the next call (retrying the same step) matches the oracle
   and the oracle's LFU policy, which never saw the failed step.
+* A prepared host call on a workspace whose error word is raised: the step
+  completes, the status call reports and clears the error, the next step is right.
 """
 import numpy as np
 import pytest
@@ -55,6 +57,33 @@ def test_device_wait_times_out_and_recovers(T):
         assert np.array_equal(idx.cpu().numpy(), ridx)
         ok, worst = within_tol(y.cpu().numpy(), ry, TOL)
         assert ok, worst
+
+
+def test_prepared_host_call_after_a_wait_gave_up():
+    # a prepared host call on a workspace whose error word another call raised: the
+    # step still completes and signals (the kernel drains), moe_workspace_status
+    # reports MOE_ETIMEOUT and re-initialises the workspace, and the handle's next
+    # step equals its first bit for bit
+    import bit_affine_quantised_affine4_b300 as moe
+    s = synth.TINY
+    gl = gpu_layer(s, seed=0)
+    layer = gl.view()
+    ws = moe.new_workspace(layer, 1)
+    x = torch.from_numpy(synth.tokens(s, 1, seed=0, stream=1500)).pin_memory()
+    hc = moe.HostCall(layer, ws, T=1)
+    y0 = torch.empty_like(x)
+    hc(x, y0)
+    assert moe.moe_workspace_status(ws) == moe.MOE_OK
+    moe.moe_debug_inject(moe.MOE_INJECT_WAIT)
+    moe.moe_layer_decode(layer, x.cuda(), ws)
+    y1 = torch.empty_like(x)
+    hc(x, y1)  # returns: the step ends without waiting on anything that will not come
+    assert moe.moe_workspace_status(ws) == moe.MOE_ETIMEOUT
+    assert moe.moe_workspace_status(ws) == moe.MOE_OK
+    y2 = torch.empty_like(x)
+    hc(x, y2)
+    assert np.array_equal(y2.numpy(), y0.numpy())
+    hc.close()
 
 
 def test_inject_rejects_unknown_kind():
