@@ -188,18 +188,27 @@ __global__ void __launch_bounds__(proj_threads<MODE>(), MODE == kProjQKV ? 4 : 2
     pdl_wait();
     pdl_launch_dependents();
 
-    // RMSNorm of the CTA's tokens (QKV mode with a gain): warp w sums tokens w, w + kWarps
+    // RMSNorm of the CTA's tokens (QKV mode with a gain): every warp sums its share of
+    // each token's squares, then the warps' partials are added in warp order
     if (MODE == kProjQKV && a.norm_w) {
-        for (int t = warp; t < Tc; t += kWarps) {
+        __shared__ float ssp[kWarps][kProjTokens];
+        for (int t = 0; t < Tc; t++) {
             const float4 *xr = reinterpret_cast<const float4 *>(a.x + (size_t)(t0 + t) * a.K);
             float ss = 0.f;
-            for (int j = lane; j < a.K / 4; j += 32) {
+            for (int j = tid; j < a.K / 4; j += kThreads) {
                 const float4 v = __ldg(xr + j);
                 ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
             }
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-            if (lane == 0) inv_r[t] = rsqrtf(ss / (float)a.K + a.norm_eps);
+            if (lane == 0) ssp[warp][t] = ss;
+        }
+        __syncthreads();
+        if (tid < Tc) {
+            float ss = 0.f;
+#pragma unroll
+            for (int w = 0; w < kWarps; w++) ss += ssp[w][tid];
+            inv_r[tid] = rsqrtf(ss / (float)a.K + a.norm_eps);
         }
         __syncthreads();
     }
