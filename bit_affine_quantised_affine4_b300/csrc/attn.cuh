@@ -111,8 +111,11 @@ inline size_t proj_smem_bytes(int K, int T) {
 // kernels of a step never write them.  The tokens (the previous kernel's output)
 // are read after the wait.  The CTA lets its dependents start only after its own
 // wait (the attention kernel relies on that).
-template <int MODE>
-__global__ void __launch_bounds__(proj_threads<MODE>(), MODE == kProjQKV ? 4 : 2) k_attn_proj(const ProjArgs a) {
+// MINB: CTAs per SM the registers must allow (the QKV projection 4; the output
+// projection 2, which leaves it more registers; a GEMV of more 16-row tiles than two
+// waves of 2 per SM takes 4).
+template <int MODE, int MINB = (MODE == kProjQKV ? 4 : 2)>
+__global__ void __launch_bounds__(proj_threads<MODE>(), MINB) k_attn_proj(const ProjArgs a) {
     constexpr int kWarps = ProjCfg<MODE>::warps, kThreads = 32 * kWarps;
     extern __shared__ __align__(128) unsigned char smem[];
     const int XS = proj_xs_stride(a.K), WR = proj_wrow(a.K), SR = proj_srow(a.K);

@@ -110,7 +110,10 @@ int proj_smem_optin() {
     if (done.load()) return MOE_OK;
     const size_t most = proj_smem_bytes<MODE>(MOE_ATTN_MAX_HIDDEN, kProjTokens);
     if (cudaFuncSetAttribute(k_attn_proj<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)most) !=
-        cudaSuccess)
+            cudaSuccess ||
+        (MODE == kProjPlain &&
+         cudaFuncSetAttribute(k_attn_proj<kProjPlain, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)most) !=
+             cudaSuccess))
         return attn_cuda_status();
     done.store(1);
     return MOE_OK;
@@ -281,6 +284,17 @@ int moe::qgemv_rows16(const uint32_t *q, const __half *s, const __half *b, int N
     o.T = 1;
     o.y = y;
     o.err = err;
+    // more tiles than two waves of 2 CTAs per SM: the build that fits 4 per SM
+    static int sms = 0;
+    if (!sms) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return attn_cuda_status();
+    }
+    if (N / 16 > 2 * sms)
+        return launch_pdl(k_attn_proj<kProjPlain, 4>, dim3(N / 16, 1), dim3(proj_threads<kProjPlain>()),
+                          proj_smem_bytes<kProjPlain>(K, 1), st, o);
     return launch_pdl(k_attn_proj<kProjPlain>, dim3(N / 16, 1), dim3(proj_threads<kProjPlain>()),
                       proj_smem_bytes<kProjPlain>(K, 1), st, o);
 }
