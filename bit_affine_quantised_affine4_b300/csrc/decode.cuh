@@ -195,7 +195,14 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
     };
     auto consumer_wait = [&](int k) -> int {
         const int s = k % a.stages;
-        if (!*err && !mbar_wait(&S.full[s], (k / a.stages) & 1, err)) {
+        // a non-blocking test first: the stage has usually landed already
+        unsigned done;
+        asm volatile("{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                     "selp.u32 %0, 1, 0, p;\n\t}"
+                     : "=r"(done)
+                     : "r"(smem_addr(&S.full[s])), "r"((unsigned)((k / a.stages) & 1))
+                     : "memory");
+        if (!done && !*err && !mbar_wait(&S.full[s], (k / a.stages) & 1, err)) {
             *err = 1;
             atomicExch(&a.ctrl[kErr], 1u);
         }
@@ -323,10 +330,11 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
         unsigned claim = 0;  // bit 0: reduce the previous tile; bit 1: reduce this one
         if (lane == 0) {
             __threadfence_block();
+            // both atomics issued before either result is used
             const unsigned n = atomicAdd(&S.tcnt[slot], 1u) + 1u;
+            const unsigned pc = p_slot >= 0 ? atomicCAS(&S.tcnt[p_slot], (unsigned)kCW, (unsigned)kCW + 1u) : 0u;
             if (final_tile && n == (unsigned)kCW) claim |= 2u;
-            if (p_slot >= 0 && atomicCAS(&S.tcnt[p_slot], (unsigned)kCW, (unsigned)kCW + 1u) == (unsigned)kCW)
-                claim |= 1u;
+            if (p_slot >= 0 && pc == (unsigned)kCW) claim |= 1u;
         }
         claim = __shfl_sync(0xffffffffu, claim, 0);
         if (claim & 1u) reduce_tile(p_slot, p_u, p_it);
