@@ -424,7 +424,7 @@ int run_layer_chunk(const moe_layer_t *l, const float *x, int T, int flags, floa
     plan.rowtok = plan.ucnt + MOE_MAX_EXPERTS;
     plan.rowpair = plan.rowtok + Rmax;
     plan.uslc = plan.rowpair + Rmax;
-    if (pf_launch(k_prefill_plan, dim3(1), dim3(256), 0, st, (const int *)ws.idx, T, l->E, l->topk, Rmax, plan) !=
+    if (pf_launch(k_prefill_plan, dim3(1), dim3(kPlanThreads), 0, st, (const int *)ws.idx, T, l->E, l->topk, Rmax, plan) !=
         cudaSuccess)
         return cuda_status();
     const long long gthreads = (long long)(Rmax + T16) * (l->H / kGroup) * 8;

@@ -52,7 +52,8 @@ namespace moe {
 constexpr int kPfKF = 4;             // K steps (groups) per packed-weight copy: one bulk copy per
                                      // tile row moves kPfKF tiles (a copy costs the same whatever its size)
 constexpr int kPfWStages = 2;        // packed-weight ring: kPfKF K steps per stage
-constexpr int kPfQStages = 4;        // operand ring: dequantised A and the token tile of one K step
+constexpr int kPfQStages = 2;        // operand ring: dequantised A and the token tiles of kPfQK K steps
+constexpr int kPfQK = 2;             // K steps per operand stage (one wait, one commit, one arrival each)
 constexpr int kPfDq = 8;             // dequantising warps (one weight tile row each per K step)
 constexpr int kPfProducer = kPfDq, kPfMmaWarp = kPfProducer + 1;
 constexpr int kPfEpi0 = kPfProducer + 2;  // first epilogue warp
@@ -64,7 +65,8 @@ constexpr int kPfMaxN = 128;         // token rows of one item: an expert with m
                                      // into slices of kPfMaxN rows, each its own item (64-row slices with
                                      // five operand stages measured slower: 318 vs 303 us per chunk)
 constexpr int kPfTileA = 128 * 128;  // dequantised A: 128 rows x 64 fp16
-constexpr int kPfQ = kPfTileA + kPfMaxN * 128;  // an operand stage: A, then the token tile
+constexpr int kPfQ = kPfTileA + kPfMaxN * 128;  // one K step of an operand stage: A, then the token tile
+static_assert(kPfKF % kPfQK == 0, "an operand stage never straddles two packed-weight stages");
 constexpr int kPfTmemCols = 256;     // two fp32 accumulators of up to 128 columns
 
 // Plan written by k_prefill_plan (ints in the workspace).
@@ -203,7 +205,26 @@ __global__ void __launch_bounds__(kRtTopkWarps * 32) k_prefill_topk(const RouteT
     float acc[NV];
 #pragma unroll
     for (int i = 0; i < NV; i++) acc[i] = 0.f;
-    for (int q = 0; q < KS; q++) {
+    // the loads of four slices are issued before their sums (added in slice order)
+    constexpr int kQ = 4;
+    int q = 0;
+    for (; q + kQ <= KS; q += kQ) {
+        float v[kQ][NV];
+#pragma unroll
+        for (int j = 0; j < kQ; j++) {
+            const float *pr = a.part + ((size_t)(q + j) * a.T + t) * a.E;
+#pragma unroll
+            for (int i = 0; i < NV; i++) {
+                const int e = lane + 32 * i;
+                v[j][i] = e < a.E ? __ldcg(pr + e) : 0.f;
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kQ; j++)
+#pragma unroll
+            for (int i = 0; i < NV; i++) acc[i] += v[j][i];
+    }
+    for (; q < KS; q++) {
         const float *pr = a.part + ((size_t)q * a.T + t) * a.E;
 #pragma unroll
         for (int i = 0; i < NV; i++) {
@@ -221,18 +242,22 @@ __global__ void __launch_bounds__(kRtTopkWarps * 32) k_prefill_topk(const RouteT
 }
 
 // ------------------------------------------------------------------ plan
-__global__ void __launch_bounds__(256) k_prefill_plan(const int *__restrict__ idx, int T, int E, int topk,
-                                                      int Rmax, PfPlan p) {
+static_assert(MOE_MAX_PREFILL_TOKENS <= 128, "the plan's token masks hold 128 tokens");
+constexpr int kPlanThreads = 1024;  // one (token, choice) pair per thread at T = 128, top-8
+__global__ void __launch_bounds__(kPlanThreads) k_prefill_plan(const int *__restrict__ idx, int T, int E, int topk,
+                                                               int Rmax, PfPlan p) {
     __shared__ unsigned mask[MOE_MAX_EXPERTS][4];  // token bit masks (T <= 128)
     __shared__ int urow_s[MOE_MAX_EXPERTS + 1], uid[MOE_MAX_EXPERTS];
+    __shared__ int idx_s[MOE_MAX_PREFILL_TOKENS * MOE_MAX_TOPK];  // the routing, read once
     const int tid = threadIdx.x;
+    for (int i = tid; i < MOE_MAX_EXPERTS * 4; i += blockDim.x) (&mask[0][0])[i] = 0u;
     pdl_wait();
     pdl_launch_dependents();
-    for (int i = tid; i < MOE_MAX_EXPERTS * 4; i += blockDim.x) (&mask[0][0])[i] = 0u;
     __syncthreads();
     const int P2 = T * topk;
     for (int q = tid; q < P2; q += blockDim.x) {
-        const int t = q / topk, e = idx[q];
+        const int t = q / topk, e = __ldcg(idx + q);
+        idx_s[q] = e;
         atomicOr(&mask[e][t >> 5], 1u << (t & 31));
     }
     __syncthreads();
@@ -297,7 +322,7 @@ __global__ void __launch_bounds__(256) k_prefill_plan(const int *__restrict__ id
     }
     __syncthreads();
     for (int q = tid; q < P2; q += blockDim.x) {
-        const int t = q / topk, e = idx[q], u = uid[e];
+        const int t = q / topk, e = idx_s[q], u = uid[e];
         int rank = 0;
         for (int w = 0; w < (t >> 5); w++) rank += __popc(mask[e][w]);
         rank += __popc(mask[e][t >> 5] & ((1u << (t & 31)) - 1u));
@@ -513,7 +538,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill_gemm(const PrefillGem
     uint8_t *base = psm_raw + ((1024u - (smem_addr(psm_raw) & 1023u)) & 1023u);
     uint8_t *wst = base;
     uint8_t *qst = wst + (size_t)kPfWStages * kPfW;
-    float *ebuf = reinterpret_cast<float *>(qst + (size_t)kPfQStages * kPfQ);  // [128 cols][64 rows]
+    float *ebuf = reinterpret_cast<float *>(qst + (size_t)kPfQStages * kPfQK * kPfQ);  // [128 cols][64 rows]
     uint8_t *hst = reinterpret_cast<uint8_t *>(ebuf + 64 * kPfMaxN);          // [128 rows][128 B]
     volatile int *err = &S.err;
 
@@ -579,7 +604,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill_gemm(const PrefillGem
                     const PfItem nx = pf_item(a, i + nC);
                     prefetch_l2(nx.a, (unsigned)(8 * nx.a_row));
                 }
-                for (int kb = 0; kb < it.nkb; kb++, f++) {
+                for (int kb = 0; kb < it.nkb; kb += kPfQK, f++) {
                     if (kb % kPfKF == 0) {
                         const int w = wf % kPfWStages, nk = min(kPfKF, it.nkb - kb);
                         if (wf >= kPfWStages && !*err &&
@@ -599,8 +624,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill_gemm(const PrefillGem
                     if (f >= kPfQStages && !*err && !mbar_wait(&S.q_free[q], ((f / kPfQStages) - 1) & 1, err))
                         fail();
                     if (*err) continue;
-                    mbar_arrive_expect_tx(&S.q_full[q], it.N * 128);
-                    bulk_g2s(qst + (size_t)q * kPfQ + kPfTileA, it.b + (size_t)kb * it.b_kb, it.N * 128, &S.q_full[q]);
+                    const int nq = min(kPfQK, it.nkb - kb);
+                    mbar_arrive_expect_tx(&S.q_full[q], nq * it.N * 128);
+                    for (int h = 0; h < nq; h++)
+                        bulk_g2s(qst + (size_t)(q * kPfQK + h) * kPfQ + kPfTileA, it.b + (size_t)(kb + h) * it.b_kb,
+                                 it.N * 128, &S.q_full[q]);
                     qlast[q] = f;
                 }
             }
@@ -622,18 +650,18 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill_gemm(const PrefillGem
                 if (n_it >= 2 && !*err && !mbar_wait(&S.acc_empty[ab], ((n_it >> 1) - 1) & 1, err)) fail();
                 tc_fence_after();
                 const uint32_t idesc = umma_idesc_f16(128, it.N);
-                for (int kb = 0; kb < it.nkb; kb++, f++) {
-                    const int q = f % kPfQStages;
+                for (int kb = 0; kb < it.nkb; kb += kPfQK, f++) {
+                    const int q = f % kPfQStages, nq = min(kPfQK, it.nkb - kb);
                     if (!pf_done(&S.q_full[q], (f / kPfQStages) & 1) && !mbar_wait(&S.q_full[q], (f / kPfQStages) & 1, err))
                         fail();
                     tc_fence_after();
-                    {
-                        const uint32_t sa = smem_addr(qst + (size_t)q * kPfQ);
+                    for (int h = 0; h < nq; h++) {
+                        const uint32_t sa = smem_addr(qst + (size_t)(q * kPfQK + h) * kPfQ);
                         const uint32_t sb = sa + kPfTileA;
 #pragma unroll
                         for (int ks = 0; ks < 4; ks++)
                             umma_f16(tmem + ab * 128, umma_desc(sa + 32 * ks), umma_desc(sb + 32 * ks), idesc,
-                                     kb > 0 || ks > 0);
+                                     kb + h > 0 || ks > 0);
                     }
                     umma_commit(&S.q_free[q]);
                 }
@@ -658,33 +686,41 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill_gemm(const PrefillGem
         int f = 0, wf = 0;
         for (int i = b; i < NI; i += nC) {
             const int nkb = pf_item(a, i).nkb;
-            for (int kb = 0; kb < nkb; kb++, f++) {
-                const int w = wf % kPfWStages, q = f % kPfQStages;
+            for (int kb = 0; kb < nkb; kb += kPfQK, f++) {
+                const int w = wf % kPfWStages, q = f % kPfQStages, nq = min(kPfQK, nkb - kb);
                 // (the waits give up at once when another warp raised the error word)
                 if (kb % kPfKF == 0 && !mbar_wait(&S.w_full[w], (wf / kPfWStages) & 1, err)) fail();
                 {
-                    // the packed tile is loaded before the wait for the operand stage
-                    const uint8_t *rs = wst + (size_t)w * kPfW + j * kPfWRow + (kb % kPfKF) * kTileBytes;
-                    const uint4 qv = *reinterpret_cast<const uint4 *>(rs + 16 * lane);
-                    const uint2 e = *reinterpret_cast<const uint2 *>(rs + 512 + 8 * r);
+                    // the packed tiles are loaded before the wait for the operand stage
+                    uint4 qv[kPfQK];
+                    uint2 e[kPfQK];
+#pragma unroll
+                    for (int h = 0; h < kPfQK; h++)
+                        if (h < nq) {
+                            const uint8_t *rs = wst + (size_t)w * kPfW + j * kPfWRow + ((kb + h) % kPfKF) * kTileBytes;
+                            qv[h] = *reinterpret_cast<const uint4 *>(rs + 16 * lane);
+                            e[h] = *reinterpret_cast<const uint2 *>(rs + 512 + 8 * r);
+                        }
                     if (f >= kPfQStages && !pf_done(&S.q_free[q], ((f / kPfQStages) - 1) & 1) &&
                         !mbar_wait(&S.q_free[q], ((f / kPfQStages) - 1) & 1, err))
                         fail();
-                    {
-                        uint8_t *as = qst + (size_t)q * kPfQ;
-                        const __half2 sa2 = __half2half2(__ushort_as_half((unsigned short)(e.x & 0xFFFFu)));
-                        const __half2 ba2 = __half2half2(__ushort_as_half((unsigned short)(e.x >> 16)));
-                        const __half2 sb2 = __half2half2(__ushort_as_half((unsigned short)(e.y & 0xFFFFu)));
-                        const __half2 bb2 = __half2half2(__ushort_as_half((unsigned short)(e.y >> 16)));
-                        *reinterpret_cast<uint4 *>(as + oa0) = deq_word(qv.x, sa2, ba2);
-                        *reinterpret_cast<uint4 *>(as + oa1) = deq_word(qv.y, sa2, ba2);
-                        *reinterpret_cast<uint4 *>(as + ob0) = deq_word(qv.z, sb2, bb2);
-                        *reinterpret_cast<uint4 *>(as + ob1) = deq_word(qv.w, sb2, bb2);
-                        fence_async_smem();
-                    }
+#pragma unroll
+                    for (int h = 0; h < kPfQK; h++)
+                        if (h < nq) {
+                            uint8_t *as = qst + (size_t)(q * kPfQK + h) * kPfQ;
+                            const __half2 sa2 = __half2half2(__ushort_as_half((unsigned short)(e[h].x & 0xFFFFu)));
+                            const __half2 ba2 = __half2half2(__ushort_as_half((unsigned short)(e[h].x >> 16)));
+                            const __half2 sb2 = __half2half2(__ushort_as_half((unsigned short)(e[h].y & 0xFFFFu)));
+                            const __half2 bb2 = __half2half2(__ushort_as_half((unsigned short)(e[h].y >> 16)));
+                            *reinterpret_cast<uint4 *>(as + oa0) = deq_word(qv[h].x, sa2, ba2);
+                            *reinterpret_cast<uint4 *>(as + oa1) = deq_word(qv[h].y, sa2, ba2);
+                            *reinterpret_cast<uint4 *>(as + ob0) = deq_word(qv[h].z, sb2, bb2);
+                            *reinterpret_cast<uint4 *>(as + ob1) = deq_word(qv[h].w, sb2, bb2);
+                        }
+                    fence_async_smem();
                     mbar_arrive(&S.q_full[q]);  // each thread, after its own stores and fence
                 }
-                if (kb % kPfKF == kPfKF - 1 || kb == nkb - 1) {
+                if ((kb + nq) % kPfKF == 0 || kb + nq == nkb) {
                     // the weight stage is consumed after its last K step
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&S.w_free[w]);
@@ -797,7 +833,7 @@ inline cudaError_t pf_launch(void (*fn)(KArgs...), dim3 grid, dim3 block, size_t
 }
 
 inline size_t prefill_gemm_smem() {
-    return 1024 + (size_t)kPfWStages * kPfW + (size_t)kPfQStages * kPfQ + 64 * kPfMaxN * 4 + kPfMaxN * 128;
+    return 1024 + (size_t)kPfWStages * kPfW + (size_t)kPfQStages * kPfQK * kPfQ + 64 * kPfMaxN * 4 + kPfMaxN * 128;
 }
 
 // ------------------------------------------------------------------ combine
