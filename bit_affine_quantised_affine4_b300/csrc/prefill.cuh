@@ -21,14 +21,16 @@
 //   combine  (grid)   y_t = sum_k gate_tk * routed_(t,k) + shared_t (+ x_t), in a
 //                     fixed order.
 //
-// Inside a GEMM CTA: one thread of the producer warp prefetches the next item's
-// weight block into L2 and fills two rings with bulk copies (TMA): a packed-weight
-// ring, one copy per tile row covering kPfKF K steps (a copy costs about the same
-// whatever its size, so fewer, larger copies), and an operand ring, one stage per K
-// step, into which it copies the token tile.  The eight dequantising warps turn one
-// weight tile each (w = s*q + b, exact, rounded once to fp16) into the swizzled A
-// operand of the same operand stage; the stage's barrier completes with the token
-// bytes and one arrival per dequantising thread.  One thread of the MMA warp issues
+// Inside a GEMM CTA, two copy warps fill two rings with bulk copies (TMA): one
+// thread of the weight warp prefetches the next item's weight block into L2 and
+// fills the packed-weight ring, one copy per tile row covering kPfKF K steps, as
+// soon as a stage is released; one thread of the token warp copies the token tiles
+// into the operand ring (kPfQK K steps per stage) as soon as the MMA releases a
+// stage, with nothing else in between.  The eight dequantising warps load a whole
+// weight stage into registers, release it, and turn one weight tile each (w = s*q +
+// b, exact, rounded once to fp16) into the swizzled A operand of the operand stage;
+// the stage's barrier completes with the token bytes and one arrival per
+// dequantising thread.  One thread of the MMA warp issues
 // the MMAs (fp16 x fp16 -> fp32 in tensor memory) and commits them to the stage's
 // release barrier.  Eight epilogue warps read the accumulator out of tensor memory
 // (two per lane quarter, splitting the columns) while the next item's K steps run
@@ -49,18 +51,19 @@
 
 namespace moe {
 
-constexpr int kPfKF = 4;             // K steps (groups) per packed-weight copy: one bulk copy per
+constexpr int kPfKF = 2;             // K steps (groups) per packed-weight copy: one bulk copy per
                                      // tile row moves kPfKF tiles (a copy costs the same whatever its size)
-constexpr int kPfWStages = 2;        // packed-weight ring: kPfKF K steps per stage
+constexpr int kPfWStages = 4;        // packed-weight ring: kPfKF K steps per stage
 constexpr int kPfQStages = 2;        // operand ring: dequantised A and the token tiles of kPfQK K steps
 constexpr int kPfQK = 2;             // K steps per operand stage (one wait, one commit, one arrival each)
 constexpr int kPfDq = 8;             // dequantising warps (one weight tile row each per K step)
 constexpr int kPfProducer = kPfDq, kPfMmaWarp = kPfProducer + 1;
 constexpr int kPfEpi0 = kPfProducer + 2;  // first epilogue warp
 constexpr int kPfEpi = 8;            // epilogue warps: each lane quarter of tensor memory twice
-constexpr int kPfThreads = (kPfEpi0 + kPfEpi) * 32;
+constexpr int kPfWProd = kPfEpi0 + kPfEpi;  // the packed-weight copies' warp
+constexpr int kPfThreads = (kPfWProd + 1) * 32;
 constexpr int kPfWRow = kPfKF * kTileBytes;  // one tile row's kPfKF tiles in a weight stage
-constexpr int kPfW = 8 * kPfWRow;            // a weight stage (18432 bytes, a multiple of 1024)
+constexpr int kPfW = 8 * kPfWRow;            // a weight stage (9216 bytes, a multiple of 1024)
 constexpr int kPfMaxN = 128;         // token rows of one item: an expert with more tokens would be cut
                                      // into slices of kPfMaxN rows, each its own item (64-row slices with
                                      // five operand stages measured slower: 318 vs 303 us per chunk)
@@ -589,37 +592,16 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill_gemm(const PrefillGem
     };
 
     if (warp == kPfProducer) {
-        // ---------------- copies (one thread): per kPfKF K steps of an item, one bulk copy
-        // per tile row into the weight ring; per K step, the token tile into the operand ring
+        // ---------------- token copies (one thread): per operand stage, its token tiles,
+        // issued as soon as the MMA releases the stage (the packed weights have their own
+        // warp, so nothing else stands between the release and the copy)
         if (lane == 0) {
-            int f = 0, wf = 0;
-            int wlast[kPfWStages], qlast[kPfQStages];
-            for (int s = 0; s < kPfWStages; s++) wlast[s] = -1;
+            int f = 0;
+            int qlast[kPfQStages];
             for (int s = 0; s < kPfQStages; s++) qlast[s] = -1;
             for (int i = b; i < NI; i += nC) {
                 const PfItem it = pf_item(a, i);
-                // this item's weight block (first item only) and the next one's, into L2
-                if (i == b) prefetch_l2(it.a, (unsigned)(8 * it.a_row));
-                if (i + nC < NI) {
-                    const PfItem nx = pf_item(a, i + nC);
-                    prefetch_l2(nx.a, (unsigned)(8 * nx.a_row));
-                }
                 for (int kb = 0; kb < it.nkb; kb += kPfQK, f++) {
-                    if (kb % kPfKF == 0) {
-                        const int w = wf % kPfWStages, nk = min(kPfKF, it.nkb - kb);
-                        if (wf >= kPfWStages && !*err &&
-                            !mbar_wait(&S.w_free[w], ((wf / kPfWStages) - 1) & 1, err))
-                            fail();
-                        if (!*err) {
-                            mbar_arrive_expect_tx(&S.w_full[w], 8 * nk * kTileBytes);
-                            uint8_t *dst = wst + (size_t)w * kPfW;
-                            for (int j = 0; j < 8; j++)
-                                bulk_g2s(dst + j * kPfWRow, it.a + j * it.a_row + (size_t)kb * kTileBytes,
-                                         nk * kTileBytes, &S.w_full[w]);
-                            wlast[w] = wf;
-                        }
-                        wf++;
-                    }
                     const int q = f % kPfQStages;
                     if (f >= kPfQStages && !*err && !mbar_wait(&S.q_free[q], ((f / kPfQStages) - 1) & 1, err))
                         fail();
@@ -634,8 +616,6 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill_gemm(const PrefillGem
             }
             // drain: the last copies of every stage have landed
             volatile int never = 0;
-            for (int s = 0; s < kPfWStages; s++)
-                if (wlast[s] >= 0) mbar_wait(&S.w_full[s], (wlast[s] / kPfWStages) & 1, &never);
             for (int s = 0; s < kPfQStages; s++)
                 if (qlast[s] >= 0) mbar_wait(&S.q_full[s], (qlast[s] / kPfQStages) & 1, &never);
         }
@@ -686,48 +666,85 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill_gemm(const PrefillGem
         int f = 0, wf = 0;
         for (int i = b; i < NI; i += nC) {
             const int nkb = pf_item(a, i).nkb;
-            for (int kb = 0; kb < nkb; kb += kPfQK, f++) {
-                const int w = wf % kPfWStages, q = f % kPfQStages, nq = min(kPfQK, nkb - kb);
+            for (int kw = 0; kw < nkb; kw += kPfKF, wf++) {
+                const int w = wf % kPfWStages, nk = min(kPfKF, nkb - kw);
                 // (the waits give up at once when another warp raised the error word)
-                if (kb % kPfKF == 0 && !mbar_wait(&S.w_full[w], (wf / kPfWStages) & 1, err)) fail();
-                {
-                    // the packed tiles are loaded before the wait for the operand stage
-                    uint4 qv[kPfQK];
-                    uint2 e[kPfQK];
+                if (!pf_done(&S.w_full[w], (wf / kPfWStages) & 1) && !mbar_wait(&S.w_full[w], (wf / kPfWStages) & 1, err))
+                    fail();
+                // the whole weight stage's packed tiles, before the operand stages' waits
+                uint4 qv[kPfKF];
+                uint2 e[kPfKF];
+                const uint8_t *rs = wst + (size_t)w * kPfW + j * kPfWRow;
 #pragma unroll
-                    for (int h = 0; h < kPfQK; h++)
-                        if (h < nq) {
-                            const uint8_t *rs = wst + (size_t)w * kPfW + j * kPfWRow + ((kb + h) % kPfKF) * kTileBytes;
-                            qv[h] = *reinterpret_cast<const uint4 *>(rs + 16 * lane);
-                            e[h] = *reinterpret_cast<const uint2 *>(rs + 512 + 8 * r);
-                        }
+                for (int h = 0; h < kPfKF; h++)
+                    if (h < nk) {
+                        qv[h] = *reinterpret_cast<const uint4 *>(rs + h * kTileBytes + 16 * lane);
+                        e[h] = *reinterpret_cast<const uint2 *>(rs + h * kTileBytes + 512 + 8 * r);
+                    }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&S.w_free[w]);  // the stage is in registers
+#pragma unroll
+                for (int st = 0; st < kPfKF / kPfQK; st++) {
+                    const int kb = kw + st * kPfQK;
+                    if (kb >= nkb) break;
+                    const int q = f % kPfQStages, nq = min(kPfQK, nkb - kb);
                     if (f >= kPfQStages && !pf_done(&S.q_free[q], ((f / kPfQStages) - 1) & 1) &&
                         !mbar_wait(&S.q_free[q], ((f / kPfQStages) - 1) & 1, err))
                         fail();
 #pragma unroll
                     for (int h = 0; h < kPfQK; h++)
                         if (h < nq) {
+                            const int x = st * kPfQK + h;
                             uint8_t *as = qst + (size_t)(q * kPfQK + h) * kPfQ;
-                            const __half2 sa2 = __half2half2(__ushort_as_half((unsigned short)(e[h].x & 0xFFFFu)));
-                            const __half2 ba2 = __half2half2(__ushort_as_half((unsigned short)(e[h].x >> 16)));
-                            const __half2 sb2 = __half2half2(__ushort_as_half((unsigned short)(e[h].y & 0xFFFFu)));
-                            const __half2 bb2 = __half2half2(__ushort_as_half((unsigned short)(e[h].y >> 16)));
-                            *reinterpret_cast<uint4 *>(as + oa0) = deq_word(qv[h].x, sa2, ba2);
-                            *reinterpret_cast<uint4 *>(as + oa1) = deq_word(qv[h].y, sa2, ba2);
-                            *reinterpret_cast<uint4 *>(as + ob0) = deq_word(qv[h].z, sb2, bb2);
-                            *reinterpret_cast<uint4 *>(as + ob1) = deq_word(qv[h].w, sb2, bb2);
+                            const __half2 sa2 = __half2half2(__ushort_as_half((unsigned short)(e[x].x & 0xFFFFu)));
+                            const __half2 ba2 = __half2half2(__ushort_as_half((unsigned short)(e[x].x >> 16)));
+                            const __half2 sb2 = __half2half2(__ushort_as_half((unsigned short)(e[x].y & 0xFFFFu)));
+                            const __half2 bb2 = __half2half2(__ushort_as_half((unsigned short)(e[x].y >> 16)));
+                            *reinterpret_cast<uint4 *>(as + oa0) = deq_word(qv[x].x, sa2, ba2);
+                            *reinterpret_cast<uint4 *>(as + oa1) = deq_word(qv[x].y, sa2, ba2);
+                            *reinterpret_cast<uint4 *>(as + ob0) = deq_word(qv[x].z, sb2, bb2);
+                            *reinterpret_cast<uint4 *>(as + ob1) = deq_word(qv[x].w, sb2, bb2);
                         }
                     fence_async_smem();
                     mbar_arrive(&S.q_full[q]);  // each thread, after its own stores and fence
-                }
-                if ((kb + nq) % kPfKF == 0 || kb + nq == nkb) {
-                    // the weight stage is consumed after its last K step
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&S.w_free[w]);
-                    wf++;
+                    f++;
                 }
             }
         }
+    } else if (warp == kPfWProd) {
+        // ---------------- packed-weight copies (one thread): per kPfKF K steps of an item,
+        // one bulk copy per tile row, issued as soon as the weight stage is released
+        if (lane == 0) {
+            int wf = 0;
+            int wlast[kPfWStages];
+            for (int s = 0; s < kPfWStages; s++) wlast[s] = -1;
+            for (int i = b; i < NI; i += nC) {
+                const PfItem it = pf_item(a, i);
+                // this item's weight block (first item only) and the next one's, into L2
+                if (i == b) prefetch_l2(it.a, (unsigned)(8 * it.a_row));
+                if (i + nC < NI) {
+                    const PfItem nx = pf_item(a, i + nC);
+                    prefetch_l2(nx.a, (unsigned)(8 * nx.a_row));
+                }
+                for (int kb = 0; kb < it.nkb; kb += kPfKF, wf++) {
+                    const int w = wf % kPfWStages, nk = min(kPfKF, it.nkb - kb);
+                    if (wf >= kPfWStages && !*err && !mbar_wait(&S.w_free[w], ((wf / kPfWStages) - 1) & 1, err))
+                        fail();
+                    if (*err) continue;
+                    mbar_arrive_expect_tx(&S.w_full[w], 8 * nk * kTileBytes);
+                    uint8_t *dst = wst + (size_t)w * kPfW;
+                    for (int j = 0; j < 8; j++)
+                        bulk_g2s(dst + j * kPfWRow, it.a + j * it.a_row + (size_t)kb * kTileBytes, nk * kTileBytes,
+                                 &S.w_full[w]);
+                    wlast[w] = wf;
+                }
+            }
+            // drain: the last copies of every stage have landed
+            volatile int never = 0;
+            for (int s = 0; s < kPfWStages; s++)
+                if (wlast[s] >= 0) mbar_wait(&S.w_full[s], (wlast[s] / kPfWStages) & 1, &never);
+        }
+        __syncwarp();
     } else {
         // ---------------- epilogue (warps 10-17), overlapping the next item's K steps
         const int etid = tid - kPfEpi0 * 32;
