@@ -13,27 +13,28 @@
 //                     (token, choice) pair.
 //   gather   (grid)   tokens -> fp16 operand tiles, per expert segment (zero rows
 //                     pad each segment), plus all tokens for the shared expert.
-//   gemm 0   (grid)   gate/up: per (expert, 64 gate + 64 up rows) item,
-//                     D[128 x n] = W x X^T over K = H on the tensor cores, then
-//                     h = gelu_tanh(gate) * up written as the down's fp16 operand.
-//   gemm 1   (grid)   down: per (expert, 128 output rows) item, D = Wd x h^T over
+//   gemm 0   (grid)   gate/up: per (expert, 128 gate + 128 up rows) item,
+//                     D[tokens x 256] = X x W^T over K = H on the tensor cores,
+//                     then h = gelu_tanh(gate) * up written as the down's fp16
+//                     operand.
+//   gemm 1   (grid)   down: per (expert, 256 output rows) item, D = h x Wd^T over
 //                     K = I (Is for the shared expert), fp32 rows out.
 //   combine  (grid)   y_t = sum_k gate_tk * routed_(t,k) + shared_t (+ x_t), in a
 //                     fixed order.
 //
-// Inside a GEMM CTA, two copy warps fill two rings with bulk copies (TMA): one
-// thread of the weight warp prefetches the next item's weight block into L2 and
-// fills the packed-weight ring, one copy per tile row covering kPfKF K steps, as
-// soon as a stage is released; one thread of the token warp copies the token tiles
-// into the operand ring (kPfQK K steps per stage) as soon as the MMA releases a
-// stage, with nothing else in between.  The eight dequantising warps load a whole
-// weight stage into registers, release it, and turn one weight tile each (w = s*q +
-// b, exact, rounded once to fp16) into the swizzled A operand of the operand stage;
-// the stage's barrier completes with the token bytes and one arrival per
-// dequantising thread.  One thread of the MMA warp issues
-// the MMAs (fp16 x fp16 -> fp32 in tensor memory) and commits them to the stage's
-// release barrier.  Eight epilogue warps read the accumulator out of tensor memory
-// (two per lane quarter, splitting the columns) while the next item's K steps run
+// Inside a GEMM CTA the tokens are the MMA's M (128 rows, the item's slice) and the
+// weights its N (256 rows: one instruction covers twice the weight rows that an
+// M = 128 weight operand would, for about 1.1x its issue time).  One thread of the
+// token warp prefetches the next item's weight block into L2 and copies the token
+// tiles (bulk copies, TMA) into the operand ring (kPfQK K steps per stage) as soon
+// as the MMA releases a stage.  The sixteen dequantising warps load their tile row
+// of the next stage straight from global memory into registers, then turn the
+// current one (w = s*q + b, exact, rounded once to fp16) into the swizzled B operand
+// of the stage; the stage's barrier completes with the token bytes and one arrival
+// per dequantising thread.  One thread of the MMA warp issues the MMAs (fp16 x fp16
+// -> fp32 in tensor memory) and commits them to the stage's release barrier.  Eight
+// epilogue warps read the accumulator out of tensor memory (a lane per token, two
+// warps per lane quarter splitting the columns) while the next item's K steps run
 // into the other of two accumulators.  Columns of both operands are stored in the
 // same permuted order within each run of 8 (see mma_core.cuh): a K permutation
 // applied to both operands leaves the product unchanged, and it lets one 32-bit
@@ -51,26 +52,21 @@
 
 namespace moe {
 
-constexpr int kPfKF = 2;             // K steps (groups) per packed-weight copy: one bulk copy per
-                                     // tile row moves kPfKF tiles (a copy costs the same whatever its size)
-constexpr int kPfWStages = 4;        // packed-weight ring: kPfKF K steps per stage
-constexpr int kPfQStages = 2;        // operand ring: dequantised A and the token tiles of kPfQK K steps
+constexpr int kPfRows = 256;         // weight rows per item: the MMA's N (the tokens are its M = 128)
+constexpr int kPfTR = kPfRows / 16;  // tile rows per item
+constexpr int kPfQStages = 2;        // operand ring: token tiles and dequantised weights of kPfQK K steps
 constexpr int kPfQK = 2;             // K steps per operand stage (one wait, one commit, one arrival each)
-constexpr int kPfDq = 8;             // dequantising warps (one weight tile row each per K step)
+constexpr int kPfDq = kPfTR;         // dequantising warps (one weight tile row each per K step)
 constexpr int kPfProducer = kPfDq, kPfMmaWarp = kPfProducer + 1;
 constexpr int kPfEpi0 = kPfProducer + 2;  // first epilogue warp
 constexpr int kPfEpi = 8;            // epilogue warps: each lane quarter of tensor memory twice
-constexpr int kPfWProd = kPfEpi0 + kPfEpi;  // the packed-weight copies' warp
-constexpr int kPfThreads = (kPfWProd + 1) * 32;
-constexpr int kPfWRow = kPfKF * kTileBytes;  // one tile row's kPfKF tiles in a weight stage
-constexpr int kPfW = 8 * kPfWRow;            // a weight stage (9216 bytes, a multiple of 1024)
-constexpr int kPfMaxN = 128;         // token rows of one item: an expert with more tokens would be cut
-                                     // into slices of kPfMaxN rows, each its own item (64-row slices with
-                                     // five operand stages measured slower: 318 vs 303 us per chunk)
-constexpr int kPfTileA = 128 * 128;  // dequantised A: 128 rows x 64 fp16
-constexpr int kPfQ = kPfTileA + kPfMaxN * 128;  // one K step of an operand stage: A, then the token tile
-static_assert(kPfKF % kPfQK == 0, "an operand stage never straddles two packed-weight stages");
-constexpr int kPfTmemCols = 256;     // two fp32 accumulators of up to 128 columns
+constexpr int kPfThreads = (kPfEpi0 + kPfEpi) * 32;
+constexpr int kPfMaxN = 128;         // token rows of one item (the MMA's M): an expert with more tokens
+                                     // is cut into slices of kPfMaxN rows, each its own item
+constexpr int kPfTileA = kPfMaxN * 128;      // token tile: 128 rows x 64 fp16 (the MMA's A)
+constexpr int kPfTileB = kPfRows * 128;      // dequantised weights: 256 rows x 64 fp16 (the MMA's B)
+constexpr int kPfQ = kPfTileA + kPfTileB;    // one K step of an operand stage
+constexpr int kPfTmemCols = 2 * kPfRows;     // two fp32 accumulators of 256 columns
 
 // Plan written by k_prefill_plan (ints in the workspace).
 struct PfPlan {
@@ -407,33 +403,42 @@ struct PrefillGemmArgs {
     unsigned *err;
 };
 
-// Item i of the launch: shared items first, then the routed experts in order.
+// Item i of the launch: shared items first, then the routed experts in order.  An
+// item is one block of kPfRows weight rows (gate/up: 128 intermediate indices, gate
+// and up rows interleaved; down: 256 output rows) times one slice of <= kPfMaxN
+// tokens; the last block of a matrix may hold half as many rows.
 struct PfItem {
-    const uint8_t *a;    // first tile of the item's 8-tile-row block (K step 0)
-    size_t a_row;        // bytes between the 8 tile rows
+    const uint8_t *a;    // first tile (K step 0) of the item's first tile row
+    size_t a_row;        // bytes between tile rows
     int nkb;             // K steps (groups)
+    int ntr;             // tile rows (kPfTR, or kPfTR / 2 for a half block): the MMA's N is 16 ntr
     const uint8_t *b;    // token tile rows of K step 0
     size_t b_kb;         // bytes between K steps of the token tiles
     int n, N;            // valid token rows, padded (multiple of 16), of this kPfMaxN-row slice
     int row0;            // first row of the slice (shared: token; routed: in the expert's segment)
-    int mb;              // M block
+    int mb;              // block of kPfRows weight rows
     int u;               // routed expert, -1 = shared
     int part;            // shared down: K part
+    int k0;              // first K step of the item in its matrix row (shared down parts)
+    int z;               // the routed expert's index (tensor coordinate); 0 for the shared expert
 };
 
-// Items: [shared M block mb, slice sl] for mb < ms, sl < ceil(T / kPfMaxN); then per
-// distinct expert u, [M block mb, slice sl] for mb < mr, sl < its slices.
+// Blocks of kPfTR tile rows in a matrix of `tr` tile rows.
+__device__ __forceinline__ int pf_blocks(int tr) { return (tr + kPfTR - 1) / kPfTR; }
 __device__ __forceinline__ int pf_shared_slices(const PrefillGemmArgs &a) { return (a.T + kPfMaxN - 1) / kPfMaxN; }
 __device__ __forceinline__ int pf_items(const PrefillGemmArgs &a) {
-    const int ms = a.kind == 0 ? a.Is / 64 : (a.H / 128) * a.sparts, mr = a.kind == 0 ? a.I / 64 : a.H / 128;
+    const int ms = a.kind == 0 ? pf_blocks(a.Ls.Ti) : pf_blocks(a.Ls.R) * a.sparts;
+    const int mr = a.kind == 0 ? pf_blocks(a.Lr.Ti) : pf_blocks(a.Lr.R);
     return ms * pf_shared_slices(a) + mr * a.uslc[a.U[0]];
 }
 __device__ __forceinline__ PfItem pf_item(const PrefillGemmArgs &a, int i) {
     PfItem it;
-    const int ms = a.kind == 0 ? a.Is / 64 : (a.H / 128) * a.sparts;  // shared (M block, K part) items
-    const int mr = a.kind == 0 ? a.I / 64 : a.H / 128;                 // routed M blocks per expert
+    const int ms = a.kind == 0 ? pf_blocks(a.Ls.Ti) : pf_blocks(a.Ls.R) * a.sparts;  // shared (block, K part) items
+    const int mr = a.kind == 0 ? pf_blocks(a.Lr.Ti) : pf_blocks(a.Lr.R);              // routed blocks per expert
     const int nss = pf_shared_slices(a);
     it.part = 0;
+    it.k0 = 0;
+    it.z = 0;
     if (i < ms * nss) {
         const int mp = i / nss, sl = i - mp * nss;
         const int mb = a.kind == 0 ? mp : mp / a.sparts;
@@ -446,13 +451,16 @@ __device__ __forceinline__ PfItem pf_item(const PrefillGemmArgs &a, int i) {
         it.b = (a.kind == 0 ? a.Bs : a.Hs) + (size_t)it.row0 * 128;
         it.b_kb = (size_t)a.T16 * 128;
         if (a.kind == 0) {
-            it.a = a.shared + (size_t)kTileBytes * (8 * mb) * a.Ls.G;
+            it.ntr = min(kPfTR, a.Ls.Ti - kPfTR * mb);
+            it.a = a.shared + (size_t)kTileBytes * (kPfTR * mb) * a.Ls.G;
             it.a_row = (size_t)kTileBytes * a.Ls.G;
             it.nkb = a.Ls.G;
         } else {
             // K part p: groups [p Gi, min((p + 1) Gi, Gis)) of the shared down rows
             const int k0 = it.part * a.Lr.Gi;
-            it.a = a.shared + a.Ls.gu_bytes + (size_t)kTileBytes * ((size_t)(8 * mb) * a.Ls.Gi + k0);
+            it.k0 = k0;
+            it.ntr = min(kPfTR, a.Ls.R - kPfTR * mb);
+            it.a = a.shared + a.Ls.gu_bytes + (size_t)kTileBytes * ((size_t)(kPfTR * mb) * a.Ls.Gi + k0);
             it.a_row = (size_t)kTileBytes * a.Ls.Gi;
             it.nkb = a.sparts > 1 ? min(a.Lr.Gi, a.Ls.Gi - k0) : a.Ls.Gi;
             it.b += (size_t)k0 * it.b_kb;
@@ -469,18 +477,21 @@ __device__ __forceinline__ PfItem pf_item(const PrefillGemmArgs &a, int i) {
         const int mb = r / ns, sl = r - mb * ns;
         it.u = u;
         it.mb = mb;
+        it.z = a.uexp[u];
         it.row0 = sl * kPfMaxN;
         it.n = min(kPfMaxN, a.ucnt[u] - it.row0);
         it.N = round16(it.n);
         it.b = (a.kind == 0 ? a.Br : a.Hr) + (size_t)(a.urow[u] + it.row0) * 128;
         it.b_kb = (size_t)a.Rmax * 128;
-        const uint8_t *blob = a.experts + (size_t)a.uexp[u] * a.stride;
+        const uint8_t *blob = a.experts + (size_t)it.z * a.stride;
         if (a.kind == 0) {
-            it.a = blob + (size_t)kTileBytes * (8 * mb) * a.Lr.G;
+            it.ntr = min(kPfTR, a.Lr.Ti - kPfTR * mb);
+            it.a = blob + (size_t)kTileBytes * (kPfTR * mb) * a.Lr.G;
             it.a_row = (size_t)kTileBytes * a.Lr.G;
             it.nkb = a.Lr.G;
         } else {
-            it.a = blob + a.Lr.gu_bytes + (size_t)kTileBytes * (8 * mb) * a.Lr.Gi;
+            it.ntr = min(kPfTR, a.Lr.R - kPfTR * mb);
+            it.a = blob + a.Lr.gu_bytes + (size_t)kTileBytes * (kPfTR * mb) * a.Lr.Gi;
             it.a_row = (size_t)kTileBytes * a.Lr.Gi;
             it.nkb = a.Lr.Gi;
         }
@@ -517,7 +528,6 @@ __device__ __forceinline__ bool pf_done(uint64_t *bar, unsigned parity) {
 }
 
 struct PfSmem {
-    uint64_t w_full[kPfWStages], w_free[kPfWStages];                 // packed-weight ring
     uint64_t q_full[kPfQStages], q_free[kPfQStages];  // operand ring
     uint64_t acc_full[2], acc_empty[2];
     uint32_t tmem;
@@ -537,22 +547,15 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill_gemm(const PrefillGem
     a.urow = pl_urow;
     a.uexp = pl_uexp;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // 1024-aligned carve-up: weight stages | operand stages | epilogue buffers
+    // 1024-aligned operand stages (per K step: token tile, dequantised weights)
     uint8_t *base = psm_raw + ((1024u - (smem_addr(psm_raw) & 1023u)) & 1023u);
-    uint8_t *wst = base;
-    uint8_t *qst = wst + (size_t)kPfWStages * kPfW;
-    float *ebuf = reinterpret_cast<float *>(qst + (size_t)kPfQStages * kPfQK * kPfQ);  // [128 cols][64 rows]
-    uint8_t *hst = reinterpret_cast<uint8_t *>(ebuf + 64 * kPfMaxN);          // [128 rows][128 B]
+    uint8_t *qst = base;
     volatile int *err = &S.err;
 
     if (tid == 0) {
-        for (int s = 0; s < kPfWStages; s++) {
-            mbar_init(&S.w_full[s], 1);
-            mbar_init(&S.w_free[s], kPfDq);
-        }
         for (int s = 0; s < kPfQStages; s++) {
-            // full: the producer's arrival with the token tile's bytes, then one arrival per
-            // thread of the dequantising group that writes the stage's A
+            // full: the token copier's arrival with the token tiles' bytes, then one
+            // arrival per dequantising thread
             mbar_init(&S.q_full[s], 1 + kPfDq * 32);
             mbar_init(&S.q_free[s], 1);
         }
@@ -592,15 +595,20 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill_gemm(const PrefillGem
     };
 
     if (warp == kPfProducer) {
-        // ---------------- token copies (one thread): per operand stage, its token tiles,
-        // issued as soon as the MMA releases the stage (the packed weights have their own
-        // warp, so nothing else stands between the release and the copy)
+        // ---------------- token copies (one thread): per operand stage, its token tiles
+        // (the MMA's A), issued as soon as the MMA releases the stage
         if (lane == 0) {
             int f = 0;
             int qlast[kPfQStages];
             for (int s = 0; s < kPfQStages; s++) qlast[s] = -1;
             for (int i = b; i < NI; i += nC) {
                 const PfItem it = pf_item(a, i);
+                // this item's weight block (first item only) and the next one's, into L2
+                if (i == b) prefetch_l2(it.a, (unsigned)(it.ntr * it.a_row));
+                if (i + nC < NI) {
+                    const PfItem nx = pf_item(a, i + nC);
+                    prefetch_l2(nx.a, (unsigned)(nx.ntr * nx.a_row));
+                }
                 for (int kb = 0; kb < it.nkb; kb += kPfQK, f++) {
                     const int q = f % kPfQStages;
                     if (f >= kPfQStages && !*err && !mbar_wait(&S.q_free[q], ((f / kPfQStages) - 1) & 1, err))
@@ -609,8 +617,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill_gemm(const PrefillGem
                     const int nq = min(kPfQK, it.nkb - kb);
                     mbar_arrive_expect_tx(&S.q_full[q], nq * it.N * 128);
                     for (int h = 0; h < nq; h++)
-                        bulk_g2s(qst + (size_t)(q * kPfQK + h) * kPfQ + kPfTileA, it.b + (size_t)(kb + h) * it.b_kb,
-                                 it.N * 128, &S.q_full[q]);
+                        bulk_g2s(qst + (size_t)(q * kPfQK + h) * kPfQ, it.b + (size_t)(kb + h) * it.b_kb, it.N * 128,
+                                 &S.q_full[q]);
                     qlast[q] = f;
                 }
             }
@@ -621,7 +629,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill_gemm(const PrefillGem
         }
         __syncwarp();
     } else if (warp == kPfMmaWarp) {
-        // ---------------- MMA issue
+        // ---------------- MMA issue: D[tokens][weight rows] += tokens x weights^T
         if (lane == 0) {
             int f = 0, n_it = 0;
             for (int i = b; i < NI; i += nC, n_it++) {
@@ -629,7 +637,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill_gemm(const PrefillGem
                 const int ab = n_it & 1;
                 if (n_it >= 2 && !*err && !mbar_wait(&S.acc_empty[ab], ((n_it >> 1) - 1) & 1, err)) fail();
                 tc_fence_after();
-                const uint32_t idesc = umma_idesc_f16(128, it.N);
+                const uint32_t idesc = umma_idesc_f16(128, 16 * it.ntr);
                 for (int kb = 0; kb < it.nkb; kb += kPfQK, f++) {
                     const int q = f % kPfQStages, nq = min(kPfQK, it.nkb - kb);
                     if (!pf_done(&S.q_full[q], (f / kPfQStages) & 1) && !mbar_wait(&S.q_full[q], (f / kPfQStages) & 1, err))
@@ -640,7 +648,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill_gemm(const PrefillGem
                         const uint32_t sb = sa + kPfTileA;
 #pragma unroll
                         for (int ks = 0; ks < 4; ks++)
-                            umma_f16(tmem + ab * 128, umma_desc(sa + 32 * ks), umma_desc(sb + 32 * ks), idesc,
+                            umma_f16(tmem + ab * kPfRows, umma_desc(sa + 32 * ks), umma_desc(sb + 32 * ks), idesc,
                                      kb + h > 0 || ks > 0);
                     }
                     umma_commit(&S.q_free[q]);
@@ -656,160 +664,141 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill_gemm(const PrefillGem
         }
         __syncwarp();
     } else if (warp < kPfProducer) {
-        // ---------------- dequantise: warp j takes tile row j of every K step
-        const int j = warp;
+        // ---------------- dequantise: warp d takes tile row d of every K step: weight rows
+        // 16 d + r and 16 d + 8 + r (gate/up: the gate and up rows of index 8 d + r, which
+        // the epilogue finds 8 columns apart in one thread; the 8 rows of a store cover
+        // every 128-byte row phase, so the swizzled stores are conflict-free).  The
+        // packed tiles come straight from global memory (the item's block is prefetched
+        // into L2 by the token copier), loaded one operand stage ahead into registers.
+        const int d = warp;
         const int r = lane >> 2, c = lane & 3;
-        const int ra = a.kind == 0 ? 8 * j + r : 16 * j + r;
-        const int rb = a.kind == 0 ? 64 + 8 * j + r : 16 * j + 8 + r;
-        const uint32_t oa0 = sw128_chunk(ra, 2 * c), oa1 = sw128_chunk(ra, 2 * c + 1);
-        const uint32_t ob0 = sw128_chunk(rb, 2 * c), ob1 = sw128_chunk(rb, 2 * c + 1);
-        int f = 0, wf = 0;
-        for (int i = b; i < NI; i += nC) {
-            const int nkb = pf_item(a, i).nkb;
-            for (int kw = 0; kw < nkb; kw += kPfKF, wf++) {
-                const int w = wf % kPfWStages, nk = min(kPfKF, nkb - kw);
-                // (the waits give up at once when another warp raised the error word)
-                if (!pf_done(&S.w_full[w], (wf / kPfWStages) & 1) && !mbar_wait(&S.w_full[w], (wf / kPfWStages) & 1, err))
-                    fail();
-                // the whole weight stage's packed tiles, before the operand stages' waits
-                uint4 qv[kPfKF];
-                uint2 e[kPfKF];
-                const uint8_t *rs = wst + (size_t)w * kPfW + j * kPfWRow;
-#pragma unroll
-                for (int h = 0; h < kPfKF; h++)
-                    if (h < nk) {
-                        qv[h] = *reinterpret_cast<const uint4 *>(rs + h * kTileBytes + 16 * lane);
-                        e[h] = *reinterpret_cast<const uint2 *>(rs + h * kTileBytes + 512 + 8 * r);
-                    }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&S.w_free[w]);  // the stage is in registers
-#pragma unroll
-                for (int st = 0; st < kPfKF / kPfQK; st++) {
-                    const int kb = kw + st * kPfQK;
-                    if (kb >= nkb) break;
-                    const int q = f % kPfQStages, nq = min(kPfQK, nkb - kb);
-                    if (f >= kPfQStages && !pf_done(&S.q_free[q], ((f / kPfQStages) - 1) & 1) &&
-                        !mbar_wait(&S.q_free[q], ((f / kPfQStages) - 1) & 1, err))
-                        fail();
-#pragma unroll
-                    for (int h = 0; h < kPfQK; h++)
-                        if (h < nq) {
-                            const int x = st * kPfQK + h;
-                            uint8_t *as = qst + (size_t)(q * kPfQK + h) * kPfQ;
-                            const __half2 sa2 = __half2half2(__ushort_as_half((unsigned short)(e[x].x & 0xFFFFu)));
-                            const __half2 ba2 = __half2half2(__ushort_as_half((unsigned short)(e[x].x >> 16)));
-                            const __half2 sb2 = __half2half2(__ushort_as_half((unsigned short)(e[x].y & 0xFFFFu)));
-                            const __half2 bb2 = __half2half2(__ushort_as_half((unsigned short)(e[x].y >> 16)));
-                            *reinterpret_cast<uint4 *>(as + oa0) = deq_word(qv[x].x, sa2, ba2);
-                            *reinterpret_cast<uint4 *>(as + oa1) = deq_word(qv[x].y, sa2, ba2);
-                            *reinterpret_cast<uint4 *>(as + ob0) = deq_word(qv[x].z, sb2, bb2);
-                            *reinterpret_cast<uint4 *>(as + ob1) = deq_word(qv[x].w, sb2, bb2);
-                        }
-                    fence_async_smem();
-                    mbar_arrive(&S.q_full[q]);  // each thread, after its own stores and fence
-                    f++;
-                }
-            }
-        }
-    } else if (warp == kPfWProd) {
-        // ---------------- packed-weight copies (one thread): per kPfKF K steps of an item,
-        // one bulk copy per tile row, issued as soon as the weight stage is released
-        if (lane == 0) {
-            int wf = 0;
-            int wlast[kPfWStages];
-            for (int s = 0; s < kPfWStages; s++) wlast[s] = -1;
-            for (int i = b; i < NI; i += nC) {
+        const int ra = 16 * d + r, rb = ra + 8;
+        const uint32_t oa0 = kPfTileA + sw128_chunk(ra, 2 * c), oa1 = kPfTileA + sw128_chunk(ra, 2 * c + 1);
+        const uint32_t ob0 = kPfTileA + sw128_chunk(rb, 2 * c), ob1 = kPfTileA + sw128_chunk(rb, 2 * c + 1);
+        // stage cursor: item i, first K step kb; the tiles of the stage in qv / e
+        struct Cur {
+            int i, kb, nkb;
+            bool active;
+            const uint8_t *row;  // this warp's tile row, K step 0
+        };
+        auto at_item = [&](int i) -> Cur {
+            Cur u{i, 0, 0, false, nullptr};
+            if (i < NI) {
                 const PfItem it = pf_item(a, i);
-                // this item's weight block (first item only) and the next one's, into L2
-                if (i == b) prefetch_l2(it.a, (unsigned)(8 * it.a_row));
-                if (i + nC < NI) {
-                    const PfItem nx = pf_item(a, i + nC);
-                    prefetch_l2(nx.a, (unsigned)(8 * nx.a_row));
-                }
-                for (int kb = 0; kb < it.nkb; kb += kPfKF, wf++) {
-                    const int w = wf % kPfWStages, nk = min(kPfKF, it.nkb - kb);
-                    if (wf >= kPfWStages && !*err && !mbar_wait(&S.w_free[w], ((wf / kPfWStages) - 1) & 1, err))
-                        fail();
-                    if (*err) continue;
-                    mbar_arrive_expect_tx(&S.w_full[w], 8 * nk * kTileBytes);
-                    uint8_t *dst = wst + (size_t)w * kPfW;
-                    for (int j = 0; j < 8; j++)
-                        bulk_g2s(dst + j * kPfWRow, it.a + j * it.a_row + (size_t)kb * kTileBytes, nk * kTileBytes,
-                                 &S.w_full[w]);
-                    wlast[w] = wf;
-                }
+                u.nkb = it.nkb;
+                u.active = d < it.ntr;
+                u.row = it.a + (size_t)d * it.a_row;
             }
-            // drain: the last copies of every stage have landed
-            volatile int never = 0;
-            for (int s = 0; s < kPfWStages; s++)
-                if (wlast[s] >= 0) mbar_wait(&S.w_full[s], (wlast[s] / kPfWStages) & 1, &never);
+            return u;
+        };
+        auto load = [&](const Cur &u, uint4 (&qv)[kPfQK], uint2 (&e)[kPfQK]) {
+            if (u.i >= NI || !u.active) return;
+#pragma unroll
+            for (int h = 0; h < kPfQK; h++)
+                if (u.kb + h < u.nkb) {
+                    const uint8_t *t = u.row + (size_t)(u.kb + h) * kTileBytes;
+                    qv[h] = __ldcs(reinterpret_cast<const uint4 *>(t) + lane);
+                    e[h] = __ldcs(reinterpret_cast<const uint2 *>(t + 512) + r);
+                }
+        };
+        Cur cur = at_item(b);
+        uint4 qv[kPfQK], nqv[kPfQK];
+        uint2 e[kPfQK], ne[kPfQK];
+        load(cur, qv, e);
+        int f = 0;
+        while (cur.i < NI) {
+            Cur nxt = cur;
+            nxt.kb += kPfQK;
+            if (nxt.kb >= nxt.nkb) nxt = at_item(cur.i + nC);
+            load(nxt, nqv, ne);
+            const int q = f % kPfQStages, nq = min(kPfQK, cur.nkb - cur.kb);
+            // (the wait gives up at once when another warp raised the error word)
+            if (f >= kPfQStages && !pf_done(&S.q_free[q], ((f / kPfQStages) - 1) & 1) &&
+                !mbar_wait(&S.q_free[q], ((f / kPfQStages) - 1) & 1, err))
+                fail();
+            if (cur.active) {
+#pragma unroll
+                for (int h = 0; h < kPfQK; h++)
+                    if (h < nq) {
+                        uint8_t *slot = qst + (size_t)(q * kPfQK + h) * kPfQ;
+                        const __half2 sa2 = __half2half2(__ushort_as_half((unsigned short)(e[h].x & 0xFFFFu)));
+                        const __half2 ba2 = __half2half2(__ushort_as_half((unsigned short)(e[h].x >> 16)));
+                        const __half2 sb2 = __half2half2(__ushort_as_half((unsigned short)(e[h].y & 0xFFFFu)));
+                        const __half2 bb2 = __half2half2(__ushort_as_half((unsigned short)(e[h].y >> 16)));
+                        *reinterpret_cast<uint4 *>(slot + oa0) = deq_word(qv[h].x, sa2, ba2);
+                        *reinterpret_cast<uint4 *>(slot + oa1) = deq_word(qv[h].y, sa2, ba2);
+                        *reinterpret_cast<uint4 *>(slot + ob0) = deq_word(qv[h].z, sb2, bb2);
+                        *reinterpret_cast<uint4 *>(slot + ob1) = deq_word(qv[h].w, sb2, bb2);
+                    }
+                fence_async_smem();
+            }
+            mbar_arrive(&S.q_full[q]);  // each thread, after its own stores and fence
+#pragma unroll
+            for (int h = 0; h < kPfQK; h++) {
+                qv[h] = nqv[h];
+                e[h] = ne[h];
+            }
+            cur = nxt;
+            f++;
         }
-        __syncwarp();
     } else {
-        // ---------------- epilogue (warps 10-17), overlapping the next item's K steps
-        const int etid = tid - kPfEpi0 * 32;
-        const int quad = warp & 3, half = (warp - kPfEpi0) >> 2;  // tensor-memory lane quarter, column half
+        // ---------------- epilogue (warps kPfEpi0..): tensor-memory lane = token slot,
+        // column = weight row; each warp takes one lane quarter and one column half,
+        // overlapping the next item's K steps
+        const int quad = warp & 3, half = (warp - kPfEpi0) >> 2;
         int n_it = 0;
         for (int i = b; i < NI; i += nC, n_it++) {
             const PfItem it = pf_item(a, i);
             const int ab = n_it & 1;
             if (!*err && !mbar_wait(&S.acc_full[ab], (n_it >> 1) & 1, err)) fail();
             tc_fence_after();
-            const uint32_t trow = tmem + ab * 128 + ((uint32_t)(32 * quad) << 16);
-            const int row = 32 * quad + lane;  // accumulator row of this thread
-            const int c_first = 16 * half;     // this warp takes every other 16-column chunk
-            if (a.kind == 0) {
-                // rows 0-63 gate, 64-127 up (intermediate index 64 mb + row % 64)
-                if (quad >= 2 && !*err)
-                    for (int c0 = c_first; c0 < it.N; c0 += 32) {
+            const uint32_t trow = tmem + ab * kPfRows + ((uint32_t)(32 * quad) << 16);
+            const int t = 32 * quad + lane;  // token slot of this thread
+            const int c_beg = (kPfRows / 2) * half, c_end = min(c_beg + kPfRows / 2, 16 * it.ntr);
+            if (!*err && 32 * quad < it.N) {
+                if (a.kind == 0) {
+                    // columns 16 j + k, 16 j + 8 + k: gate and up of intermediate index 128 mb +
+                    // 8 j + k; h in the down's operand tiles, 8 indices (one 16-byte chunk) per 16
+                    // columns, zero in the padding rows
+                    const int row = (it.u < 0 ? 0 : a.urow[it.u]) + it.row0 + t;
+                    for (int c0 = c_beg; c0 < c_end; c0 += 16) {
                         float v[16];
                         tmem_ld16(trow + c0, v);
+                        if (t < it.N) {
+                            float h[8];
 #pragma unroll
-                        for (int q = 0; q < 16; q++) ebuf[(c0 + q) * 64 + row - 64] = v[q];
-                    }
-                named_sync(1, kPfEpi * 32);
-                if (quad < 2 && !*err) {
-                    const int pos = frag_pos(row);  // operand position of column `row` of the K step
-                    for (int c0 = c_first; c0 < it.N; c0 += 32) {
-                        float v[16];
-                        tmem_ld16(trow + c0, v);
-#pragma unroll
-                        for (int q = 0; q < 16; q++) {
-                            const int jt = c0 + q;
-                            const float h = jt < it.n ? gelu_tanh(v[q]) * ebuf[jt * 64 + row] : 0.f;
-                            *reinterpret_cast<__half *>(hst + (size_t)jt * 128 + (((pos >> 3) ^ (jt & 7)) << 4) +
-                                                        (pos & 7) * 2) = __float2half_rn(h);
+                            for (int k = 0; k < 8; k++) h[k] = t < it.n ? gelu_tanh(v[k]) * v[k + 8] : 0.f;
+                            const __half2 w0 = __floats2half2_rn(h[0], h[4]), w1 = __floats2half2_rn(h[1], h[5]);
+                            const __half2 w2 = __floats2half2_rn(h[2], h[6]), w3 = __floats2half2_rn(h[3], h[7]);
+                            const int idx = (kPfRows / 2) * it.mb + c0 / 2, kbh = idx / kGroup, ch = (idx % kGroup) / 8;
+                            uint8_t *dst = it.u < 0 ? a.Hs + ((size_t)kbh * a.T16 + row) * 128
+                                                    : a.Hr + ((size_t)kbh * a.Rmax + row) * 128;
+                            *reinterpret_cast<uint4 *>(dst + ((ch ^ (row & 7)) << 4)) =
+                                make_uint4(*reinterpret_cast<const uint32_t *>(&w0), *reinterpret_cast<const uint32_t *>(&w1),
+                                           *reinterpret_cast<const uint32_t *>(&w2), *reinterpret_cast<const uint32_t *>(&w3));
                         }
                     }
-                }
-                named_sync(1, kPfEpi * 32);
-                // the item's h rows: one K step (kb = mb) of the down operand
-                uint8_t *dst = (it.u < 0 ? a.Hs + ((size_t)it.mb * a.T16 + it.row0) * 128
-                                         : a.Hr + ((size_t)it.mb * a.Rmax + a.urow[it.u] + it.row0) * 128);
-                if (!*err)
-                    for (int v = etid; v < it.N * 8; v += kPfEpi * 32)
-                        reinterpret_cast<uint4 *>(dst)[v] = reinterpret_cast<const uint4 *>(hst)[v];
-            } else if (!*err) {
-                // output row 128 mb + row, token column j
-                const int n = 128 * it.mb + row;
-                for (int c0 = c_first; c0 < it.N; c0 += 32) {
-                    float v[16];
-                    tmem_ld16(trow + c0, v);
+                } else {
+                    // columns: output rows kPfRows mb + c of the token's fp32 row
+                    float *yrow = nullptr;
+                    if (t < it.n)
+                        yrow = it.u < 0 ? (it.part ? a.Ys_more + (size_t)(it.part - 1) * a.T16 * a.H : a.Ys) +
+                                              (size_t)(it.row0 + t) * a.H
+                                        : a.Yr + (size_t)a.rowpair[a.urow[it.u] + it.row0 + t] * a.H;
+                    for (int c0 = c_beg; c0 < c_end; c0 += 16) {
+                        float v[16];
+                        tmem_ld16(trow + c0, v);
+                        if (yrow) {
+                            float4 *o = reinterpret_cast<float4 *>(yrow + kPfRows * it.mb + c0);
 #pragma unroll
-                    for (int q = 0; q < 16; q++) {
-                        const int jt = c0 + q;
-                        if (jt < it.n) {
-                            if (it.u < 0)
-                                (it.part ? a.Ys_more + (size_t)(it.part - 1) * a.T16 * a.H : a.Ys)
-                                    [(size_t)(it.row0 + jt) * a.H + n] = v[q];
-                            else
-                                a.Yr[(size_t)a.rowpair[a.urow[it.u] + it.row0 + jt] * a.H + n] = v[q];
+                            for (int k = 0; k < 4; k++) o[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
                         }
                     }
                 }
             }
+            // each warp releases the accumulator once its own reads are done
             tc_fence_before();
-            named_sync(1, kPfEpi * 32);
+            __syncwarp();
             if (lane == 0) mbar_arrive(&S.acc_empty[ab]);
         }
     }
@@ -850,7 +839,7 @@ inline cudaError_t pf_launch(void (*fn)(KArgs...), dim3 grid, dim3 block, size_t
 }
 
 inline size_t prefill_gemm_smem() {
-    return 1024 + (size_t)kPfWStages * kPfW + (size_t)kPfQStages * kPfQK * kPfQ + 64 * kPfMaxN * 4 + kPfMaxN * 128;
+    return 1024 + (size_t)kPfQStages * kPfQK * kPfQ;
 }
 
 // ------------------------------------------------------------------ combine
