@@ -499,14 +499,22 @@ __device__ __forceinline__ PfItem pf_item(const PrefillGemmArgs &a, int i) {
     return it;
 }
 
+// The 8 codes of a packed word (nibble k of each 16-bit half: one fp16 pair per k)
+// as w = s*q + b in fp16.  A code is read in place as an exact fp16 integer: a
+// nibble at bits 0-3 of a half under the exponent of 1024 is 1024 + q, one at bits
+// 4-7 under the exponent of 64 is 64 + q (its bits are the mantissa's 1/16 places);
+// one shift by 8 brings nibbles 2 and 3 to those places.  The subtraction is exact,
+// the FMA rounds once.
 __device__ __forceinline__ uint4 deq_word(uint32_t w, __half2 s2, __half2 b2) {
-    const uint32_t magic = 0x64006400u;  // fp16 1024 in both halves
     const __half2 k1024 = __halves2half2(__ushort_as_half((unsigned short)0x6400), __ushort_as_half((unsigned short)0x6400));
+    const __half2 k64 = __halves2half2(__ushort_as_half((unsigned short)0x5400), __ushort_as_half((unsigned short)0x5400));
+    const uint32_t w8 = w >> 8;
+    const uint32_t v[4] = {(w & 0x000F000Fu) | 0x64006400u, (w & 0x00F000F0u) | 0x54005400u,
+                           (w8 & 0x000F000Fu) | 0x64006400u, (w8 & 0x00F000F0u) | 0x54005400u};
     uint32_t r[4];
 #pragma unroll
     for (int k = 0; k < 4; k++) {
-        const uint32_t v = ((w >> (4 * k)) & 0x000F000Fu) | magic;
-        __half2 q = __hsub2(*reinterpret_cast<const __half2 *>(&v), k1024);  // exact codes
+        const __half2 q = __hsub2(*reinterpret_cast<const __half2 *>(&v[k]), (k & 1) ? k64 : k1024);  // exact codes
         __half2 d = __hfma2(q, s2, b2);
         r[k] = *reinterpret_cast<uint32_t *>(&d);
     }
