@@ -419,8 +419,6 @@ struct PfItem {
     int mb;              // block of kPfRows weight rows
     int u;               // routed expert, -1 = shared
     int part;            // shared down: K part
-    int k0;              // first K step of the item in its matrix row (shared down parts)
-    int z;               // the routed expert's index (tensor coordinate); 0 for the shared expert
 };
 
 // Blocks of kPfTR tile rows in a matrix of `tr` tile rows.
@@ -437,8 +435,6 @@ __device__ __forceinline__ PfItem pf_item(const PrefillGemmArgs &a, int i) {
     const int mr = a.kind == 0 ? pf_blocks(a.Lr.Ti) : pf_blocks(a.Lr.R);              // routed blocks per expert
     const int nss = pf_shared_slices(a);
     it.part = 0;
-    it.k0 = 0;
-    it.z = 0;
     if (i < ms * nss) {
         const int mp = i / nss, sl = i - mp * nss;
         const int mb = a.kind == 0 ? mp : mp / a.sparts;
@@ -458,7 +454,6 @@ __device__ __forceinline__ PfItem pf_item(const PrefillGemmArgs &a, int i) {
         } else {
             // K part p: groups [p Gi, min((p + 1) Gi, Gis)) of the shared down rows
             const int k0 = it.part * a.Lr.Gi;
-            it.k0 = k0;
             it.ntr = min(kPfTR, a.Ls.R - kPfTR * mb);
             it.a = a.shared + a.Ls.gu_bytes + (size_t)kTileBytes * ((size_t)(kPfTR * mb) * a.Ls.Gi + k0);
             it.a_row = (size_t)kTileBytes * a.Ls.Gi;
@@ -477,13 +472,12 @@ __device__ __forceinline__ PfItem pf_item(const PrefillGemmArgs &a, int i) {
         const int mb = r / ns, sl = r - mb * ns;
         it.u = u;
         it.mb = mb;
-        it.z = a.uexp[u];
         it.row0 = sl * kPfMaxN;
         it.n = min(kPfMaxN, a.ucnt[u] - it.row0);
         it.N = round16(it.n);
         it.b = (a.kind == 0 ? a.Br : a.Hr) + (size_t)(a.urow[u] + it.row0) * 128;
         it.b_kb = (size_t)a.Rmax * 128;
-        const uint8_t *blob = a.experts + (size_t)it.z * a.stride;
+        const uint8_t *blob = a.experts + (size_t)a.uexp[u] * a.stride;
         if (a.kind == 0) {
             it.ntr = min(kPfTR, a.Lr.Ti - kPfTR * mb);
             it.a = blob + (size_t)kTileBytes * (kPfTR * mb) * a.Lr.G;
