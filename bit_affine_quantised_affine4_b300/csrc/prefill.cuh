@@ -704,11 +704,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill_gemm(const PrefillGem
                 }
         };
         Cur cur = at_item(b);
-        uint4 qv[kPfQK], nqv[kPfQK];
-        uint2 e[kPfQK], ne[kPfQK];
-        load(cur, qv, e);
         int f = 0;
-        while (cur.i < NI) {
+        // one operand stage: load the next stage's tiles into (nqv, ne), write the
+        // current ones (qv, e); the loop below alternates the two register sets
+        auto step = [&](uint4 (&qv)[kPfQK], uint2 (&e)[kPfQK], uint4 (&nqv)[kPfQK], uint2 (&ne)[kPfQK]) {
             Cur nxt = cur;
             nxt.kb += kPfQK;
             if (nxt.kb >= nxt.nkb) nxt = at_item(cur.i + nC);
@@ -735,13 +734,16 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill_gemm(const PrefillGem
                 fence_async_smem();
             }
             mbar_arrive(&S.q_full[q]);  // each thread, after its own stores and fence
-#pragma unroll
-            for (int h = 0; h < kPfQK; h++) {
-                qv[h] = nqv[h];
-                e[h] = ne[h];
-            }
             cur = nxt;
             f++;
+        };
+        uint4 qa[kPfQK], qb[kPfQK];
+        uint2 ea[kPfQK], eb[kPfQK];
+        load(cur, qa, ea);
+        while (cur.i < NI) {
+            step(qa, ea, qb, eb);
+            if (cur.i >= NI) break;
+            step(qb, eb, qa, ea);
         }
     } else {
         // ---------------- epilogue (warps kPfEpi0..): tensor-memory lane = token slot,
