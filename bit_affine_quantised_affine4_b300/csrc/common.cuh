@@ -91,7 +91,8 @@ struct Ws {
     int *ih;           // [Tmax][topk]    and of its routing outputs
     float *gh;         // [Tmax][topk]
     // prefill chunk (grouped GEMMs)
-    int *plan;         // U, rows used, uexp[256], urow[256], ucnt[256], rowtok[Rmax], rowpair[Rmax]
+    int *plan;         // U, rows used, uexp[256], urow[256], ucnt[256], rowtok[Rmax], rowpair[Rmax],
+                       // uslc[257], dep[258]
     uint8_t *Br, *Bs;  // token operand tiles: [H/64][Rmax][128 B], [H/64][T16][128 B]
     uint8_t *Hr, *Hs;  // h operand tiles:     [I/64][Rmax][128 B], [Is/64][T16][128 B]
     float *Yr, *Ys;    // down rows: [Tmax*topk][H], [T16][H]
@@ -139,7 +140,7 @@ inline WsLayout ws_layout(const moe_layer_t &l, int Tmax) {
     W.gh = off;     off = up256(off + sizeof(float) * size_t(Tmax) * l.topk);
     W.decode_total = off;
     const int Rmax = prefill_rows(l, Tmax), T16 = (Tmax + 15) & ~15;
-    W.plan = off;   off = up256(off + sizeof(int) * (2 + 3 * MOE_MAX_EXPERTS + 2 * size_t(Rmax) + MOE_MAX_EXPERTS + 1));
+    W.plan = off;   off = up256(off + sizeof(int) * (2 + 3 * MOE_MAX_EXPERTS + 2 * size_t(Rmax) + 2 * MOE_MAX_EXPERTS + 3));
     W.Br = off;     off = up256(off + size_t(l.H / kGroup) * Rmax * 128);
     W.Bs = off;     off = up256(off + size_t(l.H / kGroup) * T16 * 128);
     W.Hr = off;     off = up256(off + size_t(l.I / kGroup) * Rmax * 128);

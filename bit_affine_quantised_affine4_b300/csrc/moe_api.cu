@@ -424,6 +424,7 @@ int run_layer_chunk(const moe_layer_t *l, const float *x, int T, int flags, floa
     plan.rowtok = plan.ucnt + MOE_MAX_EXPERTS;
     plan.rowpair = plan.rowtok + Rmax;
     plan.uslc = plan.rowpair + Rmax;
+    plan.dep = reinterpret_cast<unsigned *>(plan.uslc + MOE_MAX_EXPERTS + 1);
     if (pf_launch(k_prefill_plan, dim3(1), dim3(kPlanThreads), 0, st, (const int *)ws.idx, T, l->E, l->topk, Rmax, plan) !=
         cudaSuccess)
         return cuda_status();
@@ -447,12 +448,11 @@ int run_layer_chunk(const moe_layer_t *l, const float *x, int T, int flags, floa
     g.Ys_more = reinterpret_cast<float *>(ws.Br);
     g.err = &ws.ctrl[kErr];
     const int sparts = g.sparts;
-    for (int kind = 0; kind < 2; kind++) {
-        g.kind = kind;
-        g.sparts = kind == 0 ? 1 : sparts;  // (the gate/up GEMM has no K parts)
-        if (pf_launch(k_prefill_gemm, dim3(sms), dim3(kPfThreads), prefill_gemm_smem(), st, g) != cudaSuccess)
-            return cuda_status();
-    }
+    g.dep = plan.dep;
+    // both GEMMs in one launch of one CTA per SM (all resident: the down items wait on
+    // the gate/up items' counters)
+    if (pf_launch(k_prefill_gemm, dim3(sms), dim3(kPfThreads), prefill_gemm_smem(), st, g) != cudaSuccess)
+        return cuda_status();
     const long long cthreads = (long long)T * (l->H / 4);
     if (pf_launch(k_prefill_combine, dim3((unsigned)((cthreads + 255) / 256)), dim3(256), 0, st, x, T, l->H,
                   l->topk, flags, (const float *)ws.gate, (const float *)ws.Yr, (const float *)ws.Ys, sparts,

@@ -13,12 +13,16 @@
 //                     (token, choice) pair.
 //   gather   (grid)   tokens -> fp16 operand tiles, per expert segment (zero rows
 //                     pad each segment), plus all tokens for the shared expert.
-//   gemm 0   (grid)   gate/up: per (expert, 128 gate + 128 up rows) item,
-//                     D[tokens x 256] = X x W^T over K = H on the tensor cores,
-//                     then h = gelu_tanh(gate) * up written as the down's fp16
-//                     operand.
-//   gemm 1   (grid)   down: per (expert, 256 output rows) item, D = h x Wd^T over
-//                     K = I (Is for the shared expert), fp32 rows out.
+//   gemm     (1/SM)   both grouped GEMMs in one launch, one CTA per SM:
+//                     gate/up items (expert, 128 gate + 128 up rows): D[tokens x
+//                     256] = X x W^T over K = H on the tensor cores, then h =
+//                     gelu_tanh(gate) * up written as the down's fp16 operand;
+//                     then down items (expert, 256 output rows): D = h x Wd^T
+//                     over K = I (Is for the shared expert), fp32 rows out.  A
+//                     down item starts once the gate/up items it reads h from
+//                     have counted themselves done (bounded wait), so the CTAs
+//                     that finish their gate/up share early run down work
+//                     instead of idling; every CTA must be resident at once.
 //   combine  (grid)   y_t = sum_k gate_tk * routed_(t,k) + shared_t (+ x_t), in a
 //                     fixed order.
 //
@@ -69,6 +73,8 @@ constexpr int kPfQ = kPfTileA + kPfTileB;    // one K step of an operand stage
 constexpr int kPfTmemCols = 2 * kPfRows;     // two fp32 accumulators of 256 columns
 
 // Plan written by k_prefill_plan (ints in the workspace).
+constexpr int kPfDepShared = MOE_MAX_EXPERTS, kPfDepAll = MOE_MAX_EXPERTS + 1, kPfDeps = MOE_MAX_EXPERTS + 2;
+
 struct PfPlan {
     int *U;        // [1] distinct experts, [1] rows used
     int *uexp;     // [MOE_MAX_EXPERTS]
@@ -78,6 +84,8 @@ struct PfPlan {
     int *rowpair;  // [Rmax] pair t * topk + k of each row
     int *uslc;     // [MOE_MAX_EXPERTS + 1] first kPfMaxN-token slice of each expert (prefix of
                    // ceil(ucnt / kPfMaxN)); uslc[U] = all slices
+    unsigned *dep; // [kPfDeps] finished gate/up epilogue warps: per distinct expert u, then the
+                   // shared expert's (kPfDepShared) and all items' (kPfDepAll); zeroed by the plan
 };
 
 __device__ __forceinline__ int round16(int n) { return (n + 15) & ~15; }
@@ -252,6 +260,8 @@ __global__ void __launch_bounds__(kPlanThreads) k_prefill_plan(const int *__rest
     for (int i = tid; i < MOE_MAX_EXPERTS * 4; i += blockDim.x) (&mask[0][0])[i] = 0u;
     pdl_wait();
     pdl_launch_dependents();
+    // (the previous chunk's GEMM, which read the counters, has finished)
+    for (int i = tid; i < kPfDeps; i += blockDim.x) p.dep[i] = 0u;
     __syncthreads();
     const int P2 = T * topk;
     for (int q = tid; q < P2; q += blockDim.x) {
@@ -387,7 +397,6 @@ __global__ void __launch_bounds__(256) k_prefill_gather(const float *__restrict_
 
 // ------------------------------------------------------------------ grouped GEMM
 struct PrefillGemmArgs {
-    int kind;  // 0: gate/up + GeGLU, 1: down
     int H, I, Is, T, T16, Rmax;
     const int *U;  // [0] distinct experts
     const int *uexp, *urow, *ucnt, *rowpair, *uslc;
@@ -400,6 +409,7 @@ struct PrefillGemmArgs {
     float *Yr, *Ys;          // kind 1 output: fp32 rows [pair][H], [t][H]
     int sparts;              // kind 1: the shared down matrix in sparts K parts of at most I/64 groups
     float *Ys_more;          // kind 1: parts 1.. of the shared rows, [sparts - 1][T16][H]
+    unsigned *dep;           // the plan's gate/up completion counters
     unsigned *err;
 };
 
@@ -419,34 +429,36 @@ struct PfItem {
     int mb;              // block of kPfRows weight rows
     int u;               // routed expert, -1 = shared
     int part;            // shared down: K part
+    int kind;            // 0: gate/up + GeGLU, 1: down
 };
 
 // Blocks of kPfTR tile rows in a matrix of `tr` tile rows.
 __device__ __forceinline__ int pf_blocks(int tr) { return (tr + kPfTR - 1) / kPfTR; }
 __device__ __forceinline__ int pf_shared_slices(const PrefillGemmArgs &a) { return (a.T + kPfMaxN - 1) / kPfMaxN; }
-__device__ __forceinline__ int pf_items(const PrefillGemmArgs &a) {
-    const int ms = a.kind == 0 ? pf_blocks(a.Ls.Ti) : pf_blocks(a.Ls.R) * a.sparts;
-    const int mr = a.kind == 0 ? pf_blocks(a.Lr.Ti) : pf_blocks(a.Lr.R);
+__device__ __forceinline__ int pf_items(const PrefillGemmArgs &a, int kind) {
+    const int ms = kind == 0 ? pf_blocks(a.Ls.Ti) : pf_blocks(a.Ls.R) * a.sparts;
+    const int mr = kind == 0 ? pf_blocks(a.Lr.Ti) : pf_blocks(a.Lr.R);
     return ms * pf_shared_slices(a) + mr * a.uslc[a.U[0]];
 }
-__device__ __forceinline__ PfItem pf_item(const PrefillGemmArgs &a, int i) {
+__device__ __forceinline__ PfItem pf_item(const PrefillGemmArgs &a, int kind, int i) {
     PfItem it;
-    const int ms = a.kind == 0 ? pf_blocks(a.Ls.Ti) : pf_blocks(a.Ls.R) * a.sparts;  // shared (block, K part) items
-    const int mr = a.kind == 0 ? pf_blocks(a.Lr.Ti) : pf_blocks(a.Lr.R);              // routed blocks per expert
+    it.kind = kind;
+    const int ms = kind == 0 ? pf_blocks(a.Ls.Ti) : pf_blocks(a.Ls.R) * a.sparts;  // shared (block, K part) items
+    const int mr = kind == 0 ? pf_blocks(a.Lr.Ti) : pf_blocks(a.Lr.R);              // routed blocks per expert
     const int nss = pf_shared_slices(a);
     it.part = 0;
     if (i < ms * nss) {
         const int mp = i / nss, sl = i - mp * nss;
-        const int mb = a.kind == 0 ? mp : mp / a.sparts;
+        const int mb = kind == 0 ? mp : mp / a.sparts;
         it.u = -1;
         it.mb = mb;
-        it.part = a.kind == 0 ? 0 : mp - mb * a.sparts;
+        it.part = kind == 0 ? 0 : mp - mb * a.sparts;
         it.row0 = sl * kPfMaxN;
         it.n = min(kPfMaxN, a.T - it.row0);
         it.N = round16(it.n);
-        it.b = (a.kind == 0 ? a.Bs : a.Hs) + (size_t)it.row0 * 128;
+        it.b = (kind == 0 ? a.Bs : a.Hs) + (size_t)it.row0 * 128;
         it.b_kb = (size_t)a.T16 * 128;
-        if (a.kind == 0) {
+        if (kind == 0) {
             it.ntr = min(kPfTR, a.Ls.Ti - kPfTR * mb);
             it.a = a.shared + (size_t)kTileBytes * (kPfTR * mb) * a.Ls.G;
             it.a_row = (size_t)kTileBytes * a.Ls.G;
@@ -475,10 +487,10 @@ __device__ __forceinline__ PfItem pf_item(const PrefillGemmArgs &a, int i) {
         it.row0 = sl * kPfMaxN;
         it.n = min(kPfMaxN, a.ucnt[u] - it.row0);
         it.N = round16(it.n);
-        it.b = (a.kind == 0 ? a.Br : a.Hr) + (size_t)(a.urow[u] + it.row0) * 128;
+        it.b = (kind == 0 ? a.Br : a.Hr) + (size_t)(a.urow[u] + it.row0) * 128;
         it.b_kb = (size_t)a.Rmax * 128;
         const uint8_t *blob = a.experts + (size_t)a.uexp[u] * a.stride;
-        if (a.kind == 0) {
+        if (kind == 0) {
             it.ntr = min(kPfTR, a.Lr.Ti - kPfTR * mb);
             it.a = blob + (size_t)kTileBytes * (kPfTR * mb) * a.Lr.G;
             it.a_row = (size_t)kTileBytes * a.Lr.G;
@@ -589,7 +601,17 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill_gemm(const PrefillGem
     tc_fence_after();
     const uint32_t tmem = S.tmem;
 
-    const int NI = pf_items(a);
+    // one launch for both GEMMs: the gate/up items, then the down items; a down
+    // item's token copier waits until the gate/up items it reads h from are done
+    const int NI0 = pf_items(a, 0), NI = NI0 + pf_items(a, 1);
+    // (the down items run routed first: the shared expert's K parts 1.. write into the
+    // routed token tiles' area, so they wait for every gate/up item and go last)
+    const int NS1 = pf_blocks(a.Ls.R) * a.sparts * pf_shared_slices(a), NR1 = NI - NI0 - NS1;
+    auto item = [&](int i) -> PfItem {
+        if (i < NI0) return pf_item(a, 0, i);
+        const int j = i - NI0;
+        return pf_item(a, 1, j < NR1 ? j + NS1 : j - NR1);
+    };
     const int b = blockIdx.x, nC = gridDim.x;
     auto fail = [&]() {
         *err = 1;
@@ -604,12 +626,24 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill_gemm(const PrefillGem
             int qlast[kPfQStages];
             for (int s = 0; s < kPfQStages; s++) qlast[s] = -1;
             for (int i = b; i < NI; i += nC) {
-                const PfItem it = pf_item(a, i);
+                const PfItem it = item(i);
                 // this item's weight block (first item only) and the next one's, into L2
                 if (i == b) prefetch_l2(it.a, (unsigned)(it.ntr * it.a_row));
                 if (i + nC < NI) {
-                    const PfItem nx = pf_item(a, i + nC);
+                    const PfItem nx = item(i + nC);
                     prefetch_l2(nx.a, (unsigned)(nx.ntr * nx.a_row));
+                }
+                if (it.kind == 1 && !*err) {
+                    // every epilogue warp of the gate/up items this item reads h from has
+                    // stored it: the expert's, the shared expert's, or (K parts 1.., which
+                    // write into the routed token tiles) all of them
+                    const int mr0 = pf_blocks(a.Lr.Ti), ms0 = pf_blocks(a.Ls.Ti);
+                    const int d = it.u >= 0 ? it.u : it.part == 0 ? kPfDepShared : kPfDepAll;
+                    const unsigned want =
+                        (unsigned)kPfEpi * (it.u >= 0 ? mr0 * (a.uslc[it.u + 1] - a.uslc[it.u])
+                                            : it.part == 0 ? ms0 * pf_shared_slices(a) : NI0);
+                    if (!spin_geq(a.dep + d, want, a.err)) fail();
+                    fence_async_global();  // the h stores (generic proxy) before the bulk copies
                 }
                 for (int kb = 0; kb < it.nkb; kb += kPfQK, f++) {
                     const int q = f % kPfQStages;
@@ -635,7 +669,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill_gemm(const PrefillGem
         if (lane == 0) {
             int f = 0, n_it = 0;
             for (int i = b; i < NI; i += nC, n_it++) {
-                const PfItem it = pf_item(a, i);
+                const PfItem it = item(i);
                 const int ab = n_it & 1;
                 if (n_it >= 2 && !*err && !mbar_wait(&S.acc_empty[ab], ((n_it >> 1) - 1) & 1, err)) fail();
                 tc_fence_after();
@@ -686,7 +720,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill_gemm(const PrefillGem
         auto at_item = [&](int i) -> Cur {
             Cur u{i, 0, 0, false, nullptr};
             if (i < NI) {
-                const PfItem it = pf_item(a, i);
+                const PfItem it = item(i);
                 u.nkb = it.nkb;
                 u.active = d < it.ntr;
                 u.row = it.a + (size_t)d * it.a_row;
@@ -752,7 +786,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill_gemm(const PrefillGem
         const int quad = warp & 3, half = (warp - kPfEpi0) >> 2;
         int n_it = 0;
         for (int i = b; i < NI; i += nC, n_it++) {
-            const PfItem it = pf_item(a, i);
+            const PfItem it = item(i);
             const int ab = n_it & 1;
             if (!*err && !mbar_wait(&S.acc_full[ab], (n_it >> 1) & 1, err)) fail();
             tc_fence_after();
@@ -760,7 +794,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill_gemm(const PrefillGem
             const int t = 32 * quad + lane;  // token slot of this thread
             const int c_beg = (kPfRows / 2) * half, c_end = min(c_beg + kPfRows / 2, 16 * it.ntr);
             if (!*err && 32 * quad < it.N) {
-                if (a.kind == 0) {
+                if (it.kind == 0) {
                     // columns 16 j + k, 16 j + 8 + k: gate and up of intermediate index 128 mb +
                     // 8 j + k; h in the down's operand tiles, 8 indices (one 16-byte chunk) per 16
                     // columns, zero in the padding rows
@@ -802,8 +836,19 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_prefill_gemm(const PrefillGem
             }
             // each warp releases the accumulator once its own reads are done
             tc_fence_before();
+            if (it.kind == 0) {
+                // this warp's h stores, visible to the down items' bulk copies on any SM
+                fence_async_global();
+                __threadfence();
+            }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&S.acc_empty[ab]);
+            if (lane == 0) {
+                mbar_arrive(&S.acc_empty[ab]);
+                if (it.kind == 0) {
+                    atomicAdd(a.dep + (it.u < 0 ? kPfDepShared : it.u), 1u);
+                    atomicAdd(a.dep + kPfDepAll, 1u);
+                }
+            }
         }
     }
     tc_fence_before();
