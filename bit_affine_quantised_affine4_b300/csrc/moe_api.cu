@@ -360,8 +360,8 @@ int run_decode(const moe_layer_t *l, const float *x, int T, int flags, float *y,
     return decode_launch(plan, kModeShared | kModeRouted, stream);
 }
 
-// Prefill chunk: router, plan, gather, the two grouped GEMMs on the tensor
-// cores, combine (prefill.cuh).
+// Prefill chunk: router, plan, gather, both grouped GEMMs on the tensor cores in
+// one launch, combine (prefill.cuh).
 int run_layer_chunk(const moe_layer_t *l, const float *x, int T, int flags, float *y,
                     int32_t *idx_out, float *gate_out, void *d_ws, size_t ws_bytes, void *stream) {
     Ws ws;
