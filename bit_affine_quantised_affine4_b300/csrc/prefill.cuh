@@ -413,10 +413,11 @@ struct PrefillGemmArgs {
     unsigned *err;
 };
 
-// Item i of the launch: shared items first, then the routed experts in order.  An
-// item is one block of kPfRows weight rows (gate/up: 128 intermediate indices, gate
-// and up rows interleaved; down: 256 output rows) times one slice of <= kPfMaxN
-// tokens; the last block of a matrix may hold half as many rows.
+// Item i of one GEMM (kind): shared items first, then the routed experts in order.
+// An item is one block of kPfRows weight rows (gate/up: the gate and up rows of 128
+// intermediate indices, each tile row's 8 gate rows then its 8 up rows; down: 256
+// output rows) times one slice of <= kPfMaxN tokens; the last block of a matrix may
+// hold half as many rows.  (The launch runs the down items routed first.)
 struct PfItem {
     const uint8_t *a;    // first tile (K step 0) of the item's first tile row
     size_t a_row;        // bytes between tile rows
