@@ -304,6 +304,21 @@ def test_prefill_ragged_router_tiles(moe):
     _layer_check(moe, s, gl, ol, 77, 703, prefill=True)
 
 
+@pytest.mark.parametrize("shape", ["tiny", "full"])
+def test_degenerate_routing(moe, shape):
+    # every token picks the same top-k experts (a router bias of 10 on experts
+    # 0..topk-1, far above the spread of the router's dot products): each routed
+    # weight block is one item of all 128 tokens, the largest token tiles of the
+    # chunk, and each down item reads h from a single expert's gate/up items
+    s = synth.TINY if shape == "tiny" else synth.FULL
+    bias = np.zeros(s.E, dtype=np.float32)
+    bias[:s.topk] = 10.0
+    gl, ol = gpu_layer(s, seed=7, bias=bias), OracleLayer(s, seed=7, bias=bias)
+    _layer_check(moe, s, gl, ol, 128, 704, prefill=True)
+    # and a 16-token decode step whose tokens all share their experts
+    _layer_check(moe, s, gl, ol, 16, 705)
+
+
 def test_rejects_bad_calls(moe, tiny):
     s, gl, ol = tiny
     layer = gl.view()
