@@ -212,8 +212,9 @@ __global__ void __launch_bounds__(kRtTopkWarps * 32) k_prefill_topk(const RouteT
     float acc[NV];
 #pragma unroll
     for (int i = 0; i < NV; i++) acc[i] = 0.f;
-    // the loads of four slices are issued before their sums (added in slice order)
-    constexpr int kQ = 4;
+    // the loads of eleven slices (half of a 2816-wide row's) are issued before their
+    // sums (added in slice order)
+    constexpr int kQ = 11;
     int q = 0;
     for (; q + kQ <= KS; q += kQ) {
         float v[kQ][NV];
