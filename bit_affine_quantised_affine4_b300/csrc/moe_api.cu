@@ -4,6 +4,7 @@
 
 #include <cstdio>
 #include <cstring>
+#include <algorithm>
 #include <atomic>
 #include <chrono>
 #include <mutex>
@@ -428,8 +429,10 @@ int run_layer_chunk(const moe_layer_t *l, const float *x, int T, int flags, floa
     if (pf_launch(k_prefill_plan, dim3(1), dim3(kPlanThreads), 0, st, (const int *)ws.idx, T, l->E, l->topk, Rmax, plan) !=
         cudaSuccess)
         return cuda_status();
+    // (a grid-stride loop over the rows the plan used: 8 CTAs of 256 per SM)
     const long long gthreads = (long long)(Rmax + T16) * (l->H / kGroup) * 8;
-    if (pf_launch(k_prefill_gather, dim3((unsigned)((gthreads + 255) / 256)), dim3(256), 0, st, xin, T, l->H, Rmax,
+    const unsigned gblocks = (unsigned)std::min<long long>((gthreads + 255) / 256, 8LL * sms);
+    if (pf_launch(k_prefill_gather, dim3(gblocks), dim3(256), 0, st, xin, T, l->H, Rmax,
                   T16, (const int *)plan.rowtok, (const int *)plan.U, ws.Br, ws.Bs) != cudaSuccess)
         return cuda_status();
     PrefillGemmArgs g;

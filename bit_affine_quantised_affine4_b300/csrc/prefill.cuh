@@ -357,43 +357,46 @@ __global__ void __launch_bounds__(kPlanThreads) k_prefill_plan(const int *__rest
 
 // ------------------------------------------------------------------ gather
 // One thread per (row, K group, 16-byte chunk): 8 fp16 values of the token in
-// operand order.  Rows [0, Rmax) are the experts' segments (per rowtok), rows
-// [Rmax, Rmax + T16) all tokens for the shared expert.
+// operand order, over the rows the plan used (the experts' segments, per rowtok)
+// and then the T16 rows of all tokens for the shared expert; a grid-stride loop, so
+// the grid need not be sized for the most rows a chunk could use.
 __global__ void __launch_bounds__(256) k_prefill_gather(const float *__restrict__ x, int T, int H, int Rmax,
                                                         int T16, const int *__restrict__ rowtok,
                                                         const int *__restrict__ used, uint8_t *Br, uint8_t *Bs) {
     const int G = H / kGroup;
-    const long long n = (long long)(Rmax + T16) * G * 8;
-    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     pdl_wait();
     pdl_launch_dependents();
-    if (i >= n) return;
-    const int ch = (int)(i & 7);
-    const long long rk = i >> 3;
-    const int kb = (int)(rk % G);
-    const int row = (int)(rk / G);
-    int t;
-    uint8_t *dst;
-    if (row < Rmax) {
-        if (row >= used[1]) return;
-        t = rowtok[row];
-        dst = Br + ((size_t)kb * Rmax + row) * 128 + ((ch ^ (row & 7)) << 4);
-    } else {
-        const int r = row - Rmax;
-        t = r < T ? r : -1;
-        dst = Bs + ((size_t)kb * T16 + r) * 128 + ((ch ^ (r & 7)) << 4);
+    const long long per_row = (long long)G * 8;
+    const long long n_routed = (long long)__ldcg(used + 1) * per_row, n = n_routed + (long long)T16 * per_row;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (long long)gridDim.x * blockDim.x) {
+        const bool routed = i < n_routed;
+        const long long li = routed ? i : i - n_routed;
+        const int ch = (int)(li & 7);
+        const long long rk = li >> 3;
+        const int kb = (int)(rk % G);
+        const int row = (int)(rk / G);
+        int t;
+        uint8_t *dst;
+        if (routed) {
+            t = __ldcg(rowtok + row);
+            dst = Br + ((size_t)kb * Rmax + row) * 128 + ((ch ^ (row & 7)) << 4);
+        } else {
+            t = row < T ? row : -1;
+            dst = Bs + ((size_t)kb * T16 + row) * 128 + ((ch ^ (row & 7)) << 4);
+        }
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (t >= 0) {
+            // chunk ch holds columns 8ch + (0, 4, 1, 5, 2, 6, 3, 7) of the group
+            const float4 *src = reinterpret_cast<const float4 *>(x + (size_t)t * H + kb * kGroup + 8 * ch);
+            const float4 lo = __ldg(src), hi = __ldg(src + 1);
+            __half2 h0 = __floats2half2_rn(lo.x, hi.x), h1 = __floats2half2_rn(lo.y, hi.y);
+            __half2 h2 = __floats2half2_rn(lo.z, hi.z), h3 = __floats2half2_rn(lo.w, hi.w);
+            v = make_uint4(*reinterpret_cast<uint32_t *>(&h0), *reinterpret_cast<uint32_t *>(&h1),
+                           *reinterpret_cast<uint32_t *>(&h2), *reinterpret_cast<uint32_t *>(&h3));
+        }
+        *reinterpret_cast<uint4 *>(dst) = v;
     }
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (t >= 0) {
-        // chunk ch holds columns 8ch + (0, 4, 1, 5, 2, 6, 3, 7) of the group
-        const float4 *src = reinterpret_cast<const float4 *>(x + (size_t)t * H + kb * kGroup + 8 * ch);
-        const float4 lo = __ldg(src), hi = __ldg(src + 1);
-        __half2 h0 = __floats2half2_rn(lo.x, hi.x), h1 = __floats2half2_rn(lo.y, hi.y);
-        __half2 h2 = __floats2half2_rn(lo.z, hi.z), h3 = __floats2half2_rn(lo.w, hi.w);
-        v = make_uint4(*reinterpret_cast<uint32_t *>(&h0), *reinterpret_cast<uint32_t *>(&h1),
-                       *reinterpret_cast<uint32_t *>(&h2), *reinterpret_cast<uint32_t *>(&h3));
-    }
-    *reinterpret_cast<uint4 *>(dst) = v;
 }
 
 // ------------------------------------------------------------------ grouped GEMM
@@ -909,11 +912,20 @@ __global__ void __launch_bounds__(256) k_prefill_combine(const float *__restrict
     if (i >= (long long)T * H4) return;
     const int t = (int)(i / H4), n4 = (int)(i % H4);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int k = 0; k < topk; k++) {
-        const float g = gate[t * topk + k];
-        const float4 v = __ldg(reinterpret_cast<const float4 *>(Yr + (size_t)(t * topk + k) * H) + n4);
-        acc = make_float4(fmaf(g, v.x, acc.x), fmaf(g, v.y, acc.y), fmaf(g, v.z, acc.z), fmaf(g, v.w, acc.w));
-    }
+    // every choice's row loaded before the sums (added in choice order)
+    float4 v[MOE_MAX_TOPK];
+    float g[MOE_MAX_TOPK];
+#pragma unroll
+    for (int k = 0; k < MOE_MAX_TOPK; k++)
+        if (k < topk) {
+            g[k] = __ldg(gate + t * topk + k);
+            v[k] = __ldg(reinterpret_cast<const float4 *>(Yr + (size_t)(t * topk + k) * H) + n4);
+        }
+#pragma unroll
+    for (int k = 0; k < MOE_MAX_TOPK; k++)
+        if (k < topk)
+            acc = make_float4(fmaf(g[k], v[k].x, acc.x), fmaf(g[k], v[k].y, acc.y), fmaf(g[k], v[k].z, acc.z),
+                              fmaf(g[k], v[k].w, acc.w));
     for (int p = 0; p < sparts; p++) {  // the shared expert's K parts, in order
         const float *ys = p ? Ys_more + (size_t)(p - 1) * T16 * H : Ys;
         const float4 sv = __ldg(reinterpret_cast<const float4 *>(ys + (size_t)t * H) + n4);
