@@ -4,7 +4,6 @@
 
 #include <cstdio>
 #include <cstring>
-#include <algorithm>
 #include <atomic>
 #include <chrono>
 #include <mutex>
@@ -431,7 +430,8 @@ int run_layer_chunk(const moe_layer_t *l, const float *x, int T, int flags, floa
         return cuda_status();
     // (a grid-stride loop over the rows the plan used: 8 CTAs of 256 per SM)
     const long long gthreads = (long long)(Rmax + T16) * (l->H / kGroup) * 8;
-    const unsigned gblocks = (unsigned)std::min<long long>((gthreads + 255) / 256, 8LL * sms);
+    const long long gneed = (gthreads + 255) / 256;
+    const unsigned gblocks = (unsigned)(gneed < 8LL * sms ? gneed : 8LL * sms);
     if (pf_launch(k_prefill_gather, dim3(gblocks), dim3(256), 0, st, xin, T, l->H, Rmax,
                   T16, (const int *)plan.rowtok, (const int *)plan.U, ws.Br, ws.Bs) != cudaSuccess)
         return cuda_status();
